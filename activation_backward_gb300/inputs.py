@@ -1,0 +1,193 @@
+"""Seeded synthetic inputs for the conv + BN + activation backward.
+
+This module only *generates inputs*: it draws the seeded tensors and runs the
+layer's FORWARD pass (convolution, batch statistics, scale, activation) to
+produce the cached tensors a backward call consumes (``z``, ``mean``, ``var``,
+``output``).  It contains none of the backward arithmetic.  Both the CUDA path
+and the oracle take their inputs from here, so both see identical fp32 bits.
+
+Workloads (shapes from the pages):
+
+* ``lenet_conv2``  -- caffe LeNet conv2 ("LeNet反向过程", 第四层 Convolution):
+  bottom (64,20,12,12) -> top (64,50,8,8), 5x5 kernels, no BN, linear.
+* ``darknet_3x3``  -- darknet 3x3 conv + BN + leaky, 16 x 64->128 at 52x52.
+* ``yolov3_down``  -- YOLOv3 downsampling conv, 3x3 stride 2, 256->512, 52->26.
+* ``yolo_head_1x1`` -- YOLO head 1x1 conv, 1024->255 at 13x13, no BN, linear,
+  with a 90%-zero delta (the sparse detection-loss gradient pattern).
+* ``residual_block`` -- darknet residual block at 26x26: 1x1 512->256 BN+leaky,
+  then 3x3 256->512 BN+leaky, plus the shortcut (two layer calls).
+
+Random numbers come from numpy's PCG64 (``default_rng(seed)``), which gives
+the same stream on every platform; the draws happen in a fixed order
+(x, W, gamma, delta, mask, residual).  "N(0, v)" means variance v.  The forward
+convolution runs in float64 (torch CPU ``conv2d``, a library call) and is then
+rounded to fp32; the batch statistics are the biased (1/m) mean and variance
+of that fp32 ``z``; the BN shift beta is 0.
+"""
+from dataclasses import dataclass, replace
+
+import numpy as np
+
+ACT_LINEAR = 0
+ACT_LEAKY = 1
+EPS = 1e-5
+
+
+@dataclass(frozen=True)
+class Geometry:
+    N: int
+    C: int
+    H: int
+    W: int
+    K: int
+    R: int
+    S: int
+    stride: int = 1
+    pad: int = 0
+
+    @property
+    def P(self):
+        return (self.H + 2 * self.pad - self.R) // self.stride + 1
+
+    @property
+    def Q(self):
+        return (self.W + 2 * self.pad - self.S) // self.stride + 1
+
+    def gemm_flops(self):
+        """Algorithmic FLOPs of ONE of the two GEMMs (wgrad or dgrad):
+        2 * N * K * C * R * S * P * Q (multiply-adds counted as 2)."""
+        return 2 * self.N * self.K * self.C * self.R * self.S * self.P * self.Q
+
+
+@dataclass(frozen=True)
+class LayerSpec:
+    name: str
+    geom: Geometry
+    act: int
+    bn: bool
+    accumulate: int = 0
+    dist: str = "normal"  # "uniform" for LeNet
+    sparse_delta: float = 0.0  # fraction of zero delta entries
+
+
+CONFIGS = {
+    1: LayerSpec("lenet_conv2", Geometry(64, 20, 12, 12, 50, 5, 5, 1, 0), ACT_LINEAR, False,
+                 dist="uniform"),
+    2: LayerSpec("darknet_3x3", Geometry(16, 64, 52, 52, 128, 3, 3, 1, 1), ACT_LEAKY, True),
+    3: LayerSpec("yolov3_down", Geometry(16, 256, 52, 52, 512, 3, 3, 2, 1), ACT_LEAKY, True),
+    4: LayerSpec("yolo_head_1x1", Geometry(64, 1024, 13, 13, 255, 1, 1, 1, 0), ACT_LINEAR, False,
+                 sparse_delta=0.9),
+    # config 5 is a block of two layers; these are its two convolutions
+    5: LayerSpec("residual_block", Geometry(32, 512, 26, 26, 256, 1, 1, 1, 0), ACT_LEAKY, True),
+}
+BLOCK_CONV2 = Geometry(32, 256, 26, 26, 512, 3, 3, 1, 1)
+
+
+def seed_of(config_id):
+    return 1000 + int(config_id)
+
+
+def _forward_conv64(x, w, stride, pad):
+    import torch
+    with torch.no_grad():
+        z = torch.nn.functional.conv2d(torch.from_numpy(x.astype(np.float64)),
+                                       torch.from_numpy(w.astype(np.float64)), stride=stride,
+                                       padding=pad)
+    return z.numpy()
+
+
+def _leaky(v):
+    return np.where(v > 0, v, 0.1 * v)
+
+
+def _bn_forward(z32, gamma, act, eps=EPS):
+    """Forward batch-norm (training mode) + activation.  Returns mean, var
+    (biased) and the post-activation output, all fp32."""
+    z = z32.astype(np.float64)
+    mean = z.mean(axis=(0, 2, 3))
+    var = ((z - mean[None, :, None, None]) ** 2).mean(axis=(0, 2, 3))
+    mean32, var32 = mean.astype(np.float32), var.astype(np.float32)
+    xh = (z - mean32.astype(np.float64)[None, :, None, None]) / np.sqrt(
+        var32.astype(np.float64)[None, :, None, None] + np.float64(np.float32(eps)))
+    y = gamma.astype(np.float64)[None, :, None, None] * xh  # beta = 0
+    out = _leaky(y) if act == ACT_LEAKY else y
+    return mean32, var32, out.astype(np.float32)
+
+
+def _draw(rng, dist, shape, var=1.0):
+    if dist == "uniform":
+        return rng.uniform(-1.0, 1.0, size=shape).astype(np.float32)
+    return (rng.standard_normal(size=shape) * np.sqrt(var)).astype(np.float32)
+
+
+def make_layer(spec, seed, *, batch=None, residual=False, x=None, delta_var=0.01):
+    """Inputs of one layer call.  Returns a dict with the geometry and flags
+    and fp32 arrays x, W, gamma, z, mean, var, output, delta, residual.
+
+    ``batch`` overrides N (a smaller case with the same channel and spatial
+    geometry); ``x`` supplies the layer input (for the block's second layer)."""
+    g = spec.geom if batch is None else replace(spec.geom, N=int(batch))
+    rng = np.random.default_rng(seed)
+    if x is None:
+        x = _draw(rng, spec.dist, (g.N, g.C, g.H, g.W))
+    fan_in = g.C * g.R * g.S
+    if spec.dist == "uniform":
+        W = _draw(rng, "uniform", (g.K, g.C, g.R, g.S))
+    else:
+        W = _draw(rng, "normal", (g.K, g.C, g.R, g.S), var=2.0 / fan_in)  # He init
+    gamma = rng.uniform(0.5, 1.5, size=g.K).astype(np.float32) if spec.bn else None
+    if spec.dist == "uniform":
+        delta = _draw(rng, "uniform", (g.N, g.K, g.P, g.Q))
+    else:
+        delta = _draw(rng, "normal", (g.N, g.K, g.P, g.Q), var=delta_var)
+    if spec.sparse_delta > 0:
+        keep = rng.uniform(size=delta.shape) >= spec.sparse_delta
+        delta = (delta * keep).astype(np.float32)
+    res = _draw(rng, "normal", (g.N, g.C, g.H, g.W), var=0.01) if residual else None
+
+    z = _forward_conv64(x, W, g.stride, g.pad).astype(np.float32)
+    if spec.bn:
+        mean, var, output = _bn_forward(z, gamma, spec.act)
+    else:
+        mean = var = None
+        output = (_leaky(z.astype(np.float64)) if spec.act == ACT_LEAKY else z).astype(np.float32)
+        z = None  # the backward needs the pre-BN output only with BN
+    return dict(name=spec.name, geom=g, act=spec.act, bn=spec.bn, accumulate=spec.accumulate,
+                eps=EPS, x=x, W=W, gamma=gamma, z=z, mean=mean, var=var, output=output,
+                delta=delta, residual=res)
+
+
+def make_config(config_id, *, batch=None):
+    """The layer call(s) of one workload: a list of input dicts.
+
+    Configs 1-4 are one call.  Config 5 (residual block) is two calls in
+    backward order: the 3x3 conv (its delta is the block delta D, its input
+    is the 1x1 conv's output), then the 1x1 conv (its prev_delta gets the
+    shortcut residual D).  The 1x1 conv's incoming delta is, in the real block,
+    the 3x3 conv's prev_delta; here it is its own seeded N(0, 0.01) draw so
+    that each call can be checked on its own -- the chained block is built by
+    ``chain_block``."""
+    config_id = int(config_id)
+    seed = seed_of(config_id)
+    if config_id in (1, 2, 3, 4):
+        return [make_layer(CONFIGS[config_id], seed, batch=batch)]
+    if config_id != 5:
+        raise ValueError(f"unknown config {config_id}")
+    spec1 = CONFIGS[5]
+    l1 = make_layer(spec1, seed, batch=batch)  # X, W1, gamma1, z1, y1 (its output)
+    spec2 = LayerSpec("residual_block.conv2", BLOCK_CONV2, ACT_LEAKY, True)
+    l2 = make_layer(spec2, seed + 100, batch=batch, x=l1["output"])
+    # block delta D: the gradient at the block output (after the shortcut add)
+    D = l2["delta"]
+    l2 = dict(l2, name="residual_block.conv2")
+    l1 = dict(l1, name="residual_block.conv1", residual=D)
+    return [l2, l1]
+
+
+def layer_bytes_reduce(layer):
+    """Algorithmic bytes of the per-channel reduction pass: 4 B per element of
+    delta, plus output (leaky) and z (BN)."""
+    g = layer["geom"]
+    m = g.N * g.K * g.P * g.Q
+    n = 1 + (1 if layer["act"] == ACT_LEAKY else 0) + (1 if layer["bn"] else 0)
+    return 4 * m * n
