@@ -1,0 +1,170 @@
+"""Thin ctypes binding of libcba's C ABI (``include/cba.h``).
+
+Argument marshalling only: every step of the backward runs in the CUDA
+library.  Tensors are passed as device pointers (``torch.Tensor.data_ptr()``
+or plain integers); streams as ``cudaStream_t`` handles (default: torch's
+current stream).  There is no CPU path: if ``libcba.so`` is missing the
+binding raises instead of computing anything.
+"""
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libcba.so")
+
+CBA_OK = 0
+CBA_ERR_ARG = -1
+CBA_ERR_UNSUPPORTED = -2
+CBA_ERR_ALIGN = -3
+CBA_ERR_WORKSPACE = -4
+CBA_ERR_CUDA = -5
+CBA_ERR_DEVICE_TIMEOUT = -6
+
+CBA_ACT_LINEAR = 0
+CBA_ACT_LEAKY = 1
+CBA_MATH_TF32 = 0
+CBA_MATH_FFMA = 1
+
+# every symbol include/cba.h declares
+EXPORTS = ("cba_workspace_bytes", "cba_conv_bn_act_backward", "cba_conv_bn_act_backward_traced",
+           "cba_get_status",
+           "cba_selftest_bounded_wait", "cba_error_string", "cba_last_cuda_error", "cba_version")
+
+
+class cba_desc_t(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int), ("C", ctypes.c_int), ("H", ctypes.c_int),
+                ("W", ctypes.c_int), ("K", ctypes.c_int), ("R", ctypes.c_int),
+                ("S", ctypes.c_int), ("stride", ctypes.c_int), ("pad", ctypes.c_int),
+                ("act", ctypes.c_int), ("batch_normalize", ctypes.c_int),
+                ("accumulate", ctypes.c_int), ("eps", ctypes.c_float), ("math", ctypes.c_int)]
+
+
+class CbaError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__(f"{what}: {cba_error_string(code)} (code {code})")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path=LIB_PATH):
+    """Load libcba.so.  Raises if it has not been built (no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libcba.so not built ({path}); run __graft_entry__.build()")
+    L = ctypes.CDLL(path)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    L.cba_workspace_bytes.restype = sz
+    L.cba_workspace_bytes.argtypes = [ctypes.POINTER(cba_desc_t)]
+    L.cba_conv_bn_act_backward.restype = ctypes.c_int
+    L.cba_conv_bn_act_backward.argtypes = [ctypes.POINTER(cba_desc_t)] + [vp] * 15 + [sz, vp]
+    L.cba_conv_bn_act_backward_traced.restype = ctypes.c_int
+    L.cba_conv_bn_act_backward_traced.argtypes = (
+        [ctypes.POINTER(cba_desc_t)] + [vp] * 15 + [sz, vp, ctypes.POINTER(ctypes.c_void_p),
+                                                    ctypes.POINTER(ctypes.c_int)])
+    L.cba_get_status.restype = ctypes.c_int
+    L.cba_get_status.argtypes = [vp, sz, vp]
+    L.cba_selftest_bounded_wait.restype = ctypes.c_int
+    L.cba_selftest_bounded_wait.argtypes = [vp, sz, ctypes.c_uint, vp]
+    L.cba_error_string.restype = ctypes.c_char_p
+    L.cba_error_string.argtypes = [ctypes.c_int]
+    L.cba_last_cuda_error.restype = ctypes.c_int
+    L.cba_version.restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _bytes(t):
+    if isinstance(t, int):
+        raise TypeError("pass the workspace as a tensor, or (pointer, nbytes)")
+    return t.numel() * t.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_desc(N, C, H, W, K, R, S, stride=1, pad=0, act=CBA_ACT_LEAKY, batch_normalize=1,
+              accumulate=0, eps=1e-5, math=CBA_MATH_TF32):
+    return cba_desc_t(N, C, H, W, K, R, S, stride, pad, act, int(batch_normalize),
+                      int(accumulate), eps, math)
+
+
+def cba_workspace_bytes(desc):
+    return load().cba_workspace_bytes(ctypes.byref(desc))
+
+
+def cba_conv_bn_act_backward(desc, x, output, z, delta, W, gamma, mean, var, residual, dW, db,
+                             dgamma, prev_delta, dz_out, workspace, workspace_bytes=None,
+                             stream=None, check=True):
+    """Enqueue one layer backward.  Returns the C return code; raises CbaError
+    on a non-zero code when ``check``."""
+    wsb = _bytes(workspace) if workspace_bytes is None else int(workspace_bytes)
+    rc = load().cba_conv_bn_act_backward(
+        ctypes.byref(desc), _ptr(x), _ptr(output), _ptr(z), _ptr(delta), _ptr(W), _ptr(gamma),
+        _ptr(mean), _ptr(var), _ptr(residual), _ptr(dW), _ptr(db), _ptr(dgamma),
+        _ptr(prev_delta), _ptr(dz_out), _ptr(workspace), wsb, _stream(stream))
+    if check and rc != CBA_OK:
+        raise CbaError(rc, "cba_conv_bn_act_backward")
+    return rc
+
+
+def cba_conv_bn_act_backward_traced(desc, x, output, z, delta, W, gamma, mean, var, residual,
+                                    dW, db, dgamma, prev_delta, dz_out, workspace,
+                                    workspace_bytes=None, stream=None, events=None, check=True):
+    """As cba_conv_bn_act_backward; ``events`` is None or 4 torch.cuda.Event
+    (created with enable_timing=True) recorded between the phases.  Returns
+    (code, number of kernels enqueued)."""
+    wsb = _bytes(workspace) if workspace_bytes is None else int(workspace_bytes)
+    ev = None
+    if events is not None:
+        assert len(events) == 4
+        ev = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+    n = ctypes.c_int(0)
+    rc = load().cba_conv_bn_act_backward_traced(
+        ctypes.byref(desc), _ptr(x), _ptr(output), _ptr(z), _ptr(delta), _ptr(W), _ptr(gamma),
+        _ptr(mean), _ptr(var), _ptr(residual), _ptr(dW), _ptr(db), _ptr(dgamma),
+        _ptr(prev_delta), _ptr(dz_out), _ptr(workspace), wsb, _stream(stream), ev,
+        ctypes.byref(n))
+    if check and rc != CBA_OK:
+        raise CbaError(rc, "cba_conv_bn_act_backward_traced")
+    return rc, n.value
+
+
+def cba_get_status(workspace, workspace_bytes=None, stream=None):
+    wsb = _bytes(workspace) if workspace_bytes is None else int(workspace_bytes)
+    return load().cba_get_status(_ptr(workspace), wsb, _stream(stream))
+
+
+def cba_selftest_bounded_wait(workspace, timeout_us, workspace_bytes=None, stream=None):
+    wsb = _bytes(workspace) if workspace_bytes is None else int(workspace_bytes)
+    return load().cba_selftest_bounded_wait(_ptr(workspace), wsb, int(timeout_us),
+                                            _stream(stream))
+
+
+def cba_error_string(code):
+    return load().cba_error_string(int(code)).decode()
+
+
+def cba_last_cuda_error():
+    return load().cba_last_cuda_error()
+
+
+def cba_version():
+    return load().cba_version()

@@ -1,0 +1,268 @@
+// cba_api.cu -- the C ABI of libcba: argument checks, the per-call plan and
+// workspace carve-up, and the launch sequence
+//   reduction pass -> finalize -> wgrad -> dgrad (if prev_delta)
+// on the caller's stream.  Nothing here allocates, frees or synchronises
+// (except cba_get_status, which exists to synchronise).
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "cba_internal.cuh"
+
+namespace cba {
+
+namespace {
+
+int g_last_cuda_error = 0;
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+int make_plan(const cba_desc_t *d, Plan *p) {
+    if (!d || !p) return CBA_ERR_ARG;
+    std::memset(p, 0, sizeof(*p));
+    if (d->N <= 0 || d->C <= 0 || d->H <= 0 || d->W <= 0 || d->K <= 0 || d->R <= 0 ||
+        d->S <= 0 || d->stride <= 0 || d->pad < 0)
+        return CBA_ERR_ARG;
+    if (d->act != CBA_ACT_LINEAR && d->act != CBA_ACT_LEAKY) return CBA_ERR_ARG;
+    if (d->math != CBA_MATH_TF32 && d->math != CBA_MATH_FFMA) return CBA_ERR_ARG;
+    if (d->batch_normalize != 0 && d->batch_normalize != 1) return CBA_ERR_ARG;
+    if (d->accumulate != 0 && d->accumulate != 1) return CBA_ERR_ARG;
+    if (d->batch_normalize && !(std::isfinite(d->eps) && d->eps >= 0.f)) return CBA_ERR_ARG;
+    const long long P = (long long)(d->H + 2LL * d->pad - d->R) / d->stride + 1;
+    const long long Q = (long long)(d->W + 2LL * d->pad - d->S) / d->stride + 1;
+    if (d->H + 2LL * d->pad - d->R < 0 || d->W + 2LL * d->pad - d->S < 0 || P <= 0 || Q <= 0)
+        return CBA_ERR_ARG;
+    const long long lim = (1LL << 31) - 1;
+    const long long nin = (long long)d->N * d->C * d->H * d->W;
+    const long long nout = (long long)d->N * d->K * P * Q;
+    const long long nw = (long long)d->K * d->C * d->R * d->S;
+    if (nin > lim || nout > lim || nw > lim || d->pad > (1 << 20) || d->stride > (1 << 20))
+        return CBA_ERR_UNSUPPORTED;
+
+    p->N = d->N; p->C = d->C; p->H = d->H; p->W = d->W; p->K = d->K; p->R = d->R; p->S = d->S;
+    p->stride = d->stride; p->pad = d->pad; p->P = (int)P; p->Q = (int)Q;
+    p->PQ = (int)(P * Q); p->HW = d->H * d->W; p->RS = d->R * d->S; p->CRS = d->C * p->RS;
+    p->m = (long long)d->N * P * Q;
+    p->act = d->act; p->bn = d->batch_normalize; p->accumulate = d->accumulate;
+    p->math = d->math; p->eps = d->eps;
+    p->num_sms = kNumSMs;
+
+    // reduction pass: about 8 blocks of 256 threads per SM in total, at least
+    // ~2k elements per block
+    long long want = ceil_div((long long)p->num_sms * 8, p->K);
+    long long cap = std::max(1LL, p->m / 2048);
+    p->red_splits = (int)std::max(1LL, std::min(want, cap));
+
+    // SIMT wgrad: split the reduction so that ~4 blocks per SM exist
+    const long long tiles = ceil_div(p->K, 64) * ceil_div(p->CRS, 64);
+    long long sw = std::max(1LL, ceil_div((long long)p->num_sms * 4, tiles));
+    sw = std::min(sw, std::max(1LL, ceil_div(p->m, 256)));
+    long long chunk = ceil_div(ceil_div(p->m, sw), 16) * 16;
+    p->wg_chunk = chunk;
+    p->wg_splits = (int)ceil_div(p->m, chunk);
+
+    p->use_tc = (p->math == CBA_MATH_TF32) && tc_supported(*p);
+
+    // workspace carve-up
+    size_t off = 0;
+    p->off_status = off;
+    off = align_up(off + 256, 256);
+    p->off_red = off;
+    off = align_up(off + sizeof(double) * 2 * (size_t)p->red_splits * p->K, 256);
+    p->off_coef = off;
+    off = align_up(off + sizeof(Coef) * (size_t)p->K, 256);
+    p->off_wgpart = off;
+    size_t wg_simt = sizeof(float) * (size_t)p->wg_splits * p->K * p->CRS;
+    size_t wg_tc = p->use_tc ? sizeof(float) * (size_t)p->tc_wg_splits * p->K * p->CRS : 0;
+    off = align_up(off + std::max(wg_simt, wg_tc), 256);
+    p->off_wt = off;
+    if (p->use_tc) off = align_up(off + sizeof(float) * (size_t)nw, 256);
+    p->total = off;
+    return CBA_OK;
+}
+
+}  // namespace cba
+
+using namespace cba;
+
+namespace {
+
+inline bool misaligned(const void *ptr) {
+    return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0;
+}
+
+int fail_cuda(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return CBA_ERR_CUDA;
+}
+
+// Makes the device that owns `stream` (or, for the NULL stream, the device
+// that holds `ptr`) current for this library's runtime, which keeps its own
+// per-thread current device.
+cudaError_t select_device(cudaStream_t stream, const void *ptr) {
+    int dev = -1;
+    cudaError_t e = cudaSuccess;
+    if (stream) {
+        e = cudaStreamGetDevice(stream, &dev);
+    } else if (ptr) {
+        cudaPointerAttributes a;
+        e = cudaPointerGetAttributes(&a, ptr);
+        if (e == cudaSuccess) dev = a.device;
+    }
+    if (e != cudaSuccess) return e;
+    if (dev < 0) return cudaSuccess;
+    int cur = -1;
+    e = cudaGetDevice(&cur);
+    if (e == cudaSuccess && cur != dev) e = cudaSetDevice(dev);
+    return e;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t cba_workspace_bytes(const cba_desc_t *d) {
+    Plan p;
+    if (make_plan(d, &p) != CBA_OK) return 0;
+    return p.total;
+}
+
+}  // extern "C"
+
+namespace {
+
+struct Tracer {
+    void *const *ev;
+    cudaStream_t st;
+    cudaError_t mark(int i) const {
+        if (!ev) return cudaSuccess;
+        return cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+    }
+};
+
+int backward_impl(const cba_desc_t *d, const float *x, const float *output, const float *z,
+                  const float *delta, const float *Wt, const float *gamma, const float *mean,
+                  const float *var, const float *residual, float *dW, float *db, float *dgamma,
+                  float *prev_delta, float *dz_out, void *workspace, size_t workspace_bytes,
+                  void *stream, void *const *events, int *launches) {
+    Plan p;
+    int rc = make_plan(d, &p);
+    if (rc != CBA_OK) return rc;
+    if (!x || !delta || !Wt || !dW || !db) return CBA_ERR_ARG;
+    if (p.act != CBA_ACT_LINEAR && !output) return CBA_ERR_ARG;
+    if (p.bn && (!z || !gamma || !mean || !var || !dgamma)) return CBA_ERR_ARG;
+    const void *ptrs[] = {x, output, z, delta, Wt, gamma, mean, var, residual,
+                          dW, db, dgamma, prev_delta, dz_out};
+    for (const void *q : ptrs)
+        if (misaligned(q)) return CBA_ERR_ALIGN;
+    if (!workspace || workspace_bytes < p.total) return CBA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CBA_ERR_ALIGN;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Tracer tr{events, st};
+    int n_launch = 0;
+    cudaGetLastError();  // the launches below report only their own errors
+    cudaError_t e = select_device(st, delta);
+    if (e != cudaSuccess) return fail_cuda(e);
+    e = cudaMemsetAsync(workspace, 0, 256, st);  // status word
+    if (e == cudaSuccess) e = tr.mark(0);
+    if (e == cudaSuccess) e = launch_reduce(p, delta, output, z, gamma, mean, var, db, dgamma,
+                                            workspace, st, &n_launch);
+    if (e == cudaSuccess && dz_out) {
+        e = launch_dz_out(p, delta, output, z, workspace, dz_out, st);
+        ++n_launch;
+    }
+    if (e == cudaSuccess) e = tr.mark(1);
+    if (e == cudaSuccess) {
+        e = p.use_tc ? launch_wgrad_tc(p, x, delta, output, z, dW, workspace, st, &n_launch)
+                     : launch_wgrad_simt(p, x, delta, output, z, dW, workspace, st, &n_launch);
+    }
+    if (e == cudaSuccess) e = tr.mark(2);
+    if (e == cudaSuccess && prev_delta) {
+        e = p.use_tc ? launch_dgrad_tc(p, Wt, delta, output, z, residual, prev_delta, workspace,
+                                       st, &n_launch)
+                     : launch_dgrad_simt(p, Wt, delta, output, z, residual, prev_delta,
+                                         workspace, st, &n_launch);
+    }
+    if (e == cudaSuccess) e = tr.mark(3);
+    if (launches) *launches = n_launch;
+    if (e != cudaSuccess) return fail_cuda(e);
+    return CBA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cba_conv_bn_act_backward(const cba_desc_t *d, const float *x, const float *output,
+                             const float *z, const float *delta, const float *Wt,
+                             const float *gamma, const float *mean, const float *var,
+                             const float *residual, float *dW, float *db, float *dgamma,
+                             float *prev_delta, float *dz_out, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+    return backward_impl(d, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db, dgamma,
+                         prev_delta, dz_out, workspace, workspace_bytes, stream, nullptr,
+                         nullptr);
+}
+
+int cba_conv_bn_act_backward_traced(const cba_desc_t *d, const float *x, const float *output,
+                                    const float *z, const float *delta, const float *Wt,
+                                    const float *gamma, const float *mean, const float *var,
+                                    const float *residual, float *dW, float *db, float *dgamma,
+                                    float *prev_delta, float *dz_out, void *workspace,
+                                    size_t workspace_bytes, void *stream,
+                                    void *const *phase_events, int *launches) {
+    return backward_impl(d, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db, dgamma,
+                         prev_delta, dz_out, workspace, workspace_bytes, stream, phase_events,
+                         launches);
+}
+
+int cba_get_status(void *workspace, size_t workspace_bytes, void *stream) {
+    if (!workspace || workspace_bytes < 256) return CBA_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned word = 0;
+    cudaError_t e = select_device(st, workspace);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, sizeof(word), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return (word & kStatusTimeout) ? CBA_ERR_DEVICE_TIMEOUT : CBA_OK;
+}
+
+int cba_selftest_bounded_wait(void *workspace, size_t workspace_bytes, unsigned timeout_us,
+                              void *stream) {
+    if (!workspace || workspace_bytes < 256) return CBA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CBA_ERR_ALIGN;
+    if (timeout_us < 1 || timeout_us > 2000000) return CBA_ERR_ARG;
+    cudaGetLastError();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = select_device(st, workspace);
+    if (e == cudaSuccess) e = launch_selftest_wait(timeout_us, workspace, st);
+    if (e != cudaSuccess) return fail_cuda(e);
+    return CBA_OK;
+}
+
+const char *cba_error_string(int code) {
+    switch (code) {
+    case CBA_OK: return "ok";
+    case CBA_ERR_ARG: return "invalid argument (dimension, flag or required pointer)";
+    case CBA_ERR_UNSUPPORTED: return "unsupported shape (beyond the library's limits)";
+    case CBA_ERR_ALIGN: return "pointer not 16-byte aligned (workspace: 256-byte)";
+    case CBA_ERR_WORKSPACE: return "workspace missing or smaller than cba_workspace_bytes()";
+    case CBA_ERR_CUDA: return "CUDA launch or runtime error (see cba_last_cuda_error)";
+    case CBA_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out; outputs are not valid";
+    default: return "unknown error code";
+    }
+}
+
+int cba_last_cuda_error(void) { return g_last_cuda_error; }
+
+int cba_version(void) { return 100; }
+
+}  // extern "C"

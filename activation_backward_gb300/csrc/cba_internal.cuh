@@ -1,0 +1,106 @@
+// cba_internal.cuh -- shared declarations of libcba's translation units:
+// the per-call plan (geometry, workspace carve-up, launch shapes), the
+// per-channel coefficient record, the device status word, and small device
+// helpers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/cba.h"
+
+namespace cba {
+
+constexpr int kNumSMs = 152;  // GB300: 2 dies x 76 SMs (the plan uses the queried value)
+
+// Device status bits (workspace word 0).
+constexpr unsigned kStatusTimeout = 1u;
+
+// Per-channel BN-backward coefficients, written by the finalize kernel and
+// read by every GEMM operand transform:
+//   dz = a * delta' + b + c * (z - mu)
+struct __align__(16) Coef {
+    float a, b, c, mu;
+};
+
+struct Plan {
+    // geometry
+    int N, C, H, W, K, R, S, stride, pad, P, Q;
+    int PQ, HW, RS, CRS;
+    long long m;  // N*P*Q: elements per output channel
+    int act, bn, accumulate, math;
+    float eps;
+    int num_sms;
+    // reduction pass
+    int red_splits;  // blocks per channel
+    // SIMT wgrad split-K
+    int wg_splits;
+    long long wg_chunk;  // reduction positions per split (multiple of the K tile)
+    // tensor-core path
+    int use_tc;
+    int tc_wg_splits;
+    long long tc_wg_chunk;
+    // workspace layout (byte offsets from the base)
+    size_t off_status, off_red, off_coef, off_wgpart, off_wt, total;
+};
+
+// Builds the plan; returns CBA_OK or a CBA_ERR_* code.
+int make_plan(const cba_desc_t *d, Plan *p);
+
+// ---- launchers (each returns cudaSuccess or the launch error) ----
+cudaError_t launch_reduce(const Plan &p, const float *delta, const float *output, const float *z,
+                          const float *gamma, const float *mean, const float *var, float *db,
+                          float *dgamma, void *ws, cudaStream_t st, int *launches);
+cudaError_t launch_dz_out(const Plan &p, const float *delta, const float *output, const float *z,
+                          const void *ws, float *dz_out, cudaStream_t st);
+cudaError_t launch_wgrad_simt(const Plan &p, const float *x, const float *delta,
+                              const float *output, const float *z, float *dW, void *ws,
+                              cudaStream_t st, int *launches);
+cudaError_t launch_dgrad_simt(const Plan &p, const float *Wt, const float *delta,
+                              const float *output, const float *z, const float *residual,
+                              float *prev, const void *ws, cudaStream_t st, int *launches);
+cudaError_t launch_wgrad_tc(const Plan &p, const float *x, const float *delta,
+                            const float *output, const float *z, float *dW, void *ws,
+                            cudaStream_t st, int *launches);
+cudaError_t launch_dgrad_tc(const Plan &p, const float *Wt, const float *delta,
+                            const float *output, const float *z, const float *residual,
+                            float *prev, void *ws, cudaStream_t st, int *launches);
+cudaError_t launch_selftest_wait(unsigned timeout_us, void *ws, cudaStream_t st);
+bool tc_supported(const Plan &p);
+
+template <typename T>
+inline T *ws_at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+template <typename T>
+inline const T *ws_at(const void *ws, size_t off) {
+    return reinterpret_cast<const T *>(static_cast<const char *>(ws) + off);
+}
+
+// ---- device helpers ----
+
+// Activation derivative on the activation's output value (leaky: y > 0 -> 1,
+// else 0.1; linear: 1).
+template <int ACT>
+__device__ __forceinline__ float act_grad(float y) {
+    if constexpr (ACT == CBA_ACT_LEAKY) {
+        return y > 0.f ? 1.f : 0.1f;
+    } else {
+        return 1.f;
+    }
+}
+
+// The BN-input gradient of one element from its raw inputs and the channel's
+// coefficients.  Without BN, dz = delta'.
+template <int ACT, bool BN>
+__device__ __forceinline__ float dz_of(float d, float y, float zv, const Coef &cf) {
+    float dp = d * act_grad<ACT>(y);
+    if constexpr (BN) {
+        return fmaf(cf.a, dp, fmaf(cf.c, zv - cf.mu, cf.b));
+    } else {
+        return dp;
+    }
+}
+
+}  // namespace cba

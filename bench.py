@@ -1,0 +1,392 @@
+"""Benchmark of the conv + BN + activation backward on GB300.
+
+One step = one backward of the darknet 3x3 conv + BN + leaky layer
+(batch 16, 64 -> 128 channels, 52x52, stride 1, pad 1) through the C ABI:
+reduction pass -> finalize -> wgrad -> dgrad.  Inputs are resident in HBM
+when the timed region starts; L2 is flushed (a 512 MiB write) before every
+timed step, outside the per-step CUDA-event window.
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+the host cores instead, on bounded samples of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "conv+BN+act backward TFLOP/s and fraction of TF32 roofline per layer, 1×GB300"
+UNIT = "TFLOP/s"
+# nominal dense tensor rates, PFLOP/s: tf32 1.1, bf16 2.25 -> tf32 = bf16 * 1.1/2.25
+TF32_PER_BF16 = 1.1 / 2.25
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK), "fallback"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2, help="workload 1-5 (default 2)")
+    ap.add_argument("--math", default="tf32", choices=["tf32", "ffma"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target seconds of oracle work for cpu_baseline")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((float(parts[2]), float(parts[3]), float(parts[4]), parts[5:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[3][1:5]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [r[0] for r in rows if r[2] > 150.0] or [r[0] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+# ---------------------------------------------------------- oracle timing
+
+def oracle_sample_run(layer, n_img, k_sub):
+    """The oracle's full chain on a bounded sample of one layer call: the
+    first n_img images and the first k_sub output channels.  Returns
+    (seconds, GEMM FLOPs of the sample)."""
+    import numpy as np
+
+    import oracle
+    from activation_backward_gb300 import inputs
+    g = layer["geom"]
+    sub = dict(layer)
+    sl = slice(0, n_img)
+    for key in ("x", "residual"):
+        if sub.get(key) is not None:
+            sub[key] = np.ascontiguousarray(sub[key][sl])
+    for key in ("output", "z", "delta"):
+        if sub.get(key) is not None:
+            sub[key] = np.ascontiguousarray(sub[key][sl, :k_sub])
+    for key in ("gamma", "mean", "var"):
+        if sub.get(key) is not None:
+            sub[key] = np.ascontiguousarray(sub[key][:k_sub])
+    sub["W"] = np.ascontiguousarray(sub["W"][:k_sub])
+    gs = inputs.Geometry(n_img, g.C, g.H, g.W, k_sub, g.R, g.S, g.stride, g.pad)
+    t0 = time.perf_counter()
+    oracle.conv_bn_act_backward(sub["x"], sub["output"], sub["z"], sub["delta"], sub["W"],
+                                sub["gamma"], sub["mean"], sub["var"], sub["residual"],
+                                stride=g.stride, pad=g.pad, act=sub["act"],
+                                batch_normalize=sub["bn"], accumulate=sub["accumulate"],
+                                eps=sub["eps"])
+    return time.perf_counter() - t0, 2 * gs.gemm_flops()
+
+
+def pick_sample(layers, seconds):
+    """Choose (n_img, k_sub) so that one oracle run takes about `seconds`."""
+    layer = layers[0]
+    g = layer["geom"]
+    k1 = max(1, min(g.K, 16))
+    t, _ = oracle_sample_run(layer, 1, k1)
+    per = t / k1  # seconds per (image, channel)
+    units = max(1, int(seconds / max(per, 1e-9)))
+    n_img = max(1, min(g.N, units // g.K))
+    k_sub = g.K if n_img > 1 else max(1, min(g.K, units))
+    return n_img, k_sub
+
+
+def cpu_baseline(layers, seconds):
+    import oracle
+    n_img, k_sub = pick_sample(layers, seconds)
+    t, flops = oracle_sample_run(layers[0], n_img, k_sub)
+    g = layers[0]["geom"]
+    return {"value": flops / t / 1e12, "unit": UNIT, "cores": oracle.get_threads(),
+            "kind": "oracle",
+            "sample": f"{layers[0]['name']}: {n_img} of {g.N} images x {k_sub} of {g.K} output "
+                      f"channels, full chain (fp64 direct loops), {t:.2f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from activation_backward_gb300 import inputs
+    layers = inputs.make_config(args.config)
+    total = args.steps + args.warmup
+    budget = 150.0 / max(total, 1)  # ~2.5 minutes for the whole run
+    n_img, k_sub = pick_sample(layers, budget)
+    for _ in range(args.warmup):
+        oracle_sample_run(layers[0], n_img, k_sub)
+    times, flops = [], 0
+    for _ in range(args.steps):
+        t, flops = oracle_sample_run(layers[0], n_img, k_sub)
+        times.append(t)
+    tot = sum(times)
+    value = flops * args.steps / tot / 1e12
+    g = layers[0]["geom"]
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": config_dict(args, layers, 1),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.get_threads(),
+                             "kind": "oracle",
+                             "sample": f"per step {n_img} of {g.N} images x {k_sub} of {g.K} "
+                                       f"output channels"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(args, layers, ws):
+    g = layers[0]["geom"]
+    flops = sum(2 * l["geom"].gemm_flops() for l in layers)
+    return {"workload": layers[0]["name"] if args.config != 5 else "residual_block",
+            "N": g.N, "C": g.C, "H": g.H, "W": g.W, "K": g.K, "R": g.R, "S": g.S,
+            "stride": g.stride, "pad": g.pad, "bn": bool(layers[0]["bn"]),
+            "act": "leaky" if layers[0]["act"] == 1 else "linear",
+            "gemm_gflop_per_step": flops / 1e9,
+            "l2": "flushed before every step (512 MiB write, outside the timing)",
+            "parallelism": "replicas only" if ws > 1 else "single GPU"}
+
+
+# ------------------------------------------------------------- GPU timing
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import activation_backward_gb300 as cba
+    from activation_backward_gb300 import inputs
+    from activation_backward_gb300.layer import DeviceLayer
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    math = cba.CBA_MATH_TF32 if args.math == "tf32" else cba.CBA_MATH_FFMA
+    cba.load()
+
+    layers = inputs.make_config(args.config)
+    dls = [DeviceLayer(l, math=math, device=dev) for l in layers]
+    flops = sum(2 * l["geom"].gemm_flops() for l in layers)
+    red_bytes = sum(inputs.layer_bytes_reduce(l) for l in layers)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events_per_layer=None):
+        n = 0
+        for i, dl in enumerate(dls):
+            if i > 0 and args.config == 5:
+                dl.delta.copy_(dls[0].prev)  # conv1's delta is conv2's prev_delta
+            n += dl.run_traced(events_per_layer[i] if events_per_layer else None)
+        return n
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    for dl in dls:
+        assert dl.status() == cba.CBA_OK, "device status after warm-up"
+
+    mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    starts = [mk() for _ in range(args.steps)]
+    ends = [mk() for _ in range(args.steps)]
+    phase = [[[mk() for _ in range(4)] for _ in dls] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    clocks.start()
+    torch.cuda.synchronize()
+    launches = 0
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        launches += step(phase[i])
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    for dl in dls:
+        assert dl.status() == cba.CBA_OK, "device status after the timed region"
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * flops / (ms_per_step * 1e-3) / 1e12
+
+    # per-phase device times (averaged over steps): reduce, wgrad, dgrad
+    ph = {"reduce": 0.0, "wgrad": 0.0, "dgrad": 0.0}
+    for i in range(args.steps):
+        for ev in phase[i]:
+            ph["reduce"] += ev[0].elapsed_time(ev[1])
+            ph["wgrad"] += ev[1].elapsed_time(ev[2])
+            ph["dgrad"] += ev[2].elapsed_time(ev[3])
+    ph = {k: v / args.steps for k, v in ph.items()}
+
+    peaks, peak_src = load_peaks()
+    tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
+    gemm_half = flops / 2  # each of wgrad and dgrad carries half the FLOPs
+    dom = "wgrad" if ph["wgrad"] >= ph["dgrad"] else "dgrad"
+    achieved = gemm_half / (ph[dom] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": f"{dom} ({args.math})", "achieved": achieved,
+                "peak": tf32_peak, "unit": "TFLOP/s", "frac": achieved / tf32_peak,
+                "traffic": None,
+                "peak_source": f"{peak_src} bf16 {peaks['bf16_tflops']} x nominal tf32/bf16 "
+                               f"1.1/2.25 (burst)"}
+    red_gbs = red_bytes / (ph["reduce"] * 1e-3) / 1e9
+    gemm_ms = ph["wgrad"] + ph["dgrad"]
+    phases = {"reduce_ms": ph["reduce"], "wgrad_ms": ph["wgrad"], "dgrad_ms": ph["dgrad"],
+              "gemm_tflops": flops / (gemm_ms * 1e-3) / 1e12,
+              "gemm_frac_tf32": flops / (gemm_ms * 1e-3) / 1e12 / tf32_peak,
+              "reduce_gbs": red_gbs, "reduce_frac_hbm": red_gbs / peaks["hbm_gbs"],
+              "reduce_bytes": red_bytes}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(dls, layers, flops, args, stream, dev)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        cpu = cpu_baseline(layers, args.cpu_seconds)
+
+    g = layers[0]["geom"]
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "tf32" if math == cba.CBA_MATH_TF32 else "f32", "data": "synthetic",
+            "config": config_dict(args, layers, ws),
+            "roofline": roofline, "phases": phases, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def measure_e2e(dls, layers, flops, args, stream, dev):
+    """The same metric through the public call with HOST buffers: every step
+    copies the step's inputs from pinned host memory to the device, runs the
+    backward and reads the results back."""
+    import torch
+    names_in = ("x", "output", "z", "delta", "W", "gamma", "mean", "var", "residual")
+    names_out = ("dW", "db", "dgamma", "prev")
+    hosts = []
+    for dl in dls:
+        hin = {n: getattr(dl, n).cpu().pin_memory() for n in names_in
+               if getattr(dl, n) is not None}
+        hout = {n: torch.empty_like(getattr(dl, n), device="cpu").pin_memory()
+                for n in names_out if getattr(dl, n) is not None}
+        hosts.append((hin, hout))
+    h2d = sum(t.numel() * 4 for hin, _ in hosts for t in hin.values())
+    d2h = sum(t.numel() * 4 for _, hout in hosts for t in hout.values())
+
+    def one():
+        for dl, (hin, hout) in zip(dls, hosts):
+            for n, t in hin.items():
+                getattr(dl, n).copy_(t, non_blocking=True)
+            dl.run()
+            for n, t in hout.items():
+                t.copy_(getattr(dl, n), non_blocking=True)
+
+    steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(steps):
+        one()
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e) / steps
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * cba.h -- C ABI of libcba: the backward pass of a darknet/caffe-style
+ * convolutional layer (convolution + optional batch norm + activation) on
+ * one NVIDIA GB300 (sm_103a).
+ *
+ * What one call computes (source pages cited by title and section):
+ *
+ *   delta'   = delta * f'(output)                    gradient_array, leaky
+ *              f'(y) = (y > 0) ? 1 : 0.1, linear f' = 1
+ *              ("YOLOv3反向传播原理 之 全流程源码分析" §3.1, §7)
+ *   db      += sum_{n,p,q} delta'                    backward_bias (§3.1, §4)
+ *   with batch norm (training-mode statistics mean, var; §4):
+ *   dgamma  += sum_{n,p,q} delta' * x_norm           backward_scale_cpu
+ *   dz       = normalize_delta(scale_bias(delta'))   mean_delta_cpu,
+ *              variance_delta_cpu, normalize_delta_cpu; x_norm = (z - mean)
+ *              / sqrt(var + eps)
+ *   without batch norm: dz = delta'
+ *   dW      += dz . im2col(x)^T                      gemm(0,1,...,1,...) of §3.1
+ *   prev_delta (= or +=) col2im(W^T . dz) + residual gemm(1,0,...) + col2im_cpu
+ *              of §3.1 / §3.2; residual = the shortcut-layer delta (§5)
+ *
+ * The batch-norm steps are evaluated in the algebraically equal form
+ *   dz = a_k * delta' + b_k + c_k * (z - mean_k),
+ *   a_k = gamma_k / sigma_k, b_k = -a_k * S1_k / m, c_k = -a_k * S2_k / (m sigma_k),
+ *   sigma_k = sqrt(var_k + eps), S1 = sum delta', S2 = sum delta' * x_norm,
+ * m = N*P*Q, which is also caffe's BatchNormLayer::Backward_cpu times gamma
+ * ("BatchNorm 理解", Backward_cpu).
+ *
+ * Layouts: every tensor is contiguous fp32.  Activations are NCHW
+ * (batch-major): x, residual, prev_delta are [N][C][H][W]; output, z, delta,
+ * dz_out are [N][K][P][Q] with P = (H + 2 pad - R)/stride + 1 and
+ * Q = (W + 2 pad - S)/stride + 1 (floor division, im2col_cpu of §3.2).
+ * W and dW are [K][C][R][S]; gamma, mean, var, db, dgamma are [K].
+ *
+ * Ownership: every pointer is DEVICE memory owned by the caller.  The
+ * library allocates nothing and frees nothing; scratch comes from the
+ * caller's workspace (size from cba_workspace_bytes).  Calls are
+ * stream-ordered and asynchronous: they enqueue kernels on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream) and return without
+ * synchronising.  Two calls that share a workspace must not overlap in time.
+ *
+ * Errors: a negative return code; on any error nothing has been launched and
+ * no output touched, except CBA_ERR_CUDA (a launch failed; the CUDA error is
+ * cleared and recorded, see cba_last_cuda_error).  Device-side failures
+ * (a bounded wait that ran out) are reported through cba_get_status.
+ */
+#ifndef CBA_H_
+#define CBA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CBA_OK 0
+#define CBA_ERR_ARG (-1)         /* bad dimension, NULL required pointer, P or Q <= 0 */
+#define CBA_ERR_UNSUPPORTED (-2) /* shape beyond the library's limits (e.g. > 2^31 elements) */
+#define CBA_ERR_ALIGN (-3)       /* a pointer not 16-byte aligned */
+#define CBA_ERR_WORKSPACE (-4)   /* workspace NULL or smaller than cba_workspace_bytes() */
+#define CBA_ERR_CUDA (-5)        /* a CUDA launch or runtime call failed */
+#define CBA_ERR_DEVICE_TIMEOUT (-6) /* reported by cba_get_status: a device wait ran out */
+
+typedef enum { CBA_ACT_LINEAR = 0, CBA_ACT_LEAKY = 1 } cba_act_t;
+
+/* Arithmetic of the two convolution GEMMs.  TF32: tensor cores (tcgen05,
+ * inputs read as TF32, fp32 accumulation).  FFMA: fp32 fused multiply-add on
+ * the CUDA cores.  The reductions and the BN transform are fp32 (with fp64
+ * cross-block sums) in both modes. */
+typedef enum { CBA_MATH_TF32 = 0, CBA_MATH_FFMA = 1 } cba_math_t;
+
+typedef struct {
+    int N, C, H, W;     /* layer input x: batch, channels, height, width */
+    int K, R, S;        /* filters, kernel height, kernel width (groups = 1) */
+    int stride, pad;    /* the same in both spatial dimensions */
+    int act;            /* cba_act_t */
+    int batch_normalize;/* 1: BN in training mode (z, gamma, mean, var, dgamma used) */
+    int accumulate;     /* prev_delta: 0 writes, 1 adds onto its contents */
+    float eps;          /* BN epsilon inside the square root (1e-5 in darknet) */
+    int math;           /* cba_math_t */
+} cba_desc_t;
+
+/* Bytes of scratch one call with this descriptor needs (0 if the descriptor is
+ * invalid).  The workspace must be 256-byte aligned device memory. */
+size_t cba_workspace_bytes(const cba_desc_t *d);
+
+/* The backward of one conv(+BN)+activation layer; see the header comment.
+ *   x        [N,C,H,W] layer input (darknet net.input); required
+ *   output   [N,K,P,Q] post-activation output; required unless act = LINEAR
+ *   z        [N,K,P,Q] pre-BN convolution output (darknet l.x); required iff BN
+ *   delta    [N,K,P,Q] gradient at the output; required; NOT modified
+ *   W        [K,C,R,S] weights; required
+ *   gamma, mean, var [K] BN scale and batch statistics (biased variance);
+ *            required iff BN
+ *   residual [N,C,H,W] shortcut delta added into prev_delta; may be NULL
+ *   dW       [K,C,R,S] += ; required
+ *   db       [K]       += ; required
+ *   dgamma   [K]       += ; required iff BN
+ *   prev_delta [N,C,H,W] (= or += per accumulate); NULL skips the input
+ *            gradient (darknet's `if (net.delta)` at the first layer)
+ *   dz_out   [N,K,P,Q] optional debug copy of dz; usually NULL
+ *   workspace, workspace_bytes: scratch, see cba_workspace_bytes
+ *   stream   cudaStream_t to enqueue on
+ * Returns CBA_OK or a negative CBA_ERR_* code. */
+int cba_conv_bn_act_backward(const cba_desc_t *d, const float *x, const float *output,
+                             const float *z, const float *delta, const float *W,
+                             const float *gamma, const float *mean, const float *var,
+                             const float *residual, float *dW, float *db, float *dgamma,
+                             float *prev_delta, float *dz_out, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/* Same computation as cba_conv_bn_act_backward, for profiling.
+ * phase_events: NULL, or an array of 4 cudaEvent_t created by the caller;
+ *   the call records [0] before the reduction pass, [1] after it (the
+ *   per-channel coefficients are ready), [2] after the weight gradient and
+ *   [3] after the input gradient ([3] is recorded right after [2] when
+ *   prev_delta is NULL), all on `stream`.
+ * launches: NULL, or receives the number of kernels this call enqueued.
+ * Return codes as cba_conv_bn_act_backward. */
+int cba_conv_bn_act_backward_traced(const cba_desc_t *d, const float *x, const float *output,
+                                    const float *z, const float *delta, const float *W,
+                                    const float *gamma, const float *mean, const float *var,
+                                    const float *residual, float *dW, float *db, float *dgamma,
+                                    float *prev_delta, float *dz_out, void *workspace,
+                                    size_t workspace_bytes, void *stream,
+                                    void *const *phase_events, int *launches);
+
+/* Reads (and clears) the device status word of a workspace after the work on
+ * `stream` has finished: synchronises `stream`, then returns CBA_OK or
+ * CBA_ERR_DEVICE_TIMEOUT (a bounded device wait ran out; the kernel stopped
+ * early and its outputs are not valid), or CBA_ERR_CUDA. */
+int cba_get_status(void *workspace, size_t workspace_bytes, void *stream);
+
+/* Self-test of the bounded device wait: launches one block whose thread waits
+ * on a barrier phase that never completes, with a limit of `timeout_us`
+ * microseconds (1 .. 2,000,000).  The wait gives up and records
+ * CBA_ERR_DEVICE_TIMEOUT in the workspace status (read it back with
+ * cba_get_status).  Needs cba_workspace_bytes of any valid descriptor. */
+int cba_selftest_bounded_wait(void *workspace, size_t workspace_bytes, unsigned timeout_us,
+                              void *stream);
+
+/* Human-readable text of a CBA_* code (static storage). */
+const char *cba_error_string(int code);
+
+/* The cudaError_t of the last CBA_ERR_CUDA in this process (0 if none). */
+int cba_last_cuda_error(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int cba_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CBA_H_ */

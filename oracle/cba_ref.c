@@ -413,6 +413,36 @@ int cba_ref_conv_bn_act_backward(int N, int C, int H, int W, int K, int R, int S
     return rc;
 }
 
+/* Steps 1-2 of the chain alone (activation gradient, then BN backward or
+ * backward_bias), on the float inputs: dz receives the BN-input gradient the
+ * convolution GEMMs consume, db and dgamma accumulate.  Returns 0 or -1. */
+int cba_ref_backward_dz(int N, int K, int P, int Q, int act, int batch_normalize, float eps,
+                        const float *output, const float *z, const float *delta,
+                        const float *gamma, const float *mean, const float *var, double *dz,
+                        double *db, double *dgamma) {
+    if (N <= 0 || K <= 0 || P <= 0 || Q <= 0 || !delta || !dz || !db) return -1;
+    if (act != REF_ACT_LINEAR && !output) return -1;
+    if (batch_normalize && (!z || !gamma || !mean || !var || !dgamma)) return -1;
+    long nout = (long)N * K * P * Q;
+    double *y = widen(output, nout);
+    for (long i = 0; i < nout; ++i) dz[i] = (double)delta[i];
+    cba_ref_gradient_array(y, nout, act, dz);
+    free(y);
+    if (!batch_normalize) {
+        cba_ref_backward_bias(db, dz, N, K, P * Q);
+        return 0;
+    }
+    double *zz = widen(z, nout), *g = widen(gamma, K), *m = widen(mean, K), *v = widen(var, K);
+    double *xn = (double *)malloc(sizeof(double) * nout);
+    int rc = -1;
+    if (zz && g && m && v && xn) {
+        cba_ref_x_norm(zz, m, v, (double)eps, N, K, P * Q, xn);
+        rc = cba_ref_backward_batchnorm(zz, xn, m, v, g, (double)eps, N, K, P * Q, dz, db, dgamma);
+    }
+    free(zz); free(g); free(m); free(v); free(xn);
+    return rc;
+}
+
 /* ----------------------------------------- sampled outputs at full sizes */
 
 /* One weight-gradient element from its definition (gather form):

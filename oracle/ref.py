@@ -59,6 +59,9 @@ def lib():
         L.cba_ref_conv_bn_act_backward.restype = _i
         L.cba_ref_conv_bn_act_backward.argtypes = (
             [_i] * 12 + [ctypes.c_float] + [_fp] * 9 + [_dp] * 5)
+        L.cba_ref_backward_dz.restype = _i
+        L.cba_ref_backward_dz.argtypes = ([_i] * 6 + [ctypes.c_float] + [_fp] * 6 +
+                                          [_dp] * 3)
         L.cba_ref_wgrad_at.argtypes = [_dp, _fp] + geo + [_lp, _l, _dp]
         L.cba_ref_dgrad_at.argtypes = [_dp, _fp, _fp, _fp, _i] + geo + [_lp, _l, _dp]
         _lib = L
@@ -192,6 +195,26 @@ def conv_bn_act_backward(x, output, z, delta, Wt, gamma, mean, var, residual, *,
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return dict(dW=o_dW, db=o_db, dgamma=o_dg, prev_delta=o_prev, dz=o_dz)
+
+
+def backward_dz(output, z, delta, gamma, mean, var, *, act, batch_normalize, eps, db=None,
+                dgamma=None):
+    """Activation gradient + BN backward (or backward_bias) on the float inputs.
+    Returns (dz, db, dgamma) as float64 arrays (db/dgamma accumulate onto the
+    given arrays, zeros if None)."""
+    delta = np.ascontiguousarray(delta, np.float32)
+    N, K, P, Q = delta.shape
+    dz = np.empty(delta.shape)
+    o_db = np.zeros(K) if db is None else _f64(db).copy()
+    o_dg = (np.zeros(K) if dgamma is None else _f64(dgamma).copy()) if batch_normalize else None
+    f = lambda a: None if a is None else _pf(np.ascontiguousarray(a, np.float32))  # noqa: E731
+    keep = [output, z, delta, gamma, mean, var]
+    rc = lib().cba_ref_backward_dz(N, K, P, Q, int(act), int(bool(batch_normalize)),
+                                   ctypes.c_float(eps), *[f(a) for a in keep], _pd(dz), _pd(o_db),
+                                   _pd(o_dg))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return dz, o_db, o_dg
 
 
 def wgrad_at(dz, x, R, S, stride, pad, idx):

@@ -1,0 +1,209 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle.
+
+Element by element on reduced-batch versions of the five workloads (same
+channel and spatial geometry, so the tiles and ragged tails are the same),
+on sampled outputs at full size, and on edge shapes.  Bars (max |err| per
+tensor, relative to max |ref| of that tensor): 2e-3 for the TF32
+tensor-core mode, 1e-5 for the FFMA mode.
+"""
+import functools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import activation_backward_gb300 as cba
+from activation_backward_gb300 import inputs
+from activation_backward_gb300.layer import DeviceLayer
+
+pytestmark = pytest.mark.gpu
+
+TF32, FFMA = cba.CBA_MATH_TF32, cba.CBA_MATH_FFMA
+TOL = {TF32: 2e-3, FFMA: 1e-5}
+MATHS = [pytest.param(TF32, id="tf32"), pytest.param(FFMA, id="ffma")]
+KEYS = ("dW", "db", "dgamma", "prev_delta")
+
+
+@functools.lru_cache(maxsize=None)
+def config_layers(cid, batch=None):
+    return inputs.make_config(cid, batch=batch)
+
+
+def oracle_chain(ref, layer, **kw):
+    g = layer["geom"]
+    return ref.conv_bn_act_backward(layer["x"], layer["output"], layer["z"], layer["delta"],
+                                    layer["W"], layer["gamma"], layer["mean"], layer["var"],
+                                    layer["residual"], stride=g.stride, pad=g.pad,
+                                    act=layer["act"], batch_normalize=layer["bn"],
+                                    accumulate=kw.pop("accumulate", layer["accumulate"]),
+                                    eps=layer["eps"], **kw)
+
+
+def assert_close(got, exp, tol, what):
+    assert got.shape == exp.shape, (what, got.shape, exp.shape)
+    assert np.all(np.isfinite(got)), what
+    err = float(np.max(np.abs(got - exp))) if exp.size else 0.0
+    scale = float(np.max(np.abs(exp))) if exp.size else 0.0
+    assert err <= tol * scale + 1e-30, f"{what}: max|err| {err:.3e} > {tol} * {scale:.3e}"
+
+
+def run_gpu(layer, math, **kw):
+    dl = DeviceLayer(layer, math=math, **kw)
+    dl.run()
+    assert dl.status() == cba.CBA_OK
+    torch.cuda.synchronize()
+    return dl, dl.results()
+
+
+def test_the_in_tree_library_is_loaded(cuda_lib):
+    maps = open("/proc/self/maps").read()
+    here = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "activation_backward_gb300", "libcba.so")
+    assert os.path.realpath(here) in maps or here in maps
+
+
+SMALL = [(1, 4), (2, 2), (3, 2), (4, 4), (5, 2)]
+
+
+@pytest.mark.parametrize("math", MATHS)
+@pytest.mark.parametrize("cid,batch", SMALL, ids=[f"cfg{c}_n{b}" for c, b in SMALL])
+def test_parity_elementwise_reduced_batch(ref, cuda_lib, cid, batch, math):
+    for layer in config_layers(cid, batch):
+        _, got = run_gpu(layer, math)
+        exp = oracle_chain(ref, layer)
+        for k in KEYS:
+            if exp[k] is not None:
+                assert_close(got[k], exp[k], TOL[math], f"{layer['name']} {k}")
+
+
+@pytest.mark.parametrize("math", MATHS)
+@pytest.mark.parametrize("cid", [1, 2, 3, 4, 5])
+def test_parity_full_size_sampled(ref, cuda_lib, cid, math):
+    """Full workload sizes, the launch configuration the bench times.  db and
+    dgamma are checked in full; dW and prev_delta on 3000 sampled elements
+    each (plus the corners), computed one by one by the oracle."""
+    for li, layer in enumerate(config_layers(cid)):
+        g = layer["geom"]
+        _, got = run_gpu(layer, math)
+        dz, db, dg = ref.backward_dz(layer["output"], layer["z"], layer["delta"], layer["gamma"],
+                                     layer["mean"], layer["var"], act=layer["act"],
+                                     batch_normalize=layer["bn"], eps=layer["eps"])
+        tol = TOL[math]
+        assert_close(got["db"], db, tol, "db")
+        if layer["bn"]:
+            assert_close(got["dgamma"], dg, tol, "dgamma")
+        rng = np.random.default_rng(7 * cid + li)
+        nw = got["dW"].size
+        iw = np.unique(np.concatenate([rng.choice(nw, min(nw, 3000), replace=False),
+                                       [0, nw - 1]]))
+        ew = ref.wgrad_at(dz, layer["x"], g.R, g.S, g.stride, g.pad, iw)
+        assert_close(got["dW"].reshape(-1)[iw], ew, tol, "dW sampled")
+        npv = got["prev_delta"].size
+        ip = np.unique(np.concatenate([rng.choice(npv, 3000, replace=False), [0, npv - 1]]))
+        ep = ref.dgrad_at(dz, layer["W"], g.H, g.W, g.stride, g.pad, ip,
+                          residual=layer["residual"])
+        assert_close(got["prev_delta"].reshape(-1)[ip], ep, tol, "prev_delta sampled")
+
+
+EDGE = [
+    # N, C, H, W, K, R, S, stride, pad, act, bn
+    (2, 3, 7, 9, 5, 3, 3, 1, 1, 1, True),
+    (3, 17, 13, 11, 33, 3, 3, 2, 1, 1, True),
+    (2, 32, 13, 13, 255, 1, 1, 1, 0, 0, False),
+    (2, 20, 12, 12, 50, 5, 5, 1, 0, 0, False),
+    (1, 8, 6, 6, 7, 3, 3, 1, 0, 1, False),
+    (2, 5, 10, 9, 6, 2, 3, 2, 0, 1, True),
+    (1, 4, 5, 5, 3, 5, 5, 1, 2, 0, True),
+    (1, 3, 1, 1, 2, 1, 1, 1, 0, 1, True),
+    (2, 64, 9, 9, 130, 3, 3, 1, 1, 1, True),
+    (1, 129, 8, 8, 64, 3, 3, 2, 1, 1, True),
+    (4, 16, 16, 16, 16, 1, 1, 2, 0, 1, False),
+    (2, 24, 15, 14, 40, 3, 3, 3, 2, 0, True),
+]
+
+
+@pytest.mark.parametrize("math", MATHS)
+@pytest.mark.parametrize("case", EDGE, ids=[str(i) for i in range(len(EDGE))])
+def test_parity_edge_shapes(ref, cuda_lib, case, math):
+    N, C, H, W, K, R, S, st, pad, act, bn = case
+    spec = inputs.LayerSpec("edge", inputs.Geometry(N, C, H, W, K, R, S, st, pad), act, bn)
+    layer = inputs.make_layer(spec, 500 + EDGE.index(case), residual=True)
+    _, got = run_gpu(layer, math)
+    exp = oracle_chain(ref, layer)
+    for k in KEYS:
+        if exp[k] is not None:
+            assert_close(got[k], exp[k], TOL[math], k)
+
+
+@pytest.mark.parametrize("math", MATHS)
+def test_two_calls_accumulate(ref, cuda_lib, math):
+    layer = config_layers(2, 2)[0]
+    for acc in (0, 1):
+        dl = DeviceLayer(layer, math=math, accumulate=acc)
+        dl.run()
+        first = dl.results()
+        dl.run()
+        assert dl.status() == cba.CBA_OK
+        second = dl.results()
+        for k in ("dW", "db", "dgamma"):
+            assert_close(second[k], 2 * first[k], TOL[math], k)
+        exp_prev = 2 * first["prev_delta"] if acc else first["prev_delta"]
+        assert_close(second["prev_delta"], exp_prev, TOL[math], f"prev acc={acc}")
+
+
+def test_accumulate_onto_existing_prev(ref, cuda_lib):
+    layer = config_layers(3, 2)[0]
+    rng = np.random.default_rng(3)
+    seed = rng.standard_normal(layer["x"].shape).astype(np.float32)
+    _, got = run_gpu(layer, FFMA, accumulate=1, prev_init=seed)
+    exp = oracle_chain(ref, layer, accumulate=1, prev_delta=seed)
+    assert_close(got["prev_delta"], exp["prev_delta"], TOL[FFMA], "prev_delta")
+
+
+def test_prev_delta_null_skips_dgrad(ref, cuda_lib):
+    layer = config_layers(2, 2)[0]
+    _, got = run_gpu(layer, TF32, with_prev=False)
+    assert got["prev_delta"] is None
+    exp = oracle_chain(ref, layer, want_prev=False)
+    assert_close(got["dW"], exp["dW"], TOL[TF32], "dW")
+
+
+@pytest.mark.parametrize("cid", [2, 4])
+def test_dz_out_and_bn_identities(ref, cuda_lib, cid):
+    layer = config_layers(cid, 2)[0]
+    _, got = run_gpu(layer, FFMA, want_dz=True)
+    exp = oracle_chain(ref, layer, want_dz=True)
+    assert_close(got["dz"], exp["dz"], 1e-5, "dz")
+    if layer["bn"]:
+        s = got["dz"].sum(axis=(0, 2, 3))
+        assert np.max(np.abs(s)) <= 1e-4 * np.max(np.abs(got["dz"])) * got["dz"][:, 0].size ** 0.5
+
+
+@pytest.mark.parametrize("math", MATHS)
+def test_residual_block_chained(ref, cuda_lib, math):
+    """Config 5 as a chain: the 3x3 conv's prev_delta is the 1x1 conv's delta."""
+    conv2, conv1 = config_layers(5, 2)
+    dl2, got2 = run_gpu(conv2, math)
+    exp2 = oracle_chain(ref, conv2)
+    chained = dict(conv1, delta=exp2["prev_delta"].astype(np.float32))
+    dl1 = DeviceLayer(chained, math=math)
+    dl1.delta.copy_(dl2.prev)  # the GPU's own delta for the GPU chain
+    dl1.run()
+    assert dl1.status() == cba.CBA_OK
+    got1 = dl1.results()
+    exp1 = oracle_chain(ref, chained)
+    tol = 2 * TOL[math]  # two layers of rounding
+    for k in KEYS:
+        assert_close(got1[k], exp1[k], tol, f"conv1 {k}")
+
+
+def test_bounded_wait_reports_timeout(cuda_lib):
+    ws = torch.empty(4096, dtype=torch.uint8, device="cuda")
+    ws.zero_()
+    assert cba.cba_selftest_bounded_wait(ws, 2000) == cba.CBA_OK
+    assert cba.cba_get_status(ws) == cba.CBA_ERR_DEVICE_TIMEOUT
+    assert cba.cba_get_status(ws) == cba.CBA_OK  # cleared
+    # the context is still usable
+    layer = config_layers(1, 2)[0]
+    run_gpu(layer, TF32)
