@@ -135,6 +135,9 @@ def cba_conv_bn_act_backward_traced(desc, x, output, z, delta, W, gamma, mean, v
     ev = None
     if events is not None:
         assert len(events) == 4
+        for e in events:
+            if e.cuda_event == 0:  # torch creates the CUDA event on its first record
+                e.record()
         ev = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
     n = ctypes.c_int(0)
     rc = load().cba_conv_bn_act_backward_traced(

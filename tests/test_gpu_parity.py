@@ -40,12 +40,12 @@ def oracle_chain(ref, layer, **kw):
                                     eps=layer["eps"], **kw)
 
 
-def assert_close(got, exp, tol, what):
+def assert_close(got, exp, tol, what, atol=1e-30):
     assert got.shape == exp.shape, (what, got.shape, exp.shape)
     assert np.all(np.isfinite(got)), what
     err = float(np.max(np.abs(got - exp))) if exp.size else 0.0
     scale = float(np.max(np.abs(exp))) if exp.size else 0.0
-    assert err <= tol * scale + 1e-30, f"{what}: max|err| {err:.3e} > {tol} * {scale:.3e}"
+    assert err <= tol * scale + atol, f"{what}: max|err| {err:.3e} > {tol} * {scale:.3e} + {atol}"
 
 
 def run_gpu(layer, math, **kw):
@@ -131,9 +131,14 @@ def test_parity_edge_shapes(ref, cuda_lib, case, math):
     layer = inputs.make_layer(spec, 500 + EDGE.index(case), residual=True)
     _, got = run_gpu(layer, math)
     exp = oracle_chain(ref, layer)
+    # With one element per channel (N*P*Q = 1) every BN gradient is zero in
+    # exact arithmetic; fp32 leaves rounding noise of the size of the inputs
+    # times 2^-24, which an absolute floor admits.
+    atol = 1e-6 if bn and N * ((H + 2 * pad - R) // st + 1) * ((W + 2 * pad - S) // st + 1) == 1 \
+        else 1e-30
     for k in KEYS:
         if exp[k] is not None:
-            assert_close(got[k], exp[k], TOL[math], k)
+            assert_close(got[k], exp[k], TOL[math], k, atol=atol)
 
 
 @pytest.mark.parametrize("math", MATHS)
