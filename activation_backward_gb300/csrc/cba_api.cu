@@ -66,6 +66,7 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->wg_splits = (int)ceil_div(p->m, chunk);
 
     p->use_tc = (p->math == CBA_MATH_TF32) && tc_supported(*p);
+    if (p->use_tc) tc_plan(*p);
 
     // workspace carve-up
     size_t off = 0;

@@ -39,8 +39,9 @@ struct Plan {
     long long wg_chunk;  // reduction positions per split (multiple of the K tile)
     // tensor-core path
     int use_tc;
-    int tc_wg_splits;
+    int tc_wg_splits, tc_wg_bn, tc_wg_ntiles;
     long long tc_wg_chunk;
+    int tc_dg_bn, tc_dg_ntiles;
     // workspace layout (byte offsets from the base)
     size_t off_status, off_red, off_coef, off_wgpart, off_wt, total;
 };
@@ -66,8 +67,11 @@ cudaError_t launch_wgrad_tc(const Plan &p, const float *x, const float *delta,
 cudaError_t launch_dgrad_tc(const Plan &p, const float *Wt, const float *delta,
                             const float *output, const float *z, const float *residual,
                             float *prev, void *ws, cudaStream_t st, int *launches);
+cudaError_t launch_splitk_reduce(const Plan &p, const float *part, int splits, float *dW,
+                                 cudaStream_t st, int *launches);
 cudaError_t launch_selftest_wait(unsigned timeout_us, void *ws, cudaStream_t st);
 bool tc_supported(const Plan &p);
+void tc_plan(Plan &p);  // fills the tc_* fields
 
 template <typename T>
 inline T *ws_at(void *ws, size_t off) {

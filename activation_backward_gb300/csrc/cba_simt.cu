@@ -241,10 +241,16 @@ cudaError_t launch_wgrad_simt(const Plan &p, const float *x, const float *delta,
 #undef CBA_WG
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    *launches += 1;
+    return launch_splitk_reduce(p, part, p.wg_splits, dW, st, launches);
+}
+
+cudaError_t launch_splitk_reduce(const Plan &p, const float *part, int splits, float *dW,
+                                 cudaStream_t st, int *launches) {
     const long long nel = (long long)p.K * p.CRS;
     int blocks = (int)std::min<long long>((nel + 255) / 256, (long long)p.num_sms * 8);
-    splitk_reduce_kernel<<<blocks, 256, 0, st>>>(part, p.wg_splits, nel, dW);
-    *launches += 2;
+    splitk_reduce_kernel<<<blocks, 256, 0, st>>>(part, splits, nel, dW);
+    *launches += 1;
     return cudaGetLastError();
 }
 
