@@ -65,7 +65,8 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->wg_chunk = chunk;
     p->wg_splits = (int)ceil_div(p->m, chunk);
 
-    p->use_tc = (p->math == CBA_MATH_TF32) && tc_supported(*p);
+    p->use_tc2 = (p->math == CBA_MATH_TF32) && tc2_supported(*p);
+    p->use_tc = !p->use_tc2 && (p->math == CBA_MATH_TF32) && tc_supported(*p);
     if (p->use_tc) tc_plan(*p);
 
     // workspace carve-up
@@ -77,11 +78,15 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->off_coef = off;
     off = align_up(off + sizeof(Coef) * (size_t)p->K, 256);
     p->off_wgpart = off;
-    size_t wg_simt = sizeof(float) * (size_t)p->wg_splits * p->K * p->CRS;
+    size_t wg_simt = p->use_tc2 ? 0 : sizeof(float) * (size_t)p->wg_splits * p->K * p->CRS;
     size_t wg_tc = p->use_tc ? sizeof(float) * (size_t)p->tc_wg_splits * p->K * p->CRS : 0;
     off = align_up(off + std::max(wg_simt, wg_tc), 256);
     p->off_wt = off;
     if (p->use_tc) off = align_up(off + sizeof(float) * (size_t)nw, 256);
+    p->off_dzt = off;
+    if (p->use_tc2) off = align_up(off + tc2_dzt_bytes(*p), 256);
+    p->off_wr = off;
+    if (p->use_tc2) off = align_up(off + tc2_wr_bytes(*p), 256);
     p->total = off;
     return CBA_OK;
 }
@@ -176,6 +181,21 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     if (e == cudaSuccess && dz_out) {
         e = launch_dz_out(p, delta, output, z, workspace, dz_out, st);
         ++n_launch;
+    }
+    if (p.use_tc2) {
+        float *dzt = ws_at<float>(workspace, p.off_dzt);
+        if (e == cudaSuccess)
+            e = launch_dz_materialize(p, delta, output, z, workspace, dzt, st, &n_launch);
+        if (e == cudaSuccess) e = tr.mark(1);
+        if (e == cudaSuccess) e = launch_wgrad_tc2(p, x, dzt, dW, workspace, st, &n_launch);
+        if (e == cudaSuccess) e = tr.mark(2);
+        if (e == cudaSuccess && prev_delta)
+            e = launch_dgrad_tc2(p, Wt, dzt, residual, prev_delta, workspace,
+                                 ws_at<float>(workspace, p.off_wr), st, &n_launch);
+        if (e == cudaSuccess) e = tr.mark(3);
+        if (launches) *launches = n_launch;
+        if (e != cudaSuccess) return fail_cuda(e);
+        return CBA_OK;
     }
     if (e == cudaSuccess) e = tr.mark(1);
     if (e == cudaSuccess) {

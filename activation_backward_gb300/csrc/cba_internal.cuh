@@ -38,12 +38,13 @@ struct Plan {
     int wg_splits;
     long long wg_chunk;  // reduction positions per split (multiple of the K tile)
     // tensor-core path
-    int use_tc;
+    int use_tc;   // tensor cores, gather-producer kernels (cba_tc.cu)
+    int use_tc2;  // tensor cores, TMEM-operand kernels (cba_tc2.cu); preferred
     int tc_wg_splits, tc_wg_bn, tc_wg_ntiles;
     long long tc_wg_chunk;
     int tc_dg_bn, tc_dg_ntiles;
     // workspace layout (byte offsets from the base)
-    size_t off_status, off_red, off_coef, off_wgpart, off_wt, total;
+    size_t off_status, off_red, off_coef, off_wgpart, off_wt, off_dzt, off_wr, total;
 };
 
 // Builds the plan; returns CBA_OK or a CBA_ERR_* code.
@@ -72,6 +73,17 @@ cudaError_t launch_splitk_reduce(const Plan &p, const float *part, int splits, f
 cudaError_t launch_selftest_wait(unsigned timeout_us, void *ws, cudaStream_t st);
 bool tc_supported(const Plan &p);
 void tc_plan(Plan &p);  // fills the tc_* fields
+bool tc2_supported(const Plan &p);
+size_t tc2_dzt_bytes(const Plan &p);
+size_t tc2_wr_bytes(const Plan &p);
+cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float *output,
+                                  const float *z, const void *ws, float *dzt, cudaStream_t st,
+                                  int *launches);
+cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, float *dW,
+                             void *ws, cudaStream_t st, int *launches);
+cudaError_t launch_dgrad_tc2(const Plan &p, const float *Wt, const float *dzt,
+                             const float *residual, float *prev, void *ws, float *wr,
+                             cudaStream_t st, int *launches);
 
 template <typename T>
 inline T *ws_at(void *ws, size_t off) {
