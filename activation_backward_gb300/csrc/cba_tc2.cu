@@ -107,7 +107,7 @@ __global__ void repack_wr_kernel(const float *__restrict__ W, int K, int C, int 
 
 constexpr int kW2Ring = 6;  // dz row tiles resident
 constexpr int kW2NA = 4;    // A stages in TMEM (32 columns each)
-constexpr int kW2Threads = 192;
+constexpr int kW2Threads = 320;  // 8 producer warps, TMA warp, MMA warp
 
 struct Wg2Args {
     const float *x;
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         sb.abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         ptx::tmem_alloc(ptx::smem_u32(&sb.tmem_base), a.ncols);
         ptx::tmem_relinquish();
     }
@@ -175,16 +175,32 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     const uint32_t tmem = sb.tmem_base;
     const bool has_work = h0 < h1 && p_lo <= p_hi;
 
-    if (warp < 4) {
-        // ---- A producer: lane (c, s) of TMEM holds x[n][c0+c][h][q*st + s - pad]
-        const int L = warp * 32 + lane;
+    if (warp < 8) {
+        // ---- A producers: two groups of 4 warps take alternate input rows and
+        // load the next row of their group while storing the current one.
+        // TMEM lane (c, s) holds x[n][c0+c][h][q*st + s - pad] for 32 q.
+        const int grp = warp >> 2, wq = warp & 3;
+        const int L = wq * 32 + lane;
         const int cl = L / a.S, s = L - (L / a.S) * a.S;
         const bool lv = cl < ct_here;
         const float *xb = a.x + ((long long)n * a.C + c0 + (lv ? cl : 0)) * a.He * a.We;
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        const int nrows = has_work ? h1 - h0 : 0;
+        auto load_row = [&](float(&v)[32], int h) {
+            const float *xr = xb + (long long)h * a.We;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int q = q_base + j;
+                const int w = q * st + s - a.pad;
+                v[j] = (lv && q < a.Qe && w >= 0 && w < a.We) ? to_tf32(__ldg(xr + w)) : 0.f;
+            }
+        };
         bool ok = true;
-        int t = 0;
-        for (int h = h0; has_work && h < h1; ++h, ++t) {
+        float cur[32];
+        if (grp < nrows) load_row(cur, h0 + grp);
+        for (int t = grp; t < nrows; t += 2) {
+            float nxt[32];
+            if (t + 2 < nrows) load_row(nxt, h0 + t + 2);
             const int sa = t % kW2NA;
             if (t >= kW2NA)
                 ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_empty[sa]),
@@ -193,20 +209,15 @@ __global__ void __launch_bounds__(kW2Threads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            const float *xr = xb + (long long)h * a.We;
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int q = q_base + j;
-                const int w = q * st + s - a.pad;
-                v[j] = (lv && q < a.Qe && w >= 0 && w < a.We) ? to_tf32(__ldg(xr + w)) : 0.f;
-            }
-            ptx::tmem_st32(tmem + lane_addr + a_col0 + (uint32_t)(sa * 32), v);
+            ptx::tmem_st32(tmem + lane_addr + a_col0 + (uint32_t)(sa * 32), cur);
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[sa]));
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
         }
-        // ---- epilogue: D_r[(c, s)][k] -> dW[k][c][r][s]
+        // ---- epilogue: D_r[(c, s)][k] -> dW[k][c][r][s]; group g takes the
+        // 32-wide output-channel chunks kc = g, g + 2, ...
         if (has_work && ok)
             ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
                                         kLimitNs);
@@ -214,8 +225,8 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         if (ok) {
             ptx::tc_fence_after();
             const int pitch = ct_here * a.RS;  // floats per staged dW row segment
-            float *stg = reinterpret_cast<float *>(ring);
-            for (int kc = 0; kc * 32 < a.nk && k0 + kc * 32 < a.K; ++kc) {
+            float *stg = reinterpret_cast<float *>(ring) + grp * 32 * pitch;
+            for (int kc = grp; kc * 32 < a.nk && k0 + kc * 32 < a.K; kc += 2) {
                 const int krows = min(32, a.K - (k0 + kc * 32));
                 for (int r = 0; r < R; ++r) {
                     // was accumulator r written by any input row of this block?
@@ -226,9 +237,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
                     }
                     float v[32];
                     if (wr) {
-                        ptx::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) +
-                                           (uint32_t)(r * a.nk + kc * 32),
-                                       v);
+                        ptx::tmem_ld32(tmem + lane_addr + (uint32_t)(r * a.nk + kc * 32), v);
                         ptx::tmem_ld_wait();
                     } else {
 #pragma unroll
@@ -240,16 +249,18 @@ __global__ void __launch_bounds__(kW2Threads, 1)
                             for (int j = 0; j < 32; ++j)
                                 stg[j * pitch + cl * a.RS + r * a.S + s] = v[j];
                         } else {
-                            for (int j = 0; j < krows; ++j)
-                                atomicAdd(a.dW + ((long long)(k0 + kc * 32 + j) * a.C + c0 + cl) *
-                                                     a.RS + r * a.S + s,
-                                          v[j]);
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (j < krows)
+                                    atomicAdd(a.dW + ((long long)(k0 + kc * 32 + j) * a.C + c0 +
+                                                      cl) * a.RS + r * a.S + s,
+                                              v[j]);
                         }
                     }
                 }
                 if (a.bulk) {
                     ptx::fence_proxy_async_smem();
-                    ptx::named_bar_sync(1, 128);
+                    ptx::named_bar_sync(1 + grp, 128);
                     if (L < krows) {
                         ptx::bulk_reduce_add_f32(
                             a.dW + (long long)(k0 + kc * 32 + L) * a.CRS + (long long)c0 * a.RS,
@@ -257,12 +268,12 @@ __global__ void __launch_bounds__(kW2Threads, 1)
                         ptx::bulk_commit();
                         ptx::bulk_wait_read_all();
                     }
-                    ptx::named_bar_sync(1, 128);
+                    ptx::named_bar_sync(1 + grp, 128);
                 }
             }
             if (a.bulk && L < 32) ptx::bulk_wait_all();
         }
-    } else if (warp == 4) {
+    } else if (warp == 8) {
         // ---- TMA producer: dz rows p_lo..p_hi into the ring
         if (lane == 0 && has_work) {
             int issued = 0;
@@ -332,7 +343,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, a.ncols);
@@ -343,7 +354,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
 
 constexpr int kD2NA = 2;    // A stages in TMEM
 constexpr int kD2Ring = 4;  // B stages in shared memory
-constexpr int kD2Threads = 192;
+constexpr int kD2Threads = 320;  // 8 producer warps, TMA warp, MMA warp
 constexpr int kD2MaxTaps = 8;
 
 struct Dg2Args {
@@ -388,14 +399,14 @@ __global__ void __launch_bounds__(kD2Threads, 1)
             ptx::mbar_init(ptx::smem_u32(&sb.b_empty[i]), 1);
         }
         for (int i = 0; i < kD2NA; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&sb.a_full[i]), 128);
+            ptx::mbar_init(ptx::smem_u32(&sb.a_full[i]), 256);
             ptx::mbar_init(ptx::smem_u32(&sb.a_empty[i]), 1);
         }
         ptx::mbar_init(ptx::smem_u32(&sb.accum), 1);
         sb.abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         ptx::tmem_alloc(ptx::smem_u32(&sb.tmem_base), a.ncols);
         ptx::tmem_relinquish();
     }
@@ -404,26 +415,43 @@ __global__ void __launch_bounds__(kD2Threads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = sb.tmem_base;
 
-    if (warp < 4) {
-        const int L = warp * 32 + lane;
-        const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
-        // this lane's grid position in each of the block's tiles
-        int gn[2], gi[2], gj[2];
-        bool gv[2];
+    if (warp < 8) {
+        // ---- A producers.  Work unit of a group per stage: with two tiles,
+        // group g fills tile g (32 columns); with one tile, group g fills
+        // columns 16g..16g+15.  Each group loads its next stage while storing
+        // the current one.
+        const int grp = warp >> 2, wq = warp & 3;
+        const int L = wq * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        const int tt = a.T == 2 ? grp : 0;
+        const int j0 = a.T == 2 ? 0 : grp * 16;
+        const int tile = blockIdx.x * a.T + tt;
+        const long long g = (long long)tile * tstride + L;
+        const bool gv = tile < a.total_tiles && g < a.total_pos;
+        const long long gg = gv ? g : 0;
+        const long long per_img = (long long)a.Hc * a.Wx;
+        const int gn = (int)(gg / per_img);
+        const int grem = (int)(gg - (long long)gn * per_img);
+        const int gi = grem / a.Wx, gj = grem - (grem / a.Wx) * a.Wx;
+        const long long kstride = (long long)a.Pe * a.Qp;
+        auto load_stage = [&](float(&v)[32], int i) {
+            const int ri = i / a.kchunks, kc = i - (i / a.kchunks) * a.kchunks;
+            const int kb = kc * 32 + j0;
+            const int p = gi + a.dp[ri], q = gj + a.min_dq;
+            const bool pv = gv && p >= 0 && p < a.Pe && q >= 0 && q < a.Qe;
+            const float *src = a.dzt + (((long long)gn * a.K + kb) * a.Pe + (pv ? p : 0)) * a.Qp +
+                               (pv ? q : 0);
 #pragma unroll
-        for (int tt = 0; tt < 2; ++tt) {
-            const int tile = blockIdx.x * a.T + tt;
-            const long long g = (long long)tile * tstride + L;
-            gv[tt] = tt < a.T && tile < a.total_tiles && g < a.total_pos;
-            const long long gg = gv[tt] ? g : 0;
-            const long long per_img = (long long)a.Hc * a.Wx;
-            gn[tt] = (int)(gg / per_img);
-            const int rem = (int)(gg - (long long)gn[tt] * per_img);
-            gi[tt] = rem / a.Wx;
-            gj[tt] = rem - (rem / a.Wx) * a.Wx;
-        }
+            for (int j = 0; j < 32; ++j)
+                v[j] = (pv && j < (a.T == 2 ? 32 : 16) && kb + j < a.K) ? __ldg(src + j * kstride)
+                                                                         : 0.f;
+        };
         bool ok = true;
+        float cur[32];
+        if (nstages > 0) load_stage(cur, 0);
         for (int i = 0; i < nstages; ++i) {
+            float nxt[32];
+            if (i + 1 < nstages) load_stage(nxt, i + 1);
             const int sa = i % kD2NA;
             if (i >= kD2NA)
                 ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_empty[sa]),
@@ -432,82 +460,82 @@ __global__ void __launch_bounds__(kD2Threads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            const int ri = i / a.kchunks, kc = i - (i / a.kchunks) * a.kchunks;
-            const int kb = kc * 32;
-            for (int tt = 0; tt < a.T; ++tt) {
-                const int p = gi[tt] + a.dp[ri];
-                const int q = gj[tt] + a.min_dq;
-                const bool pv = gv[tt] && p >= 0 && p < a.Pe && q >= 0 && q < a.Qe;
-                const float *src =
-                    a.dzt + (((long long)gn[tt] * a.K + kb) * a.Pe + (pv ? p : 0)) * a.Qp +
-                    (pv ? q : 0);
-                const long long kstride = (long long)a.Pe * a.Qp;
-                float v[32];
+            const uint32_t col = a_col0 + (uint32_t)((sa * a.T + tt) * 32 + j0);
+            if (a.T == 2) {
+                ptx::tmem_st32(tmem + lane_addr + col, cur);
+            } else {
+                float h16[16];
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    v[j] = (pv && kb + j < a.K) ? __ldg(src + j * kstride) : 0.f;
-                ptx::tmem_st32(tmem + lane_addr + a_col0 + (uint32_t)((sa * a.T + tt) * 32), v);
+                for (int j = 0; j < 16; ++j) h16[j] = cur[j];
+                ptx::tmem_st16(tmem + lane_addr + col, h16);
             }
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[sa]));
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
         }
-        // ---- epilogue
+        // ---- epilogue.  Two tiles: group g finishes tile g with its own
+        // staging.  One tile: both groups stage half the columns each, then
+        // each writes half the output channels.
         if (ok && nstages > 0)
             ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
                                         kLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (ok) {
             ptx::tc_fence_after();
-            float *stg = reinterpret_cast<float *>(ring);
-            const long long HW = (long long)a.He * a.We;
-            for (int tt = 0; tt < a.T; ++tt) {
-                // E row of this lane -> staging
-                // ncol is a multiple of 16: 32-column loads, then a 16-column tail
-                int col = 0;
-                for (; col + 32 <= a.ncol; col += 32) {
-                    float v[32];
-                    if (nstages > 0) {
-                        ptx::tmem_ld32(tmem + lane_addr + (uint32_t)(tt * a.ncol + col), v);
-                        ptx::tmem_ld_wait();
-                    } else {
+            const bool two = a.T == 2;
+            float *stg = reinterpret_cast<float *>(ring) + (two ? grp * 128 * (int)a.pitch : 0);
+            const int half = (a.ncol / 2 + 15) / 16 * 16;
+            const int col_lo = two ? 0 : (grp == 0 ? 0 : half);
+            const int col_hi = two ? a.ncol : (grp == 0 ? half : a.ncol);
+            const int bar = two ? 1 + grp : 1, nthr = two ? 128 : 256;
+            int col = col_lo;
+            for (; col + 32 <= col_hi; col += 32) {
+                float v[32];
+                if (nstages > 0) {
+                    ptx::tmem_ld32(tmem + lane_addr + (uint32_t)(tt * a.ncol + col), v);
+                    ptx::tmem_ld_wait();
+                } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) stg[L * a.pitch + col + j] = v[j];
+                    for (int j = 0; j < 32; ++j) v[j] = 0.f;
                 }
-                if (col < a.ncol) {
-                    float v[16];
-                    if (nstages > 0) {
-                        ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(tt * a.ncol + col), v);
-                        ptx::tmem_ld_wait();
-                    } else {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                    }
+                for (int j = 0; j < 32; ++j) stg[L * a.pitch + col + j] = v[j];
+            }
+            if (col < col_hi) {  // 16-column tail
+                float v[16];
+                if (nstages > 0) {
+                    ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(tt * a.ncol + col), v);
+                    ptx::tmem_ld_wait();
+                } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) stg[L * a.pitch + col + j] = v[j];
+                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
                 }
-                ptx::named_bar_sync(1, 128);
-                const bool out = gv[tt] && L < tstride && gj[tt] < a.Wc && gi[tt] < a.Hc;
-                if (out) {
-                    const int h = gi[tt] * a.stride + a.ph, w = gj[tt] * a.stride + a.pw;
-                    const long long pix = (long long)gn[tt] * a.C * HW + (long long)h * a.We + w;
-                    for (int cl = 0; cl < a.c_tile && c0 + cl < a.C; ++cl) {
-                        float v = 0.f;
-                        for (int si = 0; si < a.ns; ++si)
-                            v += stg[(L + a.dq[si] - a.min_dq) * a.pitch + si * a.c_tile + cl];
-                        const long long idx = pix + (long long)(c0 + cl) * HW;
-                        if (a.residual) v += a.residual[idx];
-                        if (a.accumulate) v += a.prev[idx];
-                        a.prev[idx] = v;
-                    }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) stg[L * a.pitch + col + j] = v[j];
+            }
+            ptx::named_bar_sync(bar, nthr);
+            const bool out = gv && L < tstride && gj < a.Wc && gi < a.Hc;
+            if (out) {
+                const long long HW = (long long)a.He * a.We;
+                const int h = gi * a.stride + a.ph, w = gj * a.stride + a.pw;
+                const long long pix = (long long)gn * a.C * HW + (long long)h * a.We + w;
+                const int ch_half = (a.c_tile + 1) / 2;
+                const int cl_lo = two ? 0 : (grp == 0 ? 0 : ch_half);
+                const int cl_hi = two ? a.c_tile : (grp == 0 ? ch_half : a.c_tile);
+                for (int cl = cl_lo; cl < cl_hi && c0 + cl < a.C; ++cl) {
+                    float v = 0.f;
+                    for (int si = 0; si < a.ns; ++si)
+                        v += stg[(L + a.dq[si] - a.min_dq) * a.pitch + si * a.c_tile + cl];
+                    const long long idx = pix + (long long)(c0 + cl) * HW;
+                    if (a.residual) v += a.residual[idx];
+                    if (a.accumulate) v += a.prev[idx];
+                    a.prev[idx] = v;
                 }
-                ptx::named_bar_sync(1, 128);
             }
         }
-    } else if (warp == 4) {
+    } else if (warp == 8) {
         // ---- TMA producer: W slices (all kernel columns of the class) per stage
         if (lane == 0) {
             int issued = 0;
@@ -565,7 +593,7 @@ __global__ void __launch_bounds__(kD2Threads, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, a.ncols);
@@ -703,7 +731,8 @@ cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, fl
     a.splits_per_seg = (g.He + a.rows_per_split - 1) / a.rows_per_split;
     const int ct_last = p.C - ((p.C + a.ct - 1) / a.ct - 1) * a.ct;
     a.bulk = (p.CRS % 4 == 0) && ((a.ct * p.RS) % 4 == 0) && ((ct_last * p.RS) % 4 == 0);
-    if ((long long)32 * a.ct * p.RS * 4 > (long long)kW2Ring * a.nk * 128) a.bulk = 0;
+    // each producer group stages 32 rows of its dW segment in the ring
+    if ((long long)2 * 32 * a.ct * p.RS * 4 > (long long)kW2Ring * a.nk * 128) a.bulk = 0;
 
     CUtensorMap tm;
     const uint64_t d[4] = {(uint64_t)g.Qp, (uint64_t)g.Pe, (uint64_t)p.K, (uint64_t)p.N};
@@ -783,7 +812,7 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *Wt, const float *dzt,
         const uint32_t b[4] = {32, (uint32_t)a.c_tile, 1, 1};
         if (!encode_4d(&tmw, wr, d, b)) return cudaErrorInvalidValue;
         const size_t ring = (size_t)kD2Ring * a.ncol * 128;
-        const size_t stage = (size_t)128 * a.pitch * 4;
+        const size_t stage = (size_t)a.T * 128 * a.pitch * 4;  // one staging area per tile
         const size_t smem = std::max(ring, stage) + 1024;
         cudaError_t e = cudaFuncSetAttribute(dgrad_tc2_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
