@@ -185,7 +185,8 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     if (p.use_tc2) {
         float *dzt = ws_at<float>(workspace, p.off_dzt);
         if (e == cudaSuccess)
-            e = launch_dz_materialize(p, delta, output, z, workspace, dzt, st, &n_launch);
+            e = launch_dz_materialize(p, delta, output, z, workspace, dzt, prev_delta != nullptr,
+                                      st, &n_launch);
         if (e == cudaSuccess) e = tr.mark(1);
         if (e == cudaSuccess) e = launch_wgrad_tc2(p, x, dzt, dW, workspace, st, &n_launch);
         if (e == cudaSuccess) e = tr.mark(2);

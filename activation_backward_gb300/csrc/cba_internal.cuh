@@ -77,8 +77,8 @@ bool tc2_supported(const Plan &p);
 size_t tc2_dzt_bytes(const Plan &p);
 size_t tc2_wr_bytes(const Plan &p);
 cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float *output,
-                                  const float *z, const void *ws, float *dzt, cudaStream_t st,
-                                  int *launches);
+                                  const float *z, const void *ws, float *dzt, bool with_dzc,
+                                  cudaStream_t st, int *launches);
 cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, float *dW,
                              void *ws, cudaStream_t st, int *launches);
 cudaError_t launch_dgrad_tc2(const Plan &p, const float *Wt, const float *dzt,

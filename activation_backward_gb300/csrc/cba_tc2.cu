@@ -87,6 +87,49 @@ __global__ void dz_materialize_kernel(const float *__restrict__ delta,
     }
 }
 
+// dz in both layouts the GEMMs read, from one pass over delta/output/z:
+//   dzt [N][K][Pe][Qp]        rows padded to Qp (zeros), for the weight gradient
+//   dzc [N][Pp][Qpp][Kp]      channels-last with a zero border of bd_lo/bq_lo
+//                             rows/columns before the data, for the input gradient
+// A block transposes a 32 (columns) x 32 (channels) tile through shared memory.
+template <int ACT, bool BN>
+__global__ void __launch_bounds__(256)
+    dz_both_kernel(const float *__restrict__ delta, const float *__restrict__ output,
+                   const float *__restrict__ z, const Coef *__restrict__ coef, int K, int Pe,
+                   int Qe, int Qp, int Kp, int Pp, int Qpp, int bd_lo, int bq_lo, int qlo,
+                   float *__restrict__ dzt, float *__restrict__ dzc) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    const int n = blockIdx.z / Pp, pp = blockIdx.z - (blockIdx.z / Pp) * Pp, p = pp - bd_lo;
+    const bool prow = p >= 0 && p < Pe;
+    const int q0 = qlo + (int)blockIdx.x * 32, k0 = blockIdx.y * 32;
+    {
+        const int q = q0 + tx;
+        for (int kk = ty; kk < 32; kk += 8) {
+            const int k = k0 + kk;
+            float v = 0.f;
+            if (prow && k < K && q >= 0 && q < Qe) {
+                const long long off = (((long long)n * K + k) * Pe + p) * Qe + q;
+                const float y = (ACT == CBA_ACT_LEAKY) ? __ldg(output + off) : 0.f;
+                const float zz = BN ? __ldg(z + off) : 0.f;
+                v = to_tf32(dz_of<ACT, BN>(__ldg(delta + off), y, zz, coef[k]));
+            }
+            tile[kk][tx] = v;
+            if (prow && k < K && q >= 0 && q < Qp)
+                dzt[(((long long)n * K + k) * Pe + p) * Qp + q] = v;
+        }
+    }
+    __syncthreads();
+    {
+        const int k = k0 + tx;
+        for (int qq = ty; qq < 32; qq += 8) {
+            const int pq = q0 + qq + bq_lo;
+            if (pq >= 0 && pq < Qpp && k < Kp)
+                dzc[(((long long)n * Pp + pp) * Qpp + pq) * Kp + k] = tile[tx][qq];
+        }
+    }
+}
+
 // W[k][c][r][s] -> wr[r][s][c][kk] (kk < Kw; zero for kk >= K), TF32-rounded.
 __global__ void repack_wr_kernel(const float *__restrict__ W, int K, int C, int R, int S, int Kw,
                                  float *__restrict__ wr) {
@@ -105,8 +148,9 @@ __global__ void repack_wr_kernel(const float *__restrict__ W, int K, int C, int 
 
 // ------------------------------------------------------------------ wgrad
 
-constexpr int kW2Ring = 6;  // dz row tiles resident
-constexpr int kW2NA = 4;    // A stages in TMEM (32 columns each)
+constexpr int kW2RingMax = 6;  // dz row tiles resident (at most)
+constexpr int kW2NA = 4;       // A stages in TMEM (32 columns each)
+constexpr int kAStg = 3;       // cp.async staging depth of the A producers
 constexpr int kW2Threads = 320;  // 8 producer warps, TMA warp, MMA warp
 
 struct Wg2Args {
@@ -119,12 +163,13 @@ struct Wg2Args {
     int nqc;             // 32-wide output-column chunks per row
     int rows_per_split;  // input rows per block
     int splits_per_seg;
+    int ring;            // dz ring slots (>= R)
     int bulk;            // 1: bulk L2 reductions are aligned, 0: per-element atomics
     uint32_t ncols;      // TMEM columns allocated
 };
 
 struct W2Bars {
-    uint64_t dz_full[kW2Ring], dz_empty[kW2Ring], a_full[kW2NA], a_empty[kW2NA], accum;
+    uint64_t dz_full[kW2RingMax], dz_empty[kW2RingMax], a_full[kW2NA], a_empty[kW2NA], accum;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -153,7 +198,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     const uint32_t idesc = ptx::idesc_tf32(128, a.nk);
 
     if (tid == 0) {
-        for (int i = 0; i < kW2Ring; ++i) {
+        for (int i = 0; i < kW2RingMax; ++i) {
             ptx::mbar_init(ptx::smem_u32(&sb.dz_full[i]), 1);
             ptx::mbar_init(ptx::smem_u32(&sb.dz_empty[i]), 1);
         }
@@ -176,9 +221,11 @@ __global__ void __launch_bounds__(kW2Threads, 1)
     const bool has_work = h0 < h1 && p_lo <= p_hi;
 
     if (warp < 8) {
-        // ---- A producers: two groups of 4 warps take alternate input rows and
-        // load the next row of their group while storing the current one.
-        // TMEM lane (c, s) holds x[n][c0+c][h][q*st + s - pad] for 32 q.
+        // ---- A producers: two groups of 4 warps take alternate input rows.
+        // TMEM lane (c, s) holds x[n][c0+c][h][q*st + s - pad] for 32 q.  Each
+        // thread copies its 32 values for the rows kAStg ahead into a private
+        // shared-memory slot with cp.async (zero-filled outside the image),
+        // then moves the current row from the slot into TMEM.
         const int grp = warp >> 2, wq = warp & 3;
         const int L = wq * 32 + lane;
         const int cl = L / a.S, s = L - (L / a.S) * a.S;
@@ -186,21 +233,32 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         const float *xb = a.x + ((long long)n * a.C + c0 + (lv ? cl : 0)) * a.He * a.We;
         const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
         const int nrows = has_work ? h1 - h0 : 0;
-        auto load_row = [&](float(&v)[32], int h) {
-            const float *xr = xb + (long long)h * a.We;
+        float *ast = reinterpret_cast<float *>(ring + (size_t)a.ring * tile_bytes) +
+                     grp * (kAStg * 32 * 128) + L;
+        auto issue = [&](int t) {  // row h0 + t of this group into slot (t >> 1) % kAStg
+            if (t < nrows) {
+                const float *xr = xb + (long long)(h0 + t) * a.We;
+                const uint32_t dst = ptx::smem_u32(ast + ((t >> 1) % kAStg) * (32 * 128));
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int q = q_base + j;
-                const int w = q * st + s - a.pad;
-                v[j] = (lv && q < a.Qe && w >= 0 && w < a.We) ? to_tf32(__ldg(xr + w)) : 0.f;
+                for (int j = 0; j < 32; ++j) {
+                    const int q = q_base + j;
+                    const int w = q * st + s - a.pad;
+                    const bool ok = lv && q < a.Qe && w >= 0 && w < a.We;
+                    ptx::cp_async_4(dst + j * 128 * 4, ok ? xr + w : a.x, ok ? 4u : 0u);
+                }
             }
+            ptx::cp_async_commit();
         };
+#pragma unroll
+        for (int d = 0; d < kAStg; ++d) issue(grp + 2 * d);
         bool ok = true;
-        float cur[32];
-        if (grp < nrows) load_row(cur, h0 + grp);
         for (int t = grp; t < nrows; t += 2) {
-            float nxt[32];
-            if (t + 2 < nrows) load_row(nxt, h0 + t + 2);
+            ptx::cp_async_wait<kAStg - 1>();
+            const float *src = ast + ((t >> 1) % kAStg) * (32 * 128);
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = to_tf32(src[j * 128]);
+            issue(t + 2 * kAStg);
             const int sa = t % kW2NA;
             if (t >= kW2NA)
                 ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_empty[sa]),
@@ -209,13 +267,12 @@ __global__ void __launch_bounds__(kW2Threads, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            ptx::tmem_st32(tmem + lane_addr + a_col0 + (uint32_t)(sa * 32), cur);
+            ptx::tmem_st32(tmem + lane_addr + a_col0 + (uint32_t)(sa * 32), v);
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
             ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[sa]));
-#pragma unroll
-            for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
         }
+        ptx::cp_async_wait<0>();
         // ---- epilogue: D_r[(c, s)][k] -> dW[k][c][r][s]; group g takes the
         // 32-wide output-channel chunks kc = g, g + 2, ...
         if (has_work && ok)
@@ -278,10 +335,10 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         if (lane == 0 && has_work) {
             int issued = 0;
             for (int p = p_lo; p <= p_hi; ++p, ++issued) {
-                const int seq = p - p_lo, slot = seq % kW2Ring;
-                if (seq >= kW2Ring &&
+                const int seq = p - p_lo, slot = seq % a.ring;
+                if (seq >= a.ring &&
                     !ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_empty[slot]),
-                                            (uint32_t)(seq / kW2Ring - 1) & 1u, &sb.abort_flag,
+                                            (uint32_t)(seq / a.ring - 1) & 1u, &sb.abort_flag,
                                             a.status, kLimitNs))
                     break;
                 ptx::mbar_arrive_expect_tx(ptx::smem_u32(&sb.dz_full[slot]), tile_bytes);
@@ -290,9 +347,9 @@ __global__ void __launch_bounds__(kW2Threads, 1)
             }
             // no copy may be in flight when the block exits
             int no_abort = 0;
-            for (int seq = max(0, issued - kW2Ring); seq < issued; ++seq)
-                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[seq % kW2Ring]),
-                                       (uint32_t)(seq / kW2Ring) & 1u, &no_abort, a.status,
+            for (int seq = max(0, issued - a.ring); seq < issued; ++seq)
+                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[seq % a.ring]),
+                                       (uint32_t)(seq / a.ring) & 1u, &no_abort, a.status,
                                        kLimitNs);
         }
     } else {
@@ -314,9 +371,9 @@ __global__ void __launch_bounds__(kW2Threads, 1)
                     if (num < 0 || num % st) continue;
                     const int p = num / st;
                     if (p < p_lo || p > p_hi) continue;
-                    const int seq = p - p_lo, slot = seq % kW2Ring;
+                    const int seq = p - p_lo, slot = seq % a.ring;
                     ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[slot]),
-                                                (uint32_t)(seq / kW2Ring) & 1u, &sb.abort_flag,
+                                                (uint32_t)(seq / a.ring) & 1u, &sb.abort_flag,
                                                 a.status, kLimitNs);
                     if (!ok) break;
                     ptx::tc_fence_after();
@@ -332,7 +389,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
                 if (!ok) break;
                 ptx::mma_commit(ptx::smem_u32(&sb.a_empty[sa]));
                 while (p_rel <= p_hi && min(h1 - 1, p_rel * st - a.pad + R - 1) <= h) {
-                    ptx::mma_commit(ptx::smem_u32(&sb.dz_empty[(p_rel - p_lo) % kW2Ring]));
+                    ptx::mma_commit(ptx::smem_u32(&sb.dz_empty[(p_rel - p_lo) % a.ring]));
                     ++p_rel;
                 }
             }
@@ -352,61 +409,94 @@ __global__ void __launch_bounds__(kW2Threads, 1)
 
 // ------------------------------------------------------------------ dgrad
 
-constexpr int kD2NA = 2;    // A stages in TMEM
-constexpr int kD2Ring = 4;  // B stages in shared memory
-constexpr int kD2Threads = 320;  // 8 producer warps, TMA warp, MMA warp
+constexpr int kD3Stages = 3;
+constexpr int kD3Threads = 192;  // TMA warp, MMA warp, 4 epilogue warps
 constexpr int kD2MaxTaps = 8;
 
-struct Dg2Args {
-    const float *dzt;
+struct Dg3Args {
     const float *residual;
     float *prev;
     unsigned *status;
-    int C, He, We, K, Pe, Qe, Qp, stride, accumulate;
-    int ph, pw, Hc, Wc, Wx, min_dq, span;
+    int C, He, We, Pp, Qpp, bd_lo, bq_lo, stride, accumulate;
+    int ph, pw, Hc, Wc, min_dq, span;
     int nr, r_of[kD2MaxTaps], dp[kD2MaxTaps];
     int ns, s_of[kD2MaxTaps], dq[kD2MaxTaps];
-    int c_tile, ncol, kchunks, T, total_tiles;
-    long long total_pos;  // N * Hc * Wx
-    uint32_t ncols;       // TMEM columns allocated
-    uint32_t pitch;       // epilogue staging row pitch (floats)
+    int c_tile, ncol, kchunks, total_tiles;
+    long long total_pos;  // N * Pp * Qpp padded positions
+    uint32_t ncols;       // TMEM columns allocated (2 * ncol, power of 2)
 };
 
-struct D2Bars {
-    uint64_t b_full[kD2Ring], b_empty[kD2Ring], a_full[kD2NA], a_empty[kD2NA], accum;
+struct D3Bars {
+    uint64_t full[kD3Stages], empty[kD3Stages], accum;
     uint32_t tmem_base;
     int abort_flag;
 };
 
-__global__ void __launch_bounds__(kD2Threads, 1)
-    dgrad_tc2_kernel(const __grid_constant__ CUtensorMap tmw, const Dg2Args a) {
+// Output of one pixel (one staging lane): for each of its cl_hi channels, the
+// sum over the class's kernel columns of the staged E values at lane offsets
+// dq[si] (column-major staging, 128 lanes per column), plus the residual and,
+// if asked, the old value.  Restrict-qualified so that the staging reads of
+// the next channels are not ordered behind the global stores.
+__device__ __forceinline__ void dgrad_out_lane(const float *__restrict__ sl,
+                                               float *__restrict__ prev,
+                                               const float *__restrict__ residual, long long pix,
+                                               long long HW, int c0, int cl_hi, int c_tile, int ns,
+                                               const int (&dq)[kD2MaxTaps], int accumulate) {
+    for (int cl = 0; cl < cl_hi; cl += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = 0.f;
+        for (int si = 0; si < ns; ++si) {
+            const float *sc = sl + dq[si] + (si * c_tile + cl) * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (cl + u < cl_hi) v[u] += sc[u * 128];
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (cl + u < cl_hi) {
+                const long long idx = pix + (long long)(c0 + cl + u) * HW;
+                float o = v[u];
+                if (residual) o += residual[idx];
+                if (accumulate) o += prev[idx];
+                prev[idx] = o;
+            }
+        }
+    }
+}
+
+// Two 128-row tiles per block share every B stage.  A tiles come straight
+// from the channels-last zero-bordered dz (TMA, rows shifted by dp*Qpp for
+// kernel row r); no thread touches an operand.
+__global__ void __launch_bounds__(kD3Threads, 1)
+    dgrad_tc3_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmw,
+                     const Dg3Args a) {
     extern __shared__ uint8_t smem_dyn[];
-    uint8_t *ring = reinterpret_cast<uint8_t *>(
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    __shared__ D2Bars sb;
+    __shared__ D3Bars sb;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c0 = blockIdx.y * a.c_tile;
     const int tstride = 128 - a.span;
     const int nstages = a.nr * a.kchunks;
     const uint32_t b_bytes = (uint32_t)a.ncol * 128u;
-    const uint32_t a_col0 = (uint32_t)(a.T * a.ncol);
+    const uint32_t stage_bytes = 2u * 16384u + b_bytes;
     const uint32_t idesc = ptx::idesc_tf32(128, a.ncol);
+    long long m0[2];
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) m0[tt] = (long long)(blockIdx.x * 2 + tt) * tstride + a.min_dq;
 
     if (tid == 0) {
-        for (int i = 0; i < kD2Ring; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&sb.b_full[i]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sb.b_empty[i]), 1);
-        }
-        for (int i = 0; i < kD2NA; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&sb.a_full[i]), 256);
-            ptx::mbar_init(ptx::smem_u32(&sb.a_empty[i]), 1);
+        for (int i = 0; i < kD3Stages; ++i) {
+            ptx::mbar_init(ptx::smem_u32(&sb.full[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sb.empty[i]), 1);
         }
         ptx::mbar_init(ptx::smem_u32(&sb.accum), 1);
         sb.abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32(&sb.tmem_base), a.ncols);
         ptx::tmem_relinquish();
     }
@@ -415,185 +505,134 @@ __global__ void __launch_bounds__(kD2Threads, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = sb.tmem_base;
 
-    if (warp < 8) {
-        // ---- A producers.  Work unit of a group per stage: with two tiles,
-        // group g fills tile g (32 columns); with one tile, group g fills
-        // columns 16g..16g+15.  Each group loads its next stage while storing
-        // the current one.
-        const int grp = warp >> 2, wq = warp & 3;
-        const int L = wq * 32 + lane;
-        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
-        const int tt = a.T == 2 ? grp : 0;
-        const int j0 = a.T == 2 ? 0 : grp * 16;
-        const int tile = blockIdx.x * a.T + tt;
-        const long long g = (long long)tile * tstride + L;
-        const bool gv = tile < a.total_tiles && g < a.total_pos;
-        const long long gg = gv ? g : 0;
-        const long long per_img = (long long)a.Hc * a.Wx;
-        const int gn = (int)(gg / per_img);
-        const int grem = (int)(gg - (long long)gn * per_img);
-        const int gi = grem / a.Wx, gj = grem - (grem / a.Wx) * a.Wx;
-        const long long kstride = (long long)a.Pe * a.Qp;
-        auto load_stage = [&](float(&v)[32], int i) {
-            const int ri = i / a.kchunks, kc = i - (i / a.kchunks) * a.kchunks;
-            const int kb = kc * 32 + j0;
-            const int p = gi + a.dp[ri], q = gj + a.min_dq;
-            const bool pv = gv && p >= 0 && p < a.Pe && q >= 0 && q < a.Qe;
-            const float *src = a.dzt + (((long long)gn * a.K + kb) * a.Pe + (pv ? p : 0)) * a.Qp +
-                               (pv ? q : 0);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                v[j] = (pv && j < (a.T == 2 ? 32 : 16) && kb + j < a.K) ? __ldg(src + j * kstride)
-                                                                         : 0.f;
-        };
-        bool ok = true;
-        float cur[32];
-        if (nstages > 0) load_stage(cur, 0);
-        for (int i = 0; i < nstages; ++i) {
-            float nxt[32];
-            if (i + 1 < nstages) load_stage(nxt, i + 1);
-            const int sa = i % kD2NA;
-            if (i >= kD2NA)
-                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_empty[sa]),
-                                            (uint32_t)(i / kD2NA - 1) & 1u, &sb.abort_flag,
-                                            a.status, kLimitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            const uint32_t col = a_col0 + (uint32_t)((sa * a.T + tt) * 32 + j0);
-            if (a.T == 2) {
-                ptx::tmem_st32(tmem + lane_addr + col, cur);
-            } else {
-                float h16[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) h16[j] = cur[j];
-                ptx::tmem_st16(tmem + lane_addr + col, h16);
-            }
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[sa]));
-#pragma unroll
-            for (int j = 0; j < 32; ++j) cur[j] = nxt[j];
-        }
-        // ---- epilogue.  Two tiles: group g finishes tile g with its own
-        // staging.  One tile: both groups stage half the columns each, then
-        // each writes half the output channels.
-        if (ok && nstages > 0)
-            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
-                                        kLimitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-            ptx::tc_fence_after();
-            const bool two = a.T == 2;
-            float *stg = reinterpret_cast<float *>(ring) + (two ? grp * 128 * (int)a.pitch : 0);
-            const int half = (a.ncol / 2 + 15) / 16 * 16;
-            const int col_lo = two ? 0 : (grp == 0 ? 0 : half);
-            const int col_hi = two ? a.ncol : (grp == 0 ? half : a.ncol);
-            const int bar = two ? 1 + grp : 1, nthr = two ? 128 : 256;
-            int col = col_lo;
-            for (; col + 32 <= col_hi; col += 32) {
-                float v[32];
-                if (nstages > 0) {
-                    ptx::tmem_ld32(tmem + lane_addr + (uint32_t)(tt * a.ncol + col), v);
-                    ptx::tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) stg[L * a.pitch + col + j] = v[j];
-            }
-            if (col < col_hi) {  // 16-column tail
-                float v[16];
-                if (nstages > 0) {
-                    ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(tt * a.ncol + col), v);
-                    ptx::tmem_ld_wait();
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) v[j] = 0.f;
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) stg[L * a.pitch + col + j] = v[j];
-            }
-            ptx::named_bar_sync(bar, nthr);
-            const bool out = gv && L < tstride && gj < a.Wc && gi < a.Hc;
-            if (out) {
-                const long long HW = (long long)a.He * a.We;
-                const int h = gi * a.stride + a.ph, w = gj * a.stride + a.pw;
-                const long long pix = (long long)gn * a.C * HW + (long long)h * a.We + w;
-                const int ch_half = (a.c_tile + 1) / 2;
-                const int cl_lo = two ? 0 : (grp == 0 ? 0 : ch_half);
-                const int cl_hi = two ? a.c_tile : (grp == 0 ? ch_half : a.c_tile);
-                for (int cl = cl_lo; cl < cl_hi && c0 + cl < a.C; ++cl) {
-                    float v = 0.f;
-                    for (int si = 0; si < a.ns; ++si)
-                        v += stg[(L + a.dq[si] - a.min_dq) * a.pitch + si * a.c_tile + cl];
-                    const long long idx = pix + (long long)(c0 + cl) * HW;
-                    if (a.residual) v += a.residual[idx];
-                    if (a.accumulate) v += a.prev[idx];
-                    a.prev[idx] = v;
-                }
-            }
-        }
-    } else if (warp == 8) {
-        // ---- TMA producer: W slices (all kernel columns of the class) per stage
+    if (warp == 0) {
+        // ---- TMA producer: per stage (kernel row r, 32 output channels k):
+        // A of both tiles and the W slices of all kernel columns of the class
         if (lane == 0) {
             int issued = 0;
             for (int i = 0; i < nstages; ++i, ++issued) {
-                const int slot = i % kD2Ring;
-                if (i >= kD2Ring &&
-                    !ptx::mbar_wait_bounded(ptx::smem_u32(&sb.b_empty[slot]),
-                                            (uint32_t)(i / kD2Ring - 1) & 1u, &sb.abort_flag,
+                const int slot = i % kD3Stages;
+                if (i >= kD3Stages &&
+                    !ptx::mbar_wait_bounded(ptx::smem_u32(&sb.empty[slot]),
+                                            (uint32_t)(i / kD3Stages - 1) & 1u, &sb.abort_flag,
                                             a.status, kLimitNs))
                     break;
                 const int ri = i / a.kchunks, kc = i - (i / a.kchunks) * a.kchunks;
-                ptx::mbar_arrive_expect_tx(ptx::smem_u32(&sb.b_full[slot]), b_bytes);
+                const uint32_t bar = ptx::smem_u32(&sb.full[slot]);
+                uint8_t *st = smem + (size_t)slot * stage_bytes;
+                ptx::mbar_arrive_expect_tx(bar, stage_bytes);
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt)
+                    ptx::tma_load_2d(ptx::smem_u32(st + tt * 16384), &tma, kc * 32,
+                                     (int)(m0[tt] + (long long)a.dp[ri] * a.Qpp), bar);
                 for (int si = 0; si < a.ns; ++si)
-                    ptx::tma_load_4d(ptx::smem_u32(ring + (size_t)slot * b_bytes +
-                                                   (size_t)si * a.c_tile * 128),
-                                     &tmw, kc * 32, c0, a.s_of[si], a.r_of[ri],
-                                     ptx::smem_u32(&sb.b_full[slot]));
+                    ptx::tma_load_4d(ptx::smem_u32(st + 32768 + (size_t)si * a.c_tile * 128), &tmw,
+                                     kc * 32, c0, a.s_of[si], a.r_of[ri], bar);
             }
             int no_abort = 0;
-            for (int i = max(0, issued - kD2Ring); i < issued; ++i)
-                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.b_full[i % kD2Ring]),
-                                       (uint32_t)(i / kD2Ring) & 1u, &no_abort, a.status,
+            for (int i = max(0, issued - kD3Stages); i < issued; ++i)
+                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.full[i % kD3Stages]),
+                                       (uint32_t)(i / kD3Stages) & 1u, &no_abort, a.status,
                                        kLimitNs);
         }
-    } else {
+    } else if (warp == 1) {
         // ---- MMA issuer
         if (lane == 0 && nstages > 0) {
             bool ok = true;
             for (int i = 0; ok && i < nstages; ++i) {
-                const int sa = i % kD2NA, slot = i % kD2Ring;
-                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_full[sa]),
-                                            (uint32_t)(i / kD2NA) & 1u, &sb.abort_flag, a.status,
-                                            kLimitNs) &&
-                     ptx::mbar_wait_bounded(ptx::smem_u32(&sb.b_full[slot]),
-                                            (uint32_t)(i / kD2Ring) & 1u, &sb.abort_flag,
+                const int slot = i % kD3Stages;
+                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.full[slot]),
+                                            (uint32_t)(i / kD3Stages) & 1u, &sb.abort_flag,
                                             a.status, kLimitNs);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                const uint32_t b_base = ptx::smem_u32(ring + (size_t)slot * b_bytes);
-                for (int tt = 0; tt < a.T; ++tt) {
+                const uint32_t base = ptx::smem_u32(smem + (size_t)slot * stage_bytes);
+                for (int tt = 0; tt < 2; ++tt) {
+#pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t bd = ptx::smem_desc(b_base + ks * 32, 16, 1024, 2);
-                        ptx::mma_tf32_ts(tmem + (uint32_t)(tt * a.ncol),
-                                         tmem + a_col0 + (uint32_t)((sa * a.T + tt) * 32 + ks * 8),
-                                         bd, idesc, (i > 0 || ks > 0) ? 1u : 0u);
+                        const uint64_t ad = ptx::smem_desc(base + tt * 16384 + ks * 32, 16, 1024, 2);
+                        const uint64_t bd = ptx::smem_desc(base + 32768 + ks * 32, 16, 1024, 2);
+                        ptx::mma_tf32(tmem + (uint32_t)(tt * a.ncol), ad, bd, idesc,
+                                      (i > 0 || ks > 0) ? 1u : 0u);
                     }
                 }
-                ptx::mma_commit(ptx::smem_u32(&sb.a_empty[sa]));
-                ptx::mma_commit(ptx::smem_u32(&sb.b_empty[slot]));
+                ptx::mma_commit(ptx::smem_u32(&sb.empty[slot]));
             }
             ptx::mma_commit(ptx::smem_u32(&sb.accum));
             int no_abort = 0;
             ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &no_abort, a.status, kLimitNs);
         }
+    } else {
+        // ---- epilogue (warps 2-5): E -> column-major staging -> shifted sum over
+        // the kernel columns -> + residual (+ old prev_delta) -> prev_delta
+        const int wq = warp & 3;
+        const int L = wq * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        bool ok = true;
+        if (nstages > 0)
+            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
+                                        kLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+            ptx::tc_fence_after();
+            float *stg = reinterpret_cast<float *>(smem);
+            const long long HW = (long long)a.He * a.We;
+            const long long plane = (long long)a.Pp * a.Qpp;
+            for (int tt = 0; tt < 2; ++tt) {
+                int col = 0;
+                for (; col + 32 <= a.ncol; col += 32) {
+                    float v[32];
+                    if (nstages > 0) {
+                        ptx::tmem_ld32(tmem + lane_addr + (uint32_t)(tt * a.ncol + col), v);
+                        ptx::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) stg[(col + j) * 128 + L] = v[j];
+                }
+                if (col < a.ncol) {
+                    float v[16];
+                    if (nstages > 0) {
+                        ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(tt * a.ncol + col), v);
+                        ptx::tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) v[j] = 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) stg[(col + j) * 128 + L] = v[j];
+                }
+                ptx::named_bar_sync(1, 128);
+                // home lane L: padded position m = m0 + L - min_dq
+                const long long m = m0[tt] + L - a.min_dq;
+                const int tile = blockIdx.x * 2 + tt;
+                bool out = L < tstride && tile < a.total_tiles && m >= 0 && m < a.total_pos;
+                int n = 0, i = 0, j = 0;
+                if (out) {
+                    n = (int)(m / plane);
+                    const int rem = (int)(m - (long long)n * plane);
+                    i = rem / a.Qpp - a.bd_lo;
+                    j = rem % a.Qpp - a.bq_lo;
+                    out = i >= 0 && i < a.Hc && j >= 0 && j < a.Wc;
+                }
+                if (out) {
+                    const int h = i * a.stride + a.ph, w = j * a.stride + a.pw;
+                    const long long pix = (long long)n * a.C * HW + (long long)h * a.We + w;
+                    int dqr[kD2MaxTaps];
+#pragma unroll
+                    for (int si = 0; si < kD2MaxTaps; ++si) dqr[si] = a.dq[si] - a.min_dq;
+                    dgrad_out_lane(stg + L, a.prev, a.residual, pix, HW, c0,
+                                   min(a.c_tile, a.C - c0), a.c_tile, a.ns, dqr, a.accumulate);
+                }
+                ptx::named_bar_sync(1, 128);
+            }
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, a.ncols);
@@ -642,11 +681,49 @@ inline uint32_t pow2_cols(int need) {
 
 }  // namespace
 
-// Geometry the v2 kernels work in: 1x1 stride-1 unpadded layers are viewed as
-// one row per plane.
+// Geometry the TMEM/TMA kernels work in.  1x1 stride-1 unpadded layers are
+// viewed as one row per plane.  The channels-last dz copy carries a zero border
+// wide enough for every row shift dp and column shift dq of every stride
+// phase class of the input gradient.
 struct V2Geom {
     int He, We, Pe, Qe, Qp;
+    int Kp, Pp, Qpp, bd_lo, bq_lo;
 };
+
+struct ClassTaps {
+    int Hc, Wc, nr, ns, r_of[kD2MaxTaps], dp[kD2MaxTaps], s_of[kD2MaxTaps], dq[kD2MaxTaps];
+    int min_dq, max_dq, min_dp, max_dp;
+};
+
+static ClassTaps class_taps(const Plan &p, int He, int We, int cl) {
+    ClassTaps c;
+    const int sd = p.stride, ph = cl / sd, pw = cl % sd;
+    c.Hc = ph < He ? (He - ph + sd - 1) / sd : 0;
+    c.Wc = pw < We ? (We - pw + sd - 1) / sd : 0;
+    c.nr = c.ns = 0;
+    c.min_dp = c.min_dq = 1 << 30;
+    c.max_dp = c.max_dq = -(1 << 30);
+    for (int r = (ph + p.pad) % sd; r < p.R && c.nr < kD2MaxTaps; r += sd) {
+        c.r_of[c.nr] = r;
+        c.dp[c.nr] = (ph + p.pad - r) / sd;
+        c.min_dp = std::min(c.min_dp, c.dp[c.nr]);
+        c.max_dp = std::max(c.max_dp, c.dp[c.nr]);
+        ++c.nr;
+    }
+    for (int s = (pw + p.pad) % sd; s < p.S && c.ns < kD2MaxTaps; s += sd) {
+        c.s_of[c.ns] = s;
+        c.dq[c.ns] = (pw + p.pad - s) / sd;
+        c.min_dq = std::min(c.min_dq, c.dq[c.ns]);
+        c.max_dq = std::max(c.max_dq, c.dq[c.ns]);
+        ++c.ns;
+    }
+    if (c.nr == 0 || c.ns == 0) {  // no kernel tap reaches this class
+        c.nr = c.ns = 0;
+        c.min_dp = c.max_dp = c.min_dq = c.max_dq = 0;
+    }
+    return c;
+}
+
 static V2Geom v2_geom(const Plan &p) {
     V2Geom g;
     const bool flat = p.R == 1 && p.S == 1 && p.stride == 1 && p.pad == 0;
@@ -655,21 +732,41 @@ static V2Geom v2_geom(const Plan &p) {
     g.Pe = flat ? 1 : p.P;
     g.Qe = flat ? p.P * p.Q : p.Q;
     g.Qp = (g.Qe + 3) / 4 * 4;
+    g.Kp = (p.K + 3) / 4 * 4;
+    int blo = 0, bhi = 0, qlo = 0, qhi = 0;
+    for (int cl = 0; cl < p.stride * p.stride; ++cl) {
+        const ClassTaps c = class_taps(p, g.He, g.We, cl);
+        if (c.Hc == 0 || c.Wc == 0 || c.nr == 0) continue;
+        blo = std::max(blo, -c.min_dp);
+        bhi = std::max(bhi, c.Hc - 1 + c.max_dp - (g.Pe - 1));
+        qlo = std::max(qlo, -c.min_dq);
+        qhi = std::max(qhi, c.Wc - 1 + c.max_dq - (g.Qe - 1));
+    }
+    g.bd_lo = blo;
+    g.bq_lo = qlo;
+    g.Pp = g.Pe + blo + bhi;
+    g.Qpp = g.Qe + qlo + qhi;
     return g;
 }
 
+static size_t dzt_bytes_only(const Plan &p, const V2Geom &g) {
+    return ((sizeof(float) * (size_t)p.N * p.K * g.Pe * g.Qp) + 255) / 256 * 256;
+}
+
 bool tc2_supported(const Plan &p) {
-    const V2Geom g = v2_geom(p);
     if (p.stride > 4 || p.R > kD2MaxTaps || p.S > kD2MaxTaps) return false;
+    const V2Geom g = v2_geom(p);
     if ((long long)p.N * p.K * g.Pe * g.Qp >= (1LL << 31)) return false;
-    // dgrad column shift span must leave room in a 128-row tile
+    if ((long long)p.N * g.Pp * g.Qpp * g.Kp >= (1LL << 31)) return false;
+    if ((long long)p.N * g.Pp > 65535) return false;  // grid.z of the dz pass
+    // the input gradient's column shifts must leave room in a 128-row tile
     if ((p.S - 1) / p.stride + 1 > 32) return false;
     return encode_fn() != nullptr;
 }
 
 size_t tc2_dzt_bytes(const Plan &p) {
     const V2Geom g = v2_geom(p);
-    return sizeof(float) * (size_t)p.N * p.K * g.Pe * g.Qp;
+    return dzt_bytes_only(p, g) + sizeof(float) * (size_t)p.N * g.Pp * g.Qpp * g.Kp;
 }
 
 size_t tc2_wr_bytes(const Plan &p) {
@@ -677,25 +774,45 @@ size_t tc2_wr_bytes(const Plan &p) {
 }
 
 cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float *output,
-                                  const float *z, const void *ws, float *dzt, cudaStream_t st,
-                                  int *launches) {
+                                  const float *z, const void *ws, float *dzt, bool with_dzc,
+                                  cudaStream_t st, int *launches) {
     const V2Geom g = v2_geom(p);
     const Coef *coef = ws_at<Coef>(ws, p.off_coef);
-    const long long rows = (long long)p.N * p.K * g.Pe;
-    const long long total = rows * (g.Qp / 4);
-    const int blocks = (int)std::min<long long>((total + 255) / 256, (long long)p.num_sms * 16);
     const bool leaky = p.act == CBA_ACT_LEAKY;
+    if (with_dzc) {
+        float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) + dzt_bytes_only(p, g));
+        const int qlo = -g.bq_lo;
+        const int qhi = std::max(g.Qpp - g.bq_lo, g.Qp);
+        dim3 grid((unsigned)((qhi - qlo + 31) / 32), (unsigned)((g.Kp + 31) / 32),
+                  (unsigned)(p.N * g.Pp));
+#define CBA_DZB(A, B)                                                                          \
+    dz_both_kernel<A, B><<<grid, 256, 0, st>>>(delta, output, z, coef, p.K, g.Pe, g.Qe, g.Qp,   \
+                                               g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, qlo, dzt, \
+                                               dzc)
+        if (p.bn) {
+            if (leaky) CBA_DZB(CBA_ACT_LEAKY, true);
+            else CBA_DZB(CBA_ACT_LINEAR, true);
+        } else {
+            if (leaky) CBA_DZB(CBA_ACT_LEAKY, false);
+            else CBA_DZB(CBA_ACT_LINEAR, false);
+        }
+#undef CBA_DZB
+    } else {
+        const long long rows = (long long)p.N * p.K * g.Pe;
+        const long long total = rows * (g.Qp / 4);
+        const int blocks = (int)std::min<long long>((total + 255) / 256, (long long)p.num_sms * 16);
 #define CBA_DZM(A, B)                                                                            \
     dz_materialize_kernel<A, B><<<blocks, 256, 0, st>>>(delta, output, z, coef, p.K, g.Pe, g.Qe, \
                                                         g.Qp, rows, dzt)
-    if (p.bn) {
-        if (leaky) CBA_DZM(CBA_ACT_LEAKY, true);
-        else CBA_DZM(CBA_ACT_LINEAR, true);
-    } else {
-        if (leaky) CBA_DZM(CBA_ACT_LEAKY, false);
-        else CBA_DZM(CBA_ACT_LINEAR, false);
-    }
+        if (p.bn) {
+            if (leaky) CBA_DZM(CBA_ACT_LEAKY, true);
+            else CBA_DZM(CBA_ACT_LINEAR, true);
+        } else {
+            if (leaky) CBA_DZM(CBA_ACT_LEAKY, false);
+            else CBA_DZM(CBA_ACT_LINEAR, false);
+        }
 #undef CBA_DZM
+    }
     *launches += 1;
     return cudaGetLastError();
 }
@@ -731,14 +848,18 @@ cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, fl
     a.splits_per_seg = (g.He + a.rows_per_split - 1) / a.rows_per_split;
     const int ct_last = p.C - ((p.C + a.ct - 1) / a.ct - 1) * a.ct;
     a.bulk = (p.CRS % 4 == 0) && ((a.ct * p.RS) % 4 == 0) && ((ct_last * p.RS) % 4 == 0);
+    // dz ring: as many row tiles as fit next to the A staging (at least R)
+    const size_t astg = (size_t)2 * kAStg * 32 * 128 * 4;
+    a.ring = (int)std::min<size_t>(kW2RingMax, (220 * 1024 - astg) / ((size_t)a.nk * 128));
+    if (a.ring < p.R) return cudaErrorNotSupported;
     // each producer group stages 32 rows of its dW segment in the ring
-    if ((long long)2 * 32 * a.ct * p.RS * 4 > (long long)kW2Ring * a.nk * 128) a.bulk = 0;
+    if ((long long)2 * 32 * a.ct * p.RS * 4 > (long long)a.ring * a.nk * 128) a.bulk = 0;
 
     CUtensorMap tm;
     const uint64_t d[4] = {(uint64_t)g.Qp, (uint64_t)g.Pe, (uint64_t)p.K, (uint64_t)p.N};
     const uint32_t b[4] = {32, 1, (uint32_t)a.nk, 1};
     if (!encode_4d(&tm, dzt, d, b)) return cudaErrorInvalidValue;
-    const size_t smem = (size_t)kW2Ring * a.nk * 128 + 1024;
+    const size_t smem = (size_t)a.ring * a.nk * 128 + astg + 1024;
     cudaError_t e = cudaFuncSetAttribute(wgrad_tc2_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -761,65 +882,65 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *Wt, const float *dzt,
         if (e != cudaSuccess) return e;
         *launches += 1;
     }
-    const int sdv = p.stride;
-    for (int cl = 0; cl < sdv * sdv; ++cl) {
-        Dg2Args a;
-        a.dzt = dzt; a.residual = residual; a.prev = prev;
+    const float *dzc =
+        reinterpret_cast<const float *>(reinterpret_cast<const char *>(dzt) + dzt_bytes_only(p, g));
+    const long long total_pos = (long long)p.N * g.Pp * g.Qpp;
+    CUtensorMap tma;
+    {
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return cudaErrorNotSupported;
+        cuuint64_t dims[2] = {(cuuint64_t)g.Kp, (cuuint64_t)total_pos};
+        cuuint64_t strides[1] = {(cuuint64_t)g.Kp * 4};
+        cuuint32_t box[2] = {32, 128};
+        cuuint32_t es[2] = {1, 1};
+        if (fn(&tma, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(dzc), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
+            CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    for (int cl = 0; cl < p.stride * p.stride; ++cl) {
+        const ClassTaps c = class_taps(p, g.He, g.We, cl);
+        if (c.Hc == 0 || c.Wc == 0) continue;
+        Dg3Args a;
+        a.residual = residual; a.prev = prev;
         a.status = ws_at<unsigned>(ws, p.off_status);
-        a.C = p.C; a.He = g.He; a.We = g.We; a.K = p.K; a.Pe = g.Pe; a.Qe = g.Qe; a.Qp = g.Qp;
-        a.stride = sdv; a.accumulate = p.accumulate;
-        a.ph = cl / sdv; a.pw = cl % sdv;
-        a.Hc = a.ph < g.He ? (g.He - a.ph + sdv - 1) / sdv : 0;
-        a.Wc = a.pw < g.We ? (g.We - a.pw + sdv - 1) / sdv : 0;
-        if (a.Hc == 0 || a.Wc == 0) continue;
-        a.nr = 0;
-        for (int r = (a.ph + p.pad) % sdv; r < p.R; r += sdv) {
-            a.r_of[a.nr] = r;
-            a.dp[a.nr] = (a.ph + p.pad - r) / sdv;
-            ++a.nr;
+        a.C = p.C; a.He = g.He; a.We = g.We; a.Pp = g.Pp; a.Qpp = g.Qpp;
+        a.bd_lo = g.bd_lo; a.bq_lo = g.bq_lo; a.stride = p.stride; a.accumulate = p.accumulate;
+        a.ph = cl / p.stride; a.pw = cl % p.stride; a.Hc = c.Hc; a.Wc = c.Wc;
+        a.nr = c.nr; a.ns = c.ns;
+        for (int i = 0; i < kD2MaxTaps; ++i) {
+            a.r_of[i] = c.r_of[i]; a.dp[i] = c.dp[i]; a.s_of[i] = c.s_of[i]; a.dq[i] = c.dq[i];
         }
-        a.ns = 0;
-        int mn = 1 << 30, mx = -(1 << 30);
-        for (int s = (a.pw + p.pad) % sdv; s < p.S; s += sdv) {
-            a.s_of[a.ns] = s;
-            a.dq[a.ns] = (a.pw + p.pad - s) / sdv;
-            mn = std::min(mn, a.dq[a.ns]);
-            mx = std::max(mx, a.dq[a.ns]);
-            ++a.ns;
-        }
-        if (a.ns == 0) { mn = 0; mx = 0; }
-        a.min_dq = mn;
-        a.span = mx - mn;
-        a.Wx = a.Wc + a.span;
+        a.min_dq = c.min_dq;
+        a.span = c.max_dq - c.min_dq;
         const int ns1 = std::max(1, a.ns);
         // (s, c) columns per block <= 256, c_tile a multiple of 16
-        int cap = std::max(16, (256 / ns1) / 16 * 16);
+        const int cap = std::max(16, (256 / ns1) / 16 * 16);
         const int ctiles = (p.C + cap - 1) / cap;
         a.c_tile = std::min(cap, ((p.C + ctiles - 1) / ctiles + 15) / 16 * 16);
         a.ncol = ns1 * a.c_tile;
-        a.kchunks = (p.K + 31) / 32;
-        a.T = (2 * a.ncol + 2 * kD2NA * 32 <= 512) ? 2 : 1;
-        a.ncols = pow2_cols(a.T * a.ncol + a.T * kD2NA * 32);
+        a.ncols = 32;
+        while ((int)a.ncols < 2 * a.ncol) a.ncols <<= 1;
         if (a.ncols > 512) return cudaErrorNotSupported;
-        a.total_pos = (long long)p.N * a.Hc * a.Wx;
+        a.kchunks = (p.K + 31) / 32;
+        a.total_pos = total_pos;
         const int tstride = 128 - a.span;
-        a.total_tiles = (int)((a.total_pos + tstride - 1) / tstride);
-        a.pitch = (uint32_t)a.ncol + 1;
-        if (a.ns == 0) a.nr = 0;  // no kernel column reaches this class
+        a.total_tiles = (int)((total_pos + tstride - 1) / tstride);
 
         CUtensorMap tmw;
         const uint64_t d[4] = {(uint64_t)Kw, (uint64_t)p.C, (uint64_t)p.S, (uint64_t)p.R};
         const uint32_t b[4] = {32, (uint32_t)a.c_tile, 1, 1};
         if (!encode_4d(&tmw, wr, d, b)) return cudaErrorInvalidValue;
-        const size_t ring = (size_t)kD2Ring * a.ncol * 128;
-        const size_t stage = (size_t)a.T * 128 * a.pitch * 4;  // one staging area per tile
-        const size_t smem = std::max(ring, stage) + 1024;
-        cudaError_t e = cudaFuncSetAttribute(dgrad_tc2_kernel,
+        const size_t pipe = (size_t)kD3Stages * (32768 + (size_t)a.ncol * 128);
+        const size_t stage = (size_t)a.ncol * 128 * 4;  // epilogue staging
+        const size_t smem = std::max(pipe, stage) + 1024;
+        cudaError_t e = cudaFuncSetAttribute(dgrad_tc3_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)smem);
         if (e != cudaSuccess) return e;
-        dim3 grid((unsigned)((a.total_tiles + a.T - 1) / a.T), (p.C + a.c_tile - 1) / a.c_tile);
-        dgrad_tc2_kernel<<<grid, kD2Threads, smem, st>>>(tmw, a);
+        dim3 grid((unsigned)((a.total_tiles + 1) / 2), (p.C + a.c_tile - 1) / a.c_tile);
+        dgrad_tc3_kernel<<<grid, kD3Threads, smem, st>>>(tma, tmw, a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         *launches += 1;
