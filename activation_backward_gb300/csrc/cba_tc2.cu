@@ -43,6 +43,7 @@ namespace cba {
 namespace {
 
 constexpr uint64_t kLimitNs = 2000000000ull;
+constexpr int kD2MaxTaps = 8;  // kernel rows / columns per stride phase class
 
 __device__ __forceinline__ float to_tf32(float v) {
     uint32_t r;
@@ -174,6 +175,128 @@ struct W2Bars {
     int abort_flag;
 };
 
+// Epilogue of the weight gradient (producer warps 0-7; group grp takes the
+// 32-wide output-channel chunks kc = grp, grp + 2, ...): accumulator D_r lane
+// (c, s), column k -> dW[k][c][r][s], added in L2 by bulk reductions of
+// whole dW row segments (or per-element atomics when those are misaligned).
+__device__ __forceinline__ void wgrad_epilogue(const Wg2Args &a, uint32_t tmem, uint32_t lane_addr,
+                                               uint8_t *ring, int grp, int L, int cl, int s,
+                                               bool lv, int ct_here, int k0, int c0, int h0,
+                                               int h1, int p_lo, int p_hi) {
+    const int st = a.stride, R = a.R;
+    const int pitch = ct_here * a.RS;  // floats per staged dW row segment
+    float *stg = reinterpret_cast<float *>(ring) + grp * 32 * pitch;
+    for (int kc = grp; kc * 32 < a.nk && k0 + kc * 32 < a.K; kc += 2) {
+        const int krows = min(32, a.K - (k0 + kc * 32));
+        for (int r = 0; r < R; ++r) {
+            // was accumulator r written by any input row of this block?
+            bool wr = false;
+            for (int h = h0; h < h1 && !wr; ++h) {
+                const int num = h - r + a.pad;
+                wr = num >= 0 && num % st == 0 && num / st >= p_lo && num / st <= p_hi;
+            }
+            float v[32];
+            if (wr) {
+                ptx::tmem_ld32(tmem + lane_addr + (uint32_t)(r * a.nk + kc * 32), v);
+                ptx::tmem_ld_wait();
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            if (lv) {
+                if (a.bulk) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        stg[j * pitch + cl * a.RS + r * a.S + s] = v[j];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j < krows)
+                            atomicAdd(a.dW + ((long long)(k0 + kc * 32 + j) * a.C + c0 +
+                                              cl) * a.RS + r * a.S + s,
+                                      v[j]);
+                }
+            }
+        }
+        if (a.bulk) {
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar_sync(1 + grp, 128);
+            if (L < krows) {
+                ptx::bulk_reduce_add_f32(
+                    a.dW + (long long)(k0 + kc * 32 + L) * a.CRS + (long long)c0 * a.RS,
+                    ptx::smem_u32(stg + L * pitch), (uint32_t)pitch * 4u);
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();
+            }
+            ptx::named_bar_sync(1 + grp, 128);
+        }
+    }
+    if (a.bulk && L < 32) ptx::bulk_wait_all();
+}
+
+// MMA role of the weight gradient (one thread): for each input row h, wait
+// for its TMEM A stage, then for every kernel row r whose output row
+// p = (h + pad - r)/st is in range, issue the K steps into accumulator r
+// against dz row p; release A stages and dz rows as soon as their last use is
+// issued.  Output rows are consumed in increasing order, so each dz row is
+// waited for once, when it is first needed.  The issue loop carries no
+// memory traffic: each MMA's B descriptor is the ring's base descriptor plus
+// the slot and K-step offsets.
+__device__ __forceinline__ void wgrad_mma_role(const Wg2Args &a, W2Bars &sb, uint8_t *ring,
+                                               uint32_t tmem, uint32_t a_col0, uint32_t idesc,
+                                               uint32_t tile_bytes, int nsteps, int h0, int h1,
+                                               int p_lo, int p_hi) {
+    const int st = a.stride, R = a.R;
+    const uint64_t bd0 = ptx::smem_desc(ptx::smem_u32(ring), 16, 1024, 2);
+    const uint32_t slot_step = tile_bytes >> 4;  // descriptor units per ring slot
+    uint32_t written = 0;
+    int p_rel = p_lo;    // next dz row to release
+    int p_ready = p_lo - 1;  // dz rows up to here have landed
+    int t = 0;
+    bool ok = true;
+    for (int h = h0; ok && h < h1; ++h, ++t) {
+        const int sa = t % kW2NA;
+        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_full[sa]),
+                                    (uint32_t)(t / kW2NA) & 1u, &sb.abort_flag, a.status,
+                                    kLimitNs);
+        if (!ok) break;
+        // the highest output row this input row meets
+        const int p_top = min(p_hi, fdiv(h + a.pad, st));
+        while (ok && p_ready < p_top) {
+            ++p_ready;
+            const int seq = p_ready - p_lo;
+            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[seq % a.ring]),
+                                        (uint32_t)(seq / a.ring) & 1u, &sb.abort_flag,
+                                        a.status, kLimitNs);
+        }
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t a_tm = tmem + a_col0 + (uint32_t)(sa * 32);
+        for (int r = 0; r < R; ++r) {
+            const int num = h - r + a.pad;
+            if (num < 0 || num % st) continue;
+            const int p = num / st;
+            if (p < p_lo || p > p_hi) continue;
+            const uint64_t bd = bd0 + (uint64_t)((uint32_t)((p - p_lo) % a.ring) * slot_step);
+            const uint32_t d_tm = tmem + (uint32_t)(r * a.nk);
+            const uint32_t acc0 = (written >> r) & 1u;
+            written |= 1u << r;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                if (ks < nsteps)
+                    ptx::mma_tf32_ts(d_tm, a_tm + ks * 8, bd + 2 * ks, idesc, ks ? 1u : acc0);
+        }
+        ptx::mma_commit(ptx::smem_u32(&sb.a_empty[sa]));
+        while (p_rel <= p_hi && min(h1 - 1, p_rel * st - a.pad + R - 1) <= h) {
+            ptx::mma_commit(ptx::smem_u32(&sb.dz_empty[(p_rel - p_lo) % a.ring]));
+            ++p_rel;
+        }
+    }
+    ptx::mma_commit(ptx::smem_u32(&sb.accum));
+    int no_abort = 0;
+    ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &no_abort, a.status, kLimitNs);
+}
+
 __global__ void __launch_bounds__(kW2Threads, 1)
     wgrad_tc2_kernel(const __grid_constant__ CUtensorMap tm, const Wg2Args a) {
     extern __shared__ uint8_t smem_dyn[];
@@ -281,54 +404,8 @@ __global__ void __launch_bounds__(kW2Threads, 1)
         ok = __all_sync(0xffffffffu, ok) && has_work;
         if (ok) {
             ptx::tc_fence_after();
-            const int pitch = ct_here * a.RS;  // floats per staged dW row segment
-            float *stg = reinterpret_cast<float *>(ring) + grp * 32 * pitch;
-            for (int kc = grp; kc * 32 < a.nk && k0 + kc * 32 < a.K; kc += 2) {
-                const int krows = min(32, a.K - (k0 + kc * 32));
-                for (int r = 0; r < R; ++r) {
-                    // was accumulator r written by any input row of this block?
-                    bool wr = false;
-                    for (int h = h0; h < h1 && !wr; ++h) {
-                        const int num = h - r + a.pad;
-                        wr = num >= 0 && num % st == 0 && num / st >= p_lo && num / st <= p_hi;
-                    }
-                    float v[32];
-                    if (wr) {
-                        ptx::tmem_ld32(tmem + lane_addr + (uint32_t)(r * a.nk + kc * 32), v);
-                        ptx::tmem_ld_wait();
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                    }
-                    if (lv) {
-                        if (a.bulk) {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                stg[j * pitch + cl * a.RS + r * a.S + s] = v[j];
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (j < krows)
-                                    atomicAdd(a.dW + ((long long)(k0 + kc * 32 + j) * a.C + c0 +
-                                                      cl) * a.RS + r * a.S + s,
-                                              v[j]);
-                        }
-                    }
-                }
-                if (a.bulk) {
-                    ptx::fence_proxy_async_smem();
-                    ptx::named_bar_sync(1 + grp, 128);
-                    if (L < krows) {
-                        ptx::bulk_reduce_add_f32(
-                            a.dW + (long long)(k0 + kc * 32 + L) * a.CRS + (long long)c0 * a.RS,
-                            ptx::smem_u32(stg + L * pitch), (uint32_t)pitch * 4u);
-                        ptx::bulk_commit();
-                        ptx::bulk_wait_read_all();
-                    }
-                    ptx::named_bar_sync(1 + grp, 128);
-                }
-            }
-            if (a.bulk && L < 32) ptx::bulk_wait_all();
+            wgrad_epilogue(a, tmem, lane_addr, ring, grp, L, cl, s, lv, ct_here, k0, c0, h0, h1,
+                           p_lo, p_hi);
         }
     } else if (warp == 8) {
         // ---- TMA producer: dz rows p_lo..p_hi into the ring
@@ -353,50 +430,182 @@ __global__ void __launch_bounds__(kW2Threads, 1)
                                        kLimitNs);
         }
     } else {
-        // ---- MMA issuer
+        if (lane == 0 && has_work)
+            wgrad_mma_role(a, sb, ring, tmem, a_col0, idesc, tile_bytes, nsteps, h0, h1, p_lo,
+                           p_hi);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, a.ncols);
+    }
+}
+
+// wgrad with the input rows staged by TMA: the TMA warp streams x rows
+// (all ct input channels, the columns one 32-wide output chunk needs) into
+// a ring next to the dz rows; the producer warps only shift-read the staged
+// row into TMEM.  Used when x rows are 16-byte strided (W*4 % 16 == 0).
+constexpr int kW3XRing = 6;
+
+struct Wg3Extra {
+    int wbox;         // staged columns per input row
+    uint32_t xbytes;  // bytes one TMA box writes (ct * wbox * 4)
+    uint32_t xstride; // bytes between ring slots (xbytes rounded up to 128)
+};
+
+__global__ void __launch_bounds__(kW2Threads, 1)
+    wgrad_tc3_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmx,
+                     const Wg2Args a, const Wg3Extra xe) {
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *ring = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    __shared__ W2Bars sb;
+    __shared__ uint64_t x_full[kW3XRing], x_empty[kW3XRing];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int k0 = blockIdx.x * a.nk;
+    const int c0 = blockIdx.y * a.ct;
+    const int ct_here = min(a.ct, a.C - c0);
+    const int seg = blockIdx.z / a.splits_per_seg, split = blockIdx.z % a.splits_per_seg;
+    const int n = seg / a.nqc, qc = seg % a.nqc;
+    const int h0 = split * a.rows_per_split, h1 = min(a.He, h0 + a.rows_per_split);
+    const int q_base = qc * 32;
+    const int nsteps = (min(32, a.Qe - q_base) + 7) / 8;
+    const uint32_t tile_bytes = (uint32_t)a.nk * 128u;
+    const int st = a.stride, R = a.R;
+    const int p_lo = max(0, cdiv(h0 - R + 1 + a.pad, st));
+    const int p_hi = min(a.Pe - 1, fdiv(h1 - 1 + a.pad, st));
+    const uint32_t a_col0 = (uint32_t)(R * a.nk);
+    const uint32_t idesc = ptx::idesc_tf32(128, a.nk);
+    const int wstart = q_base * st - a.pad;
+    const int w0 = wstart >= 0 ? (wstart & ~3) : -((-wstart + 3) & ~3);  // floor to 4
+    uint8_t *xring = ring + (size_t)a.ring * tile_bytes;
+
+    if (tid == 0) {
+        for (int i = 0; i < kW2RingMax; ++i) {
+            ptx::mbar_init(ptx::smem_u32(&sb.dz_full[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sb.dz_empty[i]), 1);
+        }
+        for (int i = 0; i < kW2NA; ++i) {
+            ptx::mbar_init(ptx::smem_u32(&sb.a_full[i]), 128);
+            ptx::mbar_init(ptx::smem_u32(&sb.a_empty[i]), 1);
+        }
+        for (int i = 0; i < kW3XRing; ++i) {
+            ptx::mbar_init(ptx::smem_u32(&x_full[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&x_empty[i]), 128);
+        }
+        ptx::mbar_init(ptx::smem_u32(&sb.accum), 1);
+        sb.abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 9) {
+        ptx::tmem_alloc(ptx::smem_u32(&sb.tmem_base), a.ncols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sb.tmem_base;
+    const bool has_work = h0 < h1 && p_lo <= p_hi;
+    const int nrows = has_work ? h1 - h0 : 0;
+
+    if (warp < 8) {
+        // ---- A producers: two groups of 4 warps take alternate input rows;
+        // TMEM lane (c, s) <- staged x[c][q*st + s - pad] for the 32 q
+        const int grp = warp >> 2, wq = warp & 3;
+        const int L = wq * 32 + lane;
+        const int cl = L / a.S, s = L - (L / a.S) * a.S;
+        const bool lv = cl < ct_here;
+        const int off0 = wstart + s - w0;  // column of q_base in the staged row
+        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        bool ok = true;
+        for (int t = grp; t < nrows; t += 2) {
+            const int xs = t % kW3XRing;
+            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&x_full[xs]), (uint32_t)(t / kW3XRing) & 1u,
+                                        &sb.abort_flag, a.status, kLimitNs);
+            const float *xr =
+                reinterpret_cast<const float *>(xring + (size_t)xs * xe.xstride) +
+                (lv ? cl : 0) * xe.wbox + off0;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = lv ? to_tf32(xr[j * st]) : 0.f;
+            ptx::mbar_arrive(ptx::smem_u32(&x_empty[xs]));
+            const int sa = t % kW2NA;
+            if (ok && t >= kW2NA)
+                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_empty[sa]),
+                                            (uint32_t)(t / kW2NA - 1) & 1u, &sb.abort_flag,
+                                            a.status, kLimitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            ptx::tmem_st32(tmem + lane_addr + a_col0 + (uint32_t)(sa * 32), v);
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[sa]));
+        }
+        // ---- epilogue: D_r[(c, s)][k] -> dW[k][c][r][s]; group g takes the
+        // 32-wide output-channel chunks kc = g, g + 2, ...
+        if (has_work && ok)
+            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
+                                        kLimitNs);
+        ok = __all_sync(0xffffffffu, ok) && has_work;
+        if (ok) {
+            ptx::tc_fence_after();
+            wgrad_epilogue(a, tmem, lane_addr, ring, grp, L, cl, s, lv, ct_here, k0, c0, h0, h1,
+                           p_lo, p_hi);
+        }
+    } else if (warp == 8) {
+        // ---- TMA producer: x rows and dz rows merged in the order of the
+        // first input row that needs them, as far ahead as the rings allow.
+        // A slot is only ever released by work on rows whose operands were
+        // issued earlier in this order, so blocking on a slot cannot deadlock.
         if (lane == 0 && has_work) {
-            uint32_t written = 0;
-            int p_rel = p_lo;
-            int t = 0;
+            int issued = 0, next_p = p_lo, xissued = 0;
             bool ok = true;
-            for (int h = h0; ok && h < h1; ++h, ++t) {
-                const int sa = t % kW2NA;
-                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_full[sa]),
-                                            (uint32_t)(t / kW2NA) & 1u, &sb.abort_flag, a.status,
-                                            kLimitNs);
-                if (!ok) break;
-                ptx::tc_fence_after();
-                for (int r = 0; r < R; ++r) {
-                    const int num = h - r + a.pad;
-                    if (num < 0 || num % st) continue;
-                    const int p = num / st;
-                    if (p < p_lo || p > p_hi) continue;
-                    const int seq = p - p_lo, slot = seq % a.ring;
-                    ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[slot]),
-                                                (uint32_t)(seq / a.ring) & 1u, &sb.abort_flag,
-                                                a.status, kLimitNs);
+            while (ok && (xissued < nrows || next_p <= p_hi)) {
+                const int dz_need = next_p <= p_hi ? max(0, next_p * st - a.pad - h0) : (1 << 30);
+                if (next_p <= p_hi && dz_need <= xissued) {
+                    const int seq = next_p - p_lo, slot = seq % a.ring;
+                    if (seq >= a.ring)
+                        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_empty[slot]),
+                                                    (uint32_t)(seq / a.ring - 1) & 1u,
+                                                    &sb.abort_flag, a.status, kLimitNs);
                     if (!ok) break;
-                    ptx::tc_fence_after();
-                    const uint32_t b_base = ptx::smem_u32(ring + (size_t)slot * tile_bytes);
-                    for (int ks = 0; ks < nsteps; ++ks) {
-                        const uint64_t bd = ptx::smem_desc(b_base + ks * 32, 16, 1024, 2);
-                        ptx::mma_tf32_ts(tmem + (uint32_t)(r * a.nk),
-                                         tmem + a_col0 + (uint32_t)(sa * 32 + ks * 8), bd, idesc,
-                                         ((written >> r) & 1u) || ks > 0 ? 1u : 0u);
-                    }
-                    written |= 1u << r;
-                }
-                if (!ok) break;
-                ptx::mma_commit(ptx::smem_u32(&sb.a_empty[sa]));
-                while (p_rel <= p_hi && min(h1 - 1, p_rel * st - a.pad + R - 1) <= h) {
-                    ptx::mma_commit(ptx::smem_u32(&sb.dz_empty[(p_rel - p_lo) % a.ring]));
-                    ++p_rel;
+                    ptx::mbar_arrive_expect_tx(ptx::smem_u32(&sb.dz_full[slot]), tile_bytes);
+                    ptx::tma_load_4d(ptx::smem_u32(ring + (size_t)slot * tile_bytes), &tm, q_base,
+                                     next_p, k0, n, ptx::smem_u32(&sb.dz_full[slot]));
+                    ++next_p;
+                    ++issued;
+                } else {
+                    const int t = xissued, xs = t % kW3XRing;
+                    if (t >= kW3XRing)
+                        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&x_empty[xs]),
+                                                    (uint32_t)(t / kW3XRing - 1) & 1u,
+                                                    &sb.abort_flag, a.status, kLimitNs);
+                    if (!ok) break;
+                    ptx::mbar_arrive_expect_tx(ptx::smem_u32(&x_full[xs]), xe.xbytes);
+                    ptx::tma_load_4d(ptx::smem_u32(xring + (size_t)xs * xe.xstride), &tmx, w0,
+                                     h0 + t, c0, n, ptx::smem_u32(&x_full[xs]));
+                    ++xissued;
                 }
             }
-            ptx::mma_commit(ptx::smem_u32(&sb.accum));
+            // no copy may be in flight when the block exits
             int no_abort = 0;
-            ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &no_abort, a.status, kLimitNs);
+            for (int seq = max(0, issued - a.ring); seq < issued; ++seq)
+                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[seq % a.ring]),
+                                       (uint32_t)(seq / a.ring) & 1u, &no_abort, a.status,
+                                       kLimitNs);
+            for (int t = max(0, xissued - kW3XRing); t < xissued; ++t)
+                ptx::mbar_wait_bounded(ptx::smem_u32(&x_full[t % kW3XRing]),
+                                       (uint32_t)(t / kW3XRing) & 1u, &no_abort, a.status,
+                                       kLimitNs);
         }
+    } else {
+        if (lane == 0 && has_work)
+            wgrad_mma_role(a, sb, ring, tmem, a_col0, idesc, tile_bytes, nsteps, h0, h1, p_lo,
+                           p_hi);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -410,8 +619,7 @@ __global__ void __launch_bounds__(kW2Threads, 1)
 // ------------------------------------------------------------------ dgrad
 
 constexpr int kD3Stages = 3;
-constexpr int kD3Threads = 192;  // TMA warp, MMA warp, 4 epilogue warps
-constexpr int kD2MaxTaps = 8;
+constexpr int kD3Threads = 320;  // TMA warp, MMA warp, 8 epilogue warps
 
 struct Dg3Args {
     const float *residual;
@@ -563,9 +771,11 @@ __global__ void __launch_bounds__(kD3Threads, 1)
             ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &no_abort, a.status, kLimitNs);
         }
     } else {
-        // ---- epilogue (warps 2-5): E -> column-major staging -> shifted sum over
-        // the kernel columns -> + residual (+ old prev_delta) -> prev_delta
-        const int wq = warp & 3;
+        // ---- epilogue (warps 2-9, two groups; warp & 3 is the TMEM lane
+        // quarter): E -> column-major staging (each group half the columns) ->
+        // shifted sum over the kernel columns (each group half the channels)
+        // -> + residual (+ old prev_delta) -> prev_delta
+        const int eg = (warp - 2) >> 2, wq = warp & 3;
         const int L = wq * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
         bool ok = true;
@@ -578,9 +788,13 @@ __global__ void __launch_bounds__(kD3Threads, 1)
             float *stg = reinterpret_cast<float *>(smem);
             const long long HW = (long long)a.He * a.We;
             const long long plane = (long long)a.Pp * a.Qpp;
+            const int half = (a.ncol / 2 + 15) / 16 * 16;
+            const int col_lo = eg == 0 ? 0 : half, col_hi = eg == 0 ? half : a.ncol;
+            const int cl_all = min(a.c_tile, a.C - c0);
+            const int ch_half = (cl_all + 1) / 2;
             for (int tt = 0; tt < 2; ++tt) {
-                int col = 0;
-                for (; col + 32 <= a.ncol; col += 32) {
+                int col = col_lo;
+                for (; col + 32 <= col_hi; col += 32) {
                     float v[32];
                     if (nstages > 0) {
                         ptx::tmem_ld32(tmem + lane_addr + (uint32_t)(tt * a.ncol + col), v);
@@ -592,7 +806,7 @@ __global__ void __launch_bounds__(kD3Threads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) stg[(col + j) * 128 + L] = v[j];
                 }
-                if (col < a.ncol) {
+                if (col < col_hi) {  // 16-column tail
                     float v[16];
                     if (nstages > 0) {
                         ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(tt * a.ncol + col), v);
@@ -604,7 +818,7 @@ __global__ void __launch_bounds__(kD3Threads, 1)
 #pragma unroll
                     for (int j = 0; j < 16; ++j) stg[(col + j) * 128 + L] = v[j];
                 }
-                ptx::named_bar_sync(1, 128);
+                ptx::named_bar_sync(1, 256);
                 // home lane L: padded position m = m0 + L - min_dq
                 const long long m = m0[tt] + L - a.min_dq;
                 const int tile = blockIdx.x * 2 + tt;
@@ -623,10 +837,11 @@ __global__ void __launch_bounds__(kD3Threads, 1)
                     int dqr[kD2MaxTaps];
 #pragma unroll
                     for (int si = 0; si < kD2MaxTaps; ++si) dqr[si] = a.dq[si] - a.min_dq;
-                    dgrad_out_lane(stg + L, a.prev, a.residual, pix, HW, c0,
-                                   min(a.c_tile, a.C - c0), a.c_tile, a.ns, dqr, a.accumulate);
+                    const int cb = eg == 0 ? 0 : ch_half, ce = eg == 0 ? ch_half : cl_all;
+                    dgrad_out_lane(stg + L + cb * 128, a.prev, a.residual, pix, HW, c0 + cb,
+                                   ce - cb, a.c_tile, a.ns, dqr, a.accumulate);
                 }
-                ptx::named_bar_sync(1, 128);
+                ptx::named_bar_sync(1, 256);
             }
         }
     }
@@ -848,22 +1063,60 @@ cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, fl
     a.splits_per_seg = (g.He + a.rows_per_split - 1) / a.rows_per_split;
     const int ct_last = p.C - ((p.C + a.ct - 1) / a.ct - 1) * a.ct;
     a.bulk = (p.CRS % 4 == 0) && ((a.ct * p.RS) % 4 == 0) && ((ct_last * p.RS) % 4 == 0);
-    // dz ring: as many row tiles as fit next to the A staging (at least R)
+    CUtensorMap tm;
+    const uint64_t d[4] = {(uint64_t)g.Qp, (uint64_t)g.Pe, (uint64_t)p.K, (uint64_t)p.N};
+    const uint32_t b[4] = {32, 1, (uint32_t)a.nk, 1};
+    if (!encode_4d(&tm, dzt, d, b)) return cudaErrorInvalidValue;
+    dim3 grid((p.K + a.nk - 1) / a.nk, (p.C + a.ct - 1) / a.ct, (unsigned)(segs * a.splits_per_seg));
+
+    // x rows staged by TMA when they are 16-byte strided
+    const int span = 31 * p.stride + p.S;  // input columns one 32-wide output chunk reads
+    Wg3Extra xe;
+    xe.wbox = (span + 3 + 3) / 4 * 4;       // + up to 3 columns of alignment slack
+    xe.xbytes = (uint32_t)((size_t)a.ct * xe.wbox * 4);
+    xe.xstride = (xe.xbytes + 127u) / 128u * 128u;
+    const bool x_tma = (g.We % 4 == 0) && xe.wbox <= 256 &&
+                       (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+    if (x_tma) {
+        const size_t xring = (size_t)kW3XRing * xe.xstride;
+        a.ring = (int)std::min<size_t>(kW2RingMax, (220 * 1024 - xring) / ((size_t)a.nk * 128));
+        if (a.ring < p.R) return cudaErrorNotSupported;
+        if ((long long)2 * 32 * a.ct * p.RS * 4 > (long long)a.ring * a.nk * 128) a.bulk = 0;
+        CUtensorMap tmx;
+        {
+            EncodeTiledFn fn = encode_fn();
+            cuuint64_t dims[4] = {(cuuint64_t)g.We, (cuuint64_t)g.He, (cuuint64_t)p.C,
+                                  (cuuint64_t)p.N};
+            cuuint64_t strides[3] = {(cuuint64_t)g.We * 4, (cuuint64_t)g.We * g.He * 4,
+                                     (cuuint64_t)g.We * g.He * p.C * 4};
+            cuuint32_t box[4] = {(cuuint32_t)xe.wbox, 1, (cuuint32_t)a.ct, 1};
+            cuuint32_t es[4] = {1, 1, 1, 1};
+            if (fn(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return cudaErrorInvalidValue;
+        }
+        const size_t smem = (size_t)a.ring * a.nk * 128 + xring + 1024;
+        cudaError_t e = cudaFuncSetAttribute(wgrad_tc3_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (e != cudaSuccess) return e;
+        wgrad_tc3_kernel<<<grid, kW2Threads, smem, st>>>(tm, tmx, a, xe);
+        *launches += 1;
+        return cudaGetLastError();
+    }
+
+    // otherwise each producer thread gathers its own values with cp.async
     const size_t astg = (size_t)2 * kAStg * 32 * 128 * 4;
     a.ring = (int)std::min<size_t>(kW2RingMax, (220 * 1024 - astg) / ((size_t)a.nk * 128));
     if (a.ring < p.R) return cudaErrorNotSupported;
     // each producer group stages 32 rows of its dW segment in the ring
     if ((long long)2 * 32 * a.ct * p.RS * 4 > (long long)a.ring * a.nk * 128) a.bulk = 0;
-
-    CUtensorMap tm;
-    const uint64_t d[4] = {(uint64_t)g.Qp, (uint64_t)g.Pe, (uint64_t)p.K, (uint64_t)p.N};
-    const uint32_t b[4] = {32, 1, (uint32_t)a.nk, 1};
-    if (!encode_4d(&tm, dzt, d, b)) return cudaErrorInvalidValue;
     const size_t smem = (size_t)a.ring * a.nk * 128 + astg + 1024;
     cudaError_t e = cudaFuncSetAttribute(wgrad_tc2_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.K + a.nk - 1) / a.nk, (p.C + a.ct - 1) / a.ct, (unsigned)(segs * a.splits_per_seg));
     wgrad_tc2_kernel<<<grid, kW2Threads, smem, st>>>(tm, a);
     *launches += 1;
     return cudaGetLastError();
