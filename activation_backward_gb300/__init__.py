@@ -8,8 +8,9 @@ the device-side convenience wrapper; ``inputs`` generates seeded synthetic
 workloads.  The CUDA library is loaded lazily; nothing falls back to the CPU.
 """
 from ._binding import (CBA_ACT_LEAKY, CBA_ACT_LINEAR, CBA_ERR_ALIGN, CBA_ERR_ARG,  # noqa: F401
-                       CBA_ERR_CUDA, CBA_ERR_DEVICE_TIMEOUT, CBA_ERR_UNSUPPORTED,
-                       CBA_ERR_WORKSPACE, CBA_MATH_FFMA, CBA_MATH_TF32, CBA_OK, CbaError,
+                       CBA_ERR_CUDA, CBA_ERR_DEVICE_TIMEOUT, CBA_ERR_SCRATCH_LIMIT,
+                       CBA_ERR_UNSUPPORTED, CBA_ERR_WORKSPACE, CBA_MATH_FFMA, CBA_MATH_TF32,
+                       CBA_NOALLOC_MAX_K, CBA_OK, CbaError, cba_bn_act_backward_noalloc,
                        cba_conv_bn_act_backward, cba_conv_bn_act_backward_traced, cba_desc_t,
                        cba_error_string, cba_get_status, cba_last_cuda_error,
                        cba_selftest_bounded_wait, cba_version, cba_workspace_bytes, load,

@@ -19,6 +19,8 @@ CBA_ERR_ALIGN = -3
 CBA_ERR_WORKSPACE = -4
 CBA_ERR_CUDA = -5
 CBA_ERR_DEVICE_TIMEOUT = -6
+CBA_ERR_SCRATCH_LIMIT = -7
+CBA_NOALLOC_MAX_K = 16384
 
 CBA_ACT_LINEAR = 0
 CBA_ACT_LEAKY = 1
@@ -27,7 +29,7 @@ CBA_MATH_FFMA = 1
 
 # every symbol include/cba.h declares
 EXPORTS = ("cba_workspace_bytes", "cba_conv_bn_act_backward", "cba_conv_bn_act_backward_traced",
-           "cba_get_status",
+           "cba_get_status", "cba_bn_act_backward_noalloc",
            "cba_selftest_bounded_wait", "cba_error_string", "cba_last_cuda_error", "cba_version")
 
 
@@ -65,6 +67,8 @@ def load(path=LIB_PATH):
     L.cba_conv_bn_act_backward_traced.argtypes = (
         [ctypes.POINTER(cba_desc_t)] + [vp] * 15 + [sz, vp, ctypes.POINTER(ctypes.c_void_p),
                                                     ctypes.POINTER(ctypes.c_int)])
+    L.cba_bn_act_backward_noalloc.restype = ctypes.c_int
+    L.cba_bn_act_backward_noalloc.argtypes = [ctypes.POINTER(cba_desc_t)] + [vp] * 10
     L.cba_get_status.restype = ctypes.c_int
     L.cba_get_status.argtypes = [vp, sz, vp]
     L.cba_selftest_bounded_wait.restype = ctypes.c_int
@@ -148,6 +152,20 @@ def cba_conv_bn_act_backward_traced(desc, x, output, z, delta, W, gamma, mean, v
     if check and rc != CBA_OK:
         raise CbaError(rc, "cba_conv_bn_act_backward_traced")
     return rc, n.value
+
+
+def cba_bn_act_backward_noalloc(desc, output, z, delta, gamma, mean, var, db, dgamma, dz_out,
+                                stream=None, check=True):
+    """Enqueue the activation-gradient + BN-backward pass (db, dgamma, dz)
+    without a workspace; the library uses its own static device scratch.
+    Returns the C return code; raises CbaError on a non-zero code when
+    ``check``."""
+    rc = load().cba_bn_act_backward_noalloc(
+        ctypes.byref(desc), _ptr(output), _ptr(z), _ptr(delta), _ptr(gamma), _ptr(mean),
+        _ptr(var), _ptr(db), _ptr(dgamma), _ptr(dz_out), _stream(stream))
+    if check and rc != CBA_OK:
+        raise CbaError(rc, "cba_bn_act_backward_noalloc")
+    return rc
 
 
 def cba_get_status(workspace, workspace_bytes=None, stream=None):

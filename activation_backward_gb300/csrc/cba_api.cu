@@ -129,6 +129,10 @@ cudaError_t select_device(cudaStream_t stream, const void *ptr) {
 
 }  // namespace
 
+namespace cba {
+int report_cuda_error(cudaError_t e) { return fail_cuda(e); }
+}  // namespace cba
+
 extern "C" {
 
 size_t cba_workspace_bytes(const cba_desc_t *d) {
@@ -279,6 +283,8 @@ const char *cba_error_string(int code) {
     case CBA_ERR_WORKSPACE: return "workspace missing or smaller than cba_workspace_bytes()";
     case CBA_ERR_CUDA: return "CUDA launch or runtime error (see cba_last_cuda_error)";
     case CBA_ERR_DEVICE_TIMEOUT: return "a bounded device wait ran out; outputs are not valid";
+    case CBA_ERR_SCRATCH_LIMIT:
+        return "K exceeds CBA_NOALLOC_MAX_K, the static scratch of cba_bn_act_backward_noalloc";
     default: return "unknown error code";
     }
 }

@@ -71,6 +71,8 @@ cudaError_t launch_dgrad_tc(const Plan &p, const float *Wt, const float *delta,
 cudaError_t launch_splitk_reduce(const Plan &p, const float *part, int splits, float *dW,
                                  cudaStream_t st, int *launches);
 cudaError_t launch_selftest_wait(unsigned timeout_us, void *ws, cudaStream_t st);
+// Records `e` as the last CUDA error of the library; returns CBA_ERR_CUDA.
+int report_cuda_error(cudaError_t e);
 bool tc_supported(const Plan &p);
 void tc_plan(Plan &p);  // fills the tc_* fields
 bool tc2_supported(const Plan &p);

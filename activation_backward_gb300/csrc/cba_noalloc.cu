@@ -1,0 +1,132 @@
+// cba_noalloc.cu -- cba_bn_act_backward_noalloc: the activation-gradient and
+// BN-backward pass (bias and scale gradients, optionally the BN-input
+// gradient dz) for callers that cannot allocate device memory.
+//
+// Who needs it: code that may not call cudaMalloc where it runs the backward
+// and has no buffer of its own to lend as a workspace.  Examples are a plugin
+// called from another runtime's enqueue hook, where that runtime owns all
+// device memory and forbids allocation after start-up, and a latency-bounded
+// loop.  In both cases cudaMalloc can implicitly synchronise the device and
+// its latency is unbounded.
+//
+// The pass needs a small scratch for its per-block partial sums and
+// per-channel coefficients.  Here the scratch is one file-scope __device__
+// array, kScratchBytes (1 MiB), placed on every device that loads this
+// library and held there until the process exits.  The entry point allocates
+// nothing: the only CUDA calls are cudaGetSymbolAddress (once per device), the
+// kernel launches, and the device/stream queries that select the device.
+//
+// Scratch contents: every call shares the one array per device, and the array
+// keeps whatever the last call left in it.  No word is read before the same
+// call writes it: the reduction kernel writes every partial before the
+// finalize kernel reads them, and finalize writes every coefficient before
+// the dz kernel reads them.  So nothing has to start at zero, and nothing is
+// cleared.  Calls that overlap on one device (two streams, or two host
+// threads, with no ordering between them) race on the array; the caller must
+// order them, e.g. by using one stream.
+#include <mutex>
+
+#include "cba_internal.cuh"
+
+namespace cba {
+
+namespace {
+
+constexpr size_t kScratchBytes = size_t(1) << 20;  // 1 MiB per device
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+std::mutex g_mu;
+void *g_scratch_ptr[kMaxDevices] = {};
+
+inline size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+inline bool misaligned16(const void *ptr) {
+    return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0;
+}
+
+// The device the call runs on: the stream's device, else (NULL stream) the
+// device holding `ptr`; made current for this library's runtime.
+cudaError_t current_device_for(cudaStream_t stream, const void *ptr, int *dev) {
+    cudaError_t e = cudaSuccess;
+    int want = -1;
+    if (stream) {
+        e = cudaStreamGetDevice(stream, &want);
+    } else {
+        cudaPointerAttributes a;
+        e = cudaPointerGetAttributes(&a, ptr);
+        if (e == cudaSuccess) want = a.device;
+    }
+    if (e != cudaSuccess) return e;
+    int cur = -1;
+    e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return e;
+    if (want >= 0 && want != cur) {
+        e = cudaSetDevice(want);
+        cur = want;
+    }
+    *dev = cur;
+    return e;
+}
+
+// Set-up, once per device with that device current: the device address of the
+// scratch array.  The first call on each device does this.
+cudaError_t scratch_for_device(int dev, void **out) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_ptr[dev]) {
+        void *ptr = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 255u) != 0) return cudaErrorInvalidSymbol;
+        g_scratch_ptr[dev] = ptr;
+    }
+    *out = g_scratch_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+}  // namespace cba
+
+extern "C" int cba_bn_act_backward_noalloc(const cba_desc_t *d, const float *output,
+                                           const float *z, const float *delta,
+                                           const float *gamma, const float *mean,
+                                           const float *var, float *db, float *dgamma,
+                                           float *dz_out, void *stream) {
+    using namespace cba;
+    Plan p;
+    int rc = make_plan(d, &p);
+    if (rc != CBA_OK) return rc;
+    if (!delta || !db) return CBA_ERR_ARG;
+    if (p.act != CBA_ACT_LINEAR && !output) return CBA_ERR_ARG;
+    if (p.bn && (!z || !gamma || !mean || !var || !dgamma)) return CBA_ERR_ARG;
+    const void *ptrs[] = {output, z, delta, gamma, mean, var, db, dgamma, dz_out};
+    for (const void *q : ptrs)
+        if (misaligned16(q)) return CBA_ERR_ALIGN;
+    if (p.K > CBA_NOALLOC_MAX_K) return CBA_ERR_SCRATCH_LIMIT;
+
+    // scratch layout: coefficients [K] at 0, then the partials [splits][K]
+    const size_t coef_bytes = align256(sizeof(Coef) * (size_t)p.K);
+    const size_t part_unit = sizeof(double) * 2 * (size_t)p.K;  // one split
+    const long long fit = (long long)((kScratchBytes - coef_bytes) / part_unit);
+    if (fit < 1) return CBA_ERR_SCRATCH_LIMIT;  // unreachable with K <= CBA_NOALLOC_MAX_K
+    p.red_splits = (int)std::min<long long>(p.red_splits, fit);
+    p.off_coef = 0;
+    p.off_red = coef_bytes;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();  // the launches below report only their own errors
+    int dev = -1;
+    cudaError_t e = current_device_for(st, delta, &dev);
+    if (e != cudaSuccess) return report_cuda_error(e);
+    if (dev < 0 || dev >= kMaxDevices) return CBA_ERR_UNSUPPORTED;
+    void *scratch = nullptr;
+    e = scratch_for_device(dev, &scratch);
+    if (e != cudaSuccess) return report_cuda_error(e);
+    int n_launch = 0;
+    e = launch_reduce(p, delta, output, z, gamma, mean, var, db, dgamma, scratch, st, &n_launch);
+    if (e == cudaSuccess && dz_out) e = launch_dz_out(p, delta, output, z, scratch, dz_out, st);
+    if (e != cudaSuccess) return report_cuda_error(e);
+    return CBA_OK;
+}

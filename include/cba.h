@@ -60,6 +60,7 @@ extern "C" {
 #define CBA_ERR_WORKSPACE (-4)   /* workspace NULL or smaller than cba_workspace_bytes() */
 #define CBA_ERR_CUDA (-5)        /* a CUDA launch or runtime call failed */
 #define CBA_ERR_DEVICE_TIMEOUT (-6) /* reported by cba_get_status: a device wait ran out */
+#define CBA_ERR_SCRATCH_LIMIT (-7)  /* cba_bn_act_backward_noalloc: K > CBA_NOALLOC_MAX_K */
 
 typedef enum { CBA_ACT_LINEAR = 0, CBA_ACT_LEAKY = 1 } cba_act_t;
 
@@ -138,6 +139,40 @@ int cba_get_status(void *workspace, size_t workspace_bytes, void *stream);
  * cba_get_status).  Needs cba_workspace_bytes of any valid descriptor. */
 int cba_selftest_bounded_wait(void *workspace, size_t workspace_bytes, unsigned timeout_us,
                               void *stream);
+
+/* Largest K that cba_bn_act_backward_noalloc accepts (its static scratch). */
+#define CBA_NOALLOC_MAX_K 16384
+
+/* The activation-gradient and BN-backward pass of cba_conv_bn_act_backward
+ * (db, dgamma and, optionally, dz) WITHOUT a workspace and without allocating.
+ * No counterpart in the source pages: it exists for callers that cannot call
+ * cudaMalloc where they run the backward and have no buffer to lend, e.g. a
+ * plugin called from another runtime's enqueue hook (that runtime owns all
+ * device memory and forbids allocation after start-up) or a latency-bounded
+ * loop (cudaMalloc may synchronise the device).
+ *
+ * Scratch: one static 1 MiB device array inside the library, placed on every
+ * device that loads the library and held until the process exits.  The first
+ * call on each device looks up the array's address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All
+ * calls on a device share the array and it keeps the last call's contents
+ * (no call reads a word it has not written first, so nothing is cleared).
+ * Calls that overlap on one device (other streams or host threads with no
+ * ordering between them) race on it: order them, e.g. on one stream.
+ *
+ * Arguments as cba_conv_bn_act_backward (only N, K and the output size P, Q of
+ * the descriptor matter; math is ignored):
+ *   output [N,K,P,Q] required unless act = LINEAR; z, gamma, mean, var and
+ *   dgamma required iff BN; delta required; db [K] += and dgamma [K] += ;
+ *   dz_out [N,K,P,Q] receives dz when not NULL.  Device pointers, 16-byte
+ *   aligned; stream = cudaStream_t (the NULL stream: the device of delta).
+ * Returns CBA_OK, CBA_ERR_ARG / CBA_ERR_ALIGN / CBA_ERR_UNSUPPORTED,
+ * CBA_ERR_SCRATCH_LIMIT when K > CBA_NOALLOC_MAX_K (nothing is enqueued), or
+ * CBA_ERR_CUDA. */
+int cba_bn_act_backward_noalloc(const cba_desc_t *d, const float *output, const float *z,
+                                const float *delta, const float *gamma, const float *mean,
+                                const float *var, float *db, float *dgamma, float *dz_out,
+                                void *stream);
 
 /* Human-readable text of a CBA_* code (static storage). */
 const char *cba_error_string(int code);
