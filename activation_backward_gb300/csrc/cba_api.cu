@@ -188,11 +188,17 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     }
     if (p.use_tc2) {
         float *dzt = ws_at<float>(workspace, p.off_dzt);
+        // the TMA-fed weight gradient reads only the channels-last dz copy
+        const bool w4 = wgrad_tc4_supported(p, x);
+        float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) +
+                                               dzc_geom(p).dzt_bytes);
         if (e == cudaSuccess)
-            e = launch_dz_materialize(p, delta, output, z, workspace, dzt, prev_delta != nullptr,
-                                      st, &n_launch);
+            e = launch_dz_materialize(p, delta, output, z, workspace, dzt,
+                                      prev_delta != nullptr || w4, st, &n_launch, !w4);
         if (e == cudaSuccess) e = tr.mark(1);
-        if (e == cudaSuccess) e = launch_wgrad_tc2(p, x, dzt, dW, workspace, st, &n_launch);
+        if (e == cudaSuccess)
+            e = w4 ? launch_wgrad_tc4(p, x, dzc, dW, workspace, st, &n_launch)
+                   : launch_wgrad_tc2(p, x, dzt, dW, workspace, st, &n_launch);
         if (e == cudaSuccess) e = tr.mark(2);
         if (e == cudaSuccess && prev_delta)
             e = launch_dgrad_tc2(p, Wt, dzt, residual, prev_delta, workspace,

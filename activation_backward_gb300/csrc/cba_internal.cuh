@@ -78,9 +78,28 @@ void tc_plan(Plan &p);  // fills the tc_* fields
 bool tc2_supported(const Plan &p);
 size_t tc2_dzt_bytes(const Plan &p);
 size_t tc2_wr_bytes(const Plan &p);
+// dz pass: dzt ([N][K][Pe][Qp]) unless with_dzt is false, and the channels-last
+// zero-bordered dzc right after it when with_dzc.
 cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float *output,
                                   const float *z, const void *ws, float *dzt, bool with_dzc,
-                                  cudaStream_t st, int *launches);
+                                  cudaStream_t st, int *launches, bool with_dzt = true);
+
+// The geometry the TMA kernels see and the channels-last dz copy's layout:
+// dzc [N][Pp][Qpp][Kp], data at row offset bd_lo and column offset bq_lo (zero
+// border elsewhere), stored dzt_bytes after the start of the dzt region.
+struct DzcGeom {
+    int He, We, Pe, Qe, Kp, Pp, Qpp, bd_lo, bq_lo;
+    size_t dzt_bytes;
+};
+DzcGeom dzc_geom(const Plan &p);
+// Dense row-major fp32 tensor map (dims[0] innermost) with the given box;
+// 128-byte swizzle or none.  `tmap` points to a CUtensorMap.
+bool tma_encode_f32(void *tmap, const void *base, int rank, const uint64_t *dims,
+                    const uint32_t *box, bool swizzle128);
+// Weight gradient with TMA-fed input rows (cba_wgrad4.cu).
+bool wgrad_tc4_supported(const Plan &p, const float *x);
+cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, float *dW,
+                             void *ws, cudaStream_t st, int *launches);
 cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, float *dW,
                              void *ws, cudaStream_t st, int *launches);
 cudaError_t launch_dgrad_tc2(const Plan &p, const float *Wt, const float *dzt,

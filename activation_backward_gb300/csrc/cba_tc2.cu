@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(256)
                 v = to_tf32(dz_of<ACT, BN>(__ldg(delta + off), y, zz, coef[k]));
             }
             tile[kk][tx] = v;
-            if (prow && k < K && q >= 0 && q < Qp)
+            if (dzt != nullptr && prow && k < K && q >= 0 && q < Qp)
                 dzt[(((long long)n * K + k) * Pe + p) * Qp + q] = v;
         }
     }
@@ -968,6 +968,35 @@ static size_t dzt_bytes_only(const Plan &p, const V2Geom &g) {
     return ((sizeof(float) * (size_t)p.N * p.K * g.Pe * g.Qp) + 255) / 256 * 256;
 }
 
+DzcGeom dzc_geom(const Plan &p) {
+    const V2Geom g = v2_geom(p);
+    DzcGeom d;
+    d.He = g.He; d.We = g.We; d.Pe = g.Pe; d.Qe = g.Qe;
+    d.Kp = g.Kp; d.Pp = g.Pp; d.Qpp = g.Qpp; d.bd_lo = g.bd_lo; d.bq_lo = g.bq_lo;
+    d.dzt_bytes = dzt_bytes_only(p, g);
+    return d;
+}
+
+bool tma_encode_f32(void *tmap, const void *base, int rank, const uint64_t *dims,
+                    const uint32_t *box, bool swizzle128) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], strides[4];
+    cuuint32_t b[5], es[5];
+    uint64_t stride = 4;
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i > 0) strides[i - 1] = stride;
+        stride *= dims[i];
+    }
+    return fn(static_cast<CUtensorMap *>(tmap), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank,
+              const_cast<void *>(base), d, strides, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool tc2_supported(const Plan &p) {
     if (p.stride > 4 || p.R > kD2MaxTaps || p.S > kD2MaxTaps) return false;
     const V2Geom g = v2_geom(p);
@@ -990,20 +1019,20 @@ size_t tc2_wr_bytes(const Plan &p) {
 
 cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float *output,
                                   const float *z, const void *ws, float *dzt, bool with_dzc,
-                                  cudaStream_t st, int *launches) {
+                                  cudaStream_t st, int *launches, bool with_dzt) {
     const V2Geom g = v2_geom(p);
     const Coef *coef = ws_at<Coef>(ws, p.off_coef);
     const bool leaky = p.act == CBA_ACT_LEAKY;
     if (with_dzc) {
         float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) + dzt_bytes_only(p, g));
         const int qlo = -g.bq_lo;
-        const int qhi = std::max(g.Qpp - g.bq_lo, g.Qp);
+        const int qhi = with_dzt ? std::max(g.Qpp - g.bq_lo, g.Qp) : g.Qpp - g.bq_lo;
         dim3 grid((unsigned)((qhi - qlo + 31) / 32), (unsigned)((g.Kp + 31) / 32),
                   (unsigned)(p.N * g.Pp));
 #define CBA_DZB(A, B)                                                                          \
     dz_both_kernel<A, B><<<grid, 256, 0, st>>>(delta, output, z, coef, p.K, g.Pe, g.Qe, g.Qp,   \
-                                               g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, qlo, dzt, \
-                                               dzc)
+                                               g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, qlo,      \
+                                               with_dzt ? dzt : nullptr, dzc)
         if (p.bn) {
             if (leaky) CBA_DZB(CBA_ACT_LEAKY, true);
             else CBA_DZB(CBA_ACT_LINEAR, true);
