@@ -98,6 +98,7 @@ bool tma_encode_f32(void *tmap, const void *base, int rank, const uint64_t *dims
                     const uint32_t *box, bool swizzle128);
 // Weight gradient with TMA-fed input rows (cba_wgrad4.cu).
 bool wgrad_tc4_supported(const Plan &p, const float *x);
+size_t wgrad_tc4_ws_bytes(const Plan &p);  // partial tiles (0 if the shape is not covered)
 cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, float *dW,
                              void *ws, cudaStream_t st, int *launches);
 cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, float *dW,

@@ -5,26 +5,30 @@
 //
 // Substituting w = q + s - pad moves the kernel-column shift from x onto dz:
 //   dW[k][c][r][s] = sum_{n,p,w} dz[n][k][p][w - s + pad] * x[n][c][p + r - pad][w].
-// A block owns 128 output channels k (MMA M, TMEM lanes) and cb input
-// channels c, and walks a range of (n, 32-wide column chunk w0, output row p)
-// items.  Per item:
-//   A_s = dz[n][k0..k0+127][p][w0 + j - s + pad], j < 32: the dz row shifted
-//         by each kernel column s, written into TMEM by producer warps from a
-//         TMA-staged tile of the channels-last, zero-bordered dz copy;
-//   B   = x rows p - pad .. p - pad + R - 1 of channels c0..c0+cb, columns
-//         w0..w0+31: R consecutive rows of a TMA ring (128-byte swizzle,
-//         K-major), so one MMA covers all kernel rows with N = R * cb;
-//   D_s[k][(r, c)] += A_s * B^T, one accumulator per kernel column s.
-// The ring keeps every x row once; rows that wrap around the ring end are
-// also stored in R - 1 mirror slots after it, so any R consecutive rows are
+// A block owns one tile (128 output channels k = MMA M = TMEM lanes, cb
+// input channels c, one kernel column s) and walks a range of
+// (n, 32-wide column chunk w0, output row p) items.  Per item:
+//   A = dz[n][k0..k0+127][p][w0 - s + pad + j], j < 32: a TMA tile of the
+//       channels-last, zero-bordered dz copy (its column offset is free: the
+//       column is not the innermost dimension there), moved into TMEM by the
+//       producer warps (one 32-column store per lane);
+//   B = x rows p - pad .. p - pad + R - 1 of channels c0..c0+cb, columns
+//       w0..w0+31: R consecutive rows of a TMA ring (128-byte swizzle,
+//       K-major), so one MMA covers all kernel rows, N = R * cb;
+//   D[k][(r, c)] += A * B^T  (4 MMAs of K = 8).
+// The ring keeps every x row once; rows that wrap around its end are also
+// stored in R - 1 mirror slots after it, so any R consecutive rows are
 // contiguous.  Padding rows and columns come from TMA's zero fill.
-// The epilogue permutes D_s into dW's [c][r][s] order through shared memory
-// and adds each dW row segment in L2 with one bulk async reduction.
+// Each block writes its partial tile to the workspace; a second kernel sums
+// the partials of a tile in a fixed order into dW (deterministic).
 //
-// Roles: warp 0 issues TMA, warp 1 issues MMAs, warps 2-9 (two groups of
-// four, one warp per TMEM lane quarter, alternating items) write the A
-// operand and then run the epilogue.  Every wait is bounded (2 s); on a
-// timeout the block sets the workspace status bit and stops.
+// Roles: warp 0 issues the x-row TMA loads, warp 10 the dz-tile TMA loads
+// (one issuing thread costs a few hundred cycles per copy, so the two streams
+// get a thread each), warp 1 issues MMAs, warps 2-9 (two groups of four, one
+// warp per TMEM lane quarter, alternating items) move dz into TMEM, check
+// that the item's x rows have landed, and then run the epilogue.  The MMA
+// thread waits once and commits once per item.  Every wait is bounded
+// (2 s); on a timeout the block sets the workspace status bit and stops.
 #include <cuda.h>
 
 #include "cba_internal.cuh"
@@ -35,42 +39,49 @@ namespace cba {
 namespace {
 
 constexpr uint64_t kW4LimitNs = 2000000000ull;
-constexpr int kW4Threads = 320;
-constexpr int kW4MaxNR = 8;   // x ring rows (mirror slots come on top)
-constexpr int kW4ND = 4;      // dz ring slots (even: each producer group owns half)
-constexpr int kW4Stages = 2;  // A stages in TMEM (one per producer group)
+constexpr int kW4Threads = 352;
+constexpr int kW4MaxNR = 12;  // x ring rows (mirror slots come on top)
+constexpr int kW4MaxND = 8;   // dz ring slots
+// TMA loads take about a microsecond to land, so the rings are as deep as
+// shared memory allows: enough loads stay in flight to cover that latency.
+constexpr int kW4NA = 4;      // A stages in TMEM (even), one item pair (64 columns) each
+constexpr int kW4Done = 16;   // pair-completion barriers (a ring; lag stays below 16)
+
+struct W4Geom {
+    bool ok;
+    int cb, N, nctile, ktiles, ntiles, cpt, items, nwc, grid, kbox, nr, nd;
+    uint32_t xslot_bytes, dz_bytes, dz_stride, dz_off;
+    size_t smem, part_bytes;
+};
 
 struct W4Args {
-    float *dW;
+    float *part;             // [grid][N][128] partial tiles
     unsigned *status;
-    int K, C, RS, CRS;
-    int Pe, pad, nwc, Wx;
+    int S, Pe, pad, nwc, Wx;
     int bq_lo, bd_lo;
     int kbox;                // channels per dz box
-    int wdz;                 // dz columns per box (32 + S - 1)
-    int cb;                  // input channels per block
+    int cb, N;               // input channels per block, MMA N = R * cb
     int nctile;              // c tiles
-    int ctas_per_tile;
+    int cpt;                 // blocks per tile
     int items_per_tile;      // N * nwc * Pe
     int nr;                  // x ring rows
+    int nd;                  // dz ring slots
     uint32_t xslot_bytes;    // cb * 128
-    uint32_t dz_bytes;       // wdz * kbox * 4
+    uint32_t dz_bytes;       // 32 * kbox * 4
     uint32_t dz_stride;      // ring slot stride (128-byte multiple)
     uint32_t dz_off;         // byte offset of the dz ring
-    int pitch;               // floats per staged dW row (16-byte multiple, 4 mod 32)
-    int bulk;                // 1: bulk reductions aligned
 };
 
 struct W4Bars {
-    uint64_t x_full[kW4MaxNR], x_empty[kW4MaxNR];
-    uint64_t dz_full[kW4ND], dz_empty[kW4ND];
-    uint64_t a_full[kW4Stages], a_empty[kW4Stages], accum;
+    uint64_t x_full[kW4MaxNR];
+    uint64_t dz_full[kW4MaxND], dz_empty[kW4MaxND];
+    uint64_t a_full[kW4NA], done[kW4Done], accum;
     uint32_t tmem_base;
     int abort_flag;
 };
 
 struct Item {
-    int n, w0, p, seg;
+    int n, w0, p;
 };
 
 __device__ __forceinline__ Item decode(const W4Args &a, int i) {
@@ -81,11 +92,18 @@ __device__ __forceinline__ Item decode(const W4Args &a, int i) {
     const int wc = rem / a.Pe;
     it.p = rem - wc * a.Pe;
     it.w0 = wc * 32;
-    it.seg = it.n * a.nwc + wc;
     return it;
 }
 
-template <int R, int S>
+// Item bookkeeping shared by the roles.  Items advance incrementally (p
+// fastest, then the column chunk, then n).  x rows form one sequence t: a
+// segment (fixed n and column chunk) loads R rows for its first item and one
+// more per further item, and item j's window is rows t_ws(j) .. t_ws(j)+R-1.
+// Items go through the tensor core in pairs (2m, 2m + 1), which share a TMEM
+// stage, one wait and one commit: pair m's MMAs complete done[m % kW4Done];
+// the MMA thread waits only for a_full, which the producers signal once the
+// pair's A operands are in TMEM and its x rows have landed.
+template <int R>
 __global__ void __launch_bounds__(kW4Threads, 1)
     wgrad_tc4_kernel(const __grid_constant__ CUtensorMap tmx,
                      const __grid_constant__ CUtensorMap tmdz, const W4Args a) {
@@ -95,29 +113,25 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     __shared__ W4Bars sb;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = blockIdx.x / a.ctas_per_tile, split = blockIdx.x % a.ctas_per_tile;
-    const int k0 = (tile / a.nctile) * 128, c0 = (tile % a.nctile) * a.cb;
-    const int i0 = (int)((long long)split * a.items_per_tile / a.ctas_per_tile);
-    const int i1 = (int)((long long)(split + 1) * a.items_per_tile / a.ctas_per_tile);
+    const int tile = blockIdx.x / a.cpt, split = blockIdx.x % a.cpt;
+    const int s = tile % a.S, kc = tile / a.S;
+    const int k0 = (kc / a.nctile) * 128, c0 = (kc % a.nctile) * a.cb;
+    const int i0 = (int)((long long)split * a.items_per_tile / a.cpt);
+    const int i1 = (int)((long long)(split + 1) * a.items_per_tile / a.cpt);
     const bool has_work = i1 > i0;
-    const int N = R * a.cb;                                    // MMA N
-    const uint32_t acol0 = (uint32_t)(S * N);                  // first A column
+    const int cnt = has_work ? i1 - i0 : 0;
+    const uint32_t acol0 = (uint32_t)a.N;  // first A column (accumulator at 0)
     uint8_t *xring = smem;
     uint8_t *dzring = smem + a.dz_off;
 
     if (tid == 0) {
-        for (int i = 0; i < kW4MaxNR; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&sb.x_full[i]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sb.x_empty[i]), 1);
-        }
-        for (int i = 0; i < kW4ND; ++i) {
+        for (int i = 0; i < kW4MaxNR; ++i) ptx::mbar_init(ptx::smem_u32(&sb.x_full[i]), 1);
+        for (int i = 0; i < kW4Done; ++i) ptx::mbar_init(ptx::smem_u32(&sb.done[i]), 1);
+        for (int i = 0; i < kW4MaxND; ++i) {
             ptx::mbar_init(ptx::smem_u32(&sb.dz_full[i]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sb.dz_empty[i]), 128);
+            ptx::mbar_init(ptx::smem_u32(&sb.dz_empty[i]), 4);  // one arrival per warp
         }
-        for (int i = 0; i < kW4Stages; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&sb.a_full[i]), 128);
-            ptx::mbar_init(ptx::smem_u32(&sb.a_empty[i]), 1);
-        }
+        for (int i = 0; i < kW4NA; ++i) ptx::mbar_init(ptx::smem_u32(&sb.a_full[i]), 4);
         ptx::mbar_init(ptx::smem_u32(&sb.accum), 1);
         sb.abort_flag = 0;
         ptx::fence_mbar_init();
@@ -134,22 +148,26 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     if (warp == 0) {
         // ---- TMA: x rows into the ring (and its mirror slots), dz tiles
         if (lane == 0 && has_work) {
-            int t_row = 0, seg = -1, h_next = 0, j = 0;
+            Item it = decode(a, i0);
+            int wc = it.w0 >> 5;
+            int t_row = 0, h_next = it.p - a.pad, j_seg_end = -1;
+            int last_user[kW4MaxNR];  // per ring slot: last item reading the row held
+            int j = 0;
             bool ok = true;
-            for (int i = i0; ok && i < i1; ++i, ++j) {
-                const Item it = decode(a, i);
-                if (it.seg != seg) {
-                    seg = it.seg;
-                    h_next = it.p - a.pad;
-                }
+            for (; j < cnt; ++j) {
+                if (j > j_seg_end) j_seg_end = j + min(cnt - j, a.Pe - it.p) - 1;
                 const int h_top = it.p - a.pad + R - 1;
-                for (; ok && h_next <= h_top; ++h_next, ++t_row) {
+                for (; h_next <= h_top; ++h_next, ++t_row) {
                     const int slot = t_row % a.nr;
-                    if (t_row >= a.nr)
-                        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.x_empty[slot]),
-                                                    (uint32_t)(t_row / a.nr - 1) & 1u,
-                                                    &sb.abort_flag, a.status, kW4LimitNs);
+                    if (t_row >= a.nr) {
+                        const int u = last_user[slot] >> 1;  // pair of the last user
+                        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.done[u % kW4Done]),
+                                                    (uint32_t)(u / kW4Done) & 1u, &sb.abort_flag,
+                                                    a.status, kW4LimitNs);
+                    }
                     if (!ok) break;
+                    // the row sits at window position h - (p - pad) of item j
+                    last_user[slot] = min(j + (h_next - (it.p - a.pad)), j_seg_end);
                     const bool mirror = slot < R - 1;
                     const uint32_t bar = ptx::smem_u32(&sb.x_full[slot]);
                     ptx::mbar_arrive_expect_tx(bar, a.xslot_bytes * (mirror ? 2u : 1u));
@@ -161,17 +179,15 @@ __global__ void __launch_bounds__(kW4Threads, 1)
                             it.w0, h_next, c0, it.n, bar);
                 }
                 if (!ok) break;
-                const int ds = j % kW4ND;
-                if (j >= kW4ND)
-                    ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_empty[ds]),
-                                                (uint32_t)(j / kW4ND - 1) & 1u, &sb.abort_flag,
-                                                a.status, kW4LimitNs);
-                if (!ok) break;
-                const uint32_t bar = ptx::smem_u32(&sb.dz_full[ds]);
-                ptx::mbar_arrive_expect_tx(bar, a.dz_bytes);
-                // columns w0 - (S - 1 - pad) .. w0 + 31 + pad of dz row p
-                ptx::tma_load_4d(ptx::smem_u32(dzring + (size_t)ds * a.dz_stride), &tmdz, k0,
-                                 it.w0 - (S - 1 - a.pad) + a.bq_lo, it.p + a.bd_lo, it.n, bar);
+                if (++it.p == a.Pe) {  // next item; a new segment restarts the x rows
+                    it.p = 0;
+                    if (++wc == a.nwc) {
+                        wc = 0;
+                        ++it.n;
+                    }
+                    it.w0 = wc * 32;
+                    h_next = -a.pad;
+                }
             }
             // no copy may be in flight when the block exits
             int no_abort = 0;
@@ -179,61 +195,84 @@ __global__ void __launch_bounds__(kW4Threads, 1)
                 ptx::mbar_wait_bounded(ptx::smem_u32(&sb.x_full[t % a.nr]),
                                        (uint32_t)(t / a.nr) & 1u, &no_abort, a.status,
                                        kW4LimitNs);
-            for (int jj = max(0, j - kW4ND); jj < j; ++jj)
-                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[jj % kW4ND]),
-                                       (uint32_t)(jj / kW4ND) & 1u, &no_abort, a.status,
+        }
+    } else if (warp == 10) {
+        // ---- TMA: dz tiles, one per item
+        if (lane == 0 && has_work) {
+            Item it = decode(a, i0);
+            int wc = it.w0 >> 5;
+            int j = 0, ds = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (; j < cnt; ++j) {
+                if (j >= a.nd)
+                    ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_empty[ds]), ph ^ 1u,
+                                                &sb.abort_flag, a.status, kW4LimitNs);
+                if (!ok) break;
+                const uint32_t bar = ptx::smem_u32(&sb.dz_full[ds]);
+                ptx::mbar_arrive_expect_tx(bar, a.dz_bytes);
+                // dz columns w0 - s + pad .. + 31 of row p
+                ptx::tma_load_4d(ptx::smem_u32(dzring + (size_t)ds * a.dz_stride), &tmdz, k0,
+                                 it.w0 - s + a.pad + a.bq_lo, it.p + a.bd_lo, it.n, bar);
+                if (++ds == a.nd) {
+                    ds = 0;
+                    ph ^= 1u;
+                }
+                if (++it.p == a.Pe) {
+                    it.p = 0;
+                    if (++wc == a.nwc) {
+                        wc = 0;
+                        ++it.n;
+                    }
+                    it.w0 = wc * 32;
+                }
+            }
+            // no copy may be in flight when the block exits
+            int no_abort = 0;
+            for (int jj = max(0, j - a.nd); jj < j; ++jj)
+                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[jj % a.nd]),
+                                       (uint32_t)(jj / a.nd) & 1u, &no_abort, a.status,
                                        kW4LimitNs);
         }
     } else if (warp == 1) {
-        // ---- MMA issue (one thread)
+        // ---- MMA issue (one thread): per item pair one wait, 2 x nks MMAs
+        // (operands hoisted) and one commit
         if (lane == 0 && has_work) {
-            const uint32_t idesc = ptx::idesc_tf32(128, N);
+            const uint32_t idesc = ptx::idesc_tf32(128, a.N);
             const uint64_t bd0 = ptx::smem_desc(ptx::smem_u32(xring), 16, 1024, 2);
             const uint32_t slot_units = a.xslot_bytes >> 4;
-            int t_row = 0, seg = -1, h_next = 0, t_seg = 0, h_first = 0, t_ready = 0, j = 0;
+            Item it = decode(a, i0);
+            int wc = it.w0 >> 5;
+            const int nks_last = min(4, (a.Wx - (a.nwc - 1) * 32 + 7) >> 3);
+            int t_ws = 0;
             bool ok = true;
-            for (int i = i0; ok && i < i1; ++i, ++j) {
-                const Item it = decode(a, i);
-                if (it.seg != seg) {
-                    seg = it.seg;
-                    h_next = h_first = it.p - a.pad;
-                    t_seg = t_row;
-                }
-                const int h_top = it.p - a.pad + R - 1;
-                t_row += h_top - h_next + 1;
-                h_next = h_top + 1;
-                const int t_ws = t_seg + (it.p - a.pad - h_first);  // window's first row
-                while (ok && t_ready < t_ws + R) {
-                    ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.x_full[t_ready % a.nr]),
-                                                (uint32_t)(t_ready / a.nr) & 1u,
-                                                &sb.abort_flag, a.status, kW4LimitNs);
-                    ++t_ready;
-                }
-                const int stage = j & 1;
-                if (ok)
-                    ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_full[stage]),
-                                                (uint32_t)(j >> 1) & 1u, &sb.abort_flag,
-                                                a.status, kW4LimitNs);
+            for (int m = 0; 2 * m < cnt; ++m) {
+                const int stage = m % kW4NA;
+                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_full[stage]),
+                                            (uint32_t)(m / kW4NA) & 1u, &sb.abort_flag,
+                                            a.status, kW4LimitNs);
                 if (!ok) break;
                 ptx::tc_fence_after();
-                const int nks = min(4, (a.Wx - it.w0 + 7) >> 3);
-                const uint64_t bd = bd0 + (uint64_t)((uint32_t)(t_ws % a.nr) * slot_units);
-                const uint32_t a_tm = tmem + acol0 + (uint32_t)(stage * S * 32);
+                const int nitems = min(2, cnt - 2 * m);
+                for (int e = 0; e < nitems; ++e) {
+                    const uint64_t bd = bd0 + (uint64_t)((uint32_t)(t_ws % a.nr) * slot_units);
+                    const uint32_t a_tm = tmem + acol0 + (uint32_t)(stage * 64 + e * 32);
+                    ptx::mma_tf32_ts(tmem, a_tm, bd, idesc, (m > 0 || e > 0) ? 1u : 0u);
+                    if (wc + 1 < a.nwc || nks_last == 4) {
 #pragma unroll
-                for (int s = 0; s < S; ++s) {
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        if (ks < nks)
-                            ptx::mma_tf32_ts(tmem + (uint32_t)(s * N), a_tm + s * 32 + ks * 8,
-                                             bd + 2 * ks, idesc, (j > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 1; ks < 4; ++ks)
+                            ptx::mma_tf32_ts(tmem, a_tm + ks * 8, bd + 2 * ks, idesc, 1u);
+                    } else {
+                        for (int ks = 1; ks < nks_last; ++ks)
+                            ptx::mma_tf32_ts(tmem, a_tm + ks * 8, bd + 2 * ks, idesc, 1u);
+                    }
+                    t_ws += it.p + 1 == a.Pe ? R : 1;
+                    if (++it.p == a.Pe) {
+                        it.p = 0;
+                        if (++wc == a.nwc) wc = 0;
+                    }
                 }
-                ptx::mma_commit(ptx::smem_u32(&sb.a_empty[stage]));
-                // x rows the next item does not use
-                bool seg_end = i + 1 >= i1;
-                if (!seg_end) seg_end = decode(a, i + 1).seg != seg;
-                const int nrel = seg_end ? R : 1;
-                for (int u = 0; u < nrel; ++u)
-                    ptx::mma_commit(ptx::smem_u32(&sb.x_empty[(t_ws + u) % a.nr]));
+                ptx::mma_commit(ptx::smem_u32(&sb.done[m % kW4Done]));
             }
             if (!ok) {  // the epilogue must not take the drain below for a result
                 *reinterpret_cast<volatile int *>(&sb.abort_flag) = 1;
@@ -245,93 +284,83 @@ __global__ void __launch_bounds__(kW4Threads, 1)
             ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &no_abort, a.status, kW4LimitNs);
         }
     } else {
-        // ---- A producers: group g writes the items j = g, g + 2, ... into
-        // TMEM stage g.  Thread = TMEM lane kl = output channel k0 + kl.
+        // ---- A producers: group g takes the item pairs m = g, g + 2, ...;
+        // pair m goes to TMEM stage m % kW4NA (item 2m in its first 32
+        // columns, item 2m + 1 in the next 32).  Thread = TMEM lane kl =
+        // output channel k0 + kl.
         const int g = (warp - 2) >> 2, quarter = warp & 3;
         const int kl = quarter * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         const bool kv = kl < a.kbox;
+        int p = has_work ? decode(a, i0).p : 0;
+        int t_ws = 0, t_ready = 0;  // x rows this warp has seen land (lane 0)
         bool ok = true;
-        for (int j = g; has_work && i0 + j < i1; j += 2) {
-            const int ds = j % kW4ND;
-            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[ds]),
-                                        (uint32_t)(j / kW4ND) & 1u, &sb.abort_flag, a.status,
-                                        kW4LimitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            constexpr int WDZ = 32 + S - 1;
-            float v[WDZ];
-            const float *tilep = reinterpret_cast<const float *>(dzring + (size_t)ds * a.dz_stride);
-#pragma unroll
-            for (int jj = 0; jj < WDZ; ++jj) v[jj] = kv ? tilep[jj * a.kbox + kl] : 0.f;
-            ptx::mbar_arrive(ptx::smem_u32(&sb.dz_empty[ds]));
-            if (j >= 2)
-                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_empty[g]),
-                                            (uint32_t)((j >> 1) - 1) & 1u, &sb.abort_flag,
-                                            a.status, kW4LimitNs);
+        for (int m = 0; 2 * m < cnt; ++m) {
+            const int nitems = min(2, cnt - 2 * m);
+            const int t_lo = t_ws;  // rows the pair needs: t_lo .. t_hi - 1
+            int t_hi = 0;
+            for (int e = 0; e < nitems; ++e) {
+                t_hi = t_ws + R;
+                t_ws += p + 1 == a.Pe ? R : 1;
+                if (++p == a.Pe) p = 0;
+            }
+            if ((m & 1) != g) continue;
+            if (m >= kW4NA)  // the stage was last read by pair m - kW4NA
+                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.done[(m - kW4NA) % kW4Done]),
+                                            (uint32_t)((m - kW4NA) / kW4Done) & 1u,
+                                            &sb.abort_flag, a.status, kW4LimitNs);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            const uint32_t a_tm = tmem + lane_addr + acol0 + (uint32_t)(g * S * 32);
+            for (int e = 0; e < nitems; ++e) {
+                const int j = 2 * m + e;
+                const int ds = j % a.nd;
+                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[ds]),
+                                            (uint32_t)(j / a.nd) & 1u, &sb.abort_flag,
+                                            a.status, kW4LimitNs);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                float v[32];
+                const float *tilep =
+                    reinterpret_cast<const float *>(dzring + (size_t)ds * a.dz_stride);
 #pragma unroll
-            for (int s = 0; s < S; ++s) {
-                // A_s[j] = dz[w0 + j - s + pad] = tile[j + S - 1 - s]
-                float w[32];
-#pragma unroll
-                for (int q = 0; q < 32; ++q) w[q] = v[q + S - 1 - s];
-                ptx::tmem_st32(a_tm + (uint32_t)(s * 32), w);
+                for (int q = 0; q < 32; ++q) v[q] = kv ? tilep[q * a.kbox + kl] : 0.f;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.dz_empty[ds]));
+                ptx::tmem_st32(tmem + lane_addr + acol0 + (uint32_t)((m % kW4NA) * 64 + e * 32),
+                               v);
             }
+            if (!ok) break;
+            // the pair's x rows must have landed before the MMA may start
+            if (lane == 0) {
+                for (int t = max(t_ready, t_lo); ok && t < t_hi; ++t)
+                    ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.x_full[t % a.nr]),
+                                                (uint32_t)(t / a.nr) & 1u, &sb.abort_flag,
+                                                a.status, kW4LimitNs);
+                t_ready = t_hi;
+            }
+            ok = __all_sync(0xffffffffu, __shfl_sync(0xffffffffu, ok, 0));
             ptx::tmem_st_wait();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[g]));
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[m % kW4NA]));
         }
-        // ---- epilogue: D_s[k][(r, c)] -> staged dW rows [c][r][s] -> L2
+        // ---- epilogue: D[k][col] -> part[block][col][k] (coalesced over k)
         if (has_work && ok)
             ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
                                         kW4LimitNs);
         if (ok) ok = *reinterpret_cast<volatile int *>(&sb.abort_flag) == 0;
         ok = __all_sync(0xffffffffu, ok) && has_work;
-        // both groups agree before the ring memory is reused for staging
-        ok = ptx::named_bar_and(1, 256, ok);
         if (ok) {
             ptx::tc_fence_after();
-            float *stg = reinterpret_cast<float *>(smem);
-            const int cvalid = min(a.cb, a.C - c0);
-            const int ngrp = (cvalid + 3) >> 2;
-            float *row = stg + (size_t)kl * a.pitch;
-            for (int cg = g; cg < ngrp; cg += 2) {
-                float vals[4 * R * S];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-#pragma unroll
-                    for (int s = 0; s < S; ++s) {
-                        float t4[4];
-                        ptx::tmem_ld4(tmem + lane_addr + (uint32_t)(s * N + r * a.cb + cg * 4),
-                                      t4);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) vals[e * R * S + r * S + s] = t4[e];
-                    }
-                }
+            float *dst = a.part + (size_t)blockIdx.x * a.N * 128 + kl;
+            for (int cc = g; cc * 16 < a.N; cc += 2) {
+                float v[16];
+                ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(cc * 16), v);
                 ptx::tmem_ld_wait();
-                float4 *dst = reinterpret_cast<float4 *>(row + cg * 4 * R * S);
 #pragma unroll
-                for (int u = 0; u < R * S; ++u)
-                    dst[u] = make_float4(vals[4 * u], vals[4 * u + 1], vals[4 * u + 2],
-                                         vals[4 * u + 3]);
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(1, 256);
-            const bool krow = g == 0 && k0 + kl < a.K;
-            if (krow) {
-                float *dst = a.dW + (long long)(k0 + kl) * a.CRS + (long long)c0 * a.RS;
-                const int nel = cvalid * a.RS;
-                if (a.bulk) {
-                    ptx::bulk_reduce_add_f32(dst, ptx::smem_u32(row), (uint32_t)nel * 4u);
-                    ptx::bulk_commit();
-                    ptx::bulk_wait_all();
-                } else {
-                    for (int e = 0; e < nel; ++e) atomicAdd(dst + e, row[e]);
-                }
+                for (int e = 0; e < 16; ++e) dst[(size_t)(cc * 16 + e) * 128] = v[e];
             }
         }
     }
@@ -344,93 +373,150 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     }
 }
 
+// dW[k0 + kl][c0 + c][r][s] += sum over the tile's blocks b of
+// part[tile * cpt + b][r * cb + c][kl].  One block per (tile, column): warp w
+// sums the blocks b = w, w + 8, ... for all 128 kl (a float4 per lane), then
+// warp 0 adds the eight warp sums in order (a fixed order: deterministic).
+__global__ void __launch_bounds__(256)
+    wgrad_part_reduce_kernel(const float *__restrict__ part, int cpt, int N, int cb, int S,
+                             int nctile, int K, int C, int R, float *__restrict__ dW) {
+    __shared__ float4 red[8][32];
+    const int col = blockIdx.x % N, tile = blockIdx.x / N;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float4 *src = reinterpret_cast<const float4 *>(part + ((size_t)tile * cpt * N + col) * 128) + lane;
+    const size_t bstride = (size_t)N * 32;  // float4s between consecutive blocks
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int b = warp; b < cpt; b += 8) {
+        const float4 v = __ldg(src + (size_t)b * bstride);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    red[warp][lane] = acc;
+    __syncthreads();
+    if (warp == 0) {
+        float4 t = red[0][lane];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) {
+            const float4 u = red[w][lane];
+            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+        }
+        const int s = tile % S, kc = tile / S;
+        const int r = col / cb, c = (kc % nctile) * cb + col % cb;
+        if (c >= C) return;
+        const float vals[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int k = (kc / nctile) * 128 + lane * 4 + e;
+            if (k < K) dW[(((size_t)k * C + c) * R + r) * S + s] += vals[e];
+        }
+    }
+}
+
+W4Geom w4_geom(const Plan &p) {
+    W4Geom w{};
+    w.ok = false;
+    if (p.stride != 1) return w;
+    if (!((p.R == 3 && p.S == 3) || (p.R == 1 && p.S == 1))) return w;
+    if (p.pad > p.S - 1) return w;
+    const DzcGeom g = dzc_geom(p);
+    if (g.We % 4 != 0) return w;  // x rows must be 16-byte strided for TMA
+    // input channels per block: N = R * cb a multiple of 16, at most 256
+    const int cap = p.R == 1 ? 256 : 64;
+    w.cb = std::min(cap, (p.C + 15) / 16 * 16);
+    w.N = p.R * w.cb;
+    if (w.N > 256 || w.N % 16 != 0 || w.N + kW4NA * 64 > 512) return w;
+    w.nctile = (p.C + w.cb - 1) / w.cb;
+    w.ktiles = (p.K + 127) / 128;
+    w.ntiles = w.ktiles * w.nctile * p.S;
+    w.nwc = (g.We + 31) / 32;
+    const long long items = (long long)p.N * w.nwc * g.Pe;
+    if (items >= (1LL << 31)) return w;
+    w.items = (int)items;
+    w.cpt = std::max(1, std::min(w.items, p.num_sms / w.ntiles));
+    w.grid = w.ntiles * w.cpt;
+    w.kbox = std::min(128, g.Kp);
+    w.xslot_bytes = (uint32_t)w.cb * 128u;
+    w.dz_bytes = (uint32_t)(32 * w.kbox * 4);
+    w.dz_stride = (w.dz_bytes + 127u) / 128u * 128u;
+    // shared memory: dz ring, x ring with its mirror slots; as deep as fits,
+    // at least 4 dz slots and R + 2 x rows
+    const size_t budget = 224 * 1024;
+    int nd = kW4MaxND, nr = kW4MaxNR;
+    auto bytes = [&](int d, int r) {
+        return (size_t)d * w.dz_stride + (size_t)(r + p.R - 1) * w.xslot_bytes;
+    };
+    while (bytes(nd, nr) > budget && (nr > 8 || nd > 4) && nr > p.R + 2) {
+        if (nd > 4 && (nr <= 8 || nd * (size_t)w.dz_stride > (size_t)nr * w.xslot_bytes)) --nd;
+        else --nr;
+    }
+    while (bytes(nd, nr) > budget && nr > p.R + 2) --nr;
+    while (bytes(nd, nr) > budget && nd > 2) --nd;
+    if (bytes(nd, nr) > budget) return w;
+    w.nr = nr;
+    w.nd = nd;
+    const size_t dz_ring = (size_t)nd * w.dz_stride;
+    w.dz_off = (uint32_t)((size_t)(nr + p.R - 1) * w.xslot_bytes);
+    w.smem = (size_t)w.dz_off + dz_ring + 1024;
+    w.part_bytes = (size_t)w.grid * w.N * 128 * sizeof(float);
+    w.ok = true;
+    return w;
+}
+
 }  // namespace
 
+size_t wgrad_tc4_ws_bytes(const Plan &p) {
+    const W4Geom w = w4_geom(p);
+    return w.ok ? w.part_bytes : 0;
+}
+
 bool wgrad_tc4_supported(const Plan &p, const float *x) {
-    if (p.stride != 1) return false;
-    const bool k3 = p.R == 3 && p.S == 3, k1 = p.R == 1 && p.S == 1;
-    if (!k3 && !k1) return false;
-    if (p.pad > p.S - 1) return false;
-    const DzcGeom g = dzc_geom(p);
-    if (g.We % 4 != 0) return false;  // x rows must be 16-byte strided for TMA
-    if ((reinterpret_cast<uintptr_t>(x) & 15u) != 0) return false;
-    if ((long long)p.N * ((g.We + 31) / 32) * g.Pe >= (1LL << 31)) return false;
-    return true;
+    if (!w4_geom(p).ok) return false;
+    return (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
 }
 
 cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, float *dW,
                              void *ws, cudaStream_t st, int *launches) {
+    const W4Geom w = w4_geom(p);
+    if (!w.ok) return cudaErrorNotSupported;
     const DzcGeom g = dzc_geom(p);
     W4Args a;
-    a.dW = dW;
+    a.part = ws_at<float>(ws, p.off_wgpart);
     a.status = ws_at<unsigned>(ws, p.off_status);
-    a.K = p.K; a.C = p.C; a.RS = p.RS; a.CRS = p.CRS;
-    a.Pe = g.Pe; a.pad = p.pad; a.nwc = (g.We + 31) / 32; a.Wx = g.We;
+    a.S = p.S; a.Pe = g.Pe; a.pad = p.pad; a.nwc = w.nwc; a.Wx = g.We;
     a.bq_lo = g.bq_lo; a.bd_lo = g.bd_lo;
-    a.kbox = std::min(128, g.Kp);
-    a.wdz = 32 + p.S - 1;
-    // input channels per block: N = R * cb <= 256 and the S accumulators plus
-    // two A stages within 512 TMEM columns; cb a multiple of 8
-    int cb_cap = p.R == 1 ? 256 : 32;
-    int cb = std::min(cb_cap, (p.C + 7) / 8 * 8);
-    if ((p.R * cb) % 16 != 0) cb = (cb + 15) / 16 * 16;
-    if (p.S * p.R * cb + kW4Stages * p.S * 32 > 512 || p.R * cb > 256) return cudaErrorNotSupported;
-    a.cb = cb;
-    a.nctile = (p.C + cb - 1) / cb;
-    const int ktiles = (p.K + 127) / 128;
-    const int ntiles = ktiles * a.nctile;
-    a.items_per_tile = p.N * a.nwc * g.Pe;
-    a.ctas_per_tile = std::max(1, std::min(a.items_per_tile, p.num_sms / ntiles));
-    a.xslot_bytes = (uint32_t)cb * 128u;
-    a.dz_bytes = (uint32_t)(a.wdz * a.kbox * 4);
-    a.dz_stride = (a.dz_bytes + 127u) / 128u * 128u;
-    // shared memory: x ring (nr + R - 1 slots), dz ring; the staging area
-    // for the epilogue reuses it
-    const size_t budget = 220 * 1024;
-    const size_t dz_ring = (size_t)kW4ND * a.dz_stride;
-    int nr = kW4MaxNR;
-    while (nr > p.R && (size_t)(nr + p.R - 1) * a.xslot_bytes + dz_ring > budget) --nr;
-    if ((size_t)(nr + p.R - 1) * a.xslot_bytes + dz_ring > budget || nr < p.R)
-        return cudaErrorNotSupported;
-    a.nr = nr;
-    a.dz_off = (uint32_t)((size_t)(nr + p.R - 1) * a.xslot_bytes);
-    int pitch = cb * p.RS;
-    pitch = (pitch + 3) / 4 * 4;
-    while (pitch % 32 != 4) pitch += 4;
-    a.pitch = pitch;
-    const size_t main_bytes = (size_t)a.dz_off + dz_ring;
-    const size_t stage_bytes = (size_t)128 * pitch * 4;
-    const size_t smem = std::max(main_bytes, stage_bytes) + 1024;
-    if (smem > 227 * 1024) return cudaErrorNotSupported;
-    const int cvalid_last = p.C - (a.nctile - 1) * cb;
-    a.bulk = (p.CRS % 4 == 0) && ((cb * p.RS) % 4 == 0) && ((cvalid_last * p.RS) % 4 == 0) &&
-             ((reinterpret_cast<uintptr_t>(dW) & 15u) == 0);
+    a.kbox = w.kbox; a.cb = w.cb; a.N = w.N; a.nctile = w.nctile; a.cpt = w.cpt;
+    a.items_per_tile = w.items; a.nr = w.nr; a.nd = w.nd;
+    a.xslot_bytes = w.xslot_bytes; a.dz_bytes = w.dz_bytes; a.dz_stride = w.dz_stride;
+    a.dz_off = w.dz_off;
 
     alignas(64) CUtensorMap tmx, tmdz;
     {
         const uint64_t d[4] = {(uint64_t)g.We, (uint64_t)g.He, (uint64_t)p.C, (uint64_t)p.N};
-        const uint32_t b[4] = {32, 1, (uint32_t)cb, 1};
+        const uint32_t b[4] = {32, 1, (uint32_t)w.cb, 1};
         if (!tma_encode_f32(&tmx, x, 4, d, b, true)) return cudaErrorInvalidValue;
     }
     {
         const uint64_t d[4] = {(uint64_t)g.Kp, (uint64_t)g.Qpp, (uint64_t)g.Pp, (uint64_t)p.N};
-        const uint32_t b[4] = {(uint32_t)a.kbox, (uint32_t)a.wdz, 1, 1};
+        const uint32_t b[4] = {(uint32_t)w.kbox, 32, 1, 1};
         if (!tma_encode_f32(&tmdz, dzc, 4, d, b, false)) return cudaErrorInvalidValue;
     }
-    const dim3 grid((unsigned)(ntiles * a.ctas_per_tile));
     cudaError_t e;
     if (p.R == 3) {
-        e = cudaFuncSetAttribute(wgrad_tc4_kernel<3, 3>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(wgrad_tc4_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)w.smem);
         if (e != cudaSuccess) return e;
-        wgrad_tc4_kernel<3, 3><<<grid, kW4Threads, smem, st>>>(tmx, tmdz, a);
+        wgrad_tc4_kernel<3><<<w.grid, kW4Threads, w.smem, st>>>(tmx, tmdz, a);
     } else {
-        e = cudaFuncSetAttribute(wgrad_tc4_kernel<1, 1>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = cudaFuncSetAttribute(wgrad_tc4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)w.smem);
         if (e != cudaSuccess) return e;
-        wgrad_tc4_kernel<1, 1><<<grid, kW4Threads, smem, st>>>(tmx, tmdz, a);
+        wgrad_tc4_kernel<1><<<w.grid, kW4Threads, w.smem, st>>>(tmx, tmdz, a);
     }
-    *launches += 1;
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    wgrad_part_reduce_kernel<<<w.ntiles * w.N, 256, 0, st>>>(a.part, w.cpt, w.N, w.cb, p.S,
+                                                              w.nctile, p.K, p.C, p.R, dW);
+    *launches += 2;
     return cudaGetLastError();
 }
 
