@@ -51,10 +51,10 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->math = d->math; p->eps = d->eps;
     p->num_sms = kNumSMs;
 
-    // reduction pass: about 8 blocks of 256 threads per SM in total, at least
-    // ~2k elements per block
-    long long want = ceil_div((long long)p->num_sms * 8, p->K);
-    long long cap = std::max(1LL, p->m / 2048);
+    // reduction pass: about 2.5 blocks of 256 threads per SM in total (each
+    // keeps ~48 KB of loads in flight), at least ~8k elements per block
+    long long want = ceil_div((long long)p->num_sms * 5 / 2, p->K);
+    long long cap = std::max(1LL, p->m / 8192);
     p->red_splits = (int)std::max(1LL, std::min(want, cap));
 
     // SIMT wgrad: split the reduction so that ~4 blocks per SM exist
@@ -73,6 +73,9 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     size_t off = 0;
     p->off_status = off;
     off = align_up(off + 256, 256);
+    p->off_cnt = off;
+    off = align_up(off + sizeof(unsigned) * (size_t)p->K, 256);
+    p->clear_bytes = off;
     p->off_red = off;
     off = align_up(off + sizeof(double) * 2 * (size_t)p->red_splits * p->K, 256);
     p->off_coef = off;
@@ -179,7 +182,7 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     cudaGetLastError();  // the launches below report only their own errors
     cudaError_t e = select_device(st, delta);
     if (e != cudaSuccess) return fail_cuda(e);
-    e = cudaMemsetAsync(workspace, 0, 256, st);  // status word
+    e = cudaMemsetAsync(workspace, 0, p.clear_bytes, st);  // status word, reduction counters
     if (e == cudaSuccess) e = tr.mark(0);
     if (e == cudaSuccess) e = launch_reduce(p, delta, output, z, gamma, mean, var, db, dgamma,
                                             workspace, st, &n_launch);

@@ -33,7 +33,7 @@ struct Plan {
     float eps;
     int num_sms;
     // reduction pass
-    int red_splits;  // blocks per channel
+    int red_splits;  // reduction blocks (and partials) per channel
     // SIMT wgrad split-K
     int wg_splits;
     long long wg_chunk;  // reduction positions per split (multiple of the K tile)
@@ -44,7 +44,10 @@ struct Plan {
     long long tc_wg_chunk;
     int tc_dg_bn, tc_dg_ntiles;
     // workspace layout (byte offsets from the base)
-    size_t off_status, off_red, off_coef, off_wgpart, off_wt, off_dzt, off_wr, total;
+    // off_cnt: per-channel arrival counters of the reduction (zeroed with the
+    // status word at the start of every call; clear_bytes covers both)
+    size_t off_status, off_cnt, clear_bytes, off_red, off_coef, off_wgpart, off_wt, off_dzt,
+        off_wr, total;
 };
 
 // Builds the plan; returns CBA_OK or a CBA_ERR_* code.

@@ -13,17 +13,20 @@
 // per-channel coefficients.  Here the scratch is one file-scope __device__
 // array, kScratchBytes (1 MiB), placed on every device that loads this
 // library and held there until the process exits.  The entry point allocates
-// nothing: the only CUDA calls are cudaGetSymbolAddress (once per device), the
-// kernel launches, and the device/stream queries that select the device.
+// nothing: the only CUDA calls are cudaGetSymbolAddress (once per device), one
+// memset and the kernel launches on the stream, and the device/stream queries
+// that select the device.
 //
 // Scratch contents: every call shares the one array per device, and the array
-// keeps whatever the last call left in it.  No word is read before the same
-// call writes it: the reduction kernel writes every partial before the
-// finalize kernel reads them, and finalize writes every coefficient before
-// the dz kernel reads them.  So nothing has to start at zero, and nothing is
-// cleared.  Calls that overlap on one device (two streams, or two host
-// threads, with no ordering between them) race on the array; the caller must
-// order them, e.g. by using one stream.
+// keeps whatever the last call left in it.  Only the per-channel arrival
+// counters of the reduction must start at zero, so every call first clears
+// them (a memset of 4 * K bytes on the stream, not an allocation).  Every
+// other word is written before it is read in the same call: each reduction
+// block writes its partial before the channel's last block reads them all,
+// and that block writes the coefficients before the dz kernel reads them.
+// Calls that overlap on one device (two streams, or two host threads, with no
+// ordering between them) race on the array; the caller must order them, e.g.
+// by using one stream.
 #include <mutex>
 
 #include "cba_internal.cuh"
@@ -106,14 +109,17 @@ extern "C" int cba_bn_act_backward_noalloc(const cba_desc_t *d, const float *out
         if (misaligned16(q)) return CBA_ERR_ALIGN;
     if (p.K > CBA_NOALLOC_MAX_K) return CBA_ERR_SCRATCH_LIMIT;
 
-    // scratch layout: coefficients [K] at 0, then the partials [splits][K]
+    // scratch layout: arrival counters [K] at 0, coefficients [K], then the
+    // partials [splits][K]
+    const size_t cnt_bytes = align256(sizeof(unsigned) * (size_t)p.K);
     const size_t coef_bytes = align256(sizeof(Coef) * (size_t)p.K);
     const size_t part_unit = sizeof(double) * 2 * (size_t)p.K;  // one split
-    const long long fit = (long long)((kScratchBytes - coef_bytes) / part_unit);
+    const long long fit = (long long)((kScratchBytes - cnt_bytes - coef_bytes) / part_unit);
     if (fit < 1) return CBA_ERR_SCRATCH_LIMIT;  // unreachable with K <= CBA_NOALLOC_MAX_K
     p.red_splits = (int)std::min<long long>(p.red_splits, fit);
-    p.off_coef = 0;
-    p.off_red = coef_bytes;
+    p.off_cnt = 0;
+    p.off_coef = cnt_bytes;
+    p.off_red = cnt_bytes + coef_bytes;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaGetLastError();  // the launches below report only their own errors
@@ -125,7 +131,10 @@ extern "C" int cba_bn_act_backward_noalloc(const cba_desc_t *d, const float *out
     e = scratch_for_device(dev, &scratch);
     if (e != cudaSuccess) return report_cuda_error(e);
     int n_launch = 0;
-    e = launch_reduce(p, delta, output, z, gamma, mean, var, db, dgamma, scratch, st, &n_launch);
+    e = cudaMemsetAsync(scratch, 0, cnt_bytes, st);  // the reduction's arrival counters
+    if (e == cudaSuccess)
+        e = launch_reduce(p, delta, output, z, gamma, mean, var, db, dgamma, scratch, st,
+                          &n_launch);
     if (e == cudaSuccess && dz_out) e = launch_dz_out(p, delta, output, z, scratch, dz_out, st);
     if (e != cudaSuccess) return report_cuda_error(e);
     return CBA_OK;

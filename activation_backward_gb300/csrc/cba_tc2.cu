@@ -131,6 +131,100 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// dz in the channels-last layout only: dzc [N][Pp][Qpp][Kp] with a zero border
+// of bd_lo / bq_lo rows / columns before the data (zeros after it too, and in
+// the channels K .. Kp-1).  Block (bx, n * Pp + pp, kz): bx < nqc transposes
+// output columns 32 bx .. 32 bx + 31 of row pp - bd_lo for the 64 channels
+// 64 kz .. 64 kz + 63 through shared memory (each thread reads 4 consecutive
+// columns of one channel from each input, and writes 4 consecutive channels
+// of one column as a float4); bx == nqc writes the border columns.
+template <int ACT, bool BN, bool VEC>
+__global__ void __launch_bounds__(256)
+    dzc_kernel(const float *__restrict__ delta, const float *__restrict__ output,
+               const float *__restrict__ z, const Coef *__restrict__ coef, int K, int Pe, int Qe,
+               int Kp, int Pp, int Qpp, int bd_lo, int bq_lo, int nqc, float *__restrict__ dzc) {
+    __shared__ float tile[32][65];
+    const int t = threadIdx.x;
+    const int n = blockIdx.y / Pp, pp = blockIdx.y - (blockIdx.y / Pp) * Pp, p = pp - bd_lo;
+    const int k0 = blockIdx.z * 64;
+    float *rowp = dzc + ((size_t)n * Pp + pp) * Qpp * Kp;
+    const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    if ((int)blockIdx.x == nqc) {  // border columns (left and right of the data)
+        const int nright = Qpp - bq_lo - Qe;
+        const int ncols = bq_lo + nright;
+        for (int i = t; i < ncols * 16; i += 256) {
+            const int c = i >> 4, kc = k0 + (i & 15) * 4;
+            const int pq = c < bq_lo ? c : bq_lo + Qe + (c - bq_lo);
+            if (kc < Kp) *reinterpret_cast<float4 *>(rowp + (size_t)pq * Kp + kc) = zero4;
+        }
+        return;
+    }
+    const int q0 = blockIdx.x * 32;
+    if (p < 0 || p >= Pe) {  // zero border row
+        for (int i = t; i < 32 * 16; i += 256) {
+            const int qq = i >> 4, kc = k0 + (i & 15) * 4;
+            if (q0 + qq < Qe && kc < Kp)
+                *reinterpret_cast<float4 *>(rowp + (size_t)(q0 + qq + bq_lo) * Kp + kc) = zero4;
+        }
+        return;
+    }
+    {
+        const int kk = t >> 3, q4 = t & 7;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int kl = kk + 32 * pass, k = k0 + kl;
+            float v[4] = {0.f, 0.f, 0.f, 0.f};
+            if (k < K) {
+                const size_t base = (((size_t)n * K + k) * Pe + p) * Qe;
+                const Coef cf = coef[k];
+                float d[4], y[4], zz[4];
+                if (VEC && q0 + 4 * q4 < Qe) {  // rows 16-byte aligned, Qe a multiple of 4
+                    const size_t o = base + q0 + 4 * q4;
+                    const float4 d4 = __ldg(reinterpret_cast<const float4 *>(delta + o));
+                    d[0] = d4.x; d[1] = d4.y; d[2] = d4.z; d[3] = d4.w;
+                    if constexpr (ACT == CBA_ACT_LEAKY) {
+                        const float4 y4 = __ldg(reinterpret_cast<const float4 *>(output + o));
+                        y[0] = y4.x; y[1] = y4.y; y[2] = y4.z; y[3] = y4.w;
+                    } else {
+                        y[0] = y[1] = y[2] = y[3] = 0.f;
+                    }
+                    if constexpr (BN) {
+                        const float4 z4 = __ldg(reinterpret_cast<const float4 *>(z + o));
+                        zz[0] = z4.x; zz[1] = z4.y; zz[2] = z4.z; zz[3] = z4.w;
+                    } else {
+                        zz[0] = zz[1] = zz[2] = zz[3] = 0.f;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int q = q0 + 4 * q4 + e;
+                        const bool in = !VEC && q < Qe;
+                        d[e] = in ? __ldg(delta + base + q) : 0.f;
+                        y[e] = (ACT == CBA_ACT_LEAKY && in) ? __ldg(output + base + q) : 0.f;
+                        zz[e] = (BN && in) ? __ldg(z + base + q) : 0.f;
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = to_tf32(dz_of<ACT, BN>(d[e], y[e], zz[e], cf));
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tile[4 * q4 + e][kl] = v[e];
+        }
+    }
+    __syncthreads();
+    {
+        const int qq = t >> 4, k4 = t & 15;
+#pragma unroll
+        for (int pass = 0; pass < 2; ++pass) {
+            const int ql = qq + 16 * pass, q = q0 + ql, kc = k0 + 4 * k4;
+            if (q < Qe && kc < Kp)
+                *reinterpret_cast<float4 *>(rowp + (size_t)(q + bq_lo) * Kp + kc) =
+                    make_float4(tile[ql][4 * k4], tile[ql][4 * k4 + 1], tile[ql][4 * k4 + 2],
+                                tile[ql][4 * k4 + 3]);
+        }
+    }
+}
+
 // W[k][c][r][s] -> wr[r][s][c][kk] (kk < Kw; zero for kk >= K), TF32-rounded.
 __global__ void repack_wr_kernel(const float *__restrict__ W, int K, int C, int R, int S, int Kw,
                                  float *__restrict__ wr) {
@@ -1023,7 +1117,30 @@ cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float
     const V2Geom g = v2_geom(p);
     const Coef *coef = ws_at<Coef>(ws, p.off_coef);
     const bool leaky = p.act == CBA_ACT_LEAKY;
-    if (with_dzc) {
+    if (with_dzc && !with_dzt) {
+        float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) + dzt_bytes_only(p, g));
+        const int nqc = (g.Qe + 31) / 32;
+        dim3 grid((unsigned)(nqc + 1), (unsigned)(p.N * g.Pp), (unsigned)((g.Kp + 63) / 64));
+#define CBA_DZC(A, B)                                                                          \
+    do {                                                                                       \
+        if (g.Qe % 4 == 0)                                                                     \
+            dzc_kernel<A, B, true><<<grid, 256, 0, st>>>(delta, output, z, coef, p.K, g.Pe,   \
+                                                         g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo,    \
+                                                         g.bq_lo, nqc, dzc);                  \
+        else                                                                                   \
+            dzc_kernel<A, B, false><<<grid, 256, 0, st>>>(delta, output, z, coef, p.K, g.Pe,  \
+                                                          g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo,   \
+                                                          g.bq_lo, nqc, dzc);                 \
+    } while (0)
+        if (p.bn) {
+            if (leaky) CBA_DZC(CBA_ACT_LEAKY, true);
+            else CBA_DZC(CBA_ACT_LINEAR, true);
+        } else {
+            if (leaky) CBA_DZC(CBA_ACT_LEAKY, false);
+            else CBA_DZC(CBA_ACT_LINEAR, false);
+        }
+#undef CBA_DZC
+    } else if (with_dzc) {
         float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) + dzt_bytes_only(p, g));
         const int qlo = -g.bq_lo;
         const int qhi = with_dzt ? std::max(g.Qpp - g.bq_lo, g.Qp) : g.Qpp - g.bq_lo;

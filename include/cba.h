@@ -155,8 +155,9 @@ int cba_selftest_bounded_wait(void *workspace, size_t workspace_bytes, unsigned 
  * device that loads the library and held until the process exits.  The first
  * call on each device looks up the array's address (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.  All
- * calls on a device share the array and it keeps the last call's contents
- * (no call reads a word it has not written first, so nothing is cleared).
+ * calls on a device share the array and it keeps the last call's contents;
+ * each call first clears the reduction's per-channel counters (4 * K bytes,
+ * a memset on the stream) and writes every other word before reading it.
  * Calls that overlap on one device (other streams or host threads with no
  * ordering between them) race on it: order them, e.g. on one stream.
  *
