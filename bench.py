@@ -219,6 +219,28 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def profiled_traffic(phase):
+    """DRAM bytes per launch of a phase's kernels from the committed ncu summary,
+    or None when the kernel source has changed since that capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "darknet_3x3_tf32_kernels.md")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        if not line.startswith("traffic: "):
+            continue
+        f = dict(kv.split("=", 1) for kv in line.split()[1:])
+        if f.get("phase") != phase:
+            continue
+        src = os.path.join(ROOT, f["source"])
+        if not os.path.exists(src):
+            return None
+        if hashlib.sha1(open(src, "rb").read()).hexdigest() != f["sha1"]:
+            return None
+        return int(f["bytes"])
+    return None
+
+
 def config_dict(args, layers, ws):
     g = layers[0]["geom"]
     flops = sum(2 * l["geom"].gemm_flops() for l in layers)
@@ -322,9 +344,10 @@ def run_ours(args):
     gemm_half = flops / 2  # each of wgrad and dgrad carries half the FLOPs
     dom = "wgrad" if ph["wgrad"] >= ph["dgrad"] else "dgrad"
     achieved = gemm_half / (ph[dom] * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": f"{dom} ({args.math})", "achieved": achieved,
+    roofline = {"bound": "tensor", "kernel": f"{dom} phase ({args.math})", "achieved": achieved,
                 "peak": tf32_peak, "unit": "TFLOP/s", "frac": achieved / tf32_peak,
-                "traffic": None,
+                "traffic": profiled_traffic(dom) if args.config == 2 and args.math == "tf32"
+                else None,
                 "peak_source": f"{peak_src} bf16 {peaks['bf16_tflops']} x nominal tf32/bf16 "
                                f"1.1/2.25 (burst)"}
     red_gbs = red_bytes / (ph["reduce"] * 1e-3) / 1e9
