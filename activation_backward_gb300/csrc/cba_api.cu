@@ -110,18 +110,20 @@ int fail_cuda(cudaError_t e) {
     return CBA_ERR_CUDA;
 }
 
-// Makes the device that owns `stream` (or, for the NULL stream, the device
-// that holds `ptr`) current for this library's runtime, which keeps its own
-// per-thread current device.
+// Makes the device that holds `ptr` (the call's data; the stream must belong
+// to the same device) current for this library's runtime, which keeps its own
+// per-thread current device.  Without a pointer, the stream's device.  The
+// pointer query is also legal while the stream is being captured into a CUDA
+// graph, where asking the stream for its device is not.
 cudaError_t select_device(cudaStream_t stream, const void *ptr) {
     int dev = -1;
     cudaError_t e = cudaSuccess;
-    if (stream) {
-        e = cudaStreamGetDevice(stream, &dev);
-    } else if (ptr) {
+    if (ptr) {
         cudaPointerAttributes a;
         e = cudaPointerGetAttributes(&a, ptr);
         if (e == cudaSuccess) dev = a.device;
+    } else if (stream) {
+        e = cudaStreamGetDevice(stream, &dev);
     }
     if (e != cudaSuccess) return e;
     if (dev < 0) return cudaSuccess;

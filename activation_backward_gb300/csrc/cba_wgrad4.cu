@@ -55,7 +55,8 @@ struct W4Geom {
 };
 
 struct W4Args {
-    float *part;             // [grid][N][128] partial tiles
+    float *part;             // [tile][N][cpt][128] partial tiles (a tile's partials of one
+                             // column are contiguous for the reduction)
     unsigned *status;
     int S, Pe, pad, nwc, Wx;
     int bq_lo, bd_lo;
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[m % kW4NA]));
         }
-        // ---- epilogue: D[k][col] -> part[block][col][k] (coalesced over k)
+        // ---- epilogue: D[k][col] -> part[tile][col][split][k] (coalesced over k)
         if (has_work && ok)
             ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
                                         kW4LimitNs);
@@ -354,13 +355,14 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         ok = __all_sync(0xffffffffu, ok) && has_work;
         if (ok) {
             ptx::tc_fence_after();
-            float *dst = a.part + (size_t)blockIdx.x * a.N * 128 + kl;
+            float *dst = a.part + ((size_t)tile * a.N * a.cpt + split) * 128 + kl;
+            const size_t col_stride = (size_t)a.cpt * 128;
             for (int cc = g; cc * 16 < a.N; cc += 2) {
                 float v[16];
                 ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(cc * 16), v);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) dst[(size_t)(cc * 16 + e) * 128] = v[e];
+                for (int e = 0; e < 16; ++e) dst[(size_t)(cc * 16 + e) * col_stride] = v[e];
             }
         }
     }
@@ -374,7 +376,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 }
 
 // dW[k0 + kl][c0 + c][r][s] += sum over the tile's blocks b of
-// part[tile * cpt + b][r * cb + c][kl].  One block per (tile, column): warp w
+// part[tile][r * cb + c][b][kl].  One block per (tile, column): warp w
 // sums the blocks b = w, w + 8, ... for all 128 kl (a float4 per lane), then
 // warp 0 adds the eight warp sums in order (a fixed order: deterministic).
 __global__ void __launch_bounds__(256)
@@ -383,8 +385,9 @@ __global__ void __launch_bounds__(256)
     __shared__ float4 red[8][32];
     const int col = blockIdx.x % N, tile = blockIdx.x / N;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float4 *src = reinterpret_cast<const float4 *>(part + ((size_t)tile * cpt * N + col) * 128) + lane;
-    const size_t bstride = (size_t)N * 32;  // float4s between consecutive blocks
+    const float4 *src =
+        reinterpret_cast<const float4 *>(part + ((size_t)tile * N + col) * cpt * 128) + lane;
+    const size_t bstride = 32;  // float4s between consecutive blocks' partials
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
     for (int b = warp; b < cpt; b += 8) {

@@ -86,3 +86,23 @@ class DeviceLayer:
         """Host float64 copies of the outputs."""
         out = dict(dW=self.dW, db=self.db, dgamma=self.dgamma, prev_delta=self.prev, dz=self.dz)
         return {k: (None if v is None else v.double().cpu().numpy()) for k, v in out.items()}
+
+
+def capture_graph(fn, warmup=2):
+    """Capture `fn()` -- a sequence of library calls on the current stream,
+    e.g. ``layer.run`` -- into a CUDA graph and return it (replay it with
+    ``graph.replay()``).  The library calls only enqueue stream-ordered work
+    on caller-provided buffers, so a replay repeats them on the same buffers
+    without any host-side launch cost.  `fn` runs `warmup` times first,
+    outside the capture (the first call on a device sets up per-kernel
+    attributes)."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(warmup):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fn()
+    return graph

@@ -38,6 +38,9 @@
  * stream-ordered and asynchronous: they enqueue kernels on `stream` (a
  * cudaStream_t; NULL = the legacy default stream) and return without
  * synchronising.  Two calls that share a workspace must not overlap in time.
+ * cba_conv_bn_act_backward and its traced variant can be captured into a
+ * CUDA graph (stream capture) and replayed on the same buffers; make one call
+ * on the device before capturing (it sets per-kernel attributes).
  *
  * Errors: a negative return code; on any error nothing has been launched and
  * no output touched, except CBA_ERR_CUDA (a launch failed; the CUDA error is
