@@ -948,6 +948,252 @@ __global__ void __launch_bounds__(kD3Threads, 1)
     }
 }
 
+// Persistent input gradient: the CTA loops over work units (one 128-position
+// tile of one channel tile), with two TMEM accumulators so that the
+// epilogue of unit i runs while the MMAs of unit i + 1 do.  Per stage (kernel
+// row r, 32 output channels k): A = the dzc rows of the tile shifted by dp_r
+// (one TMA copy), B = the W slices of all the class's kernel columns (one
+// copy when they are consecutive).  Epilogue: each warp takes 16 channels of
+// its 32 positions, loads E[., (s, c)] for every kernel column s from TMEM,
+// shifts it down by dq_s lanes with warp shuffles (the lanes past the warp
+// come from the next warp through a small shared-memory halo), sums over s,
+// adds the residual (and the old value) and writes prev_delta.
+constexpr int kD4Stages = 4;
+constexpr int kD4Threads = 352;  // A TMA warp, MMA warp, 8 epilogue warps, W TMA warp
+
+struct D4Args {
+    Dg3Args g;
+    int ctiles;        // channel tiles
+    int total_units;   // total_tiles * ctiles
+    int nst;           // pipeline stages in use
+    int w_one;         // W slices of the class in one copy
+    uint32_t halo_off; // byte offset of the epilogue halo in shared memory
+};
+
+struct D4Bars {
+    uint64_t full[kD4Stages], empty[kD4Stages], acc_full[2], acc_empty[2], drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__global__ void __launch_bounds__(kD4Threads, 1)
+    dgrad_tc4_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmw,
+                     const __grid_constant__ CUtensorMap tmw1, const D4Args d) {
+    const Dg3Args &a = d.g;
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    __shared__ D4Bars sb;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tstride = 128 - a.span;
+    const int nstages = a.nr * a.kchunks;
+    const uint32_t b_bytes = (uint32_t)a.ncol * 128u;
+    const uint32_t stage_bytes = 16384u + b_bytes;
+    const int nunits = d.total_units > (int)blockIdx.x
+                           ? (d.total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
+                           : 0;
+
+    if (tid == 0) {
+        for (int i = 0; i < kD4Stages; ++i) {
+            ptx::mbar_init(ptx::smem_u32(&sb.full[i]), 2);  // the A and the W issuer
+            ptx::mbar_init(ptx::smem_u32(&sb.empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(ptx::smem_u32(&sb.acc_full[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sb.acc_empty[i]), 8);  // the 8 epilogue warps
+        }
+        ptx::mbar_init(ptx::smem_u32(&sb.drain), 1);
+        sb.abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&sb.tmem_base), a.ncols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sb.tmem_base;
+
+    if (warp == 0 || warp == 10) {
+        // ---- TMA: warp 0 the A tiles, warp 10 the W slices
+        if (lane == 0) {
+            const bool wside = warp == 10;
+            int gs = 0;  // global stage counter
+            bool ok = true;
+            for (int i = 0; ok && i < nunits; ++i) {
+                const int u = (int)blockIdx.x + i * (int)gridDim.x;
+                const int ct = u / a.total_tiles, tile = u - ct * a.total_tiles;
+                const int c0 = ct * a.c_tile;
+                const long long m0 = (long long)tile * tstride + a.min_dq;
+                for (int st = 0; st < nstages; ++st, ++gs) {
+                    const int slot = gs % d.nst;
+                    if (gs >= d.nst)
+                        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.empty[slot]),
+                                                    (uint32_t)(gs / d.nst - 1) & 1u,
+                                                    &sb.abort_flag, a.status, kLimitNs);
+                    if (!ok) break;
+                    const int ri = st / a.kchunks, kc = st - (st / a.kchunks) * a.kchunks;
+                    const uint32_t bar = ptx::smem_u32(&sb.full[slot]);
+                    uint8_t *sp = smem + (size_t)slot * stage_bytes;
+                    if (!wside) {
+                        ptx::mbar_arrive_expect_tx(bar, 16384u);
+                        ptx::tma_load_2d(ptx::smem_u32(sp), &tma, kc * 32,
+                                         (int)(m0 + (long long)a.dp[ri] * a.Qpp), bar);
+                    } else {
+                        ptx::mbar_arrive_expect_tx(bar, b_bytes);
+                        if (d.w_one)
+                            ptx::tma_load_4d(ptx::smem_u32(sp + 16384), &tmw, kc * 32, c0,
+                                             a.s_of[0], a.r_of[ri], bar);
+                        else
+                            for (int si = 0; si < a.ns; ++si)
+                                ptx::tma_load_4d(
+                                    ptx::smem_u32(sp + 16384 + (size_t)si * a.c_tile * 128), &tmw1,
+                                    kc * 32, c0, a.s_of[si], a.r_of[ri], bar);
+                    }
+                }
+            }
+            int no_abort = 0;
+            for (int i = max(0, gs - d.nst); i < gs; ++i)
+                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.full[i % d.nst]),
+                                       (uint32_t)(i / d.nst) & 1u, &no_abort, a.status, kLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issue: unit i into accumulator i & 1
+        if (lane == 0) {
+            const uint32_t idesc = ptx::idesc_tf32(128, a.ncol);
+            int gs = 0;
+            bool ok = true;
+            for (int i = 0; ok && i < nunits; ++i) {
+                const int b = i & 1;
+                if (i >= 2)
+                    ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.acc_empty[b]),
+                                                (uint32_t)((i >> 1) - 1) & 1u, &sb.abort_flag,
+                                                a.status, kLimitNs);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                const uint32_t dtm = tmem + (uint32_t)(b * a.ncol);
+                for (int st = 0; st < nstages; ++st, ++gs) {
+                    const int slot = gs % d.nst;
+                    ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.full[slot]),
+                                                (uint32_t)(gs / d.nst) & 1u, &sb.abort_flag,
+                                                a.status, kLimitNs);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    const uint32_t base = ptx::smem_u32(smem + (size_t)slot * stage_bytes);
+                    const uint64_t ad = ptx::smem_desc(base, 16, 1024, 2);
+                    const uint64_t bd = ptx::smem_desc(base + 16384, 16, 1024, 2);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        ptx::mma_tf32(dtm, ad + 2 * ks, bd + 2 * ks, idesc,
+                                      (st > 0 || ks > 0) ? 1u : 0u);
+                    ptx::mma_commit(ptx::smem_u32(&sb.empty[slot]));
+                }
+                if (!ok) break;
+                ptx::mma_commit(ptx::smem_u32(&sb.acc_full[b]));
+            }
+            if (!ok) {
+                *reinterpret_cast<volatile int *>(&sb.abort_flag) = 1;
+                __threadfence_block();
+            }
+            // drain: every MMA issued has finished before TMEM is released
+            ptx::mma_commit(ptx::smem_u32(&sb.drain));
+            int no_abort = 0;
+            ptx::mbar_wait_bounded(ptx::smem_u32(&sb.drain), 0, &no_abort, a.status, kLimitNs);
+        }
+    } else {
+        // ---- epilogue: group eg of 4 warps (one per TMEM lane quarter) takes
+        // the 16-channel chunks cc = eg, eg + 2, ... of the unit's channels
+        const int eg = (warp - 2) >> 2, wq = warp & 3;
+        const int L = wq * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        const long long HW = (long long)a.He * a.We;
+        const long long plane = (long long)a.Pp * a.Qpp;
+        const int span = a.span;
+        // halo[eg][wq][si][h][16]: lanes 0 .. span-1 of each warp, for the warp below
+        float *halo = reinterpret_cast<float *>(smem + d.halo_off);
+        int dqr[kD2MaxTaps];
+#pragma unroll
+        for (int si = 0; si < kD2MaxTaps; ++si) dqr[si] = a.dq[si] - a.min_dq;
+        bool ok = true;
+        for (int i = 0; ok && i < nunits; ++i) {
+            const int b = i & 1;
+            const int u = (int)blockIdx.x + i * (int)gridDim.x;
+            const int ct = u / a.total_tiles, tile = u - ct * a.total_tiles;
+            const int c0 = ct * a.c_tile;
+            const int cl_all = min(a.c_tile, a.C - c0);
+            // this lane's output pixel (padded position m = tile * tstride + L)
+            const long long m = (long long)tile * tstride + L;
+            bool out = L < tstride && m < a.total_pos;
+            long long pix = 0;
+            if (out) {
+                const int n = (int)(m / plane);
+                const int rem = (int)(m - (long long)n * plane);
+                const int ii = rem / a.Qpp - a.bd_lo, jj = rem % a.Qpp - a.bq_lo;
+                out = ii >= 0 && ii < a.Hc && jj >= 0 && jj < a.Wc;
+                pix = (long long)n * a.C * HW + (long long)(ii * a.stride + a.ph) * a.We +
+                      (jj * a.stride + a.pw);
+            }
+            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.acc_full[b]), (uint32_t)(i >> 1) & 1u,
+                                        &sb.abort_flag, a.status, kLimitNs);
+            // the group's 4 warps agree before the halo barriers below
+            ok = ptx::named_bar_and(1 + eg, 128, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            for (int cc = eg; cc * 16 < cl_all; cc += 2) {
+                float acc[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+                for (int si = 0; si < a.ns; ++si) {
+                    float v[16];
+                    ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(b * a.ncol + si * a.c_tile + cc * 16),
+                                   v);
+                    ptx::tmem_ld_wait();
+                    // publish lanes 0 .. span-1 for the warp below (positions L - 32 + ...)
+                    float *hw = halo + ((size_t)((eg * 4 + wq) * kD2MaxTaps + si) * 8) * 16;
+                    if (lane < span) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) hw[lane * 16 + e] = v[e];
+                    }
+                    ptx::named_bar_sync(1 + eg, 128);
+                    const int dsh = dqr[si];
+                    const float *hn = halo + ((size_t)((eg * 4 + ((wq + 1) & 3)) * kD2MaxTaps + si) * 8) * 16;
+                    const bool from_next = lane + dsh >= 32;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float sh = __shfl_down_sync(0xffffffffu, v[e], dsh);
+                        acc[e] += from_next ? hn[(lane + dsh - 32) * 16 + e] : sh;
+                    }
+                    ptx::named_bar_sync(1 + eg, 128);  // the halo is reused next
+                }
+                if (out) {
+                    const int nvalid = min(16, cl_all - cc * 16);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        if (e < nvalid) {
+                            const long long idx = pix + (long long)(c0 + cc * 16 + e) * HW;
+                            float o = acc[e];
+                            if (a.residual) o += a.residual[idx];
+                            if (a.accumulate) o += a.prev[idx];
+                            a.prev[idx] = o;
+                        }
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.acc_empty[b]));
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, a.ncols);
+    }
+}
+
 // -------------------------------------------------------------- host side
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -1331,6 +1577,36 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *Wt, const float *dzt,
         const uint64_t d[4] = {(uint64_t)Kw, (uint64_t)p.C, (uint64_t)p.S, (uint64_t)p.R};
         const uint32_t b[4] = {32, (uint32_t)a.c_tile, 1, 1};
         if (!encode_4d(&tmw, wr, d, b)) return cudaErrorInvalidValue;
+
+        // persistent, double-buffered kernel when the halo and two
+        // accumulators fit
+        if (a.span <= 8 && 2 * a.ncol <= 512) {
+            D4Args d4;
+            d4.g = a;
+            d4.ctiles = (p.C + a.c_tile - 1) / a.c_tile;
+            d4.total_units = a.total_tiles * d4.ctiles;
+            const size_t per_stage = 16384 + (size_t)a.ncol * 128;
+            const size_t halo_bytes = (size_t)2 * 4 * kD2MaxTaps * 8 * 16 * 4;
+            d4.nst = (int)std::min<size_t>(kD4Stages, (200 * 1024 - halo_bytes) / per_stage);
+            if (d4.nst >= 2) {
+                d4.halo_off = (uint32_t)(d4.nst * per_stage);
+                const size_t smem4 = d4.halo_off + halo_bytes + 1024;
+                d4.w_one = a.ns == 1 || p.stride == 1;
+                CUtensorMap tmwn;  // all the class's kernel columns in one box
+                const uint32_t bn[4] = {32, (uint32_t)a.c_tile,
+                                        (uint32_t)(d4.w_one ? std::max(1, a.ns) : 1), 1};
+                if (!encode_4d(&tmwn, wr, d, bn)) return cudaErrorInvalidValue;
+                cudaError_t e = cudaFuncSetAttribute(
+                    dgrad_tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem4);
+                if (e != cudaSuccess) return e;
+                const int grid4 = std::max(1, std::min(p.num_sms, d4.total_units));
+                dgrad_tc4_kernel<<<grid4, kD4Threads, smem4, st>>>(tma, tmwn, tmw, d4);
+                e = cudaGetLastError();
+                if (e != cudaSuccess) return e;
+                *launches += 1;
+                continue;
+            }
+        }
         const size_t pipe = (size_t)kD3Stages * (32768 + (size_t)a.ncol * 128);
         const size_t stage = (size_t)a.ncol * 128 * 4;  // epilogue staging
         const size_t smem = std::max(pipe, stage) + 1024;
