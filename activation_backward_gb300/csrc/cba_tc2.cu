@@ -951,15 +951,20 @@ __global__ void __launch_bounds__(kD3Threads, 1)
 // Persistent input gradient: the CTA loops over work units (one 128-position
 // tile of one channel tile), with two TMEM accumulators so that the
 // epilogue of unit i runs while the MMAs of unit i + 1 do.  Per stage (kernel
-// row r, 32 output channels k): A = the dzc rows of the tile shifted by dp_r
-// (one TMA copy), B = the W slices of all the class's kernel columns (one
-// copy when they are consecutive).  Epilogue: each warp takes 16 channels of
-// its 32 positions, loads E[., (s, c)] for every kernel column s from TMEM,
-// shifts it down by dq_s lanes with warp shuffles (the lanes past the warp
-// come from the next warp through a small shared-memory halo), sums over s,
-// adds the residual (and the old value) and writes prev_delta.
-constexpr int kD4Stages = 4;
+// row r, kpb chunks of 32 output channels k): A = the dzc rows of the tile
+// shifted by dp_r, B = the W slices of all the class's kernel columns; each
+// is one TMA copy when the chunks and slices are consecutive (a copy costs
+// the issuing SM a fixed time whatever its size, so few large copies keep
+// the tensor pipe fed).  Epilogue: each warp takes 16 channels of its 32
+// positions, loads E[., (s, c)] for its kernel columns s from TMEM, shifts it
+// down by dq_s lanes with warp shuffles (the lanes past the warp come from
+// the next warp through a small shared-memory halo, double-buffered so that
+// one barrier per chunk suffices), sums over s, adds the residual (and the
+// old value) and writes prev_delta.
+constexpr int kD4Stages = 6;
 constexpr int kD4Threads = 352;  // A TMA warp, MMA warp, 8 epilogue warps, W TMA warp
+constexpr int kD4Slots = 6;      // TMEM loads (16 columns each) one epilogue warp has in flight
+constexpr int kD4HaloLanes = 4;  // lanes a warp passes to the warp below (the class's column span)
 
 struct D4Args {
     Dg3Args g;
@@ -967,6 +972,8 @@ struct D4Args {
     int total_units;   // total_tiles * ctiles
     int nst;           // pipeline stages in use
     int w_one;         // W slices of the class in one copy
+    int kpb;           // 32-channel chunks of k per stage (1, or 2 with 3-D / 5-D copies)
+    int kst;           // stages per kernel row: ceil(kchunks / kpb)
     uint32_t halo_off; // byte offset of the epilogue halo in shared memory
 };
 
@@ -975,6 +982,110 @@ struct D4Bars {
     uint32_t tmem_base;
     int abort_flag;
 };
+
+// One epilogue batch of dgrad_tc4 for a warp: NB chunks of 16 channels (the
+// group's chunks t0 .. t0 + NB - 1) times the NS kernel columns of the class,
+// all TMEM loads in flight together.  Publishes lanes 0 .. span-1 of every
+// slot to the halo, meets the group at a barrier, shifts every column down by
+// its dq with warp shuffles (the top lanes from the next warp's halo), sums
+// the columns and writes the NB chunks.  `release` arrives on the unit's
+// accumulator-empty barrier right after the loads.
+struct D4Epi {
+    uint32_t tbase;       // TMEM address of this warp's lanes in the unit's accumulator
+    int c_tile, eg, wq, lane, span;
+    const int *dqr;
+    float *hpar;          // this batch's halo parity
+    long long pix, HW;
+    int c0, cl_all;
+    bool out;
+    const float *residual;
+    float *prev;
+    int accumulate;
+};
+
+template <int NS, int NB>
+__device__ __forceinline__ void d4_epilogue_batch(const D4Epi &E, int t0, uint64_t *release) {
+    constexpr int NV = NS * NB;
+    constexpr size_t kHSlot = (size_t)16 * kD4HaloLanes;
+    float v[NV][16];
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+        const int cc = E.eg + 2 * (t0 + q / NS);
+        ptx::tmem_ld16(E.tbase + (uint32_t)((q % NS) * E.c_tile + cc * 16), v[q]);
+    }
+    ptx::tmem_ld_wait();
+    if (release) {
+        // the unit's last loads are done: the MMAs may reuse the buffer
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (E.lane == 0) ptx::mbar_arrive(ptx::smem_u32(release));
+    }
+    if (E.lane < E.span) {
+        // value-major ([e][lane]) so that the reads below touch distinct banks
+        float *hw = E.hpar + (size_t)(E.eg * 4 + E.wq) * kD4Slots * kHSlot;
+#pragma unroll
+        for (int q = 0; q < NV; ++q)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) hw[q * kHSlot + e * kD4HaloLanes + E.lane] = v[q][e];
+    }
+    ptx::named_bar_sync(1 + E.eg, 128);
+    const float *hn = E.hpar + (size_t)(E.eg * 4 + ((E.wq + 1) & 3)) * kD4Slots * kHSlot;
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+        const int dsh = E.dqr[q % NS];
+        if (dsh != 0) {  // warp-uniform
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[q][e] = __shfl_down_sync(0xffffffffu, v[q][e], dsh);
+            // the top dsh lanes take the next warp's lanes 0 .. dsh-1
+            if (E.lane + dsh >= 32) {
+                const int hl = E.lane + dsh - 32;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[q][e] = hn[q * kHSlot + e * kD4HaloLanes + hl];
+            }
+        }
+        if (q % NS != 0) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[q - q % NS][e] += v[q][e];
+        }
+    }
+    if (E.out) {
+#pragma unroll
+        for (int t = 0; t < NB; ++t) {
+            const int cc = E.eg + 2 * (t0 + t);
+            const int nvalid = min(16, E.cl_all - cc * 16);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                if (e < nvalid) {
+                    const long long idx = E.pix + (long long)(E.c0 + cc * 16 + e) * E.HW;
+                    float o = v[t * NS][e];
+                    if (E.residual) o += E.residual[idx];
+                    if (E.accumulate) o += E.prev[idx];
+                    E.prev[idx] = o;
+                }
+            }
+        }
+    }
+}
+
+// A batch of nb (1 .. kD4Slots / NS) chunks; nb = 0 only releases.
+template <int NS>
+__device__ __forceinline__ void d4_epilogue_nb(const D4Epi &E, int t0, int nb, uint64_t *release) {
+    constexpr int BCH = kD4Slots / NS;
+    if (nb <= 0) {
+        if (release) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (E.lane == 0) ptx::mbar_arrive(ptx::smem_u32(release));
+        }
+        return;
+    }
+    if constexpr (BCH >= 6) { if (nb == 6) { d4_epilogue_batch<NS, 6>(E, t0, release); return; } }
+    if constexpr (BCH >= 5) { if (nb == 5) { d4_epilogue_batch<NS, 5>(E, t0, release); return; } }
+    if constexpr (BCH >= 4) { if (nb == 4) { d4_epilogue_batch<NS, 4>(E, t0, release); return; } }
+    if constexpr (BCH >= 3) { if (nb == 3) { d4_epilogue_batch<NS, 3>(E, t0, release); return; } }
+    if constexpr (BCH >= 2) { if (nb == 2) { d4_epilogue_batch<NS, 2>(E, t0, release); return; } }
+    d4_epilogue_batch<NS, 1>(E, t0, release);
+}
 
 __global__ void __launch_bounds__(kD4Threads, 1)
     dgrad_tc4_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmw,
@@ -986,9 +1097,11 @@ __global__ void __launch_bounds__(kD4Threads, 1)
     __shared__ D4Bars sb;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tstride = 128 - a.span;
-    const int nstages = a.nr * a.kchunks;
-    const uint32_t b_bytes = (uint32_t)a.ncol * 128u;
-    const uint32_t stage_bytes = 16384u + b_bytes;
+    const int nstages = a.nr * d.kst;
+    const uint32_t a_bytes = (uint32_t)d.kpb * 16384u;
+    const uint32_t b_chunk = (uint32_t)a.ncol * 128u;  // one k-chunk of the W slices
+    const uint32_t b_bytes = (uint32_t)d.kpb * b_chunk;
+    const uint32_t stage_bytes = a_bytes + b_bytes;
     const int nunits = d.total_units > (int)blockIdx.x
                            ? (d.total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
                            : 0;
@@ -1033,23 +1146,29 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                                                     (uint32_t)(gs / d.nst - 1) & 1u,
                                                     &sb.abort_flag, a.status, kLimitNs);
                     if (!ok) break;
-                    const int ri = st / a.kchunks, kc = st - (st / a.kchunks) * a.kchunks;
+                    const int ri = st / d.kst, kc = (st - ri * d.kst) * d.kpb;
                     const uint32_t bar = ptx::smem_u32(&sb.full[slot]);
                     uint8_t *sp = smem + (size_t)slot * stage_bytes;
+                    const int row = (int)(m0 + (long long)a.dp[ri] * a.Qpp);
                     if (!wside) {
-                        ptx::mbar_arrive_expect_tx(bar, 16384u);
-                        ptx::tma_load_2d(ptx::smem_u32(sp), &tma, kc * 32,
-                                         (int)(m0 + (long long)a.dp[ri] * a.Qpp), bar);
+                        ptx::mbar_arrive_expect_tx(bar, a_bytes);
+                        if (d.kpb == 1)
+                            ptx::tma_load_2d(ptx::smem_u32(sp), &tma, kc * 32, row, bar);
+                        else
+                            ptx::tma_load_3d(ptx::smem_u32(sp), &tma, 0, row, kc, bar);
                     } else {
                         ptx::mbar_arrive_expect_tx(bar, b_bytes);
-                        if (d.w_one)
-                            ptx::tma_load_4d(ptx::smem_u32(sp + 16384), &tmw, kc * 32, c0,
+                        if (d.kpb > 1)
+                            ptx::tma_load_5d(ptx::smem_u32(sp + a_bytes), &tmw, 0, c0, a.s_of[0],
+                                             kc, a.r_of[ri], bar);
+                        else if (d.w_one)
+                            ptx::tma_load_4d(ptx::smem_u32(sp + a_bytes), &tmw, kc * 32, c0,
                                              a.s_of[0], a.r_of[ri], bar);
                         else
                             for (int si = 0; si < a.ns; ++si)
                                 ptx::tma_load_4d(
-                                    ptx::smem_u32(sp + 16384 + (size_t)si * a.c_tile * 128), &tmw1,
-                                    kc * 32, c0, a.s_of[si], a.r_of[ri], bar);
+                                    ptx::smem_u32(sp + a_bytes + (size_t)si * a.c_tile * 128),
+                                    &tmw1, kc * 32, c0, a.s_of[si], a.r_of[ri], bar);
                     }
                 }
             }
@@ -1081,12 +1200,17 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                     if (!ok) break;
                     ptx::tc_fence_after();
                     const uint32_t base = ptx::smem_u32(smem + (size_t)slot * stage_bytes);
-                    const uint64_t ad = ptx::smem_desc(base, 16, 1024, 2);
-                    const uint64_t bd = ptx::smem_desc(base + 16384, 16, 1024, 2);
+                    const uint64_t ad0 = ptx::smem_desc(base, 16, 1024, 2);
+                    const uint64_t bd0 = ptx::smem_desc(base + a_bytes, 16, 1024, 2);
+                    for (int j = 0; j < d.kpb; ++j) {
+                        // descriptor start addresses count 16-byte units
+                        const uint64_t ad = ad0 + (uint64_t)(j * (16384 >> 4));
+                        const uint64_t bd = bd0 + (uint64_t)(j * (b_chunk >> 4));
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        ptx::mma_tf32(dtm, ad + 2 * ks, bd + 2 * ks, idesc,
-                                      (st > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < 4; ++ks)
+                            ptx::mma_tf32(dtm, ad + 2 * ks, bd + 2 * ks, idesc,
+                                          (st > 0 || j > 0 || ks > 0) ? 1u : 0u);
+                    }
                     ptx::mma_commit(ptx::smem_u32(&sb.empty[slot]));
                 }
                 if (!ok) break;
@@ -1103,18 +1227,25 @@ __global__ void __launch_bounds__(kD4Threads, 1)
         }
     } else {
         // ---- epilogue: group eg of 4 warps (one per TMEM lane quarter) takes
-        // the 16-channel chunks cc = eg, eg + 2, ... of the unit's channels
+        // the 16-channel chunks cc = eg, eg + 2, ... of the unit's channels,
+        // a batch of whole chunks at a time: every TMEM load of the batch is in
+        // flight together, the accumulator is released after the unit's last
+        // loads, and one barrier per batch publishes the halo.
         const int eg = (warp - 2) >> 2, wq = warp & 3;
         const int L = wq * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
         const long long HW = (long long)a.He * a.We;
         const long long plane = (long long)a.Pp * a.Qpp;
-        const int span = a.span;
-        // halo[eg][wq][si][h][16]: lanes 0 .. span-1 of each warp, for the warp below
+        const int span = a.span, ns = a.ns;
+        // halo[par][eg][wq][slot][16][4]: lanes 0 .. span-1 (span <= 4) of each
+        // warp, for the warp below; par alternates with the group's batches
         float *halo = reinterpret_cast<float *>(smem + d.halo_off);
+        constexpr size_t kHSlot = (size_t)16 * kD4HaloLanes;
         int dqr[kD2MaxTaps];
 #pragma unroll
         for (int si = 0; si < kD2MaxTaps; ++si) dqr[si] = a.dq[si] - a.min_dq;
+        const int bch = ns > 0 ? max(1, kD4Slots / ns) : 1;  // chunks per batch
+        int par = 0;
         bool ok = true;
         for (int i = 0; ok && i < nunits; ++i) {
             const int b = i & 1;
@@ -1122,6 +1253,7 @@ __global__ void __launch_bounds__(kD4Threads, 1)
             const int ct = u / a.total_tiles, tile = u - ct * a.total_tiles;
             const int c0 = ct * a.c_tile;
             const int cl_all = min(a.c_tile, a.C - c0);
+            const int gch = ((cl_all + 15) / 16 - eg + 1) / 2;  // this group's chunks
             // this lane's output pixel (padded position m = tile * tstride + L)
             const long long m = (long long)tile * tstride + L;
             bool out = L < tstride && m < a.total_pos;
@@ -1140,49 +1272,40 @@ __global__ void __launch_bounds__(kD4Threads, 1)
             ok = ptx::named_bar_and(1 + eg, 128, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            for (int cc = eg; cc * 16 < cl_all; cc += 2) {
-                float acc[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-                for (int si = 0; si < a.ns; ++si) {
-                    float v[16];
-                    ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(b * a.ncol + si * a.c_tile + cc * 16),
-                                   v);
-                    ptx::tmem_ld_wait();
-                    // publish lanes 0 .. span-1 for the warp below (positions L - 32 + ...)
-                    float *hw = halo + ((size_t)((eg * 4 + wq) * kD2MaxTaps + si) * 8) * 16;
-                    if (lane < span) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) hw[lane * 16 + e] = v[e];
-                    }
-                    ptx::named_bar_sync(1 + eg, 128);
-                    const int dsh = dqr[si];
-                    const float *hn = halo + ((size_t)((eg * 4 + ((wq + 1) & 3)) * kD2MaxTaps + si) * 8) * 16;
-                    const bool from_next = lane + dsh >= 32;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float sh = __shfl_down_sync(0xffffffffu, v[e], dsh);
-                        acc[e] += from_next ? hn[(lane + dsh - 32) * 16 + e] : sh;
-                    }
-                    ptx::named_bar_sync(1 + eg, 128);  // the halo is reused next
-                }
-                if (out) {
-                    const int nvalid = min(16, cl_all - cc * 16);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        if (e < nvalid) {
+            D4Epi E;
+            E.tbase = tmem + lane_addr + (uint32_t)(b * a.ncol);
+            E.c_tile = a.c_tile; E.eg = eg; E.wq = wq; E.lane = lane; E.span = span;
+            E.dqr = dqr; E.pix = pix; E.HW = HW; E.c0 = c0; E.cl_all = cl_all; E.out = out;
+            E.residual = a.residual; E.prev = a.prev; E.accumulate = a.accumulate;
+            int t0 = 0;
+            do {  // at least once, so that the accumulator is always released
+                const int nb = min(bch, gch - t0);
+                uint64_t *rel = t0 + bch >= gch ? &sb.acc_empty[b] : nullptr;
+                E.hpar = halo + (size_t)par * 8 * kD4Slots * kHSlot;
+                switch (ns) {
+                case 1: d4_epilogue_nb<1>(E, t0, nb, rel); break;
+                case 2: d4_epilogue_nb<2>(E, t0, nb, rel); break;
+                case 3: d4_epilogue_nb<3>(E, t0, nb, rel); break;
+                case 4: d4_epilogue_nb<4>(E, t0, nb, rel); break;
+                case 5: d4_epilogue_nb<5>(E, t0, nb, rel); break;
+                case 6: d4_epilogue_nb<6>(E, t0, nb, rel); break;
+                default:  // no kernel tap reaches this class: the gradient is 0
+                    d4_epilogue_nb<1>(E, t0, 0, rel);
+                    for (int t = t0; out && t < t0 + nb; ++t) {
+                        const int cc = eg + 2 * t;
+                        for (int e = 0; e < 16 && cc * 16 + e < cl_all; ++e) {
                             const long long idx = pix + (long long)(c0 + cc * 16 + e) * HW;
-                            float o = acc[e];
+                            float o = 0.f;
                             if (a.residual) o += a.residual[idx];
                             if (a.accumulate) o += a.prev[idx];
                             a.prev[idx] = o;
                         }
                     }
+                    break;
                 }
-            }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.acc_empty[b]));
+                t0 += bch;
+                par ^= 1;
+            } while (t0 < gch);
         }
     }
     ptx::tc_fence_before();
@@ -1580,27 +1703,65 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *Wt, const float *dzt,
 
         // persistent, double-buffered kernel when the halo and two
         // accumulators fit
-        if (a.span <= 8 && 2 * a.ncol <= 512) {
+        if (a.span <= kD4HaloLanes && a.ns <= kD4Slots && 2 * a.ncol <= 512) {
             D4Args d4;
             d4.g = a;
             d4.ctiles = (p.C + a.c_tile - 1) / a.c_tile;
             d4.total_units = a.total_tiles * d4.ctiles;
-            const size_t per_stage = 16384 + (size_t)a.ncol * 128;
-            const size_t halo_bytes = (size_t)2 * 4 * kD2MaxTaps * 8 * 16 * 4;
-            d4.nst = (int)std::min<size_t>(kD4Stages, (200 * 1024 - halo_bytes) / per_stage);
+            d4.w_one = a.ns == 1 || p.stride == 1;
+            const size_t halo_bytes = (size_t)2 * 8 * kD4Slots * kD4HaloLanes * 16 * 4;
+            const size_t cap = 232448 - 2048;  // dynamic shared memory, room for the static part
+            CUtensorMap tma4 = tma, tmw4;
+            // Two k-chunks per stage in one A copy (3-D view: chunk, position,
+            // channel in chunk) and one W copy (5-D view: r, chunk, s, c, k)
+            // when the channel pitch is whole chunks and the slices are
+            // adjacent: half the copies of one chunk per stage, which measured
+            // faster at equal bytes in flight.
+            d4.kpb = 1;
+            if (Kw % 32 == 0 && g.Kp % 32 == 0 && a.kchunks >= 2 && d4.w_one) {
+                const size_t ps2 = 2 * (16384 + (size_t)a.ncol * 128);
+                if (2 * ps2 + halo_bytes + 1024 <= cap) {
+                    EncodeTiledFn fn = encode_fn();
+                    cuuint64_t ad[3] = {32, (cuuint64_t)total_pos, (cuuint64_t)(g.Kp / 32)};
+                    cuuint64_t as[2] = {(cuuint64_t)g.Kp * 4, 128};
+                    cuuint32_t ab[3] = {32, 128, 2}, es[5] = {1, 1, 1, 1, 1};
+                    cuuint64_t wd[5] = {32, (cuuint64_t)p.C, (cuuint64_t)p.S, (cuuint64_t)(Kw / 32),
+                                        (cuuint64_t)p.R};
+                    cuuint64_t ws5[4] = {(cuuint64_t)Kw * 4, (cuuint64_t)p.C * Kw * 4, 128,
+                                         (cuuint64_t)p.S * p.C * Kw * 4};
+                    cuuint32_t wb[5] = {32, (cuuint32_t)a.c_tile, (cuuint32_t)std::max(1, a.ns), 2, 1};
+                    CUtensorMap t3, t5;
+                    if (fn(&t3, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(dzc), ad, as,
+                           ab, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+                        fn(&t5, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 5, wr, wd, ws5, wb, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+                        d4.kpb = 2;
+                        tma4 = t3;
+                        tmw4 = t5;
+                    }
+                }
+            }
+            d4.kst = (a.kchunks + d4.kpb - 1) / d4.kpb;
+            const size_t per_stage = (size_t)d4.kpb * (16384 + (size_t)a.ncol * 128);
+            d4.nst = (int)std::min<size_t>(kD4Stages, (cap - halo_bytes - 1024) / per_stage);
             if (d4.nst >= 2) {
                 d4.halo_off = (uint32_t)(d4.nst * per_stage);
                 const size_t smem4 = d4.halo_off + halo_bytes + 1024;
-                d4.w_one = a.ns == 1 || p.stride == 1;
-                CUtensorMap tmwn;  // all the class's kernel columns in one box
-                const uint32_t bn[4] = {32, (uint32_t)a.c_tile,
-                                        (uint32_t)(d4.w_one ? std::max(1, a.ns) : 1), 1};
-                if (!encode_4d(&tmwn, wr, d, bn)) return cudaErrorInvalidValue;
+                if (d4.kpb == 1) {
+                    // all the class's kernel columns in one box
+                    const uint32_t bn[4] = {32, (uint32_t)a.c_tile,
+                                            (uint32_t)(d4.w_one ? std::max(1, a.ns) : 1), 1};
+                    if (!encode_4d(&tmw4, wr, d, bn)) return cudaErrorInvalidValue;
+                }
                 cudaError_t e = cudaFuncSetAttribute(
                     dgrad_tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem4);
                 if (e != cudaSuccess) return e;
                 const int grid4 = std::max(1, std::min(p.num_sms, d4.total_units));
-                dgrad_tc4_kernel<<<grid4, kD4Threads, smem4, st>>>(tma, tmwn, tmw, d4);
+                dgrad_tc4_kernel<<<grid4, kD4Threads, smem4, st>>>(tma4, tmw4, tmw, d4);
                 e = cudaGetLastError();
                 if (e != cudaSuccess) return e;
                 *launches += 1;
