@@ -21,6 +21,23 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 }  // namespace
 
+void plan_reduction(Plan *p, long long max_parts) {
+    const long long target = (long long)p->num_sms * 7 / 2;
+    const long long pa = p->PQ % 4 == 0 ? p->PQ / 4 : p->PQ;  // accesses per plane
+    long long groups = std::max(1LL, std::min<long long>(p->N, ceil_div(target, p->K)));
+    groups = std::min(groups, std::max(1LL, max_parts));
+    long long pln = ceil_div(p->N, groups);
+    groups = ceil_div(p->N, pln);
+    long long pieces = 1;
+    if (groups * p->K * 2 < target) {  // too few planes: slice them as well
+        pieces = std::min(ceil_div(target, groups * p->K), std::max(1LL, pa / 256));
+        pieces = std::max(1LL, std::min(pieces, max_parts / groups));
+    }
+    p->red_pln = (int)pln;
+    p->red_groups = (int)groups;
+    p->red_pieces = (int)pieces;
+}
+
 int make_plan(const cba_desc_t *d, Plan *p) {
     if (!d || !p) return CBA_ERR_ARG;
     std::memset(p, 0, sizeof(*p));
@@ -51,11 +68,7 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->math = d->math; p->eps = d->eps;
     p->num_sms = kNumSMs;
 
-    // reduction pass: about 2.5 blocks of 256 threads per SM in total (each
-    // keeps ~48 KB of loads in flight), at least ~8k elements per block
-    long long want = ceil_div((long long)p->num_sms * 5 / 2, p->K);
-    long long cap = std::max(1LL, p->m / 8192);
-    p->red_splits = (int)std::max(1LL, std::min(want, cap));
+    plan_reduction(p, 1LL << 30);
 
     // SIMT wgrad: split the reduction so that ~4 blocks per SM exist
     const long long tiles = ceil_div(p->K, 64) * ceil_div(p->CRS, 64);
@@ -77,7 +90,7 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     off = align_up(off + sizeof(unsigned) * (size_t)p->K, 256);
     p->clear_bytes = off;
     p->off_red = off;
-    off = align_up(off + sizeof(double) * 2 * (size_t)p->red_splits * p->K, 256);
+    off = align_up(off + sizeof(float) * 2 * (size_t)p->red_groups * p->red_pieces * p->K, 256);
     p->off_coef = off;
     off = align_up(off + sizeof(Coef) * (size_t)p->K, 256);
     p->off_wgpart = off;
@@ -186,8 +199,13 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     if (e != cudaSuccess) return fail_cuda(e);
     e = cudaMemsetAsync(workspace, 0, p.clear_bytes, st);  // status word, reduction counters
     if (e == cudaSuccess) e = tr.mark(0);
-    if (e == cudaSuccess) e = launch_reduce(p, delta, output, z, gamma, mean, var, db, dgamma,
-                                            workspace, st, &n_launch);
+    // the tensor-core input gradient reads repacked weights: written by extra
+    // blocks of the reduction pass
+    const bool repack = p.use_tc2 && prev_delta != nullptr;
+    if (e == cudaSuccess)
+        e = launch_reduce(p, delta, output, z, gamma, mean, var, db, dgamma, workspace, st,
+                          &n_launch, repack ? Wt : nullptr,
+                          repack ? ws_at<float>(workspace, p.off_wr) : nullptr);
     if (e == cudaSuccess && dz_out) {
         e = launch_dz_out(p, delta, output, z, workspace, dz_out, st);
         ++n_launch;
@@ -207,7 +225,7 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
                    : launch_wgrad_tc2(p, x, dzt, dW, workspace, st, &n_launch);
         if (e == cudaSuccess) e = tr.mark(2);
         if (e == cudaSuccess && prev_delta)
-            e = launch_dgrad_tc2(p, Wt, dzt, residual, prev_delta, workspace,
+            e = launch_dgrad_tc2(p, dzt, residual, prev_delta, workspace,
                                  ws_at<float>(workspace, p.off_wr), st, &n_launch);
         if (e == cudaSuccess) e = tr.mark(3);
         if (launches) *launches = n_launch;

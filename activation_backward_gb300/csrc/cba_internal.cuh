@@ -32,8 +32,10 @@ struct Plan {
     int act, bn, accumulate, math;
     float eps;
     int num_sms;
-    // reduction pass
-    int red_splits;  // reduction blocks (and partials) per channel
+    // reduction pass: a block sums red_pln whole (n, k) planes of one channel,
+    // or one of red_pieces slices of each of them; red_groups = ceil(N /
+    // red_pln); groups * pieces partials per channel
+    int red_pln, red_groups, red_pieces;
     // SIMT wgrad split-K
     int wg_splits;
     long long wg_chunk;  // reduction positions per split (multiple of the K tile)
@@ -52,11 +54,17 @@ struct Plan {
 
 // Builds the plan; returns CBA_OK or a CBA_ERR_* code.
 int make_plan(const cba_desc_t *d, Plan *p);
+// The reduction pass's block shape (red_pln, red_groups, red_pieces): about
+// 3.5 blocks per SM, at most max_parts partials per channel.
+void plan_reduction(Plan *p, long long max_parts);
 
 // ---- launchers (each returns cudaSuccess or the launch error) ----
+// The reduction pass; with repack_W and repack_wr it also writes the input
+// gradient's repacked weights (wr[r][s][c][Kw], TF32-rounded) in extra blocks.
 cudaError_t launch_reduce(const Plan &p, const float *delta, const float *output, const float *z,
                           const float *gamma, const float *mean, const float *var, float *db,
-                          float *dgamma, void *ws, cudaStream_t st, int *launches);
+                          float *dgamma, void *ws, cudaStream_t st, int *launches,
+                          const float *repack_W = nullptr, float *repack_wr = nullptr);
 cudaError_t launch_dz_out(const Plan &p, const float *delta, const float *output, const float *z,
                           const void *ws, float *dz_out, cudaStream_t st);
 cudaError_t launch_wgrad_simt(const Plan &p, const float *x, const float *delta,
@@ -106,9 +114,9 @@ cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, fl
                              void *ws, cudaStream_t st, int *launches);
 cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, float *dW,
                              void *ws, cudaStream_t st, int *launches);
-cudaError_t launch_dgrad_tc2(const Plan &p, const float *Wt, const float *dzt,
-                             const float *residual, float *prev, void *ws, float *wr,
-                             cudaStream_t st, int *launches);
+// wr must already hold the repacked weights (launch_reduce writes them).
+cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzt, const float *residual, float *prev,
+                             void *ws, const float *wr, cudaStream_t st, int *launches);
 
 template <typename T>
 inline T *ws_at(void *ws, size_t off) {

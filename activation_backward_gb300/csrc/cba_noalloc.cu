@@ -110,13 +110,13 @@ extern "C" int cba_bn_act_backward_noalloc(const cba_desc_t *d, const float *out
     if (p.K > CBA_NOALLOC_MAX_K) return CBA_ERR_SCRATCH_LIMIT;
 
     // scratch layout: arrival counters [K] at 0, coefficients [K], then the
-    // partials [splits][K]
+    // partials [groups * pieces][K]
     const size_t cnt_bytes = align256(sizeof(unsigned) * (size_t)p.K);
     const size_t coef_bytes = align256(sizeof(Coef) * (size_t)p.K);
-    const size_t part_unit = sizeof(double) * 2 * (size_t)p.K;  // one split
+    const size_t part_unit = sizeof(float) * 2 * (size_t)p.K;  // one partial per channel
     const long long fit = (long long)((kScratchBytes - cnt_bytes - coef_bytes) / part_unit);
     if (fit < 1) return CBA_ERR_SCRATCH_LIMIT;  // unreachable with K <= CBA_NOALLOC_MAX_K
-    p.red_splits = (int)std::min<long long>(p.red_splits, fit);
+    plan_reduction(&p, fit);
     p.off_cnt = 0;
     p.off_coef = cnt_bytes;
     p.off_red = cnt_bytes + coef_bytes;

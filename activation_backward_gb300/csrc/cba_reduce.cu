@@ -1,24 +1,18 @@
-// cba_reduce.cu -- the per-channel reduction pass of the BN / bias backward.
+// One kernel.  A block sums one piece of one channel: a group of whole
+// (n, k) planes, or, when there are too few plane groups to fill the GPU, one
+// slice of each plane of the group.  Loads are 16-byte vectors when P*Q is a
+// multiple of 4, three per tensor in flight per thread; sums in fp32 per
+// thread, warp shuffles, fp32 across warps (a few thousand terms per block),
+// one float2 partial per block.  The block that finishes a channel's last
+// piece (counted in cnt[k], acquire-release, which it resets) adds the
+// partials in a fixed order in fp64 and finalises the channel in fp32 (fp64
+// division and square root are slow on this part, and the coefficients are
+// fp32 anyway).  Deterministic.  The per-channel arrival counters must be
+// zero when the kernel starts.
 //
-// One read sweep over delta (and output for leaky, z for BN) produces, per
-// output channel k,
-//   S1_k = sum_{n,p,q} delta'          (bias_updates, backward_bias)
-//   S2_k = sum_{n,p,q} delta' * x_norm (scale_updates, backward_scale_cpu)
-// with delta' = delta * f'(output) and x_norm = (z - mean)/sqrt(var + eps)
-// ("YOLOv3反向传播原理 之 全流程源码分析" §3.1, §4).  These two sums are the
-// only reductions the BN backward needs: mean_delta, variance_delta and
-// normalize_delta collapse into the per-channel affine map
-//   dz = a*delta' + b + c*(z - mean),  a = gamma/sigma, b = -a*S1/m,
-//   c = -a*S2/(m*sigma),  sigma = sqrt(var + eps),  m = N*P*Q,
-// which the finalize kernel computes once per channel for the GEMMs.
-//
-// One kernel, a few blocks per channel: each block sums a contiguous slice of
-// its channel with 16-byte vector loads when P*Q is a multiple of 4 (many in
-// flight), fp32 per thread, warp shuffles, fp64 across warps, one fp64
-// partial pair per block.  The last block of a channel adds the partials in a
-// fixed order (fp64), updates db / dgamma and writes the coefficients.
-// Deterministic.  The per-channel arrival counters must be zero when the
-// kernel starts; the last block of each channel resets its own.
+// Blocks past the reduction's own may carry an independent job: the input
+// gradient's weight repack (W[k][c][r][s] -> wr[r][s][c][k], TF32-rounded,
+// k padded to Kw with zeros), which would otherwise be a launch of its own.
 #include "cba_internal.cuh"
 
 namespace cba {
@@ -26,6 +20,7 @@ namespace cba {
 namespace {
 
 constexpr int kRedThreads = 256;
+constexpr int kRedU = 3;  // vector loads per tensor per thread in flight
 
 template <int ACT, bool BN>
 __device__ __forceinline__ void acc1(float d, float y, float zv, float mu, float rs, float &s1,
@@ -33,6 +28,15 @@ __device__ __forceinline__ void acc1(float d, float y, float zv, float mu, float
     float dp = d * act_grad<ACT>(y);
     s1 += dp;
     if constexpr (BN) s2 = fmaf(dp, (zv - mu) * rs, s2);
+}
+
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
 }
 
 // Per-channel finalisation from the S1, S2 totals: db += S1, dgamma += S2 and
@@ -48,11 +52,12 @@ __device__ __forceinline__ void finalize_channel(int k, double S1, double S2, lo
     Coef cf;
     if (bn) {
         dgamma[k] = (float)((double)dgamma[k] + S2);
-        const double sd = sqrt((double)var[k] + (double)eps);
-        const double a = (double)gamma[k] / sd;
-        cf.a = (float)a;
-        cf.b = (float)(-a * S1 / (double)m);
-        cf.c = (float)(-a * S2 / ((double)m * sd));
+        const float sd = sqrtf(var[k] + eps);
+        const float a = gamma[k] / sd;
+        const float s1m = (float)(S1 / (double)m), s2m = (float)(S2 / (double)m);
+        cf.a = a;
+        cf.b = -a * s1m;
+        cf.c = -a * s2m / sd;
         cf.mu = mean[k];
     } else {
         cf.a = 1.f;
@@ -63,89 +68,102 @@ __device__ __forceinline__ void finalize_channel(int k, double S1, double S2, lo
     coef[k] = cf;
 }
 
-// One block reduces slot j of channel k: the contiguous range j * L .. (j+1)
-// * L - 1 of the channel's m elements in (n, p, q) order (L = m / splits,
-// taken in 16-byte quads when P*Q is a multiple of 4; the range crosses the
-// per-image planes, each quad's address is computed on its own).  Few blocks
-// (a couple per SM), each looping over its range: per iteration every thread
-// issues U loads per tensor back to back (addresses clamped into the range,
-// values past its end zeroed), so enough bytes stay in flight to keep HBM
-// busy.  Sums in fp32 per thread, warp shuffles, fp64 across warps.  The fp64
-// partial pair goes to part[j][k]; the block that finishes a channel's last
-// slot (counted in cnt[k], which it resets) adds the partials in order j = 0,
-// 1, ... and finalises the channel.  Deterministic.
+struct RepackJob {
+    const float *W;
+    float *wr;
+    int K, C, R, S, Kw;
+};
+
+__device__ __forceinline__ float round_tf32(float v) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
+}
+
+__device__ void repack_part(const RepackJob &j, long long first, long long stride) {
+    const long long total = (long long)j.R * j.S * j.C * j.Kw;
+    for (long long i = first; i < total; i += stride) {
+        const int kk = (int)(i % j.Kw);
+        long long t = i / j.Kw;
+        const int c = (int)(t % j.C);
+        t /= j.C;
+        const int s = (int)(t % j.S);
+        const int r = (int)(t / j.S);
+        j.wr[i] = kk < j.K ? round_tf32(j.W[(((long long)kk * j.C + c) * j.R + r) * j.S + s]) : 0.f;
+    }
+}
+
+// Block b < K * groups * pieces: channel k = b % K, then piece, then group
+// (consecutive blocks take adjacent planes).  Group g holds planes g * pln ..
+// min(N, (g + 1) * pln) - 1; piece q covers accesses q * L .. (q + 1) * L - 1 of
+// each of its planes (L = ceil(accesses per plane / pieces)).
 template <int ACT, bool BN, bool VEC>
 __global__ void __launch_bounds__(kRedThreads)
     bn_reduce_kernel(const float *__restrict__ delta, const float *__restrict__ output,
                      const float *__restrict__ z, const float *__restrict__ gamma,
                      const float *__restrict__ mean, const float *__restrict__ var, float eps,
-                     int K, int PQ, long long m, int splits, double2 *__restrict__ part,
-                     unsigned *__restrict__ cnt, float *__restrict__ db,
-                     float *__restrict__ dgamma, Coef *__restrict__ coef) {
-    constexpr int U = 4;  // loads per tensor per thread in flight
-    const int k = (int)(blockIdx.x / splits), j = (int)(blockIdx.x - (blockIdx.x / splits) * splits);
+                     int N, int K, int PQ, long long m, int pln, int groups, int pieces,
+                     float2 *__restrict__ part, unsigned *__restrict__ cnt,
+                     float *__restrict__ db, float *__restrict__ dgamma,
+                     Coef *__restrict__ coef, RepackJob job, int nrep) {
+    const int nred = K * groups * pieces;
+    if ((int)blockIdx.x >= nred) {
+        repack_part(job, (long long)(blockIdx.x - nred) * kRedThreads + threadIdx.x,
+                    (long long)nrep * kRedThreads);
+        return;
+    }
+    const int k = (int)(blockIdx.x % K);
+    const int gq = (int)(blockIdx.x / K);
+    const int q = gq % pieces, grp = gq / pieces;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // 1/sigma in fp64, once per block (fp64 is slow on this part: not per thread)
-    __shared__ float rs_sh;
-    if (BN && tid == 0) rs_sh = (float)(1.0 / sqrt((double)var[k] + (double)eps));
-    __syncthreads();
-    const float mu = BN ? mean[k] : 0.f, rs = BN ? rs_sh : 0.f;
-    const int W = VEC ? 4 : 1;                     // elements per access
-    const int mw = (int)(m / W);                   // accesses in the channel
-    const int pqw = PQ / W;                        // accesses per plane
-    const int g0 = (int)((long long)mw * j / splits), g1 = (int)((long long)mw * (j + 1) / splits);
-    // this thread's accesses g = g0 + tid + 256 t: plane n, offset o, tracked
-    // incrementally (one division up front)
-    int g = g0 + tid;
-    int n = g / pqw, o = g - (g / pqw) * pqw;
-    const size_t plane_stride = (size_t)K * pqw;   // accesses between planes n, n+1
+    const float mu = BN ? mean[k] : 0.f;
+    const float rs = BN ? rsqrtf(var[k] + eps) : 0.f;
+    constexpr int W = VEC ? 4 : 1;            // elements per access
+    const int pa = PQ / W;                    // accesses per plane
+    const int L = (pa + pieces - 1) / pieces;
+    const int a0 = q * L, a1 = min(pa, a0 + L);
+    const int n0 = grp * pln, n1 = min(N, n0 + pln);
     float s1 = 0.f, s2 = 0.f;
-    while (g < g1) {
-        size_t idx[U];
-        bool in[U];
+    for (int n = n0; n < n1; ++n) {
+        const size_t pbase = ((size_t)n * K + k) * pa;
+        for (int base = a0 + tid; base < a1; base += kRedThreads * kRedU) {
+            if constexpr (VEC) {
+                const float4 *D = reinterpret_cast<const float4 *>(delta) + pbase;
+                const float4 *Y = reinterpret_cast<const float4 *>(output) + pbase;
+                const float4 *Z = reinterpret_cast<const float4 *>(z) + pbase;
+                float4 dd[kRedU], yy[kRedU], zz[kRedU];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            in[u] = g < g1;
-            idx[u] = (size_t)n * plane_stride + (size_t)k * pqw + (size_t)(in[u] ? o : 0);
-            g += kRedThreads;
-            o += kRedThreads;
-            while (o >= pqw) {
-                o -= pqw;
-                ++n;
-            }
-        }
-        if constexpr (VEC) {
-            float4 dd[U], yy[U], zz[U];
+                for (int u = 0; u < kRedU; ++u) {
+                    const int i = base + u * kRedThreads;
+                    const bool in = i < a1;
+                    const int ii = in ? i : a0;
+                    dd[u] = __ldg(D + ii);
+                    if constexpr (ACT == CBA_ACT_LEAKY) yy[u] = __ldg(Y + ii);
+                    if constexpr (BN) zz[u] = __ldg(Z + ii);
+                    if (!in) dd[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const size_t i = in[u] ? idx[u] : idx[0];
-                dd[u] = __ldg(reinterpret_cast<const float4 *>(delta) + i);
-                if constexpr (ACT == CBA_ACT_LEAKY) yy[u] = __ldg(reinterpret_cast<const float4 *>(output) + i);
-                if constexpr (BN) zz[u] = __ldg(reinterpret_cast<const float4 *>(z) + i);
-            }
+                for (int u = 0; u < kRedU; ++u) {
+                    if constexpr (ACT != CBA_ACT_LEAKY) yy[u] = dd[u];
+                    if constexpr (!BN) zz[u] = dd[u];
+                    acc1<ACT, BN>(dd[u].x, yy[u].x, zz[u].x, mu, rs, s1, s2);
+                    acc1<ACT, BN>(dd[u].y, yy[u].y, zz[u].y, mu, rs, s1, s2);
+                    acc1<ACT, BN>(dd[u].z, yy[u].z, zz[u].z, mu, rs, s1, s2);
+                    acc1<ACT, BN>(dd[u].w, yy[u].w, zz[u].w, mu, rs, s1, s2);
+                }
+            } else {
+                float dd[kRedU], yy[kRedU], zz[kRedU];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (!in[u]) dd[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if constexpr (ACT != CBA_ACT_LEAKY) yy[u] = dd[u];
-                if constexpr (!BN) zz[u] = dd[u];
-                acc1<ACT, BN>(dd[u].x, yy[u].x, zz[u].x, mu, rs, s1, s2);
-                acc1<ACT, BN>(dd[u].y, yy[u].y, zz[u].y, mu, rs, s1, s2);
-                acc1<ACT, BN>(dd[u].z, yy[u].z, zz[u].z, mu, rs, s1, s2);
-                acc1<ACT, BN>(dd[u].w, yy[u].w, zz[u].w, mu, rs, s1, s2);
-            }
-        } else {
-            float dd[U], yy[U], zz[U];
+                for (int u = 0; u < kRedU; ++u) {
+                    const int i = base + u * kRedThreads;
+                    const bool in = i < a1;
+                    const int ii = in ? i : a0;
+                    dd[u] = in ? __ldg(delta + pbase + ii) : 0.f;
+                    yy[u] = ACT == CBA_ACT_LEAKY ? __ldg(output + pbase + ii) : 0.f;
+                    zz[u] = BN ? __ldg(z + pbase + ii) : 0.f;
+                }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const size_t i = in[u] ? idx[u] : idx[0];
-                dd[u] = __ldg(delta + i);
-                yy[u] = ACT == CBA_ACT_LEAKY ? __ldg(output + i) : 0.f;
-                zz[u] = BN ? __ldg(z + i) : 0.f;
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (!in[u]) dd[u] = 0.f;
-                acc1<ACT, BN>(dd[u], yy[u], zz[u], mu, rs, s1, s2);
+                for (int u = 0; u < kRedU; ++u) acc1<ACT, BN>(dd[u], yy[u], zz[u], mu, rs, s1, s2);
             }
         }
     }
@@ -161,29 +179,29 @@ __global__ void __launch_bounds__(kRedThreads)
         w2[warp] = s2;
     }
     __syncthreads();
+    const int nparts = groups * pieces;
     if (tid == 0) {
-        double t1 = 0.0, t2 = 0.0;
+        float t1 = 0.f, t2 = 0.f;
 #pragma unroll
         for (int i = 0; i < kRedThreads / 32; ++i) {
-            t1 += (double)w1[i];
-            t2 += (double)w2[i];
+            t1 += w1[i];
+            t2 += w2[i];
         }
-        part[(size_t)j * K + k] = make_double2(t1, t2);
-        __threadfence();
-        last = atomicAdd(cnt + k, 1u) == (unsigned)(splits - 1) ? 1u : 0u;
+        part[(size_t)gq * K + k] = make_float2(t1, t2);
+        // release: the partial is visible to whichever block sees the count
+        // complete; acquire: that block sees every other block's partial
+        last = atom_add_acq_rel(cnt + k, 1u) == (unsigned)(nparts - 1) ? 1u : 0u;
     }
     __syncthreads();
     if (!last || warp != 0) return;
-    // the channel's last block: every partial is visible (fence + counter)
-    __threadfence();
     double S1 = 0.0, S2 = 0.0;
-    for (int s0 = 0; s0 < splits; s0 += 32) {
-        double2 v = make_double2(0.0, 0.0);
-        if (s0 + lane < splits) v = __ldcg(part + (size_t)(s0 + lane) * K + k);
-        const int cntv = min(32, splits - s0);
-        for (int i = 0; i < cntv; ++i) {  // in order of j
-            S1 += __shfl_sync(0xffffffffu, v.x, i);
-            S2 += __shfl_sync(0xffffffffu, v.y, i);
+    for (int s0 = 0; s0 < nparts; s0 += 32) {
+        float2 v = make_float2(0.f, 0.f);
+        if (s0 + lane < nparts) v = __ldcg(part + (size_t)(s0 + lane) * K + k);
+        const int cntv = min(32, nparts - s0);
+        for (int i = 0; i < cntv; ++i) {  // in the partials' order
+            S1 += (double)__shfl_sync(0xffffffffu, v.x, i);
+            S2 += (double)__shfl_sync(0xffffffffu, v.y, i);
         }
     }
     if (lane == 0) {
@@ -208,30 +226,39 @@ __global__ void dz_out_kernel(const float *__restrict__ delta, const float *__re
 
 template <int ACT, bool BN>
 void launch_reduce_t(const Plan &p, const float *delta, const float *output, const float *z,
-                     const float *gamma, const float *mean, const float *var, double2 *part,
-                     unsigned *cnt, float *db, float *dgamma, Coef *coef, cudaStream_t st) {
-    const unsigned grid = (unsigned)((long long)p.K * p.red_splits);
+                     const float *gamma, const float *mean, const float *var, float2 *part,
+                     unsigned *cnt, float *db, float *dgamma, Coef *coef, const RepackJob &job,
+                     int nrep, cudaStream_t st) {
+    const unsigned grid = (unsigned)((long long)p.K * p.red_groups * p.red_pieces + nrep);
     if (p.PQ % 4 == 0)
         bn_reduce_kernel<ACT, BN, true><<<grid, kRedThreads, 0, st>>>(
-            delta, output, z, gamma, mean, var, p.eps, p.K, p.PQ, p.m, p.red_splits, part, cnt,
-            db, dgamma, coef);
+            delta, output, z, gamma, mean, var, p.eps, p.N, p.K, p.PQ, p.m, p.red_pln,
+            p.red_groups, p.red_pieces, part, cnt, db, dgamma, coef, job, nrep);
     else
         bn_reduce_kernel<ACT, BN, false><<<grid, kRedThreads, 0, st>>>(
-            delta, output, z, gamma, mean, var, p.eps, p.K, p.PQ, p.m, p.red_splits, part, cnt,
-            db, dgamma, coef);
+            delta, output, z, gamma, mean, var, p.eps, p.N, p.K, p.PQ, p.m, p.red_pln,
+            p.red_groups, p.red_pieces, part, cnt, db, dgamma, coef, job, nrep);
 }
 
 }  // namespace
 
 cudaError_t launch_reduce(const Plan &p, const float *delta, const float *output, const float *z,
                           const float *gamma, const float *mean, const float *var, float *db,
-                          float *dgamma, void *ws, cudaStream_t st, int *launches) {
-    double2 *part = ws_at<double2>(ws, p.off_red);
+                          float *dgamma, void *ws, cudaStream_t st, int *launches,
+                          const float *repack_W, float *repack_wr) {
+    float2 *part = ws_at<float2>(ws, p.off_red);
     unsigned *cnt = ws_at<unsigned>(ws, p.off_cnt);
     Coef *coef = ws_at<Coef>(ws, p.off_coef);
+    RepackJob job{repack_W, repack_wr, p.K, p.C, p.R, p.S, (p.K + 3) / 4 * 4};
+    int nrep = 0;
+    if (repack_W && repack_wr) {
+        const long long total = (long long)p.R * p.S * p.C * job.Kw;
+        nrep = (int)std::min<long long>((total + kRedThreads - 1) / kRedThreads, 64);
+    }
     const bool leaky = p.act == CBA_ACT_LEAKY;
 #define CBA_RED(A, B) \
-    launch_reduce_t<A, B>(p, delta, output, z, gamma, mean, var, part, cnt, db, dgamma, coef, st)
+    launch_reduce_t<A, B>(p, delta, output, z, gamma, mean, var, part, cnt, db, dgamma, coef, \
+                          job, nrep, st)
     if (p.bn) {
         if (leaky) CBA_RED(CBA_ACT_LEAKY, true);
         else CBA_RED(CBA_ACT_LINEAR, true);

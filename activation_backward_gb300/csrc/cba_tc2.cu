@@ -226,21 +226,6 @@ __global__ void __launch_bounds__(256)
 }
 
 // W[k][c][r][s] -> wr[r][s][c][kk] (kk < Kw; zero for kk >= K), TF32-rounded.
-__global__ void repack_wr_kernel(const float *__restrict__ W, int K, int C, int R, int S, int Kw,
-                                 float *__restrict__ wr) {
-    const long long total = (long long)R * S * C * Kw;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int kk = (int)(i % Kw);
-        long long t = i / Kw;
-        const int c = (int)(t % C);
-        t /= C;
-        const int s = (int)(t % S);
-        const int r = (int)(t / S);
-        wr[i] = kk < K ? to_tf32(W[(((long long)kk * C + c) * R + r) * S + s]) : 0.f;
-    }
-}
-
 // ------------------------------------------------------------------ wgrad
 
 constexpr int kW2RingMax = 6;  // dz row tiles resident (at most)
@@ -1637,19 +1622,11 @@ cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, fl
     return cudaGetLastError();
 }
 
-cudaError_t launch_dgrad_tc2(const Plan &p, const float *Wt, const float *dzt,
-                             const float *residual, float *prev, void *ws, float *wr,
-                             cudaStream_t st, int *launches) {
+cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzt, const float *residual, float *prev,
+                             void *ws, const float *wr_c, cudaStream_t st, int *launches) {
     const V2Geom g = v2_geom(p);
     const int Kw = (p.K + 3) / 4 * 4;
-    {
-        const long long total = (long long)p.R * p.S * p.C * Kw;
-        const int blocks = (int)std::min<long long>((total + 255) / 256, (long long)p.num_sms * 8);
-        repack_wr_kernel<<<blocks, 256, 0, st>>>(Wt, p.K, p.C, p.R, p.S, Kw, wr);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        *launches += 1;
-    }
+    float *wr = const_cast<float *>(wr_c);  // tensor maps take a non-const base; only read
     const float *dzc =
         reinterpret_cast<const float *>(reinterpret_cast<const char *>(dzt) + dzt_bytes_only(p, g));
     const long long total_pos = (long long)p.N * g.Pp * g.Qpp;
