@@ -225,7 +225,6 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// W[k][c][r][s] -> wr[r][s][c][kk] (kk < Kw; zero for kk >= K), TF32-rounded.
 // ------------------------------------------------------------------ wgrad
 
 constexpr int kW2RingMax = 6;  // dz row tiles resident (at most)
