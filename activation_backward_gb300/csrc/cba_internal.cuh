@@ -118,6 +118,26 @@ cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, fl
 cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzt, const float *residual, float *prev,
                              void *ws, const float *wr, cudaStream_t st, int *launches);
 
+// Launches `kern` with programmatic stream serialisation: it may be scheduled
+// while the previous kernel in the stream is still finishing (that kernel's
+// blocks call griddep_launch_dependents), and it calls griddep_wait before it
+// touches memory its predecessors read or write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <typename T>
 inline T *ws_at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<char *>(ws) + off);

@@ -18,6 +18,25 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Blocks until every grid this one depends on programmatically has completed
+// and its memory operations are visible (returns at once when the launch had
+// no programmatic dependency).  A kernel launched with programmatic stream
+// serialisation must call it before it reads or writes anything its
+// predecessors touch.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid in the stream (if launched with programmatic stream
+// serialisation) be scheduled once every block of this grid has called this or
+// exited.  The next grid still waits for this one's completion before it
+// touches memory (griddep_wait).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

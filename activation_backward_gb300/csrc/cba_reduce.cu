@@ -14,6 +14,7 @@
 // gradient's weight repack (W[k][c][r][s] -> wr[r][s][c][k], TF32-rounded,
 // k padded to Kw with zeros), which would otherwise be a launch of its own.
 #include "cba_internal.cuh"
+#include "cba_ptx.cuh"
 
 namespace cba {
 
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(kRedThreads)
                      float2 *__restrict__ part, unsigned *__restrict__ cnt,
                      float *__restrict__ db, float *__restrict__ dgamma,
                      Coef *__restrict__ coef, RepackJob job, int nrep) {
+    ptx::griddep_wait();
     const int nred = K * groups * pieces;
     if ((int)blockIdx.x >= nred) {
         repack_part(job, (long long)(blockIdx.x - nred) * kRedThreads + threadIdx.x,
@@ -179,6 +181,9 @@ __global__ void __launch_bounds__(kRedThreads)
         w2[warp] = s2;
     }
     __syncthreads();
+    // this block's loads are done: the dz pass may be scheduled (it still
+    // waits for this grid to complete before it reads anything)
+    ptx::griddep_launch_dependents();
     const int nparts = groups * pieces;
     if (tid == 0) {
         float t1 = 0.f, t2 = 0.f;

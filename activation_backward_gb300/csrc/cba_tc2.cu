@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(256)
     dzc_kernel(const float *__restrict__ delta, const float *__restrict__ output,
                const float *__restrict__ z, const Coef *__restrict__ coef, int K, int Pe, int Qe,
                int Kp, int Pp, int Qpp, int bd_lo, int bq_lo, int nqc, float *__restrict__ dzc) {
+    ptx::griddep_wait();  // the coefficients come from the reduction pass
     __shared__ float tile[32][65];
     const int t = threadIdx.x;
     const int n = blockIdx.y / Pp, pp = blockIdx.y - (blockIdx.y / Pp) * Pp, p = pp - bd_lo;
@@ -212,6 +213,7 @@ __global__ void __launch_bounds__(256)
         }
     }
     __syncthreads();
+    ptx::griddep_launch_dependents();  // the weight gradient may be scheduled
     {
         const int qq = t >> 4, k4 = t & 15;
 #pragma unroll
@@ -1111,6 +1113,8 @@ __global__ void __launch_bounds__(kD4Threads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = sb.tmem_base;
+    // dzc, wr and prev are touched only after the previous kernels completed
+    ptx::griddep_wait();
 
     if (warp == 0 || warp == 10) {
         // ---- TMA: warp 0 the A tiles, warp 10 the W slices
@@ -1474,16 +1478,17 @@ cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float
         float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) + dzt_bytes_only(p, g));
         const int nqc = (g.Qe + 31) / 32;
         dim3 grid((unsigned)(nqc + 1), (unsigned)(p.N * g.Pp), (unsigned)((g.Kp + 63) / 64));
+        cudaError_t pe = cudaSuccess;
 #define CBA_DZC(A, B)                                                                          \
     do {                                                                                       \
         if (g.Qe % 4 == 0)                                                                     \
-            dzc_kernel<A, B, true><<<grid, 256, 0, st>>>(delta, output, z, coef, p.K, g.Pe,   \
-                                                         g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo,    \
-                                                         g.bq_lo, nqc, dzc);                  \
+            pe = launch_pdl(dzc_kernel<A, B, true>, grid, dim3(256), 0, st, delta, output, z,  \
+                            coef, p.K, g.Pe, g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, nqc,  \
+                            dzc);                                                              \
         else                                                                                   \
-            dzc_kernel<A, B, false><<<grid, 256, 0, st>>>(delta, output, z, coef, p.K, g.Pe,  \
-                                                          g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo,   \
-                                                          g.bq_lo, nqc, dzc);                 \
+            pe = launch_pdl(dzc_kernel<A, B, false>, grid, dim3(256), 0, st, delta, output, z, \
+                            coef, p.K, g.Pe, g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, nqc,  \
+                            dzc);                                                              \
     } while (0)
         if (p.bn) {
             if (leaky) CBA_DZC(CBA_ACT_LEAKY, true);
@@ -1493,6 +1498,7 @@ cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float
             else CBA_DZC(CBA_ACT_LINEAR, false);
         }
 #undef CBA_DZC
+        if (pe != cudaSuccess) return pe;
     } else if (with_dzc) {
         float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) + dzt_bytes_only(p, g));
         const int qlo = -g.bq_lo;
@@ -1737,8 +1743,9 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzt, const float *resid
                     dgrad_tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem4);
                 if (e != cudaSuccess) return e;
                 const int grid4 = std::max(1, std::min(p.num_sms, d4.total_units));
-                dgrad_tc4_kernel<<<grid4, kD4Threads, smem4, st>>>(tma4, tmw4, tmw, d4);
-                e = cudaGetLastError();
+                e = launch_pdl(dgrad_tc4_kernel, dim3(grid4), dim3(kD4Threads), smem4, st, tma4,
+                               tmw4, tmw, d4);
+                if (e == cudaSuccess) e = cudaGetLastError();
                 if (e != cudaSuccess) return e;
                 *launches += 1;
                 continue;

@@ -145,6 +145,8 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = sb.tmem_base;
+    // dzc and the partials are touched only after the previous kernels completed
+    ptx::griddep_wait();
 
     if (warp == 0) {
         // ---- TMA: x rows into the ring (and its mirror slots), dz tiles
@@ -368,6 +370,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     }
     ptx::tc_fence_before();
     __syncthreads();
+    ptx::griddep_launch_dependents();  // the partial-tile sum may be scheduled
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
@@ -382,6 +385,7 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 __global__ void __launch_bounds__(256)
     wgrad_part_reduce_kernel(const float *__restrict__ part, int cpt, int N, int cb, int S,
                              int nctile, int K, int C, int R, float *__restrict__ dW) {
+    ptx::griddep_wait();  // the partial tiles come from the weight-gradient kernel
     __shared__ float4 red[8][32];
     const int col = blockIdx.x % N, tile = blockIdx.x / N;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -396,6 +400,7 @@ __global__ void __launch_bounds__(256)
     }
     red[warp][lane] = acc;
     __syncthreads();
+    ptx::griddep_launch_dependents();  // the input gradient may be scheduled
     if (warp == 0) {
         float4 t = red[0][lane];
 #pragma unroll
@@ -508,17 +513,19 @@ cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, fl
         e = cudaFuncSetAttribute(wgrad_tc4_kernel<3>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)w.smem);
         if (e != cudaSuccess) return e;
-        wgrad_tc4_kernel<3><<<w.grid, kW4Threads, w.smem, st>>>(tmx, tmdz, a);
+        e = launch_pdl(wgrad_tc4_kernel<3>, dim3(w.grid), dim3(kW4Threads), w.smem, st, tmx, tmdz,
+                       a);
     } else {
         e = cudaFuncSetAttribute(wgrad_tc4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)w.smem);
         if (e != cudaSuccess) return e;
-        wgrad_tc4_kernel<1><<<w.grid, kW4Threads, w.smem, st>>>(tmx, tmdz, a);
+        e = launch_pdl(wgrad_tc4_kernel<1>, dim3(w.grid), dim3(kW4Threads), w.smem, st, tmx, tmdz,
+                       a);
     }
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    wgrad_part_reduce_kernel<<<w.ntiles * w.N, 256, 0, st>>>(a.part, w.cpt, w.N, w.cb, p.S,
-                                                              w.nctile, p.K, p.C, p.R, dW);
+    e = launch_pdl(wgrad_part_reduce_kernel, dim3(w.ntiles * w.N), dim3(256), 0, st,
+                   (const float *)a.part, w.cpt, w.N, w.cb, p.S, w.nctile, p.K, p.C, p.R, dW);
+    if (e != cudaSuccess) return e;
     *launches += 2;
     return cudaGetLastError();
 }
