@@ -40,8 +40,8 @@ namespace {
 
 constexpr uint64_t kW4LimitNs = 2000000000ull;
 constexpr int kW4Threads = 352;
-constexpr int kW4MaxNR = 12;  // x ring rows (mirror slots come on top)
-constexpr int kW4MaxND = 8;   // dz ring slots
+constexpr int kW4MaxNR = 16;  // x ring rows (mirror slots come on top)
+constexpr int kW4MaxND = 4;   // dz ring slots
 // TMA loads take about a microsecond to land, so the rings are as deep as
 // shared memory allows: enough loads stay in flight to cover that latency.
 constexpr int kW4NA = 4;      // A stages in TMEM (even), one item pair (64 columns) each
