@@ -392,11 +392,20 @@ __global__ void __launch_bounds__(256)
     const float4 *src =
         reinterpret_cast<const float4 *>(part + ((size_t)tile * N + col) * cpt * 128) + lane;
     const size_t bstride = 32;  // float4s between consecutive blocks' partials
+    // every load of a round in flight together (8 per lane), then the adds in
+    // the order b = warp, warp + 8, ... (fixed)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int b = warp; b < cpt; b += 8) {
-        const float4 v = __ldg(src + (size_t)b * bstride);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    for (int b0 = warp; b0 < cpt; b0 += 64) {
+        float4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int b = b0 + 8 * q;
+            v[q] = b < cpt ? __ldcg(src + (size_t)b * bstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            acc.x += v[q].x; acc.y += v[q].y; acc.z += v[q].z; acc.w += v[q].w;
+        }
     }
     red[warp][lane] = acc;
     __syncthreads();
