@@ -64,6 +64,24 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(value, ws, device):
+    """The largest of every rank's `value` (each rank is one replica; the job
+    takes as long as its slowest rank).  Collective only when ws > 1."""
+    if ws <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ws, flops_per_replica_step, ms_per_step):
+    """Whole-job throughput in TFLOP/s: every rank runs one replica's step,
+    all ranks' work divided by the slowest rank's step time."""
+    return ws * flops_per_replica_step / (ms_per_step * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -332,13 +350,9 @@ def run_ours(args):
     for dl in dls:
         assert dl.status() == cba.CBA_OK, "device status after the timed region"
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), ws, dev)
     ms_per_step = total_ms / args.steps
-    value = ws * flops / (ms_per_step * 1e-3) / 1e12
+    value = job_value(ws, flops, ms_per_step)
 
     # per-phase device times (reduce, wgrad, dgrad) and the step time of
     # direct, uncaptured calls: traced calls with events between the phases
