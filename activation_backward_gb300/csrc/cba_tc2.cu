@@ -137,7 +137,8 @@ __global__ void __launch_bounds__(256)
 // output columns 32 bx .. 32 bx + 31 of row pp - bd_lo for the 64 channels
 // 64 kz .. 64 kz + 63 through shared memory (each thread reads 4 consecutive
 // columns of one channel from each input, and writes 4 consecutive channels
-// of one column as a float4); bx == nqc writes the border columns.
+// of one column as a float4).  The first and last column chunks of a row also
+// write its left and right border columns.
 template <int ACT, bool BN, bool VEC>
 __global__ void __launch_bounds__(256)
     dzc_kernel(const float *__restrict__ delta, const float *__restrict__ output,
@@ -150,15 +151,14 @@ __global__ void __launch_bounds__(256)
     const int k0 = blockIdx.z * 64;
     float *rowp = dzc + ((size_t)n * Pp + pp) * Qpp * Kp;
     const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    if ((int)blockIdx.x == nqc) {  // border columns (left and right of the data)
-        const int nright = Qpp - bq_lo - Qe;
-        const int ncols = bq_lo + nright;
-        for (int i = t; i < ncols * 16; i += 256) {
+    {  // border columns: the left ones with the first column chunk, the right ones with the last
+        const int nl = blockIdx.x == 0 ? bq_lo : 0;
+        const int nr = (int)blockIdx.x == nqc - 1 ? Qpp - bq_lo - Qe : 0;
+        for (int i = t; i < (nl + nr) * 16; i += 256) {
             const int c = i >> 4, kc = k0 + (i & 15) * 4;
-            const int pq = c < bq_lo ? c : bq_lo + Qe + (c - bq_lo);
+            const int pq = c < nl ? c : bq_lo + Qe + (c - nl);
             if (kc < Kp) *reinterpret_cast<float4 *>(rowp + (size_t)pq * Kp + kc) = zero4;
         }
-        return;
     }
     const int q0 = blockIdx.x * 32;
     if (p < 0 || p >= Pe) {  // zero border row
@@ -1477,7 +1477,7 @@ cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float
     if (with_dzc && !with_dzt) {
         float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) + dzt_bytes_only(p, g));
         const int nqc = (g.Qe + 31) / 32;
-        dim3 grid((unsigned)(nqc + 1), (unsigned)(p.N * g.Pp), (unsigned)((g.Kp + 63) / 64));
+        dim3 grid((unsigned)nqc, (unsigned)(p.N * g.Pp), (unsigned)((g.Kp + 63) / 64));
         cudaError_t pe = cudaSuccess;
 #define CBA_DZC(A, B)                                                                          \
     do {                                                                                       \
