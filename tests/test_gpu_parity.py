@@ -120,6 +120,15 @@ EDGE = [
     (1, 129, 8, 8, 64, 3, 3, 2, 1, 1, True),
     (4, 16, 16, 16, 16, 1, 1, 2, 0, 1, False),
     (2, 24, 15, 14, 40, 3, 3, 3, 2, 0, True),
+    # weight gradient fed by TMA (input width a multiple of 4): a ragged last
+    # column chunk; a 1x1 layer viewed as one row per plane; two 128-channel
+    # tiles of k with an odd number of 32-channel chunks
+    (2, 24, 12, 36, 40, 3, 3, 1, 1, 1, True),
+    (2, 48, 8, 8, 24, 1, 1, 1, 0, 0, False),
+    (2, 16, 8, 12, 160, 3, 3, 1, 1, 1, True),
+    # input gradient with two k-chunks per stage and an odd chunk count (the
+    # last stage's second chunk lies past K and is zero-filled)
+    (2, 16, 10, 10, 96, 3, 3, 1, 1, 1, True),
 ]
 
 
