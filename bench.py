@@ -397,7 +397,7 @@ def run_ours(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(dls, layers, flops, args, stream, dev)
+        e2e = measure_e2e(dls, layers, flops, args, stream, dev, math)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
@@ -417,44 +417,74 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def measure_e2e(dls, layers, flops, args, stream, dev):
+def measure_e2e(dls, layers, flops, args, stream, dev, math):
     """The same metric through the public call with HOST buffers: every step
     copies the step's inputs from pinned host memory to the device, runs the
-    backward and reads the results back."""
+    backward and reads the results back.
+
+    The steps are pipelined as a data loader would run them: two sets of device
+    buffers, the inputs of step i + 1 copied on one stream while step i
+    computes on another, the results of step i read back on a third.  Events
+    keep each set's reuse in order (a set's inputs are overwritten only after
+    the step that read them has finished, its outputs only after they were
+    read back).  Every step's copies stay inside the timed region."""
     import torch
+    from activation_backward_gb300.layer import DeviceLayer
     names_in = ("x", "output", "z", "delta", "W", "gamma", "mean", "var", "residual")
     names_out = ("dW", "db", "dgamma", "prev")
-    hosts = []
-    for dl in dls:
-        hin = {n: getattr(dl, n).cpu().pin_memory() for n in names_in
-               if getattr(dl, n) is not None}
-        hout = {n: torch.empty_like(getattr(dl, n), device="cpu").pin_memory()
-                for n in names_out if getattr(dl, n) is not None}
-        hosts.append((hin, hout))
-    h2d = sum(t.numel() * 4 for hin, _ in hosts for t in hin.values())
-    d2h = sum(t.numel() * 4 for _, hout in hosts for t in hout.values())
+    sets = [dls, [DeviceLayer(l, math=math, device=dev) for l in layers]]
+    hin = [{n: getattr(dl, n).cpu().pin_memory() for n in names_in
+            if getattr(dl, n) is not None} for dl in dls]
+    hout = [[{n: torch.empty_like(getattr(dl, n), device="cpu").pin_memory()
+              for n in names_out if getattr(dl, n) is not None} for dl in dset]
+            for dset in sets]
+    h2d = sum(t.numel() * 4 for h in hin for t in h.values())
+    d2h = sum(t.numel() * 4 for h in hout[0] for t in h.values())
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    mk = lambda: torch.cuda.Event()  # noqa: E731
 
-    def one():
-        for dl, (hin, hout) in zip(dls, hosts):
-            for n, t in hin.items():
-                getattr(dl, n).copy_(t, non_blocking=True)
-            dl.run()
-            for n, t in hout.items():
-                t.copy_(getattr(dl, n), non_blocking=True)
+    def pipeline(nsteps):
+        ev_in = [mk() for _ in range(nsteps)]
+        ev_done = [mk() for _ in range(nsteps)]
+        ev_out = [mk() for _ in range(nsteps)]
+        for i in range(nsteps):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_done[i - 2])  # step i - 2 has read this set's inputs
+                for dl, h in zip(sets[b], hin):
+                    for n, t in h.items():
+                        getattr(dl, n).copy_(t, non_blocking=True)
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_out[i - 2])  # this set's outputs were read back
+            for dl in sets[b]:
+                dl.run(stream=stream)
+            ev_done[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[i])
+                for dl, h in zip(sets[b], hout[b]):
+                    for n, t in h.items():
+                        t.copy_(getattr(dl, n), non_blocking=True)
+                ev_out[i].record(s_out)
+        stream.wait_event(ev_out[nsteps - 1])
 
     steps = max(3, min(args.steps, 50))
-    for _ in range(3):
-        one()
+    pipeline(3)
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
-    for _ in range(steps):
-        one()
+    s_in.wait_event(s)
+    pipeline(steps)
     e.record(stream)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e) / steps
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
+            "overlap": "inputs of step i+1 copied while step i computes; two device "
+                       "buffer sets, three streams"}
 
 
 def main():
