@@ -40,6 +40,12 @@
 #define REF_ACT_LEAKY 1
 #define REF_ACT_LOGISTIC 2 /* only for the oracle's own self-tests */
 
+/* batch_normalize: 0 no BN, 1 training mode (batch statistics), 2 frozen
+ * statistics (the given mean/var are constants of the forward) */
+#define REF_BN_NONE 0
+#define REF_BN_BATCH 1
+#define REF_BN_FROZEN 2
+
 /* ------------------------------------------------------------------ threads */
 
 void cba_ref_set_threads(int n) {
@@ -209,6 +215,28 @@ int cba_ref_backward_batchnorm(const double *x, const double *x_norm, const doub
     return 0;
 }
 
+/* Frozen statistics: the mean and variance are constants of the forward (caffe's
+ * use_global_stats_, [BNU] Backward_cpu, "use_global_stats_为真时" branch), so
+ * the normalisation is the per-channel affine map (x - mean) / sqrt(var + eps)
+ * and its gradient is the incoming gradient divided by sqrt(var + eps).  The
+ * steps: backward_bias and backward_scale as in training mode ([YOLO] §4; the
+ * Scale layer's bias and scale gradients in caffe), scale_bias (the product
+ * with gamma, [YOLO] §4), then the division of the use_global_stats branch. */
+int cba_ref_backward_batchnorm_frozen(const double *x_norm, const double *variance,
+                                      const double *scales, double eps, int batch, int n,
+                                      int size, double *delta, double *bias_updates,
+                                      double *scale_updates) {
+    cba_ref_backward_bias(bias_updates, delta, batch, n, size);
+    cba_ref_backward_scale(x_norm, delta, batch, n, size, scale_updates);
+    cba_ref_scale_bias(delta, scales, batch, n, size);
+    for (int b = 0; b < batch; ++b)
+        for (int f = 0; f < n; ++f) {
+            const double sd = sqrt(variance[f] + eps);
+            for (int i = 0; i < size; ++i) delta[i + (long)size * (f + (long)n * b)] /= sd;
+        }
+    return 0;
+}
+
 /* The second, independent formulation of the same gradient: caffe's
  * BatchNormLayer::Backward_cpu ([BNU]), which has no scale (a separate Scale
  * layer multiplies by gamma before it).  With Y = x_norm and dY = top_diff:
@@ -323,6 +351,7 @@ void cba_ref_axpy(long n, double alpha, const double *x, double *y) {
  * backward_convolutional_layer ([YOLO] §3.1):
  *   1. gradient_array(output, act, delta)
  *   2. batch_normalize ? backward_batchnorm_layer : backward_bias
+ *      (batch_normalize = 2: the frozen-statistics form above)
  *   3. dW += delta . im2col(x)^T          (always accumulates)
  *   4. if prev_delta: prev_delta (= or +=) col2im(W^T . delta) + residual
  * Inputs are not modified (delta is copied first).  dW, db, dgamma always
@@ -341,6 +370,7 @@ int cba_ref_conv_bn_act_backward_f64(int N, int C, int H, int W, int K, int R, i
                                      double *dgamma, double *prev_delta, double *dz_out) {
     if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || K <= 0 || R <= 0 || S <= 0 || stride <= 0 || pad < 0)
         return -1;
+    if (batch_normalize < REF_BN_NONE || batch_normalize > REF_BN_FROZEN) return -1;
     int P = cba_ref_out_size(H, R, stride, pad), Q = cba_ref_out_size(W, S, stride, pad);
     if (P <= 0 || Q <= 0) return -1;
     if (!x || !delta || !Wt || !dW || !db) return -1;
@@ -356,7 +386,11 @@ int cba_ref_conv_bn_act_backward_f64(int N, int C, int H, int W, int K, int R, i
         double *xn = (double *)malloc(sizeof(double) * nout);
         if (!xn) { free(d); return -1; }
         cba_ref_x_norm(z, mean, var, eps, N, K, P * Q, xn);
-        int rc = cba_ref_backward_batchnorm(z, xn, mean, var, gamma, eps, N, K, P * Q, d, db, dgamma);
+        int rc = batch_normalize == REF_BN_FROZEN
+                     ? cba_ref_backward_batchnorm_frozen(xn, var, gamma, eps, N, K, P * Q, d, db,
+                                                         dgamma)
+                     : cba_ref_backward_batchnorm(z, xn, mean, var, gamma, eps, N, K, P * Q, d,
+                                                  db, dgamma);
         free(xn);
         if (rc) { free(d); return -1; }
     } else {
@@ -421,6 +455,7 @@ int cba_ref_backward_dz(int N, int K, int P, int Q, int act, int batch_normalize
                         const float *gamma, const float *mean, const float *var, double *dz,
                         double *db, double *dgamma) {
     if (N <= 0 || K <= 0 || P <= 0 || Q <= 0 || !delta || !dz || !db) return -1;
+    if (batch_normalize < REF_BN_NONE || batch_normalize > REF_BN_FROZEN) return -1;
     if (act != REF_ACT_LINEAR && !output) return -1;
     if (batch_normalize && (!z || !gamma || !mean || !var || !dgamma)) return -1;
     long nout = (long)N * K * P * Q;
@@ -437,7 +472,11 @@ int cba_ref_backward_dz(int N, int K, int P, int Q, int act, int batch_normalize
     int rc = -1;
     if (zz && g && m && v && xn) {
         cba_ref_x_norm(zz, m, v, (double)eps, N, K, P * Q, xn);
-        rc = cba_ref_backward_batchnorm(zz, xn, m, v, g, (double)eps, N, K, P * Q, dz, db, dgamma);
+        rc = batch_normalize == REF_BN_FROZEN
+                 ? cba_ref_backward_batchnorm_frozen(xn, v, g, (double)eps, N, K, P * Q, dz, db,
+                                                     dgamma)
+                 : cba_ref_backward_batchnorm(zz, xn, m, v, g, (double)eps, N, K, P * Q, dz, db,
+                                              dgamma);
     }
     free(zz); free(g); free(m); free(v); free(xn);
     return rc;

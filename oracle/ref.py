@@ -15,6 +15,10 @@ ACT_LINEAR = 0
 ACT_LEAKY = 1
 ACT_LOGISTIC = 2  # oracle self-tests only
 
+BN_NONE = 0
+BN_BATCH = 1     # training mode: batch statistics
+BN_FROZEN = 2    # frozen statistics: mean and var are constants of the forward
+
 _lib = None
 
 _dp = ctypes.POINTER(ctypes.c_double)
@@ -189,7 +193,7 @@ def conv_bn_act_backward(x, output, z, delta, Wt, gamma, mean, var, residual, *,
         e = ctypes.c_float(eps)
     keep = [x, output, z, delta, Wt, gamma, mean, var, residual]
     ptrs = [conv(a) for a in keep]
-    rc = fn(N, C, H, W, K, R, S, stride, pad, int(act), int(bool(batch_normalize)),
+    rc = fn(N, C, H, W, K, R, S, stride, pad, int(act), int(batch_normalize),
             int(bool(accumulate)), e, *ptrs, _pd(o_dW), _pd(o_db), _pd(o_dg), _pd(o_prev),
             _pd(o_dz))
     if rc != 0:
@@ -209,7 +213,7 @@ def backward_dz(output, z, delta, gamma, mean, var, *, act, batch_normalize, eps
     o_dg = (np.zeros(K) if dgamma is None else _f64(dgamma).copy()) if batch_normalize else None
     f = lambda a: None if a is None else _pf(np.ascontiguousarray(a, np.float32))  # noqa: E731
     keep = [output, z, delta, gamma, mean, var]
-    rc = lib().cba_ref_backward_dz(N, K, P, Q, int(act), int(bool(batch_normalize)),
+    rc = lib().cba_ref_backward_dz(N, K, P, Q, int(act), int(batch_normalize),
                                    ctypes.c_float(eps), *[f(a) for a in keep], _pd(dz), _pd(o_db),
                                    _pd(o_dg))
     if rc != 0:

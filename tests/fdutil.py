@@ -23,12 +23,18 @@ def act_fwd(act, v):
     raise ValueError(act)
 
 
-def layer_forward(x, w, gamma, beta, *, stride, pad, act, bn, eps):
+def layer_forward(x, w, gamma, beta, *, stride, pad, act, bn, eps, stats=None):
     """Forward of the layer: z = conv(x, w); BN with the batch statistics
-    (biased variance) if bn; then scale, shift and activation.  Without BN,
-    beta is the conv bias.  Returns (z, mean, var, pre_activation, output)."""
+    (biased variance) if bn, or with the fixed (mean, var) of ``stats`` (frozen
+    statistics: constants of the forward); then scale, shift and activation.
+    Without BN, beta is the conv bias.  Returns (z, mean, var, pre_activation,
+    output)."""
     z = conv64(x, w, stride, pad)
-    if bn:
+    if bn and stats is not None:
+        mean, var = (np.asarray(a, np.float64) for a in stats)
+        xh = (z - mean[None, :, None, None]) / np.sqrt(var[None, :, None, None] + eps)
+        pre = gamma[None, :, None, None] * xh + beta[None, :, None, None]
+    elif bn:
         mean = z.mean(axis=(0, 2, 3))
         var = ((z - mean[None, :, None, None]) ** 2).mean(axis=(0, 2, 3))
         xh = (z - mean[None, :, None, None]) / np.sqrt(var[None, :, None, None] + eps)

@@ -130,6 +130,64 @@ def test_chain_matches_finite_differences(ref, case):
         close(got["dgamma"], central_diff(loss_g, gamma))
 
 
+FROZEN_CASES = [
+    # N, C, H, W, K, R, S, stride, pad, act, residual
+    (2, 3, 5, 5, 4, 3, 3, 1, 1, 1, False),
+    (2, 3, 6, 5, 4, 3, 3, 2, 1, 0, True),
+    (3, 4, 4, 4, 3, 1, 1, 1, 0, 1, True),
+]
+
+
+@pytest.mark.parametrize("case", FROZEN_CASES, ids=[str(i) for i in range(len(FROZEN_CASES))])
+def test_frozen_stats_chain_matches_finite_differences(ref, case):
+    """batch_normalize = 2: the mean and variance are constants of the forward
+    (caffe use_global_stats), so the finite differences of the forward with
+    those fixed statistics are the exact gradients of every output."""
+    N, C, H, W, K, R, S, st, pad, act, res = case
+    for attempt in range(50):
+        seed = 300 + 100 * FROZEN_CASES.index(case) + attempt
+        x, w, gamma, beta, D, Dres = _draw_case((N, C, H, W, K, R, S, st, pad, act, True, res),
+                                                seed)
+        rng = _rng(seed + 5000)
+        z0 = layer_forward(x, w, gamma, beta, stride=st, pad=pad, act=0, bn=False, eps=EPS)[0]
+        # statistics that are not the batch's own: shifted mean, scaled variance
+        mean = z0.mean(axis=(0, 2, 3)) + rng.uniform(-0.5, 0.5, K)
+        var = z0.var(axis=(0, 2, 3)) * rng.uniform(0.5, 2.0, K)
+        kw = dict(stride=st, pad=pad, act=act, bn=True, eps=EPS, stats=(mean, var))
+        z, _, _, pre, out = layer_forward(x, w, gamma, beta, **kw)
+        if act != 1 or np.min(np.abs(pre)) >= 5e-3:
+            break  # clear of the leaky kink
+    else:
+        raise RuntimeError("no draw clear of the kink")
+
+    def loss_x(v):
+        L = float(np.sum(D * layer_forward(v, w, gamma, beta, **kw)[4]))
+        if Dres is not None:
+            L += float(np.sum(Dres * v))
+        return L
+
+    got = ref.conv_bn_act_backward(x, out, z, D, w, gamma, mean, var, Dres, stride=st, pad=pad,
+                                   act=act, batch_normalize=2, accumulate=0, eps=EPS,
+                                   f64_inputs=True)
+
+    def close(a, b, tol=2e-6):
+        scale = max(np.max(np.abs(b)), 1e-12)
+        assert np.max(np.abs(a - b)) <= tol * scale, (np.max(np.abs(a - b)), scale)
+
+    close(got["prev_delta"], central_diff(loss_x, x))
+    close(got["dW"], central_diff(
+        lambda v: float(np.sum(D * layer_forward(x, v, gamma, beta, **kw)[4])), w))
+    close(got["dgamma"], central_diff(
+        lambda v: float(np.sum(D * layer_forward(x, w, v, beta, **kw)[4])), gamma))
+    close(got["db"], central_diff(
+        lambda v: float(np.sum(D * layer_forward(x, w, gamma, v, **kw)[4])), beta))
+    # and it differs from the training-mode backward on the same inputs
+    trn = ref.conv_bn_act_backward(x, out, z, D, w, gamma, mean, var, Dres, stride=st, pad=pad,
+                                   act=act, batch_normalize=1, accumulate=0, eps=EPS,
+                                   f64_inputs=True)
+    assert np.max(np.abs(trn["dW"] - got["dW"])) > 1e-3 * np.max(np.abs(got["dW"]))
+
+
 # ------------------------------------- convolution gradients, other forms
 
 def _im2col(img, R, S, stride, pad):
