@@ -46,7 +46,7 @@ int make_plan(const cba_desc_t *d, Plan *p) {
         return CBA_ERR_ARG;
     if (d->act != CBA_ACT_LINEAR && d->act != CBA_ACT_LEAKY) return CBA_ERR_ARG;
     if (d->math != CBA_MATH_TF32 && d->math != CBA_MATH_FFMA) return CBA_ERR_ARG;
-    if (d->batch_normalize != 0 && d->batch_normalize != 1) return CBA_ERR_ARG;
+    if (d->batch_normalize < 0 || d->batch_normalize > 2) return CBA_ERR_ARG;
     if (d->accumulate != 0 && d->accumulate != 1) return CBA_ERR_ARG;
     if (d->batch_normalize && !(std::isfinite(d->eps) && d->eps >= 0.f)) return CBA_ERR_ARG;
     const long long P = (long long)(d->H + 2LL * d->pad - d->R) / d->stride + 1;

@@ -29,7 +29,8 @@ struct Plan {
     int N, C, H, W, K, R, S, stride, pad, P, Q;
     int PQ, HW, RS, CRS;
     long long m;  // N*P*Q: elements per output channel
-    int act, bn, accumulate, math;
+    int act, accumulate, math;
+    int bn;  // 0 no BN, 1 batch statistics, 2 frozen statistics
     float eps;
     int num_sms;
     // reduction pass: a block sums red_pln whole (n, k) planes of one channel,

@@ -41,7 +41,10 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
 }
 
 // Per-channel finalisation from the S1, S2 totals: db += S1, dgamma += S2 and
-// the coefficients of dz = a*delta' + b + c*(z - mu).
+// the coefficients of dz = a*delta' + b + c*(z - mu).  bn: 0 no BN, 1 batch
+// statistics, 2 frozen statistics (mean and var are constants of the forward:
+// the gradient is gamma * delta' / sigma, b = c = 0; caffe's use_global_stats
+// branch of BatchNormLayer::Backward_cpu, "BatchNorm 理解").
 __device__ __forceinline__ void finalize_channel(int k, double S1, double S2, long long m,
                                                  const float *__restrict__ gamma,
                                                  const float *__restrict__ mean,
@@ -57,8 +60,8 @@ __device__ __forceinline__ void finalize_channel(int k, double S1, double S2, lo
         const float a = gamma[k] / sd;
         const float s1m = (float)(S1 / (double)m), s2m = (float)(S2 / (double)m);
         cf.a = a;
-        cf.b = -a * s1m;
-        cf.c = -a * s2m / sd;
+        cf.b = bn == 2 ? 0.f : -a * s1m;
+        cf.c = bn == 2 ? 0.f : -a * s2m / sd;
         cf.mu = mean[k];
     } else {
         cf.a = 1.f;
@@ -106,7 +109,7 @@ __global__ void __launch_bounds__(kRedThreads)
                      int N, int K, int PQ, long long m, int pln, int groups, int pieces,
                      float2 *__restrict__ part, unsigned *__restrict__ cnt,
                      float *__restrict__ db, float *__restrict__ dgamma,
-                     Coef *__restrict__ coef, RepackJob job, int nrep) {
+                     Coef *__restrict__ coef, RepackJob job, int nrep, int bn_mode) {
     ptx::griddep_wait();
     const int nred = K * groups * pieces;
     if ((int)blockIdx.x >= nred) {
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kRedThreads)
     }
     if (lane == 0) {
         cnt[k] = 0u;  // ready for the next call
-        finalize_channel(k, S1, S2, m, gamma, mean, var, eps, BN ? 1 : 0, db, dgamma, coef);
+        finalize_channel(k, S1, S2, m, gamma, mean, var, eps, BN ? bn_mode : 0, db, dgamma, coef);
     }
 }
 
@@ -238,11 +241,11 @@ void launch_reduce_t(const Plan &p, const float *delta, const float *output, con
     if (p.PQ % 4 == 0)
         bn_reduce_kernel<ACT, BN, true><<<grid, kRedThreads, 0, st>>>(
             delta, output, z, gamma, mean, var, p.eps, p.N, p.K, p.PQ, p.m, p.red_pln,
-            p.red_groups, p.red_pieces, part, cnt, db, dgamma, coef, job, nrep);
+            p.red_groups, p.red_pieces, part, cnt, db, dgamma, coef, job, nrep, p.bn);
     else
         bn_reduce_kernel<ACT, BN, false><<<grid, kRedThreads, 0, st>>>(
             delta, output, z, gamma, mean, var, p.eps, p.N, p.K, p.PQ, p.m, p.red_pln,
-            p.red_groups, p.red_pieces, part, cnt, db, dgamma, coef, job, nrep);
+            p.red_groups, p.red_pieces, part, cnt, db, dgamma, coef, job, nrep, p.bn);
 }
 
 }  // namespace

@@ -157,6 +157,21 @@ def make_layer(spec, seed, *, batch=None, residual=False, x=None, delta_var=0.01
                 delta=delta, residual=res)
 
 
+def with_frozen_stats(layer, seed):
+    """The same layer call with frozen BN statistics (batch_normalize = 2): the
+    mean is moved by up to half a standard deviation and the variance scaled
+    by 0.5-2, per channel, so that they are not the batch's own.  Random draws
+    only; the other tensors are shared with ``layer``."""
+    if not layer["bn"]:
+        raise ValueError("frozen statistics need a BN layer")
+    rng = np.random.default_rng(seed)
+    K = layer["geom"].K
+    mean = layer["mean"] + rng.uniform(-0.5, 0.5, K) * np.sqrt(layer["var"])
+    var = layer["var"] * rng.uniform(0.5, 2.0, K)
+    return dict(layer, bn=2, mean=mean.astype(np.float32), var=var.astype(np.float32),
+                name=layer["name"] + " (frozen stats)")
+
+
 def make_config(config_id, *, batch=None):
     """The layer call(s) of one workload: a list of input dicts.
 

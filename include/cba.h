@@ -78,7 +78,13 @@ typedef struct {
     int K, R, S;        /* filters, kernel height, kernel width (groups = 1) */
     int stride, pad;    /* the same in both spatial dimensions */
     int act;            /* cba_act_t */
-    int batch_normalize;/* 1: BN in training mode (z, gamma, mean, var, dgamma used) */
+    int batch_normalize;/* 0: no BN.  1: BN in training mode; mean/var are the batch
+                           statistics ("YOLOv3反向传播原理" §4).  2: BN with frozen
+                           statistics; mean/var are constants of the forward, so
+                           the BN-input gradient is gamma * delta' / sqrt(var + eps)
+                           (caffe use_global_stats, "BatchNorm 理解" Backward_cpu);
+                           db and dgamma accumulate as in mode 1.  With BN, z,
+                           gamma, mean, var and dgamma are used. */
     int accumulate;     /* prev_delta: 0 writes, 1 adds onto its contents */
     float eps;          /* BN epsilon inside the square root (1e-5 in darknet) */
     int math;           /* cba_math_t */
@@ -94,8 +100,8 @@ size_t cba_workspace_bytes(const cba_desc_t *d);
  *   z        [N,K,P,Q] pre-BN convolution output (darknet l.x); required iff BN
  *   delta    [N,K,P,Q] gradient at the output; required; NOT modified
  *   W        [K,C,R,S] weights; required
- *   gamma, mean, var [K] BN scale and batch statistics (biased variance);
- *            required iff BN
+ *   gamma, mean, var [K] BN scale and statistics (batch_normalize 1: the
+ *            batch's, biased variance; 2: the frozen ones); required iff BN
  *   residual [N,C,H,W] shortcut delta added into prev_delta; may be NULL
  *   dW       [K,C,R,S] += ; required
  *   db       [K]       += ; required

@@ -59,7 +59,7 @@ def test_workspace_query_for_the_workloads(lib, cid):
 
 
 BAD = [dict(N=0), dict(C=-1), dict(K=0), dict(R=0), dict(stride=0), dict(pad=-1), dict(act=7),
-       dict(math=3), dict(batch_normalize=2), dict(accumulate=5), dict(H=2, R=5, pad=0),
+       dict(math=3), dict(batch_normalize=3), dict(batch_normalize=-1), dict(accumulate=5), dict(H=2, R=5, pad=0),
        dict(eps=float("nan"))]
 
 

@@ -66,6 +66,23 @@ def test_the_in_tree_library_is_loaded(cuda_lib):
 SMALL = [(1, 4), (2, 2), (3, 2), (4, 4), (5, 2)]
 
 
+FROZEN = [(2, 2), (3, 2), (5, 2)]
+
+
+@pytest.mark.parametrize("math", MATHS)
+@pytest.mark.parametrize("cid,batch", FROZEN, ids=[f"cfg{c}_n{b}" for c, b in FROZEN])
+def test_parity_frozen_bn_statistics(ref, cuda_lib, cid, batch, math):
+    # batch_normalize = 2: mean/var are constants of the forward; the BN-input
+    # gradient dz is compared as well (dz_out)
+    for i, layer in enumerate(config_layers(cid, batch)):
+        layer = inputs.with_frozen_stats(layer, 900 + 10 * cid + i)
+        _, got = run_gpu(layer, math, want_dz=True)
+        exp = oracle_chain(ref, layer, want_dz=True)
+        for k in KEYS + ("dz",):
+            if exp.get(k) is not None:
+                assert_close(got[k], exp[k], TOL[math], f"{layer['name']} {k}")
+
+
 @pytest.mark.parametrize("math", MATHS)
 @pytest.mark.parametrize("cid,batch", SMALL, ids=[f"cfg{c}_n{b}" for c, b in SMALL])
 def test_parity_elementwise_reduced_batch(ref, cuda_lib, cid, batch, math):

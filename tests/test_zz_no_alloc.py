@@ -68,6 +68,8 @@ def test_noalloc_matches_the_workspace_entry_point_on_calls_in_a_row(cuda_lib):
     for cid, batch, seed in cases:
         layer = inputs.make_config(cid, batch=batch)[0]
         _check_one(layer, seed)
+    # and with frozen BN statistics (batch_normalize = 2)
+    _check_one(inputs.with_frozen_stats(inputs.make_config(2, batch=2)[0], 15), 16)
 
 
 def test_noalloc_rejects_k_beyond_the_scratch_limit():
