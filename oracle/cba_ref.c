@@ -36,9 +36,21 @@
 #include <omp.h>
 #endif
 
+/* activation codes: the same numbers as the library's cba_act_t */
 #define REF_ACT_LINEAR 0
 #define REF_ACT_LEAKY 1
-#define REF_ACT_LOGISTIC 2 /* only for the oracle's own self-tests */
+#define REF_ACT_LOGISTIC 2
+#define REF_ACT_RELU 3
+#define REF_ACT_RELIE 4
+#define REF_ACT_RAMP 5
+#define REF_ACT_TANH 6
+#define REF_ACT_PLSE 7
+#define REF_ACT_ELU 8
+#define REF_ACT_SELU 9
+#define REF_ACT_LHTAN 10
+#define REF_ACT_HARDTAN 11
+#define REF_ACT_LOGGY 12
+#define REF_ACT_STAIR 13
 
 /* batch_normalize: 0 no BN, 1 training mode (batch statistics), 2 frozen
  * statistics (the given mean/var are constants of the forward) */
@@ -75,14 +87,33 @@ int cba_ref_out_size(int in, int ksize, int stride, int pad) {
 /* ------------------------------------------------------------- activation */
 
 /* Activation derivative evaluated on the activation's OUTPUT value y, as
- * gradient_array does ([YOLO] §3.1 calls gradient_array(l.output, ...)).
- * leaky_gradient: (y>0) ? 1 : .1; linear_gradient: 1; logistic_gradient:
- * (1-y)*y -- [YOLO] §7. */
+ * gradient_array does ([YOLO] §3.1 calls gradient_array(l.output, ...)).  The
+ * *_gradient functions of [YOLO] §7, each as a function of y:
+ *   linear 1; leaky y>0 ? 1 : .1; logistic (1-y)y; relu [y>0];
+ *   relie y>0 ? 1 : .01; ramp [y>0] + .1; tanh 1 - y^2;
+ *   plse y<0 or y>1 ? .01 : .125; elu [y>=0] + [y<0](y+1);
+ *   selu [y>=0] 1.0507 + [y<0](y + 1.0507*1.6732);
+ *   lhtan 0<y<1 ? 1 : .001; hardtan -1<y<1 ? 1 : 0;
+ *   loggy with t = (y+1)/2: 2(1-t)t; stair floor(y) == y ? 0 : 1. */
 double cba_ref_activation_gradient(int act, double y) {
     switch (act) {
     case REF_ACT_LINEAR: return 1.0;
     case REF_ACT_LEAKY: return (y > 0) ? 1.0 : 0.1;
     case REF_ACT_LOGISTIC: return (1.0 - y) * y;
+    case REF_ACT_RELU: return (y > 0) ? 1.0 : 0.0;
+    case REF_ACT_RELIE: return (y > 0) ? 1.0 : 0.01;
+    case REF_ACT_RAMP: return ((y > 0) ? 1.0 : 0.0) + 0.1;
+    case REF_ACT_TANH: return 1.0 - y * y;
+    case REF_ACT_PLSE: return (y < 0 || y > 1) ? 0.01 : 0.125;
+    case REF_ACT_ELU: return (y >= 0) ? 1.0 : y + 1.0;
+    case REF_ACT_SELU: return (y >= 0) ? 1.0507 : y + 1.0507 * 1.6732;
+    case REF_ACT_LHTAN: return (y > 0 && y < 1) ? 1.0 : 0.001;
+    case REF_ACT_HARDTAN: return (y > -1 && y < 1) ? 1.0 : 0.0;
+    case REF_ACT_LOGGY: {
+        const double t = (y + 1.0) / 2.0;
+        return 2.0 * (1.0 - t) * t;
+    }
+    case REF_ACT_STAIR: return (floor(y) == y) ? 0.0 : 1.0;
     default: return NAN;
     }
 }
@@ -371,6 +402,7 @@ int cba_ref_conv_bn_act_backward_f64(int N, int C, int H, int W, int K, int R, i
     if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || K <= 0 || R <= 0 || S <= 0 || stride <= 0 || pad < 0)
         return -1;
     if (batch_normalize < REF_BN_NONE || batch_normalize > REF_BN_FROZEN) return -1;
+    if (act < REF_ACT_LINEAR || act > REF_ACT_STAIR) return -1;
     int P = cba_ref_out_size(H, R, stride, pad), Q = cba_ref_out_size(W, S, stride, pad);
     if (P <= 0 || Q <= 0) return -1;
     if (!x || !delta || !Wt || !dW || !db) return -1;
@@ -456,6 +488,7 @@ int cba_ref_backward_dz(int N, int K, int P, int Q, int act, int batch_normalize
                         double *db, double *dgamma) {
     if (N <= 0 || K <= 0 || P <= 0 || Q <= 0 || !delta || !dz || !db) return -1;
     if (batch_normalize < REF_BN_NONE || batch_normalize > REF_BN_FROZEN) return -1;
+    if (act < REF_ACT_LINEAR || act > REF_ACT_STAIR) return -1;
     if (act != REF_ACT_LINEAR && !output) return -1;
     if (batch_normalize && (!z || !gamma || !mean || !var || !dgamma)) return -1;
     long nout = (long)N * K * P * Q;

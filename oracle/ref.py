@@ -11,9 +11,21 @@ import numpy as np
 
 from . import build as _build
 
+# activation codes (the library's cba_act_t)
 ACT_LINEAR = 0
 ACT_LEAKY = 1
-ACT_LOGISTIC = 2  # oracle self-tests only
+ACT_LOGISTIC = 2
+ACT_RELU = 3
+ACT_RELIE = 4
+ACT_RAMP = 5
+ACT_TANH = 6
+ACT_PLSE = 7
+ACT_ELU = 8
+ACT_SELU = 9
+ACT_LHTAN = 10
+ACT_HARDTAN = 11
+ACT_LOGGY = 12
+ACT_STAIR = 13
 
 BN_NONE = 0
 BN_BATCH = 1     # training mode: batch statistics

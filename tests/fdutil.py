@@ -13,14 +13,49 @@ def conv64(x, w, stride, pad):
                                           stride=stride, padding=pad).numpy()
 
 
+def _stair(v):
+    n = np.floor(v)
+    return np.where(n % 2 == 0, np.floor(v / 2.0), (v - n) + np.floor(v / 2.0))
+
+
+# the forward activations (the *_activate functions of the YOLOv3 back-propagation
+# page, §7), by activation code
+_ACT_FWD = {
+    0: lambda v: v,                                                   # linear
+    1: lambda v: np.where(v > 0, v, 0.1 * v),                         # leaky
+    2: lambda v: 1.0 / (1.0 + np.exp(-v)),                            # logistic
+    3: lambda v: v * (v > 0),                                         # relu
+    4: lambda v: np.where(v > 0, v, 0.01 * v),                        # relie
+    5: lambda v: v * (v > 0) + 0.1 * v,                               # ramp
+    6: lambda v: (np.exp(2 * v) - 1) / (np.exp(2 * v) + 1),           # tanh
+    7: lambda v: np.where(v < -4, 0.01 * (v + 4),
+                          np.where(v > 4, 0.01 * (v - 4) + 1, 0.125 * v + 0.5)),   # plse
+    8: lambda v: (v >= 0) * v + (v < 0) * (np.exp(v) - 1),            # elu
+    9: lambda v: (v >= 0) * 1.0507 * v + (v < 0) * 1.0507 * 1.6732 * (np.exp(v) - 1),  # selu
+    10: lambda v: np.where(v < 0, 0.001 * v, np.where(v > 1, 0.001 * (v - 1) + 1, v)),  # lhtan
+    11: lambda v: np.clip(v, -1.0, 1.0),                              # hardtan
+    12: lambda v: 2.0 / (1.0 + np.exp(-v)) - 1,                       # loggy
+    13: _stair,                                                       # stair
+}
+
+# where each forward is not differentiable
+ACT_KINKS = {1: [0.0], 3: [0.0], 4: [0.0], 5: [0.0], 7: [-4.0, 4.0], 8: [0.0], 9: [0.0],
+             10: [0.0, 1.0], 11: [-1.0, 1.0], 13: "integers"}
+
+
 def act_fwd(act, v):
-    if act == 0:
-        return v
-    if act == 1:
-        return np.where(v > 0, v, 0.1 * v)
-    if act == 2:
-        return 1.0 / (1.0 + np.exp(-v))
-    raise ValueError(act)
+    return _ACT_FWD[act](np.asarray(v, np.float64))
+
+
+def min_kink_distance(act, v):
+    """Distance of each pre-activation value from the activation's kinks."""
+    v = np.asarray(v, np.float64)
+    k = ACT_KINKS.get(act)
+    if k is None:
+        return np.full(v.shape, np.inf)
+    if k == "integers":
+        return np.abs(v - np.round(v))
+    return np.min(np.abs(v[..., None] - np.asarray(k)), axis=-1)
 
 
 def layer_forward(x, w, gamma, beta, *, stride, pad, act, bn, eps, stats=None):

@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.fdutil import central_diff, layer_forward
+from tests.fdutil import act_fwd, central_diff, layer_forward, min_kink_distance
 
 EPS = 1e-5
 
@@ -186,6 +186,64 @@ def test_frozen_stats_chain_matches_finite_differences(ref, case):
                                    act=act, batch_normalize=1, accumulate=0, eps=EPS,
                                    f64_inputs=True)
     assert np.max(np.abs(trn["dW"] - got["dW"])) > 1e-3 * np.max(np.abs(got["dW"]))
+
+
+@pytest.mark.parametrize("act", range(14))
+def test_activation_gradient_matches_fd_of_the_forward(ref, act):
+    """Each activation's gradient, a function of the output y, against the
+    central difference of the printed forward at the same pre-activation."""
+    x = np.linspace(-6.0, 6.0, 1201) + 0.0037
+    x = x[min_kink_distance(act, x) > 1e-3]
+    h = 1e-6
+    fd = (act_fwd(act, x + h) - act_fwd(act, x - h)) / (2 * h)
+    y = act_fwd(act, x)
+    got = np.array([ref.activation_gradient(act, v) for v in y])
+    assert np.max(np.abs(got - fd)) < 2e-6, np.max(np.abs(got - fd))
+
+
+ACT_CHAIN_CASES = [
+    # N, C, H, W, K, R, S, stride, pad, act, bn, residual
+    (2, 3, 5, 5, 4, 3, 3, 1, 1, 2, True, False),   # logistic
+    (2, 3, 6, 5, 4, 3, 3, 2, 1, 6, False, True),   # tanh
+    (2, 3, 5, 5, 3, 3, 3, 1, 1, 8, True, True),    # elu
+    (3, 4, 4, 4, 3, 1, 1, 1, 0, 9, False, False),  # selu
+    (2, 3, 5, 5, 4, 3, 3, 1, 1, 7, True, False),   # plse
+]
+
+
+@pytest.mark.parametrize("case", ACT_CHAIN_CASES, ids=[str(c[9]) for c in ACT_CHAIN_CASES])
+def test_chain_with_other_activations_matches_finite_differences(ref, case):
+    N, C, H, W, K, R, S, st, pad, act, bn, res = case
+    for attempt in range(50):
+        x, w, gamma, beta, D, Dres = _draw_case(case[:9] + (0, bn, res),
+                                                600 + 100 * ACT_CHAIN_CASES.index(case) + attempt)
+        kw = dict(stride=st, pad=pad, act=act, bn=bn, eps=EPS)
+        z, mean, var, pre, out = layer_forward(x, w, gamma, beta, **kw)
+        if np.min(min_kink_distance(act, pre)) > 5e-3:
+            break
+    else:
+        raise RuntimeError("no draw clear of the kinks")
+
+    def loss(xv=x, wv=w, gv=gamma, bv=beta):
+        L = float(np.sum(D * layer_forward(xv, wv, gv, bv, **kw)[4]))
+        if Dres is not None:
+            L += float(np.sum(Dres * xv))
+        return L
+
+    got = ref.conv_bn_act_backward(x, out, z if bn else None, D, w, gamma if bn else None,
+                                   mean, var, Dres, stride=st, pad=pad, act=act,
+                                   batch_normalize=int(bn), accumulate=0, eps=EPS,
+                                   f64_inputs=True)
+
+    def close(a, b, tol=2e-6):
+        scale = max(np.max(np.abs(b)), 1e-12)
+        assert np.max(np.abs(a - b)) <= tol * scale, (np.max(np.abs(a - b)), scale)
+
+    close(got["prev_delta"], central_diff(lambda v: loss(xv=v), x))
+    close(got["dW"], central_diff(lambda v: loss(wv=v), w))
+    close(got["db"], central_diff(lambda v: loss(bv=v), beta))
+    if bn:
+        close(got["dgamma"], central_diff(lambda v: loss(gv=v), gamma))
 
 
 # ------------------------------------- convolution gradients, other forms
