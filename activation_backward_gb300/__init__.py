@@ -7,7 +7,10 @@ hand-written CUDA for GB300 (sm_103a), behind a C ABI (``include/cba.h``).
 the device-side convenience wrapper; ``inputs`` generates seeded synthetic
 workloads.  The CUDA library is loaded lazily; nothing falls back to the CPU.
 """
-from ._binding import (CBA_ACT_LEAKY, CBA_ACT_LINEAR, CBA_ERR_ALIGN, CBA_ERR_ARG,  # noqa: F401
+from ._binding import (ACT_NAMES, CBA_ACT_ELU, CBA_ACT_HARDTAN, CBA_ACT_LEAKY,  # noqa: F401
+                       CBA_ACT_LHTAN, CBA_ACT_LINEAR, CBA_ACT_LOGGY, CBA_ACT_LOGISTIC,
+                       CBA_ACT_PLSE, CBA_ACT_RAMP, CBA_ACT_RELIE, CBA_ACT_RELU, CBA_ACT_SELU,
+                       CBA_ACT_STAIR, CBA_ACT_TANH, CBA_ERR_ALIGN, CBA_ERR_ARG,
                        CBA_ERR_CUDA, CBA_ERR_DEVICE_TIMEOUT, CBA_ERR_SCRATCH_LIMIT,
                        CBA_ERR_UNSUPPORTED, CBA_ERR_WORKSPACE, CBA_MATH_FFMA, CBA_MATH_TF32,
                        CBA_NOALLOC_MAX_K, CBA_OK, CbaError, cba_bn_act_backward_noalloc,

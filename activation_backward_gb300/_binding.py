@@ -24,6 +24,23 @@ CBA_NOALLOC_MAX_K = 16384
 
 CBA_ACT_LINEAR = 0
 CBA_ACT_LEAKY = 1
+CBA_ACT_LOGISTIC = 2
+CBA_ACT_RELU = 3
+CBA_ACT_RELIE = 4
+CBA_ACT_RAMP = 5
+CBA_ACT_TANH = 6
+CBA_ACT_PLSE = 7
+CBA_ACT_ELU = 8
+CBA_ACT_SELU = 9
+CBA_ACT_LHTAN = 10
+CBA_ACT_HARDTAN = 11
+CBA_ACT_LOGGY = 12
+CBA_ACT_STAIR = 13
+ACT_NAMES = {CBA_ACT_LINEAR: "linear", CBA_ACT_LEAKY: "leaky", CBA_ACT_LOGISTIC: "logistic",
+             CBA_ACT_RELU: "relu", CBA_ACT_RELIE: "relie", CBA_ACT_RAMP: "ramp",
+             CBA_ACT_TANH: "tanh", CBA_ACT_PLSE: "plse", CBA_ACT_ELU: "elu",
+             CBA_ACT_SELU: "selu", CBA_ACT_LHTAN: "lhtan", CBA_ACT_HARDTAN: "hardtan",
+             CBA_ACT_LOGGY: "loggy", CBA_ACT_STAIR: "stair"}
 CBA_MATH_TF32 = 0
 CBA_MATH_FFMA = 1
 

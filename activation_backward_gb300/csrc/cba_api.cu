@@ -44,7 +44,7 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     if (d->N <= 0 || d->C <= 0 || d->H <= 0 || d->W <= 0 || d->K <= 0 || d->R <= 0 ||
         d->S <= 0 || d->stride <= 0 || d->pad < 0)
         return CBA_ERR_ARG;
-    if (d->act != CBA_ACT_LINEAR && d->act != CBA_ACT_LEAKY) return CBA_ERR_ARG;
+    if (d->act < CBA_ACT_LINEAR || d->act > CBA_ACT_STAIR) return CBA_ERR_ARG;
     if (d->math != CBA_MATH_TF32 && d->math != CBA_MATH_FFMA) return CBA_ERR_ARG;
     if (d->batch_normalize < 0 || d->batch_normalize > 2) return CBA_ERR_ARG;
     if (d->accumulate != 0 && d->accumulate != 1) return CBA_ERR_ARG;
@@ -64,7 +64,10 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->stride = d->stride; p->pad = d->pad; p->P = (int)P; p->Q = (int)Q;
     p->PQ = (int)(P * Q); p->HW = d->H * d->W; p->RS = d->R * d->S; p->CRS = d->C * p->RS;
     p->m = (long long)d->N * P * Q;
-    p->act = d->act; p->bn = d->batch_normalize; p->accumulate = d->accumulate;
+    p->act_in = d->act;
+    p->act_pre = d->act != CBA_ACT_LINEAR && d->act != CBA_ACT_LEAKY;
+    p->act = p->act_pre ? CBA_ACT_LINEAR : d->act;
+    p->bn = d->batch_normalize; p->accumulate = d->accumulate;
     p->math = d->math; p->eps = d->eps;
     p->num_sms = kNumSMs;
 
@@ -104,6 +107,8 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     if (p->use_tc2) off = align_up(off + tc2_dzt_bytes(*p), 256);
     p->off_wr = off;
     if (p->use_tc2) off = align_up(off + tc2_wr_bytes(*p), 256);
+    p->off_dprime = off;
+    if (p->act_pre) off = align_up(off + sizeof(float) * (size_t)nout, 256);
     p->total = off;
     return CBA_OK;
 }
@@ -182,7 +187,7 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     int rc = make_plan(d, &p);
     if (rc != CBA_OK) return rc;
     if (!x || !delta || !Wt || !dW || !db) return CBA_ERR_ARG;
-    if (p.act != CBA_ACT_LINEAR && !output) return CBA_ERR_ARG;
+    if (p.act_in != CBA_ACT_LINEAR && !output) return CBA_ERR_ARG;
     if (p.bn && (!z || !gamma || !mean || !var || !dgamma)) return CBA_ERR_ARG;
     const void *ptrs[] = {x, output, z, delta, Wt, gamma, mean, var, residual,
                           dW, db, dgamma, prev_delta, dz_out};
@@ -199,6 +204,13 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     if (e != cudaSuccess) return fail_cuda(e);
     e = cudaMemsetAsync(workspace, 0, p.clear_bytes, st);  // status word, reduction counters
     if (e == cudaSuccess) e = tr.mark(0);
+    if (e == cudaSuccess && p.act_pre) {
+        // activations other than linear and leaky: delta' first, then the main
+        // kernels run in linear mode on it
+        float *dprime = ws_at<float>(workspace, p.off_dprime);
+        e = launch_gradient_array(p, delta, output, dprime, st, &n_launch);
+        delta = dprime;
+    }
     // the tensor-core input gradient reads repacked weights: written by extra
     // blocks of the reduction pass
     const bool repack = p.use_tc2 && prev_delta != nullptr;

@@ -29,7 +29,10 @@ struct Plan {
     int N, C, H, W, K, R, S, stride, pad, P, Q;
     int PQ, HW, RS, CRS;
     long long m;  // N*P*Q: elements per output channel
-    int act, accumulate, math;
+    int act, accumulate, math;  // act: the activation the main kernels apply
+    int act_in;   // the descriptor's activation (cba_act_t)
+    bool act_pre; // act_in is neither LINEAR nor LEAKY: a gradient_array pass writes
+                  // delta * f'(output) to off_dprime and the main kernels run LINEAR
     int bn;  // 0 no BN, 1 batch statistics, 2 frozen statistics
     float eps;
     int num_sms;
@@ -50,7 +53,7 @@ struct Plan {
     // off_cnt: per-channel arrival counters of the reduction (zeroed with the
     // status word at the start of every call; clear_bytes covers both)
     size_t off_status, off_cnt, clear_bytes, off_red, off_coef, off_wgpart, off_wt, off_dzt,
-        off_wr, total;
+        off_wr, off_dprime, total;
 };
 
 // Builds the plan; returns CBA_OK or a CBA_ERR_* code.
@@ -66,8 +69,13 @@ cudaError_t launch_reduce(const Plan &p, const float *delta, const float *output
                           const float *gamma, const float *mean, const float *var, float *db,
                           float *dgamma, void *ws, cudaStream_t st, int *launches,
                           const float *repack_W = nullptr, float *repack_wr = nullptr);
+// dz_out may be the delta buffer itself (an in-place transform).
 cudaError_t launch_dz_out(const Plan &p, const float *delta, const float *output, const float *z,
                           const void *ws, float *dz_out, cudaStream_t st);
+// gradient_array for the activations other than LINEAR and LEAKY (p.act_in):
+// dprime[i] = delta[i] * f'(output[i]).  dprime may be the delta buffer.
+cudaError_t launch_gradient_array(const Plan &p, const float *delta, const float *output,
+                                  float *dprime, cudaStream_t st, int *launches);
 cudaError_t launch_wgrad_simt(const Plan &p, const float *x, const float *delta,
                               const float *output, const float *z, float *dW, void *ws,
                               cudaStream_t st, int *launches);

@@ -102,7 +102,9 @@ extern "C" int cba_bn_act_backward_noalloc(const cba_desc_t *d, const float *out
     int rc = make_plan(d, &p);
     if (rc != CBA_OK) return rc;
     if (!delta || !db) return CBA_ERR_ARG;
-    if (p.act != CBA_ACT_LINEAR && !output) return CBA_ERR_ARG;
+    if (p.act_in != CBA_ACT_LINEAR && !output) return CBA_ERR_ARG;
+    // activations other than linear and leaky need a buffer for delta': dz_out
+    if (p.act_pre && !dz_out) return CBA_ERR_UNSUPPORTED;
     if (p.bn && (!z || !gamma || !mean || !var || !dgamma)) return CBA_ERR_ARG;
     const void *ptrs[] = {output, z, delta, gamma, mean, var, db, dgamma, dz_out};
     for (const void *q : ptrs)
@@ -132,6 +134,12 @@ extern "C" int cba_bn_act_backward_noalloc(const cba_desc_t *d, const float *out
     if (e != cudaSuccess) return report_cuda_error(e);
     int n_launch = 0;
     e = cudaMemsetAsync(scratch, 0, cnt_bytes, st);  // the reduction's arrival counters
+    if (e == cudaSuccess && p.act_pre) {
+        // delta' into dz_out; the reduction reads it and the dz pass then
+        // transforms it in place
+        e = launch_gradient_array(p, delta, output, dz_out, st, &n_launch);
+        delta = dz_out;
+    }
     if (e == cudaSuccess)
         e = launch_reduce(p, delta, output, z, gamma, mean, var, db, dgamma, scratch, st,
                           &n_launch);

@@ -219,9 +219,9 @@ __global__ void __launch_bounds__(kRedThreads)
 }
 
 template <int ACT, bool BN>
-__global__ void dz_out_kernel(const float *__restrict__ delta, const float *__restrict__ output,
+__global__ void dz_out_kernel(const float *delta, const float *__restrict__ output,
                               const float *__restrict__ z, const Coef *__restrict__ coef, int K,
-                              int PQ, long long total, float *__restrict__ out) {
+                              int PQ, long long total, float *out) {  // out may be delta
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const int k = (int)((i / PQ) % K);
@@ -275,6 +275,56 @@ cudaError_t launch_reduce(const Plan &p, const float *delta, const float *output
         else CBA_RED(CBA_ACT_LINEAR, false);
     }
 #undef CBA_RED
+    *launches += 1;
+    return cudaGetLastError();
+}
+
+// The activation derivative on the output y for the activations other than
+// LINEAR and LEAKY: the *_gradient functions of "YOLOv3反向传播原理" §7.
+__device__ __forceinline__ float act_grad_other(int act, float y) {
+    switch (act) {
+    case CBA_ACT_LOGISTIC: return (1.f - y) * y;
+    case CBA_ACT_RELU: return y > 0.f ? 1.f : 0.f;
+    case CBA_ACT_RELIE: return y > 0.f ? 1.f : 0.01f;
+    case CBA_ACT_RAMP: return (y > 0.f ? 1.f : 0.f) + 0.1f;
+    case CBA_ACT_TANH: return 1.f - y * y;
+    case CBA_ACT_PLSE: return (y < 0.f || y > 1.f) ? 0.01f : 0.125f;
+    case CBA_ACT_ELU: return y >= 0.f ? 1.f : y + 1.f;
+    case CBA_ACT_SELU: return y >= 0.f ? 1.0507f : y + 1.0507f * 1.6732f;
+    case CBA_ACT_LHTAN: return (y > 0.f && y < 1.f) ? 1.f : 0.001f;
+    case CBA_ACT_HARDTAN: return (y > -1.f && y < 1.f) ? 1.f : 0.f;
+    case CBA_ACT_LOGGY: {
+        const float t = (y + 1.f) * 0.5f;
+        return 2.f * (1.f - t) * t;
+    }
+    case CBA_ACT_STAIR: return floorf(y) == y ? 0.f : 1.f;
+    default: return 1.f;
+    }
+}
+
+// gradient_array of backward_convolutional_layer ("YOLOv3反向传播原理" §3.1):
+// dprime = delta * f'(output), 16-byte accesses (n4 of them) and a scalar tail.
+__global__ void gradient_array_kernel(const float *delta, const float *__restrict__ output,
+                                      float *dprime, long long n, int act) {  // dprime may be delta
+    const long long n4 = n / 4;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += stride) {
+        const float4 d = reinterpret_cast<const float4 *>(delta)[i];
+        const float4 y = __ldg(reinterpret_cast<const float4 *>(output) + i);
+        reinterpret_cast<float4 *>(dprime)[i] =
+            make_float4(d.x * act_grad_other(act, y.x), d.y * act_grad_other(act, y.y),
+                        d.z * act_grad_other(act, y.z), d.w * act_grad_other(act, y.w));
+    }
+    for (long long i = 4 * n4 + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += stride)
+        dprime[i] = delta[i] * act_grad_other(act, __ldg(output + i));
+}
+
+cudaError_t launch_gradient_array(const Plan &p, const float *delta, const float *output,
+                                  float *dprime, cudaStream_t st, int *launches) {
+    const long long n = (long long)p.N * p.K * p.PQ;
+    const long long blocks = std::min<long long>((n / 4 + 255) / 256 + 1, (long long)p.num_sms * 8);
+    gradient_array_kernel<<<(unsigned)blocks, 256, 0, st>>>(delta, output, dprime, n, p.act_in);
     *launches += 1;
     return cudaGetLastError();
 }

@@ -157,6 +157,59 @@ def make_layer(spec, seed, *, batch=None, residual=False, x=None, delta_var=0.01
                 delta=delta, residual=res)
 
 
+def _act_forward(act, v):
+    """The forward activations (the *_activate functions of the YOLOv3
+    back-propagation page, §7), float64, by activation code."""
+    if act == 0:
+        return v
+    if act == 1:
+        return _leaky(v)
+    if act == 2:
+        return 1.0 / (1.0 + np.exp(-v))
+    if act == 3:
+        return v * (v > 0)
+    if act == 4:
+        return np.where(v > 0, v, 0.01 * v)
+    if act == 5:
+        return v * (v > 0) + 0.1 * v
+    if act == 6:
+        return np.tanh(v)
+    if act == 7:
+        return np.where(v < -4, 0.01 * (v + 4), np.where(v > 4, 0.01 * (v - 4) + 1, 0.125 * v + 0.5))
+    if act == 8:
+        return np.where(v >= 0, v, np.expm1(np.minimum(v, 0)))
+    if act == 9:
+        return np.where(v >= 0, 1.0507 * v, 1.0507 * 1.6732 * np.expm1(np.minimum(v, 0)))
+    if act == 10:
+        return np.where(v < 0, 0.001 * v, np.where(v > 1, 0.001 * (v - 1) + 1, v))
+    if act == 11:
+        return np.clip(v, -1.0, 1.0)
+    if act == 12:
+        return 2.0 / (1.0 + np.exp(-v)) - 1
+    if act == 13:
+        n = np.floor(v)
+        return np.where(n % 2 == 0, np.floor(v / 2.0), (v - n) + np.floor(v / 2.0))
+    raise ValueError(f"unknown activation {act}")
+
+
+def with_activation(layer, act):
+    """The same layer call with another activation: ``output`` is recomputed as
+    act(pre-activation).  The pre-activation is gamma * (z - mean) / sqrt(var +
+    eps) for BN layers (beta = 0, as in make_layer), and is recovered from the
+    linear or leaky output of a layer without BN."""
+    if layer["bn"]:
+        z = layer["z"].astype(np.float64)
+        m = layer["mean"].astype(np.float64)[None, :, None, None]
+        v = layer["var"].astype(np.float64)[None, :, None, None]
+        pre = layer["gamma"].astype(np.float64)[None, :, None, None] * (z - m) / np.sqrt(
+            v + np.float64(np.float32(layer["eps"])))
+    else:
+        y = layer["output"].astype(np.float64)
+        pre = np.where(y > 0, y, y / 0.1) if layer["act"] == ACT_LEAKY else y
+    out = _act_forward(int(act), pre).astype(np.float32)
+    return dict(layer, act=int(act), output=out, name=f"{layer['name']} (act {int(act)})")
+
+
 def with_frozen_stats(layer, seed):
     """The same layer call with frozen BN statistics (batch_normalize = 2): the
     mean is moved by up to half a standard deviation and the variance scaled

@@ -50,6 +50,13 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2, help="workload 1-5 (default 2)")
     ap.add_argument("--math", default="tf32", choices=["tf32", "ffma"])
+    ap.add_argument("--act", default=None,
+                    choices=["linear", "leaky", "logistic", "relu", "relie", "ramp", "tanh",
+                             "plse", "elu", "selu", "lhtan", "hardtan", "loggy", "stair"],
+                    help="replace the workload's activation (outputs recomputed)")
+    ap.add_argument("--bn", default="batch", choices=["batch", "frozen"],
+                    help="BN statistics of the workload's BN layers: the batch's own "
+                         "(training mode, default) or frozen ones (batch_normalize = 2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -212,7 +219,7 @@ def run_reference(args):
         return
     import oracle
     from activation_backward_gb300 import inputs
-    layers = inputs.make_config(args.config)
+    layers = workload_layers(args)
     total = args.steps + args.warmup
     budget = 150.0 / max(total, 1)  # ~2.5 minutes for the whole run
     n_img, k_sub = pick_sample(layers, budget)
@@ -261,13 +268,29 @@ def profiled_traffic(phase):
     return None
 
 
+def workload_layers(args):
+    """The layer calls of the workload; with --bn frozen, every BN layer gets
+    frozen statistics (inputs.with_frozen_stats)."""
+    from activation_backward_gb300 import ACT_NAMES, inputs
+    layers = inputs.make_config(args.config)
+    if getattr(args, "act", None):
+        code = {v: k for k, v in ACT_NAMES.items()}[args.act]
+        layers = [inputs.with_activation(l, code) for l in layers]
+    if args.bn == "frozen":
+        layers = [inputs.with_frozen_stats(l, 700 + i) if l["bn"] else l
+                  for i, l in enumerate(layers)]
+    return layers
+
+
 def config_dict(args, layers, ws):
+    from activation_backward_gb300 import ACT_NAMES
     g = layers[0]["geom"]
     flops = sum(2 * l["geom"].gemm_flops() for l in layers)
     return {"workload": layers[0]["name"] if args.config != 5 else "residual_block",
             "N": g.N, "C": g.C, "H": g.H, "W": g.W, "K": g.K, "R": g.R, "S": g.S,
-            "stride": g.stride, "pad": g.pad, "bn": bool(layers[0]["bn"]),
-            "act": "leaky" if layers[0]["act"] == 1 else "linear",
+            "stride": g.stride, "pad": g.pad,
+            "bn": {0: False, 1: "batch statistics", 2: "frozen statistics"}[int(layers[0]["bn"])],
+            "act": ACT_NAMES[int(layers[0]["act"])],
             "gemm_gflop_per_step": flops / 1e9,
             "l2": "flushed before every step, outside the timing: 512 MiB write, then a 256 MiB "
                   "read sweep so no dirty flush lines are written back inside the step",
@@ -293,7 +316,7 @@ def run_ours(args):
     math = cba.CBA_MATH_TF32 if args.math == "tf32" else cba.CBA_MATH_FFMA
     cba.load()
 
-    layers = inputs.make_config(args.config)
+    layers = workload_layers(args)
     dls = [DeviceLayer(l, math=math, device=dev) for l in layers]
     flops = sum(2 * l["geom"].gemm_flops() for l in layers)
     red_bytes = sum(inputs.layer_bytes_reduce(l) for l in layers)

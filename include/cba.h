@@ -65,7 +65,23 @@ extern "C" {
 #define CBA_ERR_DEVICE_TIMEOUT (-6) /* reported by cba_get_status: a device wait ran out */
 #define CBA_ERR_SCRATCH_LIMIT (-7)  /* cba_bn_act_backward_noalloc: K > CBA_NOALLOC_MAX_K */
 
-typedef enum { CBA_ACT_LINEAR = 0, CBA_ACT_LEAKY = 1 } cba_act_t;
+/* Activation of the layer; its gradient is evaluated on the output y, as the
+ * *_gradient functions of "YOLOv3反向传播原理" §7 are (gradient_array, §3.1):
+ *   LINEAR 1              LEAKY   y>0 ? 1 : .1       LOGISTIC (1-y)y
+ *   RELU   [y>0]          RELIE   y>0 ? 1 : .01      RAMP     [y>0] + .1
+ *   TANH   1 - y^2        PLSE    y<0 or y>1 ? .01 : .125
+ *   ELU    [y>=0] + [y<0](y+1)    SELU [y>=0] 1.0507 + [y<0](y + 1.0507*1.6732)
+ *   LHTAN  0<y<1 ? 1 : .001       HARDTAN -1<y<1 ? 1 : 0
+ *   LOGGY  2(1-t)t, t = (y+1)/2   STAIR floor(y) == y ? 0 : 1
+ * LINEAR and LEAKY are applied inside the reduction and GEMM operand passes;
+ * the others by one extra elementwise pass that writes delta * f'(y) into the
+ * workspace (cba_workspace_bytes counts it). */
+typedef enum {
+    CBA_ACT_LINEAR = 0, CBA_ACT_LEAKY = 1, CBA_ACT_LOGISTIC = 2, CBA_ACT_RELU = 3,
+    CBA_ACT_RELIE = 4, CBA_ACT_RAMP = 5, CBA_ACT_TANH = 6, CBA_ACT_PLSE = 7, CBA_ACT_ELU = 8,
+    CBA_ACT_SELU = 9, CBA_ACT_LHTAN = 10, CBA_ACT_HARDTAN = 11, CBA_ACT_LOGGY = 12,
+    CBA_ACT_STAIR = 13
+} cba_act_t;
 
 /* Arithmetic of the two convolution GEMMs.  TF32: tensor cores (tcgen05,
  * inputs read as TF32, fp32 accumulation).  FFMA: fp32 fused multiply-add on

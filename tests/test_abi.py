@@ -58,7 +58,7 @@ def test_workspace_query_for_the_workloads(lib, cid):
             assert n < 1 << 30  # bounded scratch
 
 
-BAD = [dict(N=0), dict(C=-1), dict(K=0), dict(R=0), dict(stride=0), dict(pad=-1), dict(act=7),
+BAD = [dict(N=0), dict(C=-1), dict(K=0), dict(R=0), dict(stride=0), dict(pad=-1), dict(act=14),
        dict(math=3), dict(batch_normalize=3), dict(batch_normalize=-1), dict(accumulate=5), dict(H=2, R=5, pad=0),
        dict(eps=float("nan"))]
 

@@ -66,6 +66,22 @@ def test_the_in_tree_library_is_loaded(cuda_lib):
 SMALL = [(1, 4), (2, 2), (3, 2), (4, 4), (5, 2)]
 
 
+OTHER_ACTS = list(range(2, 14))
+
+
+@pytest.mark.parametrize("act", OTHER_ACTS, ids=[cba.ACT_NAMES[a] for a in OTHER_ACTS])
+def test_parity_other_activations(ref, cuda_lib, act):
+    # activations other than linear and leaky (a gradient_array pass, then the
+    # main kernels in linear mode): a BN layer in TF32, a layer without BN in FFMA
+    for cid, batch, math in ((2, 1, TF32), (1, 4, FFMA)):
+        layer = inputs.with_activation(config_layers(cid, batch)[0], act)
+        _, got = run_gpu(layer, math, want_dz=True)
+        exp = oracle_chain(ref, layer, want_dz=True)
+        for k in KEYS + ("dz",):
+            if exp.get(k) is not None:
+                assert_close(got[k], exp[k], TOL[math], f"{layer['name']} {k}")
+
+
 FROZEN = [(2, 2), (3, 2), (5, 2)]
 
 

@@ -70,6 +70,9 @@ def test_noalloc_matches_the_workspace_entry_point_on_calls_in_a_row(cuda_lib):
         _check_one(layer, seed)
     # and with frozen BN statistics (batch_normalize = 2)
     _check_one(inputs.with_frozen_stats(inputs.make_config(2, batch=2)[0], 15), 16)
+    # and with an activation the gradient_array pass handles (delta' goes
+    # through dz, which is then transformed in place)
+    _check_one(inputs.with_activation(inputs.make_config(2, batch=2)[0], cba.CBA_ACT_ELU), 17)
 
 
 def test_noalloc_rejects_k_beyond_the_scratch_limit():
@@ -89,3 +92,15 @@ def test_noalloc_rejects_k_beyond_the_scratch_limit():
     rc = L.cba_bn_act_backward_noalloc(ctypes.byref(d_ok), *([fake] * 2), None, *([fake] * 6),
                                         None)
     assert rc == cba.CBA_ERR_ARG
+
+
+def test_noalloc_needs_dz_for_other_activations():
+    """Activations other than linear and leaky keep delta' in dz_out: without
+    it the call returns CBA_ERR_UNSUPPORTED before any CUDA call."""
+    from activation_backward_gb300 import build
+    build.build()
+    L = B.load()
+    d = cba.make_desc(1, 2, 4, 4, 8, 1, 1, act=cba.CBA_ACT_TANH, batch_normalize=1)
+    fake = 1 << 20  # aligned, never dereferenced
+    rc = L.cba_bn_act_backward_noalloc(ctypes.byref(d), *([fake] * 8), None, None)
+    assert rc == cba.CBA_ERR_UNSUPPORTED
