@@ -259,3 +259,47 @@ def layer_bytes_reduce(layer):
     m = g.N * g.K * g.P * g.Q
     n = 1 + (1 if layer["act"] == ACT_LEAKY else 0) + (1 if layer["bn"] else 0)
     return 4 * m * n
+
+
+# ------------------------------------------------ adjacent data-movement layers
+
+def pooled_size(n, k, stride, pad):
+    """caffe PoolingLayer output size: ceil((n + 2 pad - k) / stride) + 1, one
+    less when the last window would start in the bottom padding."""
+    out = -(-(n + 2 * pad - k) // stride) + 1
+    if pad > 0 and (out - 1) * stride >= n + pad:
+        out -= 1
+    return out
+
+
+def make_pool_case(N, C, H, W, k, stride, pad, seed):
+    """Inputs of a max-pooling backward: the forward's mask (flat index h * W + w
+    of each window's first maximum in scan order, as caffe's forward records it)
+    from a seeded bottom of distinct values, and a seeded top gradient."""
+    rng = np.random.default_rng(seed)
+    bottom = rng.permutation(N * C * H * W).reshape(N, C, H, W).astype(np.float64)
+    bottom = (bottom / bottom.size - 0.5).astype(np.float32)
+    PH, PW = pooled_size(H, k, stride, pad), pooled_size(W, k, stride, pad)
+    mask = np.empty((N, C, PH, PW), np.int32)
+    for ph in range(PH):
+        h0, h1 = max(ph * stride - pad, 0), min(ph * stride - pad + k, H)
+        for pw in range(PW):
+            w0, w1 = max(pw * stride - pad, 0), min(pw * stride - pad + k, W)
+            win = bottom[:, :, h0:h1, w0:w1].reshape(N, C, -1)
+            a = np.argmax(win, axis=2)  # first maximum in scan order
+            mask[:, :, ph, pw] = (h0 + a // (w1 - w0)) * W + (w0 + a % (w1 - w0))
+    top_diff = (rng.standard_normal((N, C, PH, PW)) * 0.1).astype(np.float32)
+    return dict(N=N, C=C, H=H, W=W, k=k, stride=stride, pad=pad, PH=PH, PW=PW,
+                bottom=bottom, mask=mask, top_diff=top_diff)
+
+
+def make_route_case(batch, input_sizes, seed):
+    """Inputs of a route-layer backward: the route delta [batch, sum(sizes)] and
+    the input layers' deltas [batch, size_i] the backward adds onto."""
+    rng = np.random.default_rng(seed)
+    outputs = int(sum(input_sizes))
+    route_delta = (rng.standard_normal((batch, outputs)) * 0.1).astype(np.float32)
+    deltas = [(rng.standard_normal((batch, int(s))) * 0.1).astype(np.float32)
+              for s in input_sizes]
+    return dict(batch=batch, input_sizes=[int(s) for s in input_sizes],
+                route_delta=route_delta, input_deltas=deltas)

@@ -4,7 +4,9 @@
  *
  *   activation gradient -> batch-norm backward (bias, scale, mean_delta,
  *   variance_delta, normalize_delta) -> weight gradient -> input gradient
- *   -> shortcut-delta add.
+ *   -> shortcut-delta add;
+ * and the backward of three adjacent data-movement layers: the YOLO layer's
+ * delta copy, the route layer's split of its delta, max pooling's scatter.
  *
  * TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the bench's
  * CPU-baseline leg load this library; the product (the CUDA library) never
@@ -18,9 +20,11 @@
  *   [YOLO]  "YOLOv3反向传播原理 之 全流程源码分析" (YOLOv3 back-propagation,
  *           full-flow source analysis): §1.1 initialisation, §3.1
  *           backward_convolutional_layer, §3.2 im2col_cpu / col2im_cpu / gemm,
- *           §4 batch_normalize backward, §5 shortcut layer, §7 activations.
+ *           §4 batch_normalize backward, §5 shortcut layer, §6 route layer,
+ *           §7 activations; §2 the YOLO layer.
  *   [LENET] "【caffe源码研究】第四章：完整案例源码篇(5)：LeNet反向过程"
- *           (caffe LeNet backward): 第四层 Convolution, 第七层 ReLU.
+ *           (caffe LeNet backward): 第四层 Convolution, 第五层 Pooling,
+ *           第七层 ReLU.
  *   [BNU]   "BatchNorm 理解" (understanding BatchNorm): BatchNormLayer
  *           Forward_cpu / Backward_cpu.
  *
@@ -513,6 +517,64 @@ int cba_ref_backward_dz(int N, int K, int P, int Q, int act, int batch_normalize
     }
     free(zz); free(g); free(m); free(v); free(xn);
     return rc;
+}
+
+/* -------------------------------------------- adjacent data-movement layers */
+
+/* backward_yolo_layer ([YOLO] §2): the YOLO layer's delta goes to the previous
+ * layer's delta with one axpy of factor 1 over batch * inputs elements. */
+void cba_ref_yolo_backward(const double *l_delta, long n, double *net_delta) {
+    cba_ref_axpy(n, 1.0, l_delta, net_delta);
+}
+
+/* backward_route_layer ([YOLO] §6): the route layer's output is its inputs laid
+ * one after the other per image (outputs = sum of input_sizes values per image).
+ * For input i and image j, input_sizes[i] values at offset_i + j * outputs of
+ * the route delta are added onto input i's delta at j * input_sizes[i];
+ * offset_i is the sum of the earlier inputs' sizes. */
+void cba_ref_route_backward(const double *route_delta, int batch, int n, const int *input_sizes,
+                            double *const *input_deltas) {
+    long outputs = 0;
+    for (int i = 0; i < n; ++i) outputs += input_sizes[i];
+    long offset = 0;
+    for (int i = 0; i < n; ++i) {
+        const int size = input_sizes[i];
+        for (int j = 0; j < batch; ++j)
+            cba_ref_axpy(size, 1.0, route_delta + offset + (long)j * outputs,
+                         input_deltas[i] + (long)j * size);
+        offset += size;
+    }
+}
+
+/* Pooled size of caffe's PoolingLayer (Reshape): ceil((in + 2 pad - k) / stride)
+ * + 1, less one when the last window would start inside the bottom padding. */
+int cba_ref_pooled_size(int in, int k, int stride, int pad) {
+    int out = (int)ceil((double)(in + 2 * pad - k) / stride) + 1;
+    if (pad > 0 && (out - 1) * stride >= in + pad) --out;
+    return out;
+}
+
+/* PoolingLayer::Backward_cpu for MAX pooling ([LENET] 第五层 Pooling): the
+ * bottom gradient starts at zero and, plane by plane (n, c) and top position
+ * (ph, pw) in order, gets top_diff added at the bottom index the forward pass
+ * recorded in mask (h * width + w within the plane). */
+void cba_ref_maxpool_backward(const double *top_diff, const int *mask, int num, int channels,
+                              int height, int width, int pooled_h, int pooled_w,
+                              double *bottom_diff) {
+    const long bottom_plane = (long)height * width, top_plane = (long)pooled_h * pooled_w;
+    for (long i = 0; i < (long)num * channels * bottom_plane; ++i) bottom_diff[i] = 0.0;
+    for (int n = 0; n < num; ++n)
+        for (int c = 0; c < channels; ++c) {
+            const long plane = (long)n * channels + c;
+            const double *td = top_diff + plane * top_plane;
+            const int *mk = mask + plane * top_plane;
+            double *bd = bottom_diff + plane * bottom_plane;
+            for (int ph = 0; ph < pooled_h; ++ph)
+                for (int pw = 0; pw < pooled_w; ++pw) {
+                    const int index = ph * pooled_w + pw;
+                    bd[mk[index]] += td[index];
+                }
+        }
 }
 
 /* ----------------------------------------- sampled outputs at full sizes */

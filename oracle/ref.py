@@ -80,6 +80,12 @@ def lib():
                                           [_dp] * 3)
         L.cba_ref_wgrad_at.argtypes = [_dp, _fp] + geo + [_lp, _l, _dp]
         L.cba_ref_dgrad_at.argtypes = [_dp, _fp, _fp, _fp, _i] + geo + [_lp, _l, _dp]
+        L.cba_ref_yolo_backward.argtypes = [_dp, _l, _dp]
+        L.cba_ref_route_backward.argtypes = [_dp, _i, _i, ctypes.POINTER(_i),
+                                             ctypes.POINTER(_dp)]
+        L.cba_ref_pooled_size.restype = _i
+        L.cba_ref_pooled_size.argtypes = [_i, _i, _i, _i]
+        L.cba_ref_maxpool_backward.argtypes = [_dp, ctypes.POINTER(_i)] + [_i] * 6 + [_dp]
         _lib = L
     return _lib
 
@@ -258,4 +264,42 @@ def dgrad_at(dz, Wt, H, W, stride, pad, idx, residual=None, prev_in=None, accumu
     pin = None if prev_in is None else np.ascontiguousarray(prev_in, np.float32)
     lib().cba_ref_dgrad_at(_pd(dz), _pf(Wt), _pf(res), _pf(pin), int(bool(accumulate)), N, C, H,
                            W, K, R, S, stride, pad, idx.ctypes.data_as(_lp), idx.size, _pd(out))
+    return out
+
+
+# ------------------------------------------------ adjacent data-movement layers
+
+def yolo_backward(l_delta, net_delta):
+    """net_delta + l_delta (backward_yolo_layer); returns a new float64 array."""
+    out = _f64(net_delta).copy()
+    d = _f64(l_delta)
+    lib().cba_ref_yolo_backward(_pd(d), d.size, _pd(out))
+    return out
+
+
+def route_backward(route_delta, input_sizes, input_deltas):
+    """backward_route_layer: route_delta is [batch, sum(input_sizes)]; returns
+    the input deltas (each [batch, input_sizes[i]]) after the additions."""
+    rd = _f64(route_delta)
+    batch = rd.shape[0]
+    outs = [_f64(a).reshape(batch, -1).copy() for a in input_deltas]
+    sizes = (ctypes.c_int * len(input_sizes))(*[int(v) for v in input_sizes])
+    ptrs = (_dp * len(outs))(*[o.ctypes.data_as(_dp) for o in outs])
+    lib().cba_ref_route_backward(_pd(rd), batch, len(outs), sizes, ptrs)
+    return outs
+
+
+def pooled_size(n, k, stride, pad):
+    return lib().cba_ref_pooled_size(int(n), int(k), int(stride), int(pad))
+
+
+def maxpool_backward(top_diff, mask, height, width):
+    """PoolingLayer MAX Backward_cpu: top_diff and mask are [N, C, PH, PW] (mask:
+    int32 flat index h * width + w in the plane); returns bottom_diff [N, C, H, W]."""
+    td = _f64(top_diff)
+    mk = np.ascontiguousarray(mask, dtype=np.int32)
+    N, C, PH, PW = td.shape
+    out = np.empty((N, C, int(height), int(width)))
+    lib().cba_ref_maxpool_backward(_pd(td), mk.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
+                                   N, C, int(height), int(width), PH, PW, _pd(out))
     return out
