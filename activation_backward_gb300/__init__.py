@@ -17,4 +17,6 @@ from ._binding import (ACT_NAMES, CBA_ACT_ELU, CBA_ACT_HARDTAN, CBA_ACT_LEAKY,  
                        cba_conv_bn_act_backward, cba_conv_bn_act_backward_traced, cba_desc_t,
                        cba_error_string, cba_get_status, cba_last_cuda_error,
                        cba_selftest_bounded_wait, cba_version, cba_workspace_bytes, load,
-                       make_desc)
+                       make_desc, CBA_ROUTE_MAX_INPUTS, cba_maxpool_backward,
+                       cba_pool_desc_t, cba_pooled_size, cba_route_backward, cba_yolo_backward,
+                       make_pool_desc)

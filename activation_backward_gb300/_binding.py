@@ -47,7 +47,10 @@ CBA_MATH_FFMA = 1
 # every symbol include/cba.h declares
 EXPORTS = ("cba_workspace_bytes", "cba_conv_bn_act_backward", "cba_conv_bn_act_backward_traced",
            "cba_get_status", "cba_bn_act_backward_noalloc",
-           "cba_selftest_bounded_wait", "cba_error_string", "cba_last_cuda_error", "cba_version")
+           "cba_selftest_bounded_wait", "cba_yolo_backward", "cba_route_backward",
+           "cba_pooled_size", "cba_maxpool_backward", "cba_error_string", "cba_last_cuda_error",
+           "cba_version")
+CBA_ROUTE_MAX_INPUTS = 8
 
 
 class cba_desc_t(ctypes.Structure):
@@ -56,6 +59,11 @@ class cba_desc_t(ctypes.Structure):
                 ("S", ctypes.c_int), ("stride", ctypes.c_int), ("pad", ctypes.c_int),
                 ("act", ctypes.c_int), ("batch_normalize", ctypes.c_int),
                 ("accumulate", ctypes.c_int), ("eps", ctypes.c_float), ("math", ctypes.c_int)]
+
+
+class cba_pool_desc_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("N", "C", "H", "W", "kernel_h", "kernel_w",
+                                              "stride_h", "stride_w", "pad_h", "pad_w")]
 
 
 class CbaError(RuntimeError):
@@ -90,6 +98,16 @@ def load(path=LIB_PATH):
     L.cba_get_status.argtypes = [vp, sz, vp]
     L.cba_selftest_bounded_wait.restype = ctypes.c_int
     L.cba_selftest_bounded_wait.argtypes = [vp, sz, ctypes.c_uint, vp]
+    L.cba_yolo_backward.restype = ctypes.c_int
+    L.cba_yolo_backward.argtypes = [vp, vp, ctypes.c_longlong, vp]
+    L.cba_route_backward.restype = ctypes.c_int
+    L.cba_route_backward.argtypes = [vp, ctypes.c_int, ctypes.c_int,
+                                     ctypes.POINTER(ctypes.c_longlong),
+                                     ctypes.POINTER(ctypes.c_void_p), vp]
+    L.cba_pooled_size.restype = ctypes.c_int
+    L.cba_pooled_size.argtypes = [ctypes.c_int] * 4
+    L.cba_maxpool_backward.restype = ctypes.c_int
+    L.cba_maxpool_backward.argtypes = [ctypes.POINTER(cba_pool_desc_t), vp, vp, vp, vp]
     L.cba_error_string.restype = ctypes.c_char_p
     L.cba_error_string.argtypes = [ctypes.c_int]
     L.cba_last_cuda_error.restype = ctypes.c_int
@@ -206,3 +224,44 @@ def cba_last_cuda_error():
 
 def cba_version():
     return load().cba_version()
+
+
+# ------------------------------------------------ data-movement layers
+
+def _checked(rc, what, check):
+    if check and rc != CBA_OK:
+        raise CbaError(rc, what)
+    return rc
+
+
+def cba_yolo_backward(l_delta, net_delta, n=None, stream=None, check=True):
+    """net_delta += l_delta over n elements (default: all of l_delta)."""
+    n = l_delta.numel() if n is None else int(n)
+    rc = load().cba_yolo_backward(_ptr(l_delta), _ptr(net_delta), n, _stream(stream))
+    return _checked(rc, "cba_yolo_backward", check)
+
+
+def cba_route_backward(route_delta, input_deltas, batch=None, stream=None, check=True):
+    """Split route_delta [batch, outputs] back onto the input deltas (tensors of
+    batch * size_i elements each), adding."""
+    batch = route_delta.shape[0] if batch is None else int(batch)
+    n = len(input_deltas)
+    sizes = (ctypes.c_longlong * n)(*[t.numel() // batch for t in input_deltas])
+    ptrs = (ctypes.c_void_p * n)(*[_ptr(t) for t in input_deltas])
+    rc = load().cba_route_backward(_ptr(route_delta), batch, n, sizes, ptrs, _stream(stream))
+    return _checked(rc, "cba_route_backward", check)
+
+
+def cba_pooled_size(n, kernel, stride, pad):
+    return load().cba_pooled_size(int(n), int(kernel), int(stride), int(pad))
+
+
+def make_pool_desc(N, C, H, W, kernel, stride, pad=0):
+    return cba_pool_desc_t(N, C, H, W, kernel, kernel, stride, stride, pad, pad)
+
+
+def cba_maxpool_backward(desc, top_diff, mask, bottom_diff, stream=None, check=True):
+    """bottom_diff = scatter of top_diff to the mask's indices (gather form)."""
+    rc = load().cba_maxpool_backward(ctypes.byref(desc), _ptr(top_diff), _ptr(mask),
+                                     _ptr(bottom_diff), _stream(stream))
+    return _checked(rc, "cba_maxpool_backward", check)

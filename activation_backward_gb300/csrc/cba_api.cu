@@ -335,4 +335,60 @@ int cba_last_cuda_error(void) { return g_last_cuda_error; }
 
 int cba_version(void) { return 100; }
 
+int cba_yolo_backward(const float *l_delta, float *net_delta, long long n, void *stream) {
+    if (n < 0 || (n > 0 && (!l_delta || !net_delta))) return CBA_ERR_ARG;
+    if (n == 0) return CBA_OK;
+    cudaGetLastError();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = select_device(st, net_delta);
+    if (e == cudaSuccess) e = launch_yolo_backward(l_delta, net_delta, n, st);
+    return e == cudaSuccess ? CBA_OK : fail_cuda(e);
+}
+
+int cba_route_backward(const float *route_delta, int batch, int n_inputs,
+                       const long long *input_sizes, float *const *input_deltas, void *stream) {
+    if (!route_delta || batch < 1 || n_inputs < 1 || n_inputs > CBA_ROUTE_MAX_INPUTS ||
+        !input_sizes || !input_deltas)
+        return CBA_ERR_ARG;
+    long long outputs = 0;
+    for (int i = 0; i < n_inputs; ++i) {
+        if (input_sizes[i] < 1 || !input_deltas[i]) return CBA_ERR_ARG;
+        if (input_sizes[i] > (1LL << 50) || outputs > (1LL << 52)) return CBA_ERR_UNSUPPORTED;
+        outputs += input_sizes[i];
+    }
+    if (outputs > (1LL << 62) / batch) return CBA_ERR_UNSUPPORTED;
+    cudaGetLastError();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = select_device(st, route_delta);
+    if (e == cudaSuccess)
+        e = launch_route_backward(route_delta, batch, n_inputs, input_sizes, input_deltas, st);
+    return e == cudaSuccess ? CBA_OK : fail_cuda(e);
+}
+
+int cba_pooled_size(int in, int kernel, int stride, int pad) {
+    return pooled_size(in, kernel, stride, pad);
+}
+
+int cba_maxpool_backward(const cba_pool_desc_t *d, const float *top_diff, const int *mask,
+                         float *bottom_diff, void *stream) {
+    if (!d || !top_diff || !mask || !bottom_diff) return CBA_ERR_ARG;
+    if (d->N < 1 || d->C < 1 || d->H < 1 || d->W < 1 || d->kernel_h < 1 || d->kernel_w < 1 ||
+        d->stride_h < 1 || d->stride_w < 1 || d->pad_h < 0 || d->pad_w < 0 ||
+        d->pad_h >= d->kernel_h || d->pad_w >= d->kernel_w)
+        return CBA_ERR_ARG;
+    const int PH = pooled_size(d->H, d->kernel_h, d->stride_h, d->pad_h);
+    const int PW = pooled_size(d->W, d->kernel_w, d->stride_w, d->pad_w);
+    if (PH < 1 || PW < 1) return CBA_ERR_ARG;
+    const long long planes = (long long)d->N * d->C;
+    if ((long long)d->H * d->W >= (1LL << 31) || (long long)PH * PW >= (1LL << 31) ||
+        planes > (1LL << 62) / ((long long)d->H * d->W) ||
+        planes > (1LL << 62) / ((long long)PH * PW))
+        return CBA_ERR_UNSUPPORTED;
+    cudaGetLastError();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = select_device(st, bottom_diff);
+    if (e == cudaSuccess) e = launch_maxpool_backward(*d, PH, PW, top_diff, mask, bottom_diff, st);
+    return e == cudaSuccess ? CBA_OK : fail_cuda(e);
+}
+
 }  // extern "C"

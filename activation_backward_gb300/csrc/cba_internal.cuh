@@ -72,6 +72,14 @@ cudaError_t launch_reduce(const Plan &p, const float *delta, const float *output
 // dz_out may be the delta buffer itself (an in-place transform).
 cudaError_t launch_dz_out(const Plan &p, const float *delta, const float *output, const float *z,
                           const void *ws, float *dz_out, cudaStream_t st);
+// Data-movement layers (cba_layers.cu).
+int pooled_size(int in, int k, int stride, int pad);
+cudaError_t launch_yolo_backward(const float *l_delta, float *net_delta, long long n,
+                                 cudaStream_t st);
+cudaError_t launch_route_backward(const float *route, int batch, int n, const long long *sizes,
+                                  float *const *deltas, cudaStream_t st);
+cudaError_t launch_maxpool_backward(const cba_pool_desc_t &d, int PH, int PW, const float *top,
+                                    const int *mask, float *bottom, cudaStream_t st);
 // gradient_array for the activations other than LINEAR and LEAKY (p.act_in):
 // dprime[i] = delta[i] * f'(output[i]).  dprime may be the delta buffer.
 cudaError_t launch_gradient_array(const Plan &p, const float *delta, const float *output,

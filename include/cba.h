@@ -200,6 +200,57 @@ int cba_bn_act_backward_noalloc(const cba_desc_t *d, const float *output, const 
                                 const float *var, float *db, float *dgamma, float *dz_out,
                                 void *stream);
 
+/* ---- Backward of the data-movement layers next to the convolution ----
+ * Same conventions as above: device pointers owned by the caller, enqueued on
+ * `stream` (cudaStream_t, NULL = legacy default) without synchronising, no
+ * allocation; on an error nothing is launched.  Returns CBA_OK or a code. */
+
+/* YOLO layer ("YOLOv3反向传播原理 之 全流程源码分析" §2, backward_yolo_layer):
+ * net_delta[i] += l_delta[i] for i < n (the layer's delta passed back with one
+ * axpy of factor 1; n = batch * inputs).  l_delta and net_delta: fp32, n
+ * elements each, not overlapping.  CBA_ERR_ARG: n < 0, or a NULL pointer with
+ * n > 0. */
+int cba_yolo_backward(const float *l_delta, float *net_delta, long long n, void *stream);
+
+/* Most inputs a route layer may have in one call. */
+#define CBA_ROUTE_MAX_INPUTS 8
+
+/* Route layer (same page, §6, backward_route_layer).  Its output lays its
+ * n_inputs inputs side by side per image: outputs = sum of input_sizes, and
+ * route_delta is [batch][outputs].  For input i (offset_i = the sum of the
+ * earlier sizes) and image j:
+ *   input_deltas[i][j * input_sizes[i] + t] += route_delta[j * outputs + offset_i + t]
+ * for t < input_sizes[i].  input_sizes and input_deltas are HOST arrays of
+ * n_inputs entries; input_deltas[i] are DEVICE pointers ([batch][size_i] fp32),
+ * pairwise disjoint and disjoint from route_delta.  CBA_ERR_ARG: batch < 1,
+ * n_inputs outside 1..CBA_ROUTE_MAX_INPUTS, a size < 1, or a NULL pointer. */
+int cba_route_backward(const float *route_delta, int batch, int n_inputs,
+                       const long long *input_sizes, float *const *input_deltas, void *stream);
+
+/* Max pooling ("LeNet反向过程" 第五层 Pooling, caffe PoolingLayer MAX): bottom
+ * [N,C,H,W], top [N,C,PH,PW] with caffe's sizes PH = cba_pooled_size(H,
+ * kernel_h, stride_h, pad_h) and PW likewise. */
+typedef struct {
+    int N, C, H, W;
+    int kernel_h, kernel_w, stride_h, stride_w, pad_h, pad_w; /* 0 <= pad < kernel */
+} cba_pool_desc_t;
+
+/* caffe's pooled size: ceil((in + 2 pad - kernel) / stride) + 1, one less when
+ * the last window would start in the bottom padding; -1 on bad arguments. */
+int cba_pooled_size(int in, int kernel, int stride, int pad);
+
+/* bottom_diff = 0, then bottom_diff[n][c][mask / W][mask % W] += top_diff for
+ * every top element (mask[n][c][ph][pw] = h * W + w of the element the forward
+ * took as the window's maximum).  Each bottom element is written once: it sums
+ * the top gradients that point at it in ascending (ph, pw), the page's order.
+ * A mask value outside its own window is ignored (never dereferenced).
+ * top_diff fp32 and mask int32 [N,C,PH,PW], bottom_diff fp32 [N,C,H,W].
+ * CBA_ERR_ARG: a non-positive size, kernel or stride, pad outside 0..kernel-1,
+ * PH or PW < 1, a NULL pointer; CBA_ERR_UNSUPPORTED: N*C*H*W or N*C*PH*PW past
+ * 2^62, H*W past 2^31. */
+int cba_maxpool_backward(const cba_pool_desc_t *d, const float *top_diff, const int *mask,
+                         float *bottom_diff, void *stream);
+
 /* Human-readable text of a CBA_* code (static storage). */
 const char *cba_error_string(int code);
 
