@@ -82,12 +82,33 @@ __global__ void __launch_bounds__(kLThreads) route_backward_kernel(const RouteAr
     }
 }
 
+// Division of n < 2^31 by a divisor fixed for a launch, with one multiply-high,
+// an add and a shift: Granlund and Montgomery, "Division by invariant integers
+// using multiplication" (PLDI 1994), the round-up multiplier with
+// l = ceil(log2 d):  m = floor(2^32 (2^l - d) / d) + 1,  q = (mulhi(n, m) + n) >> l.
+// n < 2^31 keeps mulhi(n, m) + n below 2^32.
+struct FastDiv {
+    uint32_t d, mul, shift;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((1ull << l) < d) ++l;
+    const uint64_t m = ((1ull << 32) * ((1ull << l) - d)) / d + 1;
+    return FastDiv{d, (uint32_t)m, l};
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
+    return (__umulhi(n, f.mul) + n) >> f.shift;
+}
+
 struct PoolArgs {
     const float *top;  // [N*C][PH][PW]
     const int *mask;   // [N*C][PH][PW]: h * W + w of the window's recorded maximum
     float *bottom;     // [N*C][H][W]
     int H, W, PH, PW, kh, kw, sh, sw, ph, pw;
     long long total;   // N * C * H * W
+    FastDiv seg, fw, fsh, fsw;  // by the thread units per plane, W, stride_h, stride_w
 };
 
 // Top rows whose window covers bottom row h: the window of top row p is rows
@@ -97,27 +118,93 @@ __device__ __forceinline__ void covering(int h, int k, int s, int pad, int P, in
     lo = a > 0 ? (a + s - 1) / s : 0;
     hi = min(P - 1, (h + pad) / s);
 }
+__device__ __forceinline__ void covering(int h, int k, const FastDiv &s, int pad, int P, int &lo,
+                                         int &hi) {
+    const int a = h + pad - k + 1;
+    lo = a > 0 ? (int)fdiv((uint32_t)(a + (int)s.d - 1), s) : 0;
+    hi = min(P - 1, (int)fdiv((uint32_t)(h + pad), s));
+}
 
+// EPT consecutive bottom elements of one row per thread (4 when W is a
+// multiple of 4: one 16-byte store).  CH x CW bounds the windows that cover an
+// element (ceil(kernel / stride) per axis): with them fixed, every mask and top
+// load of the thread's elements is issued before the first compare, so a
+// thread keeps many loads in flight; CH = CW = 0 walks the windows at run time.
+// Either way an element sums its top gradients in ascending (ph, pw).
+// SMALL: fewer than 2^31 thread units and 2^31 elements per plane, so the
+// index arithmetic runs on 32-bit values with FastDiv; else 64-bit division.
+template <int CH, int CW, int EPT, bool SMALL>
 __global__ void __launch_bounds__(kLThreads) maxpool_backward_kernel(const PoolArgs a) {
     const long long stride = (long long)gridDim.x * blockDim.x;
     const int hw_n = a.H * a.W, phw = a.PH * a.PW;
-    for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < a.total;
-         b += stride) {
-        const long long plane = b / hw_n;
-        const int hw = (int)(b - plane * hw_n);
-        const int h = hw / a.W, w = hw - h * a.W;
-        int p0, p1, q0, q1;
-        covering(h, a.kh, a.sh, a.ph, a.PH, p0, p1);
-        covering(w, a.kw, a.sw, a.pw, a.PW, q0, q1);
+    const long long units = a.total / EPT;
+    for (long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x; u < units; u += stride) {
+        long long plane;
+        int hw0, h, w0, p0, p1;
+        if constexpr (SMALL) {
+            const uint32_t pl = fdiv((uint32_t)u, a.seg);
+            hw0 = ((int)u - (int)(pl * a.seg.d)) * EPT;
+            h = (int)fdiv((uint32_t)hw0, a.fw);
+            plane = pl;
+            covering(h, a.kh, a.fsh, a.ph, a.PH, p0, p1);
+        } else {
+            const long long b0 = u * EPT;
+            plane = b0 / hw_n;
+            hw0 = (int)(b0 - plane * hw_n);
+            h = hw0 / a.W;
+            covering(h, a.kh, a.sh, a.ph, a.PH, p0, p1);
+        }
+        w0 = hw0 - h * a.W;
+        const long long b0 = plane * hw_n + hw0;
         const int *mk = a.mask + plane * phw;
         const float *tp = a.top + plane * phw;
-        float acc = 0.f;
-        for (int p = p0; p <= p1; ++p)
-            for (int q = q0; q <= q1; ++q) {
-                const int idx = p * a.PW + q;
-                if (__ldg(mk + idx) == hw) acc += __ldg(tp + idx);
+        float acc[EPT];
+        if constexpr (CH > 0) {
+            int m[EPT][CH][CW];
+            float t[EPT][CH][CW];
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) {
+                int q0, q1;
+                if constexpr (SMALL) covering(w0 + e, a.kw, a.fsw, a.pw, a.PW, q0, q1);
+                else covering(w0 + e, a.kw, a.sw, a.pw, a.PW, q0, q1);
+#pragma unroll
+                for (int i = 0; i < CH; ++i)
+#pragma unroll
+                    for (int j = 0; j < CW; ++j) {
+                        const bool ok = p0 + i <= p1 && q0 + j <= q1;
+                        const int idx = ok ? (p0 + i) * a.PW + q0 + j : 0;
+                        m[e][i][j] = ok ? __ldg(mk + idx) : -1;
+                        t[e][i][j] = ok ? __ldg(tp + idx) : 0.f;
+                    }
             }
-        a.bottom[b] = acc;
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) {
+                acc[e] = 0.f;
+#pragma unroll
+                for (int i = 0; i < CH; ++i)
+#pragma unroll
+                    for (int j = 0; j < CW; ++j)
+                        if (m[e][i][j] == hw0 + e) acc[e] += t[e][i][j];
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPT; ++e) {
+                int q0, q1;
+                covering(w0 + e, a.kw, a.sw, a.pw, a.PW, q0, q1);
+                acc[e] = 0.f;
+                for (int p = p0; p <= p1; ++p)
+                    for (int q = q0; q <= q1; ++q) {
+                        const int idx = p * a.PW + q;
+                        const int mv = __ldg(mk + idx);
+                        const float tv = __ldg(tp + idx);
+                        if (mv == hw0 + e) acc[e] += tv;
+                    }
+            }
+        }
+        if constexpr (EPT == 4)
+            *reinterpret_cast<float4 *>(a.bottom + b0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        else
+            a.bottom[b0] = acc[0];
     }
 }
 
@@ -169,7 +256,32 @@ cudaError_t launch_maxpool_backward(const cba_pool_desc_t &d, int PH, int PW, co
     a.kh = d.kernel_h; a.kw = d.kernel_w; a.sh = d.stride_h; a.sw = d.stride_w;
     a.ph = d.pad_h; a.pw = d.pad_w;
     a.total = (long long)d.N * d.C * d.H * d.W;
-    maxpool_backward_kernel<<<grid_for(a.total), kLThreads, 0, st>>>(a);
+    const int ch = (d.kernel_h + d.stride_h - 1) / d.stride_h;
+    const int cw = (d.kernel_w + d.stride_w - 1) / d.stride_w;
+    const bool v4 = d.W % 4 == 0 && aligned16(bottom);
+    const long long units = v4 ? a.total / 4 : a.total;
+    const bool small = units < (1LL << 31);
+    a.seg = make_fastdiv((uint32_t)(v4 ? d.H * d.W / 4 : d.H * d.W));
+    a.fw = make_fastdiv((uint32_t)d.W);
+    a.fsh = make_fastdiv((uint32_t)d.stride_h);
+    a.fsw = make_fastdiv((uint32_t)d.stride_w);
+    const unsigned grid = grid_for(units);
+#define CBA_POOL(CH, CW)                                                                      \
+    do {                                                                                      \
+        if (v4 && small)                                                                      \
+            maxpool_backward_kernel<CH, CW, 4, true><<<grid, kLThreads, 0, st>>>(a);          \
+        else if (v4)                                                                          \
+            maxpool_backward_kernel<CH, CW, 4, false><<<grid, kLThreads, 0, st>>>(a);         \
+        else if (small)                                                                       \
+            maxpool_backward_kernel<CH, CW, 1, true><<<grid, kLThreads, 0, st>>>(a);          \
+        else                                                                                  \
+            maxpool_backward_kernel<CH, CW, 1, false><<<grid, kLThreads, 0, st>>>(a);         \
+    } while (0)
+    if (ch == 1 && cw == 1) CBA_POOL(1, 1);
+    else if (ch == 2 && cw == 2) CBA_POOL(2, 2);
+    else if (ch <= 3 && cw <= 3) CBA_POOL(3, 3);
+    else CBA_POOL(0, 0);
+#undef CBA_POOL
     return cudaGetLastError();
 }
 

@@ -54,6 +54,9 @@ def parse():
                     choices=["linear", "leaky", "logistic", "relu", "relie", "ramp", "tanh",
                              "plse", "elu", "selu", "lhtan", "hardtan", "loggy", "stair"],
                     help="replace the workload's activation (outputs recomputed)")
+    ap.add_argument("--layer", default="conv", choices=["conv", "maxpool", "route", "yolo"],
+                    help="conv (default): the convolution layer backward; the others time "
+                         "the data-movement layers' backward in GB/s")
     ap.add_argument("--bn", default="batch", choices=["batch", "frozen"],
                     help="BN statistics of the workload's BN layers: the batch's own "
                          "(training mode, default) or frozen ones (batch_normalize = 2)")
@@ -510,10 +513,90 @@ def measure_e2e(dls, layers, flops, args, stream, dev, math):
                        "buffer sets, three streams"}
 
 
+LAYER_WORKLOADS = {
+    # LeNet pool1 geometry (20 x 24 x 24, 2 x 2 stride 2) at a batch past the L2
+    "maxpool": dict(workload="lenet_pool1", N=4096, C=20, H=24, W=24, k=2, stride=2, pad=0),
+    # a YOLOv3 route at 26 x 26: 128 upsampled channels + 512, batch 16
+    "route": dict(workload="yolov3_route_26", batch=16, sizes=[128 * 26 * 26, 512 * 26 * 26]),
+    # a YOLOv3 detection head's delta at 52 x 52: 255 channels, batch 16
+    "yolo": dict(workload="yolov3_yolo_52", n=16 * 255 * 52 * 52),
+}
+
+
+def run_layer(args):
+    """GB/s of one data-movement layer's backward: algorithmic bytes (each
+    input read once, each output written once) over the device time, L2
+    flushed before every step.  N = 1 only (each call is one GPU's work)."""
+    import torch
+
+    import activation_backward_gb300 as cba
+    from activation_backward_gb300 import inputs
+    cba.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = LAYER_WORKLOADS[args.layer]
+    if args.layer == "maxpool":
+        c = inputs.make_pool_case(w["N"], w["C"], w["H"], w["W"], w["k"], w["stride"], w["pad"],
+                                  seed=1)
+        desc = cba.make_pool_desc(w["N"], w["C"], w["H"], w["W"], w["k"], w["stride"], w["pad"])
+        top, mask = torch.from_numpy(c["top_diff"]).to(dev), torch.from_numpy(c["mask"]).to(dev)
+        bottom = torch.empty((w["N"], w["C"], w["H"], w["W"]), device=dev)
+        nbytes = (top.numel() + mask.numel() + bottom.numel()) * 4
+        call = lambda: cba.cba_maxpool_backward(desc, top, mask, bottom)  # noqa: E731
+    elif args.layer == "route":
+        c = inputs.make_route_case(w["batch"], w["sizes"], seed=1)
+        route = torch.from_numpy(c["route_delta"]).to(dev)
+        deltas = [torch.from_numpy(a).to(dev) for a in c["input_deltas"]]
+        nbytes = (route.numel() + 2 * sum(d.numel() for d in deltas)) * 4
+        call = lambda: cba.cba_route_backward(route, deltas)  # noqa: E731
+    else:
+        g = torch.Generator(device=dev).manual_seed(1)
+        l_delta = torch.randn(w["n"], device=dev, generator=g)
+        net = torch.randn(w["n"], device=dev, generator=g)
+        nbytes = 3 * w["n"] * 4
+        call = lambda: cba.cba_yolo_backward(l_delta, net)  # noqa: E731
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = flush_buf[: 256 << 20].view(torch.int32)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(0)
+    clocks.start()
+    for a, b in ev:
+        flush_buf.zero_()
+        flush_rd.max()
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / len(ev)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks, src = load_peaks()
+    line = {"metric": f"{args.layer} backward bandwidth", "value": gbs, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": dict({k: v for k, v in w.items()},
+                           l2="flushed before every step, outside the timing"),
+            "roofline": {"bound": "hbm", "kernel": f"{args.layer}_backward_kernel",
+                         "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": f"{src} copy bandwidth"},
+            "algorithmic_bytes": nbytes, "cpu_baseline": None, "e2e": None,
+            "gpu_launches": args.steps, "clocks": clk}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.layer != "conv":
+        run_layer(args)
     else:
         run_ours(args)
 

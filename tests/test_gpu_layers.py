@@ -23,6 +23,8 @@ POOL_CASES = [
     (4, 16, 13, 13, 3, 2, 1),    # overlapping windows, padding, ceil rule
     (2, 8, 17, 23, 3, 1, 0),     # stride 1: up to 9 windows per element
     (3, 5, 10, 7, 3, 2, 0),      # the last window clipped at the edge
+    (2, 3, 14, 16, 3, 3, 1),     # stride 3 (not a power of two), 4-wide rows
+    (2, 2, 9, 20, 5, 3, 2),      # kernel 5: windows per axis past the unrolled bound
     (1, 1, 1, 1, 1, 1, 0),       # one element
 ]
 
