@@ -45,12 +45,13 @@ CBA_MATH_TF32 = 0
 CBA_MATH_FFMA = 1
 
 # every symbol include/cba.h declares
-EXPORTS = ("cba_workspace_bytes", "cba_conv_bn_act_backward", "cba_conv_bn_act_backward_traced",
+EXPORTS = ("cba_workspace_bytes", "cba_workspace_bytes_ex", "cba_conv_bn_act_backward", "cba_conv_bn_act_backward_traced",
            "cba_get_status", "cba_bn_act_backward_noalloc",
            "cba_selftest_bounded_wait", "cba_yolo_backward", "cba_route_backward",
            "cba_pooled_size", "cba_maxpool_backward", "cba_error_string", "cba_last_cuda_error",
            "cba_version")
 CBA_ROUTE_MAX_INPUTS = 8
+CBA_WS_RECOMPUTE_Z = 1
 
 
 class cba_desc_t(ctypes.Structure):
@@ -86,6 +87,8 @@ def load(path=LIB_PATH):
     vp, sz = ctypes.c_void_p, ctypes.c_size_t
     L.cba_workspace_bytes.restype = sz
     L.cba_workspace_bytes.argtypes = [ctypes.POINTER(cba_desc_t)]
+    L.cba_workspace_bytes_ex.restype = sz
+    L.cba_workspace_bytes_ex.argtypes = [ctypes.POINTER(cba_desc_t), ctypes.c_uint]
     L.cba_conv_bn_act_backward.restype = ctypes.c_int
     L.cba_conv_bn_act_backward.argtypes = [ctypes.POINTER(cba_desc_t)] + [vp] * 15 + [sz, vp]
     L.cba_conv_bn_act_backward_traced.restype = ctypes.c_int
@@ -147,6 +150,10 @@ def make_desc(N, C, H, W, K, R, S, stride=1, pad=0, act=CBA_ACT_LEAKY, batch_nor
 
 def cba_workspace_bytes(desc):
     return load().cba_workspace_bytes(ctypes.byref(desc))
+
+
+def cba_workspace_bytes_ex(desc, flags):
+    return load().cba_workspace_bytes_ex(ctypes.byref(desc), int(flags))
 
 
 def cba_conv_bn_act_backward(desc, x, output, z, delta, W, gamma, mean, var, residual, dW, db,

@@ -110,6 +110,8 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->off_dprime = off;
     if (p->act_pre) off = align_up(off + sizeof(float) * (size_t)nout, 256);
     p->total = off;
+    p->off_z = off;
+    p->total_z = p->bn ? align_up(off + sizeof(float) * (size_t)nout, 256) : off;
     return CBA_OK;
 }
 
@@ -165,6 +167,12 @@ size_t cba_workspace_bytes(const cba_desc_t *d) {
     return p.total;
 }
 
+size_t cba_workspace_bytes_ex(const cba_desc_t *d, unsigned flags) {
+    Plan p;
+    if (make_plan(d, &p) != CBA_OK || (flags & ~(unsigned)CBA_WS_RECOMPUTE_Z)) return 0;
+    return (flags & CBA_WS_RECOMPUTE_Z) ? p.total_z : p.total;
+}
+
 }  // extern "C"
 
 namespace {
@@ -188,12 +196,13 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     if (rc != CBA_OK) return rc;
     if (!x || !delta || !Wt || !dW || !db) return CBA_ERR_ARG;
     if (p.act_in != CBA_ACT_LINEAR && !output) return CBA_ERR_ARG;
-    if (p.bn && (!z || !gamma || !mean || !var || !dgamma)) return CBA_ERR_ARG;
+    if (p.bn && (!gamma || !mean || !var || !dgamma)) return CBA_ERR_ARG;
+    const bool z_free = p.bn && !z;  // z = conv(x, W) is recomputed into the workspace
     const void *ptrs[] = {x, output, z, delta, Wt, gamma, mean, var, residual,
                           dW, db, dgamma, prev_delta, dz_out};
     for (const void *q : ptrs)
         if (misaligned(q)) return CBA_ERR_ALIGN;
-    if (!workspace || workspace_bytes < p.total) return CBA_ERR_WORKSPACE;
+    if (!workspace || workspace_bytes < (z_free ? p.total_z : p.total)) return CBA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CBA_ERR_ALIGN;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -204,6 +213,11 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     if (e != cudaSuccess) return fail_cuda(e);
     e = cudaMemsetAsync(workspace, 0, p.clear_bytes, st);  // status word, reduction counters
     if (e == cudaSuccess) e = tr.mark(0);
+    if (e == cudaSuccess && z_free) {
+        float *zbuf = ws_at<float>(workspace, p.off_z);
+        e = launch_conv_forward(p, x, Wt, zbuf, st, &n_launch);
+        z = zbuf;
+    }
     if (e == cudaSuccess && p.act_pre) {
         // activations other than linear and leaky: delta' first, then the main
         // kernels run in linear mode on it

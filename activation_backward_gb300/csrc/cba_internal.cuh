@@ -54,6 +54,8 @@ struct Plan {
     // status word at the start of every call; clear_bytes covers both)
     size_t off_status, off_cnt, clear_bytes, off_red, off_coef, off_wgpart, off_wt, off_dzt,
         off_wr, off_dprime, total;
+    // z-free calls (BN without z): z = conv(x, W) goes to off_z; total_z bytes
+    size_t off_z, total_z;
 };
 
 // Builds the plan; returns CBA_OK or a CBA_ERR_* code.
@@ -72,6 +74,9 @@ cudaError_t launch_reduce(const Plan &p, const float *delta, const float *output
 // dz_out may be the delta buffer itself (an in-place transform).
 cudaError_t launch_dz_out(const Plan &p, const float *delta, const float *output, const float *z,
                           const void *ws, float *dz_out, cudaStream_t st);
+// z = conv(x, W), the pre-BN convolution output (cba_fwd.cu).
+cudaError_t launch_conv_forward(const Plan &p, const float *x, const float *W, float *z,
+                                cudaStream_t st, int *launches);
 // Data-movement layers (cba_layers.cu).
 int pooled_size(int in, int k, int stride, int pad);
 cudaError_t launch_yolo_backward(const float *l_delta, float *net_delta, long long n,

@@ -24,7 +24,8 @@ class DeviceLayer:
     at zero, or at ``prev_init`` when given."""
 
     def __init__(self, layer, math=B.CBA_MATH_TF32, device="cuda", accumulate=None,
-                 with_prev=True, with_residual=True, prev_init=None, want_dz=False):
+                 with_prev=True, with_residual=True, prev_init=None, want_dz=False,
+                 z_free=False):
         g = layer["geom"]
         self.geom = g
         self.layer = layer
@@ -35,7 +36,8 @@ class DeviceLayer:
         self.x = _dev(layer["x"], device)
         self.W = _dev(layer["W"], device)
         self.output = _dev(layer["output"], device) if layer["act"] != B.CBA_ACT_LINEAR else None
-        self.z = _dev(layer["z"], device) if layer["bn"] else None
+        # z_free: the library recomputes z = conv(x, W) in the workspace
+        self.z = _dev(layer["z"], device) if layer["bn"] and not z_free else None
         self.delta = _dev(layer["delta"], device)
         self.gamma = _dev(layer["gamma"], device) if layer["bn"] else None
         self.mean = _dev(layer["mean"], device) if layer["bn"] else None
@@ -51,7 +53,8 @@ class DeviceLayer:
             self.prev = (torch.zeros((g.N, g.C, g.H, g.W), **f) if prev_init is None
                          else _dev(prev_init, device))
         self.dz = torch.empty((g.N, g.K, g.P, g.Q), **f) if want_dz else None
-        nbytes = B.cba_workspace_bytes(self.desc)
+        nbytes = (B.cba_workspace_bytes_ex(self.desc, B.CBA_WS_RECOMPUTE_Z) if z_free
+                  else B.cba_workspace_bytes(self.desc))
         if nbytes == 0:
             raise B.CbaError(B.CBA_ERR_ARG, "cba_workspace_bytes")
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)

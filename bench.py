@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--layer", default="conv", choices=["conv", "maxpool", "route", "yolo"],
                     help="conv (default): the convolution layer backward; the others time "
                          "the data-movement layers' backward in GB/s")
+    ap.add_argument("--z-free", action="store_true",
+                    help="BN layers without z: the library recomputes z = conv(x, W)")
     ap.add_argument("--bn", default="batch", choices=["batch", "frozen"],
                     help="BN statistics of the workload's BN layers: the batch's own "
                          "(training mode, default) or frozen ones (batch_normalize = 2)")
@@ -294,6 +296,8 @@ def config_dict(args, layers, ws):
             "stride": g.stride, "pad": g.pad,
             "bn": {0: False, 1: "batch statistics", 2: "frozen statistics"}[int(layers[0]["bn"])],
             "act": ACT_NAMES[int(layers[0]["act"])],
+            "z": "recomputed by the library (conv forward)" if getattr(args, "z_free", False)
+                 else "given",
             "gemm_gflop_per_step": flops / 1e9,
             "l2": "flushed before every step, outside the timing: 512 MiB write, then a 256 MiB "
                   "read sweep so no dirty flush lines are written back inside the step",
@@ -320,7 +324,7 @@ def run_ours(args):
     cba.load()
 
     layers = workload_layers(args)
-    dls = [DeviceLayer(l, math=math, device=dev) for l in layers]
+    dls = [DeviceLayer(l, math=math, device=dev, z_free=args.z_free) for l in layers]
     flops = sum(2 * l["geom"].gemm_flops() for l in layers)
     red_bytes = sum(inputs.layer_bytes_reduce(l) for l in layers)
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -458,7 +462,7 @@ def measure_e2e(dls, layers, flops, args, stream, dev, math):
     from activation_backward_gb300.layer import DeviceLayer
     names_in = ("x", "output", "z", "delta", "W", "gamma", "mean", "var", "residual")
     names_out = ("dW", "db", "dgamma", "prev")
-    sets = [dls, [DeviceLayer(l, math=math, device=dev) for l in layers]]
+    sets = [dls, [DeviceLayer(l, math=math, device=dev, z_free=args.z_free) for l in layers]]
     hin = [{n: getattr(dl, n).cpu().pin_memory() for n in names_in
             if getattr(dl, n) is not None} for dl in dls]
     hout = [[{n: torch.empty_like(getattr(dl, n), device="cpu").pin_memory()

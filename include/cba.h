@@ -110,10 +110,22 @@ typedef struct {
  * invalid).  The workspace must be 256-byte aligned device memory. */
 size_t cba_workspace_bytes(const cba_desc_t *d);
 
+/* With CBA_WS_RECOMPUTE_Z: the bytes of a z-free call (BN on, z = NULL), which
+ * recomputes z = conv(x, W) -- the pre-BN convolution output, stride and pad
+ * of the descriptor, no bias; forward_convolutional_layer's W . im2col(x) of
+ * "YOLOv3反向传播原理" §3.2 -- into the workspace before the backward.  With
+ * flags = 0 the same as cba_workspace_bytes.  0 on an invalid descriptor or an
+ * unknown flag. */
+#define CBA_WS_RECOMPUTE_Z 1u
+size_t cba_workspace_bytes_ex(const cba_desc_t *d, unsigned flags);
+
 /* The backward of one conv(+BN)+activation layer; see the header comment.
  *   x        [N,C,H,W] layer input (darknet net.input); required
  *   output   [N,K,P,Q] post-activation output; required unless act = LINEAR
- *   z        [N,K,P,Q] pre-BN convolution output (darknet l.x); required iff BN
+ *   z        [N,K,P,Q] pre-BN convolution output (darknet l.x); with BN, NULL
+ *            recomputes it from x and W (the workspace must then hold
+ *            cba_workspace_bytes_ex(d, CBA_WS_RECOMPUTE_Z) bytes); unused
+ *            without BN
  *   delta    [N,K,P,Q] gradient at the output; required; NOT modified
  *   W        [K,C,R,S] weights; required
  *   gamma, mean, var [K] BN scale and statistics (batch_normalize 1: the

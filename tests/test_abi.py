@@ -96,8 +96,12 @@ def _call(lib, d, **ptrs):
 
 def test_required_pointers(lib):
     d = cba.make_desc(2, 3, 5, 5, 4, 3, 3, 1, 1, act=cba.CBA_ACT_LEAKY, batch_normalize=1)
-    for name in ("x", "delta", "W", "dW", "db", "output", "z", "gamma", "mean", "var", "dgamma"):
+    for name in ("x", "delta", "W", "dW", "db", "output", "gamma", "mean", "var", "dgamma"):
         assert _call(lib, d, **{name: None}) == cba.CBA_ERR_ARG, name
+    # with BN, z may be NULL (recomputed), but only with the larger workspace:
+    # the plain size stops at the workspace check, before any launch
+    plain = lib.cba_workspace_bytes(ctypes.byref(d))
+    assert _call(lib, d, z=None, wsb=plain) == cba.CBA_ERR_WORKSPACE
     # linear without BN: output, z, gamma, mean, var, dgamma may be NULL; the
     # call then stops at the (too small) workspace check, still before any launch
     d2 = cba.make_desc(2, 3, 5, 5, 4, 3, 3, 1, 1, act=cba.CBA_ACT_LINEAR, batch_normalize=0)
@@ -131,3 +135,15 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
             B.load(str(tmp_path / "missing.so"))
         finally:
             B._lib = B._lib_saved
+
+
+def test_workspace_query_for_z_free_calls(lib):
+    d = cba.make_desc(2, 3, 5, 5, 4, 3, 3, 1, 1, act=cba.CBA_ACT_LEAKY, batch_normalize=1)
+    base = lib.cba_workspace_bytes(ctypes.byref(d))
+    zfree = lib.cba_workspace_bytes_ex(ctypes.byref(d), cba.CBA_WS_RECOMPUTE_Z)
+    assert lib.cba_workspace_bytes_ex(ctypes.byref(d), 0) == base
+    assert zfree >= base + 2 * 4 * 5 * 5 * 4  # room for z [N, K, P, Q] fp32
+    assert lib.cba_workspace_bytes_ex(ctypes.byref(d), 2) == 0  # unknown flag
+    d0 = cba.make_desc(2, 3, 5, 5, 4, 3, 3, 1, 1, act=cba.CBA_ACT_LINEAR, batch_normalize=0)
+    assert lib.cba_workspace_bytes_ex(ctypes.byref(d0), cba.CBA_WS_RECOMPUTE_Z) == \
+        lib.cba_workspace_bytes(ctypes.byref(d0))  # no BN, no z

@@ -82,6 +82,22 @@ def test_parity_other_activations(ref, cuda_lib, act):
                 assert_close(got[k], exp[k], TOL[math], f"{layer['name']} {k}")
 
 
+ZFREE = [(2, 2), (3, 2), (5, 2)]
+
+
+@pytest.mark.parametrize("math", MATHS)
+@pytest.mark.parametrize("cid,batch", ZFREE, ids=[f"cfg{c}_n{b}" for c, b in ZFREE])
+def test_parity_z_free(ref, cuda_lib, cid, batch, math):
+    # BN without z: the library recomputes z = conv(x, W) (fp32) in its workspace;
+    # the oracle gets the generator's z (an fp64 convolution rounded to fp32)
+    for layer in config_layers(cid, batch):
+        _, got = run_gpu(layer, math, want_dz=True, z_free=True)
+        exp = oracle_chain(ref, layer, want_dz=True)
+        for k in KEYS + ("dz",):
+            if exp.get(k) is not None:
+                assert_close(got[k], exp[k], TOL[math], f"{layer['name']} z-free {k}")
+
+
 FROZEN = [(2, 2), (3, 2), (5, 2)]
 
 
