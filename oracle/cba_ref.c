@@ -318,14 +318,20 @@ void cba_ref_bn_backward_caffe(const double *top_diff, const double *x_norm, con
  * in [YOLO] §3.1 (col_i = im2col of image i, §3.2), and what
  * caffe_cpu_gemm(NoTrans, Trans, ..., 1., top_diff, bottom_data, 1., weight_diff)
  * computes in [LENET] 第四层 Convolution; both accumulate (beta = 1). */
-void cba_ref_conv_wgrad(const double *delta, const double *x, int N, int C, int H, int W, int K,
-                        int R, int S, int stride, int pad, double *dW) {
+/* With groups ([YOLO] §3.1, the l.groups loop of backward_convolutional_layer):
+ * output channel k belongs to group g = k / (K/groups) and sees only the
+ * input channels g*C/groups .. (g+1)*C/groups - 1; W and dW are
+ * [K][C/groups][R][S]. */
+void cba_ref_conv_wgrad_g(const double *delta, const double *x, int N, int C, int H, int W,
+                          int K, int R, int S, int stride, int pad, int groups, double *dW) {
     int P = cba_ref_out_size(H, R, stride, pad), Q = cba_ref_out_size(W, S, stride, pad);
+    const int Cg = C / groups, Kg = K / groups;
 #pragma omp parallel for schedule(dynamic)
     for (int k = 0; k < K; ++k)
-        for (int c = 0; c < C; ++c)
+        for (int cg = 0; cg < Cg; ++cg)
             for (int r = 0; r < R; ++r)
                 for (int s = 0; s < S; ++s) {
+                    const int c = (k / Kg) * Cg + cg;
                     double acc = 0.0;
                     for (int n = 0; n < N; ++n)
                         for (int p = 0; p < P; ++p) {
@@ -339,8 +345,13 @@ void cba_ref_conv_wgrad(const double *delta, const double *x, int N, int C, int 
                                 acc += drow[q] * xrow[w];
                             }
                         }
-                    dW[(((long)k * C + c) * R + r) * S + s] += acc;
+                    dW[(((long)k * Cg + cg) * R + r) * S + s] += acc;
                 }
+}
+
+void cba_ref_conv_wgrad(const double *delta, const double *x, int N, int C, int H, int W, int K,
+                        int R, int S, int stride, int pad, double *dW) {
+    cba_ref_conv_wgrad_g(delta, x, N, C, H, W, K, R, S, stride, pad, 1, dW);
 }
 
 /* Input gradient written as a scatter, the shape of col2im_cpu
@@ -349,16 +360,19 @@ void cba_ref_conv_wgrad(const double *delta, const double *x, int N, int C, int 
  * into image pixel (p*st + r - pad, q*st + s - pad) when that pixel lies
  * inside the image (col2im_add_pixel).  dx must hold the values to add onto
  * (zeros for a plain result). */
-void cba_ref_conv_dgrad(const double *delta, const double *Wt, int N, int C, int H, int W, int K,
-                        int R, int S, int stride, int pad, double *dx) {
+/* With groups: input channel c of group g = c / (C/groups) receives only from
+ * the output channels of group g, through W[k][c - g*C/groups][r][s]. */
+void cba_ref_conv_dgrad_g(const double *delta, const double *Wt, int N, int C, int H, int W,
+                          int K, int R, int S, int stride, int pad, int groups, double *dx) {
     int P = cba_ref_out_size(H, R, stride, pad), Q = cba_ref_out_size(W, S, stride, pad);
+    const int Cg = C / groups, Kg = K / groups;
 #pragma omp parallel for schedule(dynamic)
     for (int n = 0; n < N; ++n)
         for (int c = 0; c < C; ++c)
             for (int r = 0; r < R; ++r)
                 for (int s = 0; s < S; ++s)
-                    for (int k = 0; k < K; ++k) {
-                        double wv = Wt[(((long)k * C + c) * R + r) * S + s];
+                    for (int k = (c / Cg) * Kg; k < (c / Cg + 1) * Kg; ++k) {
+                        double wv = Wt[(((long)k * Cg + c % Cg) * R + r) * S + s];
                         for (int p = 0; p < P; ++p) {
                             int h = p * stride + r - pad;
                             if (h < 0 || h >= H) continue;
@@ -371,6 +385,11 @@ void cba_ref_conv_dgrad(const double *delta, const double *Wt, int N, int C, int
                             }
                         }
                     }
+}
+
+void cba_ref_conv_dgrad(const double *delta, const double *Wt, int N, int C, int H, int W, int K,
+                        int R, int S, int stride, int pad, double *dx) {
+    cba_ref_conv_dgrad_g(delta, Wt, N, C, H, W, K, R, S, stride, pad, 1, dx);
 }
 
 /* axpy_cpu: y += alpha * x  ([YOLO] §2).  The shortcut layer passes its delta
@@ -395,16 +414,20 @@ void cba_ref_axpy(long n, double alpha, const double *x, double *y) {
  * (the shortcut delta of [YOLO] §5) may be NULL; prev_delta NULL skips the
  * input gradient (the `if (net.delta)` test of [YOLO] §3.1); dz_out, if not
  * NULL, receives the BN-input gradient (the delta the GEMMs consume).
+ * groups (the l.groups loop of backward_convolutional_layer, [YOLO] §3.1):
+ * W and dW are [K][C/groups][R][S]; output channel k only meets the input
+ * channels of its group (cba_ref_conv_wgrad_g, cba_ref_conv_dgrad_g); the BN
+ * steps are per output channel and do not see the groups.
  * Returns 0, or -1 on a bad argument or an allocation failure. */
-int cba_ref_conv_bn_act_backward_f64(int N, int C, int H, int W, int K, int R, int S, int stride,
-                                     int pad, int act, int batch_normalize, int accumulate,
-                                     double eps, const double *x, const double *output,
-                                     const double *z, const double *delta, const double *Wt,
-                                     const double *gamma, const double *mean, const double *var,
-                                     const double *residual, double *dW, double *db,
-                                     double *dgamma, double *prev_delta, double *dz_out) {
+int cba_ref_conv_bn_act_backward_grouped_f64(
+    int N, int C, int H, int W, int K, int R, int S, int stride, int pad, int groups, int act,
+    int batch_normalize, int accumulate, double eps, const double *x, const double *output,
+    const double *z, const double *delta, const double *Wt, const double *gamma,
+    const double *mean, const double *var, const double *residual, double *dW, double *db,
+    double *dgamma, double *prev_delta, double *dz_out) {
     if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || K <= 0 || R <= 0 || S <= 0 || stride <= 0 || pad < 0)
         return -1;
+    if (groups < 1 || C % groups != 0 || K % groups != 0) return -1;
     if (batch_normalize < REF_BN_NONE || batch_normalize > REF_BN_FROZEN) return -1;
     if (act < REF_ACT_LINEAR || act > REF_ACT_STAIR) return -1;
     int P = cba_ref_out_size(H, R, stride, pad), Q = cba_ref_out_size(W, S, stride, pad);
@@ -434,12 +457,12 @@ int cba_ref_conv_bn_act_backward_f64(int N, int C, int H, int W, int K, int R, i
     }
     if (dz_out) memcpy(dz_out, d, sizeof(double) * nout);
 
-    cba_ref_conv_wgrad(d, x, N, C, H, W, K, R, S, stride, pad, dW);
+    cba_ref_conv_wgrad_g(d, x, N, C, H, W, K, R, S, stride, pad, groups, dW);
 
     if (prev_delta) {
         double *dx = (double *)calloc((size_t)nin, sizeof(double));
         if (!dx) { free(d); return -1; }
-        cba_ref_conv_dgrad(d, Wt, N, C, H, W, K, R, S, stride, pad, dx);
+        cba_ref_conv_dgrad_g(d, Wt, N, C, H, W, K, R, S, stride, pad, groups, dx);
         if (residual) cba_ref_axpy(nin, 1.0, residual, dx);
         if (!accumulate)
             for (long i = 0; i < nin; ++i) prev_delta[i] = 0.0;
@@ -450,6 +473,19 @@ int cba_ref_conv_bn_act_backward_f64(int N, int C, int H, int W, int K, int R, i
     return 0;
 }
 
+int cba_ref_conv_bn_act_backward_f64(int N, int C, int H, int W, int K, int R, int S, int stride,
+                                     int pad, int act, int batch_normalize, int accumulate,
+                                     double eps, const double *x, const double *output,
+                                     const double *z, const double *delta, const double *Wt,
+                                     const double *gamma, const double *mean, const double *var,
+                                     const double *residual, double *dW, double *db,
+                                     double *dgamma, double *prev_delta, double *dz_out) {
+    return cba_ref_conv_bn_act_backward_grouped_f64(N, C, H, W, K, R, S, stride, pad, 1, act,
+                                                    batch_normalize, accumulate, eps, x, output,
+                                                    z, delta, Wt, gamma, mean, var, residual, dW,
+                                                    db, dgamma, prev_delta, dz_out);
+}
+
 static double *widen(const float *src, long n) {
     if (!src) return NULL;
     double *d = (double *)malloc(sizeof(double) * (n > 0 ? n : 1));
@@ -458,8 +494,33 @@ static double *widen(const float *src, long n) {
     return d;
 }
 
-/* Same as cba_ref_conv_bn_act_backward_f64, on the float inputs the GPU sees
+/* Same as cba_ref_conv_bn_act_backward_grouped_f64, on the float inputs the GPU sees
  * (widened exactly to double).  Outputs are double. */
+int cba_ref_conv_bn_act_backward_grouped(int N, int C, int H, int W, int K, int R, int S,
+                                         int stride, int pad, int groups, int act,
+                                         int batch_normalize, int accumulate, float eps,
+                                         const float *x, const float *output, const float *z,
+                                         const float *delta, const float *Wt, const float *gamma,
+                                         const float *mean, const float *var,
+                                         const float *residual, double *dW, double *db,
+                                         double *dgamma, double *prev_delta, double *dz_out) {
+    if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || K <= 0 || R <= 0 || S <= 0 || stride <= 0 || pad < 0)
+        return -1;
+    if (groups < 1 || C % groups != 0 || K % groups != 0) return -1;
+    int P = cba_ref_out_size(H, R, stride, pad), Q = cba_ref_out_size(W, S, stride, pad);
+    if (P <= 0 || Q <= 0) return -1;
+    long nout = (long)N * K * P * Q, nin = (long)N * C * H * W,
+         nw = (long)K * (C / groups) * R * S;
+    double *dx_ = widen(x, nin), *dout = widen(output, nout), *dz = widen(z, nout);
+    double *dd = widen(delta, nout), *dWt = widen(Wt, nw), *dg = widen(gamma, K);
+    double *dm = widen(mean, K), *dv = widen(var, K), *dres = widen(residual, nin);
+    int rc = cba_ref_conv_bn_act_backward_grouped_f64(
+        N, C, H, W, K, R, S, stride, pad, groups, act, batch_normalize, accumulate, (double)eps,
+        dx_, dout, dz, dd, dWt, dg, dm, dv, dres, dW, db, dgamma, prev_delta, dz_out);
+    free(dx_); free(dout); free(dz); free(dd); free(dWt); free(dg); free(dm); free(dv); free(dres);
+    return rc;
+}
+
 int cba_ref_conv_bn_act_backward(int N, int C, int H, int W, int K, int R, int S, int stride,
                                  int pad, int act, int batch_normalize, int accumulate, float eps,
                                  const float *x, const float *output, const float *z,
@@ -467,20 +528,10 @@ int cba_ref_conv_bn_act_backward(int N, int C, int H, int W, int K, int R, int S
                                  const float *mean, const float *var, const float *residual,
                                  double *dW, double *db, double *dgamma, double *prev_delta,
                                  double *dz_out) {
-    if (N <= 0 || C <= 0 || H <= 0 || W <= 0 || K <= 0 || R <= 0 || S <= 0 || stride <= 0 || pad < 0)
-        return -1;
-    int P = cba_ref_out_size(H, R, stride, pad), Q = cba_ref_out_size(W, S, stride, pad);
-    if (P <= 0 || Q <= 0) return -1;
-    long nout = (long)N * K * P * Q, nin = (long)N * C * H * W, nw = (long)K * C * R * S;
-    double *dx_ = widen(x, nin), *dout = widen(output, nout), *dz = widen(z, nout);
-    double *dd = widen(delta, nout), *dWt = widen(Wt, nw), *dg = widen(gamma, K);
-    double *dm = widen(mean, K), *dv = widen(var, K), *dres = widen(residual, nin);
-    int rc = cba_ref_conv_bn_act_backward_f64(N, C, H, W, K, R, S, stride, pad, act,
-                                              batch_normalize, accumulate, (double)eps, dx_, dout,
-                                              dz, dd, dWt, dg, dm, dv, dres, dW, db, dgamma,
-                                              prev_delta, dz_out);
-    free(dx_); free(dout); free(dz); free(dd); free(dWt); free(dg); free(dm); free(dv); free(dres);
-    return rc;
+    return cba_ref_conv_bn_act_backward_grouped(N, C, H, W, K, R, S, stride, pad, 1, act,
+                                                batch_normalize, accumulate, eps, x, output, z,
+                                                delta, Wt, gamma, mean, var, residual, dW, db,
+                                                dgamma, prev_delta, dz_out);
 }
 
 /* Steps 1-2 of the chain alone (activation gradient, then BN backward or

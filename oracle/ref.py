@@ -75,6 +75,12 @@ def lib():
         L.cba_ref_conv_bn_act_backward.restype = _i
         L.cba_ref_conv_bn_act_backward.argtypes = (
             [_i] * 12 + [ctypes.c_float] + [_fp] * 9 + [_dp] * 5)
+        L.cba_ref_conv_bn_act_backward_grouped_f64.restype = _i
+        L.cba_ref_conv_bn_act_backward_grouped_f64.argtypes = (
+            [_i] * 13 + [_d] + [_dp] * 9 + [_dp] * 5)
+        L.cba_ref_conv_bn_act_backward_grouped.restype = _i
+        L.cba_ref_conv_bn_act_backward_grouped.argtypes = (
+            [_i] * 13 + [ctypes.c_float] + [_fp] * 9 + [_dp] * 5)
         L.cba_ref_backward_dz.restype = _i
         L.cba_ref_backward_dz.argtypes = ([_i] * 6 + [ctypes.c_float] + [_fp] * 6 +
                                           [_dp] * 3)
@@ -185,15 +191,18 @@ def conv_dgrad(delta, Wt, H, W, stride, pad, dx=None):
 
 def conv_bn_act_backward(x, output, z, delta, Wt, gamma, mean, var, residual, *, stride, pad,
                          act, batch_normalize, accumulate, eps, dW=None, db=None, dgamma=None,
-                         prev_delta=None, want_prev=True, want_dz=False, f64_inputs=False):
+                         prev_delta=None, want_prev=True, want_dz=False, f64_inputs=False,
+                         groups=1):
     """Run the whole chain.  Inputs are float32 arrays (the GPU's bits) unless
     ``f64_inputs``; returns dict(dW, db, dgamma, prev_delta, dz) of float64
     arrays.  dW/db/dgamma start from the given arrays (zeros if None) and
-    accumulate; prev_delta starts from the given array when accumulate=1."""
+    accumulate; prev_delta starts from the given array when accumulate=1.
+    With ``groups``, Wt is [K, C/groups, R, S]."""
     N, C, H, W = x.shape
-    K, _, R, S = Wt.shape
+    K, Cg, R, S = Wt.shape
+    assert Cg * groups == C
     P, Q = out_size(H, R, stride, pad), out_size(W, S, stride, pad)
-    o_dW = np.zeros((K, C, R, S)) if dW is None else _f64(dW).copy()
+    o_dW = np.zeros((K, Cg, R, S)) if dW is None else _f64(dW).copy()
     o_db = np.zeros(K) if db is None else _f64(db).copy()
     o_dg = (np.zeros(K) if dgamma is None else _f64(dgamma).copy()) if batch_normalize else None
     o_prev = None
@@ -203,15 +212,15 @@ def conv_bn_act_backward(x, output, z, delta, Wt, gamma, mean, var, residual, *,
     L = lib()
     if f64_inputs:
         conv = lambda a: _pd(_f64(a))  # noqa: E731
-        fn = L.cba_ref_conv_bn_act_backward_f64
+        fn = L.cba_ref_conv_bn_act_backward_grouped_f64
         e = float(eps)
     else:
         conv = lambda a: _pf(None if a is None else np.ascontiguousarray(a, np.float32))  # noqa
-        fn = L.cba_ref_conv_bn_act_backward
+        fn = L.cba_ref_conv_bn_act_backward_grouped
         e = ctypes.c_float(eps)
     keep = [x, output, z, delta, Wt, gamma, mean, var, residual]
     ptrs = [conv(a) for a in keep]
-    rc = fn(N, C, H, W, K, R, S, stride, pad, int(act), int(batch_normalize),
+    rc = fn(N, C, H, W, K, R, S, stride, pad, int(groups), int(act), int(batch_normalize),
             int(bool(accumulate)), e, *ptrs, _pd(o_dW), _pd(o_db), _pd(o_dg), _pd(o_prev),
             _pd(o_dz))
     if rc != 0:

@@ -6,11 +6,11 @@ import numpy as np
 import torch
 
 
-def conv64(x, w, stride, pad):
+def conv64(x, w, stride, pad, groups=1):
     with torch.no_grad():
         return torch.nn.functional.conv2d(torch.from_numpy(np.asarray(x, np.float64)),
                                           torch.from_numpy(np.asarray(w, np.float64)),
-                                          stride=stride, padding=pad).numpy()
+                                          stride=stride, padding=pad, groups=groups).numpy()
 
 
 def _stair(v):
@@ -58,13 +58,13 @@ def min_kink_distance(act, v):
     return np.min(np.abs(v[..., None] - np.asarray(k)), axis=-1)
 
 
-def layer_forward(x, w, gamma, beta, *, stride, pad, act, bn, eps, stats=None):
+def layer_forward(x, w, gamma, beta, *, stride, pad, act, bn, eps, stats=None, groups=1):
     """Forward of the layer: z = conv(x, w); BN with the batch statistics
     (biased variance) if bn, or with the fixed (mean, var) of ``stats`` (frozen
     statistics: constants of the forward); then scale, shift and activation.
     Without BN, beta is the conv bias.  Returns (z, mean, var, pre_activation,
     output)."""
-    z = conv64(x, w, stride, pad)
+    z = conv64(x, w, stride, pad, groups)
     if bn and stats is not None:
         mean, var = (np.asarray(a, np.float64) for a in stats)
         xh = (z - mean[None, :, None, None]) / np.sqrt(var[None, :, None, None] + eps)

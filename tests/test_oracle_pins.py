@@ -246,6 +246,77 @@ def test_chain_with_other_activations_matches_finite_differences(ref, case):
         close(got["dgamma"], central_diff(lambda v: loss(gv=v), gamma))
 
 
+GROUP_CASES = [
+    # N, C, H, W, K, R, S, stride, pad, act, bn, residual, groups
+    (2, 4, 5, 5, 6, 3, 3, 1, 1, 1, True, False, 2),
+    (2, 6, 6, 5, 3, 3, 3, 2, 1, 0, False, True, 3),
+    (3, 4, 4, 4, 4, 1, 1, 1, 0, 1, True, True, 4),    # depthwise 1x1
+    (2, 4, 5, 5, 4, 3, 3, 1, 1, 1, True, False, 4),   # depthwise 3x3
+]
+
+
+@pytest.mark.parametrize("case", GROUP_CASES, ids=[str(i) for i in range(len(GROUP_CASES))])
+def test_grouped_chain_matches_finite_differences(ref, case):
+    """l.groups ([YOLO] §3.1): the whole chain of a grouped convolution against
+    finite differences of torch's grouped conv2d forward."""
+    N, C, H, W, K, R, S, st, pad, act, bn, res, G = case
+    rng = _rng(800 + GROUP_CASES.index(case))
+    for attempt in range(50):
+        x = rng.standard_normal((N, C, H, W))
+        w = rng.standard_normal((K, C // G, R, S)) * 0.5
+        gamma = rng.uniform(0.5, 1.5, K)
+        beta = rng.uniform(-0.3, 0.3, K)
+        kw = dict(stride=st, pad=pad, act=act, bn=bn, eps=EPS, groups=G)
+        z, mean, var, pre, out = layer_forward(x, w, gamma, beta, **kw)
+        if act != 1 or np.min(np.abs(pre)) >= 5e-3:
+            break
+    else:
+        raise RuntimeError("no draw clear of the kink")
+    D = rng.standard_normal(pre.shape)
+    Dres = rng.standard_normal(x.shape) if res else None
+
+    def loss(xv=x, wv=w, gv=gamma, bv=beta):
+        L = float(np.sum(D * layer_forward(xv, wv, gv, bv, **kw)[4]))
+        if Dres is not None:
+            L += float(np.sum(Dres * xv))
+        return L
+
+    got = ref.conv_bn_act_backward(x, out, z if bn else None, D, w, gamma if bn else None,
+                                   mean, var, Dres, stride=st, pad=pad, act=act,
+                                   batch_normalize=int(bn), accumulate=0, eps=EPS,
+                                   f64_inputs=True, groups=G)
+
+    def close(a, b, tol=2e-6):
+        scale = max(np.max(np.abs(b)), 1e-12)
+        assert np.max(np.abs(a - b)) <= tol * scale, (np.max(np.abs(a - b)), scale)
+
+    close(got["prev_delta"], central_diff(lambda v: loss(xv=v), x))
+    close(got["dW"], central_diff(lambda v: loss(wv=v), w))
+    close(got["db"], central_diff(lambda v: loss(bv=v), beta))
+    if bn:
+        close(got["dgamma"], central_diff(lambda v: loss(gv=v), gamma))
+
+
+@pytest.mark.parametrize("G", [2, 4, 8])
+def test_grouped_conv_gradients_vs_torch(ref, G):
+    """Linear, no BN: dW and dx of a grouped convolution against torch's float64
+    grouped conv2d_weight / conv2d_input (a library special case)."""
+    rng = _rng(900 + G)
+    N, C, H, W, K, R, S, st, pad = 2, 8, 7, 6, 16, 3, 3, 2, 1
+    x = rng.standard_normal((N, C, H, W))
+    w = rng.standard_normal((K, C // G, R, S))
+    P, Q = (H + 2 * pad - R) // st + 1, (W + 2 * pad - S) // st + 1
+    D = rng.standard_normal((N, K, P, Q))
+    got = ref.conv_bn_act_backward(x, None, None, D, w, None, None, None, None, stride=st,
+                                   pad=pad, act=0, batch_normalize=0, accumulate=0, eps=EPS,
+                                   f64_inputs=True, groups=G)
+    tx, tw, tD = (torch.from_numpy(a) for a in (x, w, D))
+    gw = torch.nn.grad.conv2d_weight(tx, tw.shape, tD, stride=st, padding=pad, groups=G)
+    gx = torch.nn.grad.conv2d_input(tx.shape, tw, tD, stride=st, padding=pad, groups=G)
+    assert np.max(np.abs(got["dW"] - gw.numpy())) < 1e-10
+    assert np.max(np.abs(got["prev_delta"] - gx.numpy())) < 1e-10
+
+
 # ------------------------------------- convolution gradients, other forms
 
 def _im2col(img, R, S, stride, pad):
