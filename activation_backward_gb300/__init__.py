@@ -19,4 +19,5 @@ from ._binding import (ACT_NAMES, CBA_ACT_ELU, CBA_ACT_HARDTAN, CBA_ACT_LEAKY,  
                        cba_selftest_bounded_wait, cba_version, cba_workspace_bytes, load,
                        make_desc, CBA_ROUTE_MAX_INPUTS, cba_maxpool_backward,
                        cba_pool_desc_t, cba_pooled_size, cba_route_backward, cba_yolo_backward,
-                       make_pool_desc, CBA_WS_RECOMPUTE_Z, cba_workspace_bytes_ex)
+                       make_pool_desc, CBA_WS_RECOMPUTE_Z, cba_workspace_bytes_ex,
+                       cba_conv_bn_act_backward_grouped, cba_workspace_bytes_grouped)

@@ -45,7 +45,8 @@ CBA_MATH_TF32 = 0
 CBA_MATH_FFMA = 1
 
 # every symbol include/cba.h declares
-EXPORTS = ("cba_workspace_bytes", "cba_workspace_bytes_ex", "cba_conv_bn_act_backward", "cba_conv_bn_act_backward_traced",
+EXPORTS = ("cba_workspace_bytes", "cba_workspace_bytes_ex", "cba_workspace_bytes_grouped",
+           "cba_conv_bn_act_backward_grouped", "cba_conv_bn_act_backward", "cba_conv_bn_act_backward_traced",
            "cba_get_status", "cba_bn_act_backward_noalloc",
            "cba_selftest_bounded_wait", "cba_yolo_backward", "cba_route_backward",
            "cba_pooled_size", "cba_maxpool_backward", "cba_error_string", "cba_last_cuda_error",
@@ -87,6 +88,12 @@ def load(path=LIB_PATH):
     vp, sz = ctypes.c_void_p, ctypes.c_size_t
     L.cba_workspace_bytes.restype = sz
     L.cba_workspace_bytes.argtypes = [ctypes.POINTER(cba_desc_t)]
+    L.cba_workspace_bytes_grouped.restype = sz
+    L.cba_workspace_bytes_grouped.argtypes = [ctypes.POINTER(cba_desc_t), ctypes.c_int,
+                                              ctypes.c_uint]
+    L.cba_conv_bn_act_backward_grouped.restype = ctypes.c_int
+    L.cba_conv_bn_act_backward_grouped.argtypes = ([ctypes.POINTER(cba_desc_t), ctypes.c_int] +
+                                                   [vp] * 15 + [sz, vp])
     L.cba_workspace_bytes_ex.restype = sz
     L.cba_workspace_bytes_ex.argtypes = [ctypes.POINTER(cba_desc_t), ctypes.c_uint]
     L.cba_conv_bn_act_backward.restype = ctypes.c_int
@@ -154,6 +161,24 @@ def cba_workspace_bytes(desc):
 
 def cba_workspace_bytes_ex(desc, flags):
     return load().cba_workspace_bytes_ex(ctypes.byref(desc), int(flags))
+
+
+def cba_workspace_bytes_grouped(desc, groups, flags=0):
+    return load().cba_workspace_bytes_grouped(ctypes.byref(desc), int(groups), int(flags))
+
+
+def cba_conv_bn_act_backward_grouped(desc, groups, x, output, z, delta, W, gamma, mean, var,
+                                     residual, dW, db, dgamma, prev_delta, dz_out, workspace,
+                                     workspace_bytes=None, stream=None, check=True):
+    """Grouped-convolution layer backward (W, dW [K, C/groups, R, S])."""
+    wsb = _bytes(workspace) if workspace_bytes is None else int(workspace_bytes)
+    rc = load().cba_conv_bn_act_backward_grouped(
+        ctypes.byref(desc), int(groups), _ptr(x), _ptr(output), _ptr(z), _ptr(delta), _ptr(W),
+        _ptr(gamma), _ptr(mean), _ptr(var), _ptr(residual), _ptr(dW), _ptr(db), _ptr(dgamma),
+        _ptr(prev_delta), _ptr(dz_out), _ptr(workspace), wsb, _stream(stream))
+    if check and rc != CBA_OK:
+        raise CbaError(rc, "cba_conv_bn_act_backward_grouped")
+    return rc
 
 
 def cba_conv_bn_act_backward(desc, x, output, z, delta, W, gamma, mean, var, residual, dW, db,

@@ -190,7 +190,7 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
                   const float *delta, const float *Wt, const float *gamma, const float *mean,
                   const float *var, const float *residual, float *dW, float *db, float *dgamma,
                   float *prev_delta, float *dz_out, void *workspace, size_t workspace_bytes,
-                  void *stream, void *const *events, int *launches) {
+                  void *stream, void *const *events, int *launches, bool clear_status = true) {
     Plan p;
     int rc = make_plan(d, &p);
     if (rc != CBA_OK) return rc;
@@ -211,7 +211,11 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     cudaGetLastError();  // the launches below report only their own errors
     cudaError_t e = select_device(st, delta);
     if (e != cudaSuccess) return fail_cuda(e);
-    e = cudaMemsetAsync(workspace, 0, p.clear_bytes, st);  // status word, reduction counters
+    // status word (unless a previous call of the same grouped call set it) and
+    // the reduction counters
+    e = clear_status ? cudaMemsetAsync(workspace, 0, p.clear_bytes, st)
+                     : cudaMemsetAsync(ws_at<char>(workspace, p.off_cnt), 0,
+                                       p.clear_bytes - p.off_cnt, st);
     if (e == cudaSuccess) e = tr.mark(0);
     if (e == cudaSuccess && z_free) {
         float *zbuf = ws_at<float>(workspace, p.off_z);
@@ -276,9 +280,167 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     return CBA_OK;
 }
 
+// Workspace layout of a grouped call: the per-group workspace at 0 (so that
+// its status word is the workspace's first word), then channel-slice
+// temporaries of one group.
+struct GroupPlan {
+    cba_desc_t dg;  // the descriptor of one group: C / groups, K / groups
+    size_t sub, off_x, off_delta, off_out, off_z, off_res, off_prev, off_dz, off_w, off_dw,
+        off_vec, total;
+    long long xg, og, wg;  // elements per image of a group's x and output slices; W slice
+};
+
+int make_group_plan(const cba_desc_t *d, int groups, bool z_free, GroupPlan *gp) {
+    if (!d || groups < 1 || d->C % groups != 0 || d->K % groups != 0) return CBA_ERR_ARG;
+    Plan p;
+    int rc = make_plan(d, &p);
+    if (rc != CBA_OK) return rc;
+    gp->dg = *d;
+    gp->dg.C = d->C / groups;
+    gp->dg.K = d->K / groups;
+    Plan pg;
+    rc = make_plan(&gp->dg, &pg);
+    if (rc != CBA_OK) return rc;
+    const size_t f = sizeof(float);
+    gp->xg = (long long)gp->dg.C * d->H * d->W;
+    gp->og = (long long)gp->dg.K * p.P * p.Q;
+    gp->wg = (long long)gp->dg.K * gp->dg.C * d->R * d->S;
+    const size_t xb = f * (size_t)d->N * gp->xg, ob = f * (size_t)d->N * gp->og;
+    size_t off = align_up(z_free && p.bn ? pg.total_z : pg.total, 256);
+    gp->sub = off;
+    gp->off_x = off; off = align_up(off + xb, 256);
+    gp->off_delta = off; off = align_up(off + ob, 256);
+    gp->off_out = off; off = align_up(off + ob, 256);
+    gp->off_z = off; off = align_up(off + ob, 256);
+    gp->off_res = off; off = align_up(off + xb, 256);
+    gp->off_prev = off; off = align_up(off + xb, 256);
+    gp->off_dz = off; off = align_up(off + ob, 256);
+    gp->off_w = off; off = align_up(off + f * (size_t)gp->wg, 256);
+    gp->off_dw = off; off = align_up(off + f * (size_t)gp->wg, 256);
+    gp->off_vec = off; off = align_up(off + 5 * f * (size_t)gp->dg.K + 5 * 256, 256);
+    gp->total = off;
+    return CBA_OK;
+}
+
+// rows of `width` bytes, `height` of them, `spitch` / `dpitch` bytes apart
+inline cudaError_t copy_rows(void *dst, size_t dpitch, const void *src, size_t spitch,
+                             size_t width, size_t height, cudaStream_t st) {
+    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, cudaMemcpyDeviceToDevice,
+                             st);
+}
+
+int grouped_impl(const cba_desc_t *d, int groups, const float *x, const float *output,
+                 const float *z, const float *delta, const float *Wt, const float *gamma,
+                 const float *mean, const float *var, const float *residual, float *dW,
+                 float *db, float *dgamma, float *prev_delta, float *dz_out, void *workspace,
+                 size_t workspace_bytes, void *stream) {
+    Plan p;
+    int rc = make_plan(d, &p);
+    if (rc != CBA_OK) return rc;
+    if (!x || !delta || !Wt || !dW || !db) return CBA_ERR_ARG;
+    if (p.act_in != CBA_ACT_LINEAR && !output) return CBA_ERR_ARG;
+    if (p.bn && (!gamma || !mean || !var || !dgamma)) return CBA_ERR_ARG;
+    const bool z_free = p.bn && !z;
+    GroupPlan gp;
+    rc = make_group_plan(d, groups, z_free, &gp);
+    if (rc != CBA_OK) return rc;
+    if (!workspace || workspace_bytes < gp.total) return CBA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CBA_ERR_ALIGN;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    cudaError_t e = select_device(st, delta);
+    if (e != cudaSuccess) return fail_cuda(e);
+    const size_t f = sizeof(float);
+    const int N = d->N, Kg = gp.dg.K;
+    const size_t xrow = f * (size_t)gp.xg, orow = f * (size_t)gp.og;
+    const size_t xpitch = xrow * groups, opitch = orow * groups;
+    float *tx = ws_at<float>(workspace, gp.off_x), *td = ws_at<float>(workspace, gp.off_delta);
+    float *to = ws_at<float>(workspace, gp.off_out), *tz = ws_at<float>(workspace, gp.off_z);
+    float *tr = ws_at<float>(workspace, gp.off_res), *tp = ws_at<float>(workspace, gp.off_prev);
+    float *tdz = ws_at<float>(workspace, gp.off_dz), *tw = ws_at<float>(workspace, gp.off_w);
+    float *tdw = ws_at<float>(workspace, gp.off_dw);
+    const size_t vstride = align_up(f * (size_t)Kg, 256);
+    float *tg = ws_at<float>(workspace, gp.off_vec), *tm = ws_at<float>(workspace, gp.off_vec + vstride);
+    float *tv = ws_at<float>(workspace, gp.off_vec + 2 * vstride);
+    float *tdb = ws_at<float>(workspace, gp.off_vec + 3 * vstride);
+    float *tdg = ws_at<float>(workspace, gp.off_vec + 4 * vstride);
+    const size_t vb = f * (size_t)Kg, wb = f * (size_t)gp.wg;
+    for (int g = 0; g < groups && e == cudaSuccess; ++g) {
+        // in: the group's channel slices (strided by image), its weights and vectors
+        e = copy_rows(tx, xrow, x + g * gp.xg, xpitch, xrow, N, st);
+        if (e == cudaSuccess) e = copy_rows(td, orow, delta + g * gp.og, opitch, orow, N, st);
+        if (e == cudaSuccess && output && p.act_in != CBA_ACT_LINEAR)
+            e = copy_rows(to, orow, output + g * gp.og, opitch, orow, N, st);
+        if (e == cudaSuccess && p.bn && z)
+            e = copy_rows(tz, orow, z + g * gp.og, opitch, orow, N, st);
+        if (e == cudaSuccess && residual)
+            e = copy_rows(tr, xrow, residual + g * gp.xg, xpitch, xrow, N, st);
+        if (e == cudaSuccess && prev_delta && d->accumulate)
+            e = copy_rows(tp, xrow, prev_delta + g * gp.xg, xpitch, xrow, N, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(tw, Wt + g * gp.wg, wb, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(tdw, dW + g * gp.wg, wb, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(tdb, db + (size_t)g * Kg, vb, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && p.bn) {
+            e = cudaMemcpyAsync(tg, gamma + (size_t)g * Kg, vb, cudaMemcpyDeviceToDevice, st);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(tm, mean + (size_t)g * Kg, vb, cudaMemcpyDeviceToDevice, st);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(tv, var + (size_t)g * Kg, vb, cudaMemcpyDeviceToDevice, st);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(tdg, dgamma + (size_t)g * Kg, vb, cudaMemcpyDeviceToDevice,
+                                    st);
+        }
+        if (e != cudaSuccess) break;
+        rc = backward_impl(&gp.dg, tx, (output && p.act_in != CBA_ACT_LINEAR) ? to : nullptr,
+                           (p.bn && z) ? tz : nullptr, td, tw, p.bn ? tg : nullptr,
+                           p.bn ? tm : nullptr, p.bn ? tv : nullptr, residual ? tr : nullptr, tdw,
+                           tdb, p.bn ? tdg : nullptr, prev_delta ? tp : nullptr,
+                           dz_out ? tdz : nullptr, workspace, gp.sub, stream, nullptr, nullptr,
+                           g == 0);
+        if (rc != CBA_OK) return rc;
+        // out: the accumulated weights and vectors, prev and dz slices
+        e = cudaMemcpyAsync(dW + g * gp.wg, tdw, wb, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(db + (size_t)g * Kg, tdb, vb, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && p.bn)
+            e = cudaMemcpyAsync(dgamma + (size_t)g * Kg, tdg, vb, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && prev_delta)
+            e = copy_rows(prev_delta + g * gp.xg, xpitch, tp, xrow, xrow, N, st);
+        if (e == cudaSuccess && dz_out)
+            e = copy_rows(dz_out + g * gp.og, opitch, tdz, orow, orow, N, st);
+    }
+    if (e != cudaSuccess) return fail_cuda(e);
+    return CBA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int cba_conv_bn_act_backward_grouped(const cba_desc_t *d, int groups, const float *x,
+                                     const float *output, const float *z, const float *delta,
+                                     const float *Wt, const float *gamma, const float *mean,
+                                     const float *var, const float *residual, float *dW,
+                                     float *db, float *dgamma, float *prev_delta, float *dz_out,
+                                     void *workspace, size_t workspace_bytes, void *stream) {
+    if (groups == 1)
+        return backward_impl(d, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db,
+                             dgamma, prev_delta, dz_out, workspace, workspace_bytes, stream,
+                             nullptr, nullptr);
+    return grouped_impl(d, groups, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db,
+                        dgamma, prev_delta, dz_out, workspace, workspace_bytes, stream);
+}
+
+size_t cba_workspace_bytes_grouped(const cba_desc_t *d, int groups, unsigned flags) {
+    if (flags & ~(unsigned)CBA_WS_RECOMPUTE_Z) return 0;
+    if (groups == 1) return cba_workspace_bytes_ex(d, flags);
+    GroupPlan gp;
+    if (make_group_plan(d, groups, (flags & CBA_WS_RECOMPUTE_Z) != 0, &gp) != CBA_OK) return 0;
+    return gp.total;
+}
 
 int cba_conv_bn_act_backward(const cba_desc_t *d, const float *x, const float *output,
                              const float *z, const float *delta, const float *Wt,

@@ -87,12 +87,12 @@ def seed_of(config_id):
     return 1000 + int(config_id)
 
 
-def _forward_conv64(x, w, stride, pad):
+def _forward_conv64(x, w, stride, pad, groups=1):
     import torch
     with torch.no_grad():
         z = torch.nn.functional.conv2d(torch.from_numpy(x.astype(np.float64)),
                                        torch.from_numpy(w.astype(np.float64)), stride=stride,
-                                       padding=pad)
+                                       padding=pad, groups=groups)
     return z.numpy()
 
 
@@ -120,7 +120,7 @@ def _draw(rng, dist, shape, var=1.0):
     return (rng.standard_normal(size=shape) * np.sqrt(var)).astype(np.float32)
 
 
-def make_layer(spec, seed, *, batch=None, residual=False, x=None, delta_var=0.01):
+def make_layer(spec, seed, *, batch=None, residual=False, x=None, delta_var=0.01, groups=1):
     """Inputs of one layer call.  Returns a dict with the geometry and flags
     and fp32 arrays x, W, gamma, z, mean, var, output, delta, residual.
 
@@ -130,11 +130,12 @@ def make_layer(spec, seed, *, batch=None, residual=False, x=None, delta_var=0.01
     rng = np.random.default_rng(seed)
     if x is None:
         x = _draw(rng, spec.dist, (g.N, g.C, g.H, g.W))
-    fan_in = g.C * g.R * g.S
+    Cg = g.C // groups  # input channels a filter sees (grouped convolution)
+    fan_in = Cg * g.R * g.S
     if spec.dist == "uniform":
-        W = _draw(rng, "uniform", (g.K, g.C, g.R, g.S))
+        W = _draw(rng, "uniform", (g.K, Cg, g.R, g.S))
     else:
-        W = _draw(rng, "normal", (g.K, g.C, g.R, g.S), var=2.0 / fan_in)  # He init
+        W = _draw(rng, "normal", (g.K, Cg, g.R, g.S), var=2.0 / fan_in)  # He init
     gamma = rng.uniform(0.5, 1.5, size=g.K).astype(np.float32) if spec.bn else None
     if spec.dist == "uniform":
         delta = _draw(rng, "uniform", (g.N, g.K, g.P, g.Q))
@@ -145,7 +146,7 @@ def make_layer(spec, seed, *, batch=None, residual=False, x=None, delta_var=0.01
         delta = (delta * keep).astype(np.float32)
     res = _draw(rng, "normal", (g.N, g.C, g.H, g.W), var=0.01) if residual else None
 
-    z = _forward_conv64(x, W, g.stride, g.pad).astype(np.float32)
+    z = _forward_conv64(x, W, g.stride, g.pad, groups).astype(np.float32)
     if spec.bn:
         mean, var, output = _bn_forward(z, gamma, spec.act)
     else:
@@ -154,7 +155,15 @@ def make_layer(spec, seed, *, batch=None, residual=False, x=None, delta_var=0.01
         z = None  # the backward needs the pre-BN output only with BN
     return dict(name=spec.name, geom=g, act=spec.act, bn=spec.bn, accumulate=spec.accumulate,
                 eps=EPS, x=x, W=W, gamma=gamma, z=z, mean=mean, var=var, output=output,
-                delta=delta, residual=res)
+                delta=delta, residual=res, groups=int(groups))
+
+
+def make_grouped_config(config_id, groups, *, batch=None):
+    """A one-call workload (configs 1-4) as a grouped convolution: the same
+    geometry with W [K, C/groups, R, S]."""
+    spec = CONFIGS[int(config_id)]
+    layer = make_layer(spec, seed_of(config_id) + 31 * int(groups), batch=batch, groups=groups)
+    return dict(layer, name=f"{spec.name} (groups {int(groups)})")
 
 
 def _act_forward(act, v):

@@ -45,7 +45,8 @@ class DeviceLayer:
         res = layer.get("residual") if with_residual else None
         self.residual = _dev(res, device)
         f = dict(device=device, dtype=torch.float32)
-        self.dW = torch.zeros((g.K, g.C, g.R, g.S), **f)
+        self.groups = int(layer.get("groups", 1))
+        self.dW = torch.zeros((g.K, g.C // self.groups, g.R, g.S), **f)
         self.db = torch.zeros(g.K, **f)
         self.dgamma = torch.zeros(g.K, **f) if layer["bn"] else None
         self.prev = None
@@ -53,8 +54,8 @@ class DeviceLayer:
             self.prev = (torch.zeros((g.N, g.C, g.H, g.W), **f) if prev_init is None
                          else _dev(prev_init, device))
         self.dz = torch.empty((g.N, g.K, g.P, g.Q), **f) if want_dz else None
-        nbytes = (B.cba_workspace_bytes_ex(self.desc, B.CBA_WS_RECOMPUTE_Z) if z_free
-                  else B.cba_workspace_bytes(self.desc))
+        flags = B.CBA_WS_RECOMPUTE_Z if z_free else 0
+        nbytes = B.cba_workspace_bytes_grouped(self.desc, self.groups, flags)
         if nbytes == 0:
             raise B.CbaError(B.CBA_ERR_ARG, "cba_workspace_bytes")
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -68,6 +69,11 @@ class DeviceLayer:
             self.prev.zero_()
 
     def run(self, stream=None, check=True):
+        if self.groups > 1:
+            return B.cba_conv_bn_act_backward_grouped(
+                self.desc, self.groups, self.x, self.output, self.z, self.delta, self.W,
+                self.gamma, self.mean, self.var, self.residual, self.dW, self.db, self.dgamma,
+                self.prev, self.dz, self.workspace, stream=stream, check=check)
         return B.cba_conv_bn_act_backward(self.desc, self.x, self.output, self.z, self.delta,
                                           self.W, self.gamma, self.mean, self.var, self.residual,
                                           self.dW, self.db, self.dgamma, self.prev, self.dz,

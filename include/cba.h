@@ -147,6 +147,25 @@ int cba_conv_bn_act_backward(const cba_desc_t *d, const float *x, const float *o
                              float *prev_delta, float *dz_out, void *workspace,
                              size_t workspace_bytes, void *stream);
 
+/* Grouped convolution (the l.groups loop of backward_convolutional_layer,
+ * "YOLOv3反向传播原理" §3.1): output channels in groups of K/groups, input
+ * channels in groups of C/groups, output channel k meeting only the input
+ * channels of its group.  W and dW are [K][C/groups][R][S]; every other
+ * argument as for cba_conv_bn_act_backward (descriptor C and K are the totals,
+ * both multiples of groups).  The call runs the ungrouped backward once per
+ * group on that group's channel slices, copied into the workspace; it needs
+ * cba_workspace_bytes_grouped(d, groups, flags) bytes (flags as for
+ * cba_workspace_bytes_ex: CBA_WS_RECOMPUTE_Z for calls without z).
+ * groups = 1 is cba_conv_bn_act_backward.  CBA_ERR_ARG also when groups < 1
+ * or does not divide C and K. */
+int cba_conv_bn_act_backward_grouped(const cba_desc_t *d, int groups, const float *x,
+                                     const float *output, const float *z, const float *delta,
+                                     const float *W, const float *gamma, const float *mean,
+                                     const float *var, const float *residual, float *dW,
+                                     float *db, float *dgamma, float *prev_delta, float *dz_out,
+                                     void *workspace, size_t workspace_bytes, void *stream);
+size_t cba_workspace_bytes_grouped(const cba_desc_t *d, int groups, unsigned flags);
+
 /* Same computation as cba_conv_bn_act_backward, for profiling.
  * phase_events: NULL, or an array of 4 cudaEvent_t created by the caller;
  *   the call records [0] before the reduction pass, [1] after it (the

@@ -147,3 +147,15 @@ def test_workspace_query_for_z_free_calls(lib):
     d0 = cba.make_desc(2, 3, 5, 5, 4, 3, 3, 1, 1, act=cba.CBA_ACT_LINEAR, batch_normalize=0)
     assert lib.cba_workspace_bytes_ex(ctypes.byref(d0), cba.CBA_WS_RECOMPUTE_Z) == \
         lib.cba_workspace_bytes(ctypes.byref(d0))  # no BN, no z
+
+
+def test_workspace_query_for_grouped_calls(lib):
+    d = cba.make_desc(2, 8, 5, 5, 12, 3, 3, 1, 1, act=cba.CBA_ACT_LEAKY, batch_normalize=1)
+    assert lib.cba_workspace_bytes_grouped(ctypes.byref(d), 1, 0) == \
+        lib.cba_workspace_bytes(ctypes.byref(d))
+    g4 = lib.cba_workspace_bytes_grouped(ctypes.byref(d), 4, 0)
+    assert g4 > 0
+    assert lib.cba_workspace_bytes_grouped(ctypes.byref(d), 4, cba.CBA_WS_RECOMPUTE_Z) > g4
+    assert lib.cba_workspace_bytes_grouped(ctypes.byref(d), 3, 0) == 0  # 3 does not divide 8
+    assert lib.cba_workspace_bytes_grouped(ctypes.byref(d), 0, 0) == 0
+    assert lib.cba_workspace_bytes_grouped(ctypes.byref(d), 4, 2) == 0  # unknown flag

@@ -37,7 +37,7 @@ def oracle_chain(ref, layer, **kw):
                                     layer["residual"], stride=g.stride, pad=g.pad,
                                     act=layer["act"], batch_normalize=layer["bn"],
                                     accumulate=kw.pop("accumulate", layer["accumulate"]),
-                                    eps=layer["eps"], **kw)
+                                    eps=layer["eps"], groups=layer.get("groups", 1), **kw)
 
 
 def assert_close(got, exp, tol, what, atol=1e-30):
@@ -80,6 +80,33 @@ def test_parity_other_activations(ref, cuda_lib, act):
         for k in KEYS + ("dz",):
             if exp.get(k) is not None:
                 assert_close(got[k], exp[k], TOL[math], f"{layer['name']} {k}")
+
+
+GROUPED = [(2, 2, 2), (2, 2, 4), (2, 1, 64), (3, 2, 8)]
+
+
+@pytest.mark.parametrize("math", MATHS)
+@pytest.mark.parametrize("cid,batch,groups", GROUPED,
+                         ids=[f"cfg{c}_n{b}_g{g}" for c, b, g in GROUPED])
+def test_parity_grouped(ref, cuda_lib, cid, batch, groups, math):
+    # l.groups: one ungrouped backward per group on its channel slices
+    layer = inputs.make_grouped_config(cid, groups, batch=batch)
+    _, got = run_gpu(layer, math, want_dz=True)
+    exp = oracle_chain(ref, layer, want_dz=True)
+    for k in KEYS + ("dz",):
+        if exp.get(k) is not None:
+            assert_close(got[k], exp[k], TOL[math], f"{layer['name']} {k}")
+
+
+def test_parity_grouped_z_free_accumulate(ref, cuda_lib):
+    # grouped, z recomputed per group, prev_delta added onto its contents
+    layer = inputs.make_grouped_config(2, 4, batch=2)
+    prev0 = (np.random.default_rng(5).standard_normal(layer["x"].shape) * 0.01).astype(np.float32)
+    _, got = run_gpu(layer, TF32, z_free=True, accumulate=1, prev_init=prev0)
+    exp = oracle_chain(ref, layer, accumulate=1, prev_delta=prev0)
+    for k in KEYS:
+        if exp.get(k) is not None:
+            assert_close(got[k], exp[k], TOL[TF32], f"{layer['name']} z-free {k}")
 
 
 ZFREE = [(2, 2), (3, 2), (5, 2)]
