@@ -46,7 +46,8 @@ CBA_MATH_FFMA = 1
 
 # every symbol include/cba.h declares
 EXPORTS = ("cba_workspace_bytes", "cba_workspace_bytes_ex", "cba_workspace_bytes_grouped",
-           "cba_conv_bn_act_backward_grouped", "cba_conv_bn_act_backward", "cba_conv_bn_act_backward_traced",
+           "cba_conv_bn_act_backward_grouped", "cba_conv_bn_act_backward_grouped_traced",
+           "cba_conv_bn_act_backward", "cba_conv_bn_act_backward_traced",
            "cba_get_status", "cba_bn_act_backward_noalloc",
            "cba_selftest_bounded_wait", "cba_yolo_backward", "cba_route_backward",
            "cba_pooled_size", "cba_maxpool_backward", "cba_error_string", "cba_last_cuda_error",
@@ -94,6 +95,10 @@ def load(path=LIB_PATH):
     L.cba_conv_bn_act_backward_grouped.restype = ctypes.c_int
     L.cba_conv_bn_act_backward_grouped.argtypes = ([ctypes.POINTER(cba_desc_t), ctypes.c_int] +
                                                    [vp] * 15 + [sz, vp])
+    L.cba_conv_bn_act_backward_grouped_traced.restype = ctypes.c_int
+    L.cba_conv_bn_act_backward_grouped_traced.argtypes = (
+        [ctypes.POINTER(cba_desc_t), ctypes.c_int] + [vp] * 15 + [sz, vp,
+                                                                ctypes.POINTER(ctypes.c_int)])
     L.cba_workspace_bytes_ex.restype = sz
     L.cba_workspace_bytes_ex.argtypes = [ctypes.POINTER(cba_desc_t), ctypes.c_uint]
     L.cba_conv_bn_act_backward.restype = ctypes.c_int
@@ -179,6 +184,22 @@ def cba_conv_bn_act_backward_grouped(desc, groups, x, output, z, delta, W, gamma
     if check and rc != CBA_OK:
         raise CbaError(rc, "cba_conv_bn_act_backward_grouped")
     return rc
+
+
+def cba_conv_bn_act_backward_grouped_traced(desc, groups, x, output, z, delta, W, gamma, mean,
+                                            var, residual, dW, db, dgamma, prev_delta, dz_out,
+                                            workspace, workspace_bytes=None, stream=None,
+                                            check=True):
+    """As cba_conv_bn_act_backward_grouped; returns (rc, kernels enqueued)."""
+    wsb = _bytes(workspace) if workspace_bytes is None else int(workspace_bytes)
+    n = ctypes.c_int(0)
+    rc = load().cba_conv_bn_act_backward_grouped_traced(
+        ctypes.byref(desc), int(groups), _ptr(x), _ptr(output), _ptr(z), _ptr(delta), _ptr(W),
+        _ptr(gamma), _ptr(mean), _ptr(var), _ptr(residual), _ptr(dW), _ptr(db), _ptr(dgamma),
+        _ptr(prev_delta), _ptr(dz_out), _ptr(workspace), wsb, _stream(stream), ctypes.byref(n))
+    if check and rc != CBA_OK:
+        raise CbaError(rc, "cba_conv_bn_act_backward_grouped_traced")
+    return rc, n.value
 
 
 def cba_conv_bn_act_backward(desc, x, output, z, delta, W, gamma, mean, var, residual, dW, db,

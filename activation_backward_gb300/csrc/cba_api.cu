@@ -333,7 +333,7 @@ int grouped_impl(const cba_desc_t *d, int groups, const float *x, const float *o
                  const float *z, const float *delta, const float *Wt, const float *gamma,
                  const float *mean, const float *var, const float *residual, float *dW,
                  float *db, float *dgamma, float *prev_delta, float *dz_out, void *workspace,
-                 size_t workspace_bytes, void *stream) {
+                 size_t workspace_bytes, void *stream, int *launches) {
     Plan p;
     int rc = make_plan(d, &p);
     if (rc != CBA_OK) return rc;
@@ -365,6 +365,7 @@ int grouped_impl(const cba_desc_t *d, int groups, const float *x, const float *o
     float *tdb = ws_at<float>(workspace, gp.off_vec + 3 * vstride);
     float *tdg = ws_at<float>(workspace, gp.off_vec + 4 * vstride);
     const size_t vb = f * (size_t)Kg, wb = f * (size_t)gp.wg;
+    int total_launches = 0;
     for (int g = 0; g < groups && e == cudaSuccess; ++g) {
         // in: the group's channel slices (strided by image), its weights and vectors
         e = copy_rows(tx, xrow, x + g * gp.xg, xpitch, xrow, N, st);
@@ -394,13 +395,15 @@ int grouped_impl(const cba_desc_t *d, int groups, const float *x, const float *o
                                     st);
         }
         if (e != cudaSuccess) break;
+        int n_group = 0;
         rc = backward_impl(&gp.dg, tx, (output && p.act_in != CBA_ACT_LINEAR) ? to : nullptr,
                            (p.bn && z) ? tz : nullptr, td, tw, p.bn ? tg : nullptr,
                            p.bn ? tm : nullptr, p.bn ? tv : nullptr, residual ? tr : nullptr, tdw,
                            tdb, p.bn ? tdg : nullptr, prev_delta ? tp : nullptr,
-                           dz_out ? tdz : nullptr, workspace, gp.sub, stream, nullptr, nullptr,
-                           g == 0);
+                           dz_out ? tdz : nullptr, workspace, gp.sub, stream, nullptr,
+                           &n_group, g == 0);
         if (rc != CBA_OK) return rc;
+        total_launches += n_group;
         // out: the accumulated weights and vectors, prev and dz slices
         e = cudaMemcpyAsync(dW + g * gp.wg, tdw, wb, cudaMemcpyDeviceToDevice, st);
         if (e == cudaSuccess)
@@ -413,6 +416,7 @@ int grouped_impl(const cba_desc_t *d, int groups, const float *x, const float *o
             e = copy_rows(dz_out + g * gp.og, opitch, tdz, orow, orow, N, st);
     }
     if (e != cudaSuccess) return fail_cuda(e);
+    if (launches) *launches = total_launches;
     return CBA_OK;
 }
 
@@ -426,12 +430,28 @@ int cba_conv_bn_act_backward_grouped(const cba_desc_t *d, int groups, const floa
                                      const float *var, const float *residual, float *dW,
                                      float *db, float *dgamma, float *prev_delta, float *dz_out,
                                      void *workspace, size_t workspace_bytes, void *stream) {
+    return cba_conv_bn_act_backward_grouped_traced(d, groups, x, output, z, delta, Wt, gamma,
+                                                   mean, var, residual, dW, db, dgamma,
+                                                   prev_delta, dz_out, workspace,
+                                                   workspace_bytes, stream, nullptr);
+}
+
+int cba_conv_bn_act_backward_grouped_traced(const cba_desc_t *d, int groups, const float *x,
+                                            const float *output, const float *z,
+                                            const float *delta, const float *Wt,
+                                            const float *gamma, const float *mean,
+                                            const float *var, const float *residual, float *dW,
+                                            float *db, float *dgamma, float *prev_delta,
+                                            float *dz_out, void *workspace,
+                                            size_t workspace_bytes, void *stream,
+                                            int *launches) {
     if (groups == 1)
         return backward_impl(d, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db,
                              dgamma, prev_delta, dz_out, workspace, workspace_bytes, stream,
-                             nullptr, nullptr);
+                             nullptr, launches);
     return grouped_impl(d, groups, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db,
-                        dgamma, prev_delta, dz_out, workspace, workspace_bytes, stream);
+                        dgamma, prev_delta, dz_out, workspace, workspace_bytes, stream,
+                        launches);
 }
 
 size_t cba_workspace_bytes_grouped(const cba_desc_t *d, int groups, unsigned flags) {

@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--layer", default="conv", choices=["conv", "maxpool", "route", "yolo"],
                     help="conv (default): the convolution layer backward; the others time "
                          "the data-movement layers' backward in GB/s")
+    ap.add_argument("--groups", type=int, default=1,
+                    help="run the workload (configs 1-4) as a grouped convolution")
     ap.add_argument("--z-free", action="store_true",
                     help="BN layers without z: the library recomputes z = conv(x, W)")
     ap.add_argument("--bn", default="batch", choices=["batch", "frozen"],
@@ -277,7 +279,9 @@ def workload_layers(args):
     """The layer calls of the workload; with --bn frozen, every BN layer gets
     frozen statistics (inputs.with_frozen_stats)."""
     from activation_backward_gb300 import ACT_NAMES, inputs
-    layers = inputs.make_config(args.config)
+    groups = getattr(args, "groups", 1)
+    layers = (inputs.make_config(args.config) if groups == 1
+              else [inputs.make_grouped_config(args.config, groups)])
     if getattr(args, "act", None):
         code = {v: k for k, v in ACT_NAMES.items()}[args.act]
         layers = [inputs.with_activation(l, code) for l in layers]
@@ -290,7 +294,7 @@ def workload_layers(args):
 def config_dict(args, layers, ws):
     from activation_backward_gb300 import ACT_NAMES
     g = layers[0]["geom"]
-    flops = sum(2 * l["geom"].gemm_flops() for l in layers)
+    flops = sum(2 * l["geom"].gemm_flops() // l.get("groups", 1) for l in layers)
     return {"workload": layers[0]["name"] if args.config != 5 else "residual_block",
             "N": g.N, "C": g.C, "H": g.H, "W": g.W, "K": g.K, "R": g.R, "S": g.S,
             "stride": g.stride, "pad": g.pad,
@@ -298,6 +302,7 @@ def config_dict(args, layers, ws):
             "act": ACT_NAMES[int(layers[0]["act"])],
             "z": "recomputed by the library (conv forward)" if getattr(args, "z_free", False)
                  else "given",
+            "groups": int(layers[0].get("groups", 1)),
             "gemm_gflop_per_step": flops / 1e9,
             "l2": "flushed before every step, outside the timing: 512 MiB write, then a 256 MiB "
                   "read sweep so no dirty flush lines are written back inside the step",
@@ -325,7 +330,7 @@ def run_ours(args):
 
     layers = workload_layers(args)
     dls = [DeviceLayer(l, math=math, device=dev, z_free=args.z_free) for l in layers]
-    flops = sum(2 * l["geom"].gemm_flops() for l in layers)
+    flops = sum(2 * l["geom"].gemm_flops() // l.get("groups", 1) for l in layers)
     red_bytes = sum(inputs.layer_bytes_reduce(l) for l in layers)
     flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     flush_rd = flush_buf[: 256 << 20].view(torch.int32)
@@ -384,53 +389,66 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = job_value(ws, flops, ms_per_step)
 
-    # per-phase device times (reduce, wgrad, dgrad) and the step time of
-    # direct, uncaptured calls: traced calls with events between the phases
-    nph = min(args.steps, 50)
-    phase = [[[mk() for _ in range(4)] for _ in dls] for _ in range(nph)]
-    d_starts = [mk() for _ in range(nph)]
-    d_ends = [mk() for _ in range(nph)]
-    for i in range(nph):
-        flush()
-        d_starts[i].record(stream)
-        step(phase[i])
-        d_ends[i].record(stream)
-    torch.cuda.synchronize()
-    direct_ms = sum(s.elapsed_time(e) for s, e in zip(d_starts, d_ends)) / nph
-    ph = {"reduce": 0.0, "wgrad": 0.0, "dgrad": 0.0}
-    for i in range(nph):
-        for ev in phase[i]:
-            ph["reduce"] += ev[0].elapsed_time(ev[1])
-            ph["wgrad"] += ev[1].elapsed_time(ev[2])
-            ph["dgrad"] += ev[2].elapsed_time(ev[3])
-    ph = {k: v / nph for k, v in ph.items()}
+    grouped = any(l.get("groups", 1) > 1 for l in layers)
+    if grouped:
+        # grouped calls record no phase events: the roofline is over the step
+        peaks, peak_src = load_peaks()
+        tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
+        achieved = flops / (ms_per_step * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": f"whole grouped step ({args.math})",
+                    "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
+                    "frac": achieved / tf32_peak, "traffic": None,
+                    "peak_source": f"{peak_src} bf16 {peaks['bf16_tflops']} x nominal "
+                                   f"tf32/bf16 1.1/2.25 (burst)"}
+        phases = None
+    else:
+        # per-phase device times (reduce, wgrad, dgrad) and the step time of
+        # direct, uncaptured calls: traced calls with events between the phases
+        nph = min(args.steps, 50)
+        phase = [[[mk() for _ in range(4)] for _ in dls] for _ in range(nph)]
+        d_starts = [mk() for _ in range(nph)]
+        d_ends = [mk() for _ in range(nph)]
+        for i in range(nph):
+            flush()
+            d_starts[i].record(stream)
+            step(phase[i])
+            d_ends[i].record(stream)
+        torch.cuda.synchronize()
+        direct_ms = sum(s.elapsed_time(e) for s, e in zip(d_starts, d_ends)) / nph
+        ph = {"reduce": 0.0, "wgrad": 0.0, "dgrad": 0.0}
+        for i in range(nph):
+            for ev in phase[i]:
+                ph["reduce"] += ev[0].elapsed_time(ev[1])
+                ph["wgrad"] += ev[1].elapsed_time(ev[2])
+                ph["dgrad"] += ev[2].elapsed_time(ev[3])
+        ph = {k: v / nph for k, v in ph.items()}
 
-    peaks, peak_src = load_peaks()
-    tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
-    gemm_half = flops / 2  # each of wgrad and dgrad carries half the FLOPs
-    dom = "wgrad" if ph["wgrad"] >= ph["dgrad"] else "dgrad"
-    achieved = gemm_half / (ph[dom] * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": f"{dom} phase ({args.math})", "achieved": achieved,
-                "peak": tf32_peak, "unit": "TFLOP/s", "frac": achieved / tf32_peak,
-                "traffic": profiled_traffic(dom) if args.config == 2 and args.math == "tf32"
-                else None,
-                "peak_source": f"{peak_src} bf16 {peaks['bf16_tflops']} x nominal tf32/bf16 "
-                               f"1.1/2.25 (burst)"}
-    red_gbs = red_bytes / (ph["reduce"] * 1e-3) / 1e9
-    gemm_ms = ph["wgrad"] + ph["dgrad"]
-    phases = {"reduce_ms": ph["reduce"], "wgrad_ms": ph["wgrad"], "dgrad_ms": ph["dgrad"],
-              "gemm_tflops": flops / (gemm_ms * 1e-3) / 1e12,
-              "gemm_frac_tf32": flops / (gemm_ms * 1e-3) / 1e12 / tf32_peak,
-              "reduce_gbs": red_gbs, "reduce_frac_hbm": red_gbs / peaks["hbm_gbs"],
-              "reduce_bytes": red_bytes, "from": "traced direct calls (events between phases)",
-              "direct_call_ms_per_step": direct_ms}
+        peaks, peak_src = load_peaks()
+        tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
+        gemm_half = flops / 2  # each of wgrad and dgrad carries half the FLOPs
+        dom = "wgrad" if ph["wgrad"] >= ph["dgrad"] else "dgrad"
+        achieved = gemm_half / (ph[dom] * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": f"{dom} phase ({args.math})", "achieved": achieved,
+                    "peak": tf32_peak, "unit": "TFLOP/s", "frac": achieved / tf32_peak,
+                    "traffic": profiled_traffic(dom) if args.config == 2 and args.math == "tf32"
+                    else None,
+                    "peak_source": f"{peak_src} bf16 {peaks['bf16_tflops']} x nominal tf32/bf16 "
+                                   f"1.1/2.25 (burst)"}
+        red_gbs = red_bytes / (ph["reduce"] * 1e-3) / 1e9
+        gemm_ms = ph["wgrad"] + ph["dgrad"]
+        phases = {"reduce_ms": ph["reduce"], "wgrad_ms": ph["wgrad"], "dgrad_ms": ph["dgrad"],
+                  "gemm_tflops": flops / (gemm_ms * 1e-3) / 1e12,
+                  "gemm_frac_tf32": flops / (gemm_ms * 1e-3) / 1e12 / tf32_peak,
+                  "reduce_gbs": red_gbs, "reduce_frac_hbm": red_gbs / peaks["hbm_gbs"],
+                  "reduce_bytes": red_bytes, "from": "traced direct calls (events between phases)",
+                  "direct_call_ms_per_step": direct_ms}
 
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(dls, layers, flops, args, stream, dev, math)
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+    if rank == 0 and not args.no_cpu_baseline and ws == 1 and not grouped:
         cpu = cpu_baseline(layers, args.cpu_seconds)
 
     g = layers[0]["geom"]

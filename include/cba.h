@@ -165,6 +165,16 @@ int cba_conv_bn_act_backward_grouped(const cba_desc_t *d, int groups, const floa
                                      float *db, float *dgamma, float *prev_delta, float *dz_out,
                                      void *workspace, size_t workspace_bytes, void *stream);
 size_t cba_workspace_bytes_grouped(const cba_desc_t *d, int groups, unsigned flags);
+/* The same, for profiling: launches (NULL, or) receives the number of kernels
+ * the call enqueued (the slice copies are not kernels). */
+int cba_conv_bn_act_backward_grouped_traced(const cba_desc_t *d, int groups, const float *x,
+                                            const float *output, const float *z,
+                                            const float *delta, const float *W,
+                                            const float *gamma, const float *mean,
+                                            const float *var, const float *residual, float *dW,
+                                            float *db, float *dgamma, float *prev_delta,
+                                            float *dz_out, void *workspace,
+                                            size_t workspace_bytes, void *stream, int *launches);
 
 /* Same computation as cba_conv_bn_act_backward, for profiling.
  * phase_events: NULL, or an array of 4 cudaEvent_t created by the caller;
