@@ -111,7 +111,17 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     if (p->act_pre) off = align_up(off + sizeof(float) * (size_t)nout, 256);
     p->total = off;
     p->off_z = off;
-    p->total_z = p->bn ? align_up(off + sizeof(float) * (size_t)nout, 256) : off;
+    p->fwd_tc = false;
+    if (p->bn) {
+        cba_desc_t dv;
+        Plan pv;
+        if (d->math == CBA_MATH_TF32 && forward_desc(*d, &dv) && make_plan(&dv, &pv) == CBA_OK &&
+            pv.use_tc2) {
+            p->fwd_tc = true;
+            p->off_z = align_up(std::max(off, pv.total), 256);
+        }
+    }
+    p->total_z = p->bn ? align_up(p->off_z + sizeof(float) * (size_t)nout, 256) : off;
     return CBA_OK;
 }
 
@@ -219,7 +229,18 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     if (e == cudaSuccess) e = tr.mark(0);
     if (e == cudaSuccess && z_free) {
         float *zbuf = ws_at<float>(workspace, p.off_z);
-        e = launch_conv_forward(p, x, Wt, zbuf, st, &n_launch);
+        cba_desc_t dv;
+        Plan pv;
+        if (p.fwd_tc && forward_desc(*d, &dv) && make_plan(&dv, &pv) == CBA_OK) {
+            e = launch_conv_forward_tc(pv, x, Wt, workspace, zbuf, st, &n_launch);
+            // the forward's scratch may overlap the reduction counters: zero them
+            // again (the status word keeps what the forward set)
+            if (e == cudaSuccess)
+                e = cudaMemsetAsync(ws_at<char>(workspace, p.off_cnt), 0,
+                                    p.clear_bytes - p.off_cnt, st);
+        } else {
+            e = launch_conv_forward(p, x, Wt, zbuf, st, &n_launch);
+        }
         z = zbuf;
     }
     if (e == cudaSuccess && p.act_pre) {

@@ -11,6 +11,7 @@
 // positions (4 x 4 per thread) and walks the reduction in slices of 16,
 // staging a W slice and an im2col slice of x in shared memory (double
 // buffered: the loads of slice i + 1 are in registers while slice i is used).
+#include <algorithm>
 #include <cstdint>
 
 #include "cba_internal.cuh"
@@ -118,7 +119,68 @@ __global__ void __launch_bounds__(kFThreads) conv_forward_kernel(const FwdArgs a
     }
 }
 
+// wr of the virtual convolution (K' = C, C' = K; [r][s][c'][k'], k' padded to
+// Kw' = round4(K')): W'[k'][c'][r][s] = W[c'][k'][R-1-r][S-1-s], TF32-rounded
+// (cvt.rna) as the input gradient's own weight repack rounds.
+__global__ void __launch_bounds__(256)
+    repack_flipped_kernel(const float *__restrict__ W, float *__restrict__ wr, int Kv, int Cv,
+                          int R, int S, int Kw) {
+    const long long total = (long long)R * S * Cv * Kw;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int kk = (int)(i % Kw);
+        long long t = i / Kw;
+        const int c = (int)(t % Cv);
+        t /= Cv;
+        const int s = (int)(t % S), r = (int)(t / S);
+        float v = 0.f;
+        if (kk < Kv) {
+            const float w = W[(((long long)c * Kv + kk) * R + (R - 1 - r)) * S + (S - 1 - s)];
+            uint32_t u;
+            asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(w));
+            v = __uint_as_float(u);
+        }
+        wr[i] = v;
+    }
+}
+
 }  // namespace
+
+bool forward_desc(const cba_desc_t &d, cba_desc_t *v) {
+    if (d.stride != 1 || d.R != d.S || d.pad > d.R - 1) return false;
+    const long long P = (long long)d.H + 2LL * d.pad - d.R + 1;
+    const long long Q = (long long)d.W + 2LL * d.pad - d.S + 1;
+    if (P <= 0 || Q <= 0 || P > (1 << 30) || Q > (1 << 30)) return false;
+    *v = d;
+    v->C = d.K;          // the forward's output channels are the virtual input channels
+    v->K = d.C;
+    v->H = (int)P;
+    v->W = (int)Q;
+    v->pad = d.R - 1 - d.pad;
+    v->act = CBA_ACT_LINEAR;
+    v->batch_normalize = 0;
+    v->accumulate = 0;   // z is written
+    v->math = CBA_MATH_TF32;
+    return true;
+}
+
+cudaError_t launch_conv_forward_tc(const Plan &pv, const float *x, const float *W, void *ws,
+                                   float *z, cudaStream_t st, int *launches) {
+    const int Kw = (pv.K + 3) / 4 * 4;
+    float *wr = ws_at<float>(ws, pv.off_wr);
+    const long long total = (long long)pv.R * pv.S * pv.C * Kw;
+    const unsigned blocks = (unsigned)std::min<long long>((total + 255) / 256, 1024);
+    repack_flipped_kernel<<<blocks, 256, 0, st>>>(W, wr, pv.K, pv.C, pv.R, pv.S, Kw);
+    cudaError_t e = cudaGetLastError();
+    *launches += 1;
+    float *dzt = ws_at<float>(ws, pv.off_dzt);
+    // x in the input gradient's channels-last, zero-bordered layout (the dz pass
+    // with a linear activation and no BN passes its input through)
+    if (e == cudaSuccess)
+        e = launch_dz_materialize(pv, x, nullptr, nullptr, ws, dzt, true, st, launches, false);
+    if (e == cudaSuccess) e = launch_dgrad_tc2(pv, dzt, nullptr, z, ws, wr, st, launches);
+    return e;
+}
 
 cudaError_t launch_conv_forward(const Plan &p, const float *x, const float *W, float *z,
                                 cudaStream_t st, int *launches) {

@@ -54,8 +54,11 @@ struct Plan {
     // status word at the start of every call; clear_bytes covers both)
     size_t off_status, off_cnt, clear_bytes, off_red, off_coef, off_wgpart, off_wt, off_dzt,
         off_wr, off_dprime, total;
-    // z-free calls (BN without z): z = conv(x, W) goes to off_z; total_z bytes
+    // z-free calls (BN without z): z = conv(x, W) goes to off_z; total_z bytes.
+    // fwd_tc: the forward runs on the tensor cores as the input gradient of a
+    // virtual convolution (forward_desc), whose workspace starts at 0
     size_t off_z, total_z;
+    bool fwd_tc;
 };
 
 // Builds the plan; returns CBA_OK or a CBA_ERR_* code.
@@ -77,6 +80,15 @@ cudaError_t launch_dz_out(const Plan &p, const float *delta, const float *output
 // z = conv(x, W), the pre-BN convolution output (cba_fwd.cu).
 cudaError_t launch_conv_forward(const Plan &p, const float *x, const float *W, float *z,
                                 cudaStream_t st, int *launches);
+// For stride 1, square kernels and pad <= R - 1: the forward is the input
+// gradient of the virtual convolution with C and K swapped, H x W = P x Q, pad
+// R - 1 - pad and the weights flipped and transposed.  Returns false when the
+// descriptor does not have that form.
+bool forward_desc(const cba_desc_t &d, cba_desc_t *virt);
+// z through the tensor-core input gradient of the virtual convolution (plan
+// pv); ws is the call's workspace (pv's regions from offset 0).
+cudaError_t launch_conv_forward_tc(const Plan &pv, const float *x, const float *W, void *ws,
+                                   float *z, cudaStream_t st, int *launches);
 // Data-movement layers (cba_layers.cu).
 int pooled_size(int in, int k, int stride, int pad);
 cudaError_t launch_yolo_backward(const float *l_delta, float *net_delta, long long n,
