@@ -91,14 +91,15 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     off = align_up(off + 256, 256);
     p->off_cnt = off;
     off = align_up(off + sizeof(unsigned) * (size_t)p->K, 256);
+    p->off_wgacc = off;
+    if (p->use_tc2) off = align_up(off + wgrad_tc4_ws_bytes(*p), 256);
     p->clear_bytes = off;
     p->off_red = off;
     off = align_up(off + sizeof(float) * 2 * (size_t)p->red_groups * p->red_pieces * p->K, 256);
     p->off_coef = off;
     off = align_up(off + sizeof(Coef) * (size_t)p->K, 256);
     p->off_wgpart = off;
-    size_t wg_simt = p->use_tc2 ? wgrad_tc4_ws_bytes(*p)
-                                : sizeof(float) * (size_t)p->wg_splits * p->K * p->CRS;
+    size_t wg_simt = p->use_tc2 ? 0 : sizeof(float) * (size_t)p->wg_splits * p->K * p->CRS;
     size_t wg_tc = p->use_tc ? sizeof(float) * (size_t)p->tc_wg_splits * p->K * p->CRS : 0;
     off = align_up(off + std::max(wg_simt, wg_tc), 256);
     p->off_wt = off;

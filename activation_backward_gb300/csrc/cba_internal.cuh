@@ -52,7 +52,10 @@ struct Plan {
     // workspace layout (byte offsets from the base)
     // off_cnt: per-channel arrival counters of the reduction (zeroed with the
     // status word at the start of every call; clear_bytes covers both)
-    size_t off_status, off_cnt, clear_bytes, off_red, off_coef, off_wgpart, off_wt, off_dzt,
+    // off_wgacc: the TMA-fed weight gradient's tile accumulators, inside the
+    // cleared prefix (zeroed with the counters)
+    size_t off_status, off_cnt, off_wgacc, clear_bytes, off_red, off_coef, off_wgpart, off_wt,
+        off_dzt,
         off_wr, off_dprime, total;
     // z-free calls (BN without z): z = conv(x, W) goes to off_z; total_z bytes.
     // fwd_tc: the forward runs on the tensor cores as the input gradient of a
@@ -143,7 +146,7 @@ bool tma_encode_f32(void *tmap, const void *base, int rank, const uint64_t *dims
                     const uint32_t *box, bool swizzle128);
 // Weight gradient with TMA-fed input rows (cba_wgrad4.cu).
 bool wgrad_tc4_supported(const Plan &p, const float *x);
-size_t wgrad_tc4_ws_bytes(const Plan &p);  // partial tiles (0 if the shape is not covered)
+size_t wgrad_tc4_ws_bytes(const Plan &p);  // tile accumulators (0 if the shape is not covered)
 cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, float *dW,
                              void *ws, cudaStream_t st, int *launches);
 cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, float *dW,

@@ -19,8 +19,9 @@
 // The ring keeps every x row once; rows that wrap around its end are also
 // stored in R - 1 mirror slots after it, so any R consecutive rows are
 // contiguous.  Padding rows and columns come from TMA's zero fill.
-// Each block writes its partial tile to the workspace; a second kernel sums
-// the partials of a tile in a fixed order into dW (deterministic).
+// Each block adds its tile into a per-tile accumulator in the workspace with
+// one bulk reduce-add (the L2 does the adds, in arrival order); a second
+// kernel adds the accumulators into dW.
 //
 // Roles: warp 0 issues the x-row TMA loads, warp 10 the dz-tile TMA loads
 // (one issuing thread costs a few hundred cycles per copy, so the two streams
@@ -51,12 +52,11 @@ struct W4Geom {
     bool ok;
     int cb, N, nctile, ktiles, ntiles, cpt, items, nwc, grid, kbox, nr, nd;
     uint32_t xslot_bytes, dz_bytes, dz_stride, dz_off;
-    size_t smem, part_bytes;
+    size_t smem, acc_bytes;
 };
 
 struct W4Args {
-    float *part;             // [tile][N][cpt][128] partial tiles (a tile's partials of one
-                             // column are contiguous for the reduction)
+    float *acc;              // [tile][N][128] tile accumulators (zeroed before the call)
     unsigned *status;
     int S, Pe, pad, nwc, Wx;
     int bq_lo, bd_lo;
@@ -349,28 +349,37 @@ __global__ void __launch_bounds__(kW4Threads, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[m % kW4NA]));
         }
-        // ---- epilogue: D[k][col] -> part[tile][col][split][k] (coalesced over k)
+        // ---- epilogue: D[k][col] -> shared memory [col][k] (the x ring is idle
+        // once every MMA has completed), then one bulk reduce-add of the tile
+        // into acc[tile]
         if (has_work && ok)
             ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
                                         kW4LimitNs);
         if (ok) ok = *reinterpret_cast<volatile int *>(&sb.abort_flag) == 0;
         ok = __all_sync(0xffffffffu, ok) && has_work;
+        float *stage = reinterpret_cast<float *>(smem);
         if (ok) {
             ptx::tc_fence_after();
-            float *dst = a.part + ((size_t)tile * a.N * a.cpt + split) * 128 + kl;
-            const size_t col_stride = (size_t)a.cpt * 128;
             for (int cc = g; cc * 16 < a.N; cc += 2) {
                 float v[16];
                 ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(cc * 16), v);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) dst[(size_t)(cc * 16 + e) * col_stride] = v[e];
+                for (int e = 0; e < 16; ++e) stage[(cc * 16 + e) * 128 + kl] = v[e];
             }
+            ptx::fence_proxy_async_smem();  // the bulk copy reads these writes
+        }
+        ok = ptx::named_bar_and(1, 256, ok);  // the eight epilogue warps
+        if (ok && warp == 2 && lane == 0) {
+            ptx::bulk_reduce_add_f32(a.acc + (size_t)tile * a.N * 128, ptx::smem_u32(stage),
+                                     (uint32_t)(a.N * 128 * sizeof(float)));
+            ptx::bulk_commit();
+            ptx::bulk_wait_read_all();  // shared memory is read before the block exits
         }
     }
     ptx::tc_fence_before();
     __syncthreads();
-    ptx::griddep_launch_dependents();  // the partial-tile sum may be scheduled
+    ptx::griddep_launch_dependents();  // the accumulator apply may be scheduled
     if (warp == 1) {
         __syncwarp();
         ptx::tc_fence_after();
@@ -378,54 +387,24 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     }
 }
 
-// dW[k0 + kl][c0 + c][r][s] += sum over the tile's blocks b of
-// part[tile][r * cb + c][b][kl].  One block per (tile, column): warp w
-// sums the blocks b = w, w + 8, ... for all 128 kl (a float4 per lane), then
-// warp 0 adds the eight warp sums in order (a fixed order: deterministic).
+// dW[k][c][r][s] += acc[tile][r * cb + c_local][k_local]: the tile accumulators
+// (tile = (k tile * nctile + c tile) * S + s) added into dW, one element per
+// thread, coalesced over k on the read.
 __global__ void __launch_bounds__(256)
-    wgrad_part_reduce_kernel(const float *__restrict__ part, int cpt, int N, int cb, int S,
-                             int nctile, int K, int C, int R, float *__restrict__ dW) {
-    ptx::griddep_wait();  // the partial tiles come from the weight-gradient kernel
-    __shared__ float4 red[8][32];
-    const int col = blockIdx.x % N, tile = blockIdx.x / N;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const float4 *src =
-        reinterpret_cast<const float4 *>(part + ((size_t)tile * N + col) * cpt * 128) + lane;
-    const size_t bstride = 32;  // float4s between consecutive blocks' partials
-    // every load of a round in flight together (8 per lane), then the adds in
-    // the order b = warp, warp + 8, ... (fixed)
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int b0 = warp; b0 < cpt; b0 += 64) {
-        float4 v[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int b = b0 + 8 * q;
-            v[q] = b < cpt ? __ldcg(src + (size_t)b * bstride) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            acc.x += v[q].x; acc.y += v[q].y; acc.z += v[q].z; acc.w += v[q].w;
-        }
-    }
-    red[warp][lane] = acc;
-    __syncthreads();
-    ptx::griddep_launch_dependents();  // the input gradient may be scheduled
-    if (warp == 0) {
-        float4 t = red[0][lane];
-#pragma unroll
-        for (int w = 1; w < 8; ++w) {
-            const float4 u = red[w][lane];
-            t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
-        }
+    wgrad_acc_apply_kernel(const float *__restrict__ acc, int N, int cb, int S, int nctile,
+                           int K, int C, int R, long long total, float *__restrict__ dW) {
+    ptx::griddep_wait();  // the accumulators come from the weight-gradient kernel
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += stride) {
+        const int kl = (int)(i & 127);
+        const long long tc = i >> 7;
+        const int col = (int)(tc % N);
+        const int tile = (int)(tc / N);
         const int s = tile % S, kc = tile / S;
         const int r = col / cb, c = (kc % nctile) * cb + col % cb;
-        if (c >= C) return;
-        const float vals[4] = {t.x, t.y, t.z, t.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int k = (kc / nctile) * 128 + lane * 4 + e;
-            if (k < K) dW[(((size_t)k * C + c) * R + r) * S + s] += vals[e];
-        }
+        const int k = (kc / nctile) * 128 + kl;
+        if (c < C && k < K) dW[(((size_t)k * C + c) * R + r) * S + s] += acc[i];
     }
 }
 
@@ -473,8 +452,10 @@ W4Geom w4_geom(const Plan &p) {
     w.nd = nd;
     const size_t dz_ring = (size_t)nd * w.dz_stride;
     w.dz_off = (uint32_t)((size_t)(nr + p.R - 1) * w.xslot_bytes);
-    w.smem = (size_t)w.dz_off + dz_ring + 1024;
-    w.part_bytes = (size_t)w.grid * w.N * 128 * sizeof(float);
+    // the epilogue stages a whole tile ([N][128] fp32) in the same memory
+    w.smem = std::max((size_t)w.dz_off + dz_ring, (size_t)w.N * 128 * sizeof(float)) + 1024;
+    if (w.smem > 227 * 1024) return w;
+    w.acc_bytes = (size_t)w.ntiles * w.N * 128 * sizeof(float);
     w.ok = true;
     return w;
 }
@@ -483,7 +464,7 @@ W4Geom w4_geom(const Plan &p) {
 
 size_t wgrad_tc4_ws_bytes(const Plan &p) {
     const W4Geom w = w4_geom(p);
-    return w.ok ? w.part_bytes : 0;
+    return w.ok ? w.acc_bytes : 0;
 }
 
 bool wgrad_tc4_supported(const Plan &p, const float *x) {
@@ -497,7 +478,7 @@ cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, fl
     if (!w.ok) return cudaErrorNotSupported;
     const DzcGeom g = dzc_geom(p);
     W4Args a;
-    a.part = ws_at<float>(ws, p.off_wgpart);
+    a.acc = ws_at<float>(ws, p.off_wgacc);
     a.status = ws_at<unsigned>(ws, p.off_status);
     a.S = p.S; a.Pe = g.Pe; a.pad = p.pad; a.nwc = w.nwc; a.Wx = g.We;
     a.bq_lo = g.bq_lo; a.bd_lo = g.bd_lo;
@@ -532,8 +513,10 @@ cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, fl
                        a);
     }
     if (e != cudaSuccess) return e;
-    e = launch_pdl(wgrad_part_reduce_kernel, dim3(w.ntiles * w.N), dim3(256), 0, st,
-                   (const float *)a.part, w.cpt, w.N, w.cb, p.S, w.nctile, p.K, p.C, p.R, dW);
+    const long long total = (long long)w.ntiles * w.N * 128;
+    const unsigned ablocks = (unsigned)std::min<long long>((total + 255) / 256, p.num_sms * 4LL);
+    e = launch_pdl(wgrad_acc_apply_kernel, dim3(ablocks), dim3(256), 0, st,
+                   (const float *)a.acc, w.N, w.cb, p.S, w.nctile, p.K, p.C, p.R, total, dW);
     if (e != cudaSuccess) return e;
     *launches += 2;
     return cudaGetLastError();
