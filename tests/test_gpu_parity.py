@@ -297,3 +297,25 @@ def test_bounded_wait_reports_timeout(cuda_lib):
     # the context is still usable
     layer = config_layers(1, 2)[0]
     run_gpu(layer, TF32)
+
+
+COMBOS = [(act, bn, zf, g, m) for act in (8, 6) for bn in (1, 2) for zf in (False, True)
+          for g in (1, 2) for m in (TF32, FFMA)]
+
+
+@pytest.mark.parametrize("act,bn,z_free,groups,math", COMBOS,
+                         ids=[f"a{a}_bn{b}_z{int(z)}_g{g}_{'tf32' if m == TF32 else 'ffma'}"
+                              for a, b, z, g, m in COMBOS])
+def test_parity_feature_combinations(ref, cuda_lib, act, bn, z_free, groups, math):
+    # the features that share workspace regions, together: another activation
+    # (delta' pass), frozen statistics, z recomputed, groups; a small 3x3 layer
+    base = (inputs.make_grouped_config(2, groups, batch=1) if groups > 1
+            else config_layers(2, 1)[0])
+    layer = inputs.with_activation(base, act)
+    if bn == 2:
+        layer = inputs.with_frozen_stats(layer, 40 + act)
+    _, got = run_gpu(layer, math, want_dz=True, z_free=z_free)
+    exp = oracle_chain(ref, layer, want_dz=True)
+    for k in KEYS + ("dz",):
+        if exp.get(k) is not None:
+            assert_close(got[k], exp[k], TOL[math], f"{layer['name']} {k}")
