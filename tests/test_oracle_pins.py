@@ -452,14 +452,48 @@ def test_bn_darknet_equals_caffe(ref):
 
 
 def test_mean_delta_is_the_printed_truncated_form(ref):
-    """mean_delta_cpu omits vd * sum(-2(x-mean))/m.  With a mean that is not the
-    batch mean the omission shows; with the batch mean it vanishes."""
-    z, mean, var, gamma, d = _bn_inputs(9)
-    K = z.shape[1]
-    md = np.empty(K)
-    ref.lib().cba_ref_mean_delta(ref.ref._pd(d), ref.ref._pd(var), EPS, z.shape[0], K,
-                                 z[0, 0].size, ref.ref._pd(md))
-    assert np.allclose(md, d.sum(axis=(0, 2, 3)) * (-1 / np.sqrt(var + EPS)), rtol=1e-13)
+    """mean_delta_cpu (YOLOv3 backprop page, §4) is the derivative through the
+    mean's direct use only: it leaves out vd * sum(-2(z - mean))/m, the part
+    that reaches the mean through the variance.  Take G = dL/dxhat fixed and
+    f(mu) = sum G * (z - mu) / sqrt(v(mu) + eps) with v(mu) = mean((z - mu)^2),
+    a mean that is NOT the batch mean.  The central difference of f is then
+    mean_delta + variance_delta * sum(-2(z - mu))/m, and mean_delta alone
+    misses it by that term; at the batch mean the term is rounding-level."""
+    z, _, _, _, G = _bn_inputs(9)
+    N, K, P, Q = z.shape
+    m = N * P * Q
+    rng = _rng(19)
+    mu = z.mean(axis=(0, 2, 3)) + rng.uniform(0.3, 0.6, K) * rng.choice([-1, 1], K)
+
+    def v_of(mv):
+        return ((z - mv[None, :, None, None]) ** 2).mean(axis=(0, 2, 3))
+
+    def f(mv):
+        return float(np.sum(G * (z - mv[None, :, None, None]) /
+                            np.sqrt(v_of(mv)[None, :, None, None] + EPS)))
+
+    def oracle_parts(mv):
+        var = v_of(mv)
+        md, vd = np.empty(K), np.empty(K)
+        L = ref.lib()
+        L.cba_ref_mean_delta(ref.ref._pd(G), ref.ref._pd(var), EPS, N, K, P * Q, ref.ref._pd(md))
+        L.cba_ref_variance_delta(ref.ref._pd(z), ref.ref._pd(G), ref.ref._pd(mv),
+                                 ref.ref._pd(var), EPS, N, K, P * Q, ref.ref._pd(vd))
+        return md, vd
+
+    # per channel, f's derivative in mu_k is the k-th component of the gradient
+    fd = central_diff(f, mu)
+    md, vd = oracle_parts(mu)
+    omitted = vd * (-2.0 * (z - mu[None, :, None, None])).sum(axis=(0, 2, 3)) / m
+    assert np.max(np.abs(md + omitted - fd)) <= 1e-6 * np.max(np.abs(fd))
+    assert np.min(np.abs(omitted)) > 1e-2 * np.max(np.abs(fd))  # the omission shows
+    assert np.max(np.abs(md - fd)) > 1e-2 * np.max(np.abs(fd))
+    # at the batch mean the omitted term vanishes up to rounding
+    mb = z.mean(axis=(0, 2, 3))
+    md_b, vd_b = oracle_parts(mb)
+    om_b = vd_b * (-2.0 * (z - mb[None, :, None, None])).sum(axis=(0, 2, 3)) / m
+    assert np.max(np.abs(om_b)) <= 1e-12 * np.max(np.abs(md_b))
+    assert np.max(np.abs(md_b - central_diff(f, mb))) <= 1e-6 * np.max(np.abs(md_b))
 
 
 def test_leaky_gradient_tie_at_zero(ref):
