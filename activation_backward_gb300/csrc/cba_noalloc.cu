@@ -49,17 +49,20 @@ inline bool misaligned16(const void *ptr) {
     return ptr != nullptr && (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0;
 }
 
-// The device the call runs on: the stream's device, else (NULL stream) the
-// device holding `ptr`; made current for this library's runtime.
+// The device the call runs on: the device that holds `ptr` (the call's data;
+// the stream must belong to the same device), made current for this
+// library's runtime.  The pointer query is also legal while the stream is
+// being captured into a CUDA graph, where asking the stream for its device is
+// not; the stream is asked only when there is no pointer.
 cudaError_t current_device_for(cudaStream_t stream, const void *ptr, int *dev) {
     cudaError_t e = cudaSuccess;
     int want = -1;
-    if (stream) {
-        e = cudaStreamGetDevice(stream, &want);
-    } else {
+    if (ptr) {
         cudaPointerAttributes a;
         e = cudaPointerGetAttributes(&a, ptr);
         if (e == cudaSuccess) want = a.device;
+    } else if (stream) {
+        e = cudaStreamGetDevice(stream, &want);
     }
     if (e != cudaSuccess) return e;
     int cur = -1;
@@ -74,7 +77,9 @@ cudaError_t current_device_for(cudaStream_t stream, const void *ptr, int *dev) {
 }
 
 // Set-up, once per device with that device current: the device address of the
-// scratch array.  The first call on each device does this.
+// scratch array.  The first call on each device does this, and the address is
+// kept for the life of the process: a cudaDeviceReset after that first call
+// (which may place the array elsewhere) is not supported.
 cudaError_t scratch_for_device(int dev, void **out) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_scratch_ptr[dev]) {

@@ -1,10 +1,13 @@
 """Benchmark of the conv + BN + activation backward on GB300.
 
-One step = one backward of the darknet 3x3 conv + BN + leaky layer
-(batch 16, 64 -> 128 channels, 52x52, stride 1, pad 1) through the C ABI:
+One step = one backward of the darknet residual block (batch 32 at 26x26:
+the 3x3 conv 256 -> 512 + BN + leaky with delta D, then the 1x1 conv
+512 -> 256 + BN + leaky with the shortcut D added into the block-input
+gradient), the largest of the five workloads, through the C ABI: per layer
 reduction pass -> dz -> wgrad -> dgrad, captured once into a CUDA graph and
 replayed (the per-phase split and the direct-call time come from traced calls
-without the graph).  Inputs are resident in HBM
+without the graph).  ``per_config`` repeats the measurement, with fewer steps,
+for each of the five workloads.  Inputs are resident in HBM
 when the timed region starts; L2 is flushed before every timed step, outside
 the per-step CUDA-event window: a 512 MiB write (evicts everything), then a
 256 MiB read sweep, so that the flush's own dirty lines are written back
@@ -48,7 +51,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=2, help="workload 1-5 (default 2)")
+    ap.add_argument("--config", type=int, default=5,
+                    help="workload 1-5 (default 5, the residual block, the largest)")
     ap.add_argument("--math", default="tf32", choices=["tf32", "ffma"])
     ap.add_argument("--act", default=None,
                     choices=["linear", "leaky", "logistic", "relu", "relie", "ramp", "tanh",
@@ -66,6 +70,8 @@ def parse():
                          "(training mode, default) or frozen ones (batch_normalize = 2)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config entries (configs 1-5, 1 GPU only)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for cpu_baseline")
     return ap.parse_args()
@@ -253,35 +259,38 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def profiled_traffic(phase):
-    """DRAM bytes per launch of a phase's kernels from the committed ncu summary,
-    or None when the kernel source has changed since that capture."""
+def profiled_traffic(phase, workload, layer):
+    """DRAM bytes per launch of a phase's kernels from a committed ncu summary
+    (a line "traffic: workload=W layer=L phase=P bytes=B source=F sha1=H" in
+    profiles/*.md; workload darknet_3x3 and layer 0 when absent), or None when
+    there is none or the kernel source has changed since that capture."""
+    import glob
     import hashlib
-    path = os.path.join(ROOT, "profiles", "darknet_3x3_tf32_kernels.md")
-    if not os.path.exists(path):
-        return None
-    for line in open(path):
-        if not line.startswith("traffic: "):
-            continue
-        f = dict(kv.split("=", 1) for kv in line.split()[1:])
-        if f.get("phase") != phase:
-            continue
-        src = os.path.join(ROOT, f["source"])
-        if not os.path.exists(src):
-            return None
-        if hashlib.sha1(open(src, "rb").read()).hexdigest() != f["sha1"]:
-            return None
-        return int(f["bytes"])
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        for line in open(path):
+            if not line.startswith("traffic: "):
+                continue
+            f = dict(kv.split("=", 1) for kv in line.split()[1:])
+            if (f.get("phase") != phase or f.get("workload", "darknet_3x3") != workload
+                    or int(f.get("layer", 0)) != layer):
+                continue
+            src = os.path.join(ROOT, f["source"])
+            if not os.path.exists(src):
+                return None
+            if hashlib.sha1(open(src, "rb").read()).hexdigest() != f["sha1"]:
+                return None
+            return int(f["bytes"])
     return None
 
 
-def workload_layers(args):
-    """The layer calls of the workload; with --bn frozen, every BN layer gets
-    frozen statistics (inputs.with_frozen_stats)."""
+def workload_layers(args, cid=None):
+    """The layer calls of workload `cid` (default: --config); with --bn frozen,
+    every BN layer gets frozen statistics (inputs.with_frozen_stats)."""
     from activation_backward_gb300 import ACT_NAMES, inputs
+    cid = args.config if cid is None else cid
     groups = getattr(args, "groups", 1)
-    layers = (inputs.make_config(args.config) if groups == 1
-              else [inputs.make_grouped_config(args.config, groups)])
+    layers = (inputs.make_config(cid) if groups == 1
+              else [inputs.make_grouped_config(cid, groups)])
     if getattr(args, "act", None):
         code = {v: k for k, v in ACT_NAMES.items()}[args.act]
         layers = [inputs.with_activation(l, code) for l in layers]
@@ -295,7 +304,7 @@ def config_dict(args, layers, ws):
     from activation_backward_gb300 import ACT_NAMES
     g = layers[0]["geom"]
     flops = sum(2 * l["geom"].gemm_flops() // l.get("groups", 1) for l in layers)
-    return {"workload": layers[0]["name"] if args.config != 5 else "residual_block",
+    return {"workload": workload_name(layers),
             "N": g.N, "C": g.C, "H": g.H, "W": g.W, "K": g.K, "R": g.R, "S": g.S,
             "stride": g.stride, "pad": g.pad,
             "bn": {0: False, 1: "batch statistics", 2: "frozen statistics"}[int(layers[0]["bn"])],
@@ -312,44 +321,72 @@ def config_dict(args, layers, ws):
 
 # ------------------------------------------------------------- GPU timing
 
-def run_ours(args):
+def tf32_cublas_peak(dev):
+    """Dense TF32 tensor-core rate of this GPU as cuBLAS reaches it: fp32
+    8192^3 matmuls with TF32 allowed, best of 10, CUDA events (2 * 8192^3
+    FLOPs each).  TFLOP/s."""
     import torch
-    import torch.distributed as dist
+    n = 8192
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        g = torch.Generator(device=dev).manual_seed(3)
+        a = torch.randn(n, n, device=dev, generator=g)
+        b = torch.randn(n, n, device=dev, generator=g)
+        c = torch.empty(n, n, device=dev)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = float("inf")
+        for _ in range(10):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            torch.matmul(a, b, out=c)
+            e.record()
+            e.synchronize()
+            best = min(best, s.elapsed_time(e))
+        del a, b, c
+        torch.cuda.empty_cache()
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    return 2 * n ** 3 / (best * 1e-3) / 1e12
+
+
+def tf32_peak(peaks, peak_src, measured_tf32):
+    """The TF32 denominator of every GEMM fraction: the larger of the measured
+    bf16 rate times the nominal tf32/bf16 ratio and the live cuBLAS TF32
+    measurement (the larger one gives the smaller, conservative fraction)."""
+    ratio = peaks["bf16_tflops"] * TF32_PER_BF16
+    src = (f"max of {peak_src} bf16 {peaks['bf16_tflops']} x nominal tf32/bf16 1.1/2.25 "
+           f"(= {ratio:.1f}) and cuBLAS TF32 fp32 8192^3 measured in this run")
+    if measured_tf32 is None:
+        return ratio, src.replace(" and cuBLAS TF32 fp32 8192^3 measured in this run", "")
+    return max(ratio, measured_tf32), src + f" (= {measured_tf32:.1f})"
+
+
+def time_workload(cid, args, dev, math, steps, warmup, stream, flush, phases=True,
+                  clocks=None, ws=1):
+    """Time one workload: its library call(s) captured into a CUDA graph and
+    replayed `steps` times, L2 flushed before each (outside the events); then
+    (if `phases`) traced direct calls with events between the phases of every
+    layer.  Returns a dict with the layers, device layers, ms per step, the
+    kernels per step and the per-layer phase times."""
+    import torch
 
     import activation_backward_gb300 as cba
-    from activation_backward_gb300 import inputs
     from activation_backward_gb300.layer import DeviceLayer, capture_graph
 
-    ws, rank, local = dist_env()
-    if ws > 1:
-        dist.init_process_group("nccl", init_method="env://")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    math = cba.CBA_MATH_TF32 if args.math == "tf32" else cba.CBA_MATH_FFMA
-    cba.load()
-
-    layers = workload_layers(args)
+    layers = workload_layers(args, cid)
     dls = [DeviceLayer(l, math=math, device=dev, z_free=args.z_free) for l in layers]
-    flops = sum(2 * l["geom"].gemm_flops() // l.get("groups", 1) for l in layers)
-    red_bytes = sum(inputs.layer_bytes_reduce(l) for l in layers)
-    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    flush_rd = flush_buf[: 256 << 20].view(torch.int32)
-
-    def flush():
-        flush_buf.zero_()
-        flush_rd.max()  # read sweep: L2 ends with clean lines
-
-    stream = torch.cuda.current_stream(dev)
 
     def step(events_per_layer=None):
         n = 0
         for i, dl in enumerate(dls):
-            if i > 0 and args.config == 5:
+            if i > 0 and cid == 5:
                 dl.delta.copy_(dls[0].prev)  # conv1's delta is conv2's prev_delta
             n += dl.run_traced(events_per_layer[i] if events_per_layer else None)
         return n
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush()
         step()
     torch.cuda.synchronize()
@@ -365,14 +402,15 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    starts = [mk() for _ in range(args.steps)]
-    ends = [mk() for _ in range(args.steps)]
-    clocks = ClockSampler(local)
+    starts = [mk() for _ in range(steps)]
+    ends = [mk() for _ in range(steps)]
     if ws > 1:
+        import torch.distributed as dist
         dist.barrier()
-    clocks.start()
+    if clocks is not None:
+        clocks.start()
     torch.cuda.synchronize()
-    for i in range(args.steps):
+    for i in range(steps):
         flush()
         starts[i].record(stream)
         graph.replay()
@@ -380,85 +418,168 @@ def run_ours(args):
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
-    clk = clocks.stop()
-    launches = launches_per_step * args.steps
+    clk = clocks.stop() if clocks is not None else None
     for dl in dls:
         assert dl.status() == cba.CBA_OK, "device status after the timed region"
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = max_over_ranks(sum(step_ms), ws, dev)
-    ms_per_step = total_ms / args.steps
-    value = job_value(ws, flops, ms_per_step)
-
+    out = dict(layers=layers, dls=dls, step_ms=step_ms, clocks=clk,
+               launches_per_step=launches_per_step, phases=None, direct_ms=None)
     grouped = any(l.get("groups", 1) > 1 for l in layers)
-    if grouped:
-        # grouped calls record no phase events: the roofline is over the step
-        peaks, peak_src = load_peaks()
-        tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
-        achieved = flops / (ms_per_step * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": f"whole grouped step ({args.math})",
-                    "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
-                    "frac": achieved / tf32_peak, "traffic": None,
-                    "peak_source": f"{peak_src} bf16 {peaks['bf16_tflops']} x nominal "
-                                   f"tf32/bf16 1.1/2.25 (burst)"}
-        phases = None
-    else:
-        # per-phase device times (reduce, wgrad, dgrad) and the step time of
-        # direct, uncaptured calls: traced calls with events between the phases
-        nph = min(args.steps, 50)
-        phase = [[[mk() for _ in range(4)] for _ in dls] for _ in range(nph)]
+    if phases and not grouped:
+        nph = min(steps, 50)
+        ev = [[[mk() for _ in range(4)] for _ in dls] for _ in range(nph)]
         d_starts = [mk() for _ in range(nph)]
         d_ends = [mk() for _ in range(nph)]
         for i in range(nph):
             flush()
             d_starts[i].record(stream)
-            step(phase[i])
+            step(ev[i])
             d_ends[i].record(stream)
         torch.cuda.synchronize()
-        direct_ms = sum(s.elapsed_time(e) for s, e in zip(d_starts, d_ends)) / nph
-        ph = {"reduce": 0.0, "wgrad": 0.0, "dgrad": 0.0}
-        for i in range(nph):
-            for ev in phase[i]:
-                ph["reduce"] += ev[0].elapsed_time(ev[1])
-                ph["wgrad"] += ev[1].elapsed_time(ev[2])
-                ph["dgrad"] += ev[2].elapsed_time(ev[3])
-        ph = {k: v / nph for k, v in ph.items()}
+        out["direct_ms"] = sum(s.elapsed_time(e) for s, e in zip(d_starts, d_ends)) / nph
+        per_layer = []
+        for li in range(len(dls)):
+            ph = {"reduce": 0.0, "wgrad": 0.0, "dgrad": 0.0}
+            for i in range(nph):
+                e = ev[i][li]
+                ph["reduce"] += e[0].elapsed_time(e[1])
+                ph["wgrad"] += e[1].elapsed_time(e[2])
+                ph["dgrad"] += e[2].elapsed_time(e[3])
+            per_layer.append({k: v / nph for k, v in ph.items()})
+        out["phases"] = per_layer
+    return out
 
-        peaks, peak_src = load_peaks()
-        tf32_peak = peaks["bf16_tflops"] * TF32_PER_BF16
-        gemm_half = flops / 2  # each of wgrad and dgrad carries half the FLOPs
-        dom = "wgrad" if ph["wgrad"] >= ph["dgrad"] else "dgrad"
-        achieved = gemm_half / (ph[dom] * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": f"{dom} phase ({args.math})", "achieved": achieved,
-                    "peak": tf32_peak, "unit": "TFLOP/s", "frac": achieved / tf32_peak,
-                    "traffic": profiled_traffic(dom) if args.config == 2 and args.math == "tf32"
-                    else None,
-                    "peak_source": f"{peak_src} bf16 {peaks['bf16_tflops']} x nominal tf32/bf16 "
-                                   f"1.1/2.25 (burst)"}
-        red_gbs = red_bytes / (ph["reduce"] * 1e-3) / 1e9
-        gemm_ms = ph["wgrad"] + ph["dgrad"]
-        phases = {"reduce_ms": ph["reduce"], "wgrad_ms": ph["wgrad"], "dgrad_ms": ph["dgrad"],
-                  "gemm_tflops": flops / (gemm_ms * 1e-3) / 1e12,
-                  "gemm_frac_tf32": flops / (gemm_ms * 1e-3) / 1e12 / tf32_peak,
-                  "reduce_gbs": red_gbs, "reduce_frac_hbm": red_gbs / peaks["hbm_gbs"],
-                  "reduce_bytes": red_bytes, "from": "traced direct calls (events between phases)",
-                  "direct_call_ms_per_step": direct_ms}
+
+def summarize(t, tf32, hbm):
+    """Per-workload figures from time_workload's result: the step, the phases
+    summed over the layers, the GEMM and reduction fractions, and per layer."""
+    from activation_backward_gb300 import inputs
+    layers = t["layers"]
+    flops = sum(2 * l["geom"].gemm_flops() // l.get("groups", 1) for l in layers)
+    ms = sum(t["step_ms"]) / len(t["step_ms"])
+    d = {"workload": workload_name(layers), "ms_per_step": ms,
+         "tflops": flops / (ms * 1e-3) / 1e12, "gemm_gflop_per_step": flops / 1e9}
+    if t["phases"] is None:
+        return d
+    red_bytes = sum(inputs.layer_bytes_reduce(l) for l in layers)
+    tot = {k: sum(p[k] for p in t["phases"]) for k in ("reduce", "wgrad", "dgrad")}
+    gemm_ms = tot["wgrad"] + tot["dgrad"]
+    d.update({"reduce_ms": tot["reduce"], "wgrad_ms": tot["wgrad"], "dgrad_ms": tot["dgrad"],
+              "gemm_tflops": flops / (gemm_ms * 1e-3) / 1e12,
+              "gemm_frac_tf32": flops / (gemm_ms * 1e-3) / 1e12 / tf32,
+              "reduce_gbs": red_bytes / (tot["reduce"] * 1e-3) / 1e9,
+              "reduce_frac_hbm": red_bytes / (tot["reduce"] * 1e-3) / 1e9 / hbm,
+              "reduce_bytes": red_bytes, "direct_call_ms_per_step": t["direct_ms"]})
+    if len(layers) > 1:
+        d["layers"] = []
+        for l, p in zip(layers, t["phases"]):
+            g = l["geom"]
+            half = g.gemm_flops()
+            d["layers"].append({
+                "conv": f"{g.R}x{g.S} {g.C}->{g.K}", "reduce_ms": p["reduce"],
+                "wgrad_ms": p["wgrad"], "dgrad_ms": p["dgrad"],
+                "wgrad_frac_tf32": half / (p["wgrad"] * 1e-3) / 1e12 / tf32,
+                "dgrad_frac_tf32": half / (p["dgrad"] * 1e-3) / 1e12 / tf32,
+                "reduce_frac_hbm": inputs.layer_bytes_reduce(l) / (p["reduce"] * 1e-3) / 1e9 / hbm})
+    return d
+
+
+def workload_name(layers):
+    return "residual_block" if len(layers) == 2 else layers[0]["name"]
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import activation_backward_gb300 as cba
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    math = cba.CBA_MATH_TF32 if args.math == "tf32" else cba.CBA_MATH_FFMA
+    cba.load()
+
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = flush_buf[: 256 << 20].view(torch.int32)
+
+    def flush():
+        flush_buf.zero_()
+        flush_rd.max()  # read sweep: L2 ends with clean lines
+
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+    measured_tf32 = tf32_cublas_peak(dev) if ws == 1 else None
+    tf32, tf32_src = tf32_peak(peaks, peak_src, measured_tf32)
+    hbm = peaks["hbm_gbs"]
+
+    t = time_workload(args.config, args, dev, math, args.steps, args.warmup, stream, flush,
+                      clocks=ClockSampler(local), ws=ws)
+    layers, dls = t["layers"], t["dls"]
+    flops = sum(2 * l["geom"].gemm_flops() // l.get("groups", 1) for l in layers)
+    total_ms = max_over_ranks(sum(t["step_ms"]), ws, dev)
+    ms_per_step = total_ms / args.steps
+    value = job_value(ws, flops, ms_per_step)
+    launches = t["launches_per_step"] * args.steps
+
+    if t["phases"] is None:
+        # grouped calls record no phase events: the roofline is over the step
+        achieved = flops / (ms_per_step * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": f"whole grouped step ({args.math})",
+                    "achieved": achieved, "peak": tf32, "unit": "TFLOP/s",
+                    "frac": achieved / tf32, "traffic": None, "peak_source": tf32_src}
+        phases = None
+    else:
+        # the dominant kernel phase: the (layer, GEMM) pair that takes longest
+        best = None
+        for li, (l, p) in enumerate(zip(layers, t["phases"])):
+            for ph in ("wgrad", "dgrad"):
+                if best is None or p[ph] > best[2]:
+                    best = (li, ph, p[ph])
+        li, dom, dom_ms = best
+        g = layers[li]["geom"]
+        achieved = g.gemm_flops() / (dom_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor",
+                    "kernel": f"{dom} phase ({args.math}) of the {g.R}x{g.S} {g.C}->{g.K} conv",
+                    "achieved": achieved, "peak": tf32, "unit": "TFLOP/s",
+                    "frac": achieved / tf32,
+                    "traffic": profiled_traffic(dom, workload_name(layers), li)
+                    if args.math == "tf32" else None,
+                    "peak_source": tf32_src,
+                    "frac_of_bf16_ratio": achieved / (peaks["bf16_tflops"] * TF32_PER_BF16)}
+        phases = summarize(t, tf32, hbm)
+
+    per_config = None
+    if ws == 1 and not args.no_per_config and args.layer == "conv" and args.groups == 1:
+        per_config = {}
+        for cid in range(1, 6):
+            if cid == args.config:
+                per_config[str(cid)] = phases
+                continue
+            tc = time_workload(cid, args, dev, math, min(args.steps, 50), max(3, args.warmup),
+                               stream, flush)
+            per_config[str(cid)] = summarize(tc, tf32, hbm)
+            del tc
 
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(dls, layers, flops, args, stream, dev, math)
 
     cpu = None
+    grouped = any(l.get("groups", 1) > 1 for l in layers)
     if rank == 0 and not args.no_cpu_baseline and ws == 1 and not grouped:
         cpu = cpu_baseline(layers, args.cpu_seconds)
 
-    g = layers[0]["geom"]
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None,
             "dtype": "tf32" if math == cba.CBA_MATH_TF32 else "f32", "data": "synthetic",
             "config": config_dict(args, layers, ws),
-            "roofline": roofline, "phases": phases, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clk}
+            "roofline": roofline, "phases": phases, "per_config": per_config,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": t["clocks"],
+            "tf32_cublas_tflops": measured_tf32}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

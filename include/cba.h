@@ -220,7 +220,9 @@ int cba_selftest_bounded_wait(void *workspace, size_t workspace_bytes, unsigned 
  * Scratch: one static 1 MiB device array inside the library, placed on every
  * device that loads the library and held until the process exits.  The first
  * call on each device looks up the array's address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  All
+ * that device current; make that first call before any stream capture.  The
+ * address is kept for the life of the process, so resetting the device
+ * (cudaDeviceReset) after the first call is not supported.  All
  * calls on a device share the array and it keeps the last call's contents;
  * each call first clears the reduction's per-channel counters (4 * K bytes,
  * a memset on the stream) and writes every other word before reading it.
@@ -232,7 +234,8 @@ int cba_selftest_bounded_wait(void *workspace, size_t workspace_bytes, unsigned 
  *   output [N,K,P,Q] required unless act = LINEAR; z, gamma, mean, var and
  *   dgamma required iff BN; delta required; db [K] += and dgamma [K] += ;
  *   dz_out [N,K,P,Q] receives dz when not NULL.  Device pointers, 16-byte
- *   aligned; stream = cudaStream_t (the NULL stream: the device of delta).
+ *   aligned; stream = cudaStream_t on the device that holds delta (the call
+ *   runs on that device).
  * Returns CBA_OK, CBA_ERR_ARG / CBA_ERR_ALIGN / CBA_ERR_UNSUPPORTED,
  * CBA_ERR_SCRATCH_LIMIT when K > CBA_NOALLOC_MAX_K (nothing is enqueued), or
  * CBA_ERR_CUDA. */

@@ -75,6 +75,81 @@ def test_noalloc_matches_the_workspace_entry_point_on_calls_in_a_row(cuda_lib):
     _check_one(inputs.with_activation(inputs.make_config(2, batch=2)[0], cba.CBA_ACT_ELU), 17)
 
 
+def _oracle_close(got, exp, what, tol=1e-5):
+    got = got.detach().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got)), what
+    err = float(np.max(np.abs(got - exp)))
+    scale = float(np.max(np.abs(exp)))
+    assert err <= tol * scale + 1e-30, f"{what}: max|err| {err:.3e} vs max|ref| {scale:.3e}"
+
+
+def _noalloc_vs_oracle(ref, layer, stream=None):
+    """One no-allocation call (db, dgamma starting from zero) against the
+    oracle's activation-gradient + BN backward on the same fp32 inputs, at the
+    fp32 bar of the FFMA mode (the pass does no TF32 rounding)."""
+    dl = DeviceLayer(layer, with_prev=False, want_dz=True)
+    db = torch.zeros_like(dl.db)
+    dgamma = torch.zeros_like(dl.dgamma) if dl.dgamma is not None else None
+    dz = torch.full_like(dl.dz, float("nan"))
+    torch.cuda.synchronize()  # the uploads are done before another stream reads them
+    rc = cba.cba_bn_act_backward_noalloc(dl.desc, dl.output, dl.z, dl.delta, dl.gamma, dl.mean,
+                                         dl.var, db, dgamma, dz, stream=stream)
+    assert rc == cba.CBA_OK
+    torch.cuda.synchronize()
+    e_dz, e_db, e_dg = ref.backward_dz(layer["output"], layer["z"], layer["delta"],
+                                       layer["gamma"], layer["mean"], layer["var"],
+                                       act=layer["act"], batch_normalize=layer["bn"],
+                                       eps=layer["eps"])
+    name = layer["name"]
+    _oracle_close(db, e_db, f"{name} db")
+    if dgamma is not None:
+        _oracle_close(dgamma, e_dg, f"{name} dgamma")
+    _oracle_close(dz, e_dz, f"{name} dz")
+
+
+@pytest.mark.gpu
+def test_noalloc_matches_the_oracle_including_the_largest_k_and_a_side_stream(ref, cuda_lib):
+    # config 2 (BN, leaky) and config 4 (no BN, 90% zero delta) on torch's
+    # current stream, against the oracle directly
+    _noalloc_vs_oracle(ref, inputs.make_config(2, batch=2)[0])
+    _noalloc_vs_oracle(ref, inputs.make_config(4, batch=2)[0])
+    # K at the limit with one spatial position and N = 8: the 1 MiB scratch then
+    # holds the counters (64 KiB), the coefficients (256 KiB) and only five
+    # partials per channel
+    spec = inputs.LayerSpec("noalloc_max_k", inputs.Geometry(8, 4, 1, 1, cba.CBA_NOALLOC_MAX_K,
+                                                             1, 1), cba.CBA_ACT_LEAKY, True)
+    _noalloc_vs_oracle(ref, inputs.make_layer(spec, 77))
+    # on a stream other than torch's current one: the call still runs on the
+    # device that holds delta, ordered on that stream
+    side = torch.cuda.Stream()
+    _noalloc_vs_oracle(ref, inputs.make_config(3, batch=1)[0], stream=side)
+
+
+@pytest.mark.gpu
+def test_noalloc_on_a_side_stream_matches_the_workspace_entry_point(cuda_lib):
+    layer = inputs.make_config(5, batch=2)[0]
+    dl = DeviceLayer(layer, with_prev=False, want_dz=True)
+    dl.run()
+    assert dl.status() == cba.CBA_OK
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    db = torch.zeros_like(dl.db)
+    dgamma = torch.zeros_like(dl.dgamma)
+    dz = torch.full_like(dl.dz, float("nan"))
+    # the workspace call added onto dl's zero-initialised db / dgamma
+    for _ in range(2):  # two calls in a row on the side stream
+        db.zero_()
+        dgamma.zero_()
+        side.wait_stream(torch.cuda.current_stream())
+        rc = cba.cba_bn_act_backward_noalloc(dl.desc, dl.output, dl.z, dl.delta, dl.gamma,
+                                             dl.mean, dl.var, db, dgamma, dz, stream=side)
+        assert rc == cba.CBA_OK
+        side.synchronize()
+        _close(db, dl.db, "side stream db")
+        _close(dgamma, dl.dgamma, "side stream dgamma")
+        _close(dz, dl.dz, "side stream dz")
+
+
 def test_noalloc_rejects_k_beyond_the_scratch_limit():
     """K > CBA_NOALLOC_MAX_K returns CBA_ERR_SCRATCH_LIMIT before any CUDA
     call: the pointers are never dereferenced (host-side check, no GPU)."""
