@@ -82,6 +82,7 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->wg_splits = (int)ceil_div(p->m, chunk);
 
     p->use_tc2 = (p->math == CBA_MATH_TF32) && tc2_supported(*p);
+    p->use_wnb = p->use_tc2 && wgrad_nb_supported(*p);
     p->use_tc = !p->use_tc2 && (p->math == CBA_MATH_TF32) && tc_supported(*p);
     if (p->use_tc) tc_plan(*p);
 
@@ -92,7 +93,8 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->off_cnt = off;
     off = align_up(off + sizeof(unsigned) * (size_t)p->K, 256);
     p->off_wgacc = off;
-    if (p->use_tc2) off = align_up(off + wgrad_tc4_ws_bytes(*p), 256);
+    if (p->use_tc2)
+        off = align_up(off + (p->use_wnb ? wgrad_nb_acc_bytes(*p) : wgrad_tc4_ws_bytes(*p)), 256);
     p->clear_bytes = off;
     p->off_red = off;
     off = align_up(off + sizeof(float) * 2 * (size_t)p->red_groups * p->red_pieces * p->K, 256);
@@ -110,6 +112,10 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     if (p->use_tc2) off = align_up(off + tc2_wr_bytes(*p), 256);
     p->off_dprime = off;
     if (p->act_pre) off = align_up(off + sizeof(float) * (size_t)nout, 256);
+    p->off_xn = off;
+    if (p->use_wnb) off = align_up(off + wgrad_nb_xn_bytes(*p), 256);
+    p->off_dzn = off;
+    if (p->use_wnb) off = align_up(off + wgrad_nb_dzn_bytes(*p), 256);
     p->total = off;
     p->off_z = off;
     p->fwd_tc = false;
@@ -261,6 +267,29 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     if (e == cudaSuccess && dz_out) {
         e = launch_dz_out(p, delta, output, z, workspace, dz_out, st);
         ++n_launch;
+    }
+    if (p.use_tc2 && p.use_wnb) {
+        // dz channels-last for the input gradient; x and dz batch-innermost for
+        // the weight gradient (its layout passes count in its phase)
+        float *dzt = ws_at<float>(workspace, p.off_dzt);
+        if (e == cudaSuccess && prev_delta)
+            e = launch_dz_materialize(p, delta, output, z, workspace, dzt, true, st, &n_launch,
+                                      false);
+        if (e == cudaSuccess) e = tr.mark(1);
+        float *xn = ws_at<float>(workspace, p.off_xn), *dzn = ws_at<float>(workspace, p.off_dzn);
+        if (e == cudaSuccess) e = launch_xn(p, x, xn, st, &n_launch);
+        if (e == cudaSuccess) e = launch_dzn(p, delta, output, z, workspace, dzn, st, &n_launch);
+        if (e == cudaSuccess)
+            e = launch_wgrad_nb(p, xn, dzn, dW, workspace, ws_at<float>(workspace, p.off_wgacc), st,
+                                &n_launch);
+        if (e == cudaSuccess) e = tr.mark(2);
+        if (e == cudaSuccess && prev_delta)
+            e = launch_dgrad_tc2(p, dzt, residual, prev_delta, workspace,
+                                 ws_at<float>(workspace, p.off_wr), st, &n_launch);
+        if (e == cudaSuccess) e = tr.mark(3);
+        if (launches) *launches = n_launch;
+        if (e != cudaSuccess) return fail_cuda(e);
+        return CBA_OK;
     }
     if (p.use_tc2) {
         float *dzt = ws_at<float>(workspace, p.off_dzt);

@@ -46,6 +46,8 @@ struct Plan {
     // tensor-core path
     int use_tc;   // tensor cores, gather-producer kernels (cba_tc.cu)
     int use_tc2;  // tensor cores, TMEM-operand kernels (cba_tc2.cu); preferred
+    int use_wnb;  // (with use_tc2) the weight gradient on batch-innermost layouts
+                  // (cba_wgrad_nb.cu): x and dz re-laid out at off_xn / off_dzn
     int tc_wg_splits, tc_wg_bn, tc_wg_ntiles;
     long long tc_wg_chunk;
     int tc_dg_bn, tc_dg_ntiles;
@@ -62,6 +64,7 @@ struct Plan {
     // virtual convolution (forward_desc), whose workspace starts at 0
     size_t off_z, total_z;
     bool fwd_tc;
+    size_t off_xn, off_dzn;  // batch-innermost x and dz (use_wnb)
 };
 
 // Builds the plan; returns CBA_OK or a CBA_ERR_* code.
@@ -144,6 +147,22 @@ DzcGeom dzc_geom(const Plan &p);
 // 128-byte swizzle or none.  `tmap` points to a CUtensorMap.
 bool tma_encode_f32(void *tmap, const void *base, int rank, const uint64_t *dims,
                     const uint32_t *box, bool swizzle128);
+// The same with the swizzle span in bytes: 0 (none), 64 or 128.
+bool tma_encode_f32_swz(void *tmap, const void *base, int rank, const uint64_t *dims,
+                        const uint32_t *box, int swizzle_bytes);
+// Weight gradient on batch-innermost layouts (cba_wgrad_nb.cu): xn
+// [nc][H][W][C][nb] and dzn [nc][P][Q][K][nb] (nb = 16 or 32 images, zeros past
+// N), written by launch_xn and launch_dzn; tile accumulators of
+// wgrad_nb_acc_bytes, zeroed before the call.
+bool wgrad_nb_supported(const Plan &p);
+size_t wgrad_nb_acc_bytes(const Plan &p);
+size_t wgrad_nb_xn_bytes(const Plan &p);
+size_t wgrad_nb_dzn_bytes(const Plan &p);
+cudaError_t launch_xn(const Plan &p, const float *x, float *xn, cudaStream_t st, int *launches);
+cudaError_t launch_dzn(const Plan &p, const float *delta, const float *output, const float *z,
+                       const void *ws, float *dzn, cudaStream_t st, int *launches);
+cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, float *dW, void *ws,
+                            float *acc, cudaStream_t st, int *launches);
 // Weight gradient with TMA-fed input rows (cba_wgrad4.cu).
 bool wgrad_tc4_supported(const Plan &p, const float *x);
 size_t wgrad_tc4_ws_bytes(const Plan &p);  // tile accumulators (0 if the shape is not covered)

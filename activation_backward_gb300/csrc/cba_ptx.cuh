@@ -88,6 +88,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Brings the line holding `p` into L2 (no register result, no wait).
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ------------------------------------------------------------ async proxy
 
 // Makes this thread's generic-proxy writes to shared memory visible to the

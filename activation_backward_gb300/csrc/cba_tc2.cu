@@ -740,16 +740,21 @@ __device__ __forceinline__ void dgrad_out_lane(const float *__restrict__ sl,
             for (int u = 0; u < 8; ++u)
                 if (cl + u < cl_hi) v[u] += sc[u * 128];
         }
+        // all loads before the first store (prev may alias residual as far as
+        // the compiler knows)
+        float add[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
+            add[u] = 0.f;
             if (cl + u < cl_hi) {
                 const long long idx = pix + (long long)(c0 + cl + u) * HW;
-                float o = v[u];
-                if (residual) o += residual[idx];
-                if (accumulate) o += prev[idx];
-                prev[idx] = o;
+                if (residual) add[u] += residual[idx];
+                if (accumulate) add[u] += prev[idx];
             }
         }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (cl + u < cl_hi) prev[pix + (long long)(c0 + cl + u) * HW] = v[u] + add[u];
     }
 }
 
@@ -1035,20 +1040,27 @@ __device__ __forceinline__ void d4_epilogue_batch(const D4Epi &E, int t0, uint64
         }
     }
     if (E.out) {
+        // every load of a chunk is issued before its first store: prev may
+        // alias residual as far as the compiler knows, so loads placed after a
+        // store would each wait a full memory latency
 #pragma unroll
         for (int t = 0; t < NB; ++t) {
             const int cc = E.eg + 2 * (t0 + t);
             const int nvalid = min(16, E.cl_all - cc * 16);
+            const long long idx0 = E.pix + (long long)(E.c0 + cc * 16) * E.HW;
+            float add[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
+                add[e] = 0.f;
                 if (e < nvalid) {
-                    const long long idx = E.pix + (long long)(E.c0 + cc * 16 + e) * E.HW;
-                    float o = v[t * NS][e];
-                    if (E.residual) o += E.residual[idx];
-                    if (E.accumulate) o += E.prev[idx];
-                    E.prev[idx] = o;
+                    const long long idx = idx0 + (long long)e * E.HW;
+                    if (E.residual) add[e] += __ldg(E.residual + idx);
+                    if (E.accumulate) add[e] += E.prev[idx];
                 }
             }
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (e < nvalid) E.prev[idx0 + (long long)e * E.HW] = v[t * NS][e] + add[e];
         }
     }
 }
@@ -1254,6 +1266,17 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                 pix = (long long)n * a.C * HW + (long long)(ii * a.stride + a.ph) * a.We +
                       (jj * a.stride + a.pw);
             }
+            if (out && (a.residual || a.accumulate)) {
+                // the values the epilogue adds are known before the MMAs finish:
+                // ask the L2 for this lane's share of them now, so that the
+                // loads below do not each wait a full memory latency
+                const float *src = a.residual ? a.residual : a.prev;
+                for (int t = 0; t < gch; ++t) {
+                    const long long c = c0 + (eg + 2 * t) * 16;
+                    const int nv = min(16, cl_all - (eg + 2 * t) * 16);
+                    for (int e = 0; e < nv; ++e) ptx::prefetch_l2(src + pix + (c + e) * HW);
+                }
+            }
             ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.acc_full[b]), (uint32_t)(i >> 1) & 1u,
                                         &sb.abort_flag, a.status, kLimitNs);
             // the group's 4 warps agree before the halo barriers below
@@ -1265,6 +1288,49 @@ __global__ void __launch_bounds__(kD4Threads, 1)
             E.c_tile = a.c_tile; E.eg = eg; E.wq = wq; E.lane = lane; E.span = span;
             E.dqr = dqr; E.pix = pix; E.HW = HW; E.c0 = c0; E.cl_all = cl_all; E.out = out;
             E.residual = a.residual; E.prev = a.prev; E.accumulate = a.accumulate;
+            if (ns == 1 && span == 0) {
+                // no column shift (one kernel column, e.g. 1x1 layers): each of
+                // the group's 16-channel chunks goes straight from TMEM to prev,
+                // one channel plane (HW apart) after the other (the values it
+                // adds were prefetched into L2 above)
+                const long long cstep = 32 * HW;  // this group's next chunk
+                const bool with_res = a.residual != nullptr, with_acc = a.accumulate != 0;
+                const long long off0 = pix + (long long)(c0 + eg * 16) * HW;
+                float *dst = a.prev + off0;
+                const float *res = with_res ? a.residual + off0 : a.prev;  // read only if with_res
+                for (int t = 0; t < gch; ++t, dst += cstep, res += cstep) {
+                    const int cc = eg + 2 * t;
+                    const int nvalid = min(16, cl_all - cc * 16);
+                    float add[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        add[e] = 0.f;
+                        if (out && e < nvalid) {
+                            if (with_res) add[e] += __ldg(res + e * HW);
+                            if (with_acc) add[e] += dst[e * HW];
+                        }
+                    }
+                    float v[16];
+                    ptx::tmem_ld16(E.tbase + (uint32_t)(cc * 16), v);
+                    ptx::tmem_ld_wait();
+                    if (t == gch - 1) {  // the unit's last loads: the MMAs may reuse it
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.acc_empty[b]));
+                    }
+                    if (out) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (e < nvalid) dst[e * HW] = v[e] + add[e];
+                    }
+                }
+                if (gch <= 0) {  // no chunk for this group: release at once
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.acc_empty[b]));
+                }
+                continue;
+            }
             int t0 = 0;
             do {  // at least once, so that the accumulator is always released
                 const int nb = min(bch, gch - t0);
@@ -1428,10 +1494,17 @@ DzcGeom dzc_geom(const Plan &p) {
     return d;
 }
 
-bool tma_encode_f32(void *tmap, const void *base, int rank, const uint64_t *dims,
-                    const uint32_t *box, bool swizzle128) {
+bool tma_encode_f32_swz(void *tmap, const void *base, int rank, const uint64_t *dims,
+                        const uint32_t *box, int swizzle_bytes) {
     EncodeTiledFn fn = encode_fn();
     if (!fn || rank < 1 || rank > 5) return false;
+    CUtensorMapSwizzle sw;
+    switch (swizzle_bytes) {
+    case 0: sw = CU_TENSOR_MAP_SWIZZLE_NONE; break;
+    case 64: sw = CU_TENSOR_MAP_SWIZZLE_64B; break;
+    case 128: sw = CU_TENSOR_MAP_SWIZZLE_128B; break;
+    default: return false;
+    }
     cuuint64_t d[5], strides[4];
     cuuint32_t b[5], es[5];
     uint64_t stride = 4;
@@ -1443,9 +1516,13 @@ bool tma_encode_f32(void *tmap, const void *base, int rank, const uint64_t *dims
         stride *= dims[i];
     }
     return fn(static_cast<CUtensorMap *>(tmap), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank,
-              const_cast<void *>(base), d, strides, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              const_cast<void *>(base), d, strides, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tma_encode_f32(void *tmap, const void *base, int rank, const uint64_t *dims,
+                    const uint32_t *box, bool swizzle128) {
+    return tma_encode_f32_swz(tmap, base, rank, dims, box, swizzle128 ? 128 : 0);
 }
 
 bool tc2_supported(const Plan &p) {

@@ -1,0 +1,651 @@
+// cba_wgrad_nb.cu -- weight gradient on batch-innermost operand layouts
+// (dW[k][c][r][s] += sum_{n,p,q} dz[n][k][p][q] x[n][c][p*st + r - pad][q*st + s - pad],
+// the gemm(0,1,...) of "YOLOv3反向传播原理 之 全流程源码分析" §3.1 over the
+// im2col_cpu columns of §3.2, without the column buffer).
+//
+// The contraction runs over (n, p, q).  Both operands are laid out with the
+// batch innermost, in chunks of nb = 16 or 32 images:
+//   xn  [nc][H][W][C][nb]   x, TF32-rounded, zeros for images past N
+//   dzn [nc][P][Q][K][nb]   the BN-input gradient dz, TF32-rounded
+// so one output position (p, q) with its nb images is one K-major operand
+// row per channel (nb * 4 = 64 or 128 bytes, 64- or 128-byte swizzle), and
+// every tap shift (r, s) and the stride move only the pixel coordinates,
+// which are not the innermost dimension: TMA loads them at any offset, and
+// padding is TMA's zero fill.  No thread touches an operand.
+//
+// A block owns one tile (KT k-tiles of 128 output channels = MMA M, cb input
+// channels, one kernel row r) and a range of contraction items (one output
+// position with its nb images each).  Per item:
+//   A = dzn[(j, p, q)][k0 .. k0 + 127][nb]       a slot of the A ring
+//   B = xn[j][h = p*st + r - pad][w0 .. w0 + S - 1][c0 .. c0 + cb - 1][nb]
+//       with w0 = q*st - pad: S consecutive pixels of the pixel ring, whose
+//       rows (s, c) are contiguous, so one MMA of N = S * cb covers all S
+//       kernel columns; the first pixels of the ring are mirrored after its
+//       end, so a window that wraps is still contiguous
+//   D[k][(s, c)] += A * B^T   (nb / 8 MMAs of K = 8 per k-tile)
+// Consecutive items of an output row share S - st of their pixels, so the
+// pixel ring loads st new pixels per item.  Each block adds its D tile into a
+// per-tile accumulator in the workspace with bulk reduce-adds (the L2 sums
+// the blocks of a tile); a second kernel adds the accumulators into dW.
+//
+// Roles: warp 0 issues the A loads, warp 2 the pixel loads, warp 1 the MMAs
+// (one thread), warps 4-7 run the epilogue (TMEM lanes 0-127).  Every wait is
+// bounded (2 s); on a timeout the block sets the workspace status bit and
+// stops.
+#include <cuda.h>
+
+#include <algorithm>
+
+#include "cba_internal.cuh"
+#include "cba_ptx.cuh"
+
+namespace cba {
+
+namespace {
+
+constexpr uint64_t kWnLimitNs = 2000000000ull;
+constexpr int kWnThreads = 256;
+constexpr int kWnMaxNA = 8;   // A ring slots
+constexpr int kWnMaxNG = 8;   // pixel-ring groups (the mirror comes on top)
+
+__device__ __forceinline__ float rna_tf32(float v) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
+}
+
+// ------------------------------------------------------- layout passes
+
+// One block transposes an (8 channels x 32 columns x nb images) tile of one
+// row: reads nb x 8 rows of 32 consecutive columns (coalesced), writes for
+// each column the 8 x nb contiguous values of [..][w][c][nb].  `Src` yields
+// the value of (image n, channel c, flat element offset).
+struct XSrc {
+    const float *x;
+    __device__ __forceinline__ float operator()(long long off, int) const { return __ldg(x + off); }
+};
+
+template <int ACT, bool BN>
+struct DzSrc {
+    const float *delta, *output, *z;
+    const Coef *coef;
+    __device__ __forceinline__ float operator()(long long off, int k) const {
+        const float y = (ACT == CBA_ACT_LEAKY) ? __ldg(output + off) : 0.f;
+        const float zz = BN ? __ldg(z + off) : 0.f;
+        return dz_of<ACT, BN>(__ldg(delta + off), y, zz, coef[k]);
+    }
+};
+
+// src: [N][CH][PLANE] (channels CH, PLANE = rows x columns flattened), dst:
+// [nc][PLANE][CH][NB].  grid: x = position chunks of 32, y = nc * channel
+// chunks of 8.  Each thread issues all of its NB loads before the first store
+// to shared memory.
+template <int NB, class Src>
+__global__ void __launch_bounds__(256)
+    batch_inner_kernel(Src src, int N, int CH, int PLANE, int cchunks, float *__restrict__ dst) {
+    ptx::griddep_wait();  // dz reads the reduction's coefficients
+    __shared__ float tile[32][8 * NB + 1];
+    const int t = threadIdx.x;
+    const int pos0 = blockIdx.x * 32;
+    const int j = blockIdx.y / cchunks, c0 = (blockIdx.y % cchunks) * 8;
+    constexpr int PER = NB * 8 * 32 / 256;
+    float v[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int e = t + u * 256;
+        const int pos = e & 31, rc = e >> 5;  // rc = n_local * 8 + c_local
+        const int n = j * NB + (rc >> 3), c = c0 + (rc & 7), pp = pos0 + pos;
+        v[u] = (n < N && c < CH && pp < PLANE)
+                   ? rna_tf32(src(((long long)n * CH + c) * PLANE + pp, c))
+                   : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int e = t + u * 256;
+        const int rc = e >> 5;
+        tile[e & 31][(rc & 7) * NB + (rc >> 3)] = v[u];
+    }
+    __syncthreads();
+    ptx::griddep_launch_dependents();
+    // write: for each position, channels c0 .. c0 + 7 x NB images are contiguous
+    const int ncl = min(8, CH - c0);
+    for (int e = t; e < 32 * 8 * NB; e += 256) {
+        const int pos = e / (8 * NB), vv = e % (8 * NB);
+        const int pp = pos0 + pos;
+        if (pp < PLANE && vv < ncl * NB)
+            dst[(((long long)j * PLANE + pp) * CH + c0) * NB + vv] = tile[pos][vv];
+    }
+}
+
+}  // namespace
+
+namespace {
+
+struct WnArgs {
+    float *acc;             // [unit][KT][cols][128] tile accumulators (zeroed before the call)
+    unsigned *status;
+    int P, Q, R, S, stride, pad;
+    int ctiles, KT, cb, cols;  // cols = S * cb = the MMA's N
+    int splits;             // blocks per tile
+    long long items;        // nc * P * Q
+    int Qa, NA;             // positions per A box, A ring slots
+    int G, NG;              // pixels per group, pixel-ring groups (mirror group after them)
+    int mirror;             // 1 when S > 1 (a window may wrap the ring)
+    uint32_t rb;            // operand row bytes (nb * 4)
+    uint32_t swz;           // shared-memory descriptor swizzle code
+    uint32_t a_pos_bytes;   // 128 * rb: one position of one k-tile
+    uint32_t a_slot_bytes;  // KT * Qa * a_pos_bytes
+    uint32_t pix_bytes;     // cb * rb
+    uint32_t grp_bytes;     // G * pix_bytes
+    uint32_t b_off;         // byte offset of the pixel ring
+};
+
+struct WnBars {
+    uint64_t a_full[kWnMaxNA], a_empty[kWnMaxNA];
+    uint64_t b_full[kWnMaxNG], b_empty[kWnMaxNG];
+    uint64_t accum;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+// Items are output positions in (j, p, q) order, q fastest; a run is the
+// part of one output row (j, p) inside a block's range.  Every role walks
+// the runs the same way: A boxes of up to Qa positions from the start of each
+// run, pixel groups of G pixels from the run's first window.
+struct Run {
+    long long row;  // j * P + p
+    int qa, qb;     // positions qa .. qb - 1 of the row
+};
+
+__device__ __forceinline__ Run run_at(long long i, long long i1, int Q) {
+    Run u;
+    u.row = i / Q;
+    u.qa = (int)(i - u.row * Q);
+    u.qb = (int)(min(i1, (u.row + 1) * Q) - u.row * Q);
+    return u;
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kWnThreads, 1)
+    wgrad_nb_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
+                    const WnArgs a) {
+    extern __shared__ uint8_t smem_dyn[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
+    __shared__ WnBars sb;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int unit = blockIdx.x / a.splits, split = blockIdx.x % a.splits;
+    const int r = unit % a.R;
+    const int ct = (unit / a.R) % a.ctiles;
+    const int kt = unit / (a.R * a.ctiles);
+    const int k0 = kt * a.KT * 128, c0 = ct * a.cb;
+    const long long i0 = split * a.items / a.splits, i1 = (split + 1) * a.items / a.splits;
+    const bool has_work = i1 > i0;
+    uint8_t *aring = smem;
+    uint8_t *bring = smem + a.b_off;
+    const int ring_pix = a.NG * a.G;  // pixel slots before the mirror
+
+    if (tid == 0) {
+        for (int i = 0; i < kWnMaxNA; ++i) {
+            ptx::mbar_init(ptx::smem_u32(&sb.a_full[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sb.a_empty[i]), 1);
+        }
+        for (int i = 0; i < kWnMaxNG; ++i) {
+            ptx::mbar_init(ptx::smem_u32(&sb.b_full[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sb.b_empty[i]), 1);
+        }
+        ptx::mbar_init(ptx::smem_u32(&sb.accum), 1);
+        sb.abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        const uint32_t need = (uint32_t)(a.KT * a.cols);
+        uint32_t ncols = 32;
+        while (ncols < need) ncols <<= 1;
+        ptx::tmem_alloc(ptx::smem_u32(&sb.tmem_base), ncols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = sb.tmem_base;
+    // the operand layouts come from the previous kernels
+    ptx::griddep_wait();
+
+    if (warp == 0) {
+        // ---- A loads: boxes of up to Qa positions x KT k-tiles
+        if (lane == 0 && has_work) {
+            int slot = 0, issued = 0;
+            uint32_t ph = 0;  // parity of the slot's previous release
+            bool ok = true;
+            for (long long i = i0; ok && i < i1;) {
+                const Run rn = run_at(i, i1, a.Q);
+                const int j = (int)(rn.row / a.P), p = (int)(rn.row - (long long)j * a.P);
+                for (int q = rn.qa; q < rn.qb; q += a.Qa) {
+                    if (issued >= a.NA)
+                        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_empty[slot]), ph,
+                                                    &sb.abort_flag, a.status, kWnLimitNs);
+                    if (!ok) break;
+                    const uint32_t bar = ptx::smem_u32(&sb.a_full[slot]);
+                    ptx::mbar_arrive_expect_tx(bar, a.a_slot_bytes);
+                    for (int t = 0; t < a.KT; ++t)
+                        ptx::tma_load_4d(ptx::smem_u32(aring + (size_t)slot * a.a_slot_bytes +
+                                                       (size_t)t * a.Qa * a.a_pos_bytes),
+                                         &tma, 0, k0 + t * 128, q, j * a.P + p, bar);
+                    ++issued;
+                    if (++slot == a.NA) {
+                        slot = 0;
+                        if (issued > a.NA) ph ^= 1u;
+                    }
+                }
+                i = rn.row * a.Q + rn.qb;
+            }
+            // no copy may be in flight when the block exits: wait for the last
+            // min(issued, NA) copies (slot, phase counted back from the end)
+            int no_abort = 0;
+            for (int v = issued > a.NA ? issued - a.NA : 0; v < issued; ++v)
+                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_full[v % a.NA]),
+                                       (uint32_t)((v / a.NA) & 1), &no_abort, a.status,
+                                       kWnLimitNs);
+        }
+    } else if (warp == 2) {
+        // ---- pixel loads: per run, groups of G pixels from its first window
+        if (lane == 0 && has_work) {
+            int gs = 0, issued = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (long long i = i0; ok && i < i1;) {
+                const Run rn = run_at(i, i1, a.Q);
+                const int j = (int)(rn.row / a.P), p = (int)(rn.row - (long long)j * a.P);
+                const int h = p * a.stride + r - a.pad;
+                const int wa = rn.qa * a.stride - a.pad;
+                const int npix = (rn.qb - 1 - rn.qa) * a.stride + a.S;
+                const int ng = (npix + a.G - 1) / a.G;
+                for (int g = 0; g < ng; ++g) {
+                    if (issued >= a.NG)
+                        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.b_empty[gs]), ph,
+                                                    &sb.abort_flag, a.status, kWnLimitNs);
+                    if (!ok) break;
+                    const bool mir = a.mirror && gs == 0;
+                    const uint32_t bar = ptx::smem_u32(&sb.b_full[gs]);
+                    ptx::mbar_arrive_expect_tx(bar, a.grp_bytes * (mir ? 2u : 1u));
+                    ptx::tma_load_5d(ptx::smem_u32(bring + (size_t)gs * a.grp_bytes), &tmb, 0, c0,
+                                     wa + g * a.G, h, j, bar);
+                    if (mir)
+                        ptx::tma_load_5d(ptx::smem_u32(bring + (size_t)a.NG * a.grp_bytes), &tmb,
+                                         0, c0, wa + g * a.G, h, j, bar);
+                    ++issued;
+                    if (++gs == a.NG) {
+                        gs = 0;
+                        if (issued > a.NG) ph ^= 1u;
+                    }
+                }
+                i = rn.row * a.Q + rn.qb;
+            }
+            int no_abort = 0;
+            for (int v = issued > a.NG ? issued - a.NG : 0; v < issued; ++v)
+                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.b_full[v % a.NG]),
+                                       (uint32_t)((v / a.NG) & 1), &no_abort, a.status,
+                                       kWnLimitNs);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issue (one thread): per item KT x NB/8 MMAs of N = S * cb;
+        // an A slot is released after its last position, a pixel group once
+        // no later window of the run reaches it.  The loop keeps only
+        // incremental counters (ring slots, parities, the window's ring pixel)
+        // and adds 16-byte offsets to two precomputed descriptors.
+        if (lane == 0 && has_work) {
+            constexpr int KS = NB / 8;  // K = 8 steps per operand row
+            const uint32_t idesc = ptx::idesc_tf32(128, a.cols);
+            const uint32_t sbo = 8 * a.rb;
+            const uint64_t da0 = ptx::smem_desc(ptx::smem_u32(aring), 16, sbo, a.swz);
+            const uint64_t db0 = ptx::smem_desc(ptx::smem_u32(bring), 16, sbo, a.swz);
+            const uint32_t a_slot16 = a.a_slot_bytes >> 4, a_pos16 = a.a_pos_bytes >> 4;
+            const uint32_t a_t16 = ((uint32_t)a.Qa * a.a_pos_bytes) >> 4, pix16 = a.pix_bytes >> 4;
+            int a_slot = 0, g_wslot = 0, g_rslot = 0, ps_run = 0;
+            uint32_t a_ph = 0, g_wph = 0;
+            bool ok = true, first = true;
+            for (long long i = i0; ok && i < i1;) {
+                const Run rn = run_at(i, i1, a.Q);
+                const int npix = (rn.qb - 1 - rn.qa) * a.stride + a.S;
+                const int ng = (npix + a.G - 1) / a.G;
+                int waited = 0, released = 0;  // groups of this run
+                int ps = ps_run;               // ring pixel of the item's window
+                int u0 = 0;                    // run pixel of the item's window
+                for (int qbox = rn.qa; ok && qbox < rn.qb; qbox += a.Qa) {
+                    ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_full[a_slot]), a_ph,
+                                                &sb.abort_flag, a.status, kWnLimitNs);
+                    const int qend = min(qbox + a.Qa, rn.qb);
+                    uint32_t a_off = (uint32_t)a_slot * a_slot16;
+                    for (int q = qbox; ok && q < qend; ++q, a_off += a_pos16) {
+                        for (; ok && waited * a.G < u0 + a.S; ++waited) {
+                            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.b_full[g_wslot]), g_wph,
+                                                        &sb.abort_flag, a.status, kWnLimitNs);
+                            if (++g_wslot == a.NG) {
+                                g_wslot = 0;
+                                g_wph ^= 1u;
+                            }
+                        }
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                        const uint64_t db = db0 + (uint64_t)((uint32_t)ps * pix16);
+                        for (int t = 0; t < a.KT; ++t) {
+                            const uint64_t da = da0 + (uint64_t)(a_off + (uint32_t)t * a_t16);
+#pragma unroll
+                            for (int ks = 0; ks < KS; ++ks)
+                                ptx::mma_tf32(tmem + (uint32_t)(t * a.cols), da + 2 * ks,
+                                              db + 2 * ks, idesc, (first && ks == 0) ? 0u : 1u);
+                        }
+                        first = false;
+                        u0 += a.stride;
+                        ps += a.stride;
+                        while (ps >= ring_pix) ps -= ring_pix;
+                        // groups that end before the next window are done
+                        for (; released < ng && (released + 1) * a.G <= u0; ++released) {
+                            ptx::mma_commit(ptx::smem_u32(&sb.b_empty[g_rslot]));
+                            if (++g_rslot == a.NG) g_rslot = 0;
+                        }
+                    }
+                    if (!ok) break;
+                    ptx::mma_commit(ptx::smem_u32(&sb.a_empty[a_slot]));
+                    if (++a_slot == a.NA) {
+                        a_slot = 0;
+                        a_ph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                for (; released < ng; ++released) {  // the rest of the run's groups
+                    ptx::mma_commit(ptx::smem_u32(&sb.b_empty[g_rslot]));
+                    if (++g_rslot == a.NG) g_rslot = 0;
+                }
+                ps_run += ng * a.G;
+                while (ps_run >= ring_pix) ps_run -= ring_pix;
+                i = rn.row * a.Q + rn.qb;
+            }
+            if (!ok) {  // the epilogue must not take the drain below for a result
+                *reinterpret_cast<volatile int *>(&sb.abort_flag) = 1;
+                __threadfence_block();
+            }
+            // drain: every MMA issued has finished before TMEM is released
+            ptx::mma_commit(ptx::smem_u32(&sb.accum));
+            int no_abort = 0;
+            ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &no_abort, a.status, kWnLimitNs);
+        }
+    } else if (warp >= 4) {
+        // ---- epilogue: D[k][col] of each k-tile -> shared memory [col][k] (the
+        // rings are idle once every MMA has completed), then one bulk
+        // reduce-add of the tile into its accumulator
+        const int wq = warp & 3;
+        const int kl = wq * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        bool ok = has_work;
+        if (ok)
+            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
+                                        kWnLimitNs);
+        if (ok) ok = *reinterpret_cast<volatile int *>(&sb.abort_flag) == 0;
+        ok = __all_sync(0xffffffffu, ok);
+        float *stage = reinterpret_cast<float *>(smem);
+        for (int t = 0; t < a.KT; ++t) {
+            if (ok) {
+                ptx::tc_fence_after();
+                for (int cc = 0; cc * 16 < a.cols; ++cc) {
+                    float v[16];
+                    ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(t * a.cols + cc * 16), v);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) stage[(cc * 16 + e) * 128 + kl] = v[e];
+                }
+                ptx::fence_proxy_async_smem();  // the bulk copy reads these writes
+            }
+            ok = ptx::named_bar_and(1, 128, ok);
+            if (ok && warp == 4 && lane == 0) {
+                ptx::bulk_reduce_add_f32(a.acc + ((size_t)unit * a.KT + t) * a.cols * 128,
+                                         ptx::smem_u32(stage),
+                                         (uint32_t)(a.cols * 128 * sizeof(float)));
+                ptx::bulk_commit();
+                ptx::bulk_wait_read_all();  // the stage is read before it is reused
+            }
+            ptx::named_bar_sync(1, 128);
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::griddep_launch_dependents();  // the accumulator apply may be scheduled
+    if (warp == 1) {
+        __syncwarp();
+        ptx::tc_fence_after();
+        const uint32_t need = (uint32_t)(a.KT * a.cols);
+        uint32_t ncols = 32;
+        while (ncols < need) ncols <<= 1;
+        ptx::tmem_dealloc(tmem, ncols);
+    }
+}
+
+// dW[k][c][r][s] += acc[unit][t][s * cb + cl][kl] with unit = (kt * ctiles +
+// ct) * R + r, k = (kt * KT + t) * 128 + kl, c = ct * cb + cl: one thread per
+// dW element in dW order (coalesced read-modify-write of dW; the scattered
+// reads of the accumulators hit the L2).
+__global__ void __launch_bounds__(256)
+    wgrad_nb_apply_kernel(const float *__restrict__ acc, int KT, int cols, int cb, int S, int R,
+                          int ctiles, int C, long long total, float *__restrict__ dW) {
+    ptx::griddep_wait();  // the accumulators come from the weight-gradient kernel
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    const int RS = R * S;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += stride) {
+        const long long kc = i / RS;
+        const int rs = (int)(i - kc * RS);
+        const int r = rs / S, s = rs - r * S;
+        const int k = (int)(kc / C), c = (int)(kc - (long long)k * C);
+        const int kt = k / (128 * KT), t = (k >> 7) - kt * KT, kl = k & 127;
+        const int ct = c / cb, cl = c - ct * cb;
+        const long long unit = ((long long)kt * ctiles + ct) * R + r;
+        dW[i] += acc[((unit * KT + t) * cols + s * cb + cl) * 128 + kl];
+    }
+}
+
+}  // namespace
+
+namespace {
+
+struct WnGeom {
+    bool ok;
+    int nb, nc, cb, cols, KT, ktiles, ctiles, units, splits, grid;
+    long long items;
+    int Qa, NA, G, NG;
+    uint32_t rb, a_pos_bytes, a_slot_bytes, pix_bytes, grp_bytes, b_off;
+    size_t smem, acc_bytes, xn_bytes, dzn_bytes;
+};
+
+WnGeom wn_geom(const Plan &p) {
+    WnGeom w{};
+    w.ok = false;
+    if (p.S > 16 || p.R > 64) return w;
+    w.nb = p.N <= 16 ? 16 : 32;
+    w.nc = (p.N + w.nb - 1) / w.nb;
+    w.rb = (uint32_t)w.nb * 4;
+    // input channels per block: a multiple of 16 with S * cb <= 256 (one MMA),
+    // the one that pads C least (the larger on a tie)
+    const int cap = (256 / p.S) / 16 * 16;
+    if (cap < 16) return w;
+    int best = 16;
+    long long best_pad = (long long)((p.C + 15) / 16) * 16;
+    for (int cb = 32; cb <= cap; cb += 16) {
+        const long long pad = (long long)((p.C + cb - 1) / cb) * cb;
+        if (pad <= best_pad) {
+            best = cb;
+            best_pad = pad;
+        }
+    }
+    w.cb = best;
+    w.cols = p.S * w.cb;
+    // two k-tiles per block share every pixel when both accumulators fit
+    w.KT = (p.K > 128 && 2 * w.cols <= 512) ? 2 : 1;
+    w.ktiles = (p.K + 128 * w.KT - 1) / (128 * w.KT);
+    w.ctiles = (p.C + w.cb - 1) / w.cb;
+    const long long units = (long long)w.ktiles * w.ctiles * p.R;
+    w.items = (long long)w.nc * p.P * p.Q;
+    if (units >= (1 << 20) || w.items >= (1LL << 40)) return w;
+    w.units = (int)units;
+    w.splits = (int)std::max(1LL, std::min(w.items, (long long)(p.num_sms / w.units)));
+    w.grid = w.units * w.splits;
+    // copies of at least 16 KB: positions per A box, pixels per group (a
+    // window of S pixels spans at most two groups)
+    w.a_pos_bytes = 128u * w.rb;
+    w.Qa = std::max(1, (int)(16384 / w.a_pos_bytes));
+    w.a_slot_bytes = (uint32_t)w.KT * w.Qa * w.a_pos_bytes;
+    w.pix_bytes = (uint32_t)w.cb * w.rb;
+    w.G = std::max({p.S - 1, 1, (int)((16384 + w.pix_bytes - 1) / w.pix_bytes)});
+    if (w.G > 256) return w;
+    w.grp_bytes = (uint32_t)w.G * w.pix_bytes;
+    const size_t budget = 220 * 1024;
+    const int mirror = p.S > 1 ? 1 : 0;
+    int na = kWnMaxNA, ng = kWnMaxNG;
+    auto bytes = [&](int a_, int g_) {
+        return (size_t)a_ * w.a_slot_bytes + (size_t)(g_ + mirror) * w.grp_bytes;
+    };
+    while (bytes(na, ng) > budget && (na > 2 || ng > 2)) {
+        if (na > 2 && (ng <= 2 || (size_t)na * w.a_slot_bytes >= (size_t)ng * w.grp_bytes)) --na;
+        else --ng;
+    }
+    if (bytes(na, ng) > budget) return w;
+    w.NA = na;
+    w.NG = ng;
+    w.b_off = (uint32_t)((size_t)na * w.a_slot_bytes);
+    const size_t stage = (size_t)w.cols * 128 * sizeof(float);
+    w.smem = std::max(bytes(na, ng), stage) + 1024;
+    if (w.smem > 227 * 1024) return w;
+    w.acc_bytes = (size_t)w.units * w.KT * w.cols * 128 * sizeof(float);
+    w.xn_bytes = sizeof(float) * (size_t)w.nc * w.nb * p.H * p.W * p.C;
+    w.dzn_bytes = sizeof(float) * (size_t)w.nc * w.nb * p.P * p.Q * p.K;
+    w.ok = true;
+    return w;
+}
+
+template <int NB>
+cudaError_t launch_batch_inner_x(const Plan &p, const float *x, float *xn, cudaStream_t st) {
+    const int cchunks = (p.C + 7) / 8;
+    const int nc = (p.N + NB - 1) / NB;
+    dim3 grid((unsigned)((p.HW + 31) / 32), (unsigned)(nc * cchunks));
+    return launch_pdl(batch_inner_kernel<NB, XSrc>, grid, dim3(256), 0, st, XSrc{x}, p.N, p.C,
+                      p.HW, cchunks, xn);
+}
+
+template <int NB, int ACT, bool BN>
+cudaError_t launch_batch_inner_dz(const Plan &p, const float *delta, const float *output,
+                                  const float *z, const Coef *coef, float *dzn, cudaStream_t st) {
+    const int cchunks = (p.K + 7) / 8;
+    const int nc = (p.N + NB - 1) / NB;
+    dim3 grid((unsigned)((p.PQ + 31) / 32), (unsigned)(nc * cchunks));
+    return launch_pdl(batch_inner_kernel<NB, DzSrc<ACT, BN>>, grid, dim3(256), 0, st,
+                      DzSrc<ACT, BN>{delta, output, z, coef}, p.N, p.K, p.PQ, cchunks, dzn);
+}
+
+template <int NB>
+cudaError_t launch_dzn_nb(const Plan &p, const float *delta, const float *output, const float *z,
+                          const Coef *coef, float *dzn, cudaStream_t st) {
+    const bool leaky = p.act == CBA_ACT_LEAKY;
+    if (p.bn)
+        return leaky ? launch_batch_inner_dz<NB, CBA_ACT_LEAKY, true>(p, delta, output, z, coef,
+                                                                       dzn, st)
+                     : launch_batch_inner_dz<NB, CBA_ACT_LINEAR, true>(p, delta, output, z, coef,
+                                                                        dzn, st);
+    return leaky ? launch_batch_inner_dz<NB, CBA_ACT_LEAKY, false>(p, delta, output, z, coef, dzn,
+                                                                    st)
+                 : launch_batch_inner_dz<NB, CBA_ACT_LINEAR, false>(p, delta, output, z, coef,
+                                                                     dzn, st);
+}
+
+}  // namespace
+
+bool wgrad_nb_supported(const Plan &p) {
+    const WnGeom w = wn_geom(p);
+    if (!w.ok) return false;
+    // int32 grid dimensions and indices of the layout passes
+    if ((long long)w.nc * ((p.C + 7) / 8) > 65535 || (long long)w.nc * ((p.K + 7) / 8) > 65535)
+        return false;
+    return true;
+}
+
+size_t wgrad_nb_acc_bytes(const Plan &p) {
+    const WnGeom w = wn_geom(p);
+    return w.ok ? w.acc_bytes : 0;
+}
+
+size_t wgrad_nb_xn_bytes(const Plan &p) {
+    const WnGeom w = wn_geom(p);
+    return w.ok ? w.xn_bytes : 0;
+}
+
+size_t wgrad_nb_dzn_bytes(const Plan &p) {
+    const WnGeom w = wn_geom(p);
+    return w.ok ? w.dzn_bytes : 0;
+}
+
+cudaError_t launch_xn(const Plan &p, const float *x, float *xn, cudaStream_t st, int *launches) {
+    const WnGeom w = wn_geom(p);
+    if (!w.ok) return cudaErrorNotSupported;
+    cudaError_t e = w.nb == 16 ? launch_batch_inner_x<16>(p, x, xn, st)
+                               : launch_batch_inner_x<32>(p, x, xn, st);
+    if (e == cudaSuccess) ++*launches;
+    return e;
+}
+
+cudaError_t launch_dzn(const Plan &p, const float *delta, const float *output, const float *z,
+                       const void *ws, float *dzn, cudaStream_t st, int *launches) {
+    const WnGeom w = wn_geom(p);
+    if (!w.ok) return cudaErrorNotSupported;
+    const Coef *coef = ws_at<Coef>(ws, p.off_coef);
+    cudaError_t e = w.nb == 16 ? launch_dzn_nb<16>(p, delta, output, z, coef, dzn, st)
+                               : launch_dzn_nb<32>(p, delta, output, z, coef, dzn, st);
+    if (e == cudaSuccess) ++*launches;
+    return e;
+}
+
+cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, float *dW, void *ws,
+                            float *acc, cudaStream_t st, int *launches) {
+    const WnGeom w = wn_geom(p);
+    if (!w.ok) return cudaErrorNotSupported;
+    WnArgs a;
+    a.acc = acc;
+    a.status = ws_at<unsigned>(ws, p.off_status);
+    a.P = p.P; a.Q = p.Q; a.R = p.R; a.S = p.S; a.stride = p.stride; a.pad = p.pad;
+    a.ctiles = w.ctiles; a.KT = w.KT; a.cb = w.cb; a.cols = w.cols; a.splits = w.splits;
+    a.items = w.items; a.Qa = w.Qa; a.NA = w.NA; a.G = w.G; a.NG = w.NG;
+    a.mirror = p.S > 1 ? 1 : 0;
+    a.rb = w.rb;
+    a.swz = w.nb == 16 ? 4u : 2u;  // 64-byte or 128-byte swizzle
+    a.a_pos_bytes = w.a_pos_bytes; a.a_slot_bytes = w.a_slot_bytes;
+    a.pix_bytes = w.pix_bytes; a.grp_bytes = w.grp_bytes; a.b_off = w.b_off;
+
+    alignas(64) CUtensorMap tma, tmb;
+    const int swz_bytes = (int)w.rb;  // the row is exactly one swizzle span
+    {
+        const uint64_t d[4] = {(uint64_t)w.nb, (uint64_t)p.K, (uint64_t)p.Q,
+                               (uint64_t)w.nc * p.P};
+        const uint32_t b[4] = {(uint32_t)w.nb, 128, (uint32_t)w.Qa, 1};
+        if (!tma_encode_f32_swz(&tma, dzn, 4, d, b, swz_bytes)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t d[5] = {(uint64_t)w.nb, (uint64_t)p.C, (uint64_t)p.W, (uint64_t)p.H,
+                               (uint64_t)w.nc};
+        const uint32_t b[5] = {(uint32_t)w.nb, (uint32_t)w.cb, (uint32_t)w.G, 1, 1};
+        if (!tma_encode_f32_swz(&tmb, xn, 5, d, b, swz_bytes)) return cudaErrorInvalidValue;
+    }
+    auto kern = w.nb == 16 ? wgrad_nb_kernel<16> : wgrad_nb_kernel<32>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)w.smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(kern, dim3(w.grid), dim3(kWnThreads), w.smem, st, tma, tmb, a);
+    if (e != cudaSuccess) return e;
+    const long long total = (long long)p.K * p.C * p.R * p.S;
+    const unsigned ablocks = (unsigned)std::min<long long>((total + 255) / 256, p.num_sms * 8LL);
+    e = launch_pdl(wgrad_nb_apply_kernel, dim3(ablocks), dim3(256), 0, st, (const float *)acc,
+                   w.KT, w.cols, w.cb, p.S, p.R, w.ctiles, p.C, total, dW);
+    if (e != cudaSuccess) return e;
+    *launches += 2;
+    return cudaGetLastError();
+}
+
+}  // namespace cba
