@@ -82,7 +82,10 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->wg_splits = (int)ceil_div(p->m, chunk);
 
     p->use_tc2 = (p->math == CBA_MATH_TF32) && tc2_supported(*p);
-    p->use_wnb = p->use_tc2 && wgrad_nb_supported(*p);
+    // the batch-innermost weight gradient where the TMEM-operand one does not
+    // apply (strides, kernel sizes, rows not 16-byte strided): where both do,
+    // the latter needs no re-laid-out x and measured faster
+    p->use_wnb = p->use_tc2 && wgrad_tc4_ws_bytes(*p) == 0 && wgrad_nb_supported(*p);
     p->use_tc = !p->use_tc2 && (p->math == CBA_MATH_TF32) && tc_supported(*p);
     if (p->use_tc) tc_plan(*p);
 
@@ -272,13 +275,14 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
         // dz channels-last for the input gradient; x and dz batch-innermost for
         // the weight gradient (its layout passes count in its phase)
         float *dzt = ws_at<float>(workspace, p.off_dzt);
-        if (e == cudaSuccess && prev_delta)
-            e = launch_dz_materialize(p, delta, output, z, workspace, dzt, true, st, &n_launch,
-                                      false);
-        if (e == cudaSuccess) e = tr.mark(1);
+        float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) +
+                                               dzc_geom(p).dzt_bytes);
         float *xn = ws_at<float>(workspace, p.off_xn), *dzn = ws_at<float>(workspace, p.off_dzn);
+        if (e == cudaSuccess)
+            e = launch_dz_layouts(p, delta, output, z, workspace, dzn,
+                                  prev_delta ? dzc : nullptr, st, &n_launch);
+        if (e == cudaSuccess) e = tr.mark(1);
         if (e == cudaSuccess) e = launch_xn(p, x, xn, st, &n_launch);
-        if (e == cudaSuccess) e = launch_dzn(p, delta, output, z, workspace, dzn, st, &n_launch);
         if (e == cudaSuccess)
             e = launch_wgrad_nb(p, xn, dzn, dW, workspace, ws_at<float>(workspace, p.off_wgacc), st,
                                 &n_launch);

@@ -152,17 +152,21 @@ bool tma_encode_f32_swz(void *tmap, const void *base, int rank, const uint64_t *
                         const uint32_t *box, int swizzle_bytes);
 // Weight gradient on batch-innermost layouts (cba_wgrad_nb.cu): xn
 // [nc][H][W][C][nb] and dzn [nc][P][Q][K][nb] (nb = 16 or 32 images, zeros past
-// N), written by launch_xn and launch_dzn; tile accumulators of
+// N), written by launch_xn and launch_dz_layouts; tile accumulators of
 // wgrad_nb_acc_bytes, zeroed before the call.
 bool wgrad_nb_supported(const Plan &p);
 size_t wgrad_nb_acc_bytes(const Plan &p);
 size_t wgrad_nb_xn_bytes(const Plan &p);
 size_t wgrad_nb_dzn_bytes(const Plan &p);
 cudaError_t launch_xn(const Plan &p, const float *x, float *xn, cudaStream_t st, int *launches);
-cudaError_t launch_dzn(const Plan &p, const float *delta, const float *output, const float *z,
-                       const void *ws, float *dzn, cudaStream_t st, int *launches);
 cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, float *dW, void *ws,
                             float *acc, cudaStream_t st, int *launches);
+// One pass over delta / output / z writing dz batch-innermost (dzn) and, when
+// dzc is not NULL, channels-last with its zero border (the layout of
+// dzc_geom, read by the input gradient).
+cudaError_t launch_dz_layouts(const Plan &p, const float *delta, const float *output,
+                              const float *z, const void *ws, float *dzn, float *dzc,
+                              cudaStream_t st, int *launches);
 // Weight gradient with TMA-fed input rows (cba_wgrad4.cu).
 bool wgrad_tc4_supported(const Plan &p, const float *x);
 size_t wgrad_tc4_ws_bytes(const Plan &p);  // tile accumulators (0 if the shape is not covered)

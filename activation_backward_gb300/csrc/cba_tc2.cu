@@ -1245,6 +1245,10 @@ __global__ void __launch_bounds__(kD4Threads, 1)
 #pragma unroll
         for (int si = 0; si < kD2MaxTaps; ++si) dqr[si] = a.dq[si] - a.min_dq;
         const int bch = ns > 0 ? max(1, kD4Slots / ns) : 1;  // chunks per batch
+        // the plane-per-image form of 1x1 stride-1 layers: a tile's positions are
+        // consecutive in memory within each image, in aligned groups of 4
+        const bool flat4 = ns == 1 && span == 0 && a.He == 1 && a.stride == 1 && a.Hc == 1 &&
+                           a.bq_lo == 0 && a.Qpp == a.We && HW % 4 == 0 && tstride % 4 == 0;
         int par = 0;
         bool ok = true;
         for (int i = 0; ok && i < nunits; ++i) {
@@ -1288,28 +1292,27 @@ __global__ void __launch_bounds__(kD4Threads, 1)
             E.c_tile = a.c_tile; E.eg = eg; E.wq = wq; E.lane = lane; E.span = span;
             E.dqr = dqr; E.pix = pix; E.HW = HW; E.c0 = c0; E.cl_all = cl_all; E.out = out;
             E.residual = a.residual; E.prev = a.prev; E.accumulate = a.accumulate;
-            if (ns == 1 && span == 0) {
-                // no column shift (one kernel column, e.g. 1x1 layers): each of
-                // the group's 16-channel chunks goes straight from TMEM to prev,
-                // one channel plane (HW apart) after the other (the values it
-                // adds were prefetched into L2 above)
-                const long long cstep = 32 * HW;  // this group's next chunk
+            if (flat4) {
+                // one plane of positions per image (1x1, stride 1; HW a multiple
+                // of 4, at least 32): the warp's 32 positions x 16 channels of a
+                // chunk go from TMEM through its staging rows [16][32] in shared
+                // memory, then out as float4 along the positions (the residual /
+                // old prev read the same way): each memory instruction of the
+                // warp moves four whole 128-byte rows instead of 32 scalars
+                // spread over a channel plane each.
+                float *stg = halo + (warp - 2) * 512;
+                const long long mw = (long long)tile * tstride + wq * 32;  // lane 0's position
                 const bool with_res = a.residual != nullptr, with_acc = a.accumulate != 0;
-                const long long off0 = pix + (long long)(c0 + eg * 16) * HW;
-                float *dst = a.prev + off0;
-                const float *res = with_res ? a.residual + off0 : a.prev;  // read only if with_res
-                for (int t = 0; t < gch; ++t, dst += cstep, res += cstep) {
+                // lane -> (channel row e = k * 4 + lane / 8, positions p4 .. p4 + 3),
+                // k = 0 .. 3; the global offset of each, without the channel
+                const int p4 = (lane & 7) * 4;
+                const long long m = mw + p4;
+                const bool mv = m < a.total_pos;
+                const long long nimg = m / HW;
+                const long long pbase = nimg * a.C * HW + (m - nimg * HW);
+                for (int t = 0; t < gch; ++t) {
                     const int cc = eg + 2 * t;
                     const int nvalid = min(16, cl_all - cc * 16);
-                    float add[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        add[e] = 0.f;
-                        if (out && e < nvalid) {
-                            if (with_res) add[e] += __ldg(res + e * HW);
-                            if (with_acc) add[e] += dst[e * HW];
-                        }
-                    }
                     float v[16];
                     ptx::tmem_ld16(E.tbase + (uint32_t)(cc * 16), v);
                     ptx::tmem_ld_wait();
@@ -1318,11 +1321,82 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                         __syncwarp();
                         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.acc_empty[b]));
                     }
-                    if (out) {
+                    __syncwarp();  // the previous chunk's rows have been read
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            if (e < nvalid) dst[e * HW] = v[e] + add[e];
+                    for (int e = 0; e < 16; ++e) stg[e * 32 + lane] = v[e];
+                    __syncwarp();
+                    float4 val[4], add[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = k * 4 + (lane >> 3);
+                        val[k] = *reinterpret_cast<const float4 *>(stg + e * 32 + p4);
+                        add[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (mv && e < nvalid) {
+                            const long long o = pbase + (long long)(c0 + cc * 16 + e) * HW;
+                            if (with_res) {
+                                const float4 r = __ldg(reinterpret_cast<const float4 *>(a.residual + o));
+                                add[k].x += r.x; add[k].y += r.y; add[k].z += r.z; add[k].w += r.w;
+                            }
+                            if (with_acc) {
+                                const float4 r = *reinterpret_cast<const float4 *>(a.prev + o);
+                                add[k].x += r.x; add[k].y += r.y; add[k].z += r.z; add[k].w += r.w;
+                            }
+                        }
                     }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int e = k * 4 + (lane >> 3);
+                        if (mv && e < nvalid)
+                            *reinterpret_cast<float4 *>(a.prev + pbase +
+                                                        (long long)(c0 + cc * 16 + e) * HW) =
+                                make_float4(val[k].x + add[k].x, val[k].y + add[k].y,
+                                            val[k].z + add[k].z, val[k].w + add[k].w);
+                    }
+                }
+                if (gch <= 0) {  // no chunk for this group: release at once
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.acc_empty[b]));
+                }
+                continue;
+            }
+            if (ns == 1 && span == 0) {
+                // no column shift (one kernel column, e.g. 1x1 layers): each of
+                // the group's 16-channel chunks goes straight from TMEM to prev,
+                // one channel plane (HW apart) after the other.  Per chunk the
+                // TMEM load comes first, then the loads of the values it adds
+                // (residual, old prev; prefetched into L2 above), then the
+                // stores: measured several times faster than loading the added
+                // values ahead of the TMEM load.
+                const long long cstep = 32 * HW;  // this group's next chunk
+                const bool with_res = a.residual != nullptr, with_acc = a.accumulate != 0;
+                const long long off0 = pix + (long long)(c0 + eg * 16) * HW;
+                float *dst = a.prev + off0;
+                const float *res = with_res ? a.residual + off0 : a.prev;  // read only if with_res
+                for (int t = 0; t < gch; ++t, dst += cstep, res += cstep) {
+                    const int cc = eg + 2 * t;
+                    float v[16];
+                    ptx::tmem_ld16(E.tbase + (uint32_t)(cc * 16), v);
+                    ptx::tmem_ld_wait();
+                    if (t == gch - 1) {  // the unit's last loads: the MMAs may reuse it
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.acc_empty[b]));
+                    }
+                    if (!out) continue;
+                    const int nvalid = min(16, cl_all - cc * 16);
+                    float add[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        add[e] = 0.f;
+                        if (e < nvalid) {
+                            if (with_res) add[e] += __ldg(res + e * HW);
+                            if (with_acc) add[e] += dst[e * HW];
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        if (e < nvalid) dst[e * HW] = v[e] + add[e];
                 }
                 if (gch <= 0) {  // no chunk for this group: release at once
                     ptx::tc_fence_before();

@@ -117,6 +117,91 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// dz in both layouts the GEMMs read, from one pass over delta / output / z:
+//   dzn [nc][PQ][K][NB]            batch-innermost (weight gradient)
+//   dzc [N][Pp][Qpp][Kp]           channels-last with a zero border of bd_lo /
+//                                  bq_lo rows / columns (input gradient); the
+//                                  data at (bd_lo + pp / Qe, bq_lo + pp % Qe)
+// grid: x = position chunks of 32, y = nc * chunks of 8 channels over Kp.
+// Channels K .. Kp - 1 of dzc are written as zeros; the border by
+// dzc_border_kernel.
+template <int NB, int ACT, bool BN, bool DZC>
+__global__ void __launch_bounds__(256)
+    dz_layouts_kernel(DzSrc<ACT, BN> src, int N, int K, int Kp, int PQ, int Qe, int Pp, int Qpp,
+                      int bd_lo, int bq_lo, int cchunks, float *__restrict__ dzn,
+                      float *__restrict__ dzc) {
+    ptx::griddep_wait();  // the coefficients come from the reduction pass
+    __shared__ float tile[32][8 * NB + 1];
+    const int t = threadIdx.x;
+    const int pos0 = blockIdx.x * 32;
+    const int j = blockIdx.y / cchunks, k0 = (blockIdx.y % cchunks) * 8;
+    constexpr int PER = NB * 8 * 32 / 256;
+    float v[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int e = t + u * 256;
+        const int pos = e & 31, rc = e >> 5;
+        const int n = j * NB + (rc >> 3), k = k0 + (rc & 7), pp = pos0 + pos;
+        v[u] = (n < N && k < K && pp < PQ) ? rna_tf32(src(((long long)n * K + k) * PQ + pp, k))
+                                           : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const int e = t + u * 256;
+        const int rc = e >> 5;
+        tile[e & 31][(rc & 7) * NB + (rc >> 3)] = v[u];
+    }
+    __syncthreads();
+    ptx::griddep_launch_dependents();
+    // dzn: for each position, channels k0 .. k0 + 7 x NB images are contiguous
+    const int nkl = min(8, K - k0);
+    for (int e = t; e < 32 * 8 * NB; e += 256) {
+        const int pos = e / (8 * NB), vv = e % (8 * NB);
+        const int pp = pos0 + pos;
+        if (pp < PQ && vv < nkl * NB)
+            dzn[(((long long)j * PQ + pp) * K + k0) * NB + vv] = tile[pos][vv];
+    }
+    if constexpr (DZC) {
+        // dzc: for each (image, position), the 8 channels as two float4 (Kp and
+        // k0 are multiples of 4)
+        const int nk4 = min(2, (Kp - k0) / 4);
+        for (int e = t; e < 32 * NB; e += 256) {
+            const int pos = e & 31, nl = e >> 5;
+            const int n = j * NB + nl, pp = pos0 + pos;
+            if (n >= N || pp >= PQ) continue;
+            const int pr = pp / Qe, qc = pp - pr * Qe;
+            float4 *out = reinterpret_cast<float4 *>(
+                dzc + (((long long)n * Pp + bd_lo + pr) * Qpp + bq_lo + qc) * Kp + k0);
+            for (int h = 0; h < nk4; ++h)
+                out[h] = make_float4(tile[pos][(4 * h + 0) * NB + nl], tile[pos][(4 * h + 1) * NB + nl],
+                                     tile[pos][(4 * h + 2) * NB + nl], tile[pos][(4 * h + 3) * NB + nl]);
+        }
+    }
+}
+
+// Zeros of the channels-last dz copy's border: block = one (image, row) of
+// [N][Pp][Qpp][Kp]; a border row is zeroed whole, an inner row at its bq_lo
+// left and Qpp - bq_lo - Qe right columns.
+__global__ void __launch_bounds__(256)
+    dzc_border_kernel(float *__restrict__ dzc, int Pp, int Qpp, int Kp, int Pe, int Qe,
+                      int bd_lo, int bq_lo) {
+    ptx::griddep_wait();
+    const int row = blockIdx.x % Pp;
+    float4 *base = reinterpret_cast<float4 *>(dzc + (long long)blockIdx.x * Qpp * Kp);
+    const int k4 = Kp / 4;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < bd_lo || row >= bd_lo + Pe) {
+        for (int i = threadIdx.x; i < Qpp * k4; i += 256) base[i] = z;
+        return;
+    }
+    const int nl = bq_lo, nr = Qpp - bq_lo - Qe;
+    for (int i = threadIdx.x; i < (nl + nr) * k4; i += 256) {
+        const int c = i / k4, kk = i - c * k4;
+        const int col = c < nl ? c : bq_lo + Qe + (c - nl);
+        base[col * k4 + kk] = z;
+    }
+}
+
 }  // namespace
 
 namespace {
@@ -533,38 +618,67 @@ cudaError_t launch_batch_inner_x(const Plan &p, const float *x, float *xn, cudaS
 }
 
 template <int NB, int ACT, bool BN>
-cudaError_t launch_batch_inner_dz(const Plan &p, const float *delta, const float *output,
-                                  const float *z, const Coef *coef, float *dzn, cudaStream_t st) {
-    const int cchunks = (p.K + 7) / 8;
+cudaError_t launch_dz_layouts_t(const Plan &p, const DzcGeom &g, const float *delta,
+                                const float *output, const float *z, const Coef *coef,
+                                float *dzn, float *dzc, cudaStream_t st) {
+    const int cchunks = (g.Kp + 7) / 8;
     const int nc = (p.N + NB - 1) / NB;
     dim3 grid((unsigned)((p.PQ + 31) / 32), (unsigned)(nc * cchunks));
-    return launch_pdl(batch_inner_kernel<NB, DzSrc<ACT, BN>>, grid, dim3(256), 0, st,
-                      DzSrc<ACT, BN>{delta, output, z, coef}, p.N, p.K, p.PQ, cchunks, dzn);
+    const DzSrc<ACT, BN> src{delta, output, z, coef};
+    if (dzc)
+        return launch_pdl(dz_layouts_kernel<NB, ACT, BN, true>, grid, dim3(256), 0, st, src, p.N,
+                          p.K, g.Kp, p.PQ, g.Qe, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, cchunks, dzn, dzc);
+    return launch_pdl(dz_layouts_kernel<NB, ACT, BN, false>, grid, dim3(256), 0, st, src, p.N, p.K,
+                      g.Kp, p.PQ, g.Qe, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, cchunks, dzn, dzc);
 }
 
 template <int NB>
-cudaError_t launch_dzn_nb(const Plan &p, const float *delta, const float *output, const float *z,
-                          const Coef *coef, float *dzn, cudaStream_t st) {
+cudaError_t launch_dz_layouts_nb(const Plan &p, const DzcGeom &g, const float *delta,
+                                 const float *output, const float *z, const Coef *coef,
+                                 float *dzn, float *dzc, cudaStream_t st) {
     const bool leaky = p.act == CBA_ACT_LEAKY;
     if (p.bn)
-        return leaky ? launch_batch_inner_dz<NB, CBA_ACT_LEAKY, true>(p, delta, output, z, coef,
-                                                                       dzn, st)
-                     : launch_batch_inner_dz<NB, CBA_ACT_LINEAR, true>(p, delta, output, z, coef,
-                                                                        dzn, st);
-    return leaky ? launch_batch_inner_dz<NB, CBA_ACT_LEAKY, false>(p, delta, output, z, coef, dzn,
-                                                                    st)
-                 : launch_batch_inner_dz<NB, CBA_ACT_LINEAR, false>(p, delta, output, z, coef,
-                                                                     dzn, st);
+        return leaky ? launch_dz_layouts_t<NB, CBA_ACT_LEAKY, true>(p, g, delta, output, z, coef,
+                                                                     dzn, dzc, st)
+                     : launch_dz_layouts_t<NB, CBA_ACT_LINEAR, true>(p, g, delta, output, z, coef,
+                                                                      dzn, dzc, st);
+    return leaky ? launch_dz_layouts_t<NB, CBA_ACT_LEAKY, false>(p, g, delta, output, z, coef,
+                                                                  dzn, dzc, st)
+                 : launch_dz_layouts_t<NB, CBA_ACT_LINEAR, false>(p, g, delta, output, z, coef,
+                                                                   dzn, dzc, st);
 }
 
 }  // namespace
+
+cudaError_t launch_dz_layouts(const Plan &p, const float *delta, const float *output,
+                              const float *z, const void *ws, float *dzn, float *dzc,
+                              cudaStream_t st, int *launches) {
+    const WnGeom w = wn_geom(p);
+    if (!w.ok) return cudaErrorNotSupported;
+    const DzcGeom g = dzc_geom(p);
+    const Coef *coef = ws_at<Coef>(ws, p.off_coef);
+    cudaError_t e = w.nb == 16
+                        ? launch_dz_layouts_nb<16>(p, g, delta, output, z, coef, dzn, dzc, st)
+                        : launch_dz_layouts_nb<32>(p, g, delta, output, z, coef, dzn, dzc, st);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    if (dzc && (g.Pp != g.Pe || g.Qpp != g.Qe)) {
+        e = launch_pdl(dzc_border_kernel, dim3((unsigned)(p.N * g.Pp)), dim3(256), 0, st, dzc,
+                       g.Pp, g.Qpp, g.Kp, g.Pe, g.Qe, g.bd_lo, g.bq_lo);
+        if (e != cudaSuccess) return e;
+        ++*launches;
+    }
+    return cudaSuccess;
+}
 
 bool wgrad_nb_supported(const Plan &p) {
     const WnGeom w = wn_geom(p);
     if (!w.ok) return false;
     // int32 grid dimensions and indices of the layout passes
-    if ((long long)w.nc * ((p.C + 7) / 8) > 65535 || (long long)w.nc * ((p.K + 7) / 8) > 65535)
+    const DzcGeom g = dzc_geom(p);
+    if ((long long)w.nc * ((p.C + 7) / 8) > 65535 || (long long)w.nc * ((g.Kp + 7) / 8) > 65535)
         return false;
+    if ((long long)p.N * g.Pp >= (1LL << 31)) return false;
     return true;
 }
 
@@ -588,17 +702,6 @@ cudaError_t launch_xn(const Plan &p, const float *x, float *xn, cudaStream_t st,
     if (!w.ok) return cudaErrorNotSupported;
     cudaError_t e = w.nb == 16 ? launch_batch_inner_x<16>(p, x, xn, st)
                                : launch_batch_inner_x<32>(p, x, xn, st);
-    if (e == cudaSuccess) ++*launches;
-    return e;
-}
-
-cudaError_t launch_dzn(const Plan &p, const float *delta, const float *output, const float *z,
-                       const void *ws, float *dzn, cudaStream_t st, int *launches) {
-    const WnGeom w = wn_geom(p);
-    if (!w.ok) return cudaErrorNotSupported;
-    const Coef *coef = ws_at<Coef>(ws, p.off_coef);
-    cudaError_t e = w.nb == 16 ? launch_dzn_nb<16>(p, delta, output, z, coef, dzn, st)
-                               : launch_dzn_nb<32>(p, delta, output, z, coef, dzn, st);
     if (e == cudaSuccess) ++*launches;
     return e;
 }
