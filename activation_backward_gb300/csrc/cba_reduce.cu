@@ -21,7 +21,7 @@ namespace cba {
 namespace {
 
 constexpr int kRedThreads = 256;
-constexpr int kRedU = 3;  // vector loads per tensor per thread in flight
+constexpr int kRedU = 4;  // vector loads per tensor per thread in flight
 
 template <int ACT, bool BN>
 __device__ __forceinline__ void acc1(float d, float y, float zv, float mu, float rs, float &s1,
@@ -84,16 +84,29 @@ __device__ __forceinline__ float round_tf32(float v) {
     return __uint_as_float(r);
 }
 
-__device__ void repack_part(const RepackJob &j, long long first, long long stride) {
-    const long long total = (long long)j.R * j.S * j.C * j.Kw;
-    for (long long i = first; i < total; i += stride) {
-        const int kk = (int)(i % j.Kw);
-        long long t = i / j.Kw;
-        const int c = (int)(t % j.C);
-        t /= j.C;
-        const int s = (int)(t % j.S);
-        const int r = (int)(t / j.S);
-        j.wr[i] = kk < j.K ? round_tf32(j.W[(((long long)kk * j.C + c) * j.R + r) * j.S + s]) : 0.f;
+// W [K][C*R*S] -> wr [R][S][C][Kw] in 32 x 32 tiles (output channels k x
+// flattened (c, r, s)) through shared memory: reads coalesced along (c, r, s),
+// writes along k.  Repack block `rb` of `nrep` takes tiles rb, rb + nrep, ...
+__device__ void repack_part(const RepackJob &j, int rb, int nrep) {
+    __shared__ float tile[32][33];
+    const int CRS = j.C * j.R * j.S, RS = j.R * j.S;
+    const int tk = (j.Kw + 31) / 32, tc = (CRS + 31) / 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows of 32
+    for (int t = rb; t < tk * tc; t += nrep) {
+        const int k0 = (t / tc) * 32, q0 = (t % tc) * 32;
+        for (int r = ty; r < 32; r += kRedThreads / 32) {
+            const int k = k0 + r, q = q0 + tx;
+            tile[r][tx] = (k < j.K && q < CRS) ? round_tf32(j.W[(long long)k * CRS + q]) : 0.f;
+        }
+        __syncthreads();
+        for (int r = ty; r < 32; r += kRedThreads / 32) {
+            const int q = q0 + r, k = k0 + tx;
+            if (q < CRS && k < j.Kw) {
+                const int c = q / RS, rs = q - c * RS;  // rs = r * S + s
+                j.wr[((long long)rs * j.C + c) * j.Kw + k] = tile[tx][r];
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -113,8 +126,7 @@ __global__ void __launch_bounds__(kRedThreads)
     ptx::griddep_wait();
     const int nred = K * groups * pieces;
     if ((int)blockIdx.x >= nred) {
-        repack_part(job, (long long)(blockIdx.x - nred) * kRedThreads + threadIdx.x,
-                    (long long)nrep * kRedThreads);
+        repack_part(job, (int)blockIdx.x - nred, nrep);
         return;
     }
     const int k = (int)(blockIdx.x % K);
@@ -129,47 +141,55 @@ __global__ void __launch_bounds__(kRedThreads)
     const int a0 = q * L, a1 = min(pa, a0 + L);
     const int n0 = grp * pln, n1 = min(N, n0 + pln);
     float s1 = 0.f, s2 = 0.f;
-    for (int n = n0; n < n1; ++n) {
-        const size_t pbase = ((size_t)n * K + k) * pa;
-        for (int base = a0 + tid; base < a1; base += kRedThreads * kRedU) {
-            if constexpr (VEC) {
-                const float4 *D = reinterpret_cast<const float4 *>(delta) + pbase;
-                const float4 *Y = reinterpret_cast<const float4 *>(output) + pbase;
-                const float4 *Z = reinterpret_cast<const float4 *>(z) + pbase;
-                float4 dd[kRedU], yy[kRedU], zz[kRedU];
+    // the block's accesses (planes n0 .. n1 - 1, accesses a0 .. a1 - 1 of each)
+    // as one flat sequence, so that every round keeps kRedU loads per tensor in
+    // flight in every thread even when a plane is shorter than the block
+    const int La = a1 - a0;
+    const int total = La > 0 ? (n1 - n0) * La : 0;
+    for (int base = tid; base < total; base += kRedThreads * kRedU) {
+        size_t off[kRedU];
+        bool in[kRedU];
 #pragma unroll
-                for (int u = 0; u < kRedU; ++u) {
-                    const int i = base + u * kRedThreads;
-                    const bool in = i < a1;
-                    const int ii = in ? i : a0;
-                    dd[u] = __ldg(D + ii);
-                    if constexpr (ACT == CBA_ACT_LEAKY) yy[u] = __ldg(Y + ii);
-                    if constexpr (BN) zz[u] = __ldg(Z + ii);
-                    if (!in) dd[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
+        for (int u = 0; u < kRedU; ++u) {
+            const int f = base + u * kRedThreads;
+            in[u] = f < total;
+            const int ff = in[u] ? f : 0;
+            const int pl = ff / La;
+            off[u] = ((size_t)(n0 + pl) * K + k) * pa + (a0 + ff - pl * La);
+        }
+        if constexpr (VEC) {
+            const float4 *D = reinterpret_cast<const float4 *>(delta);
+            const float4 *Y = reinterpret_cast<const float4 *>(output);
+            const float4 *Z = reinterpret_cast<const float4 *>(z);
+            float4 dd[kRedU], yy[kRedU], zz[kRedU];
 #pragma unroll
-                for (int u = 0; u < kRedU; ++u) {
-                    if constexpr (ACT != CBA_ACT_LEAKY) yy[u] = dd[u];
-                    if constexpr (!BN) zz[u] = dd[u];
-                    acc1<ACT, BN>(dd[u].x, yy[u].x, zz[u].x, mu, rs, s1, s2);
-                    acc1<ACT, BN>(dd[u].y, yy[u].y, zz[u].y, mu, rs, s1, s2);
-                    acc1<ACT, BN>(dd[u].z, yy[u].z, zz[u].z, mu, rs, s1, s2);
-                    acc1<ACT, BN>(dd[u].w, yy[u].w, zz[u].w, mu, rs, s1, s2);
-                }
-            } else {
-                float dd[kRedU], yy[kRedU], zz[kRedU];
-#pragma unroll
-                for (int u = 0; u < kRedU; ++u) {
-                    const int i = base + u * kRedThreads;
-                    const bool in = i < a1;
-                    const int ii = in ? i : a0;
-                    dd[u] = in ? __ldg(delta + pbase + ii) : 0.f;
-                    yy[u] = ACT == CBA_ACT_LEAKY ? __ldg(output + pbase + ii) : 0.f;
-                    zz[u] = BN ? __ldg(z + pbase + ii) : 0.f;
-                }
-#pragma unroll
-                for (int u = 0; u < kRedU; ++u) acc1<ACT, BN>(dd[u], yy[u], zz[u], mu, rs, s1, s2);
+            for (int u = 0; u < kRedU; ++u) {
+                dd[u] = __ldg(D + off[u]);
+                if constexpr (ACT == CBA_ACT_LEAKY) yy[u] = __ldg(Y + off[u]);
+                if constexpr (BN) zz[u] = __ldg(Z + off[u]);
             }
+            // every load of the round is issued before the first use
+            asm volatile("" ::: "memory");
+#pragma unroll
+            for (int u = 0; u < kRedU; ++u) {
+                if (!in[u]) dd[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if constexpr (ACT != CBA_ACT_LEAKY) yy[u] = dd[u];
+                if constexpr (!BN) zz[u] = dd[u];
+                acc1<ACT, BN>(dd[u].x, yy[u].x, zz[u].x, mu, rs, s1, s2);
+                acc1<ACT, BN>(dd[u].y, yy[u].y, zz[u].y, mu, rs, s1, s2);
+                acc1<ACT, BN>(dd[u].z, yy[u].z, zz[u].z, mu, rs, s1, s2);
+                acc1<ACT, BN>(dd[u].w, yy[u].w, zz[u].w, mu, rs, s1, s2);
+            }
+        } else {
+            float dd[kRedU], yy[kRedU], zz[kRedU];
+#pragma unroll
+            for (int u = 0; u < kRedU; ++u) {
+                dd[u] = in[u] ? __ldg(delta + off[u]) : 0.f;
+                yy[u] = ACT == CBA_ACT_LEAKY ? __ldg(output + off[u]) : 0.f;
+                zz[u] = BN ? __ldg(z + off[u]) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < kRedU; ++u) acc1<ACT, BN>(dd[u], yy[u], zz[u], mu, rs, s1, s2);
         }
     }
 #pragma unroll
@@ -260,8 +280,8 @@ cudaError_t launch_reduce(const Plan &p, const float *delta, const float *output
     RepackJob job{repack_W, repack_wr, p.K, p.C, p.R, p.S, (p.K + 3) / 4 * 4};
     int nrep = 0;
     if (repack_W && repack_wr) {
-        const long long total = (long long)p.R * p.S * p.C * job.Kw;
-        nrep = (int)std::min<long long>((total + kRedThreads - 1) / kRedThreads, 64);
+        const long long tiles = (long long)((job.Kw + 31) / 32) * ((p.C * p.R * p.S + 31) / 32);
+        nrep = (int)std::min<long long>(tiles, 256);
     }
     const bool leaky = p.act == CBA_ACT_LEAKY;
 #define CBA_RED(A, B) \
