@@ -88,6 +88,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// *p += v, performed at the L2 (no value returned, nothing to wait for).  No
+// compiler memory clobber: callers never read the location back.
+__device__ __forceinline__ void red_add_f32(float *p, float v) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v));
+}
+// p[0 .. 3] += v (16-byte aligned p), performed at the L2.
+__device__ __forceinline__ void red_add_v4_f32(float *p, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w));
+}
+
 // Brings the line holding `p` into L2 (no register result, no wait).
 __device__ __forceinline__ void prefetch_l2(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));

@@ -706,6 +706,10 @@ struct Dg3Args {
     float *prev;
     unsigned *status;
     int C, He, We, Pp, Qpp, bd_lo, bq_lo, stride, accumulate;
+    // red_add: prev already holds residual (+ its old value when accumulating),
+    // written by prev_init_kernel; the output is added to it at the L2, and
+    // residual / accumulate are unset
+    int red_add;
     int ph, pw, Hc, Wc, min_dq, span;
     int nr, r_of[kD2MaxTaps], dp[kD2MaxTaps];
     int ns, s_of[kD2MaxTaps], dq[kD2MaxTaps];
@@ -729,7 +733,8 @@ __device__ __forceinline__ void dgrad_out_lane(const float *__restrict__ sl,
                                                float *__restrict__ prev,
                                                const float *__restrict__ residual, long long pix,
                                                long long HW, int c0, int cl_hi, int c_tile, int ns,
-                                               const int (&dq)[kD2MaxTaps], int accumulate) {
+                                               const int (&dq)[kD2MaxTaps], int accumulate,
+                                               int red_add) {
     for (int cl = 0; cl < cl_hi; cl += 8) {
         float v[8];
 #pragma unroll
@@ -752,9 +757,15 @@ __device__ __forceinline__ void dgrad_out_lane(const float *__restrict__ sl,
                 if (accumulate) add[u] += prev[idx];
             }
         }
+        if (red_add) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-            if (cl + u < cl_hi) prev[pix + (long long)(c0 + cl + u) * HW] = v[u] + add[u];
+            for (int u = 0; u < 8; ++u)
+                if (cl + u < cl_hi) ptx::red_add_f32(prev + pix + (long long)(c0 + cl + u) * HW, v[u]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (cl + u < cl_hi) prev[pix + (long long)(c0 + cl + u) * HW] = v[u] + add[u];
+        }
     }
 }
 
@@ -924,7 +935,7 @@ __global__ void __launch_bounds__(kD3Threads, 1)
                     for (int si = 0; si < kD2MaxTaps; ++si) dqr[si] = a.dq[si] - a.min_dq;
                     const int cb = eg == 0 ? 0 : ch_half, ce = eg == 0 ? ch_half : cl_all;
                     dgrad_out_lane(stg + L + cb * 128, a.prev, a.residual, pix, HW, c0 + cb,
-                                   ce - cb, a.c_tile, a.ns, dqr, a.accumulate);
+                                   ce - cb, a.c_tile, a.ns, dqr, a.accumulate, a.red_add);
                 }
                 ptx::named_bar_sync(1, 256);
             }
@@ -992,6 +1003,7 @@ struct D4Epi {
     const float *residual;
     float *prev;
     int accumulate;
+    int red_add;
 };
 
 template <int NS, int NB>
@@ -1058,9 +1070,15 @@ __device__ __forceinline__ void d4_epilogue_batch(const D4Epi &E, int t0, uint64
                     if (E.accumulate) add[e] += E.prev[idx];
                 }
             }
+            if (E.red_add) {
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                if (e < nvalid) E.prev[idx0 + (long long)e * E.HW] = v[t * NS][e] + add[e];
+                for (int e = 0; e < 16; ++e)
+                    if (e < nvalid) ptx::red_add_f32(E.prev + idx0 + (long long)e * E.HW, v[t * NS][e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (e < nvalid) E.prev[idx0 + (long long)e * E.HW] = v[t * NS][e] + add[e];
+            }
         }
     }
 }
@@ -1292,6 +1310,7 @@ __global__ void __launch_bounds__(kD4Threads, 1)
             E.c_tile = a.c_tile; E.eg = eg; E.wq = wq; E.lane = lane; E.span = span;
             E.dqr = dqr; E.pix = pix; E.HW = HW; E.c0 = c0; E.cl_all = cl_all; E.out = out;
             E.residual = a.residual; E.prev = a.prev; E.accumulate = a.accumulate;
+            E.red_add = a.red_add;
             if (flat4) {
                 // one plane of positions per image (1x1, stride 1; HW a multiple
                 // of 4, at least 32): the warp's 32 positions x 16 channels of a
@@ -1346,9 +1365,11 @@ __global__ void __launch_bounds__(kD4Threads, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const int e = k * 4 + (lane >> 3);
-                        if (mv && e < nvalid)
-                            *reinterpret_cast<float4 *>(a.prev + pbase +
-                                                        (long long)(c0 + cc * 16 + e) * HW) =
+                        if (!mv || e >= nvalid) continue;
+                        float *o = a.prev + pbase + (long long)(c0 + cc * 16 + e) * HW;
+                        if (a.red_add) ptx::red_add_v4_f32(o, val[k]);
+                        else
+                            *reinterpret_cast<float4 *>(o) =
                                 make_float4(val[k].x + add[k].x, val[k].y + add[k].y,
                                             val[k].z + add[k].z, val[k].w + add[k].w);
                     }
@@ -1394,9 +1415,15 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                             if (with_acc) add[e] += dst[e * HW];
                         }
                     }
+                    if (a.red_add) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        if (e < nvalid) dst[e * HW] = v[e] + add[e];
+                        for (int e = 0; e < 16; ++e)
+                            if (e < nvalid) ptx::red_add_f32(dst + e * HW, v[e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (e < nvalid) dst[e * HW] = v[e] + add[e];
+                    }
                 }
                 if (gch <= 0) {  // no chunk for this group: release at once
                     ptx::tc_fence_before();
@@ -1419,7 +1446,7 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                 case 6: d4_epilogue_nb<6>(E, t0, nb, rel); break;
                 default:  // no kernel tap reaches this class: the gradient is 0
                     d4_epilogue_nb<1>(E, t0, 0, rel);
-                    for (int t = t0; out && t < t0 + nb; ++t) {
+                    for (int t = t0; out && !a.red_add && t < t0 + nb; ++t) {
                         const int cc = eg + 2 * t;
                         for (int e = 0; e < 16 && cc * 16 + e < cl_all; ++e) {
                             const long long idx = pix + (long long)(c0 + cc * 16 + e) * HW;
@@ -1446,6 +1473,31 @@ __global__ void __launch_bounds__(kD4Threads, 1)
 }
 
 // -------------------------------------------------------------- host side
+
+// prev = residual (+ prev when accumulating), before the input gradient adds
+// its result to prev at the L2: a streaming pass, so that the input
+// gradient's epilogue reads nothing.  n elements; float4 where aligned.
+__global__ void __launch_bounds__(256)
+    prev_init_kernel(float *__restrict__ prev, const float *__restrict__ residual, long long n,
+                     int accumulate) {
+    ptx::griddep_wait();
+    const long long n4 = n / 4;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    float4 *p4 = reinterpret_cast<float4 *>(prev);
+    const float4 *r4 = reinterpret_cast<const float4 *>(residual);
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += stride) {
+        float4 r = __ldg(r4 + i);
+        if (accumulate) {
+            const float4 o = p4[i];
+            r.x += o.x; r.y += o.y; r.z += o.z; r.w += o.w;
+        }
+        p4[i] = r;
+    }
+    for (long long i = n4 * 4 + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += stride)
+        prev[i] = residual[i] + (accumulate ? prev[i] : 0.f);
+    ptx::griddep_launch_dependents();
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
@@ -1800,14 +1852,28 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzt, const float *resid
             CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    // With a residual or accumulation, prev is set to residual (+ old prev)
+    // first and every class adds its result to it at the L2 (red_add).
+    const bool red_add = residual != nullptr || p.accumulate != 0;
+    if (residual) {
+        const long long n = (long long)p.N * p.C * p.H * p.W;
+        const unsigned blocks = (unsigned)std::min<long long>((n / 4 + 255) / 256 + 1,
+                                                              (long long)p.num_sms * 8);
+        cudaError_t e = launch_pdl(prev_init_kernel, dim3(blocks), dim3(256), 0, st, prev,
+                                   residual, n, p.accumulate);
+        if (e != cudaSuccess) return e;
+        *launches += 1;
+    }
     for (int cl = 0; cl < p.stride * p.stride; ++cl) {
         const ClassTaps c = class_taps(p, g.He, g.We, cl);
         if (c.Hc == 0 || c.Wc == 0) continue;
         Dg3Args a;
-        a.residual = residual; a.prev = prev;
+        a.residual = red_add ? nullptr : residual; a.prev = prev;
+        a.red_add = red_add ? 1 : 0;
         a.status = ws_at<unsigned>(ws, p.off_status);
         a.C = p.C; a.He = g.He; a.We = g.We; a.Pp = g.Pp; a.Qpp = g.Qpp;
-        a.bd_lo = g.bd_lo; a.bq_lo = g.bq_lo; a.stride = p.stride; a.accumulate = p.accumulate;
+        a.bd_lo = g.bd_lo; a.bq_lo = g.bq_lo; a.stride = p.stride;
+        a.accumulate = red_add ? 0 : p.accumulate;
         a.ph = cl / p.stride; a.pw = cl % p.stride; a.Hc = c.Hc; a.Wc = c.Wc;
         a.nr = c.nr; a.ns = c.ns;
         for (int i = 0; i < kD2MaxTaps; ++i) {
