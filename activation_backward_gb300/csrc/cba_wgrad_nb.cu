@@ -74,6 +74,19 @@ struct DzSrc {
         const float zz = BN ? __ldg(z + off) : 0.f;
         return dz_of<ACT, BN>(__ldg(delta + off), y, zz, coef[k]);
     }
+    // four consecutive elements (off a multiple of 4), TF32-rounded
+    __device__ __forceinline__ float4 load4(long long off, int k) const {
+        const float4 d = __ldg(reinterpret_cast<const float4 *>(delta + off));
+        const float4 y = (ACT == CBA_ACT_LEAKY) ? __ldg(reinterpret_cast<const float4 *>(output + off))
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 zz = BN ? __ldg(reinterpret_cast<const float4 *>(z + off))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        const Coef cf = coef[k];
+        return make_float4(rna_tf32(dz_of<ACT, BN>(d.x, y.x, zz.x, cf)),
+                           rna_tf32(dz_of<ACT, BN>(d.y, y.y, zz.y, cf)),
+                           rna_tf32(dz_of<ACT, BN>(d.z, y.z, zz.z, cf)),
+                           rna_tf32(dz_of<ACT, BN>(d.w, y.w, zz.w, cf)));
+    }
 };
 
 // src: [N][CH][PLANE] (channels CH, PLANE = rows x columns flattened), dst:
@@ -125,7 +138,7 @@ __global__ void __launch_bounds__(256)
 // grid: x = position chunks of 32, y = nc * chunks of 8 channels over Kp.
 // Channels K .. Kp - 1 of dzc are written as zeros; the border by
 // dzc_border_kernel.
-template <int NB, int ACT, bool BN, bool DZC>
+template <int NB, int ACT, bool BN, bool DZC, bool VEC>
 __global__ void __launch_bounds__(256)
     dz_layouts_kernel(DzSrc<ACT, BN> src, int N, int K, int Kp, int PQ, int Qe, int Pp, int Qpp,
                       int bd_lo, int bq_lo, int cchunks, float *__restrict__ dzn,
@@ -135,21 +148,47 @@ __global__ void __launch_bounds__(256)
     const int t = threadIdx.x;
     const int pos0 = blockIdx.x * 32;
     const int j = blockIdx.y / cchunks, k0 = (blockIdx.y % cchunks) * 8;
-    constexpr int PER = NB * 8 * 32 / 256;
-    float v[PER];
+    if constexpr (VEC) {
+        // P*Q a multiple of 4: float4 reads along the positions, all issued
+        // before the first store to shared memory
+        constexpr int PER4 = NB * 8 * 8 / 256;
+        float4 v[PER4];
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int e = t + u * 256;
-        const int pos = e & 31, rc = e >> 5;
-        const int n = j * NB + (rc >> 3), k = k0 + (rc & 7), pp = pos0 + pos;
-        v[u] = (n < N && k < K && pp < PQ) ? rna_tf32(src(((long long)n * K + k) * PQ + pp, k))
-                                           : 0.f;
-    }
+        for (int u = 0; u < PER4; ++u) {
+            const int e = t + u * 256;
+            const int q4 = e & 7, rc = e >> 3;
+            const int n = j * NB + (rc >> 3), k = k0 + (rc & 7), pp = pos0 + 4 * q4;
+            v[u] = (n < N && k < K && pp < PQ) ? src.load4(((long long)n * K + k) * PQ + pp, k)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int e = t + u * 256;
-        const int rc = e >> 5;
-        tile[e & 31][(rc & 7) * NB + (rc >> 3)] = v[u];
+        for (int u = 0; u < PER4; ++u) {
+            const int e = t + u * 256;
+            const int q4 = e & 7, rc = e >> 3;
+            const int col = (rc & 7) * NB + (rc >> 3);
+            tile[4 * q4 + 0][col] = v[u].x;
+            tile[4 * q4 + 1][col] = v[u].y;
+            tile[4 * q4 + 2][col] = v[u].z;
+            tile[4 * q4 + 3][col] = v[u].w;
+        }
+    } else {
+        constexpr int PER = NB * 8 * 32 / 256;
+        float v[PER];
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int e = t + u * 256;
+            const int pos = e & 31, rc = e >> 5;
+            const int n = j * NB + (rc >> 3), k = k0 + (rc & 7), pp = pos0 + pos;
+            v[u] = (n < N && k < K && pp < PQ)
+                       ? rna_tf32(src(((long long)n * K + k) * PQ + pp, k))
+                       : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int e = t + u * 256;
+            const int rc = e >> 5;
+            tile[e & 31][(rc & 7) * NB + (rc >> 3)] = v[u];
+        }
     }
     __syncthreads();
     ptx::griddep_launch_dependents();
@@ -625,11 +664,12 @@ cudaError_t launch_dz_layouts_t(const Plan &p, const DzcGeom &g, const float *de
     const int nc = (p.N + NB - 1) / NB;
     dim3 grid((unsigned)((p.PQ + 31) / 32), (unsigned)(nc * cchunks));
     const DzSrc<ACT, BN> src{delta, output, z, coef};
-    if (dzc)
-        return launch_pdl(dz_layouts_kernel<NB, ACT, BN, true>, grid, dim3(256), 0, st, src, p.N,
-                          p.K, g.Kp, p.PQ, g.Qe, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, cchunks, dzn, dzc);
-    return launch_pdl(dz_layouts_kernel<NB, ACT, BN, false>, grid, dim3(256), 0, st, src, p.N, p.K,
-                      g.Kp, p.PQ, g.Qe, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, cchunks, dzn, dzc);
+    auto kern = dzc ? (p.PQ % 4 == 0 ? dz_layouts_kernel<NB, ACT, BN, true, true>
+                                     : dz_layouts_kernel<NB, ACT, BN, true, false>)
+                    : (p.PQ % 4 == 0 ? dz_layouts_kernel<NB, ACT, BN, false, true>
+                                     : dz_layouts_kernel<NB, ACT, BN, false, false>);
+    return launch_pdl(kern, grid, dim3(256), 0, st, src, p.N, p.K, g.Kp, p.PQ, g.Qe, g.Pp, g.Qpp,
+                      g.bd_lo, g.bq_lo, cchunks, dzn, dzc);
 }
 
 template <int NB>
