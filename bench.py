@@ -72,6 +72,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the per_config entries (configs 1-5, 1 GPU only)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (a smaller case for profiling)")
+    ap.add_argument("--layer-index", type=int, default=None,
+                    help="time only this layer call of the workload (config 5 has two: "
+                         "0 = the 3x3 conv, 1 = the 1x1 conv); for profiling")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target seconds of oracle work for cpu_baseline")
     return ap.parse_args()
@@ -289,14 +294,17 @@ def workload_layers(args, cid=None):
     from activation_backward_gb300 import ACT_NAMES, inputs
     cid = args.config if cid is None else cid
     groups = getattr(args, "groups", 1)
-    layers = (inputs.make_config(cid) if groups == 1
-              else [inputs.make_grouped_config(cid, groups)])
+    batch = getattr(args, "batch", None)
+    layers = (inputs.make_config(cid, batch=batch) if groups == 1
+              else [inputs.make_grouped_config(cid, groups, batch=batch)])
     if getattr(args, "act", None):
         code = {v: k for k, v in ACT_NAMES.items()}[args.act]
         layers = [inputs.with_activation(l, code) for l in layers]
     if args.bn == "frozen":
         layers = [inputs.with_frozen_stats(l, 700 + i) if l["bn"] else l
                   for i, l in enumerate(layers)]
+    if getattr(args, "layer_index", None) is not None:
+        layers = [layers[args.layer_index]]
     return layers
 
 
@@ -381,7 +389,7 @@ def time_workload(cid, args, dev, math, steps, warmup, stream, flush, phases=Tru
     def step(events_per_layer=None):
         n = 0
         for i, dl in enumerate(dls):
-            if i > 0 and cid == 5:
+            if i > 0 and cid == 5 and len(dls) == 2:
                 dl.delta.copy_(dls[0].prev)  # conv1's delta is conv2's prev_delta
             n += dl.run_traced(events_per_layer[i] if events_per_layer else None)
         return n
@@ -552,7 +560,8 @@ def run_ours(args):
         phases = summarize(t, tf32, hbm)
 
     per_config = None
-    if ws == 1 and not args.no_per_config and args.layer == "conv" and args.groups == 1:
+    if (ws == 1 and not args.no_per_config and args.layer == "conv" and args.groups == 1
+            and args.layer_index is None and args.batch is None):
         per_config = {}
         for cid in range(1, 6):
             if cid == args.config:
