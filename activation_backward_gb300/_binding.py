@@ -51,9 +51,13 @@ EXPORTS = ("cba_workspace_bytes", "cba_workspace_bytes_ex", "cba_workspace_bytes
            "cba_get_status", "cba_bn_act_backward_noalloc",
            "cba_selftest_bounded_wait", "cba_yolo_backward", "cba_route_backward",
            "cba_pooled_size", "cba_maxpool_backward", "cba_error_string", "cba_last_cuda_error",
-           "cba_version")
+           "cba_version", "cba_plan_info")
 CBA_ROUTE_MAX_INPUTS = 8
 CBA_WS_RECOMPUTE_Z = 1
+CBA_PHASE_EVENTS = 5
+CBA_PATH_FFMA = 0
+CBA_PATH_TC_ROWS = 1
+CBA_PATH_TC_BATCH_INNER = 2
 
 
 class cba_desc_t(ctypes.Structure):
@@ -62,6 +66,11 @@ class cba_desc_t(ctypes.Structure):
                 ("S", ctypes.c_int), ("stride", ctypes.c_int), ("pad", ctypes.c_int),
                 ("act", ctypes.c_int), ("batch_normalize", ctypes.c_int),
                 ("accumulate", ctypes.c_int), ("eps", ctypes.c_float), ("math", ctypes.c_int)]
+
+
+class cba_plan_info_t(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("layout_bytes_read", ctypes.c_longlong),
+                ("layout_bytes_written", ctypes.c_longlong)]
 
 
 class cba_pool_desc_t(ctypes.Structure):
@@ -97,8 +106,8 @@ def load(path=LIB_PATH):
                                                    [vp] * 15 + [sz, vp])
     L.cba_conv_bn_act_backward_grouped_traced.restype = ctypes.c_int
     L.cba_conv_bn_act_backward_grouped_traced.argtypes = (
-        [ctypes.POINTER(cba_desc_t), ctypes.c_int] + [vp] * 15 + [sz, vp,
-                                                                ctypes.POINTER(ctypes.c_int)])
+        [ctypes.POINTER(cba_desc_t), ctypes.c_int] + [vp] * 15 +
+        [sz, vp, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_int)])
     L.cba_workspace_bytes_ex.restype = sz
     L.cba_workspace_bytes_ex.argtypes = [ctypes.POINTER(cba_desc_t), ctypes.c_uint]
     L.cba_conv_bn_act_backward.restype = ctypes.c_int
@@ -127,6 +136,9 @@ def load(path=LIB_PATH):
     L.cba_error_string.argtypes = [ctypes.c_int]
     L.cba_last_cuda_error.restype = ctypes.c_int
     L.cba_version.restype = ctypes.c_int
+    L.cba_plan_info.restype = ctypes.c_int
+    L.cba_plan_info.argtypes = [ctypes.POINTER(cba_desc_t), ctypes.c_int, ctypes.c_int,
+                                ctypes.POINTER(cba_plan_info_t)]
     _lib = L
     return L
 
@@ -186,17 +198,30 @@ def cba_conv_bn_act_backward_grouped(desc, groups, x, output, z, delta, W, gamma
     return rc
 
 
+def _events(events):
+    """None, or a C array of the CUDA events of CBA_PHASE_EVENTS torch.cuda.Event."""
+    if events is None:
+        return None
+    assert len(events) == CBA_PHASE_EVENTS
+    for e in events:
+        if e.cuda_event == 0:  # torch creates the CUDA event on its first record
+            e.record()
+    return (ctypes.c_void_p * CBA_PHASE_EVENTS)(*[e.cuda_event for e in events])
+
+
 def cba_conv_bn_act_backward_grouped_traced(desc, groups, x, output, z, delta, W, gamma, mean,
                                             var, residual, dW, db, dgamma, prev_delta, dz_out,
                                             workspace, workspace_bytes=None, stream=None,
-                                            check=True):
-    """As cba_conv_bn_act_backward_grouped; returns (rc, kernels enqueued)."""
+                                            events=None, check=True):
+    """As cba_conv_bn_act_backward_grouped, with ``events`` as for
+    cba_conv_bn_act_backward_traced; returns (rc, kernels enqueued)."""
     wsb = _bytes(workspace) if workspace_bytes is None else int(workspace_bytes)
     n = ctypes.c_int(0)
     rc = load().cba_conv_bn_act_backward_grouped_traced(
         ctypes.byref(desc), int(groups), _ptr(x), _ptr(output), _ptr(z), _ptr(delta), _ptr(W),
         _ptr(gamma), _ptr(mean), _ptr(var), _ptr(residual), _ptr(dW), _ptr(db), _ptr(dgamma),
-        _ptr(prev_delta), _ptr(dz_out), _ptr(workspace), wsb, _stream(stream), ctypes.byref(n))
+        _ptr(prev_delta), _ptr(dz_out), _ptr(workspace), wsb, _stream(stream), _events(events),
+        ctypes.byref(n))
     if check and rc != CBA_OK:
         raise CbaError(rc, "cba_conv_bn_act_backward_grouped_traced")
     return rc, n.value
@@ -220,17 +245,11 @@ def cba_conv_bn_act_backward(desc, x, output, z, delta, W, gamma, mean, var, res
 def cba_conv_bn_act_backward_traced(desc, x, output, z, delta, W, gamma, mean, var, residual,
                                     dW, db, dgamma, prev_delta, dz_out, workspace,
                                     workspace_bytes=None, stream=None, events=None, check=True):
-    """As cba_conv_bn_act_backward; ``events`` is None or 4 torch.cuda.Event
+    """As cba_conv_bn_act_backward; ``events`` is None or 5 torch.cuda.Event
     (created with enable_timing=True) recorded between the phases.  Returns
     (code, number of kernels enqueued)."""
     wsb = _bytes(workspace) if workspace_bytes is None else int(workspace_bytes)
-    ev = None
-    if events is not None:
-        assert len(events) == 4
-        for e in events:
-            if e.cuda_event == 0:  # torch creates the CUDA event on its first record
-                e.record()
-        ev = (ctypes.c_void_p * 4)(*[e.cuda_event for e in events])
+    ev = _events(events)
     n = ctypes.c_int(0)
     rc = load().cba_conv_bn_act_backward_traced(
         ctypes.byref(desc), _ptr(x), _ptr(output), _ptr(z), _ptr(delta), _ptr(W), _ptr(gamma),
@@ -254,6 +273,17 @@ def cba_bn_act_backward_noalloc(desc, output, z, delta, gamma, mean, var, db, dg
     if check and rc != CBA_OK:
         raise CbaError(rc, "cba_bn_act_backward_noalloc")
     return rc
+
+
+def cba_plan_info(desc, groups=1, with_prev=True):
+    """(path, layout bytes read, layout bytes written) of a call with this
+    descriptor; raises CbaError for a descriptor the call would refuse."""
+    info = cba_plan_info_t()
+    rc = load().cba_plan_info(ctypes.byref(desc), int(groups), int(bool(with_prev)),
+                              ctypes.byref(info))
+    if rc != CBA_OK:
+        raise CbaError(rc, "cba_plan_info")
+    return info.path, info.layout_bytes_read, info.layout_bytes_written
 
 
 def cba_get_status(workspace, workspace_bytes=None, stream=None):

@@ -8,6 +8,7 @@
 #include <cstring>
 
 #include "cba_internal.cuh"
+#include "cba_repack.cuh"
 
 namespace cba {
 
@@ -38,12 +39,13 @@ void plan_reduction(Plan *p, long long max_parts) {
     p->red_pieces = (int)pieces;
 }
 
-int make_plan(const cba_desc_t *d, Plan *p) {
+int make_plan(const cba_desc_t *d, Plan *p, int groups) {
     if (!d || !p) return CBA_ERR_ARG;
     std::memset(p, 0, sizeof(*p));
     if (d->N <= 0 || d->C <= 0 || d->H <= 0 || d->W <= 0 || d->K <= 0 || d->R <= 0 ||
         d->S <= 0 || d->stride <= 0 || d->pad < 0)
         return CBA_ERR_ARG;
+    if (groups < 1 || d->C % groups != 0 || d->K % groups != 0) return CBA_ERR_ARG;
     if (d->act < CBA_ACT_LINEAR || d->act > CBA_ACT_STAIR) return CBA_ERR_ARG;
     if (d->math != CBA_MATH_TF32 && d->math != CBA_MATH_FFMA) return CBA_ERR_ARG;
     if (d->batch_normalize < 0 || d->batch_normalize > 2) return CBA_ERR_ARG;
@@ -61,6 +63,7 @@ int make_plan(const cba_desc_t *d, Plan *p) {
         return CBA_ERR_UNSUPPORTED;
 
     p->N = d->N; p->C = d->C; p->H = d->H; p->W = d->W; p->K = d->K; p->R = d->R; p->S = d->S;
+    p->groups = groups; p->Cg = d->C / groups; p->Kg = d->K / groups;
     p->stride = d->stride; p->pad = d->pad; p->P = (int)P; p->Q = (int)Q;
     p->PQ = (int)(P * Q); p->HW = d->H * d->W; p->RS = d->R * d->S; p->CRS = d->C * p->RS;
     p->m = (long long)d->N * P * Q;
@@ -81,13 +84,14 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->wg_chunk = chunk;
     p->wg_splits = (int)ceil_div(p->m, chunk);
 
-    p->use_tc2 = (p->math == CBA_MATH_TF32) && tc2_supported(*p);
-    // the batch-innermost weight gradient where the TMEM-operand one does not
-    // apply (strides, kernel sizes, rows not 16-byte strided): where both do,
-    // the latter needs no re-laid-out x and measured faster
-    p->use_wnb = p->use_tc2 && wgrad_tc4_ws_bytes(*p) == 0 && wgrad_nb_supported(*p);
-    p->use_tc = !p->use_tc2 && (p->math == CBA_MATH_TF32) && tc_supported(*p);
-    if (p->use_tc) tc_plan(*p);
+    // tensor cores: the weight gradient with TMA-fed input rows where it
+    // applies (stride-1 3x3 and 1x1 layers with 16-byte-strided input rows; it
+    // needs no re-laid-out x and measured faster there), the batch-innermost
+    // one everywhere else
+    const bool tc_math = p->math == CBA_MATH_TF32 && tc2_supported(*p);
+    const bool w4 = tc_math && wgrad_tc4_supported(*p);
+    p->use_wnb = tc_math && !w4 && wgrad_nb_supported(*p);
+    p->use_tc2 = w4 || p->use_wnb;
 
     // workspace carve-up
     size_t off = 0;
@@ -104,13 +108,10 @@ int make_plan(const cba_desc_t *d, Plan *p) {
     p->off_coef = off;
     off = align_up(off + sizeof(Coef) * (size_t)p->K, 256);
     p->off_wgpart = off;
-    size_t wg_simt = p->use_tc2 ? 0 : sizeof(float) * (size_t)p->wg_splits * p->K * p->CRS;
-    size_t wg_tc = p->use_tc ? sizeof(float) * (size_t)p->tc_wg_splits * p->K * p->CRS : 0;
-    off = align_up(off + std::max(wg_simt, wg_tc), 256);
-    p->off_wt = off;
-    if (p->use_tc) off = align_up(off + sizeof(float) * (size_t)nw, 256);
-    p->off_dzt = off;
-    if (p->use_tc2) off = align_up(off + tc2_dzt_bytes(*p), 256);
+    if (!p->use_tc2)  // split-K partials of the SIMT weight gradient
+        off = align_up(off + sizeof(float) * (size_t)p->wg_splits * p->K * p->CRS, 256);
+    p->off_dzc = off;
+    if (p->use_tc2) off = align_up(off + tc2_dzc_bytes(*p), 256);
     p->off_wr = off;
     if (p->use_tc2) off = align_up(off + tc2_wr_bytes(*p), 256);
     p->off_dprime = off;
@@ -210,9 +211,9 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
                   const float *delta, const float *Wt, const float *gamma, const float *mean,
                   const float *var, const float *residual, float *dW, float *db, float *dgamma,
                   float *prev_delta, float *dz_out, void *workspace, size_t workspace_bytes,
-                  void *stream, void *const *events, int *launches, bool clear_status = true) {
+                  void *stream, void *const *events, int *launches, int groups = 1) {
     Plan p;
-    int rc = make_plan(d, &p);
+    int rc = make_plan(d, &p, groups);
     if (rc != CBA_OK) return rc;
     if (!x || !delta || !Wt || !dW || !db) return CBA_ERR_ARG;
     if (p.act_in != CBA_ACT_LINEAR && !output) return CBA_ERR_ARG;
@@ -231,18 +232,15 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
     cudaGetLastError();  // the launches below report only their own errors
     cudaError_t e = select_device(st, delta);
     if (e != cudaSuccess) return fail_cuda(e);
-    // status word (unless a previous call of the same grouped call set it) and
-    // the reduction counters
-    e = clear_status ? cudaMemsetAsync(workspace, 0, p.clear_bytes, st)
-                     : cudaMemsetAsync(ws_at<char>(workspace, p.off_cnt), 0,
-                                       p.clear_bytes - p.off_cnt, st);
+    // status word, reduction counters and weight-gradient accumulators
+    e = cudaMemsetAsync(workspace, 0, p.clear_bytes, st);
     if (e == cudaSuccess) e = tr.mark(0);
     if (e == cudaSuccess && z_free) {
         float *zbuf = ws_at<float>(workspace, p.off_z);
         cba_desc_t dv;
         Plan pv;
         if (p.fwd_tc && forward_desc(*d, &dv) && make_plan(&dv, &pv) == CBA_OK) {
-            e = launch_conv_forward_tc(pv, x, Wt, workspace, zbuf, st, &n_launch);
+            e = launch_conv_forward_tc(pv, x, Wt, workspace, zbuf, p.Cg, p.Kg, st, &n_launch);
             // the forward's scratch may overlap the reduction counters: zero them
             // again (the status word keeps what the forward set)
             if (e == cudaSuccess)
@@ -260,218 +258,55 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
         e = launch_gradient_array(p, delta, output, dprime, st, &n_launch);
         delta = dprime;
     }
-    // the tensor-core input gradient reads repacked weights: written by extra
-    // blocks of the reduction pass
-    const bool repack = p.use_tc2 && prev_delta != nullptr;
     if (e == cudaSuccess)
         e = launch_reduce(p, delta, output, z, gamma, mean, var, db, dgamma, workspace, st,
-                          &n_launch, repack ? Wt : nullptr,
-                          repack ? ws_at<float>(workspace, p.off_wr) : nullptr);
+                          &n_launch);
     if (e == cudaSuccess && dz_out) {
         e = launch_dz_out(p, delta, output, z, workspace, dz_out, st);
         ++n_launch;
     }
-    if (p.use_tc2 && p.use_wnb) {
-        // dz channels-last for the input gradient; x and dz batch-innermost for
-        // the weight gradient (its layout passes count in its phase)
-        float *dzt = ws_at<float>(workspace, p.off_dzt);
-        float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) +
-                                               dzc_geom(p).dzt_bytes);
-        float *xn = ws_at<float>(workspace, p.off_xn), *dzn = ws_at<float>(workspace, p.off_dzn);
-        if (e == cudaSuccess)
-            e = launch_dz_layouts(p, delta, output, z, workspace, dzn,
-                                  prev_delta ? dzc : nullptr, st, &n_launch);
-        if (e == cudaSuccess) e = tr.mark(1);
-        if (e == cudaSuccess) e = launch_xn(p, x, xn, st, &n_launch);
-        if (e == cudaSuccess)
-            e = launch_wgrad_nb(p, xn, dzn, dW, workspace, ws_at<float>(workspace, p.off_wgacc), st,
-                                &n_launch);
-        if (e == cudaSuccess) e = tr.mark(2);
-        if (e == cudaSuccess && prev_delta)
-            e = launch_dgrad_tc2(p, dzt, residual, prev_delta, workspace,
-                                 ws_at<float>(workspace, p.off_wr), st, &n_launch);
-        if (e == cudaSuccess) e = tr.mark(3);
-        if (launches) *launches = n_launch;
-        if (e != cudaSuccess) return fail_cuda(e);
-        return CBA_OK;
-    }
-    if (p.use_tc2) {
-        float *dzt = ws_at<float>(workspace, p.off_dzt);
-        // the TMA-fed weight gradient reads only the channels-last dz copy
-        const bool w4 = wgrad_tc4_supported(p, x);
-        float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) +
-                                               dzc_geom(p).dzt_bytes);
-        if (e == cudaSuccess)
-            e = launch_dz_materialize(p, delta, output, z, workspace, dzt,
-                                      prev_delta != nullptr || w4, st, &n_launch, !w4);
-        if (e == cudaSuccess) e = tr.mark(1);
-        if (e == cudaSuccess)
-            e = w4 ? launch_wgrad_tc4(p, x, dzc, dW, workspace, st, &n_launch)
-                   : launch_wgrad_tc2(p, x, dzt, dW, workspace, st, &n_launch);
-        if (e == cudaSuccess) e = tr.mark(2);
-        if (e == cudaSuccess && prev_delta)
-            e = launch_dgrad_tc2(p, dzt, residual, prev_delta, workspace,
-                                 ws_at<float>(workspace, p.off_wr), st, &n_launch);
-        if (e == cudaSuccess) e = tr.mark(3);
-        if (launches) *launches = n_launch;
-        if (e != cudaSuccess) return fail_cuda(e);
-        return CBA_OK;
-    }
     if (e == cudaSuccess) e = tr.mark(1);
-    if (e == cudaSuccess) {
-        e = p.use_tc ? launch_wgrad_tc(p, x, delta, output, z, dW, workspace, st, &n_launch)
-                     : launch_wgrad_simt(p, x, delta, output, z, dW, workspace, st, &n_launch);
+    if (p.use_tc2) {
+        // the GEMM operand layouts: dz channels-last for the input gradient
+        // (and for the weight gradient with TMA-fed rows); x and dz
+        // batch-innermost for the other weight gradient
+        float *dzc = ws_at<float>(workspace, p.off_dzc);
+        float *xn = ws_at<float>(workspace, p.off_xn), *dzn = ws_at<float>(workspace, p.off_dzn);
+        if (p.use_wnb) {
+            if (e == cudaSuccess)
+                e = launch_dz_layouts(p, delta, output, z, workspace, dzn,
+                                      prev_delta ? dzc : nullptr, st, &n_launch);
+            if (e == cudaSuccess) e = launch_xn(p, x, xn, st, &n_launch);
+        } else if (e == cudaSuccess) {
+            e = launch_dzc(p, delta, output, z, workspace, dzc, st, &n_launch);
+        }
+        if (e == cudaSuccess) e = tr.mark(2);
+        // the tensor-core input gradient reads repacked weights: written by
+        // extra blocks of the weight gradient's accumulator-apply launch
+        const RepackJob rep = make_repack_job(p, Wt, ws_at<float>(workspace, p.off_wr));
+        const RepackJob *repp = prev_delta ? &rep : nullptr;
+        if (e == cudaSuccess)
+            e = p.use_wnb ? launch_wgrad_nb(p, xn, dzn, dW, workspace,
+                                            ws_at<float>(workspace, p.off_wgacc), repp, st,
+                                            &n_launch)
+                          : launch_wgrad_tc4(p, x, dzc, dW, workspace, repp, st, &n_launch);
+        if (e == cudaSuccess) e = tr.mark(3);
+        if (e == cudaSuccess && prev_delta)
+            e = launch_dgrad_tc2(p, dzc, residual, prev_delta, workspace,
+                                 ws_at<float>(workspace, p.off_wr), st, &n_launch);
+    } else {
+        // the SIMT kernels apply the BN transform while they load delta
+        if (e == cudaSuccess) e = tr.mark(2);
+        if (e == cudaSuccess) e = launch_wgrad_simt(p, x, delta, output, z, dW, workspace, st,
+                                                    &n_launch);
+        if (e == cudaSuccess) e = tr.mark(3);
+        if (e == cudaSuccess && prev_delta)
+            e = launch_dgrad_simt(p, Wt, delta, output, z, residual, prev_delta, workspace, st,
+                                  &n_launch);
     }
-    if (e == cudaSuccess) e = tr.mark(2);
-    if (e == cudaSuccess && prev_delta) {
-        e = p.use_tc ? launch_dgrad_tc(p, Wt, delta, output, z, residual, prev_delta, workspace,
-                                       st, &n_launch)
-                     : launch_dgrad_simt(p, Wt, delta, output, z, residual, prev_delta,
-                                         workspace, st, &n_launch);
-    }
-    if (e == cudaSuccess) e = tr.mark(3);
+    if (e == cudaSuccess) e = tr.mark(4);
     if (launches) *launches = n_launch;
     if (e != cudaSuccess) return fail_cuda(e);
-    return CBA_OK;
-}
-
-// Workspace layout of a grouped call: the per-group workspace at 0 (so that
-// its status word is the workspace's first word), then channel-slice
-// temporaries of one group.
-struct GroupPlan {
-    cba_desc_t dg;  // the descriptor of one group: C / groups, K / groups
-    size_t sub, off_x, off_delta, off_out, off_z, off_res, off_prev, off_dz, off_w, off_dw,
-        off_vec, total;
-    long long xg, og, wg;  // elements per image of a group's x and output slices; W slice
-};
-
-int make_group_plan(const cba_desc_t *d, int groups, bool z_free, GroupPlan *gp) {
-    if (!d || groups < 1 || d->C % groups != 0 || d->K % groups != 0) return CBA_ERR_ARG;
-    Plan p;
-    int rc = make_plan(d, &p);
-    if (rc != CBA_OK) return rc;
-    gp->dg = *d;
-    gp->dg.C = d->C / groups;
-    gp->dg.K = d->K / groups;
-    Plan pg;
-    rc = make_plan(&gp->dg, &pg);
-    if (rc != CBA_OK) return rc;
-    const size_t f = sizeof(float);
-    gp->xg = (long long)gp->dg.C * d->H * d->W;
-    gp->og = (long long)gp->dg.K * p.P * p.Q;
-    gp->wg = (long long)gp->dg.K * gp->dg.C * d->R * d->S;
-    const size_t xb = f * (size_t)d->N * gp->xg, ob = f * (size_t)d->N * gp->og;
-    size_t off = align_up(z_free && p.bn ? pg.total_z : pg.total, 256);
-    gp->sub = off;
-    gp->off_x = off; off = align_up(off + xb, 256);
-    gp->off_delta = off; off = align_up(off + ob, 256);
-    gp->off_out = off; off = align_up(off + ob, 256);
-    gp->off_z = off; off = align_up(off + ob, 256);
-    gp->off_res = off; off = align_up(off + xb, 256);
-    gp->off_prev = off; off = align_up(off + xb, 256);
-    gp->off_dz = off; off = align_up(off + ob, 256);
-    gp->off_w = off; off = align_up(off + f * (size_t)gp->wg, 256);
-    gp->off_dw = off; off = align_up(off + f * (size_t)gp->wg, 256);
-    gp->off_vec = off; off = align_up(off + 5 * f * (size_t)gp->dg.K + 5 * 256, 256);
-    gp->total = off;
-    return CBA_OK;
-}
-
-// rows of `width` bytes, `height` of them, `spitch` / `dpitch` bytes apart
-inline cudaError_t copy_rows(void *dst, size_t dpitch, const void *src, size_t spitch,
-                             size_t width, size_t height, cudaStream_t st) {
-    return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, height, cudaMemcpyDeviceToDevice,
-                             st);
-}
-
-int grouped_impl(const cba_desc_t *d, int groups, const float *x, const float *output,
-                 const float *z, const float *delta, const float *Wt, const float *gamma,
-                 const float *mean, const float *var, const float *residual, float *dW,
-                 float *db, float *dgamma, float *prev_delta, float *dz_out, void *workspace,
-                 size_t workspace_bytes, void *stream, int *launches) {
-    Plan p;
-    int rc = make_plan(d, &p);
-    if (rc != CBA_OK) return rc;
-    if (!x || !delta || !Wt || !dW || !db) return CBA_ERR_ARG;
-    if (p.act_in != CBA_ACT_LINEAR && !output) return CBA_ERR_ARG;
-    if (p.bn && (!gamma || !mean || !var || !dgamma)) return CBA_ERR_ARG;
-    const bool z_free = p.bn && !z;
-    GroupPlan gp;
-    rc = make_group_plan(d, groups, z_free, &gp);
-    if (rc != CBA_OK) return rc;
-    if (!workspace || workspace_bytes < gp.total) return CBA_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return CBA_ERR_ALIGN;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaGetLastError();
-    cudaError_t e = select_device(st, delta);
-    if (e != cudaSuccess) return fail_cuda(e);
-    const size_t f = sizeof(float);
-    const int N = d->N, Kg = gp.dg.K;
-    const size_t xrow = f * (size_t)gp.xg, orow = f * (size_t)gp.og;
-    const size_t xpitch = xrow * groups, opitch = orow * groups;
-    float *tx = ws_at<float>(workspace, gp.off_x), *td = ws_at<float>(workspace, gp.off_delta);
-    float *to = ws_at<float>(workspace, gp.off_out), *tz = ws_at<float>(workspace, gp.off_z);
-    float *tr = ws_at<float>(workspace, gp.off_res), *tp = ws_at<float>(workspace, gp.off_prev);
-    float *tdz = ws_at<float>(workspace, gp.off_dz), *tw = ws_at<float>(workspace, gp.off_w);
-    float *tdw = ws_at<float>(workspace, gp.off_dw);
-    const size_t vstride = align_up(f * (size_t)Kg, 256);
-    float *tg = ws_at<float>(workspace, gp.off_vec), *tm = ws_at<float>(workspace, gp.off_vec + vstride);
-    float *tv = ws_at<float>(workspace, gp.off_vec + 2 * vstride);
-    float *tdb = ws_at<float>(workspace, gp.off_vec + 3 * vstride);
-    float *tdg = ws_at<float>(workspace, gp.off_vec + 4 * vstride);
-    const size_t vb = f * (size_t)Kg, wb = f * (size_t)gp.wg;
-    int total_launches = 0;
-    for (int g = 0; g < groups && e == cudaSuccess; ++g) {
-        // in: the group's channel slices (strided by image), its weights and vectors
-        e = copy_rows(tx, xrow, x + g * gp.xg, xpitch, xrow, N, st);
-        if (e == cudaSuccess) e = copy_rows(td, orow, delta + g * gp.og, opitch, orow, N, st);
-        if (e == cudaSuccess && output && p.act_in != CBA_ACT_LINEAR)
-            e = copy_rows(to, orow, output + g * gp.og, opitch, orow, N, st);
-        if (e == cudaSuccess && p.bn && z)
-            e = copy_rows(tz, orow, z + g * gp.og, opitch, orow, N, st);
-        if (e == cudaSuccess && residual)
-            e = copy_rows(tr, xrow, residual + g * gp.xg, xpitch, xrow, N, st);
-        if (e == cudaSuccess && prev_delta && d->accumulate)
-            e = copy_rows(tp, xrow, prev_delta + g * gp.xg, xpitch, xrow, N, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(tw, Wt + g * gp.wg, wb, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(tdw, dW + g * gp.wg, wb, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(tdb, db + (size_t)g * Kg, vb, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess && p.bn) {
-            e = cudaMemcpyAsync(tg, gamma + (size_t)g * Kg, vb, cudaMemcpyDeviceToDevice, st);
-            if (e == cudaSuccess)
-                e = cudaMemcpyAsync(tm, mean + (size_t)g * Kg, vb, cudaMemcpyDeviceToDevice, st);
-            if (e == cudaSuccess)
-                e = cudaMemcpyAsync(tv, var + (size_t)g * Kg, vb, cudaMemcpyDeviceToDevice, st);
-            if (e == cudaSuccess)
-                e = cudaMemcpyAsync(tdg, dgamma + (size_t)g * Kg, vb, cudaMemcpyDeviceToDevice,
-                                    st);
-        }
-        if (e != cudaSuccess) break;
-        int n_group = 0;
-        rc = backward_impl(&gp.dg, tx, (output && p.act_in != CBA_ACT_LINEAR) ? to : nullptr,
-                           (p.bn && z) ? tz : nullptr, td, tw, p.bn ? tg : nullptr,
-                           p.bn ? tm : nullptr, p.bn ? tv : nullptr, residual ? tr : nullptr, tdw,
-                           tdb, p.bn ? tdg : nullptr, prev_delta ? tp : nullptr,
-                           dz_out ? tdz : nullptr, workspace, gp.sub, stream, nullptr,
-                           &n_group, g == 0);
-        if (rc != CBA_OK) return rc;
-        total_launches += n_group;
-        // out: the accumulated weights and vectors, prev and dz slices
-        e = cudaMemcpyAsync(dW + g * gp.wg, tdw, wb, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess)
-            e = cudaMemcpyAsync(db + (size_t)g * Kg, tdb, vb, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess && p.bn)
-            e = cudaMemcpyAsync(dgamma + (size_t)g * Kg, tdg, vb, cudaMemcpyDeviceToDevice, st);
-        if (e == cudaSuccess && prev_delta)
-            e = copy_rows(prev_delta + g * gp.xg, xpitch, tp, xrow, xrow, N, st);
-        if (e == cudaSuccess && dz_out)
-            e = copy_rows(dz_out + g * gp.og, opitch, tdz, orow, orow, N, st);
-    }
-    if (e != cudaSuccess) return fail_cuda(e);
-    if (launches) *launches = total_launches;
     return CBA_OK;
 }
 
@@ -485,10 +320,9 @@ int cba_conv_bn_act_backward_grouped(const cba_desc_t *d, int groups, const floa
                                      const float *var, const float *residual, float *dW,
                                      float *db, float *dgamma, float *prev_delta, float *dz_out,
                                      void *workspace, size_t workspace_bytes, void *stream) {
-    return cba_conv_bn_act_backward_grouped_traced(d, groups, x, output, z, delta, Wt, gamma,
-                                                   mean, var, residual, dW, db, dgamma,
-                                                   prev_delta, dz_out, workspace,
-                                                   workspace_bytes, stream, nullptr);
+    return backward_impl(d, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db, dgamma,
+                         prev_delta, dz_out, workspace, workspace_bytes, stream, nullptr,
+                         nullptr, groups);
 }
 
 int cba_conv_bn_act_backward_grouped_traced(const cba_desc_t *d, int groups, const float *x,
@@ -499,22 +333,16 @@ int cba_conv_bn_act_backward_grouped_traced(const cba_desc_t *d, int groups, con
                                             float *db, float *dgamma, float *prev_delta,
                                             float *dz_out, void *workspace,
                                             size_t workspace_bytes, void *stream,
-                                            int *launches) {
-    if (groups == 1)
-        return backward_impl(d, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db,
-                             dgamma, prev_delta, dz_out, workspace, workspace_bytes, stream,
-                             nullptr, launches);
-    return grouped_impl(d, groups, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db,
-                        dgamma, prev_delta, dz_out, workspace, workspace_bytes, stream,
-                        launches);
+                                            void *const *phase_events, int *launches) {
+    return backward_impl(d, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db, dgamma,
+                         prev_delta, dz_out, workspace, workspace_bytes, stream, phase_events,
+                         launches, groups);
 }
 
 size_t cba_workspace_bytes_grouped(const cba_desc_t *d, int groups, unsigned flags) {
-    if (flags & ~(unsigned)CBA_WS_RECOMPUTE_Z) return 0;
-    if (groups == 1) return cba_workspace_bytes_ex(d, flags);
-    GroupPlan gp;
-    if (make_group_plan(d, groups, (flags & CBA_WS_RECOMPUTE_Z) != 0, &gp) != CBA_OK) return 0;
-    return gp.total;
+    Plan p;
+    if (make_plan(d, &p, groups) != CBA_OK || (flags & ~(unsigned)CBA_WS_RECOMPUTE_Z)) return 0;
+    return (flags & CBA_WS_RECOMPUTE_Z) ? p.total_z : p.total;
 }
 
 int cba_conv_bn_act_backward(const cba_desc_t *d, const float *x, const float *output,
@@ -538,6 +366,32 @@ int cba_conv_bn_act_backward_traced(const cba_desc_t *d, const float *x, const f
     return backward_impl(d, x, output, z, delta, Wt, gamma, mean, var, residual, dW, db, dgamma,
                          prev_delta, dz_out, workspace, workspace_bytes, stream, phase_events,
                          launches);
+}
+
+int cba_plan_info(const cba_desc_t *d, int groups, int with_prev, cba_plan_info_t *info) {
+    if (!info) return CBA_ERR_ARG;
+    Plan p;
+    const int rc = make_plan(d, &p, groups);
+    if (rc != CBA_OK) return rc;
+    info->path = !p.use_tc2 ? CBA_PATH_FFMA : p.use_wnb ? CBA_PATH_TC_BATCH_INNER
+                                                        : CBA_PATH_TC_ROWS;
+    info->layout_bytes_read = 0;
+    info->layout_bytes_written = 0;
+    if (p.use_tc2) {
+        // dz from delta (or the delta' pass's output), output (leaky) and z (BN)
+        const long long out = (long long)sizeof(float) * p.N * p.K * p.PQ;
+        const int reads = 1 + (p.act == CBA_ACT_LEAKY ? 1 : 0) + (p.bn ? 1 : 0);
+        info->layout_bytes_read = reads * out;
+        const long long dzc = (long long)tc2_dzc_bytes(p);
+        if (p.use_wnb) {
+            info->layout_bytes_read += (long long)sizeof(float) * p.N * p.C * p.HW;  // x
+            info->layout_bytes_written = (long long)wgrad_nb_dzn_bytes(p) +
+                                         (long long)wgrad_nb_xn_bytes(p) + (with_prev ? dzc : 0);
+        } else {
+            info->layout_bytes_written = dzc;
+        }
+    }
+    return CBA_OK;
 }
 
 int cba_get_status(void *workspace, size_t workspace_bytes, void *stream) {

@@ -26,6 +26,7 @@ struct FwdArgs {
     const float *x, *W;
     float *z;
     int C, H, Wd, K, R, S, stride, pad, P, Q, PQ, RS, CRS;
+    int Cg, Kg;   // channels per group (W is [K][Cg][R][S])
     long long m;  // N * P * Q
 };
 
@@ -54,7 +55,13 @@ __global__ void __launch_bounds__(kFThreads) conv_forward_kernel(const FwdArgs a
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int l = l0 + a_l + e, k = k0 + a_k;
-            ra[e] = (l < a.CRS && k < a.K) ? __ldg(a.W + (long long)k * a.CRS + l) : 0.f;
+            float v = 0.f;
+            if (l < a.CRS && k < a.K) {
+                const int c = l / a.RS;
+                const long long o = w_off(k, c, l - c * a.RS, a.Cg, a.Kg, a.RS);
+                if (o >= 0) v = __ldg(a.W + o);
+            }
+            ra[e] = v;
         }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -121,10 +128,11 @@ __global__ void __launch_bounds__(kFThreads) conv_forward_kernel(const FwdArgs a
 
 // wr of the virtual convolution (K' = C, C' = K; [r][s][c'][k'], k' padded to
 // Kw' = round4(K')): W'[k'][c'][r][s] = W[c'][k'][R-1-r][S-1-s], TF32-rounded
-// (cvt.rna) as the input gradient's own weight repack rounds.
+// (cvt.rna) as the input gradient's own weight repack rounds; zero between
+// groups (Cg, Kg: the real layer's channels per group).
 __global__ void __launch_bounds__(256)
     repack_flipped_kernel(const float *__restrict__ W, float *__restrict__ wr, int Kv, int Cv,
-                          int R, int S, int Kw) {
+                          int R, int S, int Kw, int Cg, int Kg) {
     const long long total = (long long)R * S * Cv * Kw;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
@@ -134,10 +142,11 @@ __global__ void __launch_bounds__(256)
         t /= Cv;
         const int s = (int)(t % S), r = (int)(t / S);
         float v = 0.f;
-        if (kk < Kv) {
-            const float w = W[(((long long)c * Kv + kk) * R + (R - 1 - r)) * S + (S - 1 - s)];
+        const long long o =
+            kk < Kv ? w_off(c, kk, (R - 1 - r) * S + (S - 1 - s), Cg, Kg, R * S) : -1;
+        if (o >= 0) {
             uint32_t u;
-            asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(w));
+            asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(W[o]));
             v = __uint_as_float(u);
         }
         wr[i] = v;
@@ -165,20 +174,19 @@ bool forward_desc(const cba_desc_t &d, cba_desc_t *v) {
 }
 
 cudaError_t launch_conv_forward_tc(const Plan &pv, const float *x, const float *W, void *ws,
-                                   float *z, cudaStream_t st, int *launches) {
+                                   float *z, int Cg, int Kg, cudaStream_t st, int *launches) {
     const int Kw = (pv.K + 3) / 4 * 4;
     float *wr = ws_at<float>(ws, pv.off_wr);
     const long long total = (long long)pv.R * pv.S * pv.C * Kw;
     const unsigned blocks = (unsigned)std::min<long long>((total + 255) / 256, 1024);
-    repack_flipped_kernel<<<blocks, 256, 0, st>>>(W, wr, pv.K, pv.C, pv.R, pv.S, Kw);
+    repack_flipped_kernel<<<blocks, 256, 0, st>>>(W, wr, pv.K, pv.C, pv.R, pv.S, Kw, Cg, Kg);
     cudaError_t e = cudaGetLastError();
     *launches += 1;
-    float *dzt = ws_at<float>(ws, pv.off_dzt);
+    float *dzc = ws_at<float>(ws, pv.off_dzc);
     // x in the input gradient's channels-last, zero-bordered layout (the dz pass
     // with a linear activation and no BN passes its input through)
-    if (e == cudaSuccess)
-        e = launch_dz_materialize(pv, x, nullptr, nullptr, ws, dzt, true, st, launches, false);
-    if (e == cudaSuccess) e = launch_dgrad_tc2(pv, dzt, nullptr, z, ws, wr, st, launches);
+    if (e == cudaSuccess) e = launch_dzc(pv, x, nullptr, nullptr, ws, dzc, st, launches);
+    if (e == cudaSuccess) e = launch_dgrad_tc2(pv, dzc, nullptr, z, ws, wr, st, launches);
     return e;
 }
 
@@ -188,7 +196,7 @@ cudaError_t launch_conv_forward(const Plan &p, const float *x, const float *W, f
     a.x = x; a.W = W; a.z = z;
     a.C = p.C; a.H = p.H; a.Wd = p.W; a.K = p.K; a.R = p.R; a.S = p.S;
     a.stride = p.stride; a.pad = p.pad; a.P = p.P; a.Q = p.Q; a.PQ = p.PQ; a.RS = p.RS;
-    a.CRS = p.CRS; a.m = p.m;
+    a.CRS = p.CRS; a.m = p.m; a.Cg = p.Cg; a.Kg = p.Kg;
     const long long gx = (p.m + kFN - 1) / kFN;
     if (gx > 0x7fffffffLL) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)gx, (unsigned)((p.K + kFM - 1) / kFM));

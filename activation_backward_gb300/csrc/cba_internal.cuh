@@ -28,6 +28,11 @@ struct Plan {
     // geometry
     int N, C, H, W, K, R, S, stride, pad, P, Q;
     int PQ, HW, RS, CRS;
+    // grouped convolution: output channel k meets the Cg input channels of its
+    // group k / Kg; W and dW are [K][Cg][R][S].  The GEMM kernels compute the
+    // dense K x C product (the weights they read are zero between groups) and
+    // the kernels that read W or write dW map (k, c) with w_off below.
+    int groups, Cg, Kg;
     long long m;  // N*P*Q: elements per output channel
     int act, accumulate, math;  // act: the activation the main kernels apply
     int act_in;   // the descriptor's activation (cba_act_t)
@@ -44,20 +49,15 @@ struct Plan {
     int wg_splits;
     long long wg_chunk;  // reduction positions per split (multiple of the K tile)
     // tensor-core path
-    int use_tc;   // tensor cores, gather-producer kernels (cba_tc.cu)
     int use_tc2;  // tensor cores, TMEM-operand kernels (cba_tc2.cu); preferred
     int use_wnb;  // (with use_tc2) the weight gradient on batch-innermost layouts
                   // (cba_wgrad_nb.cu): x and dz re-laid out at off_xn / off_dzn
-    int tc_wg_splits, tc_wg_bn, tc_wg_ntiles;
-    long long tc_wg_chunk;
-    int tc_dg_bn, tc_dg_ntiles;
     // workspace layout (byte offsets from the base)
     // off_cnt: per-channel arrival counters of the reduction (zeroed with the
     // status word at the start of every call; clear_bytes covers both)
     // off_wgacc: the TMA-fed weight gradient's tile accumulators, inside the
     // cleared prefix (zeroed with the counters)
-    size_t off_status, off_cnt, off_wgacc, clear_bytes, off_red, off_coef, off_wgpart, off_wt,
-        off_dzt,
+    size_t off_status, off_cnt, off_wgacc, clear_bytes, off_red, off_coef, off_wgpart, off_dzc,
         off_wr, off_dprime, total;
     // z-free calls (BN without z): z = conv(x, W) goes to off_z; total_z bytes.
     // fwd_tc: the forward runs on the tensor cores as the input gradient of a
@@ -68,18 +68,33 @@ struct Plan {
 };
 
 // Builds the plan; returns CBA_OK or a CBA_ERR_* code.
-int make_plan(const cba_desc_t *d, Plan *p);
+int make_plan(const cba_desc_t *d, Plan *p, int groups = 1);
+
+// Offset of W[k][c - g*Cg][rs] (g = k / Kg, the group of output channel k) in
+// the [K][Cg][R*S] weight layout, or -1 when input channel c is not in that
+// group.  With one group: (k * C + c) * RS + rs.
+__host__ __device__ __forceinline__ long long w_off(int k, int c, int rs, int Cg, int Kg, int RS) {
+    const int cl = c - (k / Kg) * Cg;
+    if (cl < 0 || cl >= Cg) return -1;
+    return ((long long)k * Cg + cl) * RS + rs;
+}
 // The reduction pass's block shape (red_pln, red_groups, red_pieces): about
 // 3.5 blocks per SM, at most max_parts partials per channel.
 void plan_reduction(Plan *p, long long max_parts);
 
 // ---- launchers (each returns cudaSuccess or the launch error) ----
-// The reduction pass; with repack_W and repack_wr it also writes the input
-// gradient's repacked weights (wr[r][s][c][Kw], TF32-rounded) in extra blocks.
+// The reduction pass: db, dgamma and the per-channel coefficients.
 cudaError_t launch_reduce(const Plan &p, const float *delta, const float *output, const float *z,
                           const float *gamma, const float *mean, const float *var, float *db,
-                          float *dgamma, void *ws, cudaStream_t st, int *launches,
-                          const float *repack_W = nullptr, float *repack_wr = nullptr);
+                          float *dgamma, void *ws, cudaStream_t st, int *launches);
+
+// The input gradient's weight repack, W [K][Cg][R][S] -> wr [R][S][C][Kw]
+// (cba_repack.cuh).
+struct RepackJob {
+    const float *W;
+    float *wr;
+    int K, C, R, S, Kw, Cg, Kg;
+};
 // dz_out may be the delta buffer itself (an in-place transform).
 cudaError_t launch_dz_out(const Plan &p, const float *delta, const float *output, const float *z,
                           const void *ws, float *dz_out, cudaStream_t st);
@@ -92,9 +107,10 @@ cudaError_t launch_conv_forward(const Plan &p, const float *x, const float *W, f
 // descriptor does not have that form.
 bool forward_desc(const cba_desc_t &d, cba_desc_t *virt);
 // z through the tensor-core input gradient of the virtual convolution (plan
-// pv); ws is the call's workspace (pv's regions from offset 0).
+// pv); ws is the call's workspace (pv's regions from offset 0); Cg, Kg: the
+// real layer's input / output channels per group.
 cudaError_t launch_conv_forward_tc(const Plan &pv, const float *x, const float *W, void *ws,
-                                   float *z, cudaStream_t st, int *launches);
+                                   float *z, int Cg, int Kg, cudaStream_t st, int *launches);
 // Data-movement layers (cba_layers.cu).
 int pooled_size(int in, int k, int stride, int pad);
 cudaError_t launch_yolo_backward(const float *l_delta, float *net_delta, long long n,
@@ -113,34 +129,23 @@ cudaError_t launch_wgrad_simt(const Plan &p, const float *x, const float *delta,
 cudaError_t launch_dgrad_simt(const Plan &p, const float *Wt, const float *delta,
                               const float *output, const float *z, const float *residual,
                               float *prev, const void *ws, cudaStream_t st, int *launches);
-cudaError_t launch_wgrad_tc(const Plan &p, const float *x, const float *delta,
-                            const float *output, const float *z, float *dW, void *ws,
-                            cudaStream_t st, int *launches);
-cudaError_t launch_dgrad_tc(const Plan &p, const float *Wt, const float *delta,
-                            const float *output, const float *z, const float *residual,
-                            float *prev, void *ws, cudaStream_t st, int *launches);
 cudaError_t launch_splitk_reduce(const Plan &p, const float *part, int splits, float *dW,
                                  cudaStream_t st, int *launches);
 cudaError_t launch_selftest_wait(unsigned timeout_us, void *ws, cudaStream_t st);
 // Records `e` as the last CUDA error of the library; returns CBA_ERR_CUDA.
 int report_cuda_error(cudaError_t e);
-bool tc_supported(const Plan &p);
-void tc_plan(Plan &p);  // fills the tc_* fields
 bool tc2_supported(const Plan &p);
-size_t tc2_dzt_bytes(const Plan &p);
+size_t tc2_dzc_bytes(const Plan &p);
 size_t tc2_wr_bytes(const Plan &p);
-// dz pass: dzt ([N][K][Pe][Qp]) unless with_dzt is false, and the channels-last
-// zero-bordered dzc right after it when with_dzc.
-cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float *output,
-                                  const float *z, const void *ws, float *dzt, bool with_dzc,
-                                  cudaStream_t st, int *launches, bool with_dzt = true);
+// dz pass: dz written channels-last with its zero border (dzc_geom's layout).
+cudaError_t launch_dzc(const Plan &p, const float *delta, const float *output, const float *z,
+                       const void *ws, float *dzc, cudaStream_t st, int *launches);
 
 // The geometry the TMA kernels see and the channels-last dz copy's layout:
 // dzc [N][Pp][Qpp][Kp], data at row offset bd_lo and column offset bq_lo (zero
-// border elsewhere), stored dzt_bytes after the start of the dzt region.
+// border elsewhere).
 struct DzcGeom {
     int He, We, Pe, Qe, Kp, Pp, Qpp, bd_lo, bq_lo;
-    size_t dzt_bytes;
 };
 DzcGeom dzc_geom(const Plan &p);
 // Dense row-major fp32 tensor map (dims[0] innermost) with the given box;
@@ -159,8 +164,10 @@ size_t wgrad_nb_acc_bytes(const Plan &p);
 size_t wgrad_nb_xn_bytes(const Plan &p);
 size_t wgrad_nb_dzn_bytes(const Plan &p);
 cudaError_t launch_xn(const Plan &p, const float *x, float *xn, cudaStream_t st, int *launches);
+// rep: NULL, or the input gradient's weight repack, done by extra blocks of
+// the accumulator-apply launch (cba_repack.cuh).
 cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, float *dW, void *ws,
-                            float *acc, cudaStream_t st, int *launches);
+                            float *acc, const RepackJob *rep, cudaStream_t st, int *launches);
 // One pass over delta / output / z writing dz batch-innermost (dzn) and, when
 // dzc is not NULL, channels-last with its zero border (the layout of
 // dzc_geom, read by the input gradient).
@@ -168,14 +175,13 @@ cudaError_t launch_dz_layouts(const Plan &p, const float *delta, const float *ou
                               const float *z, const void *ws, float *dzn, float *dzc,
                               cudaStream_t st, int *launches);
 // Weight gradient with TMA-fed input rows (cba_wgrad4.cu).
-bool wgrad_tc4_supported(const Plan &p, const float *x);
+bool wgrad_tc4_supported(const Plan &p);
 size_t wgrad_tc4_ws_bytes(const Plan &p);  // tile accumulators (0 if the shape is not covered)
 cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, float *dW,
-                             void *ws, cudaStream_t st, int *launches);
-cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, float *dW,
-                             void *ws, cudaStream_t st, int *launches);
-// wr must already hold the repacked weights (launch_reduce writes them).
-cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzt, const float *residual, float *prev,
+                             void *ws, const RepackJob *rep, cudaStream_t st, int *launches);
+// wr must already hold the repacked weights (the weight gradient's launch
+// writes them).
+cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzc, const float *residual, float *prev,
                              void *ws, const float *wr, cudaStream_t st, int *launches);
 
 // Launches `kern` with programmatic stream serialisation: it may be scheduled

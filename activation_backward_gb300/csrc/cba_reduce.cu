@@ -9,10 +9,7 @@
 // division and square root are slow on this part, and the coefficients are
 // fp32 anyway).  Deterministic.  The per-channel arrival counters must be
 // zero when the kernel starts.
-//
-// Blocks past the reduction's own may carry an independent job: the input
-// gradient's weight repack (W[k][c][r][s] -> wr[r][s][c][k], TF32-rounded,
-// k padded to Kw with zeros), which would otherwise be a launch of its own.
+
 #include "cba_internal.cuh"
 #include "cba_ptx.cuh"
 
@@ -40,29 +37,35 @@ __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v) {
     return old;
 }
 
+// The per-channel inputs and running outputs of the finalisation, read by
+// thread 0 of every block when it starts (their loads overlap the block's
+// streaming, so the block that finalises the channel only waits for the other
+// blocks' partials).
+struct ChanIn {
+    float db, dgamma, gamma, mean, var;
+};
+
 // Per-channel finalisation from the S1, S2 totals: db += S1, dgamma += S2 and
 // the coefficients of dz = a*delta' + b + c*(z - mu).  bn: 0 no BN, 1 batch
 // statistics, 2 frozen statistics (mean and var are constants of the forward:
 // the gradient is gamma * delta' / sigma, b = c = 0; caffe's use_global_stats
 // branch of BatchNormLayer::Backward_cpu, "BatchNorm 理解").
 __device__ __forceinline__ void finalize_channel(int k, double S1, double S2, long long m,
-                                                 const float *__restrict__ gamma,
-                                                 const float *__restrict__ mean,
-                                                 const float *__restrict__ var, float eps, int bn,
+                                                 const ChanIn &in, float eps, int bn,
                                                  float *__restrict__ db,
                                                  float *__restrict__ dgamma,
                                                  Coef *__restrict__ coef) {
-    db[k] = (float)((double)db[k] + S1);
+    db[k] = (float)((double)in.db + S1);
     Coef cf;
     if (bn) {
-        dgamma[k] = (float)((double)dgamma[k] + S2);
-        const float sd = sqrtf(var[k] + eps);
-        const float a = gamma[k] / sd;
+        dgamma[k] = (float)((double)in.dgamma + S2);
+        const float sd = sqrtf(in.var + eps);
+        const float a = in.gamma / sd;
         const float s1m = (float)(S1 / (double)m), s2m = (float)(S2 / (double)m);
         cf.a = a;
         cf.b = bn == 2 ? 0.f : -a * s1m;
         cf.c = bn == 2 ? 0.f : -a * s2m / sd;
-        cf.mu = mean[k];
+        cf.mu = in.mean;
     } else {
         cf.a = 1.f;
         cf.b = 0.f;
@@ -70,44 +73,6 @@ __device__ __forceinline__ void finalize_channel(int k, double S1, double S2, lo
         cf.mu = 0.f;
     }
     coef[k] = cf;
-}
-
-struct RepackJob {
-    const float *W;
-    float *wr;
-    int K, C, R, S, Kw;
-};
-
-__device__ __forceinline__ float round_tf32(float v) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
-    return __uint_as_float(r);
-}
-
-// W [K][C*R*S] -> wr [R][S][C][Kw] in 32 x 32 tiles (output channels k x
-// flattened (c, r, s)) through shared memory: reads coalesced along (c, r, s),
-// writes along k.  Repack block `rb` of `nrep` takes tiles rb, rb + nrep, ...
-__device__ void repack_part(const RepackJob &j, int rb, int nrep) {
-    __shared__ float tile[32][33];
-    const int CRS = j.C * j.R * j.S, RS = j.R * j.S;
-    const int tk = (j.Kw + 31) / 32, tc = (CRS + 31) / 32;
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows of 32
-    for (int t = rb; t < tk * tc; t += nrep) {
-        const int k0 = (t / tc) * 32, q0 = (t % tc) * 32;
-        for (int r = ty; r < 32; r += kRedThreads / 32) {
-            const int k = k0 + r, q = q0 + tx;
-            tile[r][tx] = (k < j.K && q < CRS) ? round_tf32(j.W[(long long)k * CRS + q]) : 0.f;
-        }
-        __syncthreads();
-        for (int r = ty; r < 32; r += kRedThreads / 32) {
-            const int q = q0 + r, k = k0 + tx;
-            if (q < CRS && k < j.Kw) {
-                const int c = q / RS, rs = q - c * RS;  // rs = r * S + s
-                j.wr[((long long)rs * j.C + c) * j.Kw + k] = tile[tx][r];
-            }
-        }
-        __syncthreads();
-    }
 }
 
 // Block b < K * groups * pieces: channel k = b % K, then piece, then group
@@ -122,19 +87,24 @@ __global__ void __launch_bounds__(kRedThreads)
                      int N, int K, int PQ, long long m, int pln, int groups, int pieces,
                      float2 *__restrict__ part, unsigned *__restrict__ cnt,
                      float *__restrict__ db, float *__restrict__ dgamma,
-                     Coef *__restrict__ coef, RepackJob job, int nrep, int bn_mode) {
+                     Coef *__restrict__ coef, int bn_mode) {
     ptx::griddep_wait();
-    const int nred = K * groups * pieces;
-    if ((int)blockIdx.x >= nred) {
-        repack_part(job, (int)blockIdx.x - nred, nrep);
-        return;
-    }
     const int k = (int)(blockIdx.x % K);
     const int gq = (int)(blockIdx.x / K);
     const int q = gq % pieces, grp = gq / pieces;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float mu = BN ? mean[k] : 0.f;
     const float rs = BN ? rsqrtf(var[k] + eps) : 0.f;
+    ChanIn cin{};
+    if (tid == 0) {
+        cin.db = db[k];
+        if constexpr (BN) {
+            cin.dgamma = dgamma[k];
+            cin.gamma = gamma[k];
+            cin.mean = mu;
+            cin.var = var[k];
+        }
+    }
     constexpr int W = VEC ? 4 : 1;            // elements per access
     const int pa = PQ / W;                    // accesses per plane
     const int L = (pa + pieces - 1) / pieces;
@@ -168,8 +138,6 @@ __global__ void __launch_bounds__(kRedThreads)
                 if constexpr (ACT == CBA_ACT_LEAKY) yy[u] = __ldg(Y + off[u]);
                 if constexpr (BN) zz[u] = __ldg(Z + off[u]);
             }
-            // every load of the round is issued before the first use
-            asm volatile("" ::: "memory");
 #pragma unroll
             for (int u = 0; u < kRedU; ++u) {
                 if (!in[u]) dd[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -234,7 +202,7 @@ __global__ void __launch_bounds__(kRedThreads)
     }
     if (lane == 0) {
         cnt[k] = 0u;  // ready for the next call
-        finalize_channel(k, S1, S2, m, gamma, mean, var, eps, BN ? bn_mode : 0, db, dgamma, coef);
+        finalize_channel(k, S1, S2, m, cin, eps, BN ? bn_mode : 0, db, dgamma, coef);
     }
 }
 
@@ -255,38 +223,30 @@ __global__ void dz_out_kernel(const float *delta, const float *__restrict__ outp
 template <int ACT, bool BN>
 void launch_reduce_t(const Plan &p, const float *delta, const float *output, const float *z,
                      const float *gamma, const float *mean, const float *var, float2 *part,
-                     unsigned *cnt, float *db, float *dgamma, Coef *coef, const RepackJob &job,
-                     int nrep, cudaStream_t st) {
-    const unsigned grid = (unsigned)((long long)p.K * p.red_groups * p.red_pieces + nrep);
+                     unsigned *cnt, float *db, float *dgamma, Coef *coef, cudaStream_t st) {
+    const unsigned grid = (unsigned)((long long)p.K * p.red_groups * p.red_pieces);
     if (p.PQ % 4 == 0)
         bn_reduce_kernel<ACT, BN, true><<<grid, kRedThreads, 0, st>>>(
             delta, output, z, gamma, mean, var, p.eps, p.N, p.K, p.PQ, p.m, p.red_pln,
-            p.red_groups, p.red_pieces, part, cnt, db, dgamma, coef, job, nrep, p.bn);
+            p.red_groups, p.red_pieces, part, cnt, db, dgamma, coef, p.bn);
     else
         bn_reduce_kernel<ACT, BN, false><<<grid, kRedThreads, 0, st>>>(
             delta, output, z, gamma, mean, var, p.eps, p.N, p.K, p.PQ, p.m, p.red_pln,
-            p.red_groups, p.red_pieces, part, cnt, db, dgamma, coef, job, nrep, p.bn);
+            p.red_groups, p.red_pieces, part, cnt, db, dgamma, coef, p.bn);
 }
 
 }  // namespace
 
 cudaError_t launch_reduce(const Plan &p, const float *delta, const float *output, const float *z,
                           const float *gamma, const float *mean, const float *var, float *db,
-                          float *dgamma, void *ws, cudaStream_t st, int *launches,
-                          const float *repack_W, float *repack_wr) {
+                          float *dgamma, void *ws, cudaStream_t st, int *launches) {
     float2 *part = ws_at<float2>(ws, p.off_red);
     unsigned *cnt = ws_at<unsigned>(ws, p.off_cnt);
     Coef *coef = ws_at<Coef>(ws, p.off_coef);
-    RepackJob job{repack_W, repack_wr, p.K, p.C, p.R, p.S, (p.K + 3) / 4 * 4};
-    int nrep = 0;
-    if (repack_W && repack_wr) {
-        const long long tiles = (long long)((job.Kw + 31) / 32) * ((p.C * p.R * p.S + 31) / 32);
-        nrep = (int)std::min<long long>(tiles, 256);
-    }
     const bool leaky = p.act == CBA_ACT_LEAKY;
 #define CBA_RED(A, B) \
     launch_reduce_t<A, B>(p, delta, output, z, gamma, mean, var, part, cnt, db, dgamma, coef, \
-                          job, nrep, st)
+                          st)
     if (p.bn) {
         if (leaky) CBA_RED(CBA_ACT_LEAKY, true);
         else CBA_RED(CBA_ACT_LINEAR, true);

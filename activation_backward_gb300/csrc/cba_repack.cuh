@@ -1,0 +1,59 @@
+// cba_repack.cuh -- the input gradient's weight repack, W[k][c - g*Cg][r][s]
+// -> wr[r][s][c][k] (TF32-rounded, k padded to Kw with zeros, zero where input
+// channel c is outside output channel k's group), as 32 x 32 tiles that
+// extra blocks of another launch transpose through shared memory.  It rides
+// in the weight gradient's accumulator-apply launch: that kernel is
+// latency-bound and leaves most of the GPU idle, so the tiles cost almost
+// nothing there (inside the memory-bound reduction pass they delayed its
+// streaming by several microseconds).
+#pragma once
+
+#include "cba_internal.cuh"
+
+namespace cba {
+
+inline RepackJob make_repack_job(const Plan &p, const float *W, float *wr) {
+    return RepackJob{W, wr, p.K, p.C, p.R, p.S, (p.K + 3) / 4 * 4, p.Cg, p.Kg};
+}
+
+inline long long repack_tiles(const RepackJob &j) {
+    return (long long)((j.Kw + 31) / 32) * ((j.C * j.R * j.S + 31) / 32);
+}
+
+// Tiles rb, rb + nrep, ... of the repack (32 output channels k x 32 flattened
+// (c, r, s)): reads coalesced along (c, r, s), writes along k.  Every thread
+// of the block (blockDim.x a multiple of 32, at most 1024) takes part.
+__device__ __forceinline__ void repack_part(const RepackJob &j, int rb, int nrep) {
+    __shared__ float tile[32][33];
+    const int CRS = j.C * j.R * j.S, RS = j.R * j.S;
+    const int tk = (j.Kw + 31) / 32, tc = (CRS + 31) / 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5, rows = blockDim.x >> 5;
+    for (int t = rb; t < tk * tc; t += nrep) {
+        const int k0 = (t / tc) * 32, q0 = (t % tc) * 32;
+        for (int r = ty; r < 32; r += rows) {
+            const int k = k0 + r, q = q0 + tx;
+            float v = 0.f;
+            if (k < j.K && q < CRS) {
+                const int c = q / RS;
+                const long long o = w_off(k, c, q - c * RS, j.Cg, j.Kg, RS);
+                if (o >= 0) {
+                    uint32_t u;
+                    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(j.W[o]));
+                    v = __uint_as_float(u);
+                }
+            }
+            tile[r][tx] = v;
+        }
+        __syncthreads();
+        for (int r = ty; r < 32; r += rows) {
+            const int q = q0 + r, k = k0 + tx;
+            if (q < CRS && k < j.Kw) {
+                const int c = q / RS, rs = q - c * RS;  // rs = r * S + s
+                j.wr[((long long)rs * j.C + c) * j.Kw + k] = tile[tx][r];
+            }
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace cba

@@ -16,6 +16,9 @@
 //   h = p*stride + r - pad, w = q*stride + s - pad -- the gather form of
 //   col2im(W^T . dz) (§3.1, §3.2).  64 pixels x 64 channels per block; the
 //   epilogue adds the shortcut residual and, if asked, the old prev_delta.
+// Grouped layers (the l.groups loop of §3.1) run both as the dense product
+// over all K x C channel pairs: dgrad reads zero for the weights between
+// groups, and the split-K reduction adds only the pairs within a group to dW.
 #include "cba_internal.cuh"
 
 namespace cba {
@@ -118,13 +121,20 @@ __global__ void __launch_bounds__(TTH)
     }
 }
 
-// dW[i] += sum_s part[s][i], summed in a fixed order in fp64.
+// dW[i] += sum_s part[s][j], summed in a fixed order in fp64, where the
+// partials are dense ([K][C*R*S], nel elements per split) and dW holds the
+// pairs of one group ([K][Cg*R*S], ng elements): i = (k, cg, rs) reads
+// j = (k, (k / Kg) * Cg + cg, rs).
 __global__ void splitk_reduce_kernel(const float *__restrict__ part, int splits, long long nel,
+                                     long long ng, int Cg, int Kg, int C, int RS,
                                      float *__restrict__ dW) {
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nel;
+    const long long CgRS = (long long)Cg * RS;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < ng;
          i += (long long)gridDim.x * blockDim.x) {
+        const int k = (int)(i / CgRS);
+        const long long j = (long long)k * C * RS + (long long)(k / Kg) * CgRS + (i - k * CgRS);
         double s = 0.0;
-        for (int t = 0; t < splits; ++t) s += (double)part[(size_t)t * nel + i];
+        for (int t = 0; t < splits; ++t) s += (double)part[(size_t)t * nel + j];
         dW[i] = (float)((double)dW[i] + s);
     }
 }
@@ -135,7 +145,7 @@ __global__ void __launch_bounds__(TTH)
                       const float *__restrict__ output, const float *__restrict__ z,
                       const Coef *__restrict__ coef, int N, int C, int H, int W, int K, int R,
                       int S, int stride, int pad, int P, int Q, const float *__restrict__ residual,
-                      float *__restrict__ prev, int accumulate) {
+                      float *__restrict__ prev, int accumulate, int Cg, int Kg) {
     __shared__ float As[TBK][TBM + 4];
     __shared__ float Bs[TBK][TBN + 4];
     const int HW = H * W, RS = R * S, KK = RS * K;
@@ -179,7 +189,10 @@ __global__ void __launch_bounds__(TTH)
                         }
                     }
                 }
-                if (bcol < C) vb = __ldg(Wt + (((long long)k * C + bcol) * R + r) * S + s);
+                if (bcol < C) {
+                    const long long o = w_off(k, bcol, rs, Cg, Kg, RS);
+                    if (o >= 0) vb = __ldg(Wt + o);
+                }
             }
             As[l][pp] = va;
             Bs[l][pp] = vb;
@@ -247,9 +260,10 @@ cudaError_t launch_wgrad_simt(const Plan &p, const float *x, const float *delta,
 
 cudaError_t launch_splitk_reduce(const Plan &p, const float *part, int splits, float *dW,
                                  cudaStream_t st, int *launches) {
-    const long long nel = (long long)p.K * p.CRS;
-    int blocks = (int)std::min<long long>((nel + 255) / 256, (long long)p.num_sms * 8);
-    splitk_reduce_kernel<<<blocks, 256, 0, st>>>(part, splits, nel, dW);
+    const long long nel = (long long)p.K * p.CRS, ng = (long long)p.K * p.Cg * p.RS;
+    int blocks = (int)std::min<long long>((ng + 255) / 256, (long long)p.num_sms * 8);
+    splitk_reduce_kernel<<<blocks, 256, 0, st>>>(part, splits, nel, ng, p.Cg, p.Kg, p.C, p.RS,
+                                                 dW);
     *launches += 1;
     return cudaGetLastError();
 }
@@ -264,7 +278,8 @@ cudaError_t launch_dgrad_simt(const Plan &p, const float *Wt, const float *delta
 #define CBA_DG(A, B)                                                                        \
     dgrad_simt_kernel<A, B><<<grid, TTH, 0, st>>>(Wt, delta, output, z, coef, p.N, p.C, p.H, \
                                                   p.W, p.K, p.R, p.S, p.stride, p.pad, p.P, \
-                                                  p.Q, residual, prev, p.accumulate)
+                                                  p.Q, residual, prev, p.accumulate, p.Cg, \
+                                                  p.Kg)
     if (p.bn) {
         if (leaky) CBA_DG(CBA_ACT_LEAKY, true);
         else CBA_DG(CBA_ACT_LINEAR, true);

@@ -1,36 +1,37 @@
-// cba_tc2.cu -- tensor-core convolution gradients, TMEM-operand design.
+// cba_tc2.cu -- the input gradient on the tensor cores, and the dz pass that
+// feeds it.
 //
-// Both GEMMs put their A operand in tensor memory, written by 4 warps with
-// tcgen05.st, and stream their B operand through shared memory with TMA
-// (128-byte swizzle, K-major).  Writing A from registers makes any shift of
-// the convolution taps free (no 16-byte alignment rule, no shared-memory
-// traffic), and the tensor core then reads only B from shared memory.
+// dz pass (`dzc_kernel`): the BN-input gradient dz (activation derivative and
+// normalize_delta of "YOLOv3反向传播原理 之 全流程源码分析" §4, applied to delta
+// with the per-channel coefficients of the reduction pass), TF32-rounded and
+// written channels-last, dzc[n][pp][qq][k] on a grid of Pp x Qpp positions: the
+// data sits at row offset bd_lo and column offset bq_lo and a zero border
+// surrounds it, wide enough for every row and column shift below.  1x1
+// stride-1 unpadded layers view each P x Q plane as one row of length P*Q.
 //
-// The BN-input gradient dz (activation derivative and normalize_delta of
-// "YOLOv3反向传播原理 之 全流程源码分析" §4 applied to delta) is written once,
-// TF32-rounded, by a memory-bound pass (`dz_materialize_kernel`) in
-// [N][K][P][Qp] order (rows padded to Qp = Q rounded up to 4, so the rows are
-// 16-byte strided for TMA); both GEMMs read it from there.  1x1 stride-1
-// unpadded layers view each P x Q plane as one row of length P*Q.
-//
-// wgrad (dW[k][c][r][s] += sum_{n,p,q} dz[n][k][p][q] x[n][c][p*st+r-pad][q*st+s-pad],
-//        the gemm(0,1,...) of §3.1):
-//   TMEM lanes = (input channel c, kernel column s) pairs, columns = 32 output
-//   columns q of one output row; the lane (c, s) holds x[n][c][h][q*st + s - pad]
-//   for the input row h.  B = dz row p (128 output channels x 32 q) by TMA;
-//   each input row h meets the output rows p = (h + pad - r)/st, one
-//   accumulator D_r (128 x 128) per kernel row r.  dz rows live in a ring of
-//   shared-memory slots and are loaded once per block.  The epilogue adds the
-//   block's partial sums into dW in L2 with bulk async reductions.
-// dgrad (prev[n][c][h][w] = sum_{r,s,k} W[k][c][r][s] dz[n][k][(h+pad-r)/st][(w+pad-s)/st],
-//        col2im(W^T . dz) of §3.1 / §3.2 as a gather):
-//   pixels of one stride phase class (h mod st, w mod st) on a grid of rows i
-//   and columns jj; TMEM lanes = 128 consecutive grid positions, columns = 32
-//   output channels k; the lane holds dz[n][k][i + dp_r][jj + min_dq] for
-//   kernel row r.  B = W[k][c][r][s] for all kernel columns s of the class at
-//   once (N = (s, c) pairs), so the MMA computes E[(i, q)][(s, c)] and the
-//   epilogue finishes the column shift: prev(i, j) = sum_s E(i, j + dq_s)[s, c],
-//   adds the shortcut residual (§5) and, if asked, the old prev_delta.
+// Input gradient (prev[n][c][h][w] = sum_{r,s,k} W[k][c][r][s] dz[n][k][p][q]
+// with h = p*st + r - pad, w = q*st + s - pad: col2im(W^T . dz) of §3.1 / §3.2
+// written as a gather).  Output pixels are split into stride phase classes
+// (h mod st, w mod st); within a class the kernel rows r and columns s that
+// reach it give row shifts dp_r and column shifts dq_s on dz's grid.  One GEMM
+// per class:
+//   A (M = 128 grid positions x 32 channels k per step) is a TMA box of dzc,
+//     started dp_r rows further on for kernel row r: every tap shift is a
+//     tensor-map coordinate, no thread touches an operand;
+//   B (N = the class's kernel columns s times a tile of input channels c) is
+//     a box of the repacked weights wr[r][s][c][k] (written by extra blocks of
+//     the reduction pass);
+//   D[position][(s, c)] accumulates over r and k in TMEM.  The epilogue
+//     finishes the column shifts, prev(i, j) = sum_s D(i, j + dq_s)[s, c]
+//     (a warp hands the lanes at its edge to its neighbour through shared
+//     memory), and adds the shortcut delta (§5) and, when accumulating, the
+//     old prev_delta -- or, for layers with either, adds its result at the L2
+//     onto prev, which `prev_init_kernel` has first set to residual (+ prev).
+// `dgrad_tc4_kernel` is persistent, one block per SM, with two TMEM
+// accumulators so that a tile's epilogue overlaps the next tile's MMAs;
+// `dgrad_tc3_kernel` (one tile pair per block) takes the classes whose column
+// span or kernel-column count is past what the persistent kernel's halo and
+// TMEM budget hold.
 //
 // All waits are bounded (2 s); see cba_ptx.cuh.
 #include <cuda.h>
@@ -51,85 +52,8 @@ __device__ __forceinline__ float to_tf32(float v) {
     return __uint_as_float(r);
 }
 
-__host__ __device__ __forceinline__ int fdiv(int a, int b) {  // floor(a / b), b > 0
-    return a >= 0 ? a / b : -((-a + b - 1) / b);
-}
-__host__ __device__ __forceinline__ int cdiv(int a, int b) { return -fdiv(-a, b); }
 
-// ------------------------------------------------------ dz materialisation
-
-template <int ACT, bool BN>
-__global__ void dz_materialize_kernel(const float *__restrict__ delta,
-                                      const float *__restrict__ output,
-                                      const float *__restrict__ z, const Coef *__restrict__ coef,
-                                      int K, int Pe, int Qe, int Qp, long long rows,
-                                      float *__restrict__ dzt) {
-    const int qv = Qp >> 2;
-    const long long total = rows * qv;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const long long row = i / qv;
-        const int q0 = (int)(i - row * qv) * 4;
-        const int k = (int)((row / Pe) % K);
-        const Coef cf = coef[k];
-        const long long src = row * Qe;
-        float v[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int q = q0 + e;
-            v[e] = 0.f;
-            if (q < Qe) {
-                const float y = (ACT == CBA_ACT_LEAKY) ? __ldg(output + src + q) : 0.f;
-                const float zz = BN ? __ldg(z + src + q) : 0.f;
-                v[e] = to_tf32(dz_of<ACT, BN>(__ldg(delta + src + q), y, zz, cf));
-            }
-        }
-        reinterpret_cast<float4 *>(dzt)[i] = make_float4(v[0], v[1], v[2], v[3]);
-    }
-}
-
-// dz in both layouts the GEMMs read, from one pass over delta/output/z:
-//   dzt [N][K][Pe][Qp]        rows padded to Qp (zeros), for the weight gradient
-//   dzc [N][Pp][Qpp][Kp]      channels-last with a zero border of bd_lo/bq_lo
-//                             rows/columns before the data, for the input gradient
-// A block transposes a 32 (columns) x 32 (channels) tile through shared memory.
-template <int ACT, bool BN>
-__global__ void __launch_bounds__(256)
-    dz_both_kernel(const float *__restrict__ delta, const float *__restrict__ output,
-                   const float *__restrict__ z, const Coef *__restrict__ coef, int K, int Pe,
-                   int Qe, int Qp, int Kp, int Pp, int Qpp, int bd_lo, int bq_lo, int qlo,
-                   float *__restrict__ dzt, float *__restrict__ dzc) {
-    __shared__ float tile[32][33];
-    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-    const int n = blockIdx.z / Pp, pp = blockIdx.z - (blockIdx.z / Pp) * Pp, p = pp - bd_lo;
-    const bool prow = p >= 0 && p < Pe;
-    const int q0 = qlo + (int)blockIdx.x * 32, k0 = blockIdx.y * 32;
-    {
-        const int q = q0 + tx;
-        for (int kk = ty; kk < 32; kk += 8) {
-            const int k = k0 + kk;
-            float v = 0.f;
-            if (prow && k < K && q >= 0 && q < Qe) {
-                const long long off = (((long long)n * K + k) * Pe + p) * Qe + q;
-                const float y = (ACT == CBA_ACT_LEAKY) ? __ldg(output + off) : 0.f;
-                const float zz = BN ? __ldg(z + off) : 0.f;
-                v = to_tf32(dz_of<ACT, BN>(__ldg(delta + off), y, zz, coef[k]));
-            }
-            tile[kk][tx] = v;
-            if (dzt != nullptr && prow && k < K && q >= 0 && q < Qp)
-                dzt[(((long long)n * K + k) * Pe + p) * Qp + q] = v;
-        }
-    }
-    __syncthreads();
-    {
-        const int k = k0 + tx;
-        for (int qq = ty; qq < 32; qq += 8) {
-            const int pq = q0 + qq + bq_lo;
-            if (pq >= 0 && pq < Qpp && k < Kp)
-                dzc[(((long long)n * Pp + pp) * Qpp + pq) * Kp + k] = tile[tx][qq];
-        }
-    }
-}
+// ------------------------------------------------------------ dz pass
 
 // dz in the channels-last layout only: dzc [N][Pp][Qpp][Kp] with a zero border
 // of bd_lo / bq_lo rows / columns before the data (zeros after it too, and in
@@ -224,475 +148,6 @@ __global__ void __launch_bounds__(256)
                     make_float4(tile[ql][4 * k4], tile[ql][4 * k4 + 1], tile[ql][4 * k4 + 2],
                                 tile[ql][4 * k4 + 3]);
         }
-    }
-}
-
-// ------------------------------------------------------------------ wgrad
-
-constexpr int kW2RingMax = 6;  // dz row tiles resident (at most)
-constexpr int kW2NA = 4;       // A stages in TMEM (32 columns each)
-constexpr int kAStg = 3;       // cp.async staging depth of the A producers
-constexpr int kW2Threads = 320;  // 8 producer warps, TMA warp, MMA warp
-
-struct Wg2Args {
-    const float *x;
-    float *dW;
-    unsigned *status;
-    int C, He, We, K, R, S, RS, CRS, stride, pad, Pe, Qe;
-    int ct;              // input channels per block (lanes = ct * S <= 128)
-    int nk;              // output channels per block = MMA N (multiple of 32)
-    int nqc;             // 32-wide output-column chunks per row
-    int rows_per_split;  // input rows per block
-    int splits_per_seg;
-    int ring;            // dz ring slots (>= R)
-    int bulk;            // 1: bulk L2 reductions are aligned, 0: per-element atomics
-    uint32_t ncols;      // TMEM columns allocated
-};
-
-struct W2Bars {
-    uint64_t dz_full[kW2RingMax], dz_empty[kW2RingMax], a_full[kW2NA], a_empty[kW2NA], accum;
-    uint32_t tmem_base;
-    int abort_flag;
-};
-
-// Epilogue of the weight gradient (producer warps 0-7; group grp takes the
-// 32-wide output-channel chunks kc = grp, grp + 2, ...): accumulator D_r lane
-// (c, s), column k -> dW[k][c][r][s], added in L2 by bulk reductions of
-// whole dW row segments (or per-element atomics when those are misaligned).
-__device__ __forceinline__ void wgrad_epilogue(const Wg2Args &a, uint32_t tmem, uint32_t lane_addr,
-                                               uint8_t *ring, int grp, int L, int cl, int s,
-                                               bool lv, int ct_here, int k0, int c0, int h0,
-                                               int h1, int p_lo, int p_hi) {
-    const int st = a.stride, R = a.R;
-    const int pitch = ct_here * a.RS;  // floats per staged dW row segment
-    float *stg = reinterpret_cast<float *>(ring) + grp * 32 * pitch;
-    for (int kc = grp; kc * 32 < a.nk && k0 + kc * 32 < a.K; kc += 2) {
-        const int krows = min(32, a.K - (k0 + kc * 32));
-        for (int r = 0; r < R; ++r) {
-            // was accumulator r written by any input row of this block?
-            bool wr = false;
-            for (int h = h0; h < h1 && !wr; ++h) {
-                const int num = h - r + a.pad;
-                wr = num >= 0 && num % st == 0 && num / st >= p_lo && num / st <= p_hi;
-            }
-            float v[32];
-            if (wr) {
-                ptx::tmem_ld32(tmem + lane_addr + (uint32_t)(r * a.nk + kc * 32), v);
-                ptx::tmem_ld_wait();
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.f;
-            }
-            if (lv) {
-                if (a.bulk) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        stg[j * pitch + cl * a.RS + r * a.S + s] = v[j];
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j < krows)
-                            atomicAdd(a.dW + ((long long)(k0 + kc * 32 + j) * a.C + c0 +
-                                              cl) * a.RS + r * a.S + s,
-                                      v[j]);
-                }
-            }
-        }
-        if (a.bulk) {
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(1 + grp, 128);
-            if (L < krows) {
-                ptx::bulk_reduce_add_f32(
-                    a.dW + (long long)(k0 + kc * 32 + L) * a.CRS + (long long)c0 * a.RS,
-                    ptx::smem_u32(stg + L * pitch), (uint32_t)pitch * 4u);
-                ptx::bulk_commit();
-                ptx::bulk_wait_read_all();
-            }
-            ptx::named_bar_sync(1 + grp, 128);
-        }
-    }
-    if (a.bulk && L < 32) ptx::bulk_wait_all();
-}
-
-// MMA role of the weight gradient (one thread): for each input row h, wait
-// for its TMEM A stage, then for every kernel row r whose output row
-// p = (h + pad - r)/st is in range, issue the K steps into accumulator r
-// against dz row p; release A stages and dz rows as soon as their last use is
-// issued.  Output rows are consumed in increasing order, so each dz row is
-// waited for once, when it is first needed.  The issue loop carries no
-// memory traffic: each MMA's B descriptor is the ring's base descriptor plus
-// the slot and K-step offsets.
-__device__ __forceinline__ void wgrad_mma_role(const Wg2Args &a, W2Bars &sb, uint8_t *ring,
-                                               uint32_t tmem, uint32_t a_col0, uint32_t idesc,
-                                               uint32_t tile_bytes, int nsteps, int h0, int h1,
-                                               int p_lo, int p_hi) {
-    const int st = a.stride, R = a.R;
-    const uint64_t bd0 = ptx::smem_desc(ptx::smem_u32(ring), 16, 1024, 2);
-    const uint32_t slot_step = tile_bytes >> 4;  // descriptor units per ring slot
-    uint32_t written = 0;
-    int p_rel = p_lo;    // next dz row to release
-    int p_ready = p_lo - 1;  // dz rows up to here have landed
-    int t = 0;
-    bool ok = true;
-    for (int h = h0; ok && h < h1; ++h, ++t) {
-        const int sa = t % kW2NA;
-        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_full[sa]),
-                                    (uint32_t)(t / kW2NA) & 1u, &sb.abort_flag, a.status,
-                                    kLimitNs);
-        if (!ok) break;
-        // the highest output row this input row meets
-        const int p_top = min(p_hi, fdiv(h + a.pad, st));
-        while (ok && p_ready < p_top) {
-            ++p_ready;
-            const int seq = p_ready - p_lo;
-            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[seq % a.ring]),
-                                        (uint32_t)(seq / a.ring) & 1u, &sb.abort_flag,
-                                        a.status, kLimitNs);
-        }
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const uint32_t a_tm = tmem + a_col0 + (uint32_t)(sa * 32);
-        for (int r = 0; r < R; ++r) {
-            const int num = h - r + a.pad;
-            if (num < 0 || num % st) continue;
-            const int p = num / st;
-            if (p < p_lo || p > p_hi) continue;
-            const uint64_t bd = bd0 + (uint64_t)((uint32_t)((p - p_lo) % a.ring) * slot_step);
-            const uint32_t d_tm = tmem + (uint32_t)(r * a.nk);
-            const uint32_t acc0 = (written >> r) & 1u;
-            written |= 1u << r;
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                if (ks < nsteps)
-                    ptx::mma_tf32_ts(d_tm, a_tm + ks * 8, bd + 2 * ks, idesc, ks ? 1u : acc0);
-        }
-        ptx::mma_commit(ptx::smem_u32(&sb.a_empty[sa]));
-        while (p_rel <= p_hi && min(h1 - 1, p_rel * st - a.pad + R - 1) <= h) {
-            ptx::mma_commit(ptx::smem_u32(&sb.dz_empty[(p_rel - p_lo) % a.ring]));
-            ++p_rel;
-        }
-    }
-    ptx::mma_commit(ptx::smem_u32(&sb.accum));
-    int no_abort = 0;
-    ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &no_abort, a.status, kLimitNs);
-}
-
-__global__ void __launch_bounds__(kW2Threads, 1)
-    wgrad_tc2_kernel(const __grid_constant__ CUtensorMap tm, const Wg2Args a) {
-    extern __shared__ uint8_t smem_dyn[];
-    uint8_t *ring = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    __shared__ W2Bars sb;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int k0 = blockIdx.x * a.nk;
-    const int c0 = blockIdx.y * a.ct;
-    const int ct_here = min(a.ct, a.C - c0);
-    const int seg = blockIdx.z / a.splits_per_seg, split = blockIdx.z % a.splits_per_seg;
-    const int n = seg / a.nqc, qc = seg % a.nqc;
-    const int h0 = split * a.rows_per_split, h1 = min(a.He, h0 + a.rows_per_split);
-    const int q_base = qc * 32;
-    const int nsteps = (min(32, a.Qe - q_base) + 7) / 8;
-    const uint32_t tile_bytes = (uint32_t)a.nk * 128u;
-    const int st = a.stride, R = a.R;
-    const int p_lo = max(0, cdiv(h0 - R + 1 + a.pad, st));
-    const int p_hi = min(a.Pe - 1, fdiv(h1 - 1 + a.pad, st));
-    const uint32_t a_col0 = (uint32_t)(R * a.nk);
-    const uint32_t idesc = ptx::idesc_tf32(128, a.nk);
-
-    if (tid == 0) {
-        for (int i = 0; i < kW2RingMax; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&sb.dz_full[i]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sb.dz_empty[i]), 1);
-        }
-        for (int i = 0; i < kW2NA; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&sb.a_full[i]), 128);
-            ptx::mbar_init(ptx::smem_u32(&sb.a_empty[i]), 1);
-        }
-        ptx::mbar_init(ptx::smem_u32(&sb.accum), 1);
-        sb.abort_flag = 0;
-        ptx::fence_mbar_init();
-    }
-    if (warp == 9) {
-        ptx::tmem_alloc(ptx::smem_u32(&sb.tmem_base), a.ncols);
-        ptx::tmem_relinquish();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    const uint32_t tmem = sb.tmem_base;
-    const bool has_work = h0 < h1 && p_lo <= p_hi;
-
-    if (warp < 8) {
-        // ---- A producers: two groups of 4 warps take alternate input rows.
-        // TMEM lane (c, s) holds x[n][c0+c][h][q*st + s - pad] for 32 q.  Each
-        // thread copies its 32 values for the rows kAStg ahead into a private
-        // shared-memory slot with cp.async (zero-filled outside the image),
-        // then moves the current row from the slot into TMEM.
-        const int grp = warp >> 2, wq = warp & 3;
-        const int L = wq * 32 + lane;
-        const int cl = L / a.S, s = L - (L / a.S) * a.S;
-        const bool lv = cl < ct_here;
-        const float *xb = a.x + ((long long)n * a.C + c0 + (lv ? cl : 0)) * a.He * a.We;
-        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
-        const int nrows = has_work ? h1 - h0 : 0;
-        float *ast = reinterpret_cast<float *>(ring + (size_t)a.ring * tile_bytes) +
-                     grp * (kAStg * 32 * 128) + L;
-        auto issue = [&](int t) {  // row h0 + t of this group into slot (t >> 1) % kAStg
-            if (t < nrows) {
-                const float *xr = xb + (long long)(h0 + t) * a.We;
-                const uint32_t dst = ptx::smem_u32(ast + ((t >> 1) % kAStg) * (32 * 128));
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int q = q_base + j;
-                    const int w = q * st + s - a.pad;
-                    const bool ok = lv && q < a.Qe && w >= 0 && w < a.We;
-                    ptx::cp_async_4(dst + j * 128 * 4, ok ? xr + w : a.x, ok ? 4u : 0u);
-                }
-            }
-            ptx::cp_async_commit();
-        };
-#pragma unroll
-        for (int d = 0; d < kAStg; ++d) issue(grp + 2 * d);
-        bool ok = true;
-        for (int t = grp; t < nrows; t += 2) {
-            ptx::cp_async_wait<kAStg - 1>();
-            const float *src = ast + ((t >> 1) % kAStg) * (32 * 128);
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = to_tf32(src[j * 128]);
-            issue(t + 2 * kAStg);
-            const int sa = t % kW2NA;
-            if (t >= kW2NA)
-                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_empty[sa]),
-                                            (uint32_t)(t / kW2NA - 1) & 1u, &sb.abort_flag,
-                                            a.status, kLimitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            ptx::tmem_st32(tmem + lane_addr + a_col0 + (uint32_t)(sa * 32), v);
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[sa]));
-        }
-        ptx::cp_async_wait<0>();
-        // ---- epilogue: D_r[(c, s)][k] -> dW[k][c][r][s]; group g takes the
-        // 32-wide output-channel chunks kc = g, g + 2, ...
-        if (has_work && ok)
-            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
-                                        kLimitNs);
-        ok = __all_sync(0xffffffffu, ok) && has_work;
-        if (ok) {
-            ptx::tc_fence_after();
-            wgrad_epilogue(a, tmem, lane_addr, ring, grp, L, cl, s, lv, ct_here, k0, c0, h0, h1,
-                           p_lo, p_hi);
-        }
-    } else if (warp == 8) {
-        // ---- TMA producer: dz rows p_lo..p_hi into the ring
-        if (lane == 0 && has_work) {
-            int issued = 0;
-            for (int p = p_lo; p <= p_hi; ++p, ++issued) {
-                const int seq = p - p_lo, slot = seq % a.ring;
-                if (seq >= a.ring &&
-                    !ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_empty[slot]),
-                                            (uint32_t)(seq / a.ring - 1) & 1u, &sb.abort_flag,
-                                            a.status, kLimitNs))
-                    break;
-                ptx::mbar_arrive_expect_tx(ptx::smem_u32(&sb.dz_full[slot]), tile_bytes);
-                ptx::tma_load_4d(ptx::smem_u32(ring + (size_t)slot * tile_bytes), &tm, q_base, p,
-                                 k0, n, ptx::smem_u32(&sb.dz_full[slot]));
-            }
-            // no copy may be in flight when the block exits
-            int no_abort = 0;
-            for (int seq = max(0, issued - a.ring); seq < issued; ++seq)
-                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[seq % a.ring]),
-                                       (uint32_t)(seq / a.ring) & 1u, &no_abort, a.status,
-                                       kLimitNs);
-        }
-    } else {
-        if (lane == 0 && has_work)
-            wgrad_mma_role(a, sb, ring, tmem, a_col0, idesc, tile_bytes, nsteps, h0, h1, p_lo,
-                           p_hi);
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (warp == 9) {
-        __syncwarp();
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, a.ncols);
-    }
-}
-
-// wgrad with the input rows staged by TMA: the TMA warp streams x rows
-// (all ct input channels, the columns one 32-wide output chunk needs) into
-// a ring next to the dz rows; the producer warps only shift-read the staged
-// row into TMEM.  Used when x rows are 16-byte strided (W*4 % 16 == 0).
-constexpr int kW3XRing = 6;
-
-struct Wg3Extra {
-    int wbox;         // staged columns per input row
-    uint32_t xbytes;  // bytes one TMA box writes (ct * wbox * 4)
-    uint32_t xstride; // bytes between ring slots (xbytes rounded up to 128)
-};
-
-__global__ void __launch_bounds__(kW2Threads, 1)
-    wgrad_tc3_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tmx,
-                     const Wg2Args a, const Wg3Extra xe) {
-    extern __shared__ uint8_t smem_dyn[];
-    uint8_t *ring = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
-    __shared__ W2Bars sb;
-    __shared__ uint64_t x_full[kW3XRing], x_empty[kW3XRing];
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int k0 = blockIdx.x * a.nk;
-    const int c0 = blockIdx.y * a.ct;
-    const int ct_here = min(a.ct, a.C - c0);
-    const int seg = blockIdx.z / a.splits_per_seg, split = blockIdx.z % a.splits_per_seg;
-    const int n = seg / a.nqc, qc = seg % a.nqc;
-    const int h0 = split * a.rows_per_split, h1 = min(a.He, h0 + a.rows_per_split);
-    const int q_base = qc * 32;
-    const int nsteps = (min(32, a.Qe - q_base) + 7) / 8;
-    const uint32_t tile_bytes = (uint32_t)a.nk * 128u;
-    const int st = a.stride, R = a.R;
-    const int p_lo = max(0, cdiv(h0 - R + 1 + a.pad, st));
-    const int p_hi = min(a.Pe - 1, fdiv(h1 - 1 + a.pad, st));
-    const uint32_t a_col0 = (uint32_t)(R * a.nk);
-    const uint32_t idesc = ptx::idesc_tf32(128, a.nk);
-    const int wstart = q_base * st - a.pad;
-    const int w0 = wstart >= 0 ? (wstart & ~3) : -((-wstart + 3) & ~3);  // floor to 4
-    uint8_t *xring = ring + (size_t)a.ring * tile_bytes;
-
-    if (tid == 0) {
-        for (int i = 0; i < kW2RingMax; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&sb.dz_full[i]), 1);
-            ptx::mbar_init(ptx::smem_u32(&sb.dz_empty[i]), 1);
-        }
-        for (int i = 0; i < kW2NA; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&sb.a_full[i]), 128);
-            ptx::mbar_init(ptx::smem_u32(&sb.a_empty[i]), 1);
-        }
-        for (int i = 0; i < kW3XRing; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&x_full[i]), 1);
-            ptx::mbar_init(ptx::smem_u32(&x_empty[i]), 128);
-        }
-        ptx::mbar_init(ptx::smem_u32(&sb.accum), 1);
-        sb.abort_flag = 0;
-        ptx::fence_mbar_init();
-    }
-    if (warp == 9) {
-        ptx::tmem_alloc(ptx::smem_u32(&sb.tmem_base), a.ncols);
-        ptx::tmem_relinquish();
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    const uint32_t tmem = sb.tmem_base;
-    const bool has_work = h0 < h1 && p_lo <= p_hi;
-    const int nrows = has_work ? h1 - h0 : 0;
-
-    if (warp < 8) {
-        // ---- A producers: two groups of 4 warps take alternate input rows;
-        // TMEM lane (c, s) <- staged x[c][q*st + s - pad] for the 32 q
-        const int grp = warp >> 2, wq = warp & 3;
-        const int L = wq * 32 + lane;
-        const int cl = L / a.S, s = L - (L / a.S) * a.S;
-        const bool lv = cl < ct_here;
-        const int off0 = wstart + s - w0;  // column of q_base in the staged row
-        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
-        bool ok = true;
-        for (int t = grp; t < nrows; t += 2) {
-            const int xs = t % kW3XRing;
-            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&x_full[xs]), (uint32_t)(t / kW3XRing) & 1u,
-                                        &sb.abort_flag, a.status, kLimitNs);
-            const float *xr =
-                reinterpret_cast<const float *>(xring + (size_t)xs * xe.xstride) +
-                (lv ? cl : 0) * xe.wbox + off0;
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = lv ? to_tf32(xr[j * st]) : 0.f;
-            ptx::mbar_arrive(ptx::smem_u32(&x_empty[xs]));
-            const int sa = t % kW2NA;
-            if (ok && t >= kW2NA)
-                ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.a_empty[sa]),
-                                            (uint32_t)(t / kW2NA - 1) & 1u, &sb.abort_flag,
-                                            a.status, kLimitNs);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            ptx::tmem_st32(tmem + lane_addr + a_col0 + (uint32_t)(sa * 32), v);
-            ptx::tmem_st_wait();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(ptx::smem_u32(&sb.a_full[sa]));
-        }
-        // ---- epilogue: D_r[(c, s)][k] -> dW[k][c][r][s]; group g takes the
-        // 32-wide output-channel chunks kc = g, g + 2, ...
-        if (has_work && ok)
-            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
-                                        kLimitNs);
-        ok = __all_sync(0xffffffffu, ok) && has_work;
-        if (ok) {
-            ptx::tc_fence_after();
-            wgrad_epilogue(a, tmem, lane_addr, ring, grp, L, cl, s, lv, ct_here, k0, c0, h0, h1,
-                           p_lo, p_hi);
-        }
-    } else if (warp == 8) {
-        // ---- TMA producer: x rows and dz rows merged in the order of the
-        // first input row that needs them, as far ahead as the rings allow.
-        // A slot is only ever released by work on rows whose operands were
-        // issued earlier in this order, so blocking on a slot cannot deadlock.
-        if (lane == 0 && has_work) {
-            int issued = 0, next_p = p_lo, xissued = 0;
-            bool ok = true;
-            while (ok && (xissued < nrows || next_p <= p_hi)) {
-                const int dz_need = next_p <= p_hi ? max(0, next_p * st - a.pad - h0) : (1 << 30);
-                if (next_p <= p_hi && dz_need <= xissued) {
-                    const int seq = next_p - p_lo, slot = seq % a.ring;
-                    if (seq >= a.ring)
-                        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_empty[slot]),
-                                                    (uint32_t)(seq / a.ring - 1) & 1u,
-                                                    &sb.abort_flag, a.status, kLimitNs);
-                    if (!ok) break;
-                    ptx::mbar_arrive_expect_tx(ptx::smem_u32(&sb.dz_full[slot]), tile_bytes);
-                    ptx::tma_load_4d(ptx::smem_u32(ring + (size_t)slot * tile_bytes), &tm, q_base,
-                                     next_p, k0, n, ptx::smem_u32(&sb.dz_full[slot]));
-                    ++next_p;
-                    ++issued;
-                } else {
-                    const int t = xissued, xs = t % kW3XRing;
-                    if (t >= kW3XRing)
-                        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&x_empty[xs]),
-                                                    (uint32_t)(t / kW3XRing - 1) & 1u,
-                                                    &sb.abort_flag, a.status, kLimitNs);
-                    if (!ok) break;
-                    ptx::mbar_arrive_expect_tx(ptx::smem_u32(&x_full[xs]), xe.xbytes);
-                    ptx::tma_load_4d(ptx::smem_u32(xring + (size_t)xs * xe.xstride), &tmx, w0,
-                                     h0 + t, c0, n, ptx::smem_u32(&x_full[xs]));
-                    ++xissued;
-                }
-            }
-            // no copy may be in flight when the block exits
-            int no_abort = 0;
-            for (int seq = max(0, issued - a.ring); seq < issued; ++seq)
-                ptx::mbar_wait_bounded(ptx::smem_u32(&sb.dz_full[seq % a.ring]),
-                                       (uint32_t)(seq / a.ring) & 1u, &no_abort, a.status,
-                                       kLimitNs);
-            for (int t = max(0, xissued - kW3XRing); t < xissued; ++t)
-                ptx::mbar_wait_bounded(ptx::smem_u32(&x_full[t % kW3XRing]),
-                                       (uint32_t)(t / kW3XRing) & 1u, &no_abort, a.status,
-                                       kLimitNs);
-        }
-    } else {
-        if (lane == 0 && has_work)
-            wgrad_mma_role(a, sb, ring, tmem, a_col0, idesc, tile_bytes, nsteps, h0, h1, p_lo,
-                           p_hi);
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    if (warp == 9) {
-        __syncwarp();
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, a.ncols);
     }
 }
 
@@ -1531,10 +986,22 @@ bool encode_4d(CUtensorMap *m, const void *base, const uint64_t (&d)[4], const u
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-inline uint32_t pow2_cols(int need) {
-    uint32_t c = 32;
-    while ((int)c < need) c <<= 1;
-    return c;
+// One thread waits on a barrier phase that nothing completes: the bounded wait
+// must give up after timeout_us and set the status bit.
+__global__ void selftest_wait_kernel(unsigned timeout_us, unsigned *status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        ptx::mbar_init(ptx::smem_u32(&bar), 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        ptx::mbar_wait_bounded(ptx::smem_u32(&bar), 0, &abort_flag, status,
+                               (uint64_t)timeout_us * 1000ull);
+    }
+    __syncthreads();
 }
 
 }  // namespace
@@ -1607,16 +1074,11 @@ static V2Geom v2_geom(const Plan &p) {
     return g;
 }
 
-static size_t dzt_bytes_only(const Plan &p, const V2Geom &g) {
-    return ((sizeof(float) * (size_t)p.N * p.K * g.Pe * g.Qp) + 255) / 256 * 256;
-}
-
 DzcGeom dzc_geom(const Plan &p) {
     const V2Geom g = v2_geom(p);
     DzcGeom d;
     d.He = g.He; d.We = g.We; d.Pe = g.Pe; d.Qe = g.Qe;
     d.Kp = g.Kp; d.Pp = g.Pp; d.Qpp = g.Qpp; d.bd_lo = g.bd_lo; d.bq_lo = g.bq_lo;
-    d.dzt_bytes = dzt_bytes_only(p, g);
     return d;
 }
 
@@ -1654,7 +1116,6 @@ bool tma_encode_f32(void *tmap, const void *base, int rank, const uint64_t *dims
 bool tc2_supported(const Plan &p) {
     if (p.stride > 4 || p.R > kD2MaxTaps || p.S > kD2MaxTaps) return false;
     const V2Geom g = v2_geom(p);
-    if ((long long)p.N * p.K * g.Pe * g.Qp >= (1LL << 31)) return false;
     if ((long long)p.N * g.Pp * g.Qpp * g.Kp >= (1LL << 31)) return false;
     if ((long long)p.N * g.Pp > 65535) return false;  // grid.z of the dz pass
     // the input gradient's column shifts must leave room in a 128-row tile
@@ -1662,181 +1123,52 @@ bool tc2_supported(const Plan &p) {
     return encode_fn() != nullptr;
 }
 
-size_t tc2_dzt_bytes(const Plan &p) {
+size_t tc2_dzc_bytes(const Plan &p) {
     const V2Geom g = v2_geom(p);
-    return dzt_bytes_only(p, g) + sizeof(float) * (size_t)p.N * g.Pp * g.Qpp * g.Kp;
+    return sizeof(float) * (size_t)p.N * g.Pp * g.Qpp * g.Kp;
 }
 
 size_t tc2_wr_bytes(const Plan &p) {
     return sizeof(float) * (size_t)p.R * p.S * p.C * ((p.K + 3) / 4 * 4);
 }
 
-cudaError_t launch_dz_materialize(const Plan &p, const float *delta, const float *output,
-                                  const float *z, const void *ws, float *dzt, bool with_dzc,
-                                  cudaStream_t st, int *launches, bool with_dzt) {
+cudaError_t launch_dzc(const Plan &p, const float *delta, const float *output, const float *z,
+                       const void *ws, float *dzc, cudaStream_t st, int *launches) {
     const V2Geom g = v2_geom(p);
     const Coef *coef = ws_at<Coef>(ws, p.off_coef);
     const bool leaky = p.act == CBA_ACT_LEAKY;
-    if (with_dzc && !with_dzt) {
-        float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) + dzt_bytes_only(p, g));
-        const int nqc = (g.Qe + 31) / 32;
-        dim3 grid((unsigned)nqc, (unsigned)(p.N * g.Pp), (unsigned)((g.Kp + 63) / 64));
-        cudaError_t pe = cudaSuccess;
+    const int nqc = (g.Qe + 31) / 32;
+    dim3 grid((unsigned)nqc, (unsigned)(p.N * g.Pp), (unsigned)((g.Kp + 63) / 64));
+    cudaError_t e = cudaSuccess;
 #define CBA_DZC(A, B)                                                                          \
     do {                                                                                       \
         if (g.Qe % 4 == 0)                                                                     \
-            pe = launch_pdl(dzc_kernel<A, B, true>, grid, dim3(256), 0, st, delta, output, z,  \
-                            coef, p.K, g.Pe, g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, nqc,  \
-                            dzc);                                                              \
+            e = launch_pdl(dzc_kernel<A, B, true>, grid, dim3(256), 0, st, delta, output, z,   \
+                           coef, p.K, g.Pe, g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, nqc,   \
+                           dzc);                                                               \
         else                                                                                   \
-            pe = launch_pdl(dzc_kernel<A, B, false>, grid, dim3(256), 0, st, delta, output, z, \
-                            coef, p.K, g.Pe, g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, nqc,  \
-                            dzc);                                                              \
+            e = launch_pdl(dzc_kernel<A, B, false>, grid, dim3(256), 0, st, delta, output, z,  \
+                           coef, p.K, g.Pe, g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, nqc,   \
+                           dzc);                                                               \
     } while (0)
-        if (p.bn) {
-            if (leaky) CBA_DZC(CBA_ACT_LEAKY, true);
-            else CBA_DZC(CBA_ACT_LINEAR, true);
-        } else {
-            if (leaky) CBA_DZC(CBA_ACT_LEAKY, false);
-            else CBA_DZC(CBA_ACT_LINEAR, false);
-        }
-#undef CBA_DZC
-        if (pe != cudaSuccess) return pe;
-    } else if (with_dzc) {
-        float *dzc = reinterpret_cast<float *>(reinterpret_cast<char *>(dzt) + dzt_bytes_only(p, g));
-        const int qlo = -g.bq_lo;
-        const int qhi = with_dzt ? std::max(g.Qpp - g.bq_lo, g.Qp) : g.Qpp - g.bq_lo;
-        dim3 grid((unsigned)((qhi - qlo + 31) / 32), (unsigned)((g.Kp + 31) / 32),
-                  (unsigned)(p.N * g.Pp));
-#define CBA_DZB(A, B)                                                                          \
-    dz_both_kernel<A, B><<<grid, 256, 0, st>>>(delta, output, z, coef, p.K, g.Pe, g.Qe, g.Qp,   \
-                                               g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, qlo,      \
-                                               with_dzt ? dzt : nullptr, dzc)
-        if (p.bn) {
-            if (leaky) CBA_DZB(CBA_ACT_LEAKY, true);
-            else CBA_DZB(CBA_ACT_LINEAR, true);
-        } else {
-            if (leaky) CBA_DZB(CBA_ACT_LEAKY, false);
-            else CBA_DZB(CBA_ACT_LINEAR, false);
-        }
-#undef CBA_DZB
+    if (p.bn) {
+        if (leaky) CBA_DZC(CBA_ACT_LEAKY, true);
+        else CBA_DZC(CBA_ACT_LINEAR, true);
     } else {
-        const long long rows = (long long)p.N * p.K * g.Pe;
-        const long long total = rows * (g.Qp / 4);
-        const int blocks = (int)std::min<long long>((total + 255) / 256, (long long)p.num_sms * 16);
-#define CBA_DZM(A, B)                                                                            \
-    dz_materialize_kernel<A, B><<<blocks, 256, 0, st>>>(delta, output, z, coef, p.K, g.Pe, g.Qe, \
-                                                        g.Qp, rows, dzt)
-        if (p.bn) {
-            if (leaky) CBA_DZM(CBA_ACT_LEAKY, true);
-            else CBA_DZM(CBA_ACT_LINEAR, true);
-        } else {
-            if (leaky) CBA_DZM(CBA_ACT_LEAKY, false);
-            else CBA_DZM(CBA_ACT_LINEAR, false);
-        }
-#undef CBA_DZM
+        if (leaky) CBA_DZC(CBA_ACT_LEAKY, false);
+        else CBA_DZC(CBA_ACT_LINEAR, false);
     }
-    *launches += 1;
-    return cudaGetLastError();
-}
-
-cudaError_t launch_wgrad_tc2(const Plan &p, const float *x, const float *dzt, float *dW,
-                             void *ws, cudaStream_t st, int *launches) {
-    const V2Geom g = v2_geom(p);
-    Wg2Args a;
-    a.x = x;
-    a.dW = dW;
-    a.status = ws_at<unsigned>(ws, p.off_status);
-    a.C = p.C; a.He = g.He; a.We = g.We; a.K = p.K; a.R = p.R; a.S = p.S;
-    a.RS = p.RS; a.CRS = p.CRS; a.stride = p.stride; a.pad = p.pad; a.Pe = g.Pe; a.Qe = g.Qe;
-    // lanes = (c, s) pairs; channels per block a multiple of 4 (aligned dW segments)
-    int ct = 128 / p.S;
-    if (ct >= 4) ct &= ~3;
-    ct = std::max(1, std::min(ct, p.C));
-    const int mtiles = (p.C + ct - 1) / ct;
-    a.ct = (p.C + mtiles - 1) / mtiles;
-    if (a.ct >= 4 && a.ct * p.S <= 128) a.ct = std::min((a.ct + 3) / 4 * 4, 128 / p.S);
-    // output channels per block: R accumulators of nk columns + 4 A stages of 32 <= 512
-    int nk_cap = ((512 - kW2NA * 32) / p.R) / 32 * 32;
-    nk_cap = std::max(32, std::min(256, nk_cap));
-    const int ktiles = (p.K + nk_cap - 1) / nk_cap;
-    a.nk = std::min(nk_cap, ((p.K + ktiles - 1) / ktiles + 31) / 32 * 32);
-    a.ncols = pow2_cols(p.R * a.nk + kW2NA * 32);
-    if (a.ncols > 512) return cudaErrorNotSupported;
-    a.nqc = (g.Qe + 31) / 32;
-    const long long segs = (long long)p.N * a.nqc;
-    const long long units = (long long)((p.C + a.ct - 1) / a.ct) * ((p.K + a.nk - 1) / a.nk) * segs;
-    int sps = (int)std::max(1LL, std::min<long long>(g.He, (long long)p.num_sms / units));
-    a.rows_per_split = (g.He + sps - 1) / sps;
-    a.splits_per_seg = (g.He + a.rows_per_split - 1) / a.rows_per_split;
-    const int ct_last = p.C - ((p.C + a.ct - 1) / a.ct - 1) * a.ct;
-    a.bulk = (p.CRS % 4 == 0) && ((a.ct * p.RS) % 4 == 0) && ((ct_last * p.RS) % 4 == 0);
-    CUtensorMap tm;
-    const uint64_t d[4] = {(uint64_t)g.Qp, (uint64_t)g.Pe, (uint64_t)p.K, (uint64_t)p.N};
-    const uint32_t b[4] = {32, 1, (uint32_t)a.nk, 1};
-    if (!encode_4d(&tm, dzt, d, b)) return cudaErrorInvalidValue;
-    dim3 grid((p.K + a.nk - 1) / a.nk, (p.C + a.ct - 1) / a.ct, (unsigned)(segs * a.splits_per_seg));
-
-    // x rows staged by TMA when they are 16-byte strided
-    const int span = 31 * p.stride + p.S;  // input columns one 32-wide output chunk reads
-    Wg3Extra xe;
-    xe.wbox = (span + 3 + 3) / 4 * 4;       // + up to 3 columns of alignment slack
-    xe.xbytes = (uint32_t)((size_t)a.ct * xe.wbox * 4);
-    xe.xstride = (xe.xbytes + 127u) / 128u * 128u;
-    const bool x_tma = (g.We % 4 == 0) && xe.wbox <= 256 &&
-                       (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
-    if (x_tma) {
-        const size_t xring = (size_t)kW3XRing * xe.xstride;
-        a.ring = (int)std::min<size_t>(kW2RingMax, (220 * 1024 - xring) / ((size_t)a.nk * 128));
-        if (a.ring < p.R) return cudaErrorNotSupported;
-        if ((long long)2 * 32 * a.ct * p.RS * 4 > (long long)a.ring * a.nk * 128) a.bulk = 0;
-        CUtensorMap tmx;
-        {
-            EncodeTiledFn fn = encode_fn();
-            cuuint64_t dims[4] = {(cuuint64_t)g.We, (cuuint64_t)g.He, (cuuint64_t)p.C,
-                                  (cuuint64_t)p.N};
-            cuuint64_t strides[3] = {(cuuint64_t)g.We * 4, (cuuint64_t)g.We * g.He * 4,
-                                     (cuuint64_t)g.We * g.He * p.C * 4};
-            cuuint32_t box[4] = {(cuuint32_t)xe.wbox, 1, (cuuint32_t)a.ct, 1};
-            cuuint32_t es[4] = {1, 1, 1, 1};
-            if (fn(&tmx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(x), dims,
-                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-                return cudaErrorInvalidValue;
-        }
-        const size_t smem = (size_t)a.ring * a.nk * 128 + xring + 1024;
-        cudaError_t e = cudaFuncSetAttribute(wgrad_tc3_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
-        if (e != cudaSuccess) return e;
-        wgrad_tc3_kernel<<<grid, kW2Threads, smem, st>>>(tm, tmx, a, xe);
-        *launches += 1;
-        return cudaGetLastError();
-    }
-
-    // otherwise each producer thread gathers its own values with cp.async
-    const size_t astg = (size_t)2 * kAStg * 32 * 128 * 4;
-    a.ring = (int)std::min<size_t>(kW2RingMax, (220 * 1024 - astg) / ((size_t)a.nk * 128));
-    if (a.ring < p.R) return cudaErrorNotSupported;
-    // each producer group stages 32 rows of its dW segment in the ring
-    if ((long long)2 * 32 * a.ct * p.RS * 4 > (long long)a.ring * a.nk * 128) a.bulk = 0;
-    const size_t smem = (size_t)a.ring * a.nk * 128 + astg + 1024;
-    cudaError_t e = cudaFuncSetAttribute(wgrad_tc2_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+#undef CBA_DZC
     if (e != cudaSuccess) return e;
-    wgrad_tc2_kernel<<<grid, kW2Threads, smem, st>>>(tm, a);
     *launches += 1;
     return cudaGetLastError();
 }
 
-cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzt, const float *residual, float *prev,
+cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzc, const float *residual, float *prev,
                              void *ws, const float *wr_c, cudaStream_t st, int *launches) {
     const V2Geom g = v2_geom(p);
     const int Kw = (p.K + 3) / 4 * 4;
     float *wr = const_cast<float *>(wr_c);  // tensor maps take a non-const base; only read
-    const float *dzc =
-        reinterpret_cast<const float *>(reinterpret_cast<const char *>(dzt) + dzt_bytes_only(p, g));
     const long long total_pos = (long long)p.N * g.Pp * g.Qpp;
     CUtensorMap tma;
     {
@@ -1982,6 +1314,11 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzt, const float *resid
         *launches += 1;
     }
     return cudaSuccess;
+}
+
+cudaError_t launch_selftest_wait(unsigned timeout_us, void *ws, cudaStream_t st) {
+    selftest_wait_kernel<<<1, 32, 0, st>>>(timeout_us, ws_at<unsigned>(ws, 0));
+    return cudaGetLastError();
 }
 
 }  // namespace cba

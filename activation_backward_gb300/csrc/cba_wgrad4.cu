@@ -34,6 +34,7 @@
 
 #include "cba_internal.cuh"
 #include "cba_ptx.cuh"
+#include "cba_repack.cuh"
 
 namespace cba {
 
@@ -389,13 +390,22 @@ __global__ void __launch_bounds__(kW4Threads, 1)
 
 // dW[k][c][r][s] += acc[tile][r * cb + c_local][k_local]: the tile accumulators
 // (tile = (k tile * nctile + c tile) * S + s) added into dW, one element per
-// thread, coalesced over k on the read.
+// thread, coalesced over k on the read.  Grouped: only the (k, c) pairs of one
+// group, into dW[k][c - g * Cg][r][s].  The first nrep blocks transpose the
+// input gradient's weight repack instead (see cba_repack.cuh), beside the
+// apply blocks.
 __global__ void __launch_bounds__(256)
     wgrad_acc_apply_kernel(const float *__restrict__ acc, int N, int cb, int S, int nctile,
-                           int K, int C, int R, long long total, float *__restrict__ dW) {
+                           int K, int C, int R, int Cg, int Kg, long long total,
+                           float *__restrict__ dW, int napply, RepackJob rep, int nrep) {
     ptx::griddep_wait();  // the accumulators come from the weight-gradient kernel
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+    if ((int)blockIdx.x < nrep) {
+        repack_part(rep, (int)blockIdx.x, nrep);
+        return;
+    }
+    const int ab = (int)blockIdx.x - nrep;  // apply block
+    const long long stride = (long long)napply * blockDim.x;
+    for (long long i = ab * (long long)blockDim.x + threadIdx.x; i < total;
          i += stride) {
         const int kl = (int)(i & 127);
         const long long tc = i >> 7;
@@ -404,7 +414,10 @@ __global__ void __launch_bounds__(256)
         const int s = tile % S, kc = tile / S;
         const int r = col / cb, c = (kc % nctile) * cb + col % cb;
         const int k = (kc / nctile) * 128 + kl;
-        if (c < C && k < K) dW[(((size_t)k * C + c) * R + r) * S + s] += acc[i];
+        if (c < C && k < K) {
+            const long long o = w_off(k, c, r * S + s, Cg, Kg, R * S);
+            if (o >= 0) dW[o] += acc[i];
+        }
     }
 }
 
@@ -467,13 +480,10 @@ size_t wgrad_tc4_ws_bytes(const Plan &p) {
     return w.ok ? w.acc_bytes : 0;
 }
 
-bool wgrad_tc4_supported(const Plan &p, const float *x) {
-    if (!w4_geom(p).ok) return false;
-    return (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
-}
+bool wgrad_tc4_supported(const Plan &p) { return w4_geom(p).ok; }
 
 cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, float *dW,
-                             void *ws, cudaStream_t st, int *launches) {
+                             void *ws, const RepackJob *rep, cudaStream_t st, int *launches) {
     const W4Geom w = w4_geom(p);
     if (!w.ok) return cudaErrorNotSupported;
     const DzcGeom g = dzc_geom(p);
@@ -515,8 +525,11 @@ cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, fl
     if (e != cudaSuccess) return e;
     const long long total = (long long)w.ntiles * w.N * 128;
     const unsigned ablocks = (unsigned)std::min<long long>((total + 255) / 256, p.num_sms * 4LL);
-    e = launch_pdl(wgrad_acc_apply_kernel, dim3(ablocks), dim3(256), 0, st,
-                   (const float *)a.acc, w.N, w.cb, p.S, w.nctile, p.K, p.C, p.R, total, dW);
+    const RepackJob job = rep ? *rep : RepackJob{};
+    const int nrep = rep ? (int)std::min<long long>(repack_tiles(*rep), 4LL * p.num_sms) : 0;
+    e = launch_pdl(wgrad_acc_apply_kernel, dim3(ablocks + nrep), dim3(256), 0, st,
+                   (const float *)a.acc, w.N, w.cb, p.S, w.nctile, p.K, p.C, p.R, p.Cg, p.Kg,
+                   total, dW, (int)ablocks, job, nrep);
     if (e != cudaSuccess) return e;
     *launches += 2;
     return cudaGetLastError();

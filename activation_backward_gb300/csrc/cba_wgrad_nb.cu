@@ -38,6 +38,7 @@
 
 #include "cba_internal.cuh"
 #include "cba_ptx.cuh"
+#include "cba_repack.cuh"
 
 namespace cba {
 
@@ -546,22 +547,32 @@ __global__ void __launch_bounds__(kWnThreads, 1)
     }
 }
 
-// dW[k][c][r][s] += acc[unit][t][s * cb + cl][kl] with unit = (kt * ctiles +
-// ct) * R + r, k = (kt * KT + t) * 128 + kl, c = ct * cb + cl: one thread per
-// dW element in dW order (coalesced read-modify-write of dW; the scattered
-// reads of the accumulators hit the L2).
+// dW[k][cg][r][s] += acc[unit][t][s * cb + cl][kl] with unit = (kt * ctiles +
+// ct) * R + r, k = (kt * KT + t) * 128 + kl, c = ct * cb + cl, where c = (k /
+// Kg) * Cg + cg is the input channel of group-local index cg (dense: Cg = C):
+// one thread per dW element in dW order (coalesced read-modify-write of dW;
+// the scattered reads of the accumulators hit the L2).
+// The first nrep blocks transpose the input gradient's weight repack instead
+// (rep; see cba_repack.cuh): first, so that they run beside the apply blocks
+// rather than after them.
 __global__ void __launch_bounds__(256)
     wgrad_nb_apply_kernel(const float *__restrict__ acc, int KT, int cols, int cb, int S, int R,
-                          int ctiles, int C, long long total, float *__restrict__ dW) {
+                          int ctiles, int Cg, int Kg, long long total, float *__restrict__ dW,
+                          int napply, RepackJob rep, int nrep) {
     ptx::griddep_wait();  // the accumulators come from the weight-gradient kernel
-    const long long stride = (long long)gridDim.x * blockDim.x;
+    if ((int)blockIdx.x < nrep) {
+        repack_part(rep, (int)blockIdx.x, nrep);
+        return;
+    }
+    const int ab = (int)blockIdx.x - nrep;  // apply block
+    const long long stride = (long long)napply * blockDim.x;
     const int RS = R * S;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+    for (long long i = ab * (long long)blockDim.x + threadIdx.x; i < total;
          i += stride) {
         const long long kc = i / RS;
         const int rs = (int)(i - kc * RS);
         const int r = rs / S, s = rs - r * S;
-        const int k = (int)(kc / C), c = (int)(kc - (long long)k * C);
+        const int k = (int)(kc / Cg), c = (int)(kc - (long long)k * Cg) + (k / Kg) * Cg;
         const int kt = k / (128 * KT), t = (k >> 7) - kt * KT, kl = k & 127;
         const int ct = c / cb, cl = c - ct * cb;
         const long long unit = ((long long)kt * ctiles + ct) * R + r;
@@ -747,7 +758,7 @@ cudaError_t launch_xn(const Plan &p, const float *x, float *xn, cudaStream_t st,
 }
 
 cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, float *dW, void *ws,
-                            float *acc, cudaStream_t st, int *launches) {
+                            float *acc, const RepackJob *rep, cudaStream_t st, int *launches) {
     const WnGeom w = wn_geom(p);
     if (!w.ok) return cudaErrorNotSupported;
     WnArgs a;
@@ -782,10 +793,13 @@ cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, fl
     if (e != cudaSuccess) return e;
     e = launch_pdl(kern, dim3(w.grid), dim3(kWnThreads), w.smem, st, tma, tmb, a);
     if (e != cudaSuccess) return e;
-    const long long total = (long long)p.K * p.C * p.R * p.S;
+    const long long total = (long long)p.K * p.Cg * p.R * p.S;
     const unsigned ablocks = (unsigned)std::min<long long>((total + 255) / 256, p.num_sms * 8LL);
-    e = launch_pdl(wgrad_nb_apply_kernel, dim3(ablocks), dim3(256), 0, st, (const float *)acc,
-                   w.KT, w.cols, w.cb, p.S, p.R, w.ctiles, p.C, total, dW);
+    const RepackJob job = rep ? *rep : RepackJob{};
+    const int nrep = rep ? (int)std::min<long long>(repack_tiles(*rep), 4LL * p.num_sms) : 0;
+    e = launch_pdl(wgrad_nb_apply_kernel, dim3(ablocks + nrep), dim3(256), 0, st,
+                   (const float *)acc, w.KT, w.cols, w.cb, p.S, p.R, w.ctiles, p.Cg, p.Kg, total,
+                   dW, (int)ablocks, job, nrep);
     if (e != cudaSuccess) return e;
     *launches += 2;
     return cudaGetLastError();

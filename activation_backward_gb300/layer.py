@@ -80,16 +80,13 @@ class DeviceLayer:
                                           self.workspace, stream=stream, check=check)
 
     def run_traced(self, events=None, stream=None):
-        """Enqueue with 4 phase events (see cba_conv_bn_act_backward_traced);
-        returns the number of kernels enqueued.  Grouped layers take no phase
-        events (cba_conv_bn_act_backward_grouped_traced)."""
+        """Enqueue with 5 phase events (see cba_conv_bn_act_backward_traced);
+        returns the number of kernels enqueued."""
         if self.groups > 1:
-            if events is not None:
-                raise ValueError("grouped calls record no phase events")
             _, n = B.cba_conv_bn_act_backward_grouped_traced(
                 self.desc, self.groups, self.x, self.output, self.z, self.delta, self.W,
                 self.gamma, self.mean, self.var, self.residual, self.dW, self.db, self.dgamma,
-                self.prev, self.dz, self.workspace, stream=stream)
+                self.prev, self.dz, self.workspace, stream=stream, events=events)
             return n
         _, n = B.cba_conv_bn_act_backward_traced(
             self.desc, self.x, self.output, self.z, self.delta, self.W, self.gamma, self.mean,

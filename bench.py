@@ -35,6 +35,13 @@ TF32_PER_BF16 = 1.1 / 2.25
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# the phases a traced call's events bound: reduction pass, GEMM operand
+# layout pass, weight gradient, input gradient
+PHASES = ("reduce", "layout", "wgrad", "dgrad")
+SPIN_CYCLES = 2_000_000  # about 1 ms at the SM clock
+PATH_NAMES = {0: "ffma", 1: "tc_rows", 2: "tc_batch_inner"}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -288,12 +295,13 @@ def profiled_traffic(phase, workload, layer):
     return None
 
 
-def workload_layers(args, cid=None):
-    """The layer calls of workload `cid` (default: --config); with --bn frozen,
-    every BN layer gets frozen statistics (inputs.with_frozen_stats)."""
+def workload_layers(args, cid=None, groups=None):
+    """The layer calls of workload `cid` (default: --config) as a convolution
+    of `groups` groups (default: --groups); with --bn frozen, every BN layer
+    gets frozen statistics (inputs.with_frozen_stats)."""
     from activation_backward_gb300 import ACT_NAMES, inputs
     cid = args.config if cid is None else cid
-    groups = getattr(args, "groups", 1)
+    groups = getattr(args, "groups", 1) if groups is None else groups
     batch = getattr(args, "batch", None)
     layers = (inputs.make_config(cid, batch=batch) if groups == 1
               else [inputs.make_grouped_config(cid, groups, batch=batch)])
@@ -323,7 +331,9 @@ def config_dict(args, layers, ws):
             "gemm_gflop_per_step": flops / 1e9,
             "l2": "flushed before every step, outside the timing: 512 MiB write, then a 256 MiB "
                   "read sweep so no dirty flush lines are written back inside the step",
-            "launch": "the step's library calls captured into one CUDA graph, replayed",
+            "launch": "the step's library calls captured into one CUDA graph, replayed; a ~1 ms "
+                      "GPU spin precedes each timed step so that it is enqueued before the GPU "
+                      "reaches it (the events time the GPU, not the host's launch)",
             "parallelism": "replicas only" if ws > 1 else "single GPU"}
 
 
@@ -372,7 +382,7 @@ def tf32_peak(peaks, peak_src, measured_tf32):
 
 
 def time_workload(cid, args, dev, math, steps, warmup, stream, flush, phases=True,
-                  clocks=None, ws=1):
+                  clocks=None, ws=1, groups=None):
     """Time one workload: its library call(s) captured into a CUDA graph and
     replayed `steps` times, L2 flushed before each (outside the events); then
     (if `phases`) traced direct calls with events between the phases of every
@@ -383,7 +393,7 @@ def time_workload(cid, args, dev, math, steps, warmup, stream, flush, phases=Tru
     import activation_backward_gb300 as cba
     from activation_backward_gb300.layer import DeviceLayer, capture_graph
 
-    layers = workload_layers(args, cid)
+    layers = workload_layers(args, cid, groups)
     dls = [DeviceLayer(l, math=math, device=dev, z_free=args.z_free) for l in layers]
 
     def step(events_per_layer=None):
@@ -420,6 +430,7 @@ def time_workload(cid, args, dev, math, steps, warmup, stream, flush, phases=Tru
     torch.cuda.synchronize()
     for i in range(steps):
         flush()
+        torch.cuda._sleep(SPIN_CYCLES)  # the replay is enqueued before the GPU reaches it
         starts[i].record(stream)
         graph.replay()
         ends[i].record(stream)
@@ -430,16 +441,23 @@ def time_workload(cid, args, dev, math, steps, warmup, stream, flush, phases=Tru
     for dl in dls:
         assert dl.status() == cba.CBA_OK, "device status after the timed region"
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    # what each call runs, and the bytes of its GEMM operand layout pass
+    plans = [cba.cba_plan_info(dl.desc, dl.groups, dl.prev is not None) for dl in dls]
     out = dict(layers=layers, dls=dls, step_ms=step_ms, clocks=clk,
-               launches_per_step=launches_per_step, phases=None, direct_ms=None)
-    grouped = any(l.get("groups", 1) > 1 for l in layers)
-    if phases and not grouped:
+               launches_per_step=launches_per_step, phases=None, direct_ms=None,
+               paths=[PATH_NAMES[p[0]] for p in plans],
+               layout_bytes=[p[1] + p[2] for p in plans])
+    if phases:
         nph = min(steps, 50)
-        ev = [[[mk() for _ in range(4)] for _ in dls] for _ in range(nph)]
+        ev = [[[mk() for _ in range(cba.CBA_PHASE_EVENTS)] for _ in dls] for _ in range(nph)]
         d_starts = [mk() for _ in range(nph)]
         d_ends = [mk() for _ in range(nph)]
         for i in range(nph):
             flush()
+            # a ~1 ms spin first, so that the host has enqueued the whole step
+            # before the GPU reaches it: the phase events then time the
+            # kernels, not the host's launch calls
+            torch.cuda._sleep(SPIN_CYCLES)
             d_starts[i].record(stream)
             step(ev[i])
             d_ends[i].record(stream)
@@ -447,14 +465,35 @@ def time_workload(cid, args, dev, math, steps, warmup, stream, flush, phases=Tru
         out["direct_ms"] = sum(s.elapsed_time(e) for s, e in zip(d_starts, d_ends)) / nph
         per_layer = []
         for li in range(len(dls)):
-            ph = {"reduce": 0.0, "wgrad": 0.0, "dgrad": 0.0}
+            ph = {k: 0.0 for k in PHASES}
             for i in range(nph):
                 e = ev[i][li]
-                ph["reduce"] += e[0].elapsed_time(e[1])
-                ph["wgrad"] += e[1].elapsed_time(e[2])
-                ph["dgrad"] += e[2].elapsed_time(e[3])
+                for j, k in enumerate(PHASES):
+                    ph[k] += e[j].elapsed_time(e[j + 1])
             per_layer.append({k: v / nph for k, v in ph.items()})
         out["phases"] = per_layer
+        # a plain read of the reduction's bytes, one launch per layer (torch's
+        # sum over one buffer of that size, same L2 flush): what a single
+        # streaming-read kernel of this size achieves on this part
+        from activation_backward_gb300 import inputs
+        floor = []
+        for l in layers:
+            buf = torch.empty(inputs.layer_bytes_reduce(l) // 4, dtype=torch.float32, device=dev)
+            buf.fill_(1.0)
+            tot = 0.0
+            for i in range(nph + 3):
+                flush()
+                torch.cuda._sleep(SPIN_CYCLES)
+                a, b = mk(), mk()
+                a.record(stream)
+                buf.sum()
+                b.record(stream)
+                torch.cuda.synchronize()
+                if i >= 3:
+                    tot += a.elapsed_time(b)
+            floor.append(tot / nph)
+            del buf
+        out["read_floor_ms"] = floor
     return out
 
 
@@ -470,25 +509,39 @@ def summarize(t, tf32, hbm):
     if t["phases"] is None:
         return d
     red_bytes = sum(inputs.layer_bytes_reduce(l) for l in layers)
-    tot = {k: sum(p[k] for p in t["phases"]) for k in ("reduce", "wgrad", "dgrad")}
+    lay_bytes = sum(t["layout_bytes"])
+    tot = {k: sum(p[k] for p in t["phases"]) for k in PHASES}
     gemm_ms = tot["wgrad"] + tot["dgrad"]
-    d.update({"reduce_ms": tot["reduce"], "wgrad_ms": tot["wgrad"], "dgrad_ms": tot["dgrad"],
+
+    def gbs(nbytes, ms):
+        return nbytes / (ms * 1e-3) / 1e9 if ms > 0 else None
+
+    floor = sum(t["read_floor_ms"]) if t.get("read_floor_ms") else None
+    d.update({"paths": t["paths"],
+              "reduce_read_floor_ms": floor,
+              "reduce_vs_read_floor": floor / tot["reduce"] if floor else None,
+              "reduce_ms": tot["reduce"], "layout_ms": tot["layout"], "wgrad_ms": tot["wgrad"],
+              "dgrad_ms": tot["dgrad"],
               "gemm_tflops": flops / (gemm_ms * 1e-3) / 1e12,
               "gemm_frac_tf32": flops / (gemm_ms * 1e-3) / 1e12 / tf32,
-              "reduce_gbs": red_bytes / (tot["reduce"] * 1e-3) / 1e9,
-              "reduce_frac_hbm": red_bytes / (tot["reduce"] * 1e-3) / 1e9 / hbm,
-              "reduce_bytes": red_bytes, "direct_call_ms_per_step": t["direct_ms"]})
+              "reduce_gbs": gbs(red_bytes, tot["reduce"]),
+              "reduce_frac_hbm": gbs(red_bytes, tot["reduce"]) / hbm,
+              "reduce_bytes": red_bytes,
+              "layout_gbs": gbs(lay_bytes, tot["layout"]) if lay_bytes else None,
+              "layout_frac_hbm": gbs(lay_bytes, tot["layout"]) / hbm if lay_bytes else None,
+              "layout_bytes": lay_bytes, "direct_call_ms_per_step": t["direct_ms"]})
     if len(layers) > 1:
         d["layers"] = []
-        for l, p in zip(layers, t["phases"]):
+        for l, p, lb in zip(layers, t["phases"], t["layout_bytes"]):
             g = l["geom"]
-            half = g.gemm_flops()
+            half = g.gemm_flops() // l.get("groups", 1)
             d["layers"].append({
                 "conv": f"{g.R}x{g.S} {g.C}->{g.K}", "reduce_ms": p["reduce"],
-                "wgrad_ms": p["wgrad"], "dgrad_ms": p["dgrad"],
+                "layout_ms": p["layout"], "wgrad_ms": p["wgrad"], "dgrad_ms": p["dgrad"],
                 "wgrad_frac_tf32": half / (p["wgrad"] * 1e-3) / 1e12 / tf32,
                 "dgrad_frac_tf32": half / (p["dgrad"] * 1e-3) / 1e12 / tf32,
-                "reduce_frac_hbm": inputs.layer_bytes_reduce(l) / (p["reduce"] * 1e-3) / 1e9 / hbm})
+                "reduce_frac_hbm": gbs(inputs.layer_bytes_reduce(l), p["reduce"]) / hbm,
+                "layout_frac_hbm": gbs(lb, p["layout"]) / hbm if lb else None})
     return d
 
 
@@ -532,32 +585,24 @@ def run_ours(args):
     value = job_value(ws, flops, ms_per_step)
     launches = t["launches_per_step"] * args.steps
 
-    if t["phases"] is None:
-        # grouped calls record no phase events: the roofline is over the step
-        achieved = flops / (ms_per_step * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": f"whole grouped step ({args.math})",
-                    "achieved": achieved, "peak": tf32, "unit": "TFLOP/s",
-                    "frac": achieved / tf32, "traffic": None, "peak_source": tf32_src}
-        phases = None
-    else:
-        # the dominant kernel phase: the (layer, GEMM) pair that takes longest
-        best = None
-        for li, (l, p) in enumerate(zip(layers, t["phases"])):
-            for ph in ("wgrad", "dgrad"):
-                if best is None or p[ph] > best[2]:
-                    best = (li, ph, p[ph])
-        li, dom, dom_ms = best
-        g = layers[li]["geom"]
-        achieved = g.gemm_flops() / (dom_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor",
-                    "kernel": f"{dom} phase ({args.math}) of the {g.R}x{g.S} {g.C}->{g.K} conv",
-                    "achieved": achieved, "peak": tf32, "unit": "TFLOP/s",
-                    "frac": achieved / tf32,
-                    "traffic": profiled_traffic(dom, workload_name(layers), li)
-                    if args.math == "tf32" else None,
-                    "peak_source": tf32_src,
-                    "frac_of_bf16_ratio": achieved / (peaks["bf16_tflops"] * TF32_PER_BF16)}
-        phases = summarize(t, tf32, hbm)
+    # the dominant kernel phase: the (layer, GEMM) pair that takes longest
+    best = None
+    for li, (l, p) in enumerate(zip(layers, t["phases"])):
+        for ph in ("wgrad", "dgrad"):
+            if best is None or p[ph] > best[2]:
+                best = (li, ph, p[ph])
+    li, dom, dom_ms = best
+    g = layers[li]["geom"]
+    achieved = g.gemm_flops() // layers[li].get("groups", 1) / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor",
+                "kernel": f"{dom} phase ({args.math}) of the {g.R}x{g.S} {g.C}->{g.K} conv",
+                "achieved": achieved, "peak": tf32, "unit": "TFLOP/s",
+                "frac": achieved / tf32,
+                "traffic": profiled_traffic(dom, workload_name(layers), li)
+                if args.math == "tf32" else None,
+                "peak_source": tf32_src,
+                "frac_of_bf16_ratio": achieved / (peaks["bf16_tflops"] * TF32_PER_BF16)}
+    phases = summarize(t, tf32, hbm)
 
     per_config = None
     if (ws == 1 and not args.no_per_config and args.layer == "conv" and args.groups == 1
@@ -571,6 +616,13 @@ def run_ours(args):
                                stream, flush)
             per_config[str(cid)] = summarize(tc, tf32, hbm)
             del tc
+        # config 2 as a convolution of 4 groups (one call, the same kernels)
+        tc = time_workload(2, args, dev, math, min(args.steps, 50), max(3, args.warmup), stream,
+                           flush, groups=4)
+        per_config["2_groups4"] = summarize(tc, tf32, hbm)
+        per_config["2_groups4"]["step_vs_ungrouped"] = (per_config["2_groups4"]["ms_per_step"] /
+                                                        per_config["2"]["ms_per_step"])
+        del tc
 
     e2e = None
     if not args.no_e2e:

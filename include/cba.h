@@ -91,7 +91,7 @@ typedef enum { CBA_MATH_TF32 = 0, CBA_MATH_FFMA = 1 } cba_math_t;
 
 typedef struct {
     int N, C, H, W;     /* layer input x: batch, channels, height, width */
-    int K, R, S;        /* filters, kernel height, kernel width (groups = 1) */
+    int K, R, S;        /* filters, kernel height, kernel width */
     int stride, pad;    /* the same in both spatial dimensions */
     int act;            /* cba_act_t */
     int batch_normalize;/* 0: no BN.  1: BN in training mode; mean/var are the batch
@@ -152,8 +152,11 @@ int cba_conv_bn_act_backward(const cba_desc_t *d, const float *x, const float *o
  * channels in groups of C/groups, output channel k meeting only the input
  * channels of its group.  W and dW are [K][C/groups][R][S]; every other
  * argument as for cba_conv_bn_act_backward (descriptor C and K are the totals,
- * both multiples of groups).  The call runs the ungrouped backward once per
- * group on that group's channel slices, copied into the workspace; it needs
+ * both multiples of groups).  The call launches the same kernels as an
+ * ungrouped one, once for all groups: the per-channel reductions do not
+ * depend on the grouping, and the two convolution gradients run as the dense
+ * K x C product with zero weights between groups (so their cost is that of
+ * the ungrouped layer), dW receiving only the pairs within a group.  It needs
  * cba_workspace_bytes_grouped(d, groups, flags) bytes (flags as for
  * cba_workspace_bytes_ex: CBA_WS_RECOMPUTE_Z for calls without z).
  * groups = 1 is cba_conv_bn_act_backward.  CBA_ERR_ARG also when groups < 1
@@ -165,8 +168,8 @@ int cba_conv_bn_act_backward_grouped(const cba_desc_t *d, int groups, const floa
                                      float *db, float *dgamma, float *prev_delta, float *dz_out,
                                      void *workspace, size_t workspace_bytes, void *stream);
 size_t cba_workspace_bytes_grouped(const cba_desc_t *d, int groups, unsigned flags);
-/* The same, for profiling: launches (NULL, or) receives the number of kernels
- * the call enqueued (the slice copies are not kernels). */
+/* The same, for profiling: phase_events and launches as for
+ * cba_conv_bn_act_backward_traced (below). */
 int cba_conv_bn_act_backward_grouped_traced(const cba_desc_t *d, int groups, const float *x,
                                             const float *output, const float *z,
                                             const float *delta, const float *W,
@@ -174,14 +177,23 @@ int cba_conv_bn_act_backward_grouped_traced(const cba_desc_t *d, int groups, con
                                             const float *var, const float *residual, float *dW,
                                             float *db, float *dgamma, float *prev_delta,
                                             float *dz_out, void *workspace,
-                                            size_t workspace_bytes, void *stream, int *launches);
+                                            size_t workspace_bytes, void *stream,
+                                            void *const *phase_events, int *launches);
 
 /* Same computation as cba_conv_bn_act_backward, for profiling.
- * phase_events: NULL, or an array of 4 cudaEvent_t created by the caller;
- *   the call records [0] before the reduction pass, [1] after it (the
- *   per-channel coefficients are ready), [2] after the weight gradient and
- *   [3] after the input gradient ([3] is recorded right after [2] when
- *   prev_delta is NULL), all on `stream`.
+ * phase_events: NULL, or an array of CBA_PHASE_EVENTS (5) cudaEvent_t created
+ *   by the caller; the call records, all on `stream`:
+ *     [0] before the reduction pass (after the workspace's counters are
+ *         cleared; a call without z recomputes z after [0]),
+ *     [1] after it: the per-channel coefficients are ready,
+ *     [2] after the GEMM operand layout pass (dz written in the layouts the
+ *         tensor-core GEMMs read, and x re-laid out where the weight gradient
+ *         needs it; see cba_plan_info) -- right after [1] on the FFMA path,
+ *         whose GEMMs transform delta as they load it,
+ *     [3] after the weight gradient,
+ *     [4] after the input gradient (right after [3] when prev_delta is NULL).
+ *   Recording events between the kernels stops a kernel from starting while
+ *   its predecessor drains, so traced calls can take slightly longer.
  * launches: NULL, or receives the number of kernels this call enqueued.
  * Return codes as cba_conv_bn_act_backward. */
 int cba_conv_bn_act_backward_traced(const cba_desc_t *d, const float *x, const float *output,
@@ -191,6 +203,31 @@ int cba_conv_bn_act_backward_traced(const cba_desc_t *d, const float *x, const f
                                     float *prev_delta, float *dz_out, void *workspace,
                                     size_t workspace_bytes, void *stream,
                                     void *const *phase_events, int *launches);
+
+#define CBA_PHASE_EVENTS 5
+
+/* Which kernels a call with this descriptor runs, and what its operand layout
+ * pass moves: a host-side query that launches nothing (groups as for
+ * cba_conv_bn_act_backward_grouped, 1 for an ungrouped layer; with_prev:
+ * whether the call will compute prev_delta).  Fills *info and returns CBA_OK,
+ * or CBA_ERR_ARG / CBA_ERR_UNSUPPORTED for a descriptor the backward call
+ * would refuse.  The path depends on the descriptor and on whether the CUDA
+ * driver offers tensor-map encoding (without a driver every call plans the
+ * FFMA kernels). */
+typedef enum {
+    CBA_PATH_FFMA = 0,        /* both GEMMs on the CUDA cores, BN transform on load */
+    CBA_PATH_TC_ROWS = 1,     /* tcgen05 TF32; weight gradient reads x rows by TMA
+                                 (stride-1 3x3 and 1x1 layers whose input rows are
+                                 16-byte strided; a 1x1 layer's plane is one row) */
+    CBA_PATH_TC_BATCH_INNER = 2 /* tcgen05 TF32; weight gradient on batch-innermost
+                                   copies of x and dz */
+} cba_path_t;
+typedef struct {
+    int path;                      /* cba_path_t */
+    long long layout_bytes_read;   /* the operand layout pass (phase events [1]..[2]) */
+    long long layout_bytes_written;
+} cba_plan_info_t;
+int cba_plan_info(const cba_desc_t *d, int groups, int with_prev, cba_plan_info_t *info);
 
 /* Reads (and clears) the device status word of a workspace after the work on
  * `stream` has finished: synchronises `stream`, then returns CBA_OK or

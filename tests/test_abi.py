@@ -159,3 +159,24 @@ def test_workspace_query_for_grouped_calls(lib):
     assert lib.cba_workspace_bytes_grouped(ctypes.byref(d), 3, 0) == 0  # 3 does not divide 8
     assert lib.cba_workspace_bytes_grouped(ctypes.byref(d), 0, 0) == 0
     assert lib.cba_workspace_bytes_grouped(ctypes.byref(d), 4, 2) == 0  # unknown flag
+
+
+def test_plan_info_query(lib):
+    d = cba.make_desc(2, 8, 5, 5, 12, 3, 3, 1, 1, act=cba.CBA_ACT_LEAKY, batch_normalize=1)
+    path, rd, wr = cba.cba_plan_info(d)
+    assert path in (cba.CBA_PATH_FFMA, cba.CBA_PATH_TC_ROWS, cba.CBA_PATH_TC_BATCH_INNER)
+    if path == cba.CBA_PATH_FFMA:  # no operand layout pass
+        assert rd == 0 and wr == 0
+    else:
+        assert rd >= 3 * 4 * 2 * 12 * 5 * 5 and wr > 0  # delta, output, z read
+    f = cba.make_desc(2, 8, 5, 5, 12, 3, 3, 1, 1, act=cba.CBA_ACT_LEAKY, batch_normalize=1,
+                      math=cba.CBA_MATH_FFMA)
+    assert cba.cba_plan_info(f) == (cba.CBA_PATH_FFMA, 0, 0)
+    with pytest.raises(cba.CbaError):
+        cba.cba_plan_info(d, groups=3)  # 3 does not divide 8
+    bad = cba.make_desc(0, 8, 5, 5, 12, 3, 3, 1, 1)
+    with pytest.raises(cba.CbaError):
+        cba.cba_plan_info(bad)
+    info = B.cba_plan_info_t()
+    assert lib.cba_plan_info(ctypes.byref(d), 1, 1, None) == cba.CBA_ERR_ARG
+    assert lib.cba_plan_info(None, 1, 1, ctypes.byref(info)) == cba.CBA_ERR_ARG

@@ -25,8 +25,9 @@ def test_summary_of_a_two_layer_step():
     # the residual block's two layers at batch 2; fake step and phase times
     layers = inputs.make_config(5, batch=2)
     t = {"layers": layers, "step_ms": [1.0, 3.0], "direct_ms": 2.5,
-         "phases": [{"reduce": 0.1, "wgrad": 0.4, "dgrad": 0.3},
-                    {"reduce": 0.05, "wgrad": 0.2, "dgrad": 0.1}]}
+         "paths": ["tc_batch_inner", "tc_rows"], "layout_bytes": [6e6, 2e6],
+         "phases": [{"reduce": 0.1, "layout": 0.02, "wgrad": 0.4, "dgrad": 0.3},
+                    {"reduce": 0.05, "layout": 0.01, "wgrad": 0.2, "dgrad": 0.1}]}
     d = bench.summarize(t, tf32=1000.0, hbm=5000.0)
     flops = sum(2 * l["geom"].gemm_flops() for l in layers)
     assert d["workload"] == "residual_block"
@@ -36,6 +37,8 @@ def test_summary_of_a_two_layer_step():
     assert abs(d["gemm_frac_tf32"] - flops / 1e-3 / 1e12 / 1000.0) < 1e-12
     red = sum(inputs.layer_bytes_reduce(l) for l in layers)
     assert abs(d["reduce_frac_hbm"] - red / 0.15e-3 / 1e9 / 5000.0) < 1e-9
+    assert abs(d["layout_frac_hbm"] - 8e6 / 0.03e-3 / 1e9 / 5000.0) < 1e-9
+    assert abs(d["layers"][1]["layout_frac_hbm"] - 2e6 / 0.01e-3 / 1e9 / 5000.0) < 1e-9
     assert len(d["layers"]) == 2
     g = layers[0]["geom"]
     assert abs(d["layers"][0]["wgrad_frac_tf32"] - g.gemm_flops() / 0.4e-3 / 1e12 / 1000.0) < 1e-9

@@ -89,13 +89,39 @@ GROUPED = [(2, 2, 2), (2, 2, 4), (2, 1, 64), (3, 2, 8)]
 @pytest.mark.parametrize("cid,batch,groups", GROUPED,
                          ids=[f"cfg{c}_n{b}_g{g}" for c, b, g in GROUPED])
 def test_parity_grouped(ref, cuda_lib, cid, batch, groups, math):
-    # l.groups: one ungrouped backward per group on its channel slices
+    # l.groups: output channel k meets only the input channels of its group
     layer = inputs.make_grouped_config(cid, groups, batch=batch)
     _, got = run_gpu(layer, math, want_dz=True)
     exp = oracle_chain(ref, layer, want_dz=True)
     for k in KEYS + ("dz",):
         if exp.get(k) is not None:
             assert_close(got[k], exp[k], TOL[math], f"{layer['name']} {k}")
+
+
+GROUPED_EDGE = [
+    # N, C, H, W, K, R, S, stride, pad, act, bn, groups
+    # stride 2, groups of 8 input / 12 output channels (batch-innermost wgrad)
+    (2, 24, 9, 10, 36, 3, 3, 2, 1, 1, True, 3),
+    # 1x1 layer with 16-byte rows (TMA-fed wgrad): groups of 6 / 5
+    (2, 48, 8, 8, 40, 1, 1, 1, 0, 0, False, 8),
+    # depthwise: one input and one output channel per group
+    (2, 32, 7, 7, 32, 3, 3, 1, 1, 1, True, 32),
+    # groups of 130 channels straddle the 128-channel tiles
+    (1, 260, 6, 6, 260, 3, 3, 1, 1, 1, True, 2),
+]
+
+
+@pytest.mark.parametrize("math", MATHS)
+@pytest.mark.parametrize("case", GROUPED_EDGE, ids=[str(i) for i in range(len(GROUPED_EDGE))])
+def test_parity_grouped_edge_shapes(ref, cuda_lib, case, math):
+    N, C, H, W, K, R, S, st, pad, act, bn, groups = case
+    spec = inputs.LayerSpec("grouped edge", inputs.Geometry(N, C, H, W, K, R, S, st, pad), act, bn)
+    layer = inputs.make_layer(spec, 700 + GROUPED_EDGE.index(case), residual=True, groups=groups)
+    _, got = run_gpu(layer, math, want_dz=True)
+    exp = oracle_chain(ref, layer, want_dz=True)
+    for k in KEYS + ("dz",):
+        if exp.get(k) is not None:
+            assert_close(got[k], exp[k], TOL[math], f"grouped edge {case} {k}")
 
 
 def test_parity_grouped_z_free_accumulate(ref, cuda_lib):
@@ -180,6 +206,30 @@ def test_parity_full_size_sampled(ref, cuda_lib, cid, math):
         ep = ref.dgrad_at(dz, layer["W"], g.H, g.W, g.stride, g.pad, ip,
                           residual=layer["residual"])
         assert_close(got["prev_delta"].reshape(-1)[ip], ep, tol, "prev_delta sampled")
+
+
+def _desc(g, act, bn, math=TF32):
+    return cba.make_desc(g.N, g.C, g.H, g.W, g.K, g.R, g.S, g.stride, g.pad, act=act,
+                         batch_normalize=int(bn), math=math)
+
+
+def test_plan_paths(cuda_lib):
+    """The kernels each workload's calls run: every layer on the tensor cores,
+    the stride-1 3x3 and 1x1 layers whose input rows are 16-byte strided
+    (config 2's 52-wide rows, the residual block's 1x1 layer viewing each
+    26 x 26 plane as one row) with the TMA-row weight gradient, the others
+    (5x5, stride 2, 13 x 13 planes, 26-wide rows) with the batch-innermost
+    one; FFMA mode on the CUDA cores; the parity shapes below reach both
+    tensor-core paths."""
+    C = inputs.CONFIGS
+    bi, rows = cba.CBA_PATH_TC_BATCH_INNER, cba.CBA_PATH_TC_ROWS
+    for cid, path in ((1, bi), (2, rows), (3, bi), (4, bi)):
+        assert cba.cba_plan_info(_desc(C[cid].geom, C[cid].act, C[cid].bn))[0] == path, cid
+    assert cba.cba_plan_info(_desc(inputs.BLOCK_CONV2, 1, True))[0] == bi
+    assert cba.cba_plan_info(_desc(C[5].geom, 1, True))[0] == rows
+    assert cba.cba_plan_info(_desc(C[2].geom, 1, True, FFMA))[0] == cba.CBA_PATH_FFMA
+    seen = {cba.cba_plan_info(_desc(inputs.Geometry(*c[:9]), c[9], c[10]))[0] for c in EDGE}
+    assert seen == {bi, rows}
 
 
 EDGE = [
