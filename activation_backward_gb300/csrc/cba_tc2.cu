@@ -157,13 +157,12 @@ constexpr int kD3Stages = 3;
 constexpr int kD3Threads = 320;  // TMA warp, MMA warp, 8 epilogue warps
 
 struct Dg3Args {
-    const float *residual;
     float *prev;
     unsigned *status;
-    int C, He, We, Pp, Qpp, bd_lo, bq_lo, stride, accumulate;
-    // red_add: prev already holds residual (+ its old value when accumulating),
-    // written by prev_init_kernel; the output is added to it at the L2, and
-    // residual / accumulate are unset
+    int C, He, We, Pp, Qpp, bd_lo, bq_lo, stride;
+    // red_add: prev already holds what the output is added to (the residual,
+    // plus its old value when accumulating; written by prev_init_kernel): the
+    // output is added at the L2.  Otherwise it is stored.
     int red_add;
     int ph, pw, Hc, Wc, min_dq, span;
     int nr, r_of[kD2MaxTaps], dp[kD2MaxTaps];
@@ -181,15 +180,12 @@ struct D3Bars {
 
 // Output of one pixel (one staging lane): for each of its cl_hi channels, the
 // sum over the class's kernel columns of the staged E values at lane offsets
-// dq[si] (column-major staging, 128 lanes per column), plus the residual and,
-// if asked, the old value.  Restrict-qualified so that the staging reads of
-// the next channels are not ordered behind the global stores.
+// dq[si] (column-major staging, 128 lanes per column), stored or added at the
+// L2 (red_add).
 __device__ __forceinline__ void dgrad_out_lane(const float *__restrict__ sl,
-                                               float *__restrict__ prev,
-                                               const float *__restrict__ residual, long long pix,
+                                               float *__restrict__ prev, long long pix,
                                                long long HW, int c0, int cl_hi, int c_tile, int ns,
-                                               const int (&dq)[kD2MaxTaps], int accumulate,
-                                               int red_add) {
+                                               const int (&dq)[kD2MaxTaps], int red_add) {
     for (int cl = 0; cl < cl_hi; cl += 8) {
         float v[8];
 #pragma unroll
@@ -200,18 +196,6 @@ __device__ __forceinline__ void dgrad_out_lane(const float *__restrict__ sl,
             for (int u = 0; u < 8; ++u)
                 if (cl + u < cl_hi) v[u] += sc[u * 128];
         }
-        // all loads before the first store (prev may alias residual as far as
-        // the compiler knows)
-        float add[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            add[u] = 0.f;
-            if (cl + u < cl_hi) {
-                const long long idx = pix + (long long)(c0 + cl + u) * HW;
-                if (residual) add[u] += residual[idx];
-                if (accumulate) add[u] += prev[idx];
-            }
-        }
         if (red_add) {
 #pragma unroll
             for (int u = 0; u < 8; ++u)
@@ -219,7 +203,7 @@ __device__ __forceinline__ void dgrad_out_lane(const float *__restrict__ sl,
         } else {
 #pragma unroll
             for (int u = 0; u < 8; ++u)
-                if (cl + u < cl_hi) prev[pix + (long long)(c0 + cl + u) * HW] = v[u] + add[u];
+                if (cl + u < cl_hi) prev[pix + (long long)(c0 + cl + u) * HW] = v[u];
         }
     }
 }
@@ -325,7 +309,7 @@ __global__ void __launch_bounds__(kD3Threads, 1)
         // ---- epilogue (warps 2-9, two groups; warp & 3 is the TMEM lane
         // quarter): E -> column-major staging (each group half the columns) ->
         // shifted sum over the kernel columns (each group half the channels)
-        // -> + residual (+ old prev_delta) -> prev_delta
+        // -> prev_delta (stored, or added at the L2)
         const int eg = (warp - 2) >> 2, wq = warp & 3;
         const int L = wq * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
@@ -389,8 +373,8 @@ __global__ void __launch_bounds__(kD3Threads, 1)
 #pragma unroll
                     for (int si = 0; si < kD2MaxTaps; ++si) dqr[si] = a.dq[si] - a.min_dq;
                     const int cb = eg == 0 ? 0 : ch_half, ce = eg == 0 ? ch_half : cl_all;
-                    dgrad_out_lane(stg + L + cb * 128, a.prev, a.residual, pix, HW, c0 + cb,
-                                   ce - cb, a.c_tile, a.ns, dqr, a.accumulate, a.red_add);
+                    dgrad_out_lane(stg + L + cb * 128, a.prev, pix, HW, c0 + cb, ce - cb,
+                                   a.c_tile, a.ns, dqr, a.red_add);
                 }
                 ptx::named_bar_sync(1, 256);
             }
@@ -416,12 +400,13 @@ __global__ void __launch_bounds__(kD3Threads, 1)
 // positions, loads E[., (s, c)] for its kernel columns s from TMEM, shifts it
 // down by dq_s lanes with warp shuffles (the lanes past the warp come from
 // the next warp through a small shared-memory halo, double-buffered so that
-// one barrier per chunk suffices), sums over s, adds the residual (and the
-// old value) and writes prev_delta.
+// one barrier per chunk suffices), sums over s and stores prev_delta or adds
+// it at the L2.
 constexpr int kD4Stages = 6;
 constexpr int kD4Threads = 352;  // A TMA warp, MMA warp, 8 epilogue warps, W TMA warp
 constexpr int kD4Slots = 6;      // TMEM loads (16 columns each) one epilogue warp has in flight
 constexpr int kD4HaloLanes = 4;  // lanes a warp passes to the warp below (the class's column span)
+constexpr int kD4LdBatch = 2;    // TMEM loads in flight per wait in the flat 1x1 epilogue
 
 struct D4Args {
     Dg3Args g;
@@ -455,9 +440,7 @@ struct D4Epi {
     long long pix, HW;
     int c0, cl_all;
     bool out;
-    const float *residual;
     float *prev;
-    int accumulate;
     int red_add;
 };
 
@@ -507,24 +490,11 @@ __device__ __forceinline__ void d4_epilogue_batch(const D4Epi &E, int t0, uint64
         }
     }
     if (E.out) {
-        // every load of a chunk is issued before its first store: prev may
-        // alias residual as far as the compiler knows, so loads placed after a
-        // store would each wait a full memory latency
 #pragma unroll
         for (int t = 0; t < NB; ++t) {
             const int cc = E.eg + 2 * (t0 + t);
             const int nvalid = min(16, E.cl_all - cc * 16);
             const long long idx0 = E.pix + (long long)(E.c0 + cc * 16) * E.HW;
-            float add[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                add[e] = 0.f;
-                if (e < nvalid) {
-                    const long long idx = idx0 + (long long)e * E.HW;
-                    if (E.residual) add[e] += __ldg(E.residual + idx);
-                    if (E.accumulate) add[e] += E.prev[idx];
-                }
-            }
             if (E.red_add) {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -532,7 +502,7 @@ __device__ __forceinline__ void d4_epilogue_batch(const D4Epi &E, int t0, uint64
             } else {
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    if (e < nvalid) E.prev[idx0 + (long long)e * E.HW] = v[t * NS][e] + add[e];
+                    if (e < nvalid) E.prev[idx0 + (long long)e * E.HW] = v[t * NS][e];
             }
         }
     }
@@ -743,17 +713,6 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                 pix = (long long)n * a.C * HW + (long long)(ii * a.stride + a.ph) * a.We +
                       (jj * a.stride + a.pw);
             }
-            if (out && (a.residual || a.accumulate)) {
-                // the values the epilogue adds are known before the MMAs finish:
-                // ask the L2 for this lane's share of them now, so that the
-                // loads below do not each wait a full memory latency
-                const float *src = a.residual ? a.residual : a.prev;
-                for (int t = 0; t < gch; ++t) {
-                    const long long c = c0 + (eg + 2 * t) * 16;
-                    const int nv = min(16, cl_all - (eg + 2 * t) * 16);
-                    for (int e = 0; e < nv; ++e) ptx::prefetch_l2(src + pix + (c + e) * HW);
-                }
-            }
             ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.acc_full[b]), (uint32_t)(i >> 1) & 1u,
                                         &sb.abort_flag, a.status, kLimitNs);
             // the group's 4 warps agree before the halo barriers below
@@ -764,19 +723,19 @@ __global__ void __launch_bounds__(kD4Threads, 1)
             E.tbase = tmem + lane_addr + (uint32_t)(b * a.ncol);
             E.c_tile = a.c_tile; E.eg = eg; E.wq = wq; E.lane = lane; E.span = span;
             E.dqr = dqr; E.pix = pix; E.HW = HW; E.c0 = c0; E.cl_all = cl_all; E.out = out;
-            E.residual = a.residual; E.prev = a.prev; E.accumulate = a.accumulate;
-            E.red_add = a.red_add;
+            E.prev = a.prev; E.red_add = a.red_add;
             if (flat4) {
                 // one plane of positions per image (1x1, stride 1; HW a multiple
                 // of 4, at least 32): the warp's 32 positions x 16 channels of a
                 // chunk go from TMEM through its staging rows [16][32] in shared
-                // memory, then out as float4 along the positions (the residual /
-                // old prev read the same way): each memory instruction of the
-                // warp moves four whole 128-byte rows instead of 32 scalars
-                // spread over a channel plane each.
+                // memory, then out as float4 along the positions: each memory
+                // instruction of the warp moves four whole 128-byte rows instead
+                // of 32 scalars spread over a channel plane each.  The TMEM loads
+                // go kD4LdBatch chunks at a time before one wait: while the next
+                // unit's MMAs run a TMEM load waits behind them, and a wait per
+                // chunk cost ~1.5 us each.
                 float *stg = halo + (warp - 2) * 512;
                 const long long mw = (long long)tile * tstride + wq * 32;  // lane 0's position
-                const bool with_res = a.residual != nullptr, with_acc = a.accumulate != 0;
                 // lane -> (channel row e = k * 4 + lane / 8, positions p4 .. p4 + 3),
                 // k = 0 .. 3; the global offset of each, without the channel
                 const int p4 = (lane & 7) * 4;
@@ -784,49 +743,36 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                 const bool mv = m < a.total_pos;
                 const long long nimg = m / HW;
                 const long long pbase = nimg * a.C * HW + (m - nimg * HW);
-                for (int t = 0; t < gch; ++t) {
-                    const int cc = eg + 2 * t;
-                    const int nvalid = min(16, cl_all - cc * 16);
-                    float v[16];
-                    ptx::tmem_ld16(E.tbase + (uint32_t)(cc * 16), v);
+                for (int t0 = 0; t0 < gch; t0 += kD4LdBatch) {
+                    const int nb = min(kD4LdBatch, gch - t0);
+                    float vb[kD4LdBatch][16];
+#pragma unroll
+                    for (int j = 0; j < kD4LdBatch; ++j)
+                        if (j < nb) ptx::tmem_ld16(E.tbase + (uint32_t)((eg + 2 * (t0 + j)) * 16), vb[j]);
                     ptx::tmem_ld_wait();
-                    if (t == gch - 1) {  // the unit's last loads: the MMAs may reuse it
+                    if (t0 + nb >= gch) {  // the unit's last loads: the MMAs may reuse it
                         ptx::tc_fence_before();
                         __syncwarp();
                         if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.acc_empty[b]));
                     }
-                    __syncwarp();  // the previous chunk's rows have been read
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) stg[e * 32 + lane] = v[e];
-                    __syncwarp();
-                    float4 val[4], add[4];
+                    for (int j = 0; j < kD4LdBatch; ++j) {
+                        if (j >= nb) break;
+                        const int cc = eg + 2 * (t0 + j);
+                        const int nvalid = min(16, cl_all - cc * 16);
+                        __syncwarp();  // the previous chunk's rows have been read
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = k * 4 + (lane >> 3);
-                        val[k] = *reinterpret_cast<const float4 *>(stg + e * 32 + p4);
-                        add[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (mv && e < nvalid) {
-                            const long long o = pbase + (long long)(c0 + cc * 16 + e) * HW;
-                            if (with_res) {
-                                const float4 r = __ldg(reinterpret_cast<const float4 *>(a.residual + o));
-                                add[k].x += r.x; add[k].y += r.y; add[k].z += r.z; add[k].w += r.w;
-                            }
-                            if (with_acc) {
-                                const float4 r = *reinterpret_cast<const float4 *>(a.prev + o);
-                                add[k].x += r.x; add[k].y += r.y; add[k].z += r.z; add[k].w += r.w;
-                            }
+                        for (int e = 0; e < 16; ++e) stg[e * 32 + lane] = vb[j][e];
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int e = k * 4 + (lane >> 3);
+                            if (!mv || e >= nvalid) continue;
+                            const float4 val = *reinterpret_cast<const float4 *>(stg + e * 32 + p4);
+                            float *o = a.prev + pbase + (long long)(c0 + cc * 16 + e) * HW;
+                            if (a.red_add) ptx::red_add_v4_f32(o, val);
+                            else *reinterpret_cast<float4 *>(o) = val;
                         }
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int e = k * 4 + (lane >> 3);
-                        if (!mv || e >= nvalid) continue;
-                        float *o = a.prev + pbase + (long long)(c0 + cc * 16 + e) * HW;
-                        if (a.red_add) ptx::red_add_v4_f32(o, val[k]);
-                        else
-                            *reinterpret_cast<float4 *>(o) =
-                                make_float4(val[k].x + add[k].x, val[k].y + add[k].y,
-                                            val[k].z + add[k].z, val[k].w + add[k].w);
                     }
                 }
                 if (gch <= 0) {  // no chunk for this group: release at once
@@ -836,57 +782,8 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                 }
                 continue;
             }
-            if (ns == 1 && span == 0) {
-                // no column shift (one kernel column, e.g. 1x1 layers): each of
-                // the group's 16-channel chunks goes straight from TMEM to prev,
-                // one channel plane (HW apart) after the other.  Per chunk the
-                // TMEM load comes first, then the loads of the values it adds
-                // (residual, old prev; prefetched into L2 above), then the
-                // stores: measured several times faster than loading the added
-                // values ahead of the TMEM load.
-                const long long cstep = 32 * HW;  // this group's next chunk
-                const bool with_res = a.residual != nullptr, with_acc = a.accumulate != 0;
-                const long long off0 = pix + (long long)(c0 + eg * 16) * HW;
-                float *dst = a.prev + off0;
-                const float *res = with_res ? a.residual + off0 : a.prev;  // read only if with_res
-                for (int t = 0; t < gch; ++t, dst += cstep, res += cstep) {
-                    const int cc = eg + 2 * t;
-                    float v[16];
-                    ptx::tmem_ld16(E.tbase + (uint32_t)(cc * 16), v);
-                    ptx::tmem_ld_wait();
-                    if (t == gch - 1) {  // the unit's last loads: the MMAs may reuse it
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.acc_empty[b]));
-                    }
-                    if (!out) continue;
-                    const int nvalid = min(16, cl_all - cc * 16);
-                    float add[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        add[e] = 0.f;
-                        if (e < nvalid) {
-                            if (with_res) add[e] += __ldg(res + e * HW);
-                            if (with_acc) add[e] += dst[e * HW];
-                        }
-                    }
-                    if (a.red_add) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            if (e < nvalid) ptx::red_add_f32(dst + e * HW, v[e]);
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            if (e < nvalid) dst[e * HW] = v[e] + add[e];
-                    }
-                }
-                if (gch <= 0) {  // no chunk for this group: release at once
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sb.acc_empty[b]));
-                }
-                continue;
-            }
+            // every other form (the 1x1 layers whose planes are not 16-byte
+            // rows included): kD4Slots / ns chunks of TMEM loads per wait
             int t0 = 0;
             do {  // at least once, so that the accumulator is always released
                 const int nb = min(bch, gch - t0);
@@ -903,13 +800,8 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                     d4_epilogue_nb<1>(E, t0, 0, rel);
                     for (int t = t0; out && !a.red_add && t < t0 + nb; ++t) {
                         const int cc = eg + 2 * t;
-                        for (int e = 0; e < 16 && cc * 16 + e < cl_all; ++e) {
-                            const long long idx = pix + (long long)(c0 + cc * 16 + e) * HW;
-                            float o = 0.f;
-                            if (a.residual) o += a.residual[idx];
-                            if (a.accumulate) o += a.prev[idx];
-                            a.prev[idx] = o;
-                        }
+                        for (int e = 0; e < 16 && cc * 16 + e < cl_all; ++e)
+                            a.prev[pix + (long long)(c0 + cc * 16 + e) * HW] = 0.f;
                     }
                     break;
                 }
@@ -1200,12 +1092,11 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzc, const float *resid
         const ClassTaps c = class_taps(p, g.He, g.We, cl);
         if (c.Hc == 0 || c.Wc == 0) continue;
         Dg3Args a;
-        a.residual = red_add ? nullptr : residual; a.prev = prev;
+        a.prev = prev;
         a.red_add = red_add ? 1 : 0;
         a.status = ws_at<unsigned>(ws, p.off_status);
         a.C = p.C; a.He = g.He; a.We = g.We; a.Pp = g.Pp; a.Qpp = g.Qpp;
         a.bd_lo = g.bd_lo; a.bq_lo = g.bq_lo; a.stride = p.stride;
-        a.accumulate = red_add ? 0 : p.accumulate;
         a.ph = cl / p.stride; a.pw = cl % p.stride; a.Hc = c.Hc; a.Wc = c.Wc;
         a.nr = c.nr; a.ns = c.ns;
         for (int i = 0; i < kD2MaxTaps; ++i) {

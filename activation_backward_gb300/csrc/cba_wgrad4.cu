@@ -524,7 +524,7 @@ cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, fl
     }
     if (e != cudaSuccess) return e;
     const long long total = (long long)w.ntiles * w.N * 128;
-    const unsigned ablocks = (unsigned)std::min<long long>((total + 255) / 256, p.num_sms * 4LL);
+    const unsigned ablocks = (unsigned)std::min<long long>((total + 255) / 256, p.num_sms * 32LL);
     const RepackJob job = rep ? *rep : RepackJob{};
     const int nrep = rep ? (int)std::min<long long>(repack_tiles(*rep), 4LL * p.num_sms) : 0;
     e = launch_pdl(wgrad_acc_apply_kernel, dim3(ablocks + nrep), dim3(256), 0, st,

@@ -794,7 +794,7 @@ cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, fl
     e = launch_pdl(kern, dim3(w.grid), dim3(kWnThreads), w.smem, st, tma, tmb, a);
     if (e != cudaSuccess) return e;
     const long long total = (long long)p.K * p.Cg * p.R * p.S;
-    const unsigned ablocks = (unsigned)std::min<long long>((total + 255) / 256, p.num_sms * 8LL);
+    const unsigned ablocks = (unsigned)std::min<long long>((total + 255) / 256, p.num_sms * 32LL);
     const RepackJob job = rep ? *rep : RepackJob{};
     const int nrep = rep ? (int)std::min<long long>(repack_tiles(*rep), 4LL * p.num_sms) : 0;
     e = launch_pdl(wgrad_nb_apply_kernel, dim3(ablocks + nrep), dim3(256), 0, st,
