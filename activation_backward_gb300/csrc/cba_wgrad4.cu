@@ -361,12 +361,21 @@ __global__ void __launch_bounds__(kW4Threads, 1)
         float *stage = reinterpret_cast<float *>(smem);
         if (ok) {
             ptx::tc_fence_after();
-            for (int cc = g; cc * 16 < a.N; cc += 2) {
-                float v[16];
-                ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(cc * 16), v);
+            // this group's 16-column chunks g, g + 2, ..., four TMEM loads per wait
+            for (int c0 = g; c0 * 16 < a.N; c0 += 8) {
+                float v[4][16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if ((c0 + 2 * j) * 16 < a.N)
+                        ptx::tmem_ld16(tmem + lane_addr + (uint32_t)((c0 + 2 * j) * 16), v[j]);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) stage[(cc * 16 + e) * 128 + kl] = v[e];
+                for (int j = 0; j < 4; ++j)
+                    if ((c0 + 2 * j) * 16 < a.N) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            stage[((c0 + 2 * j) * 16 + e) * 128 + kl] = v[j][e];
+                    }
             }
             ptx::fence_proxy_async_smem();  // the bulk copy reads these writes
         }

@@ -251,6 +251,7 @@ struct WnArgs {
     unsigned *status;
     int P, Q, R, S, stride, pad;
     int ctiles, KT, cb, cols;  // cols = S * cb = the MMA's N
+    int stages;             // epilogue stages in shared memory: KT, or 1 (reused)
     int splits;             // blocks per tile
     long long items;        // nc * P * Q
     int Qa, NA;             // positions per A box, A ring slots
@@ -499,8 +500,10 @@ __global__ void __launch_bounds__(kWnThreads, 1)
         }
     } else if (warp >= 4) {
         // ---- epilogue: D[k][col] of each k-tile -> shared memory [col][k] (the
-        // rings are idle once every MMA has completed), then one bulk
-        // reduce-add of the tile into its accumulator
+        // rings are idle once every MMA has completed; each k-tile has its own
+        // stage, so the bulk reduce-add of one overlaps the staging of the
+        // next), then one bulk reduce-add of the tile into its accumulator.
+        // The TMEM loads go four at a time before one wait.
         const int wq = warp & 3;
         const int kl = wq * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
@@ -510,16 +513,31 @@ __global__ void __launch_bounds__(kWnThreads, 1)
                                         kWnLimitNs);
         if (ok) ok = *reinterpret_cast<volatile int *>(&sb.abort_flag) == 0;
         ok = __all_sync(0xffffffffu, ok);
-        float *stage = reinterpret_cast<float *>(smem);
+        const int nld = a.cols / 16;  // 16-column TMEM loads per k-tile
         for (int t = 0; t < a.KT; ++t) {
+            const int si = t % a.stages;
+            float *stage = reinterpret_cast<float *>(smem) + (size_t)si * a.cols * 128;
+            if (t >= a.stages) {  // the stage's previous reduce-add has read it
+                if (warp == 4 && lane == 0) ptx::bulk_wait_read_all();
+                ptx::named_bar_sync(1, 128);
+            }
             if (ok) {
                 ptx::tc_fence_after();
-                for (int cc = 0; cc * 16 < a.cols; ++cc) {
-                    float v[16];
-                    ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(t * a.cols + cc * 16), v);
+                for (int c0 = 0; c0 < nld; c0 += 4) {
+                    float v[4][16];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        if (c0 + j < nld)
+                            ptx::tmem_ld16(tmem + lane_addr + (uint32_t)(t * a.cols + (c0 + j) * 16),
+                                           v[j]);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) stage[(cc * 16 + e) * 128 + kl] = v[e];
+                    for (int j = 0; j < 4; ++j)
+                        if (c0 + j < nld) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                stage[((c0 + j) * 16 + e) * 128 + kl] = v[j][e];
+                        }
                 }
                 ptx::fence_proxy_async_smem();  // the bulk copy reads these writes
             }
@@ -529,10 +547,10 @@ __global__ void __launch_bounds__(kWnThreads, 1)
                                          ptx::smem_u32(stage),
                                          (uint32_t)(a.cols * 128 * sizeof(float)));
                 ptx::bulk_commit();
-                ptx::bulk_wait_read_all();  // the stage is read before it is reused
             }
-            ptx::named_bar_sync(1, 128);
         }
+        if (warp == 4 && lane == 0) ptx::bulk_wait_read_all();  // before the block exits
+        ptx::named_bar_sync(1, 128);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -589,6 +607,7 @@ struct WnGeom {
     int nb, nc, cb, cols, KT, ktiles, ctiles, units, splits, grid;
     long long items;
     int Qa, NA, G, NG;
+    int stages;  // epilogue stages (one per k-tile when they fit)
     uint32_t rb, a_pos_bytes, a_slot_bytes, pix_bytes, grp_bytes, b_off;
     size_t smem, acc_bytes, xn_bytes, dzn_bytes;
 };
@@ -648,8 +667,10 @@ WnGeom wn_geom(const Plan &p) {
     w.NA = na;
     w.NG = ng;
     w.b_off = (uint32_t)((size_t)na * w.a_slot_bytes);
-    const size_t stage = (size_t)w.cols * 128 * sizeof(float);
-    w.smem = std::max(bytes(na, ng), stage) + 1024;
+    // epilogue stages: one per k-tile when they fit, else one reused
+    const size_t stage1 = (size_t)w.cols * 128 * sizeof(float);
+    w.stages = (std::max(bytes(na, ng), (size_t)w.KT * stage1) + 1024 <= 227 * 1024) ? w.KT : 1;
+    w.smem = std::max(bytes(na, ng), (size_t)w.stages * stage1) + 1024;
     if (w.smem > 227 * 1024) return w;
     w.acc_bytes = (size_t)w.units * w.KT * w.cols * 128 * sizeof(float);
     w.xn_bytes = sizeof(float) * (size_t)w.nc * w.nb * p.H * p.W * p.C;
@@ -766,6 +787,7 @@ cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, fl
     a.status = ws_at<unsigned>(ws, p.off_status);
     a.P = p.P; a.Q = p.Q; a.R = p.R; a.S = p.S; a.stride = p.stride; a.pad = p.pad;
     a.ctiles = w.ctiles; a.KT = w.KT; a.cb = w.cb; a.cols = w.cols; a.splits = w.splits;
+    a.stages = w.stages;
     a.items = w.items; a.Qa = w.Qa; a.NA = w.NA; a.G = w.G; a.NG = w.NG;
     a.mirror = p.S > 1 ? 1 : 0;
     a.rb = w.rb;
