@@ -75,10 +75,13 @@ __device__ __forceinline__ void finalize_channel(int k, double S1, double S2, lo
     coef[k] = cf;
 }
 
-// Block b < K * groups * pieces: channel k = b % K, then piece, then group
-// (consecutive blocks take adjacent planes).  Group g holds planes g * pln ..
-// min(N, (g + 1) * pln) - 1; piece q covers accesses q * L .. (q + 1) * L - 1 of
-// each of its planes (L = ceil(accesses per plane / pieces)).
+// Block b < K * groups * pieces: channel k = b / (groups * pieces), its
+// piece and group gq = b % (groups * pieces) (piece fastest).  Group g holds
+// planes g * pln .. min(N, (g + 1) * pln) - 1; piece q covers accesses q * L ..
+// (q + 1) * L - 1 of each of its planes (L = ceil(accesses per plane /
+// pieces)).  The channels go in ascending order, so the last ones read are
+// still in L2 when the dz pass, which walks the channels in descending order,
+// starts.
 template <int ACT, bool BN, bool VEC>
 __global__ void __launch_bounds__(kRedThreads)
     bn_reduce_kernel(const float *__restrict__ delta, const float *__restrict__ output,
@@ -89,8 +92,9 @@ __global__ void __launch_bounds__(kRedThreads)
                      float *__restrict__ db, float *__restrict__ dgamma,
                      Coef *__restrict__ coef, int bn_mode) {
     ptx::griddep_wait();
-    const int k = (int)(blockIdx.x % K);
-    const int gq = (int)(blockIdx.x / K);
+    const int parts = groups * pieces;
+    const int k = (int)(blockIdx.x / parts);
+    const int gq = (int)(blockIdx.x - (unsigned)k * parts);
     const int q = gq % pieces, grp = gq / pieces;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float mu = BN ? mean[k] : 0.f;

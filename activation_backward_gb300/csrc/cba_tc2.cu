@@ -72,7 +72,9 @@ __global__ void __launch_bounds__(256)
     __shared__ float tile[32][65];
     const int t = threadIdx.x;
     const int n = blockIdx.y / Pp, pp = blockIdx.y - (blockIdx.y / Pp) * Pp, p = pp - bd_lo;
-    const int k0 = blockIdx.z * 64;
+    // channel chunks in descending order: the reduction pass read the high
+    // channels last, so they are the ones still in L2
+    const int k0 = (gridDim.z - 1 - blockIdx.z) * 64;
     float *rowp = dzc + ((size_t)n * Pp + pp) * Qpp * Kp;
     const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
     {  // border columns: the left ones with the first column chunk, the right ones with the last

@@ -148,7 +148,9 @@ __global__ void __launch_bounds__(256)
     __shared__ float tile[32][8 * NB + 1];
     const int t = threadIdx.x;
     const int pos0 = blockIdx.x * 32;
-    const int j = blockIdx.y / cchunks, k0 = (blockIdx.y % cchunks) * 8;
+    // channel chunks in descending order: the reduction pass read the high
+    // channels last, so they are the ones still in L2
+    const int j = blockIdx.y / cchunks, k0 = (cchunks - 1 - (int)(blockIdx.y % cchunks)) * 8;
     if constexpr (VEC) {
         // P*Q a multiple of 4: float4 reads along the positions, all issued
         // before the first store to shared memory
