@@ -22,4 +22,4 @@ from ._binding import (ACT_NAMES, CBA_ACT_ELU, CBA_ACT_HARDTAN, CBA_ACT_LEAKY,  
                        make_pool_desc, CBA_WS_RECOMPUTE_Z, cba_workspace_bytes_ex,
                        cba_conv_bn_act_backward_grouped, cba_workspace_bytes_grouped,
                        cba_plan_info, CBA_PHASE_EVENTS, CBA_PATH_FFMA, CBA_PATH_TC_ROWS,
-                       CBA_PATH_TC_BATCH_INNER)
+                       CBA_PATH_TC_BATCH_INNER, CBA_PATH_TC_GEMM_1X1)

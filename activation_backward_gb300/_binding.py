@@ -58,6 +58,7 @@ CBA_PHASE_EVENTS = 5
 CBA_PATH_FFMA = 0
 CBA_PATH_TC_ROWS = 1
 CBA_PATH_TC_BATCH_INNER = 2
+CBA_PATH_TC_GEMM_1X1 = 3
 
 
 class cba_desc_t(ctypes.Structure):

@@ -89,9 +89,11 @@ int make_plan(const cba_desc_t *d, Plan *p, int groups) {
     // needs no re-laid-out x and measured faster there), the batch-innermost
     // one everywhere else
     const bool tc_math = p->math == CBA_MATH_TF32 && tc2_supported(*p);
-    const bool w4 = tc_math && wgrad_tc4_supported(*p);
-    p->use_wnb = tc_math && !w4 && wgrad_nb_supported(*p);
-    p->use_tc2 = w4 || p->use_wnb;
+    // 1x1 stride-1 layers with 16-byte rows: both gradients as plain GEMMs
+    p->use_g1 = tc_math && gemm1x1_supported(*p);
+    const bool w4 = tc_math && !p->use_g1 && wgrad_tc4_supported(*p);
+    p->use_wnb = tc_math && !p->use_g1 && !w4 && wgrad_nb_supported(*p);
+    p->use_tc2 = p->use_g1 || w4 || p->use_wnb;
 
     // workspace carve-up
     size_t off = 0;
@@ -100,7 +102,7 @@ int make_plan(const cba_desc_t *d, Plan *p, int groups) {
     p->off_cnt = off;
     off = align_up(off + sizeof(unsigned) * (size_t)p->K, 256);
     p->off_wgacc = off;
-    if (p->use_tc2)
+    if (p->use_tc2 && !p->use_g1)
         off = align_up(off + (p->use_wnb ? wgrad_nb_acc_bytes(*p) : wgrad_tc4_ws_bytes(*p)), 256);
     p->clear_bytes = off;
     p->off_red = off;
@@ -120,6 +122,8 @@ int make_plan(const cba_desc_t *d, Plan *p, int groups) {
     if (p->use_wnb) off = align_up(off + wgrad_nb_xn_bytes(*p), 256);
     p->off_dzn = off;
     if (p->use_wnb) off = align_up(off + wgrad_nb_dzn_bytes(*p), 256);
+    p->off_dzt = off;
+    if (p->use_g1) off = align_up(off + gemm1x1_dzt_bytes(*p), 256);
     p->total = off;
     p->off_z = off;
     p->fwd_tc = false;
@@ -272,6 +276,26 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
         // batch-innermost for the other weight gradient
         float *dzc = ws_at<float>(workspace, p.off_dzc);
         float *xn = ws_at<float>(workspace, p.off_xn), *dzn = ws_at<float>(workspace, p.off_dzn);
+        float *dzt = ws_at<float>(workspace, p.off_dzt);
+        const RepackJob rep = make_repack_job(p, Wt, ws_at<float>(workspace, p.off_wr));
+        const RepackJob *repp = prev_delta ? &rep : nullptr;
+        if (p.use_g1) {
+            // dz in the input's order for the weight gradient and channels-last
+            // for the input gradient, then two plain GEMMs
+            if (e == cudaSuccess)
+                e = launch_dzc(p, delta, output, z, workspace, dzc, st, &n_launch, dzt);
+            if (e == cudaSuccess) e = tr.mark(2);
+            if (e == cudaSuccess)
+                e = launch_gemm1x1_wgrad(p, dzt, x, dW, workspace, repp, st, &n_launch);
+            if (e == cudaSuccess) e = tr.mark(3);
+            if (e == cudaSuccess && prev_delta)
+                e = launch_gemm1x1_dgrad(p, ws_at<float>(workspace, p.off_wr), dzc, residual,
+                                         prev_delta, workspace, st, &n_launch);
+            if (e == cudaSuccess) e = tr.mark(4);
+            if (launches) *launches = n_launch;
+            if (e != cudaSuccess) return fail_cuda(e);
+            return CBA_OK;
+        }
         if (p.use_wnb) {
             if (e == cudaSuccess)
                 e = launch_dz_layouts(p, delta, output, z, workspace, dzn,
@@ -283,8 +307,6 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
         if (e == cudaSuccess) e = tr.mark(2);
         // the tensor-core input gradient reads repacked weights: written by
         // extra blocks of the weight gradient's accumulator-apply launch
-        const RepackJob rep = make_repack_job(p, Wt, ws_at<float>(workspace, p.off_wr));
-        const RepackJob *repp = prev_delta ? &rep : nullptr;
         if (e == cudaSuccess)
             e = p.use_wnb ? launch_wgrad_nb(p, xn, dzn, dW, workspace,
                                             ws_at<float>(workspace, p.off_wgacc), repp, st,
@@ -373,8 +395,10 @@ int cba_plan_info(const cba_desc_t *d, int groups, int with_prev, cba_plan_info_
     Plan p;
     const int rc = make_plan(d, &p, groups);
     if (rc != CBA_OK) return rc;
-    info->path = !p.use_tc2 ? CBA_PATH_FFMA : p.use_wnb ? CBA_PATH_TC_BATCH_INNER
-                                                        : CBA_PATH_TC_ROWS;
+    info->path = !p.use_tc2  ? CBA_PATH_FFMA
+                 : p.use_g1  ? CBA_PATH_TC_GEMM_1X1
+                 : p.use_wnb ? CBA_PATH_TC_BATCH_INNER
+                             : CBA_PATH_TC_ROWS;
     info->layout_bytes_read = 0;
     info->layout_bytes_written = 0;
     if (p.use_tc2) {
@@ -387,6 +411,8 @@ int cba_plan_info(const cba_desc_t *d, int groups, int with_prev, cba_plan_info_
             info->layout_bytes_read += (long long)sizeof(float) * p.N * p.C * p.HW;  // x
             info->layout_bytes_written = (long long)wgrad_nb_dzn_bytes(p) +
                                          (long long)wgrad_nb_xn_bytes(p) + (with_prev ? dzc : 0);
+        } else if (p.use_g1) {
+            info->layout_bytes_written = dzc + (long long)gemm1x1_dzt_bytes(p);
         } else {
             info->layout_bytes_written = dzc;
         }

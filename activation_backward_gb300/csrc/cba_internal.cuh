@@ -49,9 +49,11 @@ struct Plan {
     int wg_splits;
     long long wg_chunk;  // reduction positions per split (multiple of the K tile)
     // tensor-core path
-    int use_tc2;  // tensor cores, TMEM-operand kernels (cba_tc2.cu); preferred
+    int use_tc2;  // tensor cores (TF32 tcgen05 kernels); else the FFMA kernels
     int use_wnb;  // (with use_tc2) the weight gradient on batch-innermost layouts
                   // (cba_wgrad_nb.cu): x and dz re-laid out at off_xn / off_dzn
+    int use_g1;   // (with use_tc2) 1x1 layers as plain GEMMs (cba_gemm1x1.cu), with
+                  // dz also in [N][K][H*W] order at off_dzt
     // workspace layout (byte offsets from the base)
     // off_cnt: per-channel arrival counters of the reduction (zeroed with the
     // status word at the start of every call; clear_bytes covers both)
@@ -65,6 +67,7 @@ struct Plan {
     size_t off_z, total_z;
     bool fwd_tc;
     size_t off_xn, off_dzn;  // batch-innermost x and dz (use_wnb)
+    size_t off_dzt;          // dz in [N][K][H*W] order (use_g1)
 };
 
 // Builds the plan; returns CBA_OK or a CBA_ERR_* code.
@@ -137,9 +140,15 @@ int report_cuda_error(cudaError_t e);
 bool tc2_supported(const Plan &p);
 size_t tc2_dzc_bytes(const Plan &p);
 size_t tc2_wr_bytes(const Plan &p);
-// dz pass: dz written channels-last with its zero border (dzc_geom's layout).
+// dz pass: dz written channels-last with its zero border (dzc_geom's layout),
+// and, when dzt is not NULL, also in the input's [N][K][P][Q] order.
 cudaError_t launch_dzc(const Plan &p, const float *delta, const float *output, const float *z,
-                       const void *ws, float *dzc, cudaStream_t st, int *launches);
+                       const void *ws, float *dzc, cudaStream_t st, int *launches,
+                       float *dzt = nullptr);
+// prev = residual (+ prev when accumulating): the shortcut pre-pass before an
+// input gradient that adds its result at the L2.
+cudaError_t launch_prev_init(const Plan &p, const float *residual, float *prev, cudaStream_t st,
+                             int *launches);
 
 // The geometry the TMA kernels see and the channels-last dz copy's layout:
 // dzc [N][Pp][Qpp][Kp], data at row offset bd_lo and column offset bq_lo (zero
@@ -174,6 +183,18 @@ cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, fl
 cudaError_t launch_dz_layouts(const Plan &p, const float *delta, const float *output,
                               const float *z, const void *ws, float *dzn, float *dzc,
                               cudaStream_t st, int *launches);
+// Both gradients of 1x1 stride-1 unpadded layers as plain TMA-fed GEMMs
+// (cba_gemm1x1.cu): dzt is dz in [N][K][H*W] order, dzc the channels-last copy,
+// wr the repacked weights (written by the weight-gradient launch when rep is
+// not NULL).
+bool gemm1x1_supported(const Plan &p);
+size_t gemm1x1_dzt_bytes(const Plan &p);
+cudaError_t launch_gemm1x1_wgrad(const Plan &p, const float *dzt, const float *x, float *dW,
+                                 const void *ws, const RepackJob *rep, cudaStream_t st,
+                                 int *launches);
+cudaError_t launch_gemm1x1_dgrad(const Plan &p, const float *wr, const float *dzc,
+                                 const float *residual, float *prev, void *ws, cudaStream_t st,
+                                 int *launches);
 // Weight gradient with TMA-fed input rows (cba_wgrad4.cu).
 bool wgrad_tc4_supported(const Plan &p);
 size_t wgrad_tc4_ws_bytes(const Plan &p);  // tile accumulators (0 if the shape is not covered)

@@ -9,6 +9,7 @@
 #pragma once
 
 #include "cba_internal.cuh"
+#include "cba_ptx.cuh"
 
 namespace cba {
 
@@ -53,6 +54,43 @@ __device__ __forceinline__ void repack_part(const RepackJob &j, int rb, int nrep
             }
         }
         __syncthreads();
+    }
+}
+
+// The same, run by a group of `nthreads` threads (a multiple of 32; `t` is a
+// thread's index in the group) that synchronise on named barrier `bar`, with
+// the 32 x 33 tile in `tile` (shared memory): for kernels whose other warps
+// are busy with other roles.
+__device__ __forceinline__ void repack_part_group(const RepackJob &j, int rb, int nrep, float *tile,
+                                                  int t, int nthreads, int bar) {
+    const int CRS = j.C * j.R * j.S, RS = j.R * j.S;
+    const int tk = (j.Kw + 31) / 32, tc = (CRS + 31) / 32;
+    const int tx = t & 31, ty = t >> 5, rows = nthreads >> 5;
+    for (int u = rb; u < tk * tc; u += nrep) {
+        const int k0 = (u / tc) * 32, q0 = (u % tc) * 32;
+        for (int r = ty; r < 32; r += rows) {
+            const int k = k0 + r, q = q0 + tx;
+            float v = 0.f;
+            if (k < j.K && q < CRS) {
+                const int c = q / RS;
+                const long long o = w_off(k, c, q - c * RS, j.Cg, j.Kg, RS);
+                if (o >= 0) {
+                    uint32_t w;
+                    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(w) : "f"(j.W[o]));
+                    v = __uint_as_float(w);
+                }
+            }
+            tile[r * 33 + tx] = v;
+        }
+        ptx::named_bar_sync(bar, nthreads);
+        for (int r = ty; r < 32; r += rows) {
+            const int q = q0 + r, k = k0 + tx;
+            if (q < CRS && k < j.Kw) {
+                const int c = q / RS, rs = q - c * RS;
+                j.wr[((long long)rs * j.C + c) * j.Kw + k] = tile[tx * 33 + r];
+            }
+        }
+        ptx::named_bar_sync(bar, nthreads);
     }
 }
 

@@ -67,7 +67,8 @@ template <int ACT, bool BN, bool VEC>
 __global__ void __launch_bounds__(256)
     dzc_kernel(const float *__restrict__ delta, const float *__restrict__ output,
                const float *__restrict__ z, const Coef *__restrict__ coef, int K, int Pe, int Qe,
-               int Kp, int Pp, int Qpp, int bd_lo, int bq_lo, int nqc, float *__restrict__ dzc) {
+               int Kp, int Pp, int Qpp, int bd_lo, int bq_lo, int nqc, float *__restrict__ dzc,
+               float *__restrict__ dzt) {
     ptx::griddep_wait();  // the coefficients come from the reduction pass
     __shared__ float tile[32][65];
     const int t = threadIdx.x;
@@ -133,6 +134,18 @@ __global__ void __launch_bounds__(256)
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) v[e] = to_tf32(dz_of<ACT, BN>(d[e], y[e], zz[e], cf));
+                if (dzt != nullptr) {  // dz in the input's own [N][K][Pe][Qe] order too
+                    const int q = q0 + 4 * q4;
+                    if (VEC) {
+                        if (q < Qe)
+                            *reinterpret_cast<float4 *>(dzt + base + q) =
+                                make_float4(v[0], v[1], v[2], v[3]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (q + e < Qe) dzt[base + q + e] = v[e];
+                    }
+                }
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) tile[4 * q4 + e][kl] = v[e];
@@ -1027,7 +1040,7 @@ size_t tc2_wr_bytes(const Plan &p) {
 }
 
 cudaError_t launch_dzc(const Plan &p, const float *delta, const float *output, const float *z,
-                       const void *ws, float *dzc, cudaStream_t st, int *launches) {
+                       const void *ws, float *dzc, cudaStream_t st, int *launches, float *dzt) {
     const V2Geom g = v2_geom(p);
     const Coef *coef = ws_at<Coef>(ws, p.off_coef);
     const bool leaky = p.act == CBA_ACT_LEAKY;
@@ -1039,11 +1052,11 @@ cudaError_t launch_dzc(const Plan &p, const float *delta, const float *output, c
         if (g.Qe % 4 == 0)                                                                     \
             e = launch_pdl(dzc_kernel<A, B, true>, grid, dim3(256), 0, st, delta, output, z,   \
                            coef, p.K, g.Pe, g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, nqc,   \
-                           dzc);                                                               \
+                           dzc, dzt);                                                          \
         else                                                                                   \
             e = launch_pdl(dzc_kernel<A, B, false>, grid, dim3(256), 0, st, delta, output, z,  \
                            coef, p.K, g.Pe, g.Qe, g.Kp, g.Pp, g.Qpp, g.bd_lo, g.bq_lo, nqc,   \
-                           dzc);                                                               \
+                           dzc, dzt);                                                          \
     } while (0)
     if (p.bn) {
         if (leaky) CBA_DZC(CBA_ACT_LEAKY, true);
@@ -1056,6 +1069,18 @@ cudaError_t launch_dzc(const Plan &p, const float *delta, const float *output, c
     if (e != cudaSuccess) return e;
     *launches += 1;
     return cudaGetLastError();
+}
+
+cudaError_t launch_prev_init(const Plan &p, const float *residual, float *prev, cudaStream_t st,
+                             int *launches) {
+    const long long n = (long long)p.N * p.C * p.H * p.W;
+    const unsigned blocks =
+        (unsigned)std::min<long long>((n / 4 + 255) / 256 + 1, (long long)p.num_sms * 8);
+    cudaError_t e = launch_pdl(prev_init_kernel, dim3(blocks), dim3(256), 0, st, prev, residual, n,
+                               p.accumulate);
+    if (e != cudaSuccess) return e;
+    *launches += 1;
+    return cudaSuccess;
 }
 
 cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzc, const float *residual, float *prev,
@@ -1082,13 +1107,8 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzc, const float *resid
     // first and every class adds its result to it at the L2 (red_add).
     const bool red_add = residual != nullptr || p.accumulate != 0;
     if (residual) {
-        const long long n = (long long)p.N * p.C * p.H * p.W;
-        const unsigned blocks = (unsigned)std::min<long long>((n / 4 + 255) / 256 + 1,
-                                                              (long long)p.num_sms * 8);
-        cudaError_t e = launch_pdl(prev_init_kernel, dim3(blocks), dim3(256), 0, st, prev,
-                                   residual, n, p.accumulate);
+        cudaError_t e = launch_prev_init(p, residual, prev, st, launches);
         if (e != cudaSuccess) return e;
-        *launches += 1;
     }
     for (int cl = 0; cl < p.stride * p.stride; ++cl) {
         const ClassTaps c = class_taps(p, g.He, g.We, cl);

@@ -39,7 +39,7 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 # layout pass, weight gradient, input gradient
 PHASES = ("reduce", "layout", "wgrad", "dgrad")
 SPIN_CYCLES = 2_000_000  # about 1 ms at the SM clock
-PATH_NAMES = {0: "ffma", 1: "tc_rows", 2: "tc_batch_inner"}
+PATH_NAMES = {0: "ffma", 1: "tc_rows", 2: "tc_batch_inner", 3: "tc_gemm_1x1"}
 
 
 def load_peaks():

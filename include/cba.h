@@ -219,8 +219,11 @@ typedef enum {
     CBA_PATH_TC_ROWS = 1,     /* tcgen05 TF32; weight gradient reads x rows by TMA
                                  (stride-1 3x3 and 1x1 layers whose input rows are
                                  16-byte strided; a 1x1 layer's plane is one row) */
-    CBA_PATH_TC_BATCH_INNER = 2 /* tcgen05 TF32; weight gradient on batch-innermost
-                                   copies of x and dz */
+    CBA_PATH_TC_BATCH_INNER = 2, /* tcgen05 TF32; weight gradient on batch-innermost
+                                    copies of x and dz */
+    CBA_PATH_TC_GEMM_1X1 = 3     /* tcgen05 TF32; 1x1 stride-1 unpadded layers with
+                                    16-byte rows (H*W and C multiples of 4, one
+                                    group): both gradients as plain TMA-fed GEMMs */
 } cba_path_t;
 typedef struct {
     int path;                      /* cba_path_t */

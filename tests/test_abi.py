@@ -164,7 +164,8 @@ def test_workspace_query_for_grouped_calls(lib):
 def test_plan_info_query(lib):
     d = cba.make_desc(2, 8, 5, 5, 12, 3, 3, 1, 1, act=cba.CBA_ACT_LEAKY, batch_normalize=1)
     path, rd, wr = cba.cba_plan_info(d)
-    assert path in (cba.CBA_PATH_FFMA, cba.CBA_PATH_TC_ROWS, cba.CBA_PATH_TC_BATCH_INNER)
+    assert path in (cba.CBA_PATH_FFMA, cba.CBA_PATH_TC_ROWS, cba.CBA_PATH_TC_BATCH_INNER,
+                    cba.CBA_PATH_TC_GEMM_1X1)
     if path == cba.CBA_PATH_FFMA:  # no operand layout pass
         assert rd == 0 and wr == 0
     else:

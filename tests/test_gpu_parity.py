@@ -223,13 +223,15 @@ def test_plan_paths(cuda_lib):
     tensor-core paths."""
     C = inputs.CONFIGS
     bi, rows = cba.CBA_PATH_TC_BATCH_INNER, cba.CBA_PATH_TC_ROWS
+    g1 = cba.CBA_PATH_TC_GEMM_1X1
     for cid, path in ((1, bi), (2, rows), (3, bi), (4, bi)):
         assert cba.cba_plan_info(_desc(C[cid].geom, C[cid].act, C[cid].bn))[0] == path, cid
     assert cba.cba_plan_info(_desc(inputs.BLOCK_CONV2, 1, True))[0] == bi
-    assert cba.cba_plan_info(_desc(C[5].geom, 1, True))[0] == rows
+    assert cba.cba_plan_info(_desc(C[5].geom, 1, True))[0] == g1
+    assert cba.cba_plan_info(_desc(C[5].geom, 1, True), groups=2)[0] == rows
     assert cba.cba_plan_info(_desc(C[2].geom, 1, True, FFMA))[0] == cba.CBA_PATH_FFMA
     seen = {cba.cba_plan_info(_desc(inputs.Geometry(*c[:9]), c[9], c[10]))[0] for c in EDGE}
-    assert seen == {bi, rows}
+    assert seen == {bi, rows, g1}
 
 
 EDGE = [
@@ -255,6 +257,9 @@ EDGE = [
     # input gradient with two k-chunks per stage and an odd chunk count (the
     # last stage's second chunk lies past K and is zero-filled)
     (2, 16, 10, 10, 96, 3, 3, 1, 1, 1, True),
+    # 1x1 layers as plain GEMMs: partial channel, position and k tiles
+    (3, 36, 6, 10, 70, 1, 1, 1, 0, 1, True),
+    (2, 260, 16, 20, 300, 1, 1, 1, 0, 1, True),
 ]
 
 
@@ -302,6 +307,20 @@ def test_accumulate_onto_existing_prev(ref, cuda_lib):
     _, got = run_gpu(layer, FFMA, accumulate=1, prev_init=seed)
     exp = oracle_chain(ref, layer, accumulate=1, prev_delta=seed)
     assert_close(got["prev_delta"], exp["prev_delta"], TOL[FFMA], "prev_delta")
+
+
+def test_accumulate_onto_existing_prev_1x1(ref, cuda_lib):
+    # the plain-GEMM 1x1 path adds at the L2 onto prev (with the shortcut
+    # pre-pass putting residual + old prev there first)
+    spec = inputs.LayerSpec("1x1 acc", inputs.Geometry(2, 40, 8, 12, 56, 1, 1, 1, 0), 1, True)
+    layer = inputs.make_layer(spec, 811, residual=True)
+    seed = np.random.default_rng(4).standard_normal(layer["x"].shape).astype(np.float32)
+    for math in MATHS:
+        _, got = run_gpu(layer, math.values[0], accumulate=1, prev_init=seed)
+        exp = oracle_chain(ref, layer, accumulate=1, prev_delta=seed)
+        for k in KEYS:
+            if exp.get(k) is not None:
+                assert_close(got[k], exp[k], TOL[math.values[0]], f"1x1 acc {k}")
 
 
 def test_prev_delta_null_skips_dgrad(ref, cuda_lib):
