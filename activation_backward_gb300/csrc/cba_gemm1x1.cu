@@ -22,8 +22,8 @@
 // units (output tiles, or tile and contraction range) with two TMEM
 // accumulators, so a unit's epilogue overlaps the next unit's MMAs.
 //
-// Roles: warp 0 issues the TMA loads, warp 1 owns TMEM and issues the MMAs,
-// warps 2-5 (one per TMEM lane quarter) run the epilogue.  Every wait is
+// Roles: warps 0 and 6 issue the TMA loads (A and B), warp 1 owns TMEM and
+// issues the MMAs, warps 2-5 (one per TMEM lane quarter) run the epilogue.  Every wait is
 // bounded (2 s); on a timeout the block sets the workspace status bit, stops,
 // waits (bounded) for its copies in flight, frees its TMEM and returns.
 #include <cuda.h>
@@ -39,7 +39,7 @@ namespace cba {
 namespace {
 
 constexpr uint64_t kG1LimitNs = 2000000000ull;
-constexpr int kG1Threads = 192;
+constexpr int kG1Threads = 224;  // A TMA warp, MMA warp, 4 epilogue warps, B TMA warp
 constexpr int kG1N = 256;                      // MMA N: positions (dgrad) or channels (wgrad)
 constexpr int kG1Stages = 4;
 constexpr uint32_t kG1ABytes = 128u * 128u;    // 128 rows x 32 fp32
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kG1Threads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < kG1Stages; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&sb.full[i]), 1);
+            ptx::mbar_init(ptx::smem_u32(&sb.full[i]), 2);  // the A and the B issuer
             ptx::mbar_init(ptx::smem_u32(&sb.empty[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -138,9 +138,12 @@ __global__ void __launch_bounds__(kG1Threads, 1)
     // the operands (dz copies, repacked weights) come from the previous kernels
     ptx::griddep_wait();
 
-    if (warp == 0) {
-        // ---- TMA: both operands of every contraction chunk into one stage
+    if (warp == 0 || warp == 6) {
+        // ---- TMA: warp 0 the A boxes, warp 6 the B boxes of every contraction
+        // chunk (one issuing thread starts a box every few hundred cycles, so
+        // the two operands get a thread each)
         if (lane == 0) {
+            const bool bside = warp == 6;
             int gs = 0;
             bool ok = true;
             for (int i = 0; ok && i < nunits; ++i) {
@@ -154,15 +157,15 @@ __global__ void __launch_bounds__(kG1Threads, 1)
                     if (!ok) break;
                     const uint32_t sp = ptx::smem_u32(smem + (size_t)slot * kG1StageBytes);
                     const uint32_t bar = ptx::smem_u32(&sb.full[slot]);
-                    ptx::mbar_arrive_expect_tx(bar, kG1StageBytes);
+                    ptx::mbar_arrive_expect_tx(bar, bside ? kG1BBytes : kG1ABytes);
                     if (a.mode == 0) {
                         const int kc = (int)g * 32;
-                        ptx::tma_load_2d(sp, &tma, kc, un.m0, bar);  // wr (k, c)
-                        ptx::tma_load_2d(sp + kG1ABytes, &tmb, kc, un.img * a.HW + un.n0, bar);
+                        if (!bside) ptx::tma_load_2d(sp, &tma, kc, un.m0, bar);  // wr (k, c)
+                        else ptx::tma_load_2d(sp + kG1ABytes, &tmb, kc, un.img * a.HW + un.n0, bar);
                     } else {
                         const int n = (int)(g / a.nhc), hc = (int)(g - (long long)n * a.nhc);
-                        ptx::tma_load_3d(sp, &tma, hc * 32, un.m0, n, bar);              // dz (hw, k, n)
-                        ptx::tma_load_3d(sp + kG1ABytes, &tmb, hc * 32, un.n0, n, bar);  // x (hw, c, n)
+                        if (!bside) ptx::tma_load_3d(sp, &tma, hc * 32, un.m0, n, bar);  // dz (hw, k, n)
+                        else ptx::tma_load_3d(sp + kG1ABytes, &tmb, hc * 32, un.n0, n, bar);  // x
                     }
                 }
             }
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kG1Threads, 1)
             int no_abort = 0;
             ptx::mbar_wait_bounded(ptx::smem_u32(&sb.drain), 0, &no_abort, a.status, kG1LimitNs);
         }
-    } else {
+    } else if (warp >= 2 && warp <= 5) {
         // ---- epilogue: warp w reads TMEM lanes 32 (w & 3) .. + 31 (rows of D).
         // Each 32-column box goes through swizzled shared memory (row = lane,
         // 16-byte chunk j of a row at j ^ (row & 7): conflict-free writes) to
