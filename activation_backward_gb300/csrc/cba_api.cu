@@ -298,9 +298,8 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
         }
         if (p.use_wnb) {
             if (e == cudaSuccess)
-                e = launch_dz_layouts(p, delta, output, z, workspace, dzn,
-                                      prev_delta ? dzc : nullptr, st, &n_launch);
-            if (e == cudaSuccess) e = launch_xn(p, x, xn, st, &n_launch);
+                e = launch_layouts(p, delta, output, z, x, workspace, dzn,
+                                   prev_delta ? dzc : nullptr, xn, st, &n_launch);
         } else if (e == cudaSuccess) {
             e = launch_dzc(p, delta, output, z, workspace, dzc, st, &n_launch);
         }

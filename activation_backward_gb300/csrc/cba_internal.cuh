@@ -166,23 +166,22 @@ bool tma_encode_f32_swz(void *tmap, const void *base, int rank, const uint64_t *
                         const uint32_t *box, int swizzle_bytes);
 // Weight gradient on batch-innermost layouts (cba_wgrad_nb.cu): xn
 // [nc][H][W][C][nb] and dzn [nc][P][Q][K][nb] (nb = 16 or 32 images, zeros past
-// N), written by launch_xn and launch_dz_layouts; tile accumulators of
-// wgrad_nb_acc_bytes, zeroed before the call.
+// N), written by launch_layouts; tile accumulators of wgrad_nb_acc_bytes,
+// zeroed before the call.
 bool wgrad_nb_supported(const Plan &p);
 size_t wgrad_nb_acc_bytes(const Plan &p);
 size_t wgrad_nb_xn_bytes(const Plan &p);
 size_t wgrad_nb_dzn_bytes(const Plan &p);
-cudaError_t launch_xn(const Plan &p, const float *x, float *xn, cudaStream_t st, int *launches);
 // rep: NULL, or the input gradient's weight repack, done by extra blocks of
 // the accumulator-apply launch (cba_repack.cuh).
 cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, float *dW, void *ws,
                             float *acc, const RepackJob *rep, cudaStream_t st, int *launches);
-// One pass over delta / output / z writing dz batch-innermost (dzn) and, when
-// dzc is not NULL, channels-last with its zero border (the layout of
-// dzc_geom, read by the input gradient).
-cudaError_t launch_dz_layouts(const Plan &p, const float *delta, const float *output,
-                              const float *z, const void *ws, float *dzn, float *dzc,
-                              cudaStream_t st, int *launches);
+// The layout pass of that weight gradient, one launch: dz batch-innermost
+// (dzn), channels-last with its zero border when dzc is not NULL (the layout
+// of dzc_geom, read by the input gradient), and x batch-innermost (xn).
+cudaError_t launch_layouts(const Plan &p, const float *delta, const float *output,
+                           const float *z, const float *x, const void *ws, float *dzn,
+                           float *dzc, float *xn, cudaStream_t st, int *launches);
 // Both gradients of 1x1 stride-1 unpadded layers as plain TMA-fed GEMMs
 // (cba_gemm1x1.cu): dzt is dz in [N][K][H*W] order, dzc the channels-last copy,
 // wr the repacked weights (written by the weight-gradient launch when rep is

@@ -57,15 +57,6 @@ __device__ __forceinline__ float rna_tf32(float v) {
 
 // ------------------------------------------------------- layout passes
 
-// One block transposes an (8 channels x 32 columns x nb images) tile of one
-// row: reads nb x 8 rows of 32 consecutive columns (coalesced), writes for
-// each column the 8 x nb contiguous values of [..][w][c][nb].  `Src` yields
-// the value of (image n, channel c, flat element offset).
-struct XSrc {
-    const float *x;
-    __device__ __forceinline__ float operator()(long long off, int) const { return __ldg(x + off); }
-};
-
 template <int ACT, bool BN>
 struct DzSrc {
     const float *delta, *output, *z;
@@ -90,79 +81,31 @@ struct DzSrc {
     }
 };
 
-// src: [N][CH][PLANE] (channels CH, PLANE = rows x columns flattened), dst:
-// [nc][PLANE][CH][NB].  grid: x = position chunks of 32, y = nc * channel
-// chunks of 8.  Each thread issues all of its NB loads before the first store
-// to shared memory.
-template <int NB, class Src>
-__global__ void __launch_bounds__(256)
-    batch_inner_kernel(Src src, int N, int CH, int PLANE, int cchunks, float *__restrict__ dst) {
-    ptx::griddep_wait();  // dz reads the reduction's coefficients
-    __shared__ float tile[32][8 * NB + 1];
-    const int t = threadIdx.x;
-    const int pos0 = blockIdx.x * 32;
-    const int j = blockIdx.y / cchunks, c0 = (blockIdx.y % cchunks) * 8;
-    constexpr int PER = NB * 8 * 32 / 256;
-    float v[PER];
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int e = t + u * 256;
-        const int pos = e & 31, rc = e >> 5;  // rc = n_local * 8 + c_local
-        const int n = j * NB + (rc >> 3), c = c0 + (rc & 7), pp = pos0 + pos;
-        v[u] = (n < N && c < CH && pp < PLANE)
-                   ? rna_tf32(src(((long long)n * CH + c) * PLANE + pp, c))
-                   : 0.f;
-    }
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const int e = t + u * 256;
-        const int rc = e >> 5;
-        tile[e & 31][(rc & 7) * NB + (rc >> 3)] = v[u];
-    }
-    __syncthreads();
-    ptx::griddep_launch_dependents();
-    // write: for each position, channels c0 .. c0 + 7 x NB images are contiguous
-    const int ncl = min(8, CH - c0);
-    for (int e = t; e < 32 * 8 * NB; e += 256) {
-        const int pos = e / (8 * NB), vv = e % (8 * NB);
-        const int pp = pos0 + pos;
-        if (pp < PLANE && vv < ncl * NB)
-            dst[(((long long)j * PLANE + pp) * CH + c0) * NB + vv] = tile[pos][vv];
-    }
+// Four consecutive elements of x (off a multiple of 4), TF32-rounded.
+__device__ __forceinline__ float4 x_load4(const float *x, long long off) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(x + off));
+    return make_float4(rna_tf32(v.x), rna_tf32(v.y), rna_tf32(v.z), rna_tf32(v.w));
 }
 
-// dz in both layouts the GEMMs read, from one pass over delta / output / z:
-//   dzn [nc][PQ][K][NB]            batch-innermost (weight gradient)
-//   dzc [N][Pp][Qpp][Kp]           channels-last with a zero border of bd_lo /
-//                                  bq_lo rows / columns (input gradient); the
-//                                  data at (bd_lo + pp / Qe, bq_lo + pp % Qe)
-// grid: x = position chunks of 32, y = nc * chunks of 8 channels over Kp.
-// Channels K .. Kp - 1 of dzc are written as zeros; the border by
-// dzc_border_kernel.
-template <int NB, int ACT, bool BN, bool DZC, bool VEC>
-__global__ void __launch_bounds__(256)
-    dz_layouts_kernel(DzSrc<ACT, BN> src, int N, int K, int Kp, int PQ, int Qe, int Pp, int Qpp,
-                      int bd_lo, int bq_lo, int cchunks, float *__restrict__ dzn,
-                      float *__restrict__ dzc) {
-    ptx::griddep_wait();  // the coefficients come from the reduction pass
-    __shared__ float tile[32][8 * NB + 1];
+// Loads the (NB images of chunk j) x (8 channels c0 ..) x (32 positions pos0 ..)
+// tile of src [N][CH][PLANE] into tile[position][channel * NB + image]
+// (TF32-rounded, zeros past N, CH and PLANE).  VEC: PLANE a multiple of 4, float4
+// reads along the positions.  Every load of the thread is issued before the
+// first store to shared memory.
+template <int NB, bool VEC, class Load1, class Load4>
+__device__ __forceinline__ void bi_load_tile(Load1 load1, Load4 load4, int N, int CH, int PLANE,
+                                             int j, int c0, int pos0, float (*tile)[8 * NB + 1]) {
     const int t = threadIdx.x;
-    const int pos0 = blockIdx.x * 32;
-    // channel chunks in descending order: the reduction pass read the high
-    // channels last, so they are the ones still in L2
-    const int j = blockIdx.y / cchunks, k0 = (cchunks - 1 - (int)(blockIdx.y % cchunks)) * 8;
     if constexpr (VEC) {
-        // P*Q a multiple of 4: float4 reads along the positions, all issued
-        // before the first store to shared memory
         constexpr int PER4 = NB * 8 * 8 / 256;
         float4 v[PER4];
 #pragma unroll
         for (int u = 0; u < PER4; ++u) {
             const int e = t + u * 256;
             const int q4 = e & 7, rc = e >> 3;
-            const int n = j * NB + (rc >> 3), k = k0 + (rc & 7), pp = pos0 + 4 * q4;
-            v[u] = (n < N && k < K && pp < PQ) ? src.load4(((long long)n * K + k) * PQ + pp, k)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int n = j * NB + (rc >> 3), c = c0 + (rc & 7), pp = pos0 + 4 * q4;
+            v[u] = (n < N && c < CH && pp < PLANE) ? load4(((long long)n * CH + c) * PLANE + pp, c)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < PER4; ++u) {
@@ -181,9 +124,9 @@ __global__ void __launch_bounds__(256)
         for (int u = 0; u < PER; ++u) {
             const int e = t + u * 256;
             const int pos = e & 31, rc = e >> 5;
-            const int n = j * NB + (rc >> 3), k = k0 + (rc & 7), pp = pos0 + pos;
-            v[u] = (n < N && k < K && pp < PQ)
-                       ? rna_tf32(src(((long long)n * K + k) * PQ + pp, k))
+            const int n = j * NB + (rc >> 3), c = c0 + (rc & 7), pp = pos0 + pos;
+            v[u] = (n < N && c < CH && pp < PLANE)
+                       ? rna_tf32(load1(((long long)n * CH + c) * PLANE + pp, c))
                        : 0.f;
         }
 #pragma unroll
@@ -193,53 +136,108 @@ __global__ void __launch_bounds__(256)
             tile[e & 31][(rc & 7) * NB + (rc >> 3)] = v[u];
         }
     }
-    __syncthreads();
-    ptx::griddep_launch_dependents();
-    // dzn: for each position, channels k0 .. k0 + 7 x NB images are contiguous
-    const int nkl = min(8, K - k0);
-    for (int e = t; e < 32 * 8 * NB; e += 256) {
+}
+
+// Writes the tile batch-innermost: dst [nc][PLANE][CH][NB], for each position
+// the 8 channels x NB images contiguous.
+template <int NB>
+__device__ __forceinline__ void bi_store_tile(const float (*tile)[8 * NB + 1], int CH, int PLANE,
+                                              int j, int c0, int pos0, float *__restrict__ dst) {
+    const int ncl = min(8, CH - c0);
+    for (int e = threadIdx.x; e < 32 * 8 * NB; e += 256) {
         const int pos = e / (8 * NB), vv = e % (8 * NB);
         const int pp = pos0 + pos;
-        if (pp < PQ && vv < nkl * NB)
-            dzn[(((long long)j * PQ + pp) * K + k0) * NB + vv] = tile[pos][vv];
-    }
-    if constexpr (DZC) {
-        // dzc: for each (image, position), the 8 channels as two float4 (Kp and
-        // k0 are multiples of 4)
-        const int nk4 = min(2, (Kp - k0) / 4);
-        for (int e = t; e < 32 * NB; e += 256) {
-            const int pos = e & 31, nl = e >> 5;
-            const int n = j * NB + nl, pp = pos0 + pos;
-            if (n >= N || pp >= PQ) continue;
-            const int pr = pp / Qe, qc = pp - pr * Qe;
-            float4 *out = reinterpret_cast<float4 *>(
-                dzc + (((long long)n * Pp + bd_lo + pr) * Qpp + bq_lo + qc) * Kp + k0);
-            for (int h = 0; h < nk4; ++h)
-                out[h] = make_float4(tile[pos][(4 * h + 0) * NB + nl], tile[pos][(4 * h + 1) * NB + nl],
-                                     tile[pos][(4 * h + 2) * NB + nl], tile[pos][(4 * h + 3) * NB + nl]);
-        }
+        if (pp < PLANE && vv < ncl * NB)
+            dst[(((long long)j * PLANE + pp) * CH + c0) * NB + vv] = tile[pos][vv];
     }
 }
 
-// Zeros of the channels-last dz copy's border: block = one (image, row) of
-// [N][Pp][Qpp][Kp]; a border row is zeroed whole, an inner row at its bq_lo
-// left and Qpp - bq_lo - Qe right columns.
-__global__ void __launch_bounds__(256)
-    dzc_border_kernel(float *__restrict__ dzc, int Pp, int Qpp, int Kp, int Pe, int Qe,
-                      int bd_lo, int bq_lo) {
-    ptx::griddep_wait();
-    const int row = blockIdx.x % Pp;
-    float4 *base = reinterpret_cast<float4 *>(dzc + (long long)blockIdx.x * Qpp * Kp);
-    const int k4 = Kp / 4;
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row < bd_lo || row >= bd_lo + Pe) {
-        for (int i = threadIdx.x; i < Qpp * k4; i += 256) base[i] = z;
+// The layout pass of the batch-innermost weight gradient, one launch.  Blocks,
+// in this order (a 1-D grid):
+//   dz tiles:  dzn [nc][PQ][K][NB] batch-innermost (weight gradient) and, with
+//              DZC, dzc [N][Pp][Qpp][Kp] channels-last with a zero border of
+//              bd_lo / bq_lo rows / columns (input gradient; channels K .. Kp-1
+//              zero).  Channel chunks in descending order: the reduction pass
+//              read the high channels last, so they are the ones still in L2.
+//   x tiles:   xn [nc][HW][C][NB] (TF32-rounded).
+//   border:    one (image, row) of dzc per block: a border row zeroed whole, an
+//              inner row at its bq_lo left and Qpp - bq_lo - Qe right columns.
+struct LayoutArgs {
+    int N, K, Kp, PQ, Qe, Pp, Qpp, Pe, bd_lo, bq_lo;
+    int kchunks, npx_dz, ndz;      // dz: channel chunks of 8 (over Kp), position chunks, blocks
+    int C, HW, xchunks, npx_x, nx;  // x: channel chunks, position chunks, blocks
+    int nborder;                    // border rows (0 without dzc or border)
+    const float *x;
+    float *dzn, *dzc, *xn;
+};
+
+template <int NB, int ACT, bool BN, bool DZC, bool VEC, bool XVEC>
+__global__ void __launch_bounds__(256) layouts_kernel(DzSrc<ACT, BN> src, LayoutArgs la) {
+    ptx::griddep_wait();  // the coefficients come from the reduction pass
+    __shared__ float tile[32][8 * NB + 1];
+    const int t = threadIdx.x;
+    int bid = (int)blockIdx.x;
+    if (bid < la.ndz) {
+        const int px = bid % la.npx_dz, py = bid / la.npx_dz;
+        const int j = py / la.kchunks, k0 = (la.kchunks - 1 - py % la.kchunks) * 8;
+        const int pos0 = px * 32;
+        bi_load_tile<NB, VEC>(
+            [&](long long off, int k) { return src(off, k); },
+            [&](long long off, int k) { return src.load4(off, k); }, la.N, la.K, la.PQ, j, k0,
+            pos0, tile);
+        __syncthreads();
+        ptx::griddep_launch_dependents();
+        bi_store_tile<NB>(tile, la.K, la.PQ, j, k0, pos0, la.dzn);
+        if constexpr (DZC) {
+            // dzc: for each (image, position), the 8 channels as two float4 (Kp
+            // and k0 are multiples of 4)
+            const int nk4 = min(2, (la.Kp - k0) / 4);
+            for (int e = t; e < 32 * NB; e += 256) {
+                const int pos = e & 31, nl = e >> 5;
+                const int n = j * NB + nl, pp = pos0 + pos;
+                if (n >= la.N || pp >= la.PQ) continue;
+                const int pr = pp / la.Qe, qc = pp - pr * la.Qe;
+                float4 *out = reinterpret_cast<float4 *>(
+                    la.dzc +
+                    (((long long)n * la.Pp + la.bd_lo + pr) * la.Qpp + la.bq_lo + qc) * la.Kp + k0);
+                for (int h = 0; h < nk4; ++h)
+                    out[h] = make_float4(tile[pos][(4 * h + 0) * NB + nl],
+                                         tile[pos][(4 * h + 1) * NB + nl],
+                                         tile[pos][(4 * h + 2) * NB + nl],
+                                         tile[pos][(4 * h + 3) * NB + nl]);
+            }
+        }
         return;
     }
-    const int nl = bq_lo, nr = Qpp - bq_lo - Qe;
-    for (int i = threadIdx.x; i < (nl + nr) * k4; i += 256) {
+    bid -= la.ndz;
+    if (bid < la.nx) {
+        const int px = bid % la.npx_x, py = bid / la.npx_x;
+        const int j = py / la.xchunks, c0 = (py % la.xchunks) * 8;
+        const int pos0 = px * 32;
+        const float *x = la.x;
+        bi_load_tile<NB, XVEC>([&](long long off, int) { return __ldg(x + off); },
+                               [&](long long off, int) { return x_load4(x, off); }, la.N, la.C,
+                               la.HW, j, c0, pos0, tile);
+        __syncthreads();
+        ptx::griddep_launch_dependents();
+        bi_store_tile<NB>(tile, la.C, la.HW, j, c0, pos0, la.xn);
+        return;
+    }
+    bid -= la.nx;
+    if (!DZC || bid >= la.nborder) return;
+    ptx::griddep_launch_dependents();
+    const int row = bid % la.Pp;
+    float4 *base = reinterpret_cast<float4 *>(la.dzc + (long long)bid * la.Qpp * la.Kp);
+    const int k4 = la.Kp / 4;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < la.bd_lo || row >= la.bd_lo + la.Pe) {
+        for (int i = t; i < la.Qpp * k4; i += 256) base[i] = z;
+        return;
+    }
+    const int nl = la.bq_lo, nr = la.Qpp - la.bq_lo - la.Qe;
+    for (int i = t; i < (nl + nr) * k4; i += 256) {
         const int c = i / k4, kk = i - c * k4;
-        const int col = c < nl ? c : bq_lo + Qe + (c - nl);
+        const int col = c < nl ? c : la.bq_lo + la.Qe + (c - nl);
         base[col * k4 + kk] = z;
     }
 }
@@ -681,77 +679,51 @@ WnGeom wn_geom(const Plan &p) {
     return w;
 }
 
-template <int NB>
-cudaError_t launch_batch_inner_x(const Plan &p, const float *x, float *xn, cudaStream_t st) {
-    const int cchunks = (p.C + 7) / 8;
-    const int nc = (p.N + NB - 1) / NB;
-    dim3 grid((unsigned)((p.HW + 31) / 32), (unsigned)(nc * cchunks));
-    return launch_pdl(batch_inner_kernel<NB, XSrc>, grid, dim3(256), 0, st, XSrc{x}, p.N, p.C,
-                      p.HW, cchunks, xn);
-}
-
 template <int NB, int ACT, bool BN>
-cudaError_t launch_dz_layouts_t(const Plan &p, const DzcGeom &g, const float *delta,
-                                const float *output, const float *z, const Coef *coef,
-                                float *dzn, float *dzc, cudaStream_t st) {
-    const int cchunks = (g.Kp + 7) / 8;
-    const int nc = (p.N + NB - 1) / NB;
-    dim3 grid((unsigned)((p.PQ + 31) / 32), (unsigned)(nc * cchunks));
+cudaError_t launch_layouts_t(const Plan &p, const DzcGeom &g, const float *delta,
+                             const float *output, const float *z, const Coef *coef,
+                             const LayoutArgs &la, unsigned blocks, cudaStream_t st) {
     const DzSrc<ACT, BN> src{delta, output, z, coef};
-    auto kern = dzc ? (p.PQ % 4 == 0 ? dz_layouts_kernel<NB, ACT, BN, true, true>
-                                     : dz_layouts_kernel<NB, ACT, BN, true, false>)
-                    : (p.PQ % 4 == 0 ? dz_layouts_kernel<NB, ACT, BN, false, true>
-                                     : dz_layouts_kernel<NB, ACT, BN, false, false>);
-    return launch_pdl(kern, grid, dim3(256), 0, st, src, p.N, p.K, g.Kp, p.PQ, g.Qe, g.Pp, g.Qpp,
-                      g.bd_lo, g.bq_lo, cchunks, dzn, dzc);
+    const bool vec = p.PQ % 4 == 0, xvec = p.HW % 4 == 0;
+    auto kern = la.dzc ? (vec ? (xvec ? layouts_kernel<NB, ACT, BN, true, true, true>
+                                      : layouts_kernel<NB, ACT, BN, true, true, false>)
+                              : (xvec ? layouts_kernel<NB, ACT, BN, true, false, true>
+                                      : layouts_kernel<NB, ACT, BN, true, false, false>))
+                       : (vec ? (xvec ? layouts_kernel<NB, ACT, BN, false, true, true>
+                                      : layouts_kernel<NB, ACT, BN, false, true, false>)
+                              : (xvec ? layouts_kernel<NB, ACT, BN, false, false, true>
+                                      : layouts_kernel<NB, ACT, BN, false, false, false>));
+    (void)g;
+    return launch_pdl(kern, dim3(blocks), dim3(256), 0, st, src, la);
 }
 
 template <int NB>
-cudaError_t launch_dz_layouts_nb(const Plan &p, const DzcGeom &g, const float *delta,
-                                 const float *output, const float *z, const Coef *coef,
-                                 float *dzn, float *dzc, cudaStream_t st) {
+cudaError_t launch_layouts_nb(const Plan &p, const DzcGeom &g, const float *delta,
+                              const float *output, const float *z, const Coef *coef,
+                              const LayoutArgs &la, unsigned blocks, cudaStream_t st) {
     const bool leaky = p.act == CBA_ACT_LEAKY;
     if (p.bn)
-        return leaky ? launch_dz_layouts_t<NB, CBA_ACT_LEAKY, true>(p, g, delta, output, z, coef,
-                                                                     dzn, dzc, st)
-                     : launch_dz_layouts_t<NB, CBA_ACT_LINEAR, true>(p, g, delta, output, z, coef,
-                                                                      dzn, dzc, st);
-    return leaky ? launch_dz_layouts_t<NB, CBA_ACT_LEAKY, false>(p, g, delta, output, z, coef,
-                                                                  dzn, dzc, st)
-                 : launch_dz_layouts_t<NB, CBA_ACT_LINEAR, false>(p, g, delta, output, z, coef,
-                                                                   dzn, dzc, st);
+        return leaky ? launch_layouts_t<NB, CBA_ACT_LEAKY, true>(p, g, delta, output, z, coef, la,
+                                                                  blocks, st)
+                     : launch_layouts_t<NB, CBA_ACT_LINEAR, true>(p, g, delta, output, z, coef,
+                                                                   la, blocks, st);
+    return leaky ? launch_layouts_t<NB, CBA_ACT_LEAKY, false>(p, g, delta, output, z, coef, la,
+                                                               blocks, st)
+                 : launch_layouts_t<NB, CBA_ACT_LINEAR, false>(p, g, delta, output, z, coef, la,
+                                                                blocks, st);
 }
 
 }  // namespace
 
-cudaError_t launch_dz_layouts(const Plan &p, const float *delta, const float *output,
-                              const float *z, const void *ws, float *dzn, float *dzc,
-                              cudaStream_t st, int *launches) {
-    const WnGeom w = wn_geom(p);
-    if (!w.ok) return cudaErrorNotSupported;
-    const DzcGeom g = dzc_geom(p);
-    const Coef *coef = ws_at<Coef>(ws, p.off_coef);
-    cudaError_t e = w.nb == 16
-                        ? launch_dz_layouts_nb<16>(p, g, delta, output, z, coef, dzn, dzc, st)
-                        : launch_dz_layouts_nb<32>(p, g, delta, output, z, coef, dzn, dzc, st);
-    if (e != cudaSuccess) return e;
-    ++*launches;
-    if (dzc && (g.Pp != g.Pe || g.Qpp != g.Qe)) {
-        e = launch_pdl(dzc_border_kernel, dim3((unsigned)(p.N * g.Pp)), dim3(256), 0, st, dzc,
-                       g.Pp, g.Qpp, g.Kp, g.Pe, g.Qe, g.bd_lo, g.bq_lo);
-        if (e != cudaSuccess) return e;
-        ++*launches;
-    }
-    return cudaSuccess;
-}
-
 bool wgrad_nb_supported(const Plan &p) {
     const WnGeom w = wn_geom(p);
     if (!w.ok) return false;
-    // int32 grid dimensions and indices of the layout passes
+    // int32 indices of the layout pass and its 1-D grid
     const DzcGeom g = dzc_geom(p);
-    if ((long long)w.nc * ((p.C + 7) / 8) > 65535 || (long long)w.nc * ((g.Kp + 7) / 8) > 65535)
-        return false;
+    const long long blocks = (long long)w.nc * ((p.PQ + 31) / 32) * ((g.Kp + 7) / 8) +
+                             (long long)w.nc * ((p.HW + 31) / 32) * ((p.C + 7) / 8) +
+                             (long long)p.N * g.Pp;
+    if (blocks >= (1LL << 31)) return false;
     if ((long long)p.N * g.Pp >= (1LL << 31)) return false;
     return true;
 }
@@ -771,13 +743,36 @@ size_t wgrad_nb_dzn_bytes(const Plan &p) {
     return w.ok ? w.dzn_bytes : 0;
 }
 
-cudaError_t launch_xn(const Plan &p, const float *x, float *xn, cudaStream_t st, int *launches) {
+cudaError_t launch_layouts(const Plan &p, const float *delta, const float *output,
+                           const float *z, const float *x, const void *ws, float *dzn,
+                           float *dzc, float *xn, cudaStream_t st, int *launches) {
     const WnGeom w = wn_geom(p);
     if (!w.ok) return cudaErrorNotSupported;
-    cudaError_t e = w.nb == 16 ? launch_batch_inner_x<16>(p, x, xn, st)
-                               : launch_batch_inner_x<32>(p, x, xn, st);
-    if (e == cudaSuccess) ++*launches;
-    return e;
+    const DzcGeom g = dzc_geom(p);
+    const int nc = (p.N + w.nb - 1) / w.nb;
+    LayoutArgs la{};
+    la.N = p.N; la.K = p.K; la.Kp = g.Kp; la.PQ = p.PQ; la.Qe = g.Qe; la.Pp = g.Pp;
+    la.Qpp = g.Qpp; la.Pe = g.Pe; la.bd_lo = g.bd_lo; la.bq_lo = g.bq_lo;
+    la.kchunks = (g.Kp + 7) / 8;
+    la.npx_dz = (p.PQ + 31) / 32;
+    la.C = p.C; la.HW = p.HW;
+    la.xchunks = (p.C + 7) / 8;
+    la.npx_x = (p.HW + 31) / 32;
+    la.x = x; la.dzn = dzn; la.dzc = dzc; la.xn = xn;
+    const long long ndz = (long long)la.npx_dz * nc * la.kchunks;
+    const long long nx = (long long)la.npx_x * nc * la.xchunks;
+    const long long nborder =
+        (dzc && (g.Pp != g.Pe || g.Qpp != g.Qe)) ? (long long)p.N * g.Pp : 0;
+    if (ndz + nx + nborder >= (1LL << 31)) return cudaErrorInvalidValue;
+    la.ndz = (int)ndz; la.nx = (int)nx; la.nborder = (int)nborder;
+    const unsigned blocks = (unsigned)(ndz + nx + nborder);
+    const Coef *coef = ws_at<Coef>(ws, p.off_coef);
+    cudaError_t e = w.nb == 16
+                        ? launch_layouts_nb<16>(p, g, delta, output, z, coef, la, blocks, st)
+                        : launch_layouts_nb<32>(p, g, delta, output, z, coef, la, blocks, st);
+    if (e != cudaSuccess) return e;
+    ++*launches;
+    return cudaSuccess;
 }
 
 cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, float *dW, void *ws,
