@@ -257,9 +257,12 @@ EDGE = [
     # input gradient with two k-chunks per stage and an odd chunk count (the
     # last stage's second chunk lies past K and is zero-filled)
     (2, 16, 10, 10, 96, 3, 3, 1, 1, 1, True),
-    # 1x1 layers as plain GEMMs: partial channel, position and k tiles
+    # 1x1 layers as plain GEMMs: partial channel, position and k tiles; tiny
+    # planes, channels and k (boxes mostly out of bounds)
     (3, 36, 6, 10, 70, 1, 1, 1, 0, 1, True),
     (2, 260, 16, 20, 300, 1, 1, 1, 0, 1, True),
+    (1, 4, 2, 2, 3, 1, 1, 1, 0, 1, True),
+    (3, 8, 3, 4, 40, 1, 1, 1, 0, 0, False),
 ]
 
 
