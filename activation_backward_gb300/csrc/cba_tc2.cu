@@ -36,6 +36,9 @@
 // All waits are bounded (2 s); see cba_ptx.cuh.
 #include <cuda.h>
 
+#include <cstring>
+#include <vector>
+
 #include "cba_internal.cuh"
 #include "cba_ptx.cuh"
 
@@ -419,6 +422,7 @@ __global__ void __launch_bounds__(kD3Threads, 1)
 // it at the L2.
 constexpr int kD4Stages = 6;
 constexpr int kD4Threads = 352;  // A TMA warp, MMA warp, 8 epilogue warps, W TMA warp
+constexpr int kD4MaxClasses = 4;  // stride phase classes in one launch (stride <= 2)
 constexpr int kD4Slots = 6;      // TMEM loads (16 columns each) one epilogue warp has in flight
 constexpr int kD4HaloLanes = 4;  // lanes a warp passes to the warp below (the class's column span)
 constexpr int kD4LdBatch = 2;    // TMEM loads in flight per wait in the flat 1x1 epilogue
@@ -543,9 +547,11 @@ __device__ __forceinline__ void d4_epilogue_nb(const D4Epi &E, int t0, int nb, u
     d4_epilogue_batch<NS, 1>(E, t0, release);
 }
 
-__global__ void __launch_bounds__(kD4Threads, 1)
-    dgrad_tc4_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmw,
-                     const __grid_constant__ CUtensorMap tmw1, const D4Args d) {
+// The persistent input-gradient GEMM of one stride phase class, run by block
+// bid of the class's nblk blocks.
+__device__ __forceinline__ void dgrad_tc4_body(const CUtensorMap *tma, const CUtensorMap *tmw,
+                                               const CUtensorMap *tmw1, const D4Args &d, int bid,
+                                               int nblk) {
     const Dg3Args &a = d.g;
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -558,8 +564,8 @@ __global__ void __launch_bounds__(kD4Threads, 1)
     const uint32_t b_chunk = (uint32_t)a.ncol * 128u;  // one k-chunk of the W slices
     const uint32_t b_bytes = (uint32_t)d.kpb * b_chunk;
     const uint32_t stage_bytes = a_bytes + b_bytes;
-    const int nunits = d.total_units > (int)blockIdx.x
-                           ? (d.total_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1
+    const int nunits = d.total_units > bid
+                           ? (d.total_units - 1 - bid) / nblk + 1
                            : 0;
 
     if (tid == 0) {
@@ -593,7 +599,7 @@ __global__ void __launch_bounds__(kD4Threads, 1)
             int gs = 0;  // global stage counter
             bool ok = true;
             for (int i = 0; ok && i < nunits; ++i) {
-                const int u = (int)blockIdx.x + i * (int)gridDim.x;
+                const int u = bid + i * nblk;
                 const int ct = u / a.total_tiles, tile = u - ct * a.total_tiles;
                 const int c0 = ct * a.c_tile;
                 const long long m0 = (long long)tile * tstride + a.min_dq;
@@ -611,22 +617,22 @@ __global__ void __launch_bounds__(kD4Threads, 1)
                     if (!wside) {
                         ptx::mbar_arrive_expect_tx(bar, a_bytes);
                         if (d.kpb == 1)
-                            ptx::tma_load_2d(ptx::smem_u32(sp), &tma, kc * 32, row, bar);
+                            ptx::tma_load_2d(ptx::smem_u32(sp), tma, kc * 32, row, bar);
                         else
-                            ptx::tma_load_3d(ptx::smem_u32(sp), &tma, 0, row, kc, bar);
+                            ptx::tma_load_3d(ptx::smem_u32(sp), tma, 0, row, kc, bar);
                     } else {
                         ptx::mbar_arrive_expect_tx(bar, b_bytes);
                         if (d.kpb > 1)
-                            ptx::tma_load_5d(ptx::smem_u32(sp + a_bytes), &tmw, 0, c0, a.s_of[0],
+                            ptx::tma_load_5d(ptx::smem_u32(sp + a_bytes), tmw, 0, c0, a.s_of[0],
                                              kc, a.r_of[ri], bar);
                         else if (d.w_one)
-                            ptx::tma_load_4d(ptx::smem_u32(sp + a_bytes), &tmw, kc * 32, c0,
+                            ptx::tma_load_4d(ptx::smem_u32(sp + a_bytes), tmw, kc * 32, c0,
                                              a.s_of[0], a.r_of[ri], bar);
                         else
                             for (int si = 0; si < a.ns; ++si)
                                 ptx::tma_load_4d(
                                     ptx::smem_u32(sp + a_bytes + (size_t)si * a.c_tile * 128),
-                                    &tmw1, kc * 32, c0, a.s_of[si], a.r_of[ri], bar);
+                                    tmw1, kc * 32, c0, a.s_of[si], a.r_of[ri], bar);
                     }
                 }
             }
@@ -711,7 +717,7 @@ __global__ void __launch_bounds__(kD4Threads, 1)
         bool ok = true;
         for (int i = 0; ok && i < nunits; ++i) {
             const int b = i & 1;
-            const int u = (int)blockIdx.x + i * (int)gridDim.x;
+            const int u = bid + i * nblk;
             const int ct = u / a.total_tiles, tile = u - ct * a.total_tiles;
             const int c0 = ct * a.c_tile;
             const int cl_all = min(a.c_tile, a.C - c0);
@@ -832,6 +838,34 @@ __global__ void __launch_bounds__(kD4Threads, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, a.ncols);
     }
+}
+
+__global__ void __launch_bounds__(kD4Threads, 1)
+    dgrad_tc4_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmw,
+                     const __grid_constant__ CUtensorMap tmw1, const D4Args d) {
+    dgrad_tc4_body(&tma, &tmw, &tmw1, d, (int)blockIdx.x, (int)gridDim.x);
+}
+
+// All stride phase classes of a layer in one launch: blocks first[c] ..
+// first[c + 1] - 1 run class c (its own tensor maps and arguments, copied to
+// shared memory), each class's block count in proportion to its work, so
+// that the classes run side by side instead of one launch after another.
+struct D4Classes {
+    CUtensorMap tma[kD4MaxClasses], tmw[kD4MaxClasses], tmw1[kD4MaxClasses];
+    D4Args d[kD4MaxClasses];
+    int first[kD4MaxClasses + 1];
+    int ncls;
+};
+
+__global__ void __launch_bounds__(kD4Threads, 1)
+    dgrad_tc4_classes_kernel(const __grid_constant__ D4Classes m) {
+    __shared__ D4Args sd;
+    int cls = 0;
+    while (cls + 1 < m.ncls && (int)blockIdx.x >= m.first[cls + 1]) ++cls;
+    if (threadIdx.x == 0) sd = m.d[cls];
+    __syncthreads();
+    dgrad_tc4_body(&m.tma[cls], &m.tmw[cls], &m.tmw1[cls], sd, (int)blockIdx.x - m.first[cls],
+                   m.first[cls + 1] - m.first[cls]);
 }
 
 // -------------------------------------------------------------- host side
@@ -1110,6 +1144,14 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzc, const float *resid
         cudaError_t e = launch_prev_init(p, residual, prev, st, launches);
         if (e != cudaSuccess) return e;
     }
+    // the classes that take the persistent kernel, launched together below
+    struct Tc4Class {
+        D4Args d4;
+        CUtensorMap tma4, tmw4, tmw;
+        size_t smem;
+        long long unit_work;  // (stages per unit + 1) x W columns per stage
+    };
+    std::vector<Tc4Class> tc4;
     for (int cl = 0; cl < p.stride * p.stride; ++cl) {
         const ClassTaps c = class_taps(p, g.He, g.We, cl);
         if (c.Hc == 0 || c.Wc == 0) continue;
@@ -1201,15 +1243,16 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzc, const float *resid
                                             (uint32_t)(d4.w_one ? std::max(1, a.ns) : 1), 1};
                     if (!encode_4d(&tmw4, wr, d, bn)) return cudaErrorInvalidValue;
                 }
-                cudaError_t e = cudaFuncSetAttribute(
-                    dgrad_tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem4);
-                if (e != cudaSuccess) return e;
-                const int grid4 = std::max(1, std::min(p.num_sms, d4.total_units));
-                e = launch_pdl(dgrad_tc4_kernel, dim3(grid4), dim3(kD4Threads), smem4, st, tma4,
-                               tmw4, tmw, d4);
-                if (e == cudaSuccess) e = cudaGetLastError();
-                if (e != cudaSuccess) return e;
-                *launches += 1;
+                Tc4Class t;
+                t.d4 = d4;
+                t.tma4 = tma4;
+                t.tmw4 = tmw4;
+                t.tmw = tmw;
+                t.smem = smem4;
+                // (+ 1 stage for the epilogue: a class no tap reaches still
+                // writes its zeros)
+                t.unit_work = ((long long)a.nr * d4.kst * d4.kpb + 1) * a.ncol;
+                tc4.push_back(t);
                 continue;
             }
         }
@@ -1226,6 +1269,74 @@ cudaError_t launch_dgrad_tc2(const Plan &p, const float *dzc, const float *resid
         if (e != cudaSuccess) return e;
         *launches += 1;
     }
+    const int ntc4 = (int)tc4.size();
+    if (ntc4 == 0) return cudaSuccess;
+    size_t smem = 0;
+    for (int k = 0; k < ntc4; ++k) smem = std::max(smem, tc4[k].smem);
+    // blocks per class: in proportion to its work (units x unit work), at
+    // least one and at most one per unit, the total within one per SM; the
+    // SMs left over go one at a time to the class that would finish last
+    int blocks[kD4MaxClasses];
+    bool together = ntc4 > 1 && ntc4 <= kD4MaxClasses;
+    if (together) {
+        long double total = 0;
+        for (int k = 0; k < ntc4; ++k) total += (long double)tc4[k].d4.total_units * tc4[k].unit_work;
+        int used = 0;
+        for (int k = 0; k < ntc4; ++k) {
+            const long double share =
+                total > 0 ? p.num_sms * (long double)tc4[k].d4.total_units * tc4[k].unit_work / total
+                          : 1;
+            blocks[k] = (int)std::max<long long>(
+                1, std::min<long long>(tc4[k].d4.total_units, (long long)share));
+            used += blocks[k];
+        }
+        together = used <= p.num_sms;
+        auto finish = [&](int k, int b) {
+            return (long long)((tc4[k].d4.total_units + b - 1) / b) * tc4[k].unit_work;
+        };
+        while (together && used < p.num_sms) {
+            int worst = -1;
+            for (int k = 0; k < ntc4; ++k)
+                if (blocks[k] < tc4[k].d4.total_units &&
+                    (worst < 0 || finish(k, blocks[k]) > finish(worst, blocks[worst])))
+                    worst = k;
+            if (worst < 0) break;
+            ++blocks[worst];
+            ++used;
+        }
+    }
+    if (!together) {
+        for (int k = 0; k < ntc4; ++k) {
+            cudaError_t e = cudaFuncSetAttribute(
+                dgrad_tc4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc4[k].smem);
+            if (e != cudaSuccess) return e;
+            const int grid4 = std::max(1, std::min(p.num_sms, tc4[k].d4.total_units));
+            e = launch_pdl(dgrad_tc4_kernel, dim3(grid4), dim3(kD4Threads), tc4[k].smem, st,
+                           tc4[k].tma4, tc4[k].tmw4, tc4[k].tmw, tc4[k].d4);
+            if (e == cudaSuccess) e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            *launches += 1;
+        }
+        return cudaSuccess;
+    }
+    D4Classes m;
+    std::memset(&m, 0, sizeof(m));
+    m.ncls = ntc4;
+    m.first[0] = 0;
+    for (int k = 0; k < ntc4; ++k) {
+        m.tma[k] = tc4[k].tma4;
+        m.tmw[k] = tc4[k].tmw4;
+        m.tmw1[k] = tc4[k].tmw;
+        m.d[k] = tc4[k].d4;
+        m.first[k + 1] = m.first[k] + blocks[k];
+    }
+    cudaError_t e = cudaFuncSetAttribute(dgrad_tc4_classes_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(dgrad_tc4_classes_kernel, dim3(m.first[ntc4]), dim3(kD4Threads), smem, st, m);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    *launches += 1;
     return cudaSuccess;
 }
 

@@ -397,35 +397,46 @@ __global__ void __launch_bounds__(kW4Threads, 1)
     }
 }
 
-// dW[k][c][r][s] += acc[tile][r * cb + c_local][k_local]: the tile accumulators
-// (tile = (k tile * nctile + c tile) * S + s) added into dW, one element per
-// thread, coalesced over k on the read.  Grouped: only the (k, c) pairs of one
-// group, into dW[k][c - g * Cg][r][s].  The first nrep blocks transpose the
-// input gradient's weight repack instead (see cba_repack.cuh), beside the
-// apply blocks.
+// dW[k][cg][r][s] += acc[tile][r * cb + c_local][k_local]: the tile
+// accumulators (tile = (k tile * nctile + c tile) * S + s) added into dW, one
+// thread per (k, cg, r), which adds its S contiguous dW elements (coalesced
+// along the warp) from S accumulator entries (scattered reads that hit the
+// L2); 32-bit index arithmetic, computed once per thread.  The input channel
+// of group-local index cg is c = (k / Kg) * Cg + cg (dense: Cg = C, Kg = K).
+// The first nrep blocks transpose the input gradient's weight repack instead
+// (see cba_repack.cuh), beside the apply blocks.
 __global__ void __launch_bounds__(256)
     wgrad_acc_apply_kernel(const float *__restrict__ acc, int N, int cb, int S, int nctile,
-                           int K, int C, int R, int Cg, int Kg, long long total,
-                           float *__restrict__ dW, int napply, RepackJob rep, int nrep) {
+                           int R, int Cg, int Kg, int nrows, float *__restrict__ dW, int napply,
+                           RepackJob rep, int nrep) {
     ptx::griddep_wait();  // the accumulators come from the weight-gradient kernel
     if ((int)blockIdx.x < nrep) {
         repack_part(rep, (int)blockIdx.x, nrep);
         return;
     }
     const int ab = (int)blockIdx.x - nrep;  // apply block
-    const long long stride = (long long)napply * blockDim.x;
-    for (long long i = ab * (long long)blockDim.x + threadIdx.x; i < total;
-         i += stride) {
-        const int kl = (int)(i & 127);
-        const long long tc = i >> 7;
-        const int col = (int)(tc % N);
-        const int tile = (int)(tc / N);
-        const int s = tile % S, kc = tile / S;
-        const int r = col / cb, c = (kc % nctile) * cb + col % cb;
-        const int k = (kc / nctile) * 128 + kl;
-        if (c < C && k < K) {
-            const long long o = w_off(k, c, r * S + s, Cg, Kg, R * S);
-            if (o >= 0) dW[o] += acc[i];
+    const size_t tile_stride = (size_t)N * 128;
+    for (int row = ab * (int)blockDim.x + (int)threadIdx.x; row < nrows;
+         row += napply * (int)blockDim.x) {
+        const int kc = row / R, r = row - kc * R;  // row = (k * Cg + cg) * R + r
+        const int k = kc / Cg, cg = kc - k * Cg;
+        const int c = cg + (k / Kg) * Cg;
+        const int kt = k >> 7, kl = k & 127;
+        const int ct = c / cb, cl = c - ct * cb;
+        const float *ap = acc + (size_t)(kt * nctile + ct) * S * tile_stride +
+                          ((size_t)r * cb + cl) * 128 + kl;
+        float *wp = dW + (size_t)row * S;
+        for (int s0 = 0; s0 < S; s0 += 4) {
+            float av[4], wv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (s0 + u < S) {
+                    av[u] = ap[(size_t)(s0 + u) * tile_stride];
+                    wv[u] = wp[s0 + u];
+                }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (s0 + u < S) wp[s0 + u] = wv[u] + av[u];
         }
     }
 }
@@ -489,7 +500,10 @@ size_t wgrad_tc4_ws_bytes(const Plan &p) {
     return w.ok ? w.acc_bytes : 0;
 }
 
-bool wgrad_tc4_supported(const Plan &p) { return w4_geom(p).ok; }
+bool wgrad_tc4_supported(const Plan &p) {
+    // int32 dW row index of the accumulator apply
+    return w4_geom(p).ok && (long long)p.K * p.Cg * p.R < (1LL << 31);
+}
 
 cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, float *dW,
                              void *ws, const RepackJob *rep, cudaStream_t st, int *launches) {
@@ -532,13 +546,13 @@ cudaError_t launch_wgrad_tc4(const Plan &p, const float *x, const float *dzc, fl
                        a);
     }
     if (e != cudaSuccess) return e;
-    const long long total = (long long)w.ntiles * w.N * 128;
-    const unsigned ablocks = (unsigned)std::min<long long>((total + 255) / 256, p.num_sms * 32LL);
+    const int nrows = p.K * p.Cg * p.R;  // dW rows of S elements, < 2^31 (wgrad_tc4_supported)
+    const unsigned ablocks = (unsigned)std::min<long long>((nrows + 255) / 256, p.num_sms * 32LL);
     const RepackJob job = rep ? *rep : RepackJob{};
     const int nrep = rep ? (int)std::min<long long>(repack_tiles(*rep), 4LL * p.num_sms) : 0;
     e = launch_pdl(wgrad_acc_apply_kernel, dim3(ablocks + nrep), dim3(256), 0, st,
-                   (const float *)a.acc, w.N, w.cb, p.S, w.nctile, p.K, p.C, p.R, p.Cg, p.Kg,
-                   total, dW, (int)ablocks, job, nrep);
+                   (const float *)a.acc, w.N, w.cb, p.S, w.nctile, p.R, p.Cg, p.Kg, nrows, dW,
+                   (int)ablocks, job, nrep);
     if (e != cudaSuccess) return e;
     *launches += 2;
     return cudaGetLastError();

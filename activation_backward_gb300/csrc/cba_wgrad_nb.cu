@@ -29,9 +29,11 @@
 // the blocks of a tile); a second kernel adds the accumulators into dW.
 //
 // Roles: warp 0 issues the A loads, warp 2 the pixel loads, warp 1 the MMAs
-// (one thread), warps 4-7 run the epilogue (TMEM lanes 0-127).  Every wait is
-// bounded (2 s); on a timeout the block sets the workspace status bit and
-// stops.
+// (one thread), warps 4-7 run the epilogue (TMEM lanes 0-127); until the
+// tile is done they transpose their share of the input gradient's weight
+// repack (cba_repack.cuh) when shared memory has room for its tile.  Every
+// wait is bounded (2 s); on a timeout the block sets the workspace status bit
+// and stops.
 #include <cuda.h>
 
 #include <algorithm>
@@ -264,6 +266,7 @@ struct WnArgs {
     uint32_t pix_bytes;     // cb * rb
     uint32_t grp_bytes;     // G * pix_bytes
     uint32_t b_off;         // byte offset of the pixel ring
+    uint32_t rep_off;       // byte offset of the weight-repack tile (when rep.W is set)
 };
 
 struct WnBars {
@@ -294,7 +297,7 @@ __device__ __forceinline__ Run run_at(long long i, long long i1, int Q) {
 template <int NB>
 __global__ void __launch_bounds__(kWnThreads, 1)
     wgrad_nb_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
-                    const WnArgs a) {
+                    const WnArgs a, const RepackJob rep) {
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -507,6 +510,12 @@ __global__ void __launch_bounds__(kWnThreads, 1)
         const int wq = warp & 3;
         const int kl = wq * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        if (rep.W != nullptr) {
+            // the input gradient's weight repack, its tiles spread over the
+            // blocks, while this block's MMAs run (its own 32 x 33 tile)
+            repack_part_group(rep, (int)blockIdx.x, (int)gridDim.x,
+                              reinterpret_cast<float *>(smem + a.rep_off), tid - 128, 128, 1);
+        }
         bool ok = has_work;
         if (ok)
             ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
@@ -568,14 +577,15 @@ __global__ void __launch_bounds__(kWnThreads, 1)
 // dW[k][cg][r][s] += acc[unit][t][s * cb + cl][kl] with unit = (kt * ctiles +
 // ct) * R + r, k = (kt * KT + t) * 128 + kl, c = ct * cb + cl, where c = (k /
 // Kg) * Cg + cg is the input channel of group-local index cg (dense: Cg = C):
-// one thread per dW element in dW order (coalesced read-modify-write of dW;
-// the scattered reads of the accumulators hit the L2).
+// one thread per (k, cg, r), which adds its S contiguous dW elements
+// (coalesced along the warp) from S accumulator entries (scattered reads that
+// hit the L2); 32-bit index arithmetic, computed once per thread.
 // The first nrep blocks transpose the input gradient's weight repack instead
 // (rep; see cba_repack.cuh): first, so that they run beside the apply blocks
 // rather than after them.
 __global__ void __launch_bounds__(256)
     wgrad_nb_apply_kernel(const float *__restrict__ acc, int KT, int cols, int cb, int S, int R,
-                          int ctiles, int Cg, int Kg, long long total, float *__restrict__ dW,
+                          int ctiles, int Cg, int Kg, int nrows, float *__restrict__ dW,
                           int napply, RepackJob rep, int nrep) {
     ptx::griddep_wait();  // the accumulators come from the weight-gradient kernel
     if ((int)blockIdx.x < nrep) {
@@ -583,18 +593,30 @@ __global__ void __launch_bounds__(256)
         return;
     }
     const int ab = (int)blockIdx.x - nrep;  // apply block
-    const long long stride = (long long)napply * blockDim.x;
-    const int RS = R * S;
-    for (long long i = ab * (long long)blockDim.x + threadIdx.x; i < total;
-         i += stride) {
-        const long long kc = i / RS;
-        const int rs = (int)(i - kc * RS);
-        const int r = rs / S, s = rs - r * S;
-        const int k = (int)(kc / Cg), c = (int)(kc - (long long)k * Cg) + (k / Kg) * Cg;
+    const size_t unit_stride = (size_t)KT * cols * 128;  // one unit's accumulators
+    for (int row = ab * (int)blockDim.x + (int)threadIdx.x; row < nrows;
+         row += napply * (int)blockDim.x) {
+        const int kc = row / R, r = row - kc * R;  // row = (k * Cg + cg) * R + r
+        const int k = kc / Cg, cg = kc - k * Cg;
+        const int c = cg + (k / Kg) * Cg;
         const int kt = k / (128 * KT), t = (k >> 7) - kt * KT, kl = k & 127;
         const int ct = c / cb, cl = c - ct * cb;
-        const long long unit = ((long long)kt * ctiles + ct) * R + r;
-        dW[i] += acc[((unit * KT + t) * cols + s * cb + cl) * 128 + kl];
+        const float *ap = acc + (size_t)((kt * ctiles + ct) * R + r) * unit_stride +
+                          ((size_t)t * cols + cl) * 128 + kl;
+        float *wp = dW + (size_t)row * S;
+        // batches of 8 kernel columns: every load of a batch before its adds
+        for (int s0 = 0; s0 < S; s0 += 8) {
+            float av[8], wv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (s0 + u < S) {
+                    av[u] = ap[(size_t)(s0 + u) * cb * 128];
+                    wv[u] = wp[s0 + u];
+                }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (s0 + u < S) wp[s0 + u] = wv[u] + av[u];
+        }
     }
 }
 
@@ -725,6 +747,8 @@ bool wgrad_nb_supported(const Plan &p) {
                              (long long)p.N * g.Pp;
     if (blocks >= (1LL << 31)) return false;
     if ((long long)p.N * g.Pp >= (1LL << 31)) return false;
+    // int32 dW row index of the accumulator apply
+    if ((long long)p.K * p.Cg * p.R >= (1LL << 31)) return false;
     return true;
 }
 
@@ -791,6 +815,16 @@ cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, fl
     a.swz = w.nb == 16 ? 4u : 2u;  // 64-byte or 128-byte swizzle
     a.a_pos_bytes = w.a_pos_bytes; a.a_slot_bytes = w.a_slot_bytes;
     a.pix_bytes = w.pix_bytes; a.grp_bytes = w.grp_bytes; a.b_off = w.b_off;
+    // the weight repack rides in this kernel when a block's contraction range
+    // is long enough to hide it (at least 32 items; shorter ranges ended later
+    // with it) and its 32 x 33 tile fits after the rings and epilogue stages,
+    // else in the apply launch
+    const size_t rep_tile = 32 * 33 * sizeof(float);
+    const bool rep_here = rep != nullptr && w.items / w.splits >= 32 &&
+                          w.smem + rep_tile + 512 <= 227 * 1024;  // + barriers
+    a.rep_off = (uint32_t)(w.smem - 1024);  // the rings / stages end here (1 KB alignment slack)
+    const size_t smem = w.smem + (rep_here ? rep_tile : 0);
+    const RepackJob gjob = rep_here ? *rep : RepackJob{};
 
     alignas(64) CUtensorMap tma, tmb;
     const int swz_bytes = (int)w.rb;  // the row is exactly one swizzle span
@@ -808,16 +842,17 @@ cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, fl
     }
     auto kern = w.nb == 16 ? wgrad_nb_kernel<16> : wgrad_nb_kernel<32>;
     cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)w.smem);
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, dim3(w.grid), dim3(kWnThreads), w.smem, st, tma, tmb, a);
+    e = launch_pdl(kern, dim3(w.grid), dim3(kWnThreads), smem, st, tma, tmb, a, gjob);
     if (e != cudaSuccess) return e;
-    const long long total = (long long)p.K * p.Cg * p.R * p.S;
-    const unsigned ablocks = (unsigned)std::min<long long>((total + 255) / 256, p.num_sms * 32LL);
-    const RepackJob job = rep ? *rep : RepackJob{};
-    const int nrep = rep ? (int)std::min<long long>(repack_tiles(*rep), 4LL * p.num_sms) : 0;
+    const int nrows = p.K * p.Cg * p.R;  // dW rows of S elements, < 2^31 (wgrad_nb_supported)
+    const unsigned ablocks = (unsigned)std::min<long long>((nrows + 255) / 256, p.num_sms * 32LL);
+    const RepackJob job = rep && !rep_here ? *rep : RepackJob{};
+    const int nrep =
+        rep && !rep_here ? (int)std::min<long long>(repack_tiles(*rep), 4LL * p.num_sms) : 0;
     e = launch_pdl(wgrad_nb_apply_kernel, dim3(ablocks + nrep), dim3(256), 0, st,
-                   (const float *)acc, w.KT, w.cols, w.cb, p.S, p.R, w.ctiles, p.Cg, p.Kg, total,
+                   (const float *)acc, w.KT, w.cols, w.cb, p.S, p.R, w.ctiles, p.Cg, p.Kg, nrows,
                    dW, (int)ablocks, job, nrep);
     if (e != cudaSuccess) return e;
     *launches += 2;
