@@ -1,11 +1,12 @@
 // cba_repack.cuh -- the input gradient's weight repack, W[k][c - g*Cg][r][s]
 // -> wr[r][s][c][k] (TF32-rounded, k padded to Kw with zeros, zero where input
 // channel c is outside output channel k's group), as 32 x 32 tiles that
-// extra blocks of another launch transpose through shared memory.  It rides
-// in the weight gradient's accumulator-apply launch: that kernel is
-// latency-bound and leaves most of the GPU idle, so the tiles cost almost
-// nothing there (inside the memory-bound reduction pass they delayed its
-// streaming by several microseconds).
+// threads of another kernel transpose through shared memory: the idle
+// epilogue warps of a weight-gradient GEMM while its MMAs run (the 1x1 plain
+// GEMM, and the batch-innermost GEMM when its contraction ranges are long),
+// else extra blocks of the weight gradient's accumulator-apply launch, which
+// is latency-bound.  (Inside the memory-bound reduction pass the tiles
+// delayed its streaming by several microseconds.)
 #pragma once
 
 #include "cba_internal.cuh"

@@ -29,6 +29,9 @@
 //     onto prev, which `prev_init_kernel` has first set to residual (+ prev).
 // `dgrad_tc4_kernel` is persistent, one block per SM, with two TMEM
 // accumulators so that a tile's epilogue overlaps the next tile's MMAs;
+// `dgrad_tc4_classes_kernel` runs the classes of a strided layer side by side
+// in one launch (each class on its own share of the SMs, in proportion to its
+// work), so that the small classes do not each leave most of the GPU idle;
 // `dgrad_tc3_kernel` (one tile pair per block) takes the classes whose column
 // span or kernel-column count is past what the persistent kernel's halo and
 // TMEM budget hold.
