@@ -666,10 +666,14 @@ WnGeom wn_geom(const Plan &p) {
     w.units = (int)units;
     w.splits = (int)std::max(1LL, std::min(w.items, (long long)(p.num_sms / w.units)));
     w.grid = w.units * w.splits;
-    // copies of at least 16 KB: positions per A box, pixels per group (a
-    // window of S pixels spans at most two groups)
+    // A boxes of at least 32 KB (positions per box) and pixel groups of at
+    // least 16 KB (a window of S pixels spans at most two groups): an issuing
+    // thread's cost per barrier wait and copy, not the bytes in flight, sets
+    // the copy rate, so fewer, larger copies per position keep the MMAs fed
+    // (one 16 KB box of 128 dz rows per position and k-tile: 117 us for the
+    // residual block's 3x3 weight-gradient phase; two positions per box: 104)
     w.a_pos_bytes = 128u * w.rb;
-    w.Qa = std::max(1, (int)(16384 / w.a_pos_bytes));
+    w.Qa = std::max(1, (int)(32768 / w.a_pos_bytes));
     w.a_slot_bytes = (uint32_t)w.KT * w.Qa * w.a_pos_bytes;
     w.pix_bytes = (uint32_t)w.cb * w.rb;
     w.G = std::max({p.S - 1, 1, (int)((16384 + w.pix_bytes - 1) / w.pix_bytes)});
