@@ -666,20 +666,21 @@ WnGeom wn_geom(const Plan &p) {
     w.units = (int)units;
     w.splits = (int)std::max(1LL, std::min(w.items, (long long)(p.num_sms / w.units)));
     w.grid = w.units * w.splits;
-    // A boxes of at least 32 KB (positions per box) and pixel groups of at
-    // least 16 KB (a window of S pixels spans at most two groups): an issuing
+    // A boxes and pixel groups of at least 32 KB (positions per box, pixels
+    // per group; a window of S pixels spans at most two groups): an issuing
     // thread's cost per barrier wait and copy, not the bytes in flight, sets
     // the copy rate, so fewer, larger copies per position keep the MMAs fed
-    // (one 16 KB box of 128 dz rows per position and k-tile: 117 us for the
-    // residual block's 3x3 weight-gradient phase; two positions per box: 104)
+    // (the residual block's 3x3 weight-gradient phase: 117 us with 16 KB of
+    // dz rows per box and 16 KB pixel groups, 103 with 32 KB boxes, 99 with
+    // 32 KB groups as well)
     w.a_pos_bytes = 128u * w.rb;
     w.Qa = std::max(1, (int)(32768 / w.a_pos_bytes));
     w.a_slot_bytes = (uint32_t)w.KT * w.Qa * w.a_pos_bytes;
     w.pix_bytes = (uint32_t)w.cb * w.rb;
-    w.G = std::max({p.S - 1, 1, (int)((16384 + w.pix_bytes - 1) / w.pix_bytes)});
+    w.G = std::max({p.S - 1, 1, (int)((32768 + w.pix_bytes - 1) / w.pix_bytes)});
     if (w.G > 256) return w;
     w.grp_bytes = (uint32_t)w.G * w.pix_bytes;
-    const size_t budget = 220 * 1024;
+    const size_t budget = 226 * 1024;  // 227 KB less the alignment slack
     const int mirror = p.S > 1 ? 1 : 0;
     int na = kWnMaxNA, ng = kWnMaxNG;
     auto bytes = [&](int a_, int g_) {
