@@ -296,20 +296,27 @@ int backward_impl(const cba_desc_t *d, const float *x, const float *output, cons
             if (e != cudaSuccess) return fail_cuda(e);
             return CBA_OK;
         }
+        // the tensor-core input gradient reads repacked weights: written by
+        // extra blocks of the weight gradient's accumulator-apply launch, a
+        // latency-bound kernel where they cost little; on the batch-innermost
+        // path, for weights of at most 2 MB, by extra blocks of the layout pass
+        // instead (measured: the LeNet and YOLO-head steps 4-7 us faster that
+        // way, the 4.7 MB repacks of the 3x3 layers 1-3 us slower)
+        const bool rep_layouts =
+            p.use_wnb && repp && (long long)p.K * p.Cg * p.R * p.S * 4 <= (2LL << 20);
         if (p.use_wnb) {
             if (e == cudaSuccess)
                 e = launch_layouts(p, delta, output, z, x, workspace, dzn,
-                                   prev_delta ? dzc : nullptr, xn, st, &n_launch);
+                                   prev_delta ? dzc : nullptr, xn, rep_layouts ? repp : nullptr,
+                                   st, &n_launch);
         } else if (e == cudaSuccess) {
             e = launch_dzc(p, delta, output, z, workspace, dzc, st, &n_launch);
         }
         if (e == cudaSuccess) e = tr.mark(2);
-        // the tensor-core input gradient reads repacked weights: written by
-        // extra blocks of the weight gradient's accumulator-apply launch
         if (e == cudaSuccess)
             e = p.use_wnb ? launch_wgrad_nb(p, xn, dzn, dW, workspace,
-                                            ws_at<float>(workspace, p.off_wgacc), repp, st,
-                                            &n_launch)
+                                            ws_at<float>(workspace, p.off_wgacc),
+                                            rep_layouts ? nullptr : repp, st, &n_launch)
                           : launch_wgrad_tc4(p, x, dzc, dW, workspace, repp, st, &n_launch);
         if (e == cudaSuccess) e = tr.mark(3);
         if (e == cudaSuccess && prev_delta)

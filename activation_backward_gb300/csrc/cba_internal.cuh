@@ -178,10 +178,12 @@ cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, fl
                             float *acc, const RepackJob *rep, cudaStream_t st, int *launches);
 // The layout pass of that weight gradient, one launch: dz batch-innermost
 // (dzn), channels-last with its zero border when dzc is not NULL (the layout
-// of dzc_geom, read by the input gradient), and x batch-innermost (xn).
+// of dzc_geom, read by the input gradient), x batch-innermost (xn), and, when
+// rep is not NULL, the input gradient's weight repack (cba_repack.cuh).
 cudaError_t launch_layouts(const Plan &p, const float *delta, const float *output,
                            const float *z, const float *x, const void *ws, float *dzn,
-                           float *dzc, float *xn, cudaStream_t st, int *launches);
+                           float *dzc, float *xn, const RepackJob *rep, cudaStream_t st,
+                           int *launches);
 // Both gradients of 1x1 stride-1 unpadded layers as plain TMA-fed GEMMs
 // (cba_gemm1x1.cu): dzt is dz in [N][K][H*W] order, dzc the channels-last copy,
 // wr the repacked weights (written by the weight-gradient launch when rep is

@@ -29,11 +29,9 @@
 // the blocks of a tile); a second kernel adds the accumulators into dW.
 //
 // Roles: warp 0 issues the A loads, warp 2 the pixel loads, warp 1 the MMAs
-// (one thread), warps 4-7 run the epilogue (TMEM lanes 0-127); until the
-// tile is done they transpose their share of the input gradient's weight
-// repack (cba_repack.cuh) when shared memory has room for its tile.  Every
-// wait is bounded (2 s); on a timeout the block sets the workspace status bit
-// and stops.
+// (one thread), warps 4-7 run the epilogue (TMEM lanes 0-127).  Every wait is
+// bounded (2 s); on a timeout the block sets the workspace status bit and
+// stops.
 #include <cuda.h>
 
 #include <algorithm>
@@ -169,6 +167,8 @@ struct LayoutArgs {
     int kchunks, npx_dz, ndz;      // dz: channel chunks of 8 (over Kp), position chunks, blocks
     int C, HW, xchunks, npx_x, nx;  // x: channel chunks, position chunks, blocks
     int nborder;                    // border rows (0 without dzc or border)
+    int nrep;                       // weight-repack blocks (0: none)
+    RepackJob rep;
     const float *x;
     float *dzn, *dzc, *xn;
 };
@@ -226,21 +226,32 @@ __global__ void __launch_bounds__(256) layouts_kernel(DzSrc<ACT, BN> src, Layout
         return;
     }
     bid -= la.nx;
-    if (!DZC || bid >= la.nborder) return;
-    ptx::griddep_launch_dependents();
-    const int row = bid % la.Pp;
-    float4 *base = reinterpret_cast<float4 *>(la.dzc + (long long)bid * la.Qpp * la.Kp);
-    const int k4 = la.Kp / 4;
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (row < la.bd_lo || row >= la.bd_lo + la.Pe) {
-        for (int i = t; i < la.Qpp * k4; i += 256) base[i] = z;
+    if (bid < la.nborder) {
+        ptx::griddep_launch_dependents();
+        if constexpr (DZC) {
+            const int row = bid % la.Pp;
+            float4 *base = reinterpret_cast<float4 *>(la.dzc + (long long)bid * la.Qpp * la.Kp);
+            const int k4 = la.Kp / 4;
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (row < la.bd_lo || row >= la.bd_lo + la.Pe) {
+                for (int i = t; i < la.Qpp * k4; i += 256) base[i] = z;
+                return;
+            }
+            const int nl = la.bq_lo, nr = la.Qpp - la.bq_lo - la.Qe;
+            for (int i = t; i < (nl + nr) * k4; i += 256) {
+                const int c = i / k4, kk = i - c * k4;
+                const int col = c < nl ? c : la.bq_lo + la.Qe + (c - nl);
+                base[col * k4 + kk] = z;
+            }
+        }
         return;
     }
-    const int nl = la.bq_lo, nr = la.Qpp - la.bq_lo - la.Qe;
-    for (int i = t; i < (nl + nr) * k4; i += 256) {
-        const int c = i / k4, kk = i - c * k4;
-        const int col = c < nl ? c : la.bq_lo + la.Qe + (c - nl);
-        base[col * k4 + kk] = z;
+    bid -= la.nborder;
+    if (bid < la.nrep) {
+        // the input gradient's weight repack (cba_repack.cuh), through this
+        // block's tile buffer
+        ptx::griddep_launch_dependents();
+        repack_part_group(la.rep, bid, la.nrep, &tile[0][0], t, 256, 1);
     }
 }
 
@@ -266,7 +277,6 @@ struct WnArgs {
     uint32_t pix_bytes;     // cb * rb
     uint32_t grp_bytes;     // G * pix_bytes
     uint32_t b_off;         // byte offset of the pixel ring
-    uint32_t rep_off;       // byte offset of the weight-repack tile (when rep.W is set)
 };
 
 struct WnBars {
@@ -297,7 +307,7 @@ __device__ __forceinline__ Run run_at(long long i, long long i1, int Q) {
 template <int NB>
 __global__ void __launch_bounds__(kWnThreads, 1)
     wgrad_nb_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
-                    const WnArgs a, const RepackJob rep) {
+                    const WnArgs a) {
     extern __shared__ uint8_t smem_dyn[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_dyn) + 1023) & ~uintptr_t(1023));
@@ -510,12 +520,6 @@ __global__ void __launch_bounds__(kWnThreads, 1)
         const int wq = warp & 3;
         const int kl = wq * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
-        if (rep.W != nullptr) {
-            // the input gradient's weight repack, its tiles spread over the
-            // blocks, while this block's MMAs run (its own 32 x 33 tile)
-            repack_part_group(rep, (int)blockIdx.x, (int)gridDim.x,
-                              reinterpret_cast<float *>(smem + a.rep_off), tid - 128, 128, 1);
-        }
         bool ok = has_work;
         if (ok)
             ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sb.accum), 0, &sb.abort_flag, a.status,
@@ -749,7 +753,7 @@ bool wgrad_nb_supported(const Plan &p) {
     const DzcGeom g = dzc_geom(p);
     const long long blocks = (long long)w.nc * ((p.PQ + 31) / 32) * ((g.Kp + 7) / 8) +
                              (long long)w.nc * ((p.HW + 31) / 32) * ((p.C + 7) / 8) +
-                             (long long)p.N * g.Pp;
+                             (long long)p.N * g.Pp + 4LL * p.num_sms;  // + weight-repack blocks
     if (blocks >= (1LL << 31)) return false;
     if ((long long)p.N * g.Pp >= (1LL << 31)) return false;
     // int32 dW row index of the accumulator apply
@@ -774,7 +778,8 @@ size_t wgrad_nb_dzn_bytes(const Plan &p) {
 
 cudaError_t launch_layouts(const Plan &p, const float *delta, const float *output,
                            const float *z, const float *x, const void *ws, float *dzn,
-                           float *dzc, float *xn, cudaStream_t st, int *launches) {
+                           float *dzc, float *xn, const RepackJob *rep, cudaStream_t st,
+                           int *launches) {
     const WnGeom w = wn_geom(p);
     if (!w.ok) return cudaErrorNotSupported;
     const DzcGeom g = dzc_geom(p);
@@ -792,9 +797,12 @@ cudaError_t launch_layouts(const Plan &p, const float *delta, const float *outpu
     const long long nx = (long long)la.npx_x * nc * la.xchunks;
     const long long nborder =
         (dzc && (g.Pp != g.Pe || g.Qpp != g.Qe)) ? (long long)p.N * g.Pp : 0;
-    if (ndz + nx + nborder >= (1LL << 31)) return cudaErrorInvalidValue;
+    const long long nrep = rep ? std::min<long long>(repack_tiles(*rep), 4LL * p.num_sms) : 0;
+    if (ndz + nx + nborder + nrep >= (1LL << 31)) return cudaErrorInvalidValue;
     la.ndz = (int)ndz; la.nx = (int)nx; la.nborder = (int)nborder;
-    const unsigned blocks = (unsigned)(ndz + nx + nborder);
+    la.nrep = (int)nrep;
+    la.rep = rep ? *rep : RepackJob{};
+    const unsigned blocks = (unsigned)(ndz + nx + nborder + nrep);
     const Coef *coef = ws_at<Coef>(ws, p.off_coef);
     cudaError_t e = w.nb == 16
                         ? launch_layouts_nb<16>(p, g, delta, output, z, coef, la, blocks, st)
@@ -820,16 +828,7 @@ cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, fl
     a.swz = w.nb == 16 ? 4u : 2u;  // 64-byte or 128-byte swizzle
     a.a_pos_bytes = w.a_pos_bytes; a.a_slot_bytes = w.a_slot_bytes;
     a.pix_bytes = w.pix_bytes; a.grp_bytes = w.grp_bytes; a.b_off = w.b_off;
-    // the weight repack rides in this kernel when a block's contraction range
-    // is long enough to hide it (at least 32 items; shorter ranges ended later
-    // with it) and its 32 x 33 tile fits after the rings and epilogue stages,
-    // else in the apply launch
-    const size_t rep_tile = 32 * 33 * sizeof(float);
-    const bool rep_here = rep != nullptr && w.items / w.splits >= 32 &&
-                          w.smem + rep_tile + 512 <= 227 * 1024;  // + barriers
-    a.rep_off = (uint32_t)(w.smem - 1024);  // the rings / stages end here (1 KB alignment slack)
-    const size_t smem = w.smem + (rep_here ? rep_tile : 0);
-    const RepackJob gjob = rep_here ? *rep : RepackJob{};
+    const size_t smem = w.smem;
 
     alignas(64) CUtensorMap tma, tmb;
     const int swz_bytes = (int)w.rb;  // the row is exactly one swizzle span
@@ -849,13 +848,12 @@ cudaError_t launch_wgrad_nb(const Plan &p, const float *xn, const float *dzn, fl
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(kern, dim3(w.grid), dim3(kWnThreads), smem, st, tma, tmb, a, gjob);
+    e = launch_pdl(kern, dim3(w.grid), dim3(kWnThreads), smem, st, tma, tmb, a);
     if (e != cudaSuccess) return e;
     const int nrows = p.K * p.Cg * p.R;  // dW rows of S elements, < 2^31 (wgrad_nb_supported)
     const unsigned ablocks = (unsigned)std::min<long long>((nrows + 255) / 256, p.num_sms * 32LL);
-    const RepackJob job = rep && !rep_here ? *rep : RepackJob{};
-    const int nrep =
-        rep && !rep_here ? (int)std::min<long long>(repack_tiles(*rep), 4LL * p.num_sms) : 0;
+    const RepackJob job = rep ? *rep : RepackJob{};
+    const int nrep = rep ? (int)std::min<long long>(repack_tiles(*rep), 4LL * p.num_sms) : 0;
     e = launch_pdl(wgrad_nb_apply_kernel, dim3(ablocks + nrep), dim3(256), 0, st,
                    (const float *)acc, w.KT, w.cols, w.cb, p.S, p.R, w.ctiles, p.Cg, p.Kg, nrows,
                    dW, (int)ablocks, job, nrep);
