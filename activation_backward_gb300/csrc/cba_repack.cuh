@@ -2,11 +2,11 @@
 // -> wr[r][s][c][k] (TF32-rounded, k padded to Kw with zeros, zero where input
 // channel c is outside output channel k's group), as 32 x 32 tiles that
 // threads of another kernel transpose through shared memory: the idle
-// epilogue warps of a weight-gradient GEMM while its MMAs run (the 1x1 plain
-// GEMM, and the batch-innermost GEMM when its contraction ranges are long),
-// else extra blocks of the weight gradient's accumulator-apply launch, which
-// is latency-bound.  (Inside the memory-bound reduction pass the tiles
-// delayed its streaming by several microseconds.)
+// epilogue warps of the 1x1 plain GEMM while its MMAs run; extra blocks of
+// the batch-innermost layout pass for weights of at most 2 MB; else extra
+// blocks of the weight gradient's accumulator-apply launch, which is
+// latency-bound.  (Inside the memory-bound reduction pass the tiles delayed
+// its streaming by several microseconds.)
 #pragma once
 
 #include "cba_internal.cuh"
