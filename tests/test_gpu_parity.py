@@ -326,6 +326,20 @@ def test_accumulate_onto_existing_prev_1x1(ref, cuda_lib):
                 assert_close(got[k], exp[k], TOL[math.values[0]], f"1x1 acc {k}")
 
 
+def test_strided_1x1_without_residual_stores_zero_classes(ref, cuda_lib):
+    # 1x1 stride 2: three of the four stride phase classes have no kernel tap,
+    # so the input gradient must store zeros there (no shortcut to add onto);
+    # the classes run side by side in one launch
+    spec = inputs.LayerSpec("1x1 s2", inputs.Geometry(3, 24, 14, 18, 40, 1, 1, 2, 0), 1, True)
+    layer = inputs.make_layer(spec, 907, residual=False)
+    for math in MATHS:
+        _, got = run_gpu(layer, math.values[0])
+        exp = oracle_chain(ref, layer)
+        for k in KEYS:
+            if exp.get(k) is not None:
+                assert_close(got[k], exp[k], TOL[math.values[0]], f"1x1 s2 {k}")
+
+
 def test_prev_delta_null_skips_dgrad(ref, cuda_lib):
     layer = config_layers(2, 2)[0]
     _, got = run_gpu(layer, TF32, with_prev=False)
