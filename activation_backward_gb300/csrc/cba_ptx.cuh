@@ -1,6 +1,7 @@
 // cba_ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers with bounded
-// waits, tcgen05 (TMEM allocation, MMA, commit, loads, fences), async-proxy
-// fences, cp.async and the global nanosecond timer.
+// waits, tcgen05 (TMEM allocation, MMA, commit, loads and stores, fences),
+// TMA tensor copies and bulk reductions, async-proxy fences, programmatic
+// dependent launch and the global nanosecond timer.
 #pragma once
 
 #include <cstdint>
@@ -99,42 +100,12 @@ __device__ __forceinline__ void red_add_v4_f32(float *p, float4 v) {
                  "f"(v.z), "f"(v.w));
 }
 
-// Brings the line holding `p` into L2 (no register result, no wait).
-__device__ __forceinline__ void prefetch_l2(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // ------------------------------------------------------------ async proxy
 
 // Makes this thread's generic-proxy writes to shared memory visible to the
 // async proxy (tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- cp.async
-
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src),
-                 "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-// Arrive on an mbarrier when all of this thread's prior cp.async copies have
-// landed (the arrive counts against the barrier's expected count).
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -192,15 +163,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
-// 32 lanes x 32 bit, 4 consecutive columns -> 4 registers per thread.
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
-    uint32_t r[4];
-    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
-}
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -234,19 +196,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
         "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
         "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
         "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-        : "memory");
-}
-// 32 lanes x 32 bit, 16 consecutive columns <- 16 registers per thread.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15]))
         : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {
@@ -325,13 +274,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int 
 
 // Tiled tensor store / reduce-add (f32, at the L2) of a shared-memory box,
 // completed through the bulk-group mechanism (bulk_commit, bulk_wait_*).
-__device__ __forceinline__ void tma_store_2d(const void *tmap, uint32_t src, int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(tmap)),
-        "r"(src), "r"(c0), "r"(c1)
-        : "memory");
-}
 __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int c0, int c1,
                                              int c2) {
     asm volatile(
